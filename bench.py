@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the gated delta-rule hot path on one GB300 (replicas on N GPUs).
+
+Headline: GDN chunked forward, B=2, T=4096, H=Hg=16, K=V=128, bf16 q/k/v, fp32
+g/beta, 64-token chunks, fp32 initial state in and final state out.  One step
+is one library call over that batch (gate cumsum, intra-chunk solve + WY,
+sequential state pass and output, all inside the call).  L2 is flushed
+(a 512 MB write) before every step; CUDA events on the launch stream time
+each step.  The same JSON line also carries, measured the same way, the
+per-channel-gate (KDA) forward (B=1, T=8192, H=HV=32) and the decode step
+(B=pool=256, HV=32, H=16, T = 1, 2, 4, bf16 state updated in place).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (independent
+replicas, no collective on the data path); rank 0 prints one JSON line with the
+whole-job throughput (tokens of all ranks / slowest rank's time).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "GDN chunk-fwd tokens/s and % roofline at 1 GB300; decode state GB/s vs HBM peak"
+UNIT = "tokens/s"
+WORKLOAD = ("GDN chunked prefill: B=2, T=4096, H=Hg=16, K=V=128, bf16 q/k/v, fp32 g/beta "
+            "(logsigmoid(N(0,1)+3) per token), BT=64, h0 ~ N(0,0.1) fp32, final state returned")
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ accounting
+
+def gdn_bytes(B, T, H, Hg, K, V, N, h0=True, ht=True, elt=2):
+    """Algorithmic HBM bytes of one chunked forward: every input read once, o written
+    once, initial/final state read/written once."""
+    per_token = Hg * K * elt * 2 + H * V * elt * 2 + H * 4 * 2
+    return B * T * per_token + N * H * K * V * 4 * (int(h0) + int(ht))
+
+
+def kda_bytes(B, T, H, HV, K, V, N, h0=False, ht=True, elt=2):
+    per_token = H * K * elt * 2 + HV * V * elt * 2 + HV * K * 4 + HV * 4
+    return B * T * per_token + N * HV * K * V * 4 * (int(h0) + int(ht))
+
+
+def chunk_flops(B, T, H, K, V, BT=64):
+    """6KV + 5 BT K per token and value head: w h, k^T v_new, q h (three BT x K x V
+    GEMMs per chunk) and KK^T, w, u, qk^T, Aqk v_new counted on the triangle."""
+    return B * T * H * (6 * K * V + 5 * BT * K)
+
+
+def decode_state_bytes(B, HV, K, V):
+    return 2 * B * HV * K * V * 2
+
+
+def decode_total_bytes(B, T, H, HV, K, V):
+    return (decode_state_bytes(B, HV, K, V) + B * T * (2 * H * K * 2 + 2 * HV * V * 2 + 2 * HV * 2)
+            + 2 * HV * 4)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the
+    current kernel source (sha of its .cu file)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for ln in open(path):
+        f = ln.split()
+        if len(f) < 3 or f[0] != kernel:
+            continue
+        kv = dict(x.split("=", 1) for x in f[1:] if "=" in x)
+        src = os.path.join(ROOT, "gated_delta_rule_kk_gb300", "csrc", kv.get("source", ""))
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
+        if sha != kv.get("sha"):
+            return None
+        return float(kv["bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = sorted({names[i] for _, _, r in rows for i, x in enumerate(r) if x.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": seen, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ timing
+
+def time_steps(fn, steps, warmup, flush, stream):
+    """Warm up, then time `steps` calls with events on `stream`, flushing L2 before
+    each.  Returns per-step milliseconds."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def to_dev(inp, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, dev):
+    import gated_delta_rule_kk_gb300 as gdn
+    from gated_delta_rule_kk_gb300 import synth
+
+    hbm, tc_burst, tc_sust, peak_src = measured_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # ---- headline: GDN chunked forward
+    inp = synth.gdn_prefill()
+    dm = inp["dims"]
+    d = to_dev(inp, dev)
+    o = torch.empty_like(d["v"])
+    ht = torch.empty((dm["N"], dm["H"], dm["K"], dm["V"]), dtype=torch.float32, device=dev)
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                          initial_state=d["h0"], out=o, final_state=ht)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_wall0 = time.perf_counter()
+        ms = time_steps(step, args.steps, args.warmup, flush, stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    status = gdn.gdn_check_device_error()
+    if status != gdn.Status.OK:
+        raise RuntimeError(f"device error during bench: {status.name}")
+    tot_ms = sum(ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_step = tot_ms / args.steps
+    tokens = dm["B"] * dm["T"]
+    value = tokens * args.steps * world / (tot_ms / 1e3)
+    nbytes = gdn_bytes(dm["B"], dm["T"], dm["H"], dm["Hg"], dm["K"], dm["V"], dm["N"])
+    flops = chunk_flops(dm["B"], dm["T"], dm["H"], dm["K"], dm["V"])
+    achieved_gbs = nbytes / (ms_step / 1e3) / 1e9
+    t_roof = max(nbytes / (hbm * 1e9), flops / (tc_burst * 1e12))
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy draws, see gated_delta_rule_kk_gb300/synth.py)",
+        "config": {"workload": WORKLOAD, "global_batch": dm["B"] * world, "seq_len": dm["T"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed (512 MB write) before every timed step"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm, "traffic": traffic_record("gdn_chunk"),
+                     "peak_source": peak_src, "algorithmic_bytes": nbytes,
+                     "algorithmic_flops": flops,
+                     "frac_of_roofline_time": t_roof / (ms_step / 1e3)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+    keys = ("q", "k", "v", "g", "beta", "h0")
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in keys)
+    d2h = o_h.numel() * o_h.element_size() + ht_h.numel() * ht_h.element_size()
+
+    def e2e_step():
+        for k in keys:
+            d[k].copy_(pin[k], non_blocking=True)
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                          initial_state=d["h0"], out=o, final_state=ht)
+        o_h.copy_(o, non_blocking=True)
+        ht_h.copy_(ht, non_blocking=True)
+
+    e2e_ms = time_steps(e2e_step, min(args.steps, 10), 2, flush, stream)
+    e2e_tot = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_tot], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_tot = float(t.item())
+    result["e2e"] = {"value": tokens * len(e2e_ms) * world / (e2e_tot / 1e3), "unit": UNIT,
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del d, o, ht, pin
+
+    # ---- the other rows of the hot path, same timing rules
+    rows = {}
+    if not args.no_rows:
+        rsteps = max(3, min(args.steps, 10))
+        kin = synth.kda_prefill()
+        km = kin["dims"]
+        kd = to_dev(kin, dev)
+        ko = torch.empty_like(kd["v"])
+        kht = torch.empty((km["N"], km["H"], km["K"], km["V"]), dtype=torch.float32, device=dev)
+        kms = time_steps(lambda: gdn.kda_chunk_fwd(kd["q"], kd["k"], kd["v"], kd["g"], kd["beta"],
+                                                   out=ko, final_state=kht),
+                         rsteps, max(3, args.warmup // 2), flush, stream)
+        kt = statistics.mean(kms)
+        kb = kda_bytes(km["B"], km["T"], km["Hg"], km["H"], km["K"], km["V"], km["N"])
+        kf = chunk_flops(km["B"], km["T"], km["H"], km["K"], km["V"])
+        rows["kda"] = {
+            "workload": "KDA chunked prefill: B=1, T=8192, H=HV=32, K=V=128, bf16, per-channel "
+                        "gate (chunk-local cumsum of logsigmoid(N(0,1)+4)), h0=0, ht returned",
+            "tokens_per_s": km["B"] * km["T"] / (kt / 1e3), "ms_per_call": kt,
+            "roofline": {"bound": "hbm", "achieved": kb / (kt / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": kb / (kt / 1e3) / 1e9 / hbm,
+                         "algorithmic_bytes": kb, "algorithmic_flops": kf,
+                         "traffic": traffic_record("kda_chunk")}}
+        del kd, ko, kht, kin
+        for T in (1, 2, 4):
+            din = synth.decode(T)
+            dd = to_dev(din, dev)
+            m = din["dims"]
+            dout = torch.empty_like(dd["v"])
+            dms = time_steps(lambda: gdn.gdn_decode(dd["q"], dd["k"], dd["v"], dd["a"], dd["b"],
+                                                    dd["A_log"], dd["dt_bias"], dd["state"],
+                                                    scale=dd["scale"], out=dout),
+                             rsteps, max(3, args.warmup // 2), flush, stream)
+            dt = statistics.mean(dms)
+            sb = decode_state_bytes(m["B"], m["HV"], m["K"], m["V"])
+            tb = decode_total_bytes(m["B"], T, m["H"], m["HV"], m["K"], m["V"])
+            rows[f"decode_t{T}"] = {
+                "workload": f"GDN decode: B=pool=256, T={T}, H=16, HV=32, K=V=128, bf16 state",
+                "us_per_call": dt * 1e3, "state_gb_per_s": sb / (dt / 1e3) / 1e9,
+                "total_gb_per_s": tb / (dt / 1e3) / 1e9,
+                "roofline": {"bound": "hbm", "achieved": tb / (dt / 1e3) / 1e9, "peak": hbm,
+                             "unit": "GB/s", "frac": tb / (dt / 1e3) / 1e9 / hbm,
+                             "state_frac": sb / (dt / 1e3) / 1e9 / hbm,
+                             "algorithmic_bytes": tb, "traffic": traffic_record(f"decode_t{T}")}}
+            del dd, dout, din
+        status = gdn.gdn_check_device_error()
+        if status != gdn.Status.OK:
+            raise RuntimeError(f"device error during bench rows: {status.name}")
+    result["rows"] = rows
+    return result
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_sample(target_s):
+    """Time the fp64 oracle on whole (sequence, head) chains of the headline
+    workload until about `target_s` seconds have passed.  Returns
+    (token-equivalents per second, seconds, chains)."""
+    from gated_delta_rule_kk_gb300 import synth
+    from oracle import recurrence as R
+    inp = synth.gdn_prefill()
+    dm = inp["dims"]
+    t0 = time.perf_counter()
+    chains = 0
+    while True:
+        n, h = chains % dm["B"], (chains // dm["B"]) % dm["H"]
+        R.gdn_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
+                        h0=inp["h0"], heads=[h], seqs=[n])
+        chains += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    # one chain is T tokens of one of H value heads: T / H token-equivalents
+    tok = chains * dm["T"] / dm["H"]
+    return tok / el, el, chains
+
+
+def run_reference(args):
+    """The oracle on the host cores, as the reference arm."""
+    from gated_delta_rule_kk_gb300 import synth
+    from oracle import recurrence as R
+    inp = synth.gdn_prefill()
+    dm = inp["dims"]
+    times = []
+    for i in range(args.warmup + args.steps):
+        n, h = i % dm["B"], (i // dm["B"]) % dm["H"]
+        t0 = time.perf_counter()
+        R.gdn_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
+                        h0=inp["h0"], heads=[h], seqs=[n])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tok = dm["T"] / dm["H"]
+    value = tok / statistics.mean(times)
+    sample = (f"one whole (sequence, head) chain of the headline workload per step "
+              f"({dm['T']} tokens x 1 of {dm['H']} heads = {tok:.0f} token-equivalents)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "global_batch": dm["B"],
+                                        "seq_len": dm["T"], "parallelism": "host CPU"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the KDA and decode rows")
+    ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    result = run_ours(args, rank, world, dev)
+    if rank == 0:
+        v, el, chains = oracle_sample(args.cpu_baseline_s)
+        result["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{chains} whole (sequence, head) chains of the headline workload "
+                      f"({el:.1f} s, fp64 numpy token recurrence, one thread)"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

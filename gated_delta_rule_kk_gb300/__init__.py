@@ -1,0 +1,8 @@
+"""Gated delta-rule (GDN / KDA) chunked forward and decode for GB300 (sm_103a).
+
+The arithmetic lives in the CUDA library built from ``csrc/`` (see
+``build_lib.py``); this package holds its ctypes binding and the seeded
+synthetic input generators.
+"""
+from .api import gdn_check_device_error, gdn_chunk_fwd, gdn_decode, kda_chunk_fwd  # noqa: F401
+from ._lib import GdnError, Status  # noqa: F401

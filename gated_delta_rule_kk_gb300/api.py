@@ -1,0 +1,162 @@
+"""Python entry points with the C names: torch tensors in, library call, tensors out.
+
+Only argument marshalling happens here (shape reading, dtype/contiguity
+checks, output allocation through PyTorch's caching allocator, the current
+stream).  All arithmetic runs in the CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import DType, GdnChunkArgs, GdnDecodeArgs, KdaChunkArgs
+
+CHUNK = 64
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtypes, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _io_dtype(q):
+    if q.dtype == torch.bfloat16:
+        return DType.BF16, (torch.bfloat16,)
+    if q.dtype == torch.float32:
+        return DType.F32, (torch.float32,)
+    raise ValueError(f"q/k/v must be float32 or bfloat16, got {q.dtype}")
+
+
+def _chunk_common(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out,
+                  final_state, value_heads_name):
+    dev = q.device
+    dt, dts = _io_dtype(q)
+    _need(q, "q", dts, dev)
+    _need(k, "k", dts, dev)
+    _need(v, "v", dts, dev)
+    _need(g, "g", (torch.float32,), dev)
+    _need(beta, "beta", (torch.float32,), dev)
+    B, T, Hk, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    if k.shape != q.shape or v.shape[:2] != (B, T):
+        raise ValueError("q, k must be [B,T,Hk,K] and v [B,T,Hv,V]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _need(initial_state, "initial_state", (torch.float32,), dev)
+        if tuple(initial_state.shape) != (N, Hv, K, V):
+            raise ValueError(f"initial_state must be [{N},{Hv},{K},{V}]")
+    if out is None:
+        out = torch.empty((B, T, Hv, V), dtype=q.dtype, device=dev)
+    else:
+        _need(out, "out", dts, dev)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, Hv, K, V), dtype=torch.float32, device=dev)
+    elif final_state is not None:
+        _need(final_state, "final_state", (torch.float32,), dev)
+    return dt, (B, T, Hk, Hv, K, V, N), out, final_state
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                  output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
+                  stream=None):
+    """GDN chunked forward.  Returns ``(o, ht)`` (``ht`` None if not requested).
+
+    q, k [B,T,Hg,K]; v [B,T,H,V]; g, beta [B,T,H] float32; initial_state
+    [N,H,K,V] float32; cu_seqlens [N+1] int32 (then B == 1).
+    """
+    dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
+        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H")
+    a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                     h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
+                     B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
+                     g_is_cumsum=int(bool(g_is_cumsum)),
+                     scale=float(scale) if scale is not None else 0.0,
+                     workspace=None, workspace_bytes=0)
+    lib = _lib.load()
+    _lib.check(lib.gdn_chunk_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_fwd")
+    return out, ht
+
+
+def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                  output_final_state=True, g_is_cumsum=True, out=None, final_state=None,
+                  stream=None):
+    """KDA chunked forward.  Returns ``(o, ht)``.
+
+    q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV,K] float32 (chunk-local cumsum
+    when g_is_cumsum); beta [B,T,HV]; initial_state [N,HV,K,V] float32.
+    """
+    dt, (B, T, H, HV, K, V, N), out, ht = _chunk_common(
+        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "HV")
+    a = KdaChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                     h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
+                     B=B, T=T, H=H, HV=HV, K=K, V=V, N=N, chunk_size=CHUNK,
+                     g_is_cumsum=int(bool(g_is_cumsum)),
+                     scale=float(scale) if scale is not None else 0.0,
+                     workspace=None, workspace_bytes=0)
+    lib = _lib.load()
+    _lib.check(lib.kda_chunk_fwd(ctypes.byref(a), _stream(stream)), "kda_chunk_fwd")
+    return out, ht
+
+
+def gdn_decode(q, k, v, a, b, A_log, dt_bias, state, slot_indices=None, scale=None,
+               softplus_beta=1.0, softplus_threshold=20.0, eps=1e-6, use_qk_l2norm=True,
+               out=None, stream=None):
+    """Decode T = 1..4 tokens; ``state`` [pool,HV,V,K] bf16 is updated in place.  Returns o."""
+    dev = q.device
+    bf = (torch.bfloat16,)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (state, "state")):
+        _need(t, n, bf, dev)
+    _need(A_log, "A_log", (torch.float32,), dev)
+    _need(dt_bias, "dt_bias", (torch.float32,), dev)
+    if slot_indices is not None:
+        _need(slot_indices, "slot_indices", (torch.int32,), dev)
+    B, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    pool = state.shape[0]
+    if out is None:
+        out = torch.empty((B, T, HV, V), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(out, "out", bf, dev)
+    args = GdnDecodeArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), a=_ptr(a), b=_ptr(b),
+                         A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), state=_ptr(state),
+                         slot_indices=_ptr(slot_indices), o=_ptr(out),
+                         B=B, T=T, H=H, HV=HV, K=K, V=V, pool=pool,
+                         use_qk_l2norm=int(bool(use_qk_l2norm)),
+                         scale=float(scale) if scale is not None else 0.0,
+                         softplus_beta=float(softplus_beta),
+                         softplus_threshold=float(softplus_threshold), eps=float(eps))
+    lib = _lib.load()
+    _lib.check(lib.gdn_decode(ctypes.byref(args), _stream(stream)), "gdn_decode")
+    return out
+
+
+def gdn_check_device_error(stream=None):
+    """Synchronise ``stream`` and return (and clear) the device error word as a Status."""
+    code = ctypes.c_int32(0)
+    lib = _lib.load()
+    _lib.check(lib.gdn_check_device_error(_stream(stream), ctypes.byref(code)),
+               "gdn_check_device_error")
+    return _lib.Status(code.value)

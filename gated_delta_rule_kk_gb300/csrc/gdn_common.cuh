@@ -1,0 +1,34 @@
+// Shared device helpers of the gated delta-rule library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Chunk length of the chunked forward (sglang fla/chunk_fwd.py: BT = 64).
+constexpr int BT = 64;
+// Longest key dimension the chunk kernels take.
+constexpr int KMAX = 128;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Record the first device-side error in the library's error word.
+__device__ __forceinline__ void record_error(int *err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Host: device address of the error word of the current device.
+int *device_error_word();
+
+}  // namespace gdn

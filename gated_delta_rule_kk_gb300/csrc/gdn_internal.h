@@ -1,0 +1,41 @@
+// Internal launch interface between the C entry points (gdn_abi.cu) and the
+// kernel translation units.  Plain host types only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// One chunked-forward problem, already validated.  `H` counts value heads and
+// `Hk` key/query heads for both gate kinds.
+struct ChunkParams {
+  const void *q, *k, *v;
+  const float *g, *beta, *h0;
+  float *ht;
+  void *o;
+  const int32_t *cu_seqlens;
+  int *err;
+  int B, T, H, Hk, K, V, N;
+  int g_is_cumsum;
+  float scale;
+};
+
+struct DecodeParams {
+  const void *q, *k, *v, *a, *b;
+  const float *A_log, *dt_bias;
+  void *state;
+  const int32_t *slot_indices;
+  void *o;
+  int *err;
+  int B, T, H, HV, K, V, pool;
+  int use_qk_l2norm;
+  float scale, softplus_beta, softplus_threshold, eps;
+};
+
+// Each launcher enqueues its kernel(s) and returns the launch status.
+cudaError_t launch_chunk_simt(const ChunkParams &p, bool bf16, bool per_channel_gate,
+                              cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
+
+}  // namespace gdn

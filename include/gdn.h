@@ -1,0 +1,203 @@
+/*
+ * gdn.h - C interface of the GB300 (sm_103a) gated delta-rule library.
+ *
+ * The method: a linear-attention state S (V x K per value head) evolves per
+ * token t as
+ *     S_t = S_{t-1} * D_t * (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = scale * S_t q_t,
+ * with D_t = exp(g_t) * I (GDN, one log-gate per token and head) or
+ * D_t = diag(exp(g_t[0..K))) (KDA, one log-gate per token, head and key
+ * channel).  The token form (decay, pred = S k, delta = beta (v - pred),
+ * S += delta k^T, o = S q) is the one of the FlashInfer page
+ * gdn_decode_bf16_state.py (per-token helpers); the chunked form with BT = 64
+ * token chunks follows the sglang page fla/chunk_fwd.py (fused KK^T + solve
+ * kernel, Steps 1-5, and chunk_gated_delta_rule_fwd_intra), the KDA page
+ * _fla/ops/common/chunk_h.py (chunk_fwd_kernel_h, chunk_fwd_h) and the vLLM
+ * kimi_k3 kda/chunk_intra page (chunk_kda_fwd_kernel_inter_solve_fused).
+ *
+ * Conventions shared by every entry point
+ *  - Memory: every tensor pointer is a DEVICE pointer owned by the caller.
+ *    The library never allocates, frees or retains device memory; outputs are
+ *    written in place.  Tensors are dense, row-major, last index fastest, in
+ *    the layouts given per argument.  Every tensor pointer must be 16-byte
+ *    aligned (GDN_ERR_MISALIGNED otherwise).
+ *  - Streams: work is enqueued on the caller's stream (NULL = the legacy
+ *    default stream) and the call returns without waiting for it.
+ *  - Errors: every call returns a gdn_status_t and never throws, exits or
+ *    prints.  Argument errors are found on the host before anything is
+ *    enqueued (nothing is written then).  Errors that only the device can see
+ *    (bad cu_seqlens, bad slot index, a bounded wait that ran out) are
+ *    recorded in a device-side error word, which gdn_check_device_error()
+ *    reads and clears.  gdn_last_error_message() describes the last host-side
+ *    failure of the calling thread.
+ *  - Log-gates are natural logarithms (exp, not exp2).
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,  /* NULL required pointer, bad size or flag    */
+  GDN_ERR_UNSUPPORTED = 2,  /* valid request this library does not serve */
+  GDN_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned    */
+  GDN_ERR_WORKSPACE = 4,    /* workspace smaller than *_workspace_size     */
+  GDN_ERR_CUDA = 5,         /* a CUDA runtime call failed                  */
+  GDN_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up              */
+  GDN_ERR_BAD_SEQLENS = 7,  /* device: cu_seqlens not rising from 0 to T   */
+  GDN_ERR_BAD_SLOT = 8      /* device: a slot index outside [0, pool)      */
+} gdn_status_t;
+
+typedef enum gdn_dtype {
+  GDN_F32 = 0,   /* float32 q, k, v, o  */
+  GDN_BF16 = 1   /* bfloat16 q, k, v, o */
+} gdn_dtype_t;
+
+/*
+ * Chunked forward with one scalar log-gate per token and value head (GDN).
+ * Shapes follow chunk_gated_delta_rule_fwd_intra (sglang fla/chunk_fwd.py)
+ * and chunk_fwd_h (KDA _fla/ops/common/chunk_h.py):
+ *   q, k   [B, T, Hg, K]  dtype       key/query heads; value head h reads
+ *                                     key head h / (H / Hg)
+ *   v, o   [B, T, H, V]   dtype       o is written
+ *   g      [B, T, H]      float32     natural-log gate per token; with
+ *                                     g_is_cumsum = 1 it is instead the
+ *                                     inclusive cumulative sum inside each
+ *                                     64-token chunk (chunks counted from
+ *                                     each sequence's first token)
+ *   beta   [B, T, H]      float32
+ *   h0     [N, H, K, V]   float32     initial state h = S^T, NULL = zeros
+ *   ht     [N, H, K, V]   float32     final state, NULL = not returned
+ *   cu_seqlens [N + 1]    int32       NULL: N = B sequences of T tokens.
+ *                                     Else B must be 1 and sequence n is
+ *                                     tokens cu_seqlens[n] .. cu_seqlens[n+1]
+ *                                     (0 = cu_seqlens[0] <= ... <= cu_seqlens[N]
+ *                                     = T, checked on the device)
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, H % Hg == 0.
+ * scale <= 0 selects 1/sqrt(K).  No workspace is needed (workspace may be
+ * NULL with workspace_bytes = 0).
+ */
+typedef struct gdn_chunk_args {
+  int32_t dtype;               /* gdn_dtype_t of q, k, v, o */
+  const void *q, *k, *v;
+  const float *g, *beta;
+  const float *h0;
+  float *ht;
+  void *o;
+  const int32_t *cu_seqlens;
+  int32_t B, T, H, Hg, K, V, N;
+  int32_t chunk_size;
+  int32_t g_is_cumsum;
+  float scale;
+  void *workspace;
+  size_t workspace_bytes;
+} gdn_chunk_args;
+
+/* Bytes of workspace gdn_chunk_fwd needs for these arguments (currently 0). */
+gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *args, size_t *bytes);
+
+/* Enqueue the GDN chunked forward (gate cumsum, intra-chunk (I+A)^-1 with the
+ * WY vectors w, u, the sequential inter-chunk state pass and the output) on
+ * `stream`.  Writes o and, if given, ht. */
+gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *args, gdn_stream_t stream);
+
+/*
+ * Chunked forward with one log-gate per token, value head and key channel
+ * (KDA).  Shapes follow chunk_kda_fwd_kernel_inter_solve_fused (vLLM kimi_k3
+ * kda/chunk_intra page):
+ *   q, k   [B, T, H, K]   dtype       value head hv reads key head hv / (HV / H)
+ *   v, o   [B, T, HV, V]  dtype
+ *   g      [B, T, HV, K]  float32     chunk-local inclusive cumulative sum of
+ *                                     the per-channel log-gates when
+ *                                     g_is_cumsum = 1 (as that kernel takes
+ *                                     it), raw per-token log-gates when 0
+ *   beta   [B, T, HV]     float32
+ *   h0, ht [N, HV, K, V]  float32     as for GDN
+ *   cu_seqlens            as for GDN
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0.
+ */
+typedef struct kda_chunk_args {
+  int32_t dtype;
+  const void *q, *k, *v;
+  const float *g, *beta;
+  const float *h0;
+  float *ht;
+  void *o;
+  const int32_t *cu_seqlens;
+  int32_t B, T, H, HV, K, V, N;
+  int32_t chunk_size;
+  int32_t g_is_cumsum;
+  float scale;
+  void *workspace;
+  size_t workspace_bytes;
+} kda_chunk_args;
+
+gdn_status_t kda_chunk_workspace_size(const kda_chunk_args *args, size_t *bytes);
+gdn_status_t kda_chunk_fwd(const kda_chunk_args *args, gdn_stream_t stream);
+
+/*
+ * Decode step for T = 1..4 new tokens per batch entry against a pooled
+ * bfloat16 state, updated in place (FlashInfer gdn_decode_bf16_state.py,
+ * public gated_delta_rule and compute_single_gate):
+ *   q, k     [B, T, H, K]     bf16
+ *   v        [B, T, HV, V]    bf16      value head hv reads key head hv/(HV/H)
+ *   a, b     [B, T, HV]       bf16      gate inputs
+ *   A_log    [HV]             float32
+ *   dt_bias  [HV]             float32
+ *   state    [pool, HV, V, K] bf16      K fastest; slot slot_indices[b] is
+ *                                       read, advanced by the T tokens in
+ *                                       float32 and written back once
+ *                                       (round to nearest even)
+ *   slot_indices [B]          int32     NULL = identity (needs pool >= B).
+ *                                       Slots must be distinct; a slot
+ *                                       outside [0, pool) records
+ *                                       GDN_ERR_BAD_SLOT and that entry's o
+ *                                       is written as zeros.
+ *   o        [B, T, HV, V]    bf16
+ * Per token: g = -exp(A_log) * softplus(a + dt_bias) with
+ *   softplus(x) = log(1 + exp(beta_sp x)) / beta_sp if beta_sp x <= threshold
+ *   else x; beta = sigmoid(b); if use_qk_l2norm, q and k are divided by
+ *   sqrt(sum(x^2) + eps); q is multiplied by scale.
+ * Limits: K == V == 128, 1 <= T <= 4, HV % H == 0.  scale <= 0 selects
+ * 1/sqrt(K); softplus_beta <= 0 selects 1; eps < 0 selects 1e-6.
+ */
+typedef struct gdn_decode_args {
+  const void *q, *k, *v;
+  const void *a, *b;
+  const float *A_log, *dt_bias;
+  void *state;
+  const int32_t *slot_indices;
+  void *o;
+  int32_t B, T, H, HV, K, V, pool;
+  int32_t use_qk_l2norm;
+  float scale, softplus_beta, softplus_threshold, eps;
+} gdn_decode_args;
+
+gdn_status_t gdn_decode(const gdn_decode_args *args, gdn_stream_t stream);
+
+/* Wait for `stream`, then read and clear the device error word of the current
+ * device into *code (a gdn_status_t value, GDN_OK if nothing was recorded).
+ * The word is shared by every stream of the device: the first error recorded
+ * since the last clear is kept. */
+gdn_status_t gdn_check_device_error(gdn_stream_t stream, int32_t *code);
+
+/* Static, NUL-terminated name of a status. */
+const char *gdn_status_string(gdn_status_t status);
+
+/* Description of the calling thread's last host-side failure ("" if none). */
+const char *gdn_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

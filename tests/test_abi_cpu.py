@@ -1,0 +1,179 @@
+"""Host-side checks of the C interface that need no GPU.
+
+The library is loaded (built first if needed), every function the header
+declares must be exported, the ctypes structures must match the C layout
+(checked by compiling a probe against include/gdn.h with gcc), and argument
+errors must come back as status codes before any CUDA call is made.
+"""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+from gated_delta_rule_kk_gb300 import _lib, build_lib
+from gated_delta_rule_kk_gb300._lib import GdnChunkArgs, GdnDecodeArgs, KdaChunkArgs, Status
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|gdn_status_t)\s*(\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("gdn_chunk_fwd", "kda_chunk_fwd", "gdn_decode", "gdn_check_device_error",
+              "gdn_chunk_workspace_size", "kda_chunk_workspace_size", "gdn_status_string",
+              "gdn_last_error_message"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    for s in Status:
+        assert lib.gdn_status_string(int(s)).decode() == "GDN_" + ("OK" if s == 0 else "ERR_" + s.name)
+    assert lib.gdn_status_string(99).decode() == "GDN_ERR_UNKNOWN"
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_ctypes_structs_match_c_layout():
+    probe = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "gdn.h"
+#define F(S, f) printf(#S " " #f " %zu\n", offsetof(S, f));
+int main(void) {
+  printf("gdn_chunk_args size %zu\n", sizeof(gdn_chunk_args));
+  printf("kda_chunk_args size %zu\n", sizeof(kda_chunk_args));
+  printf("gdn_decode_args size %zu\n", sizeof(gdn_decode_args));
+  %FIELDS%
+  return 0;
+}
+"""
+    lines = []
+    for cname, cls in (("gdn_chunk_args", GdnChunkArgs), ("kda_chunk_args", KdaChunkArgs),
+                       ("gdn_decode_args", GdnDecodeArgs)):
+        for fname, _ in cls._fields_:
+            lines.append(f"F({cname}, {fname})")
+    src = probe.replace("%FIELDS%", "\n  ".join(lines))
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "probe.c")
+        exe = os.path.join(d, "probe")
+        open(c, "w").write(src)
+        subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
+        out = subprocess.check_output([exe], text=True).split("\n")
+    got = {}
+    for ln in out:
+        if ln.strip():
+            s, f, v = ln.split()
+            got[(s, f)] = int(v)
+    for cname, cls in (("gdn_chunk_args", GdnChunkArgs), ("kda_chunk_args", KdaChunkArgs),
+                       ("gdn_decode_args", GdnDecodeArgs)):
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
+
+
+# ---- argument checks: all of these return before any CUDA call -------------
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def good_chunk(**kw):
+    a = dict(dtype=1, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, ht=None, o=FAKE,
+             cu_seqlens=None, B=2, T=128, H=4, Hg=2, K=128, V=128, N=2, chunk_size=64,
+             g_is_cumsum=0, scale=0.0, workspace=None, workspace_bytes=0)
+    a.update(kw)
+    return GdnChunkArgs(**a)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(q=None), Status.INVALID_ARG),
+    (dict(o=None), Status.INVALID_ARG),
+    (dict(beta=None), Status.INVALID_ARG),
+    (dict(k=FAKE + 2), Status.MISALIGNED),
+    (dict(h0=FAKE + 8), Status.MISALIGNED),
+    (dict(dtype=7), Status.INVALID_ARG),
+    (dict(chunk_size=32), Status.UNSUPPORTED),
+    (dict(K=256), Status.UNSUPPORTED),
+    (dict(H=5), Status.UNSUPPORTED),
+    (dict(B=0), Status.INVALID_ARG),
+    (dict(N=3), Status.INVALID_ARG),
+    (dict(cu_seqlens=FAKE), Status.INVALID_ARG),  # B=2 with cu_seqlens
+    (dict(g_is_cumsum=2), Status.INVALID_ARG),
+    (dict(scale=float("nan")), Status.INVALID_ARG),
+])
+def test_gdn_chunk_argument_errors(lib, change, expect):
+    a = good_chunk(**change)
+    st = lib.gdn_chunk_fwd(ctypes.byref(a), None)
+    assert st == expect, (change, Status(st), lib.gdn_last_error_message())
+    assert lib.gdn_last_error_message().decode() != ""
+
+
+def test_null_args_pointer(lib):
+    assert lib.gdn_chunk_fwd(None, None) == Status.INVALID_ARG
+    assert lib.kda_chunk_fwd(None, None) == Status.INVALID_ARG
+    assert lib.gdn_decode(None, None) == Status.INVALID_ARG
+    assert lib.gdn_check_device_error(None, None) == Status.INVALID_ARG
+
+
+def test_kda_head_grouping_error(lib):
+    a = KdaChunkArgs(dtype=1, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, o=FAKE, B=1, T=64,
+                     H=3, HV=4, K=128, V=128, N=1, chunk_size=64, g_is_cumsum=1)
+    assert lib.kda_chunk_fwd(ctypes.byref(a), None) == Status.UNSUPPORTED
+
+
+def good_decode(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, state=FAKE,
+             slot_indices=None, o=FAKE, B=4, T=1, H=2, HV=4, K=128, V=128, pool=4,
+             use_qk_l2norm=1, scale=0.0, softplus_beta=1.0, softplus_threshold=20.0, eps=1e-6)
+    a.update(kw)
+    return GdnDecodeArgs(**a)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(T=0), Status.UNSUPPORTED),
+    (dict(T=5), Status.UNSUPPORTED),
+    (dict(K=64), Status.UNSUPPORTED),
+    (dict(V=96), Status.UNSUPPORTED),
+    (dict(HV=3), Status.UNSUPPORTED),
+    (dict(pool=2), Status.INVALID_ARG),   # identity slots need pool >= B
+    (dict(state=None), Status.INVALID_ARG),
+    (dict(A_log=FAKE + 4), Status.MISALIGNED),
+    (dict(slot_indices=FAKE + 4), Status.MISALIGNED),
+    (dict(use_qk_l2norm=3), Status.INVALID_ARG),
+    (dict(eps=float("inf")), Status.INVALID_ARG),
+])
+def test_decode_argument_errors(lib, change, expect):
+    a = good_decode(**change)
+    assert lib.gdn_decode(ctypes.byref(a), None) == expect
+
+
+def test_workspace_size_is_zero(lib):
+    a = good_chunk()
+    n = ctypes.c_size_t(123)
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
+    assert n.value == 0
+    k = KdaChunkArgs()
+    n = ctypes.c_size_t(123)
+    assert lib.kda_chunk_workspace_size(ctypes.byref(k), ctypes.byref(n)) == Status.OK
+    assert n.value == 0

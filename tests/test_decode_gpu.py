@@ -1,0 +1,107 @@
+"""Decode step (T = 1..4) on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_kk_gb300 import Status, gdn_check_device_error, gdn_decode
+from gated_delta_rule_kk_gb300 import synth
+from oracle import recurrence as R
+
+from _util import TOL_BF16, assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp, **kw):
+    d = to_dev(inp)
+    state = d["state"].clone()
+    o = gdn_decode(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], state,
+                   slot_indices=d["slot_indices"], scale=d["scale"], **kw)
+    return o, state
+
+
+def oracle_for(inp, batch, **kw):
+    """Oracle on the batch entries `batch`, with only their slots of the pool."""
+    slots = inp["slot_indices"]
+    slots = np.arange(inp["dims"]["B"]) if slots is None else slots.numpy()
+    sel = list(batch)
+    return R.gdn_decode(inp["q"][sel], inp["k"][sel], inp["v"][sel], inp["a"][sel],
+                        inp["b"][sel], inp["A_log"], inp["dt_bias"],
+                        inp["state"][torch.as_tensor(np.asarray(slots)[sel])], None,
+                        scale=inp["scale"], **kw)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_small_batch(T):
+    inp = synth.decode_inputs(300 + T, 6, T, 2, 4, 128, 128)
+    o, state = run_gpu(inp)
+    assert gdn_check_device_error() == Status.OK
+    o_ref, st_ref = oracle_for(inp, range(6))
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(state, st_ref, TOL_BF16, "state")
+
+
+def test_permuted_slots_pool_larger_than_batch():
+    slots = [5, 0, 3]
+    inp = synth.decode_inputs(311, 3, 2, 1, 2, 128, 128, pool=7, slots=slots)
+    o, state = run_gpu(inp)
+    assert gdn_check_device_error() == Status.OK
+    o_ref, st_ref = oracle_for(inp, range(3))
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(state[slots], st_ref, TOL_BF16, "state")
+    untouched = [1, 2, 4, 6]
+    assert torch.equal(state[untouched].cpu(), inp["state"][untouched])
+
+
+def test_without_l2norm_and_custom_gate_params():
+    inp = synth.decode_inputs(312, 4, 3, 2, 2, 128, 128)
+    inp["q"] = (inp["q"].float() * 0.05).bfloat16()
+    inp["k"] = (inp["k"].float() * 0.05).bfloat16()
+    kw = dict(use_qk_l2norm=False, softplus_beta=2.0, softplus_threshold=1.0)
+    o, state = run_gpu(inp, **kw)
+    o_ref, st_ref = oracle_for(inp, range(4), use_qk_l2norm=False, softplus_beta=2.0,
+                               softplus_threshold=1.0)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(state, st_ref, TOL_BF16, "state")
+
+
+def test_bad_slot_is_reported_and_skipped():
+    inp = synth.decode_inputs(313, 3, 1, 1, 1, 128, 128, pool=3, slots=[0, 9, 2])
+    o, state = run_gpu(inp)
+    assert gdn_check_device_error() == Status.BAD_SLOT
+    assert torch.count_nonzero(o[1]).item() == 0
+    o_ref, st_ref = oracle_for(dict(inp, slot_indices=torch.tensor([0, 0, 2], dtype=torch.int32)),
+                               [0, 2])
+    assert_close(o[[0, 2]], o_ref, TOL_BF16, "o")
+    assert_close(state[[0, 2]], st_ref, TOL_BF16, "state")
+    assert torch.equal(state[1].cpu(), inp["state"][1])
+
+
+def test_chained_calls_equal_one_multi_token_call():
+    inp = synth.decode_inputs(314, 4, 4, 2, 4, 128, 128)
+    o4, st4 = run_gpu(inp)
+    d = to_dev(inp)
+    st = d["state"].clone()
+    outs = []
+    for t in range(4):
+        sl = slice(t, t + 1)
+        outs.append(gdn_decode(d["q"][:, sl].contiguous(), d["k"][:, sl].contiguous(),
+                               d["v"][:, sl].contiguous(), d["a"][:, sl].contiguous(),
+                               d["b"][:, sl].contiguous(), d["A_log"], d["dt_bias"], st))
+    # single-token calls round the state to bf16 between tokens, so compare
+    # both against the oracle rather than bit for bit
+    o_ref, st_ref = oracle_for(inp, range(4))
+    assert_close(torch.cat(outs, dim=1), o_ref, TOL_BF16, "chained o")
+    assert_close(st, st_ref, TOL_BF16, "chained state")
+    assert_close(o4, o_ref, TOL_BF16, "o")
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_decode_workload_sampled(T):
+    inp = synth.decode(T)
+    o, state = run_gpu(inp)
+    assert gdn_check_device_error() == Status.OK
+    sample = [0, 1, 77, 128, 200, 255]
+    o_ref, st_ref = oracle_for(inp, sample)
+    assert_close(o[sample], o_ref, TOL_BF16, "o")
+    assert_close(state[sample], st_ref, TOL_BF16, "state")

@@ -1,0 +1,86 @@
+"""KDA (per-channel gate) chunked forward on the GPU against the fp64 oracle."""
+import pytest
+import torch
+
+from gated_delta_rule_kk_gb300 import Status, gdn_check_device_error, gdn_chunk_fwd, kda_chunk_fwd
+from gated_delta_rule_kk_gb300 import synth
+from oracle import recurrence as R
+
+from _util import TOL_BF16, TOL_F32, assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp):
+    d = to_dev(inp)
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                          initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+                          g_is_cumsum=d["g_is_cumsum"])
+    assert gdn_check_device_error() == Status.OK
+    return o, ht
+
+
+def run_oracle(inp, heads=None, seqs=None):
+    return R.kda_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                           scale=inp["scale"], h0=inp["h0"], cu_seqlens=inp["cu_seqlens"],
+                           g_is_cumsum=inp["g_is_cumsum"], heads=heads, seqs=seqs)
+
+
+@pytest.mark.parametrize("T,K,V,H,HV,dtype,h0", [
+    (150, 32, 32, 1, 2, torch.float32, True),     # tail, grouped value heads
+    (64, 128, 64, 2, 2, torch.float32, False),
+    (257, 128, 128, 2, 4, torch.bfloat16, True),
+    (5, 48, 40, 1, 1, torch.float32, True),       # shorter than a sub-chunk
+])
+def test_small_shapes(T, K, V, H, HV, dtype, h0):
+    inp = synth.prefill_inputs(200 + T, 1, T, HV, H, K, V, dtype=dtype,
+                               h0_std=0.1 if h0 else None, per_channel=True)
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert_close(o, o_ref, tol, "o")
+    assert_close(ht, ht_ref, tol, "ht")
+
+
+def test_raw_gate_input_and_varlen():
+    lengths = [70, 0, 9, 128]
+    T = sum(lengths)
+    inp = synth.prefill_inputs(31, 1, T, 2, 2, 64, 64, dtype=torch.float32, h0_std=0.1,
+                               lengths=lengths, per_channel=True)
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(o, o_ref, TOL_F32, "o")
+    assert_close(ht, ht_ref, TOL_F32, "ht")
+    # the same gates handed over raw (difference the chunk-local cumsum back)
+    cu = inp["cu_seqlens"].tolist()
+    g = inp["g"].double().clone()
+    raw = g.clone()
+    for n in range(len(lengths)):
+        for t in range(cu[n], cu[n + 1]):
+            if (t - cu[n]) % 64:
+                raw[:, t] = g[:, t] - g[:, t - 1]
+    inp2 = dict(inp, g=raw.float(), g_is_cumsum=False)
+    o2, ht2 = run_gpu(inp2)
+    o_ref2, ht_ref2 = run_oracle(inp2)
+    assert_close(o2, o_ref2, TOL_F32, "o (raw gate)")
+    assert_close(ht2, ht_ref2, TOL_F32, "ht (raw gate)")
+
+
+def test_channel_constant_gate_equals_gdn():
+    inp = synth.prefill_inputs(41, 1, 200, 2, 2, 64, 64, dtype=torch.float32, h0_std=0.1)
+    d = to_dev(inp)
+    o1, ht1 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"])
+    gk = d["g"][..., None].expand(-1, -1, -1, 64).contiguous()
+    o2, ht2 = kda_chunk_fwd(d["q"], d["k"], d["v"], gk, d["beta"], initial_state=d["h0"],
+                            g_is_cumsum=False)
+    assert_close(o2, o1.cpu().double().numpy(), 1e-5, "o")
+    assert_close(ht2, ht1.cpu().double().numpy(), 1e-5, "ht")
+
+
+def test_kda_prefill_workload_sampled():
+    inp = synth.kda_prefill()
+    o, ht = run_gpu(inp)
+    for h in (0, 17, 31):
+        o_ref, ht_ref = run_oracle(inp, heads=[h], seqs=[0])
+        assert_close(o[0, :, h], o_ref[0, :, h], TOL_BF16, f"o head {h}")
+        assert_close(ht[0, h], ht_ref[0, h], TOL_BF16, f"ht head {h}")
