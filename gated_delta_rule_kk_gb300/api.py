@@ -79,9 +79,26 @@ def _chunk_common(q, k, v, g, beta, initial_state, cu_seqlens, output_final_stat
     return dt, (B, T, Hk, Hv, K, V, N), out, final_state
 
 
+def _attach_workspace(args, size_fn, workspace, device):
+    """Ask the library how much scratch the call needs and hand it a buffer
+    (from PyTorch's caching allocator unless the caller passes one)."""
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _lib.check(size_fn(lib)(ctypes.byref(args), ctypes.byref(n)), "workspace_size")
+    if n.value == 0:
+        return None
+    if workspace is None:
+        workspace = torch.empty(n.value, dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < n.value or not workspace.is_cuda:
+        raise ValueError(f"workspace needs {n.value} bytes on the GPU")
+    args.workspace = ctypes.c_void_p(workspace.data_ptr())
+    args.workspace_bytes = workspace.numel() * workspace.element_size()
+    return workspace
+
+
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
-                  stream=None):
+                  workspace=None, stream=None):
     """GDN chunked forward.  Returns ``(o, ht)`` (``ht`` None if not requested).
 
     q, k [B,T,Hg,K]; v [B,T,H,V]; g, beta [B,T,H] float32; initial_state
@@ -95,14 +112,16 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
                      g_is_cumsum=int(bool(g_is_cumsum)),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
+    ws = _attach_workspace(a, lambda lib: lib.gdn_chunk_workspace_size, workspace, q.device)
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_fwd")
+    del ws  # the caching allocator keeps it valid for work already on `stream`
     return out, ht
 
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=True, out=None, final_state=None,
-                  stream=None):
+                  workspace=None, stream=None):
     """KDA chunked forward.  Returns ``(o, ht)``.
 
     q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV,K] float32 (chunk-local cumsum
@@ -116,8 +135,10 @@ def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
                      g_is_cumsum=int(bool(g_is_cumsum)),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
+    ws = _attach_workspace(a, lambda lib: lib.kda_chunk_workspace_size, workspace, q.device)
     lib = _lib.load()
     _lib.check(lib.kda_chunk_fwd(ctypes.byref(a), _stream(stream)), "kda_chunk_fwd")
+    del ws
     return out, ht
 
 

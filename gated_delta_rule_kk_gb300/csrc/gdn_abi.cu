@@ -89,6 +89,44 @@ gdn_status_t cuda_status(cudaError_t e, const char *what) {
   return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+ChunkParams gdn_params(const gdn_chunk_args &a) {
+  ChunkParams p{};
+  p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.beta = a.beta; p.h0 = a.h0; p.ht = a.ht;
+  p.o = a.o; p.cu_seqlens = a.cu_seqlens;
+  p.B = a.B; p.T = a.T; p.H = a.H; p.Hk = a.Hg; p.K = a.K; p.V = a.V; p.N = a.N;
+  p.g_is_cumsum = a.g_is_cumsum;
+  p.scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)(a.K > 0 ? a.K : 1));
+  return p;
+}
+
+ChunkParams kda_params(const kda_chunk_args &a) {
+  ChunkParams p{};
+  p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.beta = a.beta; p.h0 = a.h0; p.ht = a.ht;
+  p.o = a.o; p.cu_seqlens = a.cu_seqlens;
+  p.B = a.B; p.T = a.T; p.H = a.HV; p.Hk = a.H; p.K = a.K; p.V = a.V; p.N = a.N;
+  p.g_is_cumsum = a.g_is_cumsum;
+  p.scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)(a.K > 0 ? a.K : 1));
+  return p;
+}
+
+// Launch either path: the tensor-core kernels when they serve the arguments,
+// else the exact fp32 CUDA-core kernel.
+gdn_status_t run_chunk(ChunkParams &p, bool bf16, bool kda, void *ws, size_t ws_bytes,
+                       cudaStream_t s) {
+  const bool tc = chunk_tc_supported(p, bf16);
+  if (tc) {
+    const size_t need = chunk_tc_workspace(p);
+    if (ws == nullptr || ws_bytes < need)
+      return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+      return fail(GDN_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+  }
+  p.err = device_error_word();
+  if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
+  if (tc) return cuda_status(launch_chunk_tc(p, kda, ws, s), "tensor-core chunk launch");
+  return cuda_status(launch_chunk_simt(p, bf16, kda, s), "chunk launch");
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -116,12 +154,16 @@ const char *gdn_last_error_message(void) { return g_msg; }
 gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *a, size_t *bytes) {
   if (a == nullptr || bytes == nullptr) return fail(GDN_ERR_INVALID_ARG, "NULL argument");
   *bytes = 0;
+  ChunkParams p = gdn_params(*a);
+  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *bytes = chunk_tc_workspace(p);
   return GDN_OK;
 }
 
 gdn_status_t kda_chunk_workspace_size(const kda_chunk_args *a, size_t *bytes) {
   if (a == nullptr || bytes == nullptr) return fail(GDN_ERR_INVALID_ARG, "NULL argument");
   *bytes = 0;
+  ChunkParams p = kda_params(*a);
+  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *bytes = chunk_tc_workspace(p);
   return GDN_OK;
 }
 
@@ -132,16 +174,9 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *a, gdn_stream_t stream) {
                                 a->cu_seqlens, a->B, a->T, a->Hg, a->H, a->K, a->V, a->N,
                                 a->chunk_size, a->g_is_cumsum, a->scale, "Hg");
   if (st != GDN_OK) return st;
-  ChunkParams p{};
-  p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0; p.ht = a->ht;
-  p.o = a->o; p.cu_seqlens = a->cu_seqlens;
-  p.B = a->B; p.T = a->T; p.H = a->H; p.Hk = a->Hg; p.K = a->K; p.V = a->V; p.N = a->N;
-  p.g_is_cumsum = a->g_is_cumsum;
-  p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)a->K);
-  p.err = device_error_word();
-  if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return cuda_status(launch_chunk_simt(p, a->dtype == GDN_BF16, false, s), "gdn chunk launch");
+  ChunkParams p = gdn_params(*a);
+  return run_chunk(p, a->dtype == GDN_BF16, false, a->workspace, a->workspace_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status_t kda_chunk_fwd(const kda_chunk_args *a, gdn_stream_t stream) {
@@ -151,16 +186,9 @@ gdn_status_t kda_chunk_fwd(const kda_chunk_args *a, gdn_stream_t stream) {
                                 a->cu_seqlens, a->B, a->T, a->H, a->HV, a->K, a->V, a->N,
                                 a->chunk_size, a->g_is_cumsum, a->scale, "H");
   if (st != GDN_OK) return st;
-  ChunkParams p{};
-  p.q = a->q; p.k = a->k; p.v = a->v; p.g = a->g; p.beta = a->beta; p.h0 = a->h0; p.ht = a->ht;
-  p.o = a->o; p.cu_seqlens = a->cu_seqlens;
-  p.B = a->B; p.T = a->T; p.H = a->HV; p.Hk = a->H; p.K = a->K; p.V = a->V; p.N = a->N;
-  p.g_is_cumsum = a->g_is_cumsum;
-  p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)a->K);
-  p.err = device_error_word();
-  if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return cuda_status(launch_chunk_simt(p, a->dtype == GDN_BF16, true, s), "kda chunk launch");
+  ChunkParams p = kda_params(*a);
+  return run_chunk(p, a->dtype == GDN_BF16, true, a->workspace, a->workspace_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status_t gdn_decode(const gdn_decode_args *a, gdn_stream_t stream) {

@@ -38,4 +38,11 @@ cudaError_t launch_chunk_simt(const ChunkParams &p, bool bf16, bool per_channel_
                               cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 
+// Tensor-core chunked forward (bf16, K = 128, V % 32 == 0): whether it serves
+// these arguments, the workspace it needs, and the launch.
+bool chunk_tc_supported(const ChunkParams &p, bool bf16);
+size_t chunk_tc_workspace(const ChunkParams &p);
+cudaError_t launch_chunk_tc(const ChunkParams &p, bool per_channel_gate, void *workspace,
+                            cudaStream_t stream);
+
 }  // namespace gdn

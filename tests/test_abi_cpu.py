@@ -168,12 +168,30 @@ def test_decode_argument_errors(lib, change, expect):
     assert lib.gdn_decode(ctypes.byref(a), None) == expect
 
 
-def test_workspace_size_is_zero(lib):
+def test_workspace_size(lib):
+    # the tensor-core path (bf16, K = 128, V % 32 == 0) needs per-(chunk, head)
+    # operand blocks of 66048 bytes plus a 256-byte chunk table
     a = good_chunk()
     n = ctypes.c_size_t(123)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
+    assert n.value == 256 + 2 * 2 * 4 * 66048
+    # packed sequences: at most ceil(T/64) + N chunks
+    a = good_chunk(B=1, N=3, cu_seqlens=FAKE, T=200)
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
+    assert n.value == 256 + (4 + 3) * 4 * 66048
+    # the exact fp32 path needs none
+    a = good_chunk(dtype=0)
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
     assert n.value == 0
-    k = KdaChunkArgs()
-    n = ctypes.c_size_t(123)
+    k = KdaChunkArgs(dtype=1, B=1, T=64, H=2, HV=2, K=128, V=64, N=1, chunk_size=64)
     assert lib.kda_chunk_workspace_size(ctypes.byref(k), ctypes.byref(n)) == Status.OK
-    assert n.value == 0
+    assert n.value == 256 + 1 * 2 * 66048
+
+
+def test_workspace_errors_found_on_host(lib):
+    a = good_chunk(workspace=None, workspace_bytes=0)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.WORKSPACE
+    a = good_chunk(workspace=FAKE, workspace_bytes=100)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.WORKSPACE
+    a = good_chunk(workspace=FAKE + 16, workspace_bytes=1 << 30)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.MISALIGNED
