@@ -1,42 +1,50 @@
 // Chunked forward on the 5th-generation tensor cores (tcgen05, TMEM
-// accumulators, TMA/bulk copies), bf16 inputs, K = 128, V a multiple of 32.
+// accumulators, TMA and bulk copies), bf16 inputs, K = 128, V in {32..128}
+// a multiple of 32.
 //
-// Two kernels per call (plus a tiny chunk-table kernel for packed sequences):
+// Two kernels per call (plus a one-thread chunk-table kernel for packed
+// sequences):
 //
-// 1. intra (one CTA per (chunk, value head), all chunks in parallel).  With
-//    gamma the chunk-local cumulative gate and S = [k; q] k^T (one M=128
-//    tcgen05 GEMM):
-//      A   = beta_i S_kk[i,j] exp(gamma_i - gamma_j), i > j      (sglang
-//      Aqk = scale S_qk[i,j] exp(gamma_i - gamma_j),  i >= j     fla/chunk_fwd.py,
-//      T   = (I + A)^-1  (fp32: 16x16 diagonal blocks by forward  fused kernel
-//            substitution, then the block merge; Steps 3-4)       Steps 1-4)
-//      Tw  = T diag(beta exp(gamma)),  Tu = T diag(beta)
-//      [w; Aqk w] = [Tw; Aqk Tw] k          (WY recompute, tcgen05)
-//    and stores per (chunk, head) a block that holds everything the
-//    sequential pass needs as ready-made tcgen05 operand images:
-//      WQ = [-w ; scale exp(gamma) q - Aqk w]   (128 x 128, K-major)
-//      TU = [Tu ; Aqk Tu]                       (128 x 64,  K-major)
-//      KT = k exp(gamma_L - gamma)              (64 x 128, as keys x tokens)
-//      exp(gamma_L) per key row
-//    For the per-channel gate (KDA, vLLM kimi_k3 kda/chunk_intra) the
-//    exponentials move into the operands: S = [k e^g; q e^g] (k e^-g)^T with
-//    the chunk start as reference row, w = T diag(beta) (k e^g), and
-//    KT = k exp(gamma_L - gamma) per channel.
+// 1. intra: one CTA per (chunk, value head), all chunks in parallel.  With
+//    gamma the chunk-local cumulative gate and S = [k; q] k^T (one M = 128
+//    tcgen05 GEMM; sglang fla/chunk_fwd.py, fused KK^T + solve kernel):
+//      A   = beta_i S_kk[i,j] exp(gamma_i - gamma_j), i > j       (Steps 1-2)
+//      Aqk = scale S_qk[i,j] exp(gamma_i - gamma_j),  i >= j
+//      T   = (I + A)^-1 in fp32: 16 x 16 diagonal blocks by forward
+//            substitution, then the block merge                     (Steps 3-4)
+//      w   = T diag(beta e^gamma) k,  u = T diag(beta) v         (WY recompute)
+//    T enters the two WY GEMMs as a hi + lo pair of bf16 matrices, so w and u
+//    carry fp32-grade accuracy.  Per (chunk, head) the kernel stores a block
+//    the sequential pass consumes directly:
+//      W   -w (bf16, 64 x 128)            U   u (fp32, per 32-wide V tile)
+//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)  SC  exp(gamma_L) per key row,
+//                                              exp(gamma_L - gamma_i) and
+//                                              scale exp(gamma_i) per token
+//    For the per-channel gate (KDA, vLLM kimi_k3 kda/chunk_intra,
+//    chunk_kda_fwd_kernel_inter_solve_fused) the exponentials move into the
+//    operands: S = [k e^g; q e^g] (k e^-g)^T with the chunk start as the
+//    reference row, w = T diag(beta) (k e^g), and the block also holds
+//    QH = q e^g and KT = k e^{gamma_L - g}.
 //
-// 2. chain (one CTA per (32-wide V tile, value head, sequence)), the
-//    sequential inter-chunk pass with the fp32 state tile h[128, 32] held in
-//    registers (one key row per thread) for the whole sequence:
-//      D  = TU v_tile                  ([u; Aqk u])
-//      D += WQ bf16(h)                 (rows 0..63: v_new = u - w h,
-//                                       rows 64..127: o = q~ h + Aqk v_new)
-//      h  = exp(gamma_L) h + KT^T v_new
-//    (KDA _fla/ops/common/chunk_h.py, chunk_fwd_kernel_h, gives the state
-//    recurrence this delta form extends; o is fused into the same GEMM.)
+// 2. chain: one CTA per (32-wide V tile, value head, sequence), the
+//    sequential inter-chunk pass, warp-specialised: warp 4 streams the
+//    chunk operands in (bulk copies and TMA), warp 5 issues the tcgen05
+//    GEMMs, warps 0-3 (one TMEM lane and one key row of the fp32 state tile
+//    h[128, 32] per thread, kept in registers for the whole sequence) run
+//    the epilogues.  Per chunk
+//      D1  = [-w ; q~] bf16(h)            rows 0..63: -w h, rows 64..127: q h
+//      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
+//      DH  = k~^T (e^{gamma_L - gamma} v_new)
+//      D5  = [Aqk_lo ; Aqk_hi] v_new
+//      h   = exp(gamma_L) h + DH
+//      o   = scale e^gamma (q h) + Aqk v_new
+//    (KDA _fla/ops/common/chunk_h.py, chunk_fwd_kernel_h, is the gated state
+//    recurrence that this delta form extends; the output is fused into it.)
 //
 // Shared-memory operand images use the canonical no-swizzle layout: element
 // (r, c) of an image with column-group stride `cs` sits at
 // (c / 8) * cs + r * 16 + (c % 8) * 2 bytes, i.e. every group of 8 columns is
-// a contiguous run of 16-byte rows.  Read with rows as M/N (K-major) the
+// a contiguous run of 16-byte rows.  Read with rows as M/N (K-major) its
 // descriptor has LBO = cs, SBO = 128; read with rows as K (MN-major) it has
 // LBO = 128, SBO = cs.
 #include <cuda.h>
@@ -51,13 +59,16 @@ namespace tc {
 
 constexpr int KD = 128;
 constexpr int VTILE = 32;
-constexpr uint32_t WQ_BYTES = 32768, TU_BYTES = 16384, KT_BYTES = 16384, GATE_BYTES = 512;
-constexpr uint32_t OFF_WQ = 0, OFF_TU = WQ_BYTES, OFF_KT = OFF_TU + TU_BYTES,
-                   OFF_GATE = OFF_KT + KT_BYTES;
-constexpr uint32_t BLOCK_BYTES = OFF_GATE + GATE_BYTES;  // 66048
-constexpr uint32_t VT_BYTES = 64 * VTILE * 2;            // 4096
-constexpr uint32_t STAGE_BYTES = BLOCK_BYTES + VT_BYTES;
+constexpr int VMAX = 128;
 constexpr float GATE_FACTOR_LIMIT = 80.f;  // |gamma| bound for split exponentials
+
+// per (chunk, head) block in the workspace
+constexpr uint32_t OFF_W = 0, OFF_AQ = 16384, OFF_SC = 32768, OFF_U = 33792;
+__host__ __device__ constexpr uint32_t block_bytes(int V, bool kda) {
+  return OFF_U + (uint32_t)V * 256u + (kda ? 32768u : 0u);
+}
+__host__ __device__ constexpr uint32_t off_qh(int V) { return OFF_U + (uint32_t)V * 256u; }
+__host__ __device__ constexpr uint32_t off_kt(int V) { return off_qh(V) + 16384u; }
 
 __device__ __forceinline__ uint32_t img_off(int r, int c, uint32_t cs) {
   return (uint32_t)(c >> 3) * cs + (uint32_t)r * 16u + (uint32_t)(c & 7) * 2u;
@@ -87,6 +98,16 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
   return u;
 }
 
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 16 significant bits.
+__device__ __forceinline__ void split8(const float *f, uint4 &hi, uint4 &lo) {
+  float r[8];
+  hi = pack8(f);
+  unpack8(hi, r);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) r[e] = f[e] - r[e];
+  lo = pack8(r);
+}
+
 struct TcParams {
   const float *g, *beta, *h0;
   float *ht;
@@ -99,12 +120,8 @@ struct TcParams {
   int B, T, H, Hk, V, N, NT;  // NT: chunks per sequence without cu_seqlens
   int g_is_cumsum;
   float scale;
+  uint32_t block;          // bytes per (chunk, head) block
 };
-
-// Bounded wait shared by all threads; false means it gave up.
-__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
-  return ptx::mbar_wait_bounded(bar, parity);
-}
 
 // ---------------------------------------------------------------------------
 // chunk table for packed sequences: table[n] = sum_{m<n} ceil(len_m / 64)
@@ -201,47 +218,48 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
 }
 
 // ---------------------------------------------------------------------------
-// intra kernel
+// intra kernel (128 threads)
 //
 // shared memory (bytes):
 //   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys), cs 2048
-//   TA   [32768, 65536)    [Tw | Tu ; Aqk Tw | Aqk Tu] (128 x 128), cs 2048;
-//                          during the solve its start holds the merge scratch,
-//                          after the WY GEMM its first half holds KT (cs 1024)
-//   R1   [65536, 98816)    A, T fp32 (64 x 65 each); later WQ (cs 2048)
-//   AQK  [98816, 107008)   Aqk bf16 (64 x 64), cs 1024; KDA: also k e^-g
-//                          (64 x 128, cs 1024) in [98816, 115200)
-//   small                  gamma, factors, gate, barriers
-constexpr uint32_t I_KQ = 0, I_TA = 32768, I_R1 = 65536, I_AQK = 98816;
-constexpr uint32_t I_KB = I_AQK + 8192;     // KDA: k e^{-gamma} image (16 KB)
-constexpr uint32_t I_KT = I_KB + 16384;     // KDA: KT image (16 KB)
+//   VS   [32768, 49152)    v (64 tokens x V), cs 1024
+//   R1   [49152, 82432)    KDA gamma (fp32 64 x 128); then A | T (fp32, 64 x 65
+//                          each); after the solve Tw hi | Tw lo (64 x 64, cs
+//                          1024) over A
+//   AQ   [82432, 98816)    [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
+//                          Tu hi | Tu lo
+//   KB   [98816, 115200)   KDA: k e^-g (64 x 128, cs 1024)
+//   KT   [115200, 131584)  KDA: k e^{gamma_L - g} (64 x 128, cs 1024)
+//   small                  scales, gamma, factors, merge scratch, barriers
+constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 82432, I_KB = 98816,
+                   I_KT = 115200;
 template <bool KDA>
 struct IntraLayout {
-  static constexpr uint32_t SMALL = KDA ? I_KT + 16384 : I_AQK + 8192 + 1024;
-  static constexpr uint32_t SMEM = SMALL + 4096;
+  static constexpr uint32_t SMALL = KDA ? I_KT + 16384 : I_KB;
+  static constexpr uint32_t SMEM = SMALL + 8192;
 };
 
 template <bool KDA>
 __global__ void __launch_bounds__(128, 1)
 intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-             TcParams p) {
+             const __grid_constant__ CUtensorMap tm_v, TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *KQ = smem + I_KQ;
-  unsigned char *TA = smem + I_TA;
+  unsigned char *VS = smem + I_VS;
   float *Asm = reinterpret_cast<float *>(smem + I_R1);
   float *Tsm = Asm + 64 * 65;
-  unsigned char *WQ = smem + I_R1;
-  unsigned char *AQK = smem + I_AQK;
+  unsigned char *TW = smem + I_R1;   // Tw hi, Tw lo (after the solve)
+  unsigned char *AQ = smem + I_AQ;   // Aqk pair, later Tu hi, Tu lo
   unsigned char *KB = smem + I_KB;
-  unsigned char *KTs = KDA ? smem + I_KT : TA;  // GDN: KT reuses TA's first half
-  float *Xs = reinterpret_cast<float *>(smem + I_TA);
-  float *gam = reinterpret_cast<float *>(smem + IntraLayout<KDA>::SMALL);  // [64]
+  unsigned char *KTs = smem + I_KT;
+  float *sc = reinterpret_cast<float *>(smem + IntraLayout<KDA>::SMALL);  // decay, rs, qs
+  float *gam = sc + 256;                                   // [64]
   float *bet = gam + 64;                                   // [64]
   float *eg = bet + 64;                                    // [64] e^{gamma}
   float *eng = eg + 64;                                    // [64] e^{-gamma}
-  float *gate = eng + 64;                                  // [128] e^{gamma_L}
-  float *gl = gate + 128;                                  // [128] KDA gamma_L
-  uint64_t *bars = reinterpret_cast<uint64_t *>(gl + 128); // tma, mma
+  float *gl = eng + 64;                                    // [128] KDA gamma_L
+  float *Xs = gl + 128;                                    // merge scratch 3 x 16 x 17
+  uint64_t *bars = reinterpret_cast<uint64_t *>(Xs + 3 * 16 * 17 + 4);  // tma, mma
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
   int *flags = reinterpret_cast<int *>(tmem_slot + 1);     // [0]: split exps ok
 
@@ -250,11 +268,11 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   ChunkPos cp;
   if (!locate_chunk(p, blockIdx.x, cp)) return;
   const int hk = h / (p.H / p.Hk);
+  const int V = p.V;
   const int s0 = cp.bos + cp.c * BT;
   const int L = min(BT, cp.eos - s0);
   const int row0 = cp.b * p.T + s0;  // token row in the [B*T] flattening
-  const int chunk_id = blockIdx.x;
-  unsigned char *blk = p.blocks + ((size_t)chunk_id * p.H + h) * BLOCK_BYTES;
+  unsigned char *blk = p.blocks + ((size_t)blockIdx.x * p.H + h) * p.block;
 
   if (tid == 0) {
     ptx::mbar_init(&bars[0], 1);
@@ -262,28 +280,29 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::fence_mbar_init();
     flags[0] = 1;
   }
-  if (warp == 0) ptx::tmem_alloc<128>(tmem_slot);
+  if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(&bars[0], 32768);
+    ptx::mbar_arrive_expect_tx(&bars[0], 32768 + (uint32_t)V * 128);
 #pragma unroll 1
     for (int j = 0; j < 16; ++j) {
       ptx::tma_load_3d(KQ + j * 2048, &tm_k, 8 * j, hk, row0, &bars[0]);
       ptx::tma_load_3d(KQ + j * 2048 + 1024, &tm_q, 8 * j, hk, row0, &bars[0]);
     }
+#pragma unroll 1
+    for (int j = 0; j < V / 8; ++j) ptx::tma_load_3d(VS + j * 1024, &tm_v, 8 * j, h, row0, &bars[0]);
   }
 
-  // ---- gates: gamma (chunk-local inclusive cumsum), beta
+  // ---- gates: gamma (chunk-local inclusive cumsum), beta, scales
   if (tid < 64) bet[tid] = tid < L ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
-  bool gate_ok = true;
   if (!KDA) {
     if (warp == 0) {
-      float a0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
-      float a1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+      const float a0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
+      const float a1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
       float c0, c1;
       if (p.g_is_cumsum) {
         c0 = a0;
@@ -308,50 +327,53 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       if (!__all_sync(0xffffffffu, ok) && lane == 0) flags[0] = 0;
     }
     __syncthreads();
+    const float gL = gam[L - 1];
     if (tid < 64) {
       eg[tid] = __expf(gam[tid]);
       eng[tid] = __expf(-gam[tid]);
+      sc[128 + tid] = tid < L ? __expf(gL - gam[tid]) : 0.f;  // rs: e^{gamma_L - gamma_i}
+      sc[192 + tid] = p.scale * __expf(gam[tid]);              // qs: scale e^{gamma_i}
     }
-    if (tid < KD) gate[tid] = __expf(gam[L - 1]);
+    sc[tid] = __expf(gL);                                      // decay per key row
   } else {
     // thread c owns key channel c: running cumsum down the 64 rows into R1
-    // (fp32 [64][128]); gamma of padded rows repeats row L - 1
-    float *G = Asm;  // R1 is free until the solve
+    // (fp32 [64][128]); padded rows repeat row L - 1
+    float *G = Asm;
     const int c = tid;
     float acc = 0.f, mn = 0.f, mx = 0.f;
     for (int i = 0; i < 64; ++i) {
-      float gv;
       if (i < L) {
         const float raw = p.g[((size_t)(row0 + i) * p.H + h) * KD + c];
         acc = p.g_is_cumsum ? raw : acc + raw;
-        gv = acc;
-      } else {
-        gv = acc;
       }
-      G[i * KD + c] = gv;
-      mn = fminf(mn, gv);
-      mx = fmaxf(mx, gv);
+      G[i * KD + c] = acc;
+      mn = fminf(mn, acc);
+      mx = fmaxf(mx, acc);
     }
     gl[c] = acc;
-    gate[c] = __expf(acc);
-    gate_ok = mn >= -GATE_FACTOR_LIMIT && mx <= GATE_FACTOR_LIMIT;
-    if (!__syncthreads_and(gate_ok) && tid == 0) flags[0] = 0;
+    sc[c] = __expf(acc);
+    if (tid < 64) {
+      sc[128 + tid] = tid < L ? 1.f : 0.f;
+      sc[192 + tid] = p.scale;
+    }
+    const bool ok = mn >= -GATE_FACTOR_LIMIT && mx <= GATE_FACTOR_LIMIT;
+    if (!__syncthreads_and(ok) && tid == 0) flags[0] = 0;
   }
   __syncthreads();
 
-  const bool ok_tma = wait_all(&bars[0], 0);
+  const bool ok_tma = ptx::mbar_wait_bounded(&bars[0], 0);
   if (!__syncthreads_and(ok_tma)) {
     if (tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 0) ptx::tmem_dealloc<128>(tmem);
+    if (warp == 0) ptx::tmem_dealloc<256>(tmem);
     return;
   }
   const bool split = flags[0] != 0;
 
   if (KDA) {
-    // KQ <- [k e^g ; q e^g] (never overflows: gamma <= 80),
-    // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g} (exact)
+    // KQ <- [k e^g ; q e^g] (bounded by |k|, |q| for gates <= 0),
+    // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g}
     const float *G = Asm;
     for (int pc = tid; pc < 64 * 16; pc += 128) {
       const int i = pc & 63, cg = pc >> 6;
@@ -381,7 +403,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
 
   // ---- S = [k; q] k^T  (M = 128, N = 64, K = 128)
-  const uint32_t dS = tmem;  // columns [0, 64)
   uint32_t mma_phase = 0;
   if (tid == 0) {
     ptx::tc_fence_after();
@@ -392,11 +413,11 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     for (int ks = 0; ks < 8; ++ks) {
       const uint64_t a = ptx::sdesc(KQ + ks * 2 * 2048, 2048, 128);
       const uint64_t b = ptx::sdesc(Bop + ks * 2 * b_cs, b_cs, 128);
-      ptx::mma_bf16(dS, a, b, id, ks > 0);
+      ptx::mma_bf16(tmem, a, b, id, ks > 0);
     }
     ptx::mma_commit(&bars[1]);
   }
-  const bool ok1 = wait_all(&bars[1], mma_phase);
+  const bool ok1 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
   mma_phase ^= 1;
   ptx::tc_fence_after();
 
@@ -404,8 +425,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   {
     float srow[64];
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    ptx::tmem_ld32(dS + lane_base, srow);
-    ptx::tmem_ld32(dS + lane_base + 32, srow + 32);
+    ptx::tmem_ld32(tmem + lane_base, srow);
+    ptx::tmem_ld32(tmem + lane_base + 32, srow + 32);
     const int i = tid & 63;
     const bool is_q = tid >= 64;
     if (KDA && !split) {
@@ -413,8 +434,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       // range): raw k/q from global memory, gamma from R1
       const float *G = Asm;
       const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.kraw);
-      const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.qraw);
-      const __nv_bfloat16 *xg = is_q ? qg : kg;
+      const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(is_q ? p.qraw : p.kraw);
       for (int j = 0; j < 64; ++j) {
         float acc = 0.f;
         if (i < L && j <= i) {
@@ -433,35 +453,45 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       const float bi = bet[i];
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
-        float f;
-        if (KDA) f = 1.f;
-        else f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
+        float f = 1.f;
+        if (!KDA) f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
         Asm[i * 65 + j] = (j < i && i < L) ? bi * f * srow[j] : 0.f;
       }
     } else {
-      // Aqk (bf16 image, cs 1024): scale S_qk e^{g_i - g_j}, j <= i < L
+      // Aqk = scale S_qk e^{g_i - g_j} (j <= i < L) as a bf16 pair:
+      // hi in rows 64.., lo in rows 0.. of the AQ image
 #pragma unroll
       for (int cg = 0; cg < 8; ++cg) {
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int j = cg * 8 + e;
-          float f;
-          if (KDA) f = 1.f;
-          else f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
+          float f = 1.f;
+          if (!KDA) f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
           v8[e] = (j <= i && i < L) ? p.scale * f * srow[j] : 0.f;
         }
-        *reinterpret_cast<uint4 *>(AQK + img_off(i, 8 * cg, 1024)) = pack8(v8);
+        uint4 hi, lo;
+        split8(v8, hi, lo);
+        *reinterpret_cast<uint4 *>(AQ + img_off(64 + i, 8 * cg, 2048)) = hi;
+        *reinterpret_cast<uint4 *>(AQ + img_off(i, 8 * cg, 2048)) = lo;
       }
     }
   }
+  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
+  if (tid == 0) {
+    ptx::bulk_s2g(blk + OFF_AQ, AQ, 16384);
+    ptx::bulk_commit();
+  }
 
   // ---- T = (I + A)^-1 (fp32)
   unit_lower_inverse_64(Asm, Tsm, Xs, tid);
+  if (tid == 0) ptx::bulk_wait_read<0>();  // AQ may be overwritten after the barrier
+  __syncthreads();
 
-  // ---- TA rows 0..63: Tw = T diag(dw), Tu = T diag(beta)  (lower triangle)
+  // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) -> TW hi | lo;
+  //      Tu = T diag(beta) -> AQ region hi | lo  (64 x 64 each, cs 1024)
   for (int pc = tid; pc < 64 * 16; pc += 128) {
     const int i = pc & 63, cg = pc >> 6;
     const bool is_u = cg >= 8;
@@ -471,148 +501,127 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     for (int e = 0; e < 8; ++e) {
       const int j = j0 + e;
       const float t = (j <= i) ? Tsm[i * 65 + j] : 0.f;
-      const float d = is_u ? bet[j] : (KDA ? bet[j] : bet[j] * eg[j]);
+      const float d = (is_u || KDA) ? bet[j] : bet[j] * eg[j];
       v8[e] = t * d;
     }
-    *reinterpret_cast<uint4 *>(TA + img_off(i, 8 * cg, 2048)) = pack8(v8);
+    uint4 hi, lo;
+    split8(v8, hi, lo);
+    unsigned char *dst = is_u ? AQ : TW;
+    *reinterpret_cast<uint4 *>(dst + img_off(i, j0, 1024)) = hi;
+    *reinterpret_cast<uint4 *>(dst + 8192 + img_off(i, j0, 1024)) = lo;
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
 
-  // ---- P = Aqk [Tw | Tu]  (M = 64, N = 128, K = 64)
-  const uint32_t dP = tmem;
+  // ---- w = Tw k (N = 128 keys) and u = Tu v (N = V), M = 64, K = 64 tokens,
+  //      each as hi + lo passes accumulating in TMEM
+  const uint32_t dW = tmem, dU = tmem + 128;
   if (tid == 0) {
     ptx::tc_fence_after();
-    const uint32_t id = ptx::idesc_bf16(64, 128, 0, 1);
+    const uint32_t idw = ptx::idesc_bf16(64, 128, 0, 1);
+    const uint32_t idu = ptx::idesc_bf16(64, V, 0, 1);
 #pragma unroll 1
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = ptx::sdesc(AQK + ks * 2 * 1024, 1024, 128);
-      const uint64_t b = ptx::sdesc(TA + ks * 256, 128, 2048);
-      ptx::mma_bf16(dP, a, b, id, ks > 0);
-    }
-    ptx::mma_commit(&bars[1]);
-  }
-  const bool ok2 = wait_all(&bars[1], mma_phase);
-  mma_phase ^= 1;
-  ptx::tc_fence_after();
-  {
-    // M = 64 layout: row 16 w + l lives in lane 32 w + l (l < 16)
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int i = warp * 16 + (lane & 15);
+    for (int part = 0; part < 2; ++part) {
 #pragma unroll 1
-    for (int half = 0; half < 4; ++half) {
-      float v[32];
-      ptx::tmem_ld32(dP + lane_base + half * 32, v);
-      if (lane < 16) {
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8)
-          *reinterpret_cast<uint4 *>(TA + img_off(64 + i, half * 32 + q8 * 8, 2048)) =
-              pack8(v + q8 * 8);
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t b = ptx::sdesc(KQ + ks * 256, 128, 2048);
+        ptx::mma_bf16(dW, ptx::sdesc(TW + part * 8192 + ks * 2048, 1024, 128), b, idw,
+                      part > 0 || ks > 0);
+        const uint64_t bv = ptx::sdesc(VS + ks * 256, 128, 1024);
+        ptx::mma_bf16(dU, ptx::sdesc(AQ + part * 8192 + ks * 2048, 1024, 128), bv, idu,
+                      part > 0 || ks > 0);
       }
     }
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  __syncthreads();
-
-  // ---- [w; Aqk w] = [Tw; Aqk Tw] k  (M = 128, N = 128 keys, K = 64 tokens);
-  //      meanwhile TU (second half of TA) streams out to the block
-  const uint32_t dW = tmem;
-  if (tid == 0) {
-    ptx::tc_fence_after();
-    const uint32_t id = ptx::idesc_bf16(128, 128, 0, 1);
-#pragma unroll 1
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = ptx::sdesc(TA + ks * 2 * 2048, 2048, 128);
-      const uint64_t b = ptx::sdesc(KQ + ks * 256, 128, 2048);
-      ptx::mma_bf16(dW, a, b, id, ks > 0);
-    }
     ptx::mma_commit(&bars[1]);
-    ptx::bulk_s2g(blk + OFF_TU, TA + 16384, TU_BYTES);
+    if (KDA) {
+      // q e^g (KQ rows 64..127, cs 2048) -> QH (cs 1024); KT as is
+#pragma unroll 1
+      for (int g8 = 0; g8 < 16; ++g8)
+        ptx::bulk_s2g(blk + off_qh(V) + g8 * 1024, KQ + g8 * 2048 + 1024, 1024);
+      ptx::bulk_s2g(blk + off_kt(V), KTs, 16384);
+    }
+    ptx::bulk_s2g(blk + OFF_SC, sc, 1024);
     ptx::bulk_commit();
   }
-  const bool ok3 = wait_all(&bars[1], mma_phase);
+  const bool ok2 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
   mma_phase ^= 1;
   ptx::tc_fence_after();
-
-  // ---- WQ, KT
   {
+    // M = 64 layout: row 16 w + l lives in TMEM lane 32 w + l (l < 16)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int r = tid;
-    const int i = r & 63;
-    const bool is_q = r >= 64;
-    const float gli = KDA ? 0.f : gam[L - 1];
-    const float fq = KDA ? p.scale : p.scale * eg[i];
-    const float fk = KDA ? 0.f : (split ? gate[0] * eng[i] : __expf(gli - gam[i]));
+    const int i = warp * 16 + (lane & 15);
 #pragma unroll 1
     for (int q4 = 0; q4 < 4; ++q4) {
       float v[32];
       ptx::tmem_ld32(dW + lane_base + q4 * 32, v);
+      if (lane < 16) {
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        const int c0 = q4 * 32 + q8 * 8;
-        float out[8];
-        if (!is_q) {
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float out[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) out[e] = -v[q8 * 8 + e];
-        } else {
-          float qf[8];
-          unpack8(*reinterpret_cast<const uint4 *>(KQ + img_off(64 + i, c0, 2048)), qf);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) out[e] = fq * qf[e] - v[q8 * 8 + e];
+          *reinterpret_cast<uint4 *>(blk + OFF_W + img_off(i, q4 * 32 + q8 * 8, 1024)) =
+              pack8(out);
         }
-        *reinterpret_cast<uint4 *>(WQ + img_off(r, c0, 2048)) = pack8(out);
       }
     }
-    if (!KDA && !is_q) {
-      // KT row i: k e^{gamma_L - gamma_i} (zero beyond the chunk)
 #pragma unroll 1
-      for (int cg = 0; cg < 16; ++cg) {
-        float kr[8], kt[8];
-        unpack8(*reinterpret_cast<const uint4 *>(KQ + img_off(i, 8 * cg, 2048)), kr);
+    for (int t = 0; t < V / 32; ++t) {
+      float v[32];
+      ptx::tmem_ld32(dU + lane_base + t * 32, v);
+      if (lane < 16) {
+        float4 *dst = reinterpret_cast<float4 *>(blk + OFF_U + t * 8192 + i * 128);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kt[e] = (i < L) ? kr[e] * fk : 0.f;
-        *reinterpret_cast<uint4 *>(KTs + img_off(i, 8 * cg, 1024)) = pack8(kt);
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
     }
   }
-  ptx::fence_proxy_async_smem();
+  if (tid == 0) ptx::bulk_wait<0>();
+  if (!(ok1 && ok2) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
   ptx::tc_fence_before();
   __syncthreads();
-  if (tid == 0) {
-    ptx::bulk_s2g(blk + OFF_WQ, WQ, WQ_BYTES);
-    ptx::bulk_s2g(blk + OFF_KT, KTs, KT_BYTES);
-    ptx::bulk_s2g(blk + OFF_GATE, gate, GATE_BYTES);
-    ptx::bulk_commit();
-    ptx::bulk_wait<0>();
-  }
-  if (!(ok1 && ok2 && ok3) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc<128>(tmem);
+  if (warp == 0) ptx::tmem_dealloc<256>(tmem);
 }
 
 // ---------------------------------------------------------------------------
-// chain kernel
+// chain kernel (192 threads: warps 0-3 epilogue, warp 4 producer, warp 5 MMA)
 //
-// shared memory: two stages of [operand block (66048 B) | v tile (4096 B)],
-// then the bf16 state image H (128 keys x 32, cs 2048) and v_new image VN
-// (64 tokens x 32, cs 1024).
-constexpr uint32_t C_STAGE0 = 0, C_H = 2 * STAGE_BYTES, C_VN = C_H + 8192,
-                   C_SMALL = C_VN + 4096, C_SMEM = C_SMALL + 256;
+// shared memory: two stages of
+//   AW  [0, 32768)       [-w ; q~] (128 x 128, cs 2048)
+//   KT  [32768, 49152)   k~ (64 tokens x 128 keys, cs 1024)
+//   AQ  [49152, 65536)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
+//   U   [65536, 73728)   u tile, fp32 64 x 32
+//   SC  [73728, 74752)   decay[128], rs[64], qs[64]
+// then H (128 keys x 32, cs 2048), VN hi/lo and VS hi/lo (64 x 32, cs 1024)
+// and the fp32 exchange X (64 x 33).
+constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 49152, S_U = 65536, S_SC = 73728,
+                   STAGE_BYTES = 74752;
+constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 8192, C_VS = C_VN + 8192,
+                   C_X = C_VS + 8192, C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
+constexpr int CHAIN_THREADS = 192;
 
-__global__ void __launch_bounds__(128, 1)
-chain_kernel(const __grid_constant__ CUtensorMap tm_v, TcParams p) {
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+             TcParams p, int kda) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *Himg = smem + C_H;
-  unsigned char *VN = smem + C_VN;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C_SMALL);  // full0, full1, mma
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3);
+  unsigned char *VN = smem + C_VN;   // hi at +0, lo at +4096
+  unsigned char *VSi = smem + C_VS;  // hi at +0, lo at +4096
+  float *X = reinterpret_cast<float *>(smem + C_X);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C_BAR);
+  uint64_t *full = bar, *empty = bar + 2, *d1 = bar + 4, *d35 = bar + 5, *vnready = bar + 6,
+           *hready = bar + 7;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 8);
+  volatile int *abort_flag = reinterpret_cast<int *>(bar + 9);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int v0 = blockIdx.x * VTILE;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int vt = blockIdx.x;
+  const int v0 = vt * VTILE;
   const int h = blockIdx.y;
   const int n = blockIdx.z;
+  const int hk = h / (p.H / p.Hk);
   int bos, eos, b, base;
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
@@ -629,41 +638,104 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_v, TcParams p) {
   const int nch = (eos - bos + BT - 1) / BT;
 
   if (tid == 0) {
-    ptx::mbar_init(&bars[0], 1);
-    ptx::mbar_init(&bars[1], 1);
-    ptx::mbar_init(&bars[2], 1);
+    ptx::mbar_init(&full[0], 1);
+    ptx::mbar_init(&full[1], 1);
+    ptx::mbar_init(&empty[0], 5);
+    ptx::mbar_init(&empty[1], 5);
+    ptx::mbar_init(d1, 1);
+    ptx::mbar_init(d35, 1);
+    ptx::mbar_init(vnready, 2);
+    ptx::mbar_init(hready, 4);
     ptx::fence_mbar_init();
+    *abort_flag = 0;
   }
   if (warp == 0) ptx::tmem_alloc<128>(tmem_slot);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t dD1 = tmem, dDH = tmem + 32, dD5 = tmem + 64;
 
-  auto issue = [&](int c) {
-    const int s = c & 1;
-    unsigned char *st = smem + C_STAGE0 + s * STAGE_BYTES;
-    ptx::mbar_arrive_expect_tx(&bars[s], STAGE_BYTES);
-    ptx::bulk_g2s(st, p.blocks + ((size_t)(base + c) * p.H + h) * BLOCK_BYTES, BLOCK_BYTES,
-                  &bars[s]);
-    const int trow = b * p.T + bos + c * BT;
-#pragma unroll
-    for (int vg = 0; vg < 4; ++vg)
-      ptx::tma_load_3d(st + BLOCK_BYTES + vg * 1024, &tm_v, v0 + 8 * vg, h, trow, &bars[s]);
-  };
-  if (tid == 0) {
-    if (nch > 0) issue(0);
-    if (nch > 1) issue(1);
-  }
-
-  // initial state: thread c owns key row c of the tile
-  float hs[VTILE];
-  {
-    const int c = tid;
+  if (warp == 4) {
+    // ---------------- producer
+    if (lane == 0) {
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1, k = c >> 1;
+        if (k > 0 && !ptx::mbar_wait_bounded(&empty[s], (uint32_t)((k - 1) & 1))) {
+          record_error(p.err, GDN_ERR_TIMEOUT);  // keep going: no role may stall the others
+          *abort_flag = 1;
+        }
+        unsigned char *st = smem + s * STAGE_BYTES;
+        const unsigned char *src = p.blocks + ((size_t)(base + c) * p.H + h) * p.block;
+        const int trow = b * p.T + bos + c * BT;
+        ptx::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+#pragma unroll 1
+        for (int g8 = 0; g8 < 16; ++g8) {
+          ptx::bulk_g2s(st + S_AW + g8 * 2048, src + OFF_W + g8 * 1024, 1024, &full[s]);
+          if (kda) {
+            ptx::bulk_g2s(st + S_AW + g8 * 2048 + 1024, src + off_qh(p.V) + g8 * 1024, 1024,
+                          &full[s]);
+          } else {
+            ptx::tma_load_3d(st + S_AW + g8 * 2048 + 1024, &tm_q, 8 * g8, hk, trow, &full[s]);
+            ptx::tma_load_3d(st + S_KT + g8 * 1024, &tm_k, 8 * g8, hk, trow, &full[s]);
+          }
+        }
+        if (kda) ptx::bulk_g2s(st + S_KT, src + off_kt(p.V), 16384, &full[s]);
+        ptx::bulk_g2s(st + S_AQ, src + OFF_AQ, 16384, &full[s]);
+        ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &full[s]);
+        ptx::bulk_g2s(st + S_SC, src + OFF_SC, 1024, &full[s]);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_kmn = ptx::idesc_bf16(128, VTILE, 0, 1);   // A K-major, B MN-major
+      const uint32_t id_mnmn = ptx::idesc_bf16(128, VTILE, 1, 1);  // both MN-major
+      bool ok = true;
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1, k = c >> 1;
+        unsigned char *st = smem + s * STAGE_BYTES;
+        ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)(k & 1)) && ok;
+        ok = ptx::mbar_wait_bounded(hready, (uint32_t)(c & 1)) && ok;
+        ptx::tc_fence_after();
+        // D1 = [-w ; q~] h
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks)
+          ptx::mma_bf16(dD1, ptx::sdesc(st + S_AW + ks * 4096, 2048, 128),
+                        ptx::sdesc(Himg + ks * 256, 128, 2048), id_kmn, ks > 0);
+        ptx::mma_commit(d1);
+        ok = ptx::mbar_wait_bounded(vnready, (uint32_t)(c & 1)) && ok;
+        ptx::tc_fence_after();
+        // DH = k~^T (vs_hi + vs_lo);  D5 = [Aqk_lo ; Aqk_hi] (vn_hi + vn_lo)
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part)
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks) {
+            ptx::mma_bf16(dDH, ptx::sdesc(st + S_KT + ks * 256, 128, 1024),
+                          ptx::sdesc(VSi + part * 4096 + ks * 256, 128, 1024), id_mnmn,
+                          part > 0 || ks > 0);
+            ptx::mma_bf16(dD5, ptx::sdesc(st + S_AQ + ks * 4096, 2048, 128),
+                          ptx::sdesc(VN + part * 4096 + ks * 256, 128, 1024), id_kmn,
+                          part > 0 || ks > 0);
+          }
+        ptx::mma_commit(d35);
+        ptx::mma_commit(&empty[s]);
+      }
+      if (!ok) {
+        record_error(p.err, GDN_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 0-3: thread r = TMEM lane r = key row r
+    const int r = tid;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float hs[VTILE];
     if (p.h0) {
       const float4 *src =
-          reinterpret_cast<const float4 *>(p.h0 + (((size_t)n * p.H + h) * KD + c) * p.V + v0);
+          reinterpret_cast<const float4 *>(p.h0 + (((size_t)n * p.H + h) * KD + r) * p.V + v0);
 #pragma unroll
       for (int q = 0; q < VTILE / 4; ++q) {
         const float4 x = src[q];
@@ -675,104 +747,107 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_v, TcParams p) {
     }
 #pragma unroll
     for (int vg = 0; vg < 4; ++vg)
-      *reinterpret_cast<uint4 *>(Himg + img_off(c, 8 * vg, 2048)) = pack8(hs + 8 * vg);
-  }
-  ptx::fence_proxy_async_smem();
-  __syncthreads();
+      *reinterpret_cast<uint4 *>(Himg + img_off(r, 8 * vg, 2048)) = pack8(hs + 8 * vg);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(hready);
 
-  uint32_t mma_phase = 0;
-  bool ok = true;
-  const uint32_t id_u = ptx::idesc_bf16(128, VTILE, 0, 1);
-  const uint32_t id_c3 = ptx::idesc_bf16(128, VTILE, 1, 1);
+    bool ok = true;
 #pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    const int s = c & 1;
-    unsigned char *st = smem + C_STAGE0 + s * STAGE_BYTES;
-    const uint32_t dU = tmem + s * 32;
-    const uint32_t dH = tmem + 64;
-    const int L = min(BT, eos - bos - c * BT);
-    ok = wait_all(&bars[s], (uint32_t)((c >> 1) & 1)) && ok;
-    if (tid == 0) {
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & 1, k = c >> 1;
+      const unsigned char *st = smem + s * STAGE_BYTES;
+      const int L = min(BT, eos - bos - c * BT);
+      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)(k & 1)) && ok;
+      ok = ptx::mbar_wait_bounded(d1, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
-      // D = TU v_tile
-#pragma unroll 1
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t a = ptx::sdesc(st + OFF_TU + ks * 2 * 2048, 2048, 128);
-        const uint64_t bb = ptx::sdesc(st + BLOCK_BYTES + ks * 256, 128, 1024);
-        ptx::mma_bf16(dU, a, bb, id_u, ks > 0);
+      const float *scs = reinterpret_cast<const float *>(st + S_SC);
+      float qh[VTILE];
+      {
+        float d[32];
+        ptx::tmem_ld32(dD1 + lane_base, d);
+        if (r < 64) {
+          const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128);
+          const float rs = scs[128 + r];
+          float vn[32], vs[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 u = u4[q];
+            vn[4 * q] = u.x + d[4 * q];
+            vn[4 * q + 1] = u.y + d[4 * q + 1];
+            vn[4 * q + 2] = u.z + d[4 * q + 2];
+            vn[4 * q + 3] = u.w + d[4 * q + 3];
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) vs[j] = rs * vn[j];
+#pragma unroll
+          for (int vg = 0; vg < 4; ++vg) {
+            uint4 hi, lo;
+            split8(vn + 8 * vg, hi, lo);
+            *reinterpret_cast<uint4 *>(VN + img_off(r, 8 * vg, 1024)) = hi;
+            *reinterpret_cast<uint4 *>(VN + 4096 + img_off(r, 8 * vg, 1024)) = lo;
+            split8(vs + 8 * vg, hi, lo);
+            *reinterpret_cast<uint4 *>(VSi + img_off(r, 8 * vg, 1024)) = hi;
+            *reinterpret_cast<uint4 *>(VSi + 4096 + img_off(r, 8 * vg, 1024)) = lo;
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(vnready);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) qh[j] = d[j];
+        }
       }
-      // D += WQ h
-#pragma unroll 1
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t a = ptx::sdesc(st + OFF_WQ + ks * 2 * 2048, 2048, 128);
-        const uint64_t bb = ptx::sdesc(Himg + ks * 256, 128, 2048);
-        ptx::mma_bf16(dU, a, bb, id_u, 1);
-      }
-      ptx::mma_commit(&bars[2]);
-    }
-    const float decay = reinterpret_cast<const float *>(st + OFF_GATE)[tid];
-    ok = wait_all(&bars[2], mma_phase) && ok;
-    mma_phase ^= 1;
-    ptx::tc_fence_after();
-    {
-      float d[32];
-      ptx::tmem_ld32(dU + lane_base, d);
-      if (tid < 64) {
+      const float decay = scs[r];
+      const float qs = r >= 64 ? scs[192 + r - 64] : 0.f;
+      ok = ptx::mbar_wait_bounded(d35, (uint32_t)(c & 1)) && ok;
+      ptx::tc_fence_after();
+      {
+        float d[32];
+        ptx::tmem_ld32(dDH + lane_base, d);
+#pragma unroll
+        for (int j = 0; j < VTILE; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
 #pragma unroll
         for (int vg = 0; vg < 4; ++vg)
-          *reinterpret_cast<uint4 *>(VN + img_off(tid, 8 * vg, 1024)) = pack8(d + 8 * vg);
-      } else {
-        const int i = tid - 64;
+          *reinterpret_cast<uint4 *>(Himg + img_off(r, 8 * vg, 2048)) = pack8(hs + 8 * vg);
+        ptx::fence_proxy_async_smem();
+      }
+      float d5[32];
+      ptx::tmem_ld32(dD5 + lane_base, d5);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(hready);
+      if (r < 64) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) X[r * 33 + j] = d5[j];
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (r >= 64) {
+        const int i = r - 64;
         if (i < L) {
+          float ov[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = fmaf(qs, qh[j], d5[j] + X[i * 33 + j]);
           uint4 *dst = reinterpret_cast<uint4 *>(
               p.o + ((size_t)(b * p.T + bos + c * BT + i) * p.H + h) * p.V + v0);
 #pragma unroll
-          for (int vg = 0; vg < 4; ++vg) dst[vg] = pack8(d + 8 * vg);
+          for (int vg = 0; vg < 4; ++vg) dst[vg] = pack8(ov + 8 * vg);
         }
       }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[s]);
     }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      // D_H = KT^T v_new  (M = 128 keys, K = 64 tokens)
-#pragma unroll 1
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t a = ptx::sdesc(st + OFF_KT + ks * 256, 128, 1024);
-        const uint64_t bb = ptx::sdesc(VN + ks * 256, 128, 1024);
-        ptx::mma_bf16(dH, a, bb, id_c3, ks > 0);
-      }
-      ptx::mma_commit(&bars[2]);
-    }
-    ok = wait_all(&bars[2], mma_phase) && ok;
-    mma_phase ^= 1;
-    ptx::tc_fence_after();
-    {
-      float d[32];
-      ptx::tmem_ld32(dH + lane_base, d);
+    if (!ok) {
+      if (lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+    } else if (p.ht && *abort_flag == 0) {
+      float4 *dst =
+          reinterpret_cast<float4 *>(p.ht + (((size_t)n * p.H + h) * KD + r) * p.V + v0);
 #pragma unroll
-      for (int j = 0; j < VTILE; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
-#pragma unroll
-      for (int vg = 0; vg < 4; ++vg)
-        *reinterpret_cast<uint4 *>(Himg + img_off(tid, 8 * vg, 2048)) = pack8(hs + 8 * vg);
+      for (int q = 0; q < VTILE / 4; ++q)
+        dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
     }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    if (!__syncthreads_and(ok)) break;
-    if (tid == 0 && c + 2 < nch) {
-      ptx::fence_proxy_async_smem();  // generic reads of stage s precede the refill
-      issue(c + 2);
-    }
-  }
-  if (!ok) {
-    if (tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
-  } else if (p.ht) {
-    float4 *dst =
-        reinterpret_cast<float4 *>(p.ht + (((size_t)n * p.H + h) * KD + tid) * p.V + v0);
-#pragma unroll
-    for (int q = 0; q < VTILE / 4; ++q)
-      dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -818,12 +893,13 @@ size_t max_chunks(int B, int T, int N, bool varlen) {
 }  // namespace tc
 
 bool chunk_tc_supported(const ChunkParams &p, bool bf16) {
-  return bf16 && p.K == tc::KD && p.V % tc::VTILE == 0 && p.T > 0;
+  return bf16 && p.K == tc::KD && p.V % tc::VTILE == 0 && p.V <= tc::VMAX && p.T > 0;
 }
 
-size_t chunk_tc_workspace(const ChunkParams &p) {
+size_t chunk_tc_workspace(const ChunkParams &p, bool kda) {
   const bool varlen = p.cu_seqlens != nullptr;
-  return tc::table_bytes(p.N) + tc::max_chunks(p.B, p.T, p.N, varlen) * (size_t)p.H * tc::BLOCK_BYTES;
+  return tc::table_bytes(p.N) +
+         tc::max_chunks(p.B, p.T, p.N, varlen) * (size_t)p.H * tc::block_bytes(p.V, kda);
 }
 
 cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStream_t stream) {
@@ -846,6 +922,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   p.NT = (cp.T + BT - 1) / BT;
   p.g_is_cumsum = cp.g_is_cumsum;
   p.scale = cp.scale;
+  p.block = block_bytes(cp.V, kda);
   if (varlen) {
     chunk_table_kernel<<<1, 32, 0, stream>>>(cp.cu_seqlens, cp.N, cp.T, p.table, cp.err);
     cudaError_t e = cudaGetLastError();
@@ -856,12 +933,13 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const uint32_t ismem = kda ? IntraLayout<true>::SMEM : IntraLayout<false>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(ik, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ismem);
   if (e != cudaSuccess) return e;
-  ik<<<dim3((unsigned)nchunks, cp.H), 128, ismem, stream>>>(mk, mq, p);
+  ik<<<dim3((unsigned)nchunks, cp.H), 128, ismem, stream>>>(mk, mq, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), 128, C_SMEM, stream>>>(mv, p);
+  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(mk, mq, p,
+                                                                                 kda ? 1 : 0);
   return cudaGetLastError();
 }
 

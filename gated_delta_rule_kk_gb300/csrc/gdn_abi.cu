@@ -115,7 +115,7 @@ gdn_status_t run_chunk(ChunkParams &p, bool bf16, bool kda, void *ws, size_t ws_
                        cudaStream_t s) {
   const bool tc = chunk_tc_supported(p, bf16);
   if (tc) {
-    const size_t need = chunk_tc_workspace(p);
+    const size_t need = chunk_tc_workspace(p, kda);
     if (ws == nullptr || ws_bytes < need)
       return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -155,7 +155,7 @@ gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *a, size_t *bytes) {
   if (a == nullptr || bytes == nullptr) return fail(GDN_ERR_INVALID_ARG, "NULL argument");
   *bytes = 0;
   ChunkParams p = gdn_params(*a);
-  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *bytes = chunk_tc_workspace(p);
+  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *bytes = chunk_tc_workspace(p, false);
   return GDN_OK;
 }
 
@@ -163,7 +163,7 @@ gdn_status_t kda_chunk_workspace_size(const kda_chunk_args *a, size_t *bytes) {
   if (a == nullptr || bytes == nullptr) return fail(GDN_ERR_INVALID_ARG, "NULL argument");
   *bytes = 0;
   ChunkParams p = kda_params(*a);
-  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *bytes = chunk_tc_workspace(p);
+  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *bytes = chunk_tc_workspace(p, true);
   return GDN_OK;
 }
 

@@ -41,7 +41,7 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 // Tensor-core chunked forward (bf16, K = 128, V % 32 == 0): whether it serves
 // these arguments, the workspace it needs, and the launch.
 bool chunk_tc_supported(const ChunkParams &p, bool bf16);
-size_t chunk_tc_workspace(const ChunkParams &p);
+size_t chunk_tc_workspace(const ChunkParams &p, bool per_channel_gate);
 cudaError_t launch_chunk_tc(const ChunkParams &p, bool per_channel_gate, void *workspace,
                             cudaStream_t stream);
 

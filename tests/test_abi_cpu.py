@@ -169,23 +169,29 @@ def test_decode_argument_errors(lib, change, expect):
 
 
 def test_workspace_size(lib):
-    # the tensor-core path (bf16, K = 128, V % 32 == 0) needs per-(chunk, head)
-    # operand blocks of 66048 bytes plus a 256-byte chunk table
+    # the tensor-core path (bf16, K = 128, V % 32 == 0, V <= 128) needs per
+    # (chunk, head) operand blocks of 33792 + 256 V bytes (+32 KB with the
+    # per-channel gate) plus a 256-byte chunk table
+    blk = 33792 + 256 * 128
     a = good_chunk()
     n = ctypes.c_size_t(123)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
-    assert n.value == 256 + 2 * 2 * 4 * 66048
+    assert n.value == 256 + 2 * 2 * 4 * blk
     # packed sequences: at most ceil(T/64) + N chunks
     a = good_chunk(B=1, N=3, cu_seqlens=FAKE, T=200)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
-    assert n.value == 256 + (4 + 3) * 4 * 66048
+    assert n.value == 256 + (4 + 3) * 4 * blk
+    # V beyond 128 takes the CUDA-core path
+    a = good_chunk(V=160)
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
+    assert n.value == 0
     # the exact fp32 path needs none
     a = good_chunk(dtype=0)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
     assert n.value == 0
     k = KdaChunkArgs(dtype=1, B=1, T=64, H=2, HV=2, K=128, V=64, N=1, chunk_size=64)
     assert lib.kda_chunk_workspace_size(ctypes.byref(k), ctypes.byref(n)) == Status.OK
-    assert n.value == 256 + 1 * 2 * 66048
+    assert n.value == 256 + 1 * 2 * (33792 + 256 * 64 + 32768)
 
 
 def test_workspace_errors_found_on_host(lib):
