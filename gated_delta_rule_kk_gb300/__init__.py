@@ -4,5 +4,8 @@ The arithmetic lives in the CUDA library built from ``csrc/`` (see
 ``build_lib.py``); this package holds its ctypes binding and the seeded
 synthetic input generators.
 """
-from .api import gdn_check_device_error, gdn_chunk_fwd, gdn_decode, kda_chunk_fwd  # noqa: F401
+from .api import (  # noqa: F401
+    gdn_check_device_error, gdn_chunk_fwd, gdn_chunk_fwd_noalloc, gdn_decode,
+    gdn_noalloc_scratch_bytes, kda_chunk_fwd,
+)
 from ._lib import GdnError, Status  # noqa: F401

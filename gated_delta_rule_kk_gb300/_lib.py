@@ -81,6 +81,8 @@ SIGNATURES = {
     "kda_chunk_workspace_size": ([ctypes.POINTER(KdaChunkArgs), ctypes.POINTER(c_size_t)], c_int32),
     "kda_chunk_fwd": ([ctypes.POINTER(KdaChunkArgs), c_void_p], c_int32),
     "gdn_decode": ([ctypes.POINTER(GdnDecodeArgs), c_void_p], c_int32),
+    "gdn_chunk_fwd_noalloc": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
+    "gdn_noalloc_scratch_bytes": ([], c_size_t),
     "gdn_check_device_error": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),
     "gdn_status_string": ([c_int32], ctypes.c_char_p),
     "gdn_last_error_message": ([], ctypes.c_char_p),

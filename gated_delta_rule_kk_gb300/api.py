@@ -119,6 +119,35 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     return out, ht
 
 
+def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                          output_final_state=True, g_is_cumsum=False, out=None,
+                          final_state=None, stream=None):
+    """``gdn_chunk_fwd`` for callers that cannot allocate device memory.
+
+    No workspace is requested or allocated: the library uses a fixed device
+    array of ``gdn_noalloc_scratch_bytes()`` bytes instead, shared by every
+    call on the device (order calls that could overlap).  Outputs are
+    allocated here only when ``out`` / ``final_state`` are not passed.
+    """
+    dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
+        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H")
+    a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                     h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
+                     B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
+                     g_is_cumsum=int(bool(g_is_cumsum)),
+                     scale=float(scale) if scale is not None else 0.0,
+                     workspace=None, workspace_bytes=0)
+    lib = _lib.load()
+    _lib.check(lib.gdn_chunk_fwd_noalloc(ctypes.byref(a), _stream(stream)),
+               "gdn_chunk_fwd_noalloc")
+    return out, ht
+
+
+def gdn_noalloc_scratch_bytes():
+    """Size of the fixed scratch array behind ``gdn_chunk_fwd_noalloc``."""
+    return int(_lib.load().gdn_noalloc_scratch_bytes())
+
+
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=True, out=None, final_state=None,
                   workspace=None, stream=None):

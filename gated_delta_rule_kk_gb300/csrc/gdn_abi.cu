@@ -128,6 +128,9 @@ gdn_status_t run_chunk(ChunkParams &p, bool bf16, bool kda, void *ws, size_t ws_
 }
 
 }  // namespace
+
+gdn_status_t set_host_error(gdn_status_t st, const char *msg) { return fail(st, "%s", msg); }
+
 }  // namespace gdn
 
 using namespace gdn;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gdn.h"
+
 namespace gdn {
 
 // One chunked-forward problem, already validated.  `H` counts value heads and
@@ -44,5 +46,8 @@ bool chunk_tc_supported(const ChunkParams &p, bool bf16);
 size_t chunk_tc_workspace(const ChunkParams &p, bool per_channel_gate);
 cudaError_t launch_chunk_tc(const ChunkParams &p, bool per_channel_gate, void *workspace,
                             cudaStream_t stream);
+
+// Record `msg` as the calling thread's last host-side error; returns `st`.
+gdn_status_t set_host_error(gdn_status_t st, const char *msg);
 
 }  // namespace gdn

@@ -83,8 +83,12 @@ typedef enum gdn_dtype {
  *                                     (0 = cu_seqlens[0] <= ... <= cu_seqlens[N]
  *                                     = T, checked on the device)
  * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, H % Hg == 0.
- * scale <= 0 selects 1/sqrt(K).  No workspace is needed (workspace may be
- * NULL with workspace_bytes = 0).
+ * scale <= 0 selects 1/sqrt(K).
+ * Workspace: bf16 inputs with K == 128 and V a multiple of 32 up to 128 run on
+ * the tensor cores and need `workspace` (device, 256-byte aligned,
+ * caller-owned, contents irrelevant before and after the call) of at least
+ * gdn_chunk_workspace_size() bytes, else GDN_ERR_WORKSPACE.  Every other
+ * shape runs the exact fp32 CUDA-core kernel and needs none.
  */
 typedef struct gdn_chunk_args {
   int32_t dtype;               /* gdn_dtype_t of q, k, v, o */
@@ -102,7 +106,9 @@ typedef struct gdn_chunk_args {
   size_t workspace_bytes;
 } gdn_chunk_args;
 
-/* Bytes of workspace gdn_chunk_fwd needs for these arguments (currently 0). */
+/* Bytes of workspace gdn_chunk_fwd needs for these arguments (0 when the
+ * CUDA-core kernel serves them).  Reads only sizes, dtype and whether
+ * cu_seqlens is NULL. */
 gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *args, size_t *bytes);
 
 /* Enqueue the GDN chunked forward (gate cumsum, intra-chunk (I+A)^-1 with the
@@ -124,6 +130,8 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *args, gdn_stream_t stream);
  *   h0, ht [N, HV, K, V]  float32     as for GDN
  *   cu_seqlens            as for GDN
  * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0.
+ * Workspace: as for GDN (tensor cores for bf16, K == 128, V % 32 == 0,
+ * V <= 128; kda_chunk_workspace_size() bytes).
  */
 typedef struct kda_chunk_args {
   int32_t dtype;
@@ -183,6 +191,27 @@ typedef struct gdn_decode_args {
 } gdn_decode_args;
 
 gdn_status_t gdn_decode(const gdn_decode_args *args, gdn_stream_t stream);
+
+/*
+ * GDN chunked forward without a workspace, for callers that cannot allocate
+ * device memory (a host runtime that owns a fixed device-memory budget and
+ * forbids cudaMalloc from plugins, or a latency-critical loop that must not
+ * hit cudaMalloc's implicit synchronisation).  The pages have no counterpart
+ * to this entry point; it is a convenience of this library.
+ * Same arguments and results as gdn_chunk_fwd; `workspace` and
+ * `workspace_bytes` are ignored.  Scratch comes from a fixed device array of
+ * gdn_noalloc_scratch_bytes() bytes (32 MiB) that every GPU loading the
+ * library holds until the process exits; a problem whose
+ * gdn_chunk_workspace_size exceeds it returns GDN_ERR_WORKSPACE and enqueues
+ * nothing.  All calls on a device share that array: calls that may overlap
+ * on the GPU (e.g. on different streams) race and must be ordered by the
+ * caller.  The first call on each device resolves the array's device address
+ * (with that device current), so make it before any stream capture.
+ */
+gdn_status_t gdn_chunk_fwd_noalloc(const gdn_chunk_args *args, gdn_stream_t stream);
+
+/* Size in bytes of the fixed scratch array used by gdn_chunk_fwd_noalloc. */
+size_t gdn_noalloc_scratch_bytes(void);
 
 /* Wait for `stream`, then read and clear the device error word of the current
  * device into *code (a gdn_status_t value, GDN_OK if nothing was recorded).

@@ -30,7 +30,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|gdn_status_t)\s*(\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|gdn_status_t|size_t)\s*(\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_expected_entry_points():
