@@ -15,23 +15,24 @@
 //      w   = T diag(beta e^gamma) k,  u = T diag(beta) v         (WY recompute)
 //    T enters the two WY GEMMs as a hi + lo pair of bf16 matrices, so w and u
 //    carry fp32-grade accuracy.  Per (chunk, head) the kernel stores a block
-//    the sequential pass consumes directly:
-//      W   -w (bf16, 64 x 128)            U   u (fp32, per 32-wide V tile)
-//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)  SC  exp(gamma_L) per key row,
-//                                              exp(gamma_L - gamma_i) and
+//    of ready-made operand images the sequential pass consumes directly:
+//      AW  [-w ; q] (bf16)                U   u (fp32, per 32-wide V tile)
+//      KT  k (bf16)                       SC  exp(gamma_L) per key row,
+//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)      exp(gamma_L - gamma_i) and
 //                                              scale exp(gamma_i) per token
 //    For the per-channel gate (KDA, vLLM kimi_k3 kda/chunk_intra,
 //    chunk_kda_fwd_kernel_inter_solve_fused) the exponentials move into the
 //    operands: S = [k e^g; q e^g] (k e^-g)^T with the chunk start as the
-//    reference row, w = T diag(beta) (k e^g), and the block also holds
-//    QH = q e^g and KT = k e^{gamma_L - g}.
+//    reference row, w = T diag(beta) (k e^g), AW holds q e^g and KT holds
+//    k e^{gamma_L - g}.
 //
 // 2. chain: one CTA per (32-wide V tile, value head, sequence), the
-//    sequential inter-chunk pass, warp-specialised: warp 4 streams the
-//    chunk operands in (bulk copies and TMA), warp 5 issues the tcgen05
-//    GEMMs, warps 0-3 (one TMEM lane and one key row of the fp32 state tile
-//    h[128, 32] per thread, kept in registers for the whole sequence) run
-//    the epilogues.  Per chunk
+//    sequential inter-chunk pass, warp-specialised: warp 8 streams the
+//    chunk's operand block in (five bulk copies), warp 9 issues the tcgen05
+//    GEMMs, warps 0-7 run the epilogues (warps w and w + 4 share TMEM lane
+//    quarter w % 4 and split its 32 columns; each thread keeps 16 columns of
+//    one key row of the fp32 state tile h[128, 32] in registers for the
+//    whole sequence).  Per chunk
 //      D1  = [-w ; q~] bf16(h)            rows 0..63: -w h, rows 64..127: q h
 //      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
 //      DH  = k~^T (e^{gamma_L - gamma} v_new)
@@ -62,13 +63,14 @@ constexpr int VTILE = 32;
 constexpr int VMAX = 128;
 constexpr float GATE_FACTOR_LIMIT = 80.f;  // |gamma| bound for split exponentials
 
-// per (chunk, head) block in the workspace
-constexpr uint32_t OFF_W = 0, OFF_AQ = 16384, OFF_SC = 32768, OFF_U = 33792;
-__host__ __device__ constexpr uint32_t block_bytes(int V, bool kda) {
-  return OFF_U + (uint32_t)V * 256u + (kda ? 32768u : 0u);
+// per (chunk, head) block in the workspace: the chain's operand images
+//   AW  [-w ; q~] (128 x 128 bf16, cs 2048)   KT  k~ (64 x 128 bf16, cs 1024)
+//   AQ  [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048) SC  decay[128], rs[64], qs[64]
+//   U   u, fp32 [V / 32 tiles][64][32]
+constexpr uint32_t OFF_AW = 0, OFF_KT = 32768, OFF_AQ = 49152, OFF_SC = 65536, OFF_U = 66560;
+__host__ __device__ constexpr uint32_t block_bytes(int V, bool) {
+  return OFF_U + (uint32_t)V * 256u;
 }
-__host__ __device__ constexpr uint32_t off_qh(int V) { return OFF_U + (uint32_t)V * 256u; }
-__host__ __device__ constexpr uint32_t off_kt(int V) { return off_qh(V) + 16384u; }
 
 __device__ __forceinline__ uint32_t img_off(int r, int c, uint32_t cs) {
   return (uint32_t)(c >> 3) * cs + (uint32_t)r * 16u + (uint32_t)(c & 7) * 2u;
@@ -482,12 +484,19 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   __syncthreads();
   if (tid == 0) {
     ptx::bulk_s2g(blk + OFF_AQ, AQ, 16384);
+    if (KDA) {
+      ptx::bulk_s2g(blk + OFF_KT, KTs, 16384);
+    } else {
+      // raw k (KQ rows 0..63, cs 2048) -> KT (cs 1024)
+#pragma unroll 1
+      for (int g8 = 0; g8 < 16; ++g8) ptx::bulk_s2g(blk + OFF_KT + g8 * 1024, KQ + g8 * 2048, 1024);
+    }
     ptx::bulk_commit();
   }
 
   // ---- T = (I + A)^-1 (fp32)
   unit_lower_inverse_64(Asm, Tsm, Xs, tid);
-  if (tid == 0) ptx::bulk_wait_read<0>();  // AQ may be overwritten after the barrier
+  if (tid == 0) ptx::bulk_wait_read<0>();  // AQ and k rows may be overwritten after the barrier
   __syncthreads();
 
   // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) -> TW hi | lo;
@@ -534,13 +543,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
     ptx::mma_commit(&bars[1]);
-    if (KDA) {
-      // q e^g (KQ rows 64..127, cs 2048) -> QH (cs 1024); KT as is
-#pragma unroll 1
-      for (int g8 = 0; g8 < 16; ++g8)
-        ptx::bulk_s2g(blk + off_qh(V) + g8 * 1024, KQ + g8 * 2048 + 1024, 1024);
-      ptx::bulk_s2g(blk + off_kt(V), KTs, 16384);
-    }
     ptx::bulk_s2g(blk + OFF_SC, sc, 1024);
     ptx::bulk_commit();
   }
@@ -548,7 +550,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   mma_phase ^= 1;
   ptx::tc_fence_after();
   {
-    // M = 64 layout: row 16 w + l lives in TMEM lane 32 w + l (l < 16)
+    // M = 64 layout: row 16 w + l lives in TMEM lane 32 w + l (l < 16);
+    // -w replaces k in rows 0..63 of KQ (the WY GEMM has finished with it)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int i = warp * 16 + (lane & 15);
 #pragma unroll 1
@@ -561,8 +564,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
           float out[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) out[e] = -v[q8 * 8 + e];
-          *reinterpret_cast<uint4 *>(blk + OFF_W + img_off(i, q4 * 32 + q8 * 8, 1024)) =
-              pack8(out);
+          *reinterpret_cast<uint4 *>(KQ + img_off(i, q4 * 32 + q8 * 8, 2048)) = pack8(out);
         }
       }
     }
@@ -578,50 +580,86 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
   }
-  if (tid == 0) ptx::bulk_wait<0>();
-  if (!(ok1 && ok2) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+  // KQ is now the chain's A operand [-w ; q] (cs 2048)
+  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
+    ptx::bulk_commit();
+    ptx::bulk_wait<0>();
+  }
+  if (!(ok1 && ok2) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
   __syncthreads();
   if (warp == 0) ptx::tmem_dealloc<256>(tmem);
 }
 
 // ---------------------------------------------------------------------------
-// chain kernel (192 threads: warps 0-3 epilogue, warp 4 producer, warp 5 MMA)
+// chain kernel (320 threads: warps 0-7 epilogue, warp 8 producer, warp 9 MMA)
 //
-// shared memory: two stages of
+// shared memory: two stages holding one operand block each
 //   AW  [0, 32768)       [-w ; q~] (128 x 128, cs 2048)
 //   KT  [32768, 49152)   k~ (64 tokens x 128 keys, cs 1024)
 //   AQ  [49152, 65536)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
-//   U   [65536, 73728)   u tile, fp32 64 x 32
-//   SC  [73728, 74752)   decay[128], rs[64], qs[64]
-// then H (128 keys x 32, cs 2048), VN hi/lo and VS hi/lo (64 x 32, cs 1024)
-// and the fp32 exchange X (64 x 33).
-constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 49152, S_U = 65536, S_SC = 73728,
+//   SC  [65536, 66560)   decay[128], rs[64], qs[64]
+//   U   [66560, 74752)   u tile, fp32 64 x 32
+// then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo] and
+// VS = [vs_hi | vs_lo] (64 tokens x 64, cs 1024) and the fp32 exchange X.
+// Every bf16 pair rides in the N dimension of one GEMM (N = 64), so the
+// split costs no extra tcgen05 instructions; each accumulator holds the two
+// halves side by side and the epilogue adds them.
+constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 49152, S_SC = 65536, S_U = 66560,
                    STAGE_BYTES = 74752;
-constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 8192, C_VS = C_VN + 8192,
+constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_VS = C_VN + 8192,
                    C_X = C_VS + 8192, C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
-constexpr int CHAIN_THREADS = 192;
+constexpr int CHAIN_THREADS = 320;
+constexpr int EPI_WARPS = 8;
 
-__global__ void __launch_bounds__(CHAIN_THREADS, 1)
-chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-             TcParams p, int kda) {
+// start-address field of a shared-memory descriptor advanced by `bytes`
+__device__ __forceinline__ uint64_t adv(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
+// columns [c0, c0 + 16) of a 64-column accumulator holding the hi product in
+// columns 0..31 and the lo product in 32..63, summed
+__device__ __forceinline__ void tmem_ld_pair16(uint32_t taddr, int c0, float *v) {
+  float lo[16];
+  ptx::tmem_ld16(taddr + c0, v);
+  ptx::tmem_ld16(taddr + 32 + c0, lo);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] += lo[j];
+}
+
+// 16 values -> hi/lo bf16 halves of an image with column-group stride cs
+// (hi in columns c0.., lo in columns 32 + c0..)
+__device__ __forceinline__ void store_pair16(unsigned char *img, int r, int c0, uint32_t cs,
+                                             const float *v) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint4 hi, lo;
+    split8(v + 8 * g, hi, lo);
+    *reinterpret_cast<uint4 *>(img + img_off(r, c0 + 8 * g, cs)) = hi;
+    *reinterpret_cast<uint4 *>(img + img_off(r, 32 + c0 + 8 * g, cs)) = lo;
+  }
+}
+
+__global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *Himg = smem + C_H;
-  unsigned char *VN = smem + C_VN;   // hi at +0, lo at +4096
-  unsigned char *VSi = smem + C_VS;  // hi at +0, lo at +4096
+  unsigned char *VN = smem + C_VN;
+  unsigned char *VSi = smem + C_VS;
   float *X = reinterpret_cast<float *>(smem + C_X);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C_BAR);
-  uint64_t *full = bar, *empty = bar + 2, *d1 = bar + 4, *d35 = bar + 5, *vnready = bar + 6,
-           *hready = bar + 7;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 8);
-  volatile int *abort_flag = reinterpret_cast<int *>(bar + 9);
+  uint64_t *full = bar, *empty = bar + 2, *d1 = bar + 4, *d3 = bar + 5, *d5 = bar + 6,
+           *vnready = bar + 7, *hready = bar + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 9);
+  volatile int *abort_flag = reinterpret_cast<int *>(bar + 10);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int vt = blockIdx.x;
   const int v0 = vt * VTILE;
   const int h = blockIdx.y;
   const int n = blockIdx.z;
-  const int hk = h / (p.H / p.Hk);
   int bos, eos, b, base;
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
@@ -640,24 +678,25 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   if (tid == 0) {
     ptx::mbar_init(&full[0], 1);
     ptx::mbar_init(&full[1], 1);
-    ptx::mbar_init(&empty[0], 5);
-    ptx::mbar_init(&empty[1], 5);
+    ptx::mbar_init(&empty[0], 1 + EPI_WARPS);
+    ptx::mbar_init(&empty[1], 1 + EPI_WARPS);
     ptx::mbar_init(d1, 1);
-    ptx::mbar_init(d35, 1);
-    ptx::mbar_init(vnready, 2);
-    ptx::mbar_init(hready, 4);
+    ptx::mbar_init(d3, 1);
+    ptx::mbar_init(d5, 1);
+    ptx::mbar_init(vnready, 4);
+    ptx::mbar_init(hready, EPI_WARPS);
     ptx::fence_mbar_init();
     *abort_flag = 0;
   }
-  if (warp == 0) ptx::tmem_alloc<128>(tmem_slot);
+  if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t dD1 = tmem, dDH = tmem + 32, dD5 = tmem + 64;
+  const uint32_t dD1 = tmem, dDH = tmem + 64, dD5 = tmem + 128;
 
-  if (warp == 4) {
-    // ---------------- producer
+  if (warp == EPI_WARPS) {
+    // ---------------- producer: one operand block per chunk, five bulk copies
     if (lane == 0) {
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
@@ -668,59 +707,46 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         }
         unsigned char *st = smem + s * STAGE_BYTES;
         const unsigned char *src = p.blocks + ((size_t)(base + c) * p.H + h) * p.block;
-        const int trow = b * p.T + bos + c * BT;
         ptx::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-#pragma unroll 1
-        for (int g8 = 0; g8 < 16; ++g8) {
-          ptx::bulk_g2s(st + S_AW + g8 * 2048, src + OFF_W + g8 * 1024, 1024, &full[s]);
-          if (kda) {
-            ptx::bulk_g2s(st + S_AW + g8 * 2048 + 1024, src + off_qh(p.V) + g8 * 1024, 1024,
-                          &full[s]);
-          } else {
-            ptx::tma_load_3d(st + S_AW + g8 * 2048 + 1024, &tm_q, 8 * g8, hk, trow, &full[s]);
-            ptx::tma_load_3d(st + S_KT + g8 * 1024, &tm_k, 8 * g8, hk, trow, &full[s]);
-          }
-        }
-        if (kda) ptx::bulk_g2s(st + S_KT, src + off_kt(p.V), 16384, &full[s]);
-        ptx::bulk_g2s(st + S_AQ, src + OFF_AQ, 16384, &full[s]);
+        ptx::bulk_g2s(st + S_AW, src + OFF_AW, OFF_SC + 1024, &full[s]);  // AW, KT, AQ, SC
         ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &full[s]);
-        ptx::bulk_g2s(st + S_SC, src + OFF_SC, 1024, &full[s]);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == EPI_WARPS + 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_kmn = ptx::idesc_bf16(128, VTILE, 0, 1);   // A K-major, B MN-major
-      const uint32_t id_mnmn = ptx::idesc_bf16(128, VTILE, 1, 1);  // both MN-major
+      const uint32_t id_kmn = ptx::idesc_bf16(128, 2 * VTILE, 0, 1);   // A K-major, B MN-major
+      const uint32_t id_mnmn = ptx::idesc_bf16(128, 2 * VTILE, 1, 1);  // both MN-major
+      const uint64_t dH0 = ptx::sdesc(Himg, 128, 2048);
+      const uint64_t dVS0 = ptx::sdesc(VSi, 128, 1024);
+      const uint64_t dVN0 = ptx::sdesc(VN, 128, 1024);
       bool ok = true;
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1, k = c >> 1;
         unsigned char *st = smem + s * STAGE_BYTES;
+        const uint64_t aw = ptx::sdesc(st + S_AW, 2048, 128);
+        const uint64_t kt = ptx::sdesc(st + S_KT, 128, 1024);
+        const uint64_t aq = ptx::sdesc(st + S_AQ, 2048, 128);
         ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)(k & 1)) && ok;
         ok = ptx::mbar_wait_bounded(hready, (uint32_t)(c & 1)) && ok;
         ptx::tc_fence_after();
-        // D1 = [-w ; q~] h
-#pragma unroll 1
+        // D1 = [-w ; q~] [h_hi | h_lo]
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          ptx::mma_bf16(dD1, ptx::sdesc(st + S_AW + ks * 4096, 2048, 128),
-                        ptx::sdesc(Himg + ks * 256, 128, 2048), id_kmn, ks > 0);
+          ptx::mma_bf16(dD1, adv(aw, ks * 4096), adv(dH0, ks * 256), id_kmn, ks > 0);
         ptx::mma_commit(d1);
         ok = ptx::mbar_wait_bounded(vnready, (uint32_t)(c & 1)) && ok;
         ptx::tc_fence_after();
-        // DH = k~^T (vs_hi + vs_lo);  D5 = [Aqk_lo ; Aqk_hi] (vn_hi + vn_lo)
-#pragma unroll 1
-        for (int part = 0; part < 2; ++part)
-#pragma unroll 1
-          for (int ks = 0; ks < 4; ++ks) {
-            ptx::mma_bf16(dDH, ptx::sdesc(st + S_KT + ks * 256, 128, 1024),
-                          ptx::sdesc(VSi + part * 4096 + ks * 256, 128, 1024), id_mnmn,
-                          part > 0 || ks > 0);
-            ptx::mma_bf16(dD5, ptx::sdesc(st + S_AQ + ks * 4096, 2048, 128),
-                          ptx::sdesc(VN + part * 4096 + ks * 256, 128, 1024), id_kmn,
-                          part > 0 || ks > 0);
-          }
-        ptx::mma_commit(d35);
+        // DH = k~^T [vs_hi | vs_lo]  (critical path), then D5 = AQ [vn_hi | vn_lo]
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVS0, ks * 256), id_mnmn, ks > 0);
+        ptx::mma_commit(d3);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN0, ks * 256), id_kmn, ks > 0);
+        ptx::mma_commit(d5);
         ptx::mma_commit(&empty[s]);
       }
       if (!ok) {
@@ -729,25 +755,25 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
   } else {
-    // ---------------- epilogue warps 0-3: thread r = TMEM lane r = key row r
-    const int r = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float hs[VTILE];
+    // ---------------- epilogue warps 0-7: row r = TMEM lane, columns c0..c0+15
+    const int qd = warp & 3;
+    const int c0 = (warp >> 2) * 16;
+    const int r = qd * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    float hs[16];
     if (p.h0) {
-      const float4 *src =
-          reinterpret_cast<const float4 *>(p.h0 + (((size_t)n * p.H + h) * KD + r) * p.V + v0);
+      const float4 *src = reinterpret_cast<const float4 *>(
+          p.h0 + (((size_t)n * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
-      for (int q = 0; q < VTILE / 4; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const float4 x = src[q];
         hs[4 * q] = x.x; hs[4 * q + 1] = x.y; hs[4 * q + 2] = x.z; hs[4 * q + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < VTILE; ++j) hs[j] = 0.f;
+      for (int j = 0; j < 16; ++j) hs[j] = 0.f;
     }
-#pragma unroll
-    for (int vg = 0; vg < 4; ++vg)
-      *reinterpret_cast<uint4 *>(Himg + img_off(r, 8 * vg, 2048)) = pack8(hs + 8 * vg);
+    store_pair16(Himg, r, c0, 2048, hs);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(hready);
@@ -759,19 +785,21 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       const unsigned char *st = smem + s * STAGE_BYTES;
       const int L = min(BT, eos - bos - c * BT);
       ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)(k & 1)) && ok;
+      const float *scs = reinterpret_cast<const float *>(st + S_SC);
+      const float decay = scs[r];
+      const float qs = r >= 64 ? scs[192 + r - 64] : 0.f;
       ok = ptx::mbar_wait_bounded(d1, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
-      const float *scs = reinterpret_cast<const float *>(st + S_SC);
-      float qh[VTILE];
+      float qh[16];
       {
-        float d[32];
-        ptx::tmem_ld32(dD1 + lane_base, d);
+        float d[16];
+        tmem_ld_pair16(dD1 + lane_base, c0, d);
         if (r < 64) {
-          const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128);
+          const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128 + c0 * 4);
           const float rs = scs[128 + r];
-          float vn[32], vs[32];
+          float vn[16], vs[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < 4; ++q) {
             const float4 u = u4[q];
             vn[4 * q] = u.x + d[4 * q];
             vn[4 * q + 1] = u.y + d[4 * q + 1];
@@ -779,79 +807,69 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
             vn[4 * q + 3] = u.w + d[4 * q + 3];
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) vs[j] = rs * vn[j];
-#pragma unroll
-          for (int vg = 0; vg < 4; ++vg) {
-            uint4 hi, lo;
-            split8(vn + 8 * vg, hi, lo);
-            *reinterpret_cast<uint4 *>(VN + img_off(r, 8 * vg, 1024)) = hi;
-            *reinterpret_cast<uint4 *>(VN + 4096 + img_off(r, 8 * vg, 1024)) = lo;
-            split8(vs + 8 * vg, hi, lo);
-            *reinterpret_cast<uint4 *>(VSi + img_off(r, 8 * vg, 1024)) = hi;
-            *reinterpret_cast<uint4 *>(VSi + 4096 + img_off(r, 8 * vg, 1024)) = lo;
-          }
+          for (int j = 0; j < 16; ++j) vs[j] = rs * vn[j];
+          store_pair16(VSi, r, c0, 1024, vs);
+          store_pair16(VN, r, c0, 1024, vn);
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(vnready);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) qh[j] = d[j];
+          for (int j = 0; j < 16; ++j) qh[j] = d[j];
         }
       }
-      const float decay = scs[r];
-      const float qs = r >= 64 ? scs[192 + r - 64] : 0.f;
-      ok = ptx::mbar_wait_bounded(d35, (uint32_t)(c & 1)) && ok;
+      ok = ptx::mbar_wait_bounded(d3, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
       {
-        float d[32];
-        ptx::tmem_ld32(dDH + lane_base, d);
+        float d[16];
+        tmem_ld_pair16(dDH + lane_base, c0, d);
 #pragma unroll
-        for (int j = 0; j < VTILE; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
-#pragma unroll
-        for (int vg = 0; vg < 4; ++vg)
-          *reinterpret_cast<uint4 *>(Himg + img_off(r, 8 * vg, 2048)) = pack8(hs + 8 * vg);
+        for (int j = 0; j < 16; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
+        store_pair16(Himg, r, c0, 2048, hs);
         ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(hready);
       }
-      float d5[32];
-      ptx::tmem_ld32(dD5 + lane_base, d5);
+      ok = ptx::mbar_wait_bounded(d5, (uint32_t)(c & 1)) && ok;
+      ptx::tc_fence_after();
+      float d5v[16];
+      tmem_ld_pair16(dD5 + lane_base, c0, d5v);
       ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(hready);
       if (r < 64) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) X[r * 33 + j] = d5[j];
+        for (int j = 0; j < 16; ++j) X[r * 33 + c0 + j] = d5v[j];
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (r >= 64) {
         const int i = r - 64;
         if (i < L) {
-          float ov[32];
+          float ov[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = fmaf(qs, qh[j], d5[j] + X[i * 33 + j]);
+          for (int j = 0; j < 16; ++j) ov[j] = fmaf(qs, qh[j], d5v[j] + X[i * 33 + c0 + j]);
           uint4 *dst = reinterpret_cast<uint4 *>(
-              p.o + ((size_t)(b * p.T + bos + c * BT + i) * p.H + h) * p.V + v0);
-#pragma unroll
-          for (int vg = 0; vg < 4; ++vg) dst[vg] = pack8(ov + 8 * vg);
+              p.o + ((size_t)(b * p.T + bos + c * BT + i) * p.H + h) * p.V + v0 + c0);
+          dst[0] = pack8(ov);
+          dst[1] = pack8(ov + 8);
         }
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[s]);
     }
     if (!ok) {
       if (lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
     } else if (p.ht && *abort_flag == 0) {
-      float4 *dst =
-          reinterpret_cast<float4 *>(p.ht + (((size_t)n * p.H + h) * KD + r) * p.V + v0);
+      float4 *dst = reinterpret_cast<float4 *>(p.ht + (((size_t)n * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
-      for (int q = 0; q < VTILE / 4; ++q)
+      for (int q = 0; q < 4; ++q)
         dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc<128>(tmem);
+  if (warp == 0) ptx::tmem_dealloc<256>(tmem);
 }
 
 // ---------------------------------------------------------------------------
@@ -938,8 +956,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(mk, mq, p,
-                                                                                 kda ? 1 : 0);
+  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
