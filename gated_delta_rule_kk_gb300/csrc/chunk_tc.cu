@@ -173,8 +173,9 @@ __device__ __forceinline__ bool locate_chunk(const TcParams &p, int id, ChunkPos
 // ---------------------------------------------------------------------------
 // (I + A)^-1 for strictly lower-triangular 64x64 A (fp32, row stride 65) by
 // 16x16 diagonal-block forward substitution and a three-level block merge
-// (T_ij = -T_ii sum_{j<=m<i} A_im T_mj).  128 threads; X is scratch for
+// (T_ij = -T_ii sum_{j<=m<i} A_im T_mj).  NT threads; X is scratch for
 // 3 x 16 x 17 floats.  Only the lower block triangle of T is written.
+template <int NT>
 __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int tid) {
   constexpr int LD = 65, XLD = 17;
   if (tid < 64) {
@@ -192,10 +193,11 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
   }
   __syncthreads();
   // level d: blocks (b + d, b) for b = 0 .. 3 - d
+#pragma unroll 1
   for (int d = 1; d <= 3; ++d) {
     const int nblk = 4 - d;
     // X_b = sum_{m = b .. b+d-1} A_{b+d, m} T_{m, b}
-    for (int e = tid; e < nblk * 256; e += 128) {
+    for (int e = tid; e < nblk * 256; e += NT) {
       const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
       const int ro = (b + d) * 16 + r;
       float acc = 0.f;
@@ -207,7 +209,7 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
     }
     __syncthreads();
     // T_{b+d, b} = -T_{b+d, b+d} X_b
-    for (int e = tid; e < nblk * 256; e += 128) {
+    for (int e = tid; e < nblk * 256; e += NT) {
       const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
       const int o = (b + d) * 16;
       float acc = 0.f;
@@ -220,10 +222,12 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
 }
 
 // ---------------------------------------------------------------------------
-// intra kernel (128 threads)
+// intra kernel (256 threads; warps w and w + 4 share TMEM lane quarter w % 4
+// and split the columns of every accumulator row)
 //
 // shared memory (bytes):
-//   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys), cs 2048
+//   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys), cs 2048;
+//                          at the end [-w ; q], the chain's A operand
 //   VS   [32768, 49152)    v (64 tokens x V), cs 1024
 //   R1   [49152, 82432)    KDA gamma (fp32 64 x 128); then A | T (fp32, 64 x 65
 //                          each); after the solve Tw hi | Tw lo (64 x 64, cs
@@ -235,6 +239,7 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
 //   small                  scales, gamma, factors, merge scratch, barriers
 constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 82432, I_KB = 98816,
                    I_KT = 115200;
+constexpr int INTRA_THREADS = 256;
 template <bool KDA>
 struct IntraLayout {
   static constexpr uint32_t SMALL = KDA ? I_KT + 16384 : I_KB;
@@ -242,9 +247,10 @@ struct IntraLayout {
 };
 
 template <bool KDA>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(INTRA_THREADS, 1)
 intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-             const __grid_constant__ CUtensorMap tm_v, TcParams p) {
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+             TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *KQ = smem + I_KQ;
   unsigned char *VS = smem + I_VS;
@@ -266,6 +272,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   int *flags = reinterpret_cast<int *>(tmem_slot + 1);     // [0]: split exps ok
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
   const int h = blockIdx.y;
   ChunkPos cp;
   if (!locate_chunk(p, blockIdx.x, cp)) return;
@@ -280,6 +287,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::mbar_init(&bars[0], 1);
     ptx::mbar_init(&bars[1], 1);
     ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(&bars[0], 32768 + (uint32_t)V * 128 + (KDA ? 32768u : 0u));
     flags[0] = 1;
   }
   if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
@@ -288,21 +296,30 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(&bars[0], 32768 + (uint32_t)V * 128);
+  // three issuing threads, one per tensor
+  if (lane == 0 && warp < 3) {
+    if (warp == 0) {
 #pragma unroll 1
-    for (int j = 0; j < 16; ++j) {
-      ptx::tma_load_3d(KQ + j * 2048, &tm_k, 8 * j, hk, row0, &bars[0]);
-      ptx::tma_load_3d(KQ + j * 2048 + 1024, &tm_q, 8 * j, hk, row0, &bars[0]);
+      for (int j = 0; j < 16; ++j) ptx::tma_load_3d(KQ + j * 2048, &tm_k, 8 * j, hk, row0, &bars[0]);
+    } else if (warp == 1) {
+#pragma unroll 1
+      for (int j = 0; j < 16; ++j)
+        ptx::tma_load_3d(KQ + j * 2048 + 1024, &tm_q, 8 * j, hk, row0, &bars[0]);
+    } else {
+#pragma unroll 1
+      for (int j = 0; j < V / 8; ++j) ptx::tma_load_3d(VS + j * 1024, &tm_v, 8 * j, h, row0, &bars[0]);
+      // KDA: the fp32 gate tile (64 tokens x 128 channels, row-major) into R1
+      if (KDA) ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
     }
-#pragma unroll 1
-    for (int j = 0; j < V / 8; ++j) ptx::tma_load_3d(VS + j * 1024, &tm_v, 8 * j, h, row0, &bars[0]);
   }
 
   // ---- gates: gamma (chunk-local inclusive cumsum), beta, scales
-  if (tid < 64) bet[tid] = tid < L ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
+  if (warp == 4 || warp == 5) {
+    const int i = tid - 128;
+    bet[i] = i < L ? p.beta[(size_t)(row0 + i) * p.H + h] : 0.f;
+  }
   if (!KDA) {
-    if (warp == 0) {
+    if (warp == 3) {
       const float a0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
       const float a1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
       float c0, c1;
@@ -335,31 +352,15 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       eng[tid] = __expf(-gam[tid]);
       sc[128 + tid] = tid < L ? __expf(gL - gam[tid]) : 0.f;  // rs: e^{gamma_L - gamma_i}
       sc[192 + tid] = p.scale * __expf(gam[tid]);              // qs: scale e^{gamma_i}
+    } else if (tid < 192) {
+      sc[tid - 64] = __expf(gL);                               // decay per key row
     }
-    sc[tid] = __expf(gL);                                      // decay per key row
   } else {
-    // thread c owns key channel c: running cumsum down the 64 rows into R1
-    // (fp32 [64][128]); padded rows repeat row L - 1
-    float *G = Asm;
-    const int c = tid;
-    float acc = 0.f, mn = 0.f, mx = 0.f;
-    for (int i = 0; i < 64; ++i) {
-      if (i < L) {
-        const float raw = p.g[((size_t)(row0 + i) * p.H + h) * KD + c];
-        acc = p.g_is_cumsum ? raw : acc + raw;
-      }
-      G[i * KD + c] = acc;
-      mn = fminf(mn, acc);
-      mx = fmaxf(mx, acc);
+    if (tid >= KD && tid < KD + 64) {
+      const int i = tid - KD;
+      sc[128 + i] = i < L ? 1.f : 0.f;
+      sc[192 + i] = p.scale;
     }
-    gl[c] = acc;
-    sc[c] = __expf(acc);
-    if (tid < 64) {
-      sc[128 + tid] = tid < L ? 1.f : 0.f;
-      sc[192 + tid] = p.scale;
-    }
-    const bool ok = mn >= -GATE_FACTOR_LIMIT && mx <= GATE_FACTOR_LIMIT;
-    if (!__syncthreads_and(ok) && tid == 0) flags[0] = 0;
   }
   __syncthreads();
 
@@ -371,22 +372,47 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     if (warp == 0) ptx::tmem_dealloc<256>(tmem);
     return;
   }
+  if (KDA) {
+    // thread c < 128 owns key channel c: running cumsum down the TMA-loaded
+    // gate tile in place (rows >= L repeat row L - 1)
+    float *G = Asm;
+    float mn = 0.f, mx = 0.f;
+    if (tid < KD) {
+      const int c = tid;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < 64; ++i) {
+        if (i < L) acc = p.g_is_cumsum ? G[i * KD + c] : acc + G[i * KD + c];
+        G[i * KD + c] = acc;
+        mn = fminf(mn, acc);
+        mx = fmaxf(mx, acc);
+      }
+      gl[c] = acc;
+      sc[c] = __expf(acc);
+    }
+    const bool ok = mn >= -GATE_FACTOR_LIMIT && mx <= GATE_FACTOR_LIMIT;
+    if (!__syncthreads_and(ok) && tid == 0) flags[0] = 0;
+    __syncthreads();
+  }
   const bool split = flags[0] != 0;
 
   if (KDA) {
     // KQ <- [k e^g ; q e^g] (bounded by |k|, |q| for gates <= 0),
     // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g}
     const float *G = Asm;
-    for (int pc = tid; pc < 64 * 16; pc += 128) {
+    for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
       const int i = pc & 63, cg = pc >> 6;
       uint4 *kp = reinterpret_cast<uint4 *>(KQ + img_off(i, 8 * cg, 2048));
       uint4 *qp = reinterpret_cast<uint4 *>(KQ + img_off(64 + i, 8 * cg, 2048));
       float kf[8], qf[8], a[8], b[8], c[8], t[8];
       unpack8(*kp, kf);
       unpack8(*qp, qf);
+      const float4 ga = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg);
+      const float4 gb = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg + 4);
+      const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float gv = G[i * KD + 8 * cg + e];
+        const float gv = gr[e];
         const float ep = __expf(gv);
         a[e] = kf[e] * ep;
         b[e] = qf[e] * ep;
@@ -411,7 +437,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
     const unsigned char *Bop = KDA ? KB : KQ;
     const uint32_t b_cs = KDA ? 1024u : 2048u;
-#pragma unroll 1
+#pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const uint64_t a = ptx::sdesc(KQ + ks * 2 * 2048, 2048, 128);
       const uint64_t b = ptx::sdesc(Bop + ks * 2 * b_cs, b_cs, 128);
@@ -423,21 +449,23 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   mma_phase ^= 1;
   ptx::tc_fence_after();
 
-  // ---- gating: thread r holds row r of S (r < 64: kk, r >= 64: qk)
+  // ---- gating: thread (qd, hf, lane) holds row r = 32 qd + lane of S,
+  //      columns 32 hf .. 32 hf + 31 (r < 64: kk, r >= 64: qk)
   {
-    float srow[64];
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    ptx::tmem_ld32(tmem + lane_base, srow);
-    ptx::tmem_ld32(tmem + lane_base + 32, srow + 32);
-    const int i = tid & 63;
-    const bool is_q = tid >= 64;
+    const int r = qd * 32 + lane;
+    const int i = r & 63;
+    const bool is_q = r >= 64;
+    const int j0 = hf * 32;
+    float srow[32];
+    ptx::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + j0, srow);
     if (KDA && !split) {
       // exact per-element exponentials (only when |gamma| leaves the split
       // range): raw k/q from global memory, gamma from R1
       const float *G = Asm;
       const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.kraw);
       const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(is_q ? p.qraw : p.kraw);
-      for (int j = 0; j < 64; ++j) {
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = j0 + jj;
         float acc = 0.f;
         if (i < L && j <= i) {
           const size_t oi = ((size_t)(row0 + i) * p.Hk + hk) * KD;
@@ -446,7 +474,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
             acc = fmaf(__bfloat162float(xg[oi + c]) * __bfloat162float(kg[oj + c]),
                        __expf(G[i * KD + c] - G[j * KD + c]), acc);
         }
-        srow[j] = acc;
+        srow[jj] = acc;
       }
       __syncthreads();  // everyone done reading gamma before A overwrites R1
     }
@@ -454,28 +482,29 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       // A (fp32, row stride 65) for the solve: beta_i S_kk e^{g_i - g_j}, j < i < L
       const float bi = bet[i];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = j0 + jj;
         float f = 1.f;
         if (!KDA) f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
-        Asm[i * 65 + j] = (j < i && i < L) ? bi * f * srow[j] : 0.f;
+        Asm[i * 65 + j] = (j < i && i < L) ? bi * f * srow[jj] : 0.f;
       }
     } else {
       // Aqk = scale S_qk e^{g_i - g_j} (j <= i < L) as a bf16 pair:
       // hi in rows 64.., lo in rows 0.. of the AQ image
 #pragma unroll
-      for (int cg = 0; cg < 8; ++cg) {
+      for (int cg = 0; cg < 4; ++cg) {
         float v8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int j = cg * 8 + e;
+          const int j = j0 + cg * 8 + e;
           float f = 1.f;
           if (!KDA) f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
-          v8[e] = (j <= i && i < L) ? p.scale * f * srow[j] : 0.f;
+          v8[e] = (j <= i && i < L) ? p.scale * f * srow[cg * 8 + e] : 0.f;
         }
         uint4 hi, lo;
         split8(v8, hi, lo);
-        *reinterpret_cast<uint4 *>(AQ + img_off(64 + i, 8 * cg, 2048)) = hi;
-        *reinterpret_cast<uint4 *>(AQ + img_off(i, 8 * cg, 2048)) = lo;
+        *reinterpret_cast<uint4 *>(AQ + img_off(64 + i, j0 + 8 * cg, 2048)) = hi;
+        *reinterpret_cast<uint4 *>(AQ + img_off(i, j0 + 8 * cg, 2048)) = lo;
       }
     }
   }
@@ -484,24 +513,22 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   __syncthreads();
   if (tid == 0) {
     ptx::bulk_s2g(blk + OFF_AQ, AQ, 16384);
-    if (KDA) {
-      ptx::bulk_s2g(blk + OFF_KT, KTs, 16384);
-    } else {
-      // raw k (KQ rows 0..63, cs 2048) -> KT (cs 1024)
-#pragma unroll 1
-      for (int g8 = 0; g8 < 16; ++g8) ptx::bulk_s2g(blk + OFF_KT + g8 * 1024, KQ + g8 * 2048, 1024);
-    }
+    if (KDA) ptx::bulk_s2g(blk + OFF_KT, KTs, 16384);
+    ptx::bulk_commit();
+  } else if (!KDA && warp == 1 && lane < 16) {
+    // raw k (KQ rows 0..63, cs 2048) -> KT (cs 1024), one 1 KB group per lane
+    ptx::bulk_s2g(blk + OFF_KT + lane * 1024, KQ + lane * 2048, 1024);
     ptx::bulk_commit();
   }
 
   // ---- T = (I + A)^-1 (fp32)
-  unit_lower_inverse_64(Asm, Tsm, Xs, tid);
-  if (tid == 0) ptx::bulk_wait_read<0>();  // AQ and k rows may be overwritten after the barrier
-  __syncthreads();
+  unit_lower_inverse_64<INTRA_THREADS>(Asm, Tsm, Xs, tid);
+  if (tid == 0 || (!KDA && warp == 1 && lane < 16)) ptx::bulk_wait_read<0>();
+  __syncthreads();  // AQ and the k rows may be overwritten now
 
   // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) -> TW hi | lo;
   //      Tu = T diag(beta) -> AQ region hi | lo  (64 x 64 each, cs 1024)
-  for (int pc = tid; pc < 64 * 16; pc += 128) {
+  for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
     const int i = pc & 63, cg = pc >> 6;
     const bool is_u = cg >= 8;
     const int j0 = (cg & 7) * 8;
@@ -530,9 +557,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::tc_fence_after();
     const uint32_t idw = ptx::idesc_bf16(64, 128, 0, 1);
     const uint32_t idu = ptx::idesc_bf16(64, V, 0, 1);
-#pragma unroll 1
+#pragma unroll
     for (int part = 0; part < 2; ++part) {
-#pragma unroll 1
+#pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const uint64_t b = ptx::sdesc(KQ + ks * 256, 128, 2048);
         ptx::mma_bf16(dW, ptx::sdesc(TW + part * 8192 + ks * 2048, 1024, 128), b, idw,
@@ -550,12 +577,12 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   mma_phase ^= 1;
   ptx::tc_fence_after();
   {
-    // M = 64 layout: row 16 w + l lives in TMEM lane 32 w + l (l < 16);
+    // M = 64 layout: row 16 qd + l lives in TMEM lane 32 qd + l (l < 16);
     // -w replaces k in rows 0..63 of KQ (the WY GEMM has finished with it)
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int i = warp * 16 + (lane & 15);
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const int i = qd * 16 + (lane & 15);
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 2 * hf; q4 < 2 * hf + 2; ++q4) {
       float v[32];
       ptx::tmem_ld32(dW + lane_base + q4 * 32, v);
       if (lane < 16) {
@@ -569,7 +596,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
 #pragma unroll 1
-    for (int t = 0; t < V / 32; ++t) {
+    for (int t = hf; t < V / 32; t += 2) {
       float v[32];
       ptx::tmem_ld32(dU + lane_base + t * 32, v);
       if (lane < 16) {
@@ -888,6 +915,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// [rows][heads][128] fp32 gate tensor, boxes of 128 x 1 x 64 (one tile).
+bool make_gate_map(CUtensorMap *m, const float *base, int heads, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3] = {(cuuint64_t)KD, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t gstride[2] = {(cuuint64_t)KD * 4, (cuuint64_t)heads * KD * 4};
+  cuuint32_t box[3] = {KD, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), gdim, gstride, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [rows][heads][dim] bf16 tensor, boxes of 8 x 1 x 64 (16-byte rows).
 bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long rows) {
   auto fn = encode_fn();
@@ -923,11 +963,16 @@ size_t chunk_tc_workspace(const ChunkParams &p, bool kda) {
 cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStream_t stream) {
   using namespace tc;
   const bool varlen = cp.cu_seqlens != nullptr;
-  CUtensorMap mk, mq, mv;
+  CUtensorMap mk, mq, mv, mg;
   const long long rows = (long long)cp.B * cp.T;
   if (!make_map(&mk, cp.k, KD, cp.Hk, rows) || !make_map(&mq, cp.q, KD, cp.Hk, rows) ||
       !make_map(&mv, cp.v, cp.V, cp.H, rows))
     return cudaErrorInvalidValue;
+  if (kda) {
+    if (!make_gate_map(&mg, cp.g, cp.H, rows)) return cudaErrorInvalidValue;
+  } else {
+    mg = mk;  // unused by the scalar-gate kernel
+  }
   TcParams p{};
   p.g = cp.g; p.beta = cp.beta; p.h0 = cp.h0; p.ht = cp.ht;
   p.kraw = cp.k; p.qraw = cp.q;
@@ -951,7 +996,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const uint32_t ismem = kda ? IntraLayout<true>::SMEM : IntraLayout<false>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(ik, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ismem);
   if (e != cudaSuccess) return e;
-  ik<<<dim3((unsigned)nchunks, cp.H), 128, ismem, stream>>>(mk, mq, mv, p);
+  ik<<<dim3((unsigned)nchunks, cp.H), INTRA_THREADS, ismem, stream>>>(mk, mq, mv, mg, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
