@@ -111,3 +111,18 @@ def test_decode_workload_sampled(T):
     o_ref, st_ref = oracle_for(inp, sample)
     assert_close(o[sample], o_ref, TOL_BF16, "o")
     assert_close(state[sample], st_ref, TOL_BF16, "state")
+
+
+@pytest.mark.parametrize("T", [2, 4])
+def test_strong_decay(T):
+    """Gates from e^-3 down to exact fp32 zero: the kernel keeps the state as a
+    running scale times the registers and folds the scale back in before it
+    underflows; both branches must agree with the oracle."""
+    inp = synth.decode_inputs(315 + T, 5, T, 2, 4, 128, 128)
+    inp["A_log"] = torch.tensor([5.0, 4.0, 3.0, 0.0], dtype=torch.float32)
+    inp["dt_bias"] = torch.tensor([1.0, 1.0, 0.5, 0.0], dtype=torch.float32)
+    o, state = run_gpu(inp)
+    assert gdn_check_device_error() == Status.OK
+    o_ref, st_ref = oracle_for(inp, range(5))
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(state, st_ref, TOL_BF16, "state")
