@@ -2,34 +2,36 @@
 //
 // FlashInfer gdn_decode_bf16_state.py (compute_single_gate,
 // normalize_and_store_qk_to_smem, the per-token helpers and the public
-// gated_delta_rule) gives the arithmetic: per token
-//   g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b),
-//   q^ = scale q / sqrt(|q|^2 + eps), k^ = k / sqrt(|k|^2 + eps),
+// gated_delta_rule) gives the arithmetic: per token t
+//   g_t = -exp(A_log) softplus(a_t + dt_bias),  beta_t = sigmoid(b_t),
+//   q^ = scale q / sqrt(|q|^2 + eps),  k^ = k / sqrt(|k|^2 + eps),
 //   S <- e^g S;  delta = beta (v - S k^);  S <- S + delta k^T;  o = S q^.
 //
-// Design (ours): a persistent kernel, two CTAs of eight warps per SM, with no
-// block-wide barrier inside the item loop.  Each CTA walks (batch entry,
-// value head) items through a ring of NSTAGE shared-memory stages; a stage
-// holds the 32 KB state slot, the q/k/v rows and a small header (the slot
-// index), filled by bulk (TMA) copies NSTAGE items ahead.  Thread t owns rows
-// {t/8 + 32 i : i < 4} of the [V, K] state and the 16 columns
-// {8 (t%8) + j, 64 + 8 (t%8) + j : j < 8}: every quarter-warp touches 128
-// contiguous bytes (bank-conflict free), and the eight column slices of a row
-// group sit in one warp, so the L2 norms, k^.q^ and the row sums are
-// three-step butterfly shuffles.  Warps run independently: each counts
-// itself out of a stage with one shared-memory atomic, and the last warp out
-// issues the refill.  Gate inputs are prefetched into registers one item
-// ahead and the gates are computed warp-locally.  q and k enter raw: the four
-// row groups of a warp split the tokens' norms and k.q, and the L2 factors are
-// applied to row sums.  All T tokens run on fp32 registers with packed
-// two-lane FMAs, holding S / c for a running decay scale c (the product of
-// the gates so far), so a token costs three FMAs per state element:
-//   y_k = (S/c) k,  y_q = (S/c) q,
-//   delta = beta (v - c e^g fk y_k),  o = c e^g fq y_q + delta (k^ . q^),
-//   S/c' += (delta fk / c') k  with c' = c e^g;
-// when c' would fall below 2^-40 the scale is folded back into the registers.
-// Row sums are a reduce-scatter over the eight column lanes.  The slot is
-// written back once, times c, rounded to bf16 (round to nearest even).
+// Design (ours).  The T tokens of one (batch entry, value head) item are
+// taken together in the chunk (WY) form of that recurrence.  With
+// G_t = e^{g_0 + ... + g_t}, R_ts = e^{g_{s+1} + ... + g_t} (R_tt = 1) and the
+// initial state S0:
+//   y_t = S0 k^_t,  z_t = S0 q^_t                         (2T dot products)
+//   delta_t = beta_t v_t - beta_t G_t y_t - sum_{s<t} beta_t R_ts (k^_s.k^_t) delta_s
+//   o_t = G_t z_t + sum_{s<=t} R_ts (k^_s.q^_t) delta_s
+//   S_T = G_{T-1} S0 + sum_s R_{T-1,s} delta_s k^_s^T   (one rank-T update)
+// so the state is read, dotted with 2T vectors at once and updated once,
+// with no dependent per-token chain over the [V, K] tile.
+//
+// Kernel: persistent, two CTAs of eight warps per SM, no block-wide barrier
+// in the item loop.  Each CTA walks its items through NSTAGE shared-memory
+// stages filled by bulk (TMA) copies of the 32 KB state slot and the q/k/v
+// rows.  Per item one warp prepares the stage: it turns q and k into
+// normalised fp32 vectors (in place, in a lane-friendly permuted order) and
+// writes the gates and the scalar coefficients above into the stage header.
+// The first warp to finish item i prepares item i + PREP_AHEAD and the last
+// warp to finish item i issues the copies of item i + NSTAGE, so warps wait
+// on one another only through those per-stage events.  Thread t owns rows
+// {t/8 + 32 i : i < 4} of the state and the 16 columns
+// {8 (t%8) + j, 64 + 8 (t%8) + j : j < 8}; row sums are reduce-scatters over
+// the eight column lanes of a row group.  State arithmetic is fp32 on
+// registers with packed two-lane FMAs; the slot is written back once, rounded
+// to bf16 (round to nearest even).
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "ptx.cuh"
@@ -40,18 +42,29 @@ namespace {
 constexpr int DK = 128, DV = 128;
 constexpr int NWARPS = 8, DTHREADS = NWARPS * 32;
 constexpr uint32_t SLOT_BYTES = DK * DV * 2;  // 32 KB bf16 state slot
-constexpr uint32_t ROW_BYTES = DK * 2;        // one q/k/v row (256 B)
+constexpr uint32_t ROW_BYTES = DK * 2;        // one bf16 q/k/v row
+constexpr uint32_t VEC_BYTES = DK * 4;        // one fp32 q/k vector slot
 constexpr int ROWS_PER_THREAD = 4;
+constexpr int NSTAGE = 3;
+constexpr int PREP_AHEAD = 2;  // the first warp out of item i prepares item i + 2
+
+// Stage header (32-bit words): slot index, G_{T-1}, beta_t G_t, beta_t, G_t,
+// R_{T-1,t}, beta_t R_ts (k^_s.k^_t) [t][s], R_ts (k^_s.q^_t) [t][s].
+constexpr int H_SLOT = 0, H_GT = 1, H_BG = 4, H_BE = 8, H_GAM = 12, H_C = 16, H_A = 20,
+              H_B = 36;
 
 template <int T>
 struct DecodeSmem {
-  // stage: [state 32 KB][q rows][k rows][v rows][header: slot index]
-  static constexpr uint32_t HDR = SLOT_BYTES + 3 * T * ROW_BYTES;
-  static constexpr uint32_t STAGE_BYTES = HDR + 16;
+  // stage: [state 32 KB][2T vector slots: k_0..k_{T-1}, q_0..q_{T-1}][v rows][header]
+  // A vector slot receives the bf16 row in its first half; the preparing warp
+  // rewrites it as the fp32 normalised vector.
+  static constexpr uint32_t VEC = SLOT_BYTES;
+  static constexpr uint32_t VROWS = VEC + 2 * T * VEC_BYTES;
+  static constexpr uint32_t HDR = VROWS + T * ROW_BYTES;
+  static constexpr uint32_t STAGE_BYTES = HDR + 256;
   static constexpr uint32_t TX = SLOT_BYTES + 3 * T * ROW_BYTES;
-  static constexpr int NSTAGE = 3;
-  // after the stages: full barriers, then the per-stage done counters
-  static constexpr size_t BYTES = (size_t)NSTAGE * STAGE_BYTES + NSTAGE * 8 + NSTAGE * 4;
+  // after the stages: full and prepared barriers, then the per-stage done counters
+  static constexpr size_t BYTES = (size_t)NSTAGE * STAGE_BYTES + NSTAGE * 16 + NSTAGE * 4;
 };
 
 __device__ __forceinline__ float softplus_f(float x, float beta, float thr) {
@@ -59,7 +72,7 @@ __device__ __forceinline__ float softplus_f(float x, float beta, float thr) {
   return bx <= thr ? log1pf(expf(bx)) / beta : x;
 }
 
-// two fp32 FMAs in one instruction (each rounded to nearest)
+// Packed fp32 pairs (each half rounded to nearest).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 r;
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
@@ -70,6 +83,16 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return r;
 }
 
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // eight bf16 -> four fp32 pairs
 __device__ __forceinline__ void unpack8(uint4 u, float2 *f) {
   const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -77,33 +100,73 @@ __device__ __forceinline__ void unpack8(uint4 u, float2 *f) {
   for (int e = 0; e < 4; ++e) f[e] = __bfloat1622float2(h2[e]);
 }
 
-// sum over the eight column-slice lanes of a row group (lane bits 0..2)
-__device__ __forceinline__ float sum8(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 1);
-  x += __shfl_xor_sync(0xffffffffu, x, 2);
-  x += __shfl_xor_sync(0xffffffffu, x, 4);
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
   return x;
 }
 
-// Reduce-scatter over the eight column-slice lanes of a row group: v[0..3]
-// are this lane's partial S k of rows 0..3, v[4..7] its partial S q.  Lane
-// cs returns the full sum of v[4 (cs >> 2) + (cs & 3)]: lanes 0-3 hold S k of
-// row cs, lanes 4-7 S q of row cs - 4.
-__device__ __forceinline__ float reduce_scatter8(const float *v, int cs) {
+__device__ __forceinline__ float pick(bool hi, float a_lo, float a_hi) { return hi ? a_hi : a_lo; }
+
+// Row sums over the eight column lanes of a row group.  v[t][i] is this
+// lane's partial sum for token t and row i; on return y[t] holds the full sum
+// of row cs & 3 for every token (the same on lanes cs and cs ^ 4).
+template <int T>
+__device__ __forceinline__ void row_sums(const float (&v)[T][ROWS_PER_THREAD], int cs,
+                                         float (&y)[T]) {
   const bool b2 = cs & 4, b1 = cs & 2, b0 = cs & 1;
-  float w[4], x[2];
+  if constexpr (T >= 3) {
+    // tokens {2 b2, 2 b2 + 1} stay on this lane, then rows by bits 1 and 0
+    auto val = [&](int t, int i) { return t < T ? v[t][i] : 0.f; };
+    float x[2][4], w[2][2], u[2];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float keep = b2 ? v[4 + j] : v[j], send = b2 ? v[j] : v[4 + j];
-    w[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
+    for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const float keep = b1 ? w[2 + j] : w[j], send = b1 ? w[j] : w[2 + j];
-    x[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      for (int i = 0; i < 4; ++i) {
+        const float lo = val(tt, i), hi = val(2 + tt, i);
+        x[tt][i] = pick(b2, lo, hi) + __shfl_xor_sync(0xffffffffu, pick(b2, hi, lo), 4);
+      }
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii)
+        w[tt][ii] = pick(b1, x[tt][ii], x[tt][2 + ii]) +
+                    __shfl_xor_sync(0xffffffffu, pick(b1, x[tt][2 + ii], x[tt][ii]), 2);
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+      u[tt] = pick(b0, w[tt][0], w[tt][1]) +
+              __shfl_xor_sync(0xffffffffu, pick(b0, w[tt][1], w[tt][0]), 1);
+    const float o0 = __shfl_xor_sync(0xffffffffu, u[0], 4);
+    const float o1 = __shfl_xor_sync(0xffffffffu, u[1], 4);
+    const float all[4] = {pick(b2, u[0], o0), pick(b2, u[1], o1), pick(b2, o0, u[0]),
+                          pick(b2, o1, u[1])};
+#pragma unroll
+    for (int t = 0; t < T; ++t) y[t] = all[t];
+  } else if constexpr (T == 2) {
+    // token b2 stays on this lane
+    float x[4], w[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      x[i] = pick(b2, v[0][i], v[1][i]) +
+             __shfl_xor_sync(0xffffffffu, pick(b2, v[1][i], v[0][i]), 4);
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii)
+      w[ii] = pick(b1, x[ii], x[2 + ii]) +
+              __shfl_xor_sync(0xffffffffu, pick(b1, x[2 + ii], x[ii]), 2);
+    const float u = pick(b0, w[0], w[1]) + __shfl_xor_sync(0xffffffffu, pick(b0, w[1], w[0]), 1);
+    const float other = __shfl_xor_sync(0xffffffffu, u, 4);
+    y[0] = pick(b2, u, other);
+    y[1] = pick(b2, other, u);
+  } else {
+    float x[4], w[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = v[0][i] + __shfl_xor_sync(0xffffffffu, v[0][i], 4);
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii)
+      w[ii] = pick(b1, x[ii], x[2 + ii]) +
+              __shfl_xor_sync(0xffffffffu, pick(b1, x[2 + ii], x[ii]), 2);
+    y[0] = pick(b0, w[0], w[1]) + __shfl_xor_sync(0xffffffffu, pick(b0, w[1], w[0]), 1);
   }
-  const float keep = b0 ? x[1] : x[0], send = b0 ? x[0] : x[1];
-  return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
 __device__ __forceinline__ int slot_of(const DecodeParams &p, int item) {
@@ -121,11 +184,11 @@ __device__ __forceinline__ void issue(const DecodeParams &p, unsigned char *st, 
   const int bi = item / HV, hv = item % HV, hk = hv / (HV / p.H);
   int *hdr = reinterpret_cast<int *>(st + L::HDR);
   if (slot < 0 || slot >= p.pool) {
-    *hdr = -1;
+    hdr[H_SLOT] = -1;
     ptx::mbar_arrive(full);
     return;
   }
-  *hdr = slot;
+  hdr[H_SLOT] = slot;
   ptx::fence_proxy_async_smem();
   ptx::mbar_arrive_expect_tx(full, L::TX);
   const __nv_bfloat16 *state = static_cast<const __nv_bfloat16 *>(p.state);
@@ -137,9 +200,9 @@ __device__ __forceinline__ void issue(const DecodeParams &p, unsigned char *st, 
   for (int t = 0; t < T; ++t) {
     const size_t qk_off = (((size_t)bi * T + t) * p.H + hk) * DK;
     const size_t v_off = (((size_t)bi * T + t) * HV + hv) * DV;
-    ptx::bulk_g2s(st + SLOT_BYTES + t * ROW_BYTES, q + qk_off, ROW_BYTES, full);
-    ptx::bulk_g2s(st + SLOT_BYTES + (T + t) * ROW_BYTES, k + qk_off, ROW_BYTES, full);
-    ptx::bulk_g2s(st + SLOT_BYTES + (2 * T + t) * ROW_BYTES, v + v_off, ROW_BYTES, full);
+    ptx::bulk_g2s(st + L::VEC + t * VEC_BYTES, k + qk_off, ROW_BYTES, full);
+    ptx::bulk_g2s(st + L::VEC + (T + t) * VEC_BYTES, q + qk_off, ROW_BYTES, full);
+    ptx::bulk_g2s(st + L::VROWS + t * ROW_BYTES, v + v_off, ROW_BYTES, full);
   }
 }
 
@@ -161,27 +224,127 @@ __device__ __forceinline__ GateIn load_gate_in(const DecodeParams &p, int item, 
   return g;
 }
 
+// Prepare a landed stage (one warp): normalised fp32 q/k vectors in place,
+// gates and coefficients in the header; then every lane arrives on `prep`.
+// Lane l handles the four vector entries that consumer lane cs = l % 8 reads
+// as its float4 number l / 8, so both sides touch contiguous bytes.
+template <int T>
+__device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, uint64_t *full,
+                                     uint64_t *prep, uint32_t parity, GateIn gin, int lane) {
+  using L = DecodeSmem<T>;
+  if (!ptx::mbar_wait_bounded(full, parity)) record_error(p.err, GDN_ERR_TIMEOUT);
+  float *hdr = reinterpret_cast<float *>(st + L::HDR);
+  if (*reinterpret_cast<const int *>(hdr) >= 0) {
+    const int j = lane >> 3, csl = lane & 7;
+    const int c0 = (j >> 1) * 64 + csl * 8 + (j & 1) * 4;
+    float x[2 * T][4];
+#pragma unroll
+    for (int n = 0; n < 2 * T; ++n) {
+      const uint2 raw = *reinterpret_cast<const uint2 *>(st + L::VEC + n * VEC_BYTES + c0 * 2);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+      x[n][0] = a.x;
+      x[n][1] = a.y;
+      x[n][2] = b.x;
+      x[n][3] = b.y;
+    }
+    // L2 norms (q also takes the output scale)
+#pragma unroll
+    for (int n = 0; n < 2 * T; ++n) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = fmaf(x[n][e], x[n][e], ss);
+      ss = warp_sum(ss);
+      float f = p.use_qk_l2norm ? rsqrtf(ss + p.eps) : 1.f;
+      if (n >= T) f *= p.scale;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] *= f;
+    }
+    // Gram scalars: gk[t][s] = k^_s . k^_t (s < t), gq[t][s] = k^_s . q^_t (s <= t)
+    float gk[T][T], gq[T][T];
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int s = 0; s < T; ++s) {
+        float dk = 0.f, dq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dk = fmaf(x[s][e], x[t][e], dk);
+          dq = fmaf(x[s][e], x[T + t][e], dq);
+        }
+        gk[t][s] = s < t ? warp_sum(dk) : 0.f;
+        gq[t][s] = s <= t ? warp_sum(dq) : 0.f;
+      }
+    __syncwarp();  // every raw row has been read before it is overwritten
+#pragma unroll
+    for (int n = 0; n < 2 * T; ++n)
+      *reinterpret_cast<float4 *>(st + L::VEC + n * VEC_BYTES + lane * 16) =
+          make_float4(x[n][0], x[n][1], x[n][2], x[n][3]);
+
+    // gates (lane t for token t), then the coefficients (uniform over lanes)
+    float gl = 1.f, bl = 0.f;
+    if (lane < T) {
+      gl = expf(-expf(gin.A_log) *
+                softplus_f(gin.a + gin.dt_bias, p.softplus_beta, p.softplus_threshold));
+      bl = 1.f / (1.f + expf(-gin.b));
+    }
+    float gam[T], be[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      gam[t] = __shfl_sync(0xffffffffu, gl, t);
+      be[t] = __shfl_sync(0xffffffffu, bl, t);
+    }
+    float G[T], R[T][T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      G[t] = t == 0 ? gam[0] : G[t - 1] * gam[t];
+      R[t][t] = 1.f;
+#pragma unroll
+      for (int s = t - 1; s >= 0; --s) R[t][s] = R[t][s + 1] * gam[s + 1];
+    }
+    if (lane == 0) {
+      hdr[H_GT] = G[T - 1];
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        hdr[H_BG + t] = be[t] * G[t];
+        hdr[H_BE + t] = be[t];
+        hdr[H_GAM + t] = G[t];
+        hdr[H_C + t] = R[T - 1][t];
+#pragma unroll
+        for (int s = 0; s < T; ++s) {
+          hdr[H_A + 4 * t + s] = s < t ? be[t] * R[t][s] * gk[t][s] : 0.f;
+          hdr[H_B + 4 * t + s] = s <= t ? R[t][s] * gq[t][s] : 0.f;
+        }
+      }
+    }
+  }
+  ptx::mbar_arrive(prep);  // each lane releases its own writes
+}
+
 template <int T>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
   using L = DecodeSmem<T>;
-  constexpr int NSTAGE = L::NSTAGE;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NSTAGE * L::STAGE_BYTES);
-  int *done = reinterpret_cast<int *>(full + NSTAGE);
+  uint64_t *prep = full + NSTAGE;
+  int *done = reinterpret_cast<int *>(prep + NSTAGE);
 
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
+  const int lane = tid & 31, warp = tid >> 5;
   const int rg = tid >> 3;   // row group: rows rg + 32 i
   const int cs = tid & 7;    // column slice: pieces cs and cs + 8
+  const int rsel = cs & 3;   // after row_sums: this lane holds row rg + 32 rsel
   const int HV = p.HV;
   const int nitems = p.B * HV;
   const int stride = gridDim.x;
+  const int zmask = p.B >> 31;  // zero (B > 0), opaque to the compiler
   __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
   __nv_bfloat16 *state = static_cast<__nv_bfloat16 *>(p.state);
 
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&prep[s], 32);
       done[s] = 0;
     }
     ptx::fence_mbar_init();
@@ -190,11 +353,18 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       const int item = blockIdx.x + s * stride;
-      if (item < nitems) issue<T>(p, smem + (size_t)s * L::STAGE_BYTES, &full[s], item, slot_of(p, item));
+      if (item < nitems)
+        issue<T>(p, smem + (size_t)s * L::STAGE_BYTES, &full[s], item, slot_of(p, item));
     }
   }
+  // the first PREP_AHEAD items are prepared by warps 0 .. PREP_AHEAD-1
+  if (warp < PREP_AHEAD) {
+    const int item = blockIdx.x + warp * stride;
+    if (item < nitems)
+      prepare<T>(p, smem + (size_t)warp * L::STAGE_BYTES, &full[warp], &prep[warp], 0u,
+                 load_gate_in(p, item, lane, T), lane);
+  }
 
-  GateIn gin = load_gate_in(p, blockIdx.x < nitems ? blockIdx.x : 0, lane, T);
 #pragma unroll 1
   for (int it = 0;; ++it) {
     const int item = blockIdx.x + it * stride;
@@ -203,24 +373,14 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
     const uint32_t parity = (uint32_t)((it / NSTAGE) & 1);
     const int bi = item / HV, hv = item % HV;
     const int refill = item + NSTAGE * stride;
-    // prefetch: the slot of the item this stage takes next, the next item's gates
-    const int next_slot = (lane == 0 && refill < nitems) ? slot_of(p, refill) : 0;
-    const GateIn gnext = load_gate_in(p, item + stride < nitems ? item + stride : item, lane, T);
-    // this item's gates, lane t for token t
-    float gexp_l = 0.f, beta_l = 0.f;
-    if (lane < T) {
-      gexp_l = expf(-expf(gin.A_log) *
-                    softplus_f(gin.a + gin.dt_bias, p.softplus_beta, p.softplus_threshold));
-      beta_l = 1.f / (1.f + expf(-gin.b));
-    }
-    gin = gnext;
+    const int ahead = item + PREP_AHEAD * stride;
 
     if (!ptx::mbar_wait_bounded(&full[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
-    const unsigned char *st = smem + (size_t)s * L::STAGE_BYTES;
-    const int slot = *reinterpret_cast<const int *>(st + L::HDR);
+    unsigned char *st = smem + (size_t)s * L::STAGE_BYTES;
+    const float *hdr = reinterpret_cast<const float *>(st + L::HDR);
+    const int slot = *reinterpret_cast<const int *>(hdr);
 
     float2 S[ROWS_PER_THREAD][8];
-    float c = 1.f;  // the true state is c * S (running decay scale)
     if (slot >= 0) {
       const __nv_bfloat16 *ss = reinterpret_cast<const __nv_bfloat16 *>(st);
 #pragma unroll
@@ -231,132 +391,130 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
           unpack8(*reinterpret_cast<const uint4 *>(ss + row * DK + (cs + 8 * pc) * 8),
                   &S[i][pc * 4]);
       }
-      const __nv_bfloat16 *sq = reinterpret_cast<const __nv_bfloat16 *>(st + SLOT_BYTES);
+      if (!ptx::mbar_wait_bounded(&prep[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
 
-      // Norms: the four row groups of a warp take tokens grp % T; lane 8 t
-      // then holds token t's factors.
-      float fk, fq, kqh;
-      {
-        const int tn = ((lane >> 3) & 3) % T;
-        float2 kr[8], qr[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sq + (T + tn) * DK + cs * 8), &kr[0]);
-        unpack8(*reinterpret_cast<const uint4 *>(sq + (T + tn) * DK + 64 + cs * 8), &kr[4]);
-        unpack8(*reinterpret_cast<const uint4 *>(sq + tn * DK + cs * 8), &qr[0]);
-        unpack8(*reinterpret_cast<const uint4 *>(sq + tn * DK + 64 + cs * 8), &qr[4]);
-        float2 akk = make_float2(0.f, 0.f), aqq = akk, akq = akk;
+      // y_t = S0 k^_t and z_t = S0 q^_t of row rg + 32 rsel
+      float y[T], z[T];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          akk = ffma2(kr[j], kr[j], akk);
-          aqq = ffma2(qr[j], qr[j], aqq);
-          akq = ffma2(kr[j], qr[j], akq);
+      for (int kind = 0; kind < 2; ++kind) {
+        float part[T][ROWS_PER_THREAD];
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float4 *vp =
+              reinterpret_cast<const float4 *>(st + L::VEC + (kind * T + t) * VEC_BYTES) + cs;
+          float2 xv[8];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const float4 f = vp[8 * jj];
+            xv[2 * jj] = make_float2(f.x, f.y);
+            xv[2 * jj + 1] = make_float2(f.z, f.w);
+          }
+#pragma unroll
+          for (int i = 0; i < ROWS_PER_THREAD; ++i) {
+            float2 acc = fmul2(S[i][0], xv[0]);
+#pragma unroll
+            for (int m = 1; m < 8; ++m) acc = ffma2(S[i][m], xv[m], acc);
+            part[t][i] = acc.x + acc.y;
+          }
         }
-        const float ssk = sum8(akk.x + akk.y), ssq = sum8(aqq.x + aqq.y);
-        const float kqr = sum8(akq.x + akq.y);
-        fk = p.use_qk_l2norm ? rsqrtf(ssk + p.eps) : 1.f;
-        fq = (p.use_qk_l2norm ? rsqrtf(ssq + p.eps) : 1.f) * p.scale;
-        kqh = fk * fq * kqr;
+        if (kind == 0)
+          row_sums<T>(part, cs, y);
+        else
+          row_sums<T>(part, cs, z);
       }
 
-      const bool qlane = cs >= 4;  // after the reduction: lanes 0-3 hold S k, lanes 4-7 S q
-      const int rsel = cs & 3;     // ... of row rg + 32 rsel
+      // deltas and outputs of row rg + 32 rsel (the same on lanes cs and cs ^ 4)
+      float dl[T];
 #pragma unroll
       for (int t = 0; t < T; ++t) {
-        const float fk_t = __shfl_sync(0xffffffffu, fk, 8 * t);
-        const float fq_t = __shfl_sync(0xffffffffu, fq, 8 * t);
-        const float kq_t = __shfl_sync(0xffffffffu, kqh, 8 * t);
-        const float ge = __shfl_sync(0xffffffffu, gexp_l, t);
-        const float be = __shfl_sync(0xffffffffu, beta_l, t);
-        float2 kr[8], qr[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sq + (T + t) * DK + cs * 8), &kr[0]);
-        unpack8(*reinterpret_cast<const uint4 *>(sq + (T + t) * DK + 64 + cs * 8), &kr[4]);
-        unpack8(*reinterpret_cast<const uint4 *>(sq + t * DK + cs * 8), &qr[0]);
-        unpack8(*reinterpret_cast<const uint4 *>(sq + t * DK + 64 + cs * 8), &qr[4]);
+        const float vv = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(
+            st + L::VROWS + t * ROW_BYTES)[rg + 32 * rsel]);
+        float d = fmaf(hdr[H_BE + t], vv, -hdr[H_BG + t] * y[t]);
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) d = fmaf(-hdr[H_A + 4 * t + s2], dl[s2], d);
+        dl[t] = d;
+      }
+      if (cs < 4) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          float ov = hdr[H_GAM + t] * z[t];
+#pragma unroll
+          for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[s2], ov);
+          o[(((size_t)bi * T + t) * HV + hv) * DV + rg + 32 * rsel] = __float2bfloat16_rn(ov);
+        }
+      }
 
-        // raw row dots S k and S q, partial over this lane's 16 columns
-        float vals[2 * ROWS_PER_THREAD];
+      // S <- G_{T-1} S + sum_t R_{T-1,t} delta_t k^_t^T
+      const float gt = hdr[H_GT];
+#pragma unroll
+      for (int i = 0; i < ROWS_PER_THREAD; ++i)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) S[i][m] = fmul2(make_float2(gt, gt), S[i][m]);
+      // Token t's vector loads take a (zero) offset computed from token t-1's
+      // first result, so the compiler cannot hoist all T vectors at once.
+      int chain = 0;
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const float4 *vp =
+            reinterpret_cast<const float4 *>(st + L::VEC + t * VEC_BYTES + chain) + cs;
+        float2 kv[8];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float4 f = vp[8 * jj];
+          kv[2 * jj] = make_float2(f.x, f.y);
+          kv[2 * jj + 1] = make_float2(f.z, f.w);
+        }
+        const float ct = hdr[H_C + t];
 #pragma unroll
         for (int i = 0; i < ROWS_PER_THREAD; ++i) {
-          float2 ak = make_float2(0.f, 0.f), aq = ak;
+          const float cf = ct * __shfl_sync(0xffffffffu, dl[t], i, 8);
+          const float2 c2 = make_float2(cf, cf);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            ak = ffma2(S[i][j], kr[j], ak);
-            aq = ffma2(S[i][j], qr[j], aq);
-          }
-          vals[i] = ak.x + ak.y;
-          vals[ROWS_PER_THREAD + i] = aq.x + aq.y;
+          for (int m = 0; m < 8; ++m) S[i][m] = ffma2(c2, kv[m], S[i][m]);
         }
-        const float y = reduce_scatter8(vals, cs);
-
-        const float cg = c * ge;  // decay of the true state through token t
-        const float vv = __bfloat162float(sq[(2 * T + t) * DK + rg + 32 * rsel]);
-        const float delta = be * (vv - cg * fk_t * y);      // valid on lanes 0-3
-        const float dq = __shfl_xor_sync(0xffffffffu, delta, 4);
-        if (qlane)
-          o[(((size_t)bi * T + t) * HV + hv) * DV + rg + 32 * rsel] =
-              __float2bfloat16_rn(fmaf(cg * fq_t, y, dq * kq_t));
-        float d[ROWS_PER_THREAD];
-#pragma unroll
-        for (int i = 0; i < ROWS_PER_THREAD; ++i) d[i] = __shfl_sync(0xffffffffu, delta, i, 8);
-
-        if (cg >= 0x1p-40f) {
-          // S <- S + (delta fk / cg) k_raw, and the scale takes the decay
-          const float f = fk_t / cg;
-#pragma unroll
-          for (int i = 0; i < ROWS_PER_THREAD; ++i) {
-            const float2 d2 = make_float2(d[i] * f, d[i] * f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) S[i][j] = ffma2(d2, kr[j], S[i][j]);
-          }
-          c = cg;
-        } else {
-          // the scale would underflow: fold it into S
-          const float2 g2 = make_float2(cg, cg), z2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int i = 0; i < ROWS_PER_THREAD; ++i) {
-            const float2 d2 = make_float2(d[i] * fk_t, d[i] * fk_t);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) S[i][j] = ffma2(g2, S[i][j], ffma2(d2, kr[j], z2));
-          }
-          c = 1.f;
-        }
+        chain = __float_as_int(S[0][0].x) & zmask;
       }
     }
 
-    // This warp has read all of stage s; the last warp out refills it.
+    // This warp has read all of stage s.  The last warp out refills it; the
+    // first warp out prepares the item PREP_AHEAD ahead after its write-back.
     __syncwarp();
+    int order = 0;
     if (lane == 0) {
       __threadfence_block();
-      if (atomicAdd(&done[s], 1) == NWARPS - 1) {
+      order = atomicAdd(&done[s], 1);
+      if (order == NWARPS - 1) {
         done[s] = 0;
         __threadfence_block();
-        if (refill < nitems)
-          issue<T>(p, smem + (size_t)s * L::STAGE_BYTES, &full[s], refill, next_slot);
+        if (refill < nitems) issue<T>(p, st, &full[s], refill, slot_of(p, refill));
       }
     }
-    __syncwarp();
+    order = __shfl_sync(0xffffffffu, order, 0);
 
     if (slot < 0) {
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
       for (int idx = tid; idx < T * DV; idx += DTHREADS)
         o[(((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV] = __float2bfloat16_rn(0.f);
-      continue;
-    }
-    // write the slot back once
-    __nv_bfloat16 *dst = state + ((size_t)slot * HV + hv) * DV * DK;
+    } else {
+      __nv_bfloat16 *dst = state + ((size_t)slot * HV + hv) * DV * DK;
 #pragma unroll
-    for (int i = 0; i < ROWS_PER_THREAD; ++i) {
-      const int row = rg + 32 * i;
+      for (int i = 0; i < ROWS_PER_THREAD; ++i) {
+        const int row = rg + 32 * i;
 #pragma unroll
-      for (int pc = 0; pc < 2; ++pc) {
-        uint4 w;
-        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&w);
+        for (int pc = 0; pc < 2; ++pc) {
+          uint4 w;
+          __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 x = S[i][pc * 4 + e];
-          h2[e] = __float22bfloat162_rn(make_float2(c * x.x, c * x.y));
+          for (int e = 0; e < 4; ++e) h2[e] = __float22bfloat162_rn(S[i][pc * 4 + e]);
+          *reinterpret_cast<uint4 *>(dst + row * DK + (cs + 8 * pc) * 8) = w;
         }
-        *reinterpret_cast<uint4 *>(dst + row * DK + (cs + 8 * pc) * 8) = w;
       }
+    }
+    if (order == 0 && ahead < nitems) {
+      const int sa = (it + PREP_AHEAD) % NSTAGE;
+      prepare<T>(p, smem + (size_t)sa * L::STAGE_BYTES, &full[sa], &prep[sa],
+                 (uint32_t)(((it + PREP_AHEAD) / NSTAGE) & 1), load_gate_in(p, ahead, lane, T),
+                 lane);
     }
   }
 }
@@ -380,8 +538,14 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
+  // persistent grid: as many CTAs as are resident at once (two per SM)
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T>, DTHREADS, bytes);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
   const int items = p.B * p.HV;
-  const int grid = items < 2 * sm_count() ? items : 2 * sm_count();
+  const int cap = per_sm * sm_count();
+  const int grid = items < cap ? items : cap;
   decode_kernel<T><<<grid, DTHREADS, bytes, stream>>>(p);
   return cudaGetLastError();
 }
