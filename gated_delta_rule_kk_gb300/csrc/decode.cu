@@ -36,6 +36,8 @@
 #include "gdn_internal.h"
 #include "ptx.cuh"
 
+#include <type_traits>
+
 namespace gdn {
 namespace {
 
@@ -108,41 +110,16 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ float pick(bool hi, float a_lo, float a_hi) { return hi ? a_hi : a_lo; }
 
-// Row sums over the eight column lanes of a row group.  v[t][i] is this
-// lane's partial sum for token t and row i; on return y[t] holds the full sum
-// of row cs & 3 for every token (the same on lanes cs and cs ^ 4).
+// Row sums over the eight column lanes of a row group, for one or two
+// tokens.  v[t][i] is this lane's partial sum for token t and row i; on
+// return y[t] holds the full sum of row cs & 3 (the same on lanes cs and
+// cs ^ 4).
 template <int T>
 __device__ __forceinline__ void row_sums(const float (&v)[T][ROWS_PER_THREAD], int cs,
                                          float (&y)[T]) {
   const bool b2 = cs & 4, b1 = cs & 2, b0 = cs & 1;
-  if constexpr (T >= 3) {
-    // tokens {2 b2, 2 b2 + 1} stay on this lane, then rows by bits 1 and 0
-    auto val = [&](int t, int i) { return t < T ? v[t][i] : 0.f; };
-    float x[2][4], w[2][2], u[2];
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = val(tt, i), hi = val(2 + tt, i);
-        x[tt][i] = pick(b2, lo, hi) + __shfl_xor_sync(0xffffffffu, pick(b2, hi, lo), 4);
-      }
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-      for (int ii = 0; ii < 2; ++ii)
-        w[tt][ii] = pick(b1, x[tt][ii], x[tt][2 + ii]) +
-                    __shfl_xor_sync(0xffffffffu, pick(b1, x[tt][2 + ii], x[tt][ii]), 2);
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-      u[tt] = pick(b0, w[tt][0], w[tt][1]) +
-              __shfl_xor_sync(0xffffffffu, pick(b0, w[tt][1], w[tt][0]), 1);
-    const float o0 = __shfl_xor_sync(0xffffffffu, u[0], 4);
-    const float o1 = __shfl_xor_sync(0xffffffffu, u[1], 4);
-    const float all[4] = {pick(b2, u[0], o0), pick(b2, u[1], o1), pick(b2, o0, u[0]),
-                          pick(b2, o1, u[1])};
-#pragma unroll
-    for (int t = 0; t < T; ++t) y[t] = all[t];
-  } else if constexpr (T == 2) {
+  static_assert(T == 1 || T == 2, "row sums are taken one or two tokens at a time");
+  if constexpr (T == 2) {
     // token b2 stays on this lane
     float x[4], w[2];
 #pragma unroll
@@ -393,15 +370,15 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
       }
       if (!ptx::mbar_wait_bounded(&prep[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
 
-      // y_t = S0 k^_t and z_t = S0 q^_t of row rg + 32 rsel
+      // y_t = S0 k^_t and z_t = S0 q^_t of row rg + 32 rsel, two tokens at a time
       float y[T], z[T];
+      auto dots = [&](auto n0_c, auto nt_c, float *out) {
+        constexpr int N0 = decltype(n0_c)::value, NT = decltype(nt_c)::value;
+        float part[NT][ROWS_PER_THREAD];
 #pragma unroll
-      for (int kind = 0; kind < 2; ++kind) {
-        float part[T][ROWS_PER_THREAD];
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < NT; ++t) {
           const float4 *vp =
-              reinterpret_cast<const float4 *>(st + L::VEC + (kind * T + t) * VEC_BYTES) + cs;
+              reinterpret_cast<const float4 *>(st + L::VEC + (N0 + t) * VEC_BYTES) + cs;
           float2 xv[8];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -417,10 +394,24 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
             part[t][i] = acc.x + acc.y;
           }
         }
-        if (kind == 0)
-          row_sums<T>(part, cs, y);
-        else
-          row_sums<T>(part, cs, z);
+        float r[NT];
+        row_sums<NT>(part, cs, r);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) out[t] = r[t];
+      };
+      using C0 = std::integral_constant<int, 0>;
+      using C2 = std::integral_constant<int, 2>;
+      using CT = std::integral_constant<int, T>;
+      using CT2 = std::integral_constant<int, T + 2>;
+      if constexpr (T <= 2) {
+        dots(C0{}, CT{}, y);
+        dots(CT{}, CT{}, z);
+      } else {
+        using CR = std::integral_constant<int, T - 2>;
+        dots(C0{}, C2{}, y);
+        dots(C2{}, CR{}, y + 2);
+        dots(CT{}, C2{}, z);
+        dots(CT2{}, CR{}, z + 2);
       }
 
       // deltas and outputs of row rg + 32 rsel (the same on lanes cs and cs ^ 4)
