@@ -17,7 +17,7 @@
 //    carry fp32-grade accuracy.  Per (chunk, head) the kernel stores a block
 //    of ready-made operand images the sequential pass consumes directly:
 //      AW  [-w ; q] (bf16)                U   u (fp32, per 32-wide V tile)
-//      KT  k (bf16)                       SC  exp(gamma_L) per key row,
+//      KT  k e^{gamma_L - gamma} (bf16)   SC  exp(gamma_L) per key row,
 //      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)      exp(gamma_L - gamma_i) and
 //                                              scale exp(gamma_i) per token
 //    For the per-channel gate (KDA, vLLM kimi_k3 kda/chunk_intra,
@@ -35,7 +35,7 @@
 //    whole sequence).  Per chunk
 //      D1  = [-w ; q~] bf16(h)            rows 0..63: -w h, rows 64..127: q h
 //      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
-//      DH  = k~^T (e^{gamma_L - gamma} v_new)
+//      DH  = k~^T v_new                  (k~ = k e^{gamma_L - gamma}, from KT)
 //      D5  = [Aqk_lo ; Aqk_hi] v_new
 //      h   = exp(gamma_L) h + DH
 //      o   = scale e^gamma (q h) + Aqk v_new
@@ -171,51 +171,93 @@ __device__ __forceinline__ bool locate_chunk(const TcParams &p, int id, ChunkPos
 }
 
 // ---------------------------------------------------------------------------
-// (I + A)^-1 for strictly lower-triangular 64x64 A (fp32, row stride 65) by
-// 16x16 diagonal-block forward substitution and a three-level block merge
-// (T_ij = -T_ii sum_{j<=m<i} A_im T_mj).  NT threads; X is scratch for
-// 3 x 16 x 17 floats.  Only the lower block triangle of T is written.
+// (I + A)^-1 for strictly lower-triangular 64x64 A (fp32, row stride SLD, rows
+// 16-byte aligned) by 16x16 diagonal-block forward substitution and a
+// three-level block merge (T_ij = -T_ii sum_{j<=m<i} A_im T_mj).  NT threads;
+// X is scratch for 3 x 16 x XLD floats.  Only the lower block triangle of T
+// is written.  The merges run as 2 x 2 register tiles fed by 16-byte row
+// loads of A and 8-byte row loads of T, so shared-memory traffic is one load
+// per two FMAs or better.
+constexpr int SLD = 68, XLD = 18;
 template <int NT>
 __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int tid) {
-  constexpr int LD = 65, XLD = 17;
   if (tid < 64) {
+    // thread (o, j): column j of diagonal block o
     const int o = (tid >> 4) * 16, j = tid & 15;
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float acc = (i == j) ? 1.f : 0.f;
+      float a[16];
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc = fmaf(-A[(o + i) * LD + o + m], x[m], acc);
-      x[i] = acc;
+      for (int q = 0; q < 4; ++q) {
+        if (4 * q < i) {
+          const float4 v = *reinterpret_cast<const float4 *>(A + (o + i) * SLD + o + 4 * q);
+          a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+        }
+      }
+      float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) {
+        if (m & 1) acc1 = fmaf(-a[m], x[m], acc1);
+        else acc0 = fmaf(-a[m], x[m], acc0);
+      }
+      x[i] = acc0 + acc1;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Tm[(o + i) * LD + o + j] = x[i];
+    for (int i = 0; i < 16; ++i) Tm[(o + i) * SLD + o + j] = x[i];
   }
   __syncthreads();
-  // level d: blocks (b + d, b) for b = 0 .. 3 - d
+  // level d: blocks (b + d, b) for b = 0 .. 3 - d; 64 two-by-two tiles per block
 #pragma unroll 1
   for (int d = 1; d <= 3; ++d) {
-    const int nblk = 4 - d;
+    const int ntile = (4 - d) * 64;
     // X_b = sum_{m = b .. b+d-1} A_{b+d, m} T_{m, b}
-    for (int e = tid; e < nblk * 256; e += NT) {
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      const int ro = (b + d) * 16 + r;
-      float acc = 0.f;
-      for (int mb = b; mb < b + d; ++mb)
+    for (int e = tid; e < ntile; e += NT) {
+      const int b = e >> 6, rr = ((e >> 3) & 7) * 2, cc = (e & 7) * 2;
+      const float *a0 = A + ((b + d) * 16 + rr) * SLD;
+      const float *a1 = a0 + SLD;
+      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+#pragma unroll 2
+      for (int k = b * 16; k < (b + d) * 16; k += 4) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(a0 + k);
+        const float4 x1 = *reinterpret_cast<const float4 *>(a1 + k);
+        const float r0[4] = {x0.x, x0.y, x0.z, x0.w}, r1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          acc = fmaf(A[ro * LD + mb * 16 + m], Tm[(mb * 16 + m) * LD + b * 16 + cc], acc);
-      X[(b * 16 + r) * XLD + cc] = acc;
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 t = *reinterpret_cast<const float2 *>(Tm + (k + kk) * SLD + b * 16 + cc);
+          s00 = fmaf(r0[kk], t.x, s00);
+          s01 = fmaf(r0[kk], t.y, s01);
+          s10 = fmaf(r1[kk], t.x, s10);
+          s11 = fmaf(r1[kk], t.y, s11);
+        }
+      }
+      *reinterpret_cast<float2 *>(X + (b * 16 + rr) * XLD + cc) = make_float2(s00, s01);
+      *reinterpret_cast<float2 *>(X + (b * 16 + rr + 1) * XLD + cc) = make_float2(s10, s11);
     }
     __syncthreads();
     // T_{b+d, b} = -T_{b+d, b+d} X_b
-    for (int e = tid; e < nblk * 256; e += NT) {
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+    for (int e = tid; e < ntile; e += NT) {
+      const int b = e >> 6, rr = ((e >> 3) & 7) * 2, cc = (e & 7) * 2;
       const int o = (b + d) * 16;
-      float acc = 0.f;
+      const float *t0 = Tm + (o + rr) * SLD + o;
+      const float *t1 = t0 + SLD;
+      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc = fmaf(Tm[(o + r) * LD + o + m], X[(b * 16 + m) * XLD + cc], acc);
-      Tm[(o + r) * LD + b * 16 + cc] = -acc;
+      for (int k = 0; k < 16; k += 4) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(t0 + k);
+        const float4 x1 = *reinterpret_cast<const float4 *>(t1 + k);
+        const float r0[4] = {x0.x, x0.y, x0.z, x0.w}, r1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float2 xv = *reinterpret_cast<const float2 *>(X + (b * 16 + k + kk) * XLD + cc);
+          s00 = fmaf(r0[kk], xv.x, s00);
+          s01 = fmaf(r0[kk], xv.y, s01);
+          s10 = fmaf(r1[kk], xv.x, s10);
+          s11 = fmaf(r1[kk], xv.y, s11);
+        }
+      }
+      *reinterpret_cast<float2 *>(Tm + (o + rr) * SLD + b * 16 + cc) = make_float2(-s00, -s01);
+      *reinterpret_cast<float2 *>(Tm + (o + rr + 1) * SLD + b * 16 + cc) = make_float2(-s10, -s11);
     }
     __syncthreads();
   }
@@ -229,16 +271,16 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
 //   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys), cs 2048;
 //                          at the end [-w ; q], the chain's A operand
 //   VS   [32768, 49152)    v (64 tokens x V), cs 1024
-//   R1   [49152, 82432)    KDA gamma (fp32 64 x 128); then A | T (fp32, 64 x 65
+//   R1   [49152, 83968)    KDA gamma (fp32 64 x 128); then A | T (fp32, 64 x 68
 //                          each); after the solve Tw hi | Tw lo (64 x 64, cs
 //                          1024) over A
-//   AQ   [82432, 98816)    [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
+//   AQ   [83968, 100352)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
 //                          Tu hi | Tu lo
-//   KB   [98816, 115200)   KDA: k e^-g (64 x 128, cs 1024)
-//   KT   [115200, 131584)  KDA: k e^{gamma_L - g} (64 x 128, cs 1024)
+//   KB   [100352, 116736)  KDA: k e^-g (64 x 128, cs 1024)
+//   KT   [116736, 133120)  KDA: k e^{gamma_L - g} (64 x 128, cs 1024)
 //   small                  scales, gamma, factors, merge scratch, barriers
-constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 82432, I_KB = 98816,
-                   I_KT = 115200;
+constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 83968, I_KB = 100352,
+                   I_KT = 116736;
 constexpr int INTRA_THREADS = 256;
 template <bool KDA>
 struct IntraLayout {
@@ -255,7 +297,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   unsigned char *KQ = smem + I_KQ;
   unsigned char *VS = smem + I_VS;
   float *Asm = reinterpret_cast<float *>(smem + I_R1);
-  float *Tsm = Asm + 64 * 65;
+  float *Tsm = Asm + 64 * SLD;
   unsigned char *TW = smem + I_R1;   // Tw hi, Tw lo (after the solve)
   unsigned char *AQ = smem + I_AQ;   // Aqk pair, later Tu hi, Tu lo
   unsigned char *KB = smem + I_KB;
@@ -266,8 +308,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   float *eg = bet + 64;                                    // [64] e^{gamma}
   float *eng = eg + 64;                                    // [64] e^{-gamma}
   float *gl = eng + 64;                                    // [128] KDA gamma_L
-  float *Xs = gl + 128;                                    // merge scratch 3 x 16 x 17
-  uint64_t *bars = reinterpret_cast<uint64_t *>(Xs + 3 * 16 * 17 + 4);  // tma, mma
+  float *Xs = gl + 128;                                    // merge scratch 3 x 16 x XLD
+  uint64_t *bars = reinterpret_cast<uint64_t *>(Xs + 3 * 16 * XLD + 4);  // tma, mma
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
   int *flags = reinterpret_cast<int *>(tmem_slot + 1);     // [0]: split exps ok
 
@@ -445,6 +487,19 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     }
     ptx::mma_commit(&bars[1]);
   }
+  if (!KDA) {
+    // KT = k e^{gamma_L - gamma_i} (zero on padding rows), straight into the
+    // block while the GEMM runs; the chain's state update takes it as is
+    for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
+      const int i = pc & 63, cg = pc >> 6;
+      float kf[8];
+      unpack8(*reinterpret_cast<const uint4 *>(KQ + img_off(i, 8 * cg, 2048)), kf);
+      const float r = sc[128 + i];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) kf[e] *= r;
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 1024)) = pack8(kf);
+    }
+  }
   const bool ok1 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
   mma_phase ^= 1;
   ptx::tc_fence_after();
@@ -479,14 +534,19 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       __syncthreads();  // everyone done reading gamma before A overwrites R1
     }
     if (!is_q) {
-      // A (fp32, row stride 65) for the solve: beta_i S_kk e^{g_i - g_j}, j < i < L
+      // A (fp32, row stride SLD) for the solve: beta_i S_kk e^{g_i - g_j}, j < i < L
       const float bi = bet[i];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = j0 + jj;
-        float f = 1.f;
-        if (!KDA) f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
-        Asm[i * 65 + j] = (j < i && i < L) ? bi * f * srow[jj] : 0.f;
+      for (int j4 = 0; j4 < 32; j4 += 4) {
+        float a4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = j0 + j4 + e;
+          float f = 1.f;
+          if (!KDA) f = split ? eg[i] * eng[j] : __expf(gam[i] - gam[j]);
+          a4[e] = (j < i && i < L) ? bi * f * srow[j4 + e] : 0.f;
+        }
+        *reinterpret_cast<float4 *>(Asm + i * SLD + j0 + j4) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
     } else {
       // Aqk = scale S_qk e^{g_i - g_j} (j <= i < L) as a bf16 pair:
@@ -515,15 +575,11 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::bulk_s2g(blk + OFF_AQ, AQ, 16384);
     if (KDA) ptx::bulk_s2g(blk + OFF_KT, KTs, 16384);
     ptx::bulk_commit();
-  } else if (!KDA && warp == 1 && lane < 16) {
-    // raw k (KQ rows 0..63, cs 2048) -> KT (cs 1024), one 1 KB group per lane
-    ptx::bulk_s2g(blk + OFF_KT + lane * 1024, KQ + lane * 2048, 1024);
-    ptx::bulk_commit();
   }
 
   // ---- T = (I + A)^-1 (fp32)
   unit_lower_inverse_64<INTRA_THREADS>(Asm, Tsm, Xs, tid);
-  if (tid == 0 || (!KDA && warp == 1 && lane < 16)) ptx::bulk_wait_read<0>();
+  if (tid == 0) ptx::bulk_wait_read<0>();
   __syncthreads();  // AQ and the k rows may be overwritten now
 
   // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) -> TW hi | lo;
@@ -532,11 +588,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     const int i = pc & 63, cg = pc >> 6;
     const bool is_u = cg >= 8;
     const int j0 = (cg & 7) * 8;
-    float v8[8];
+    float v8[8], t8[8];
+    {
+      const float4 x0 = *reinterpret_cast<const float4 *>(Tsm + i * SLD + j0);
+      const float4 x1 = *reinterpret_cast<const float4 *>(Tsm + i * SLD + j0 + 4);
+      t8[0] = x0.x; t8[1] = x0.y; t8[2] = x0.z; t8[3] = x0.w;
+      t8[4] = x1.x; t8[5] = x1.y; t8[6] = x1.z; t8[7] = x1.w;
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int j = j0 + e;
-      const float t = (j <= i) ? Tsm[i * 65 + j] : 0.f;
+      const float t = (j <= i) ? t8[e] : 0.f;
       const float d = (is_u || KDA) ? bet[j] : bet[j] * eg[j];
       v8[e] = t * d;
     }
@@ -630,15 +692,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 //   AQ  [49152, 65536)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
 //   SC  [65536, 66560)   decay[128], rs[64], qs[64]
 //   U   [66560, 74752)   u tile, fp32 64 x 32
-// then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo] and
-// VS = [vs_hi | vs_lo] (64 tokens x 64, cs 1024) and the fp32 exchange X.
+// then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo]
+// (64 tokens x 64, cs 1024) and the fp32 exchange X.  The epilogue warps are
+// done with a stage once v_new is formed (SC and U read), so they release it
+// then, not after the output: the next block streams in a step earlier.
 // Every bf16 pair rides in the N dimension of one GEMM (N = 64), so the
 // split costs no extra tcgen05 instructions; each accumulator holds the two
 // halves side by side and the epilogue adds them.
 constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 49152, S_SC = 65536, S_U = 66560,
                    STAGE_BYTES = 74752;
-constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_VS = C_VN + 8192,
-                   C_X = C_VS + 8192, C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
+constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_X = C_VN + 8192,
+                   C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
 constexpr int CHAIN_THREADS = 320;
 constexpr int EPI_WARPS = 8;
 
@@ -674,7 +738,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char *Himg = smem + C_H;
   unsigned char *VN = smem + C_VN;
-  unsigned char *VSi = smem + C_VS;
   float *X = reinterpret_cast<float *>(smem + C_X);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C_BAR);
   uint64_t *full = bar, *empty = bar + 2, *d1 = bar + 4, *d3 = bar + 5, *d5 = bar + 6,
@@ -745,7 +808,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       const uint32_t id_kmn = ptx::idesc_bf16(128, 2 * VTILE, 0, 1);   // A K-major, B MN-major
       const uint32_t id_mnmn = ptx::idesc_bf16(128, 2 * VTILE, 1, 1);  // both MN-major
       const uint64_t dH0 = ptx::sdesc(Himg, 128, 2048);
-      const uint64_t dVS0 = ptx::sdesc(VSi, 128, 1024);
       const uint64_t dVN0 = ptx::sdesc(VN, 128, 1024);
       bool ok = true;
 #pragma unroll 1
@@ -765,10 +827,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         ptx::mma_commit(d1);
         ok = ptx::mbar_wait_bounded(vnready, (uint32_t)(c & 1)) && ok;
         ptx::tc_fence_after();
-        // DH = k~^T [vs_hi | vs_lo]  (critical path), then D5 = AQ [vn_hi | vn_lo]
+        // DH = k~^T [vn_hi | vn_lo]  (critical path), then D5 = AQ [vn_hi | vn_lo]
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVS0, ks * 256), id_mnmn, ks > 0);
+          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, ks * 256), id_mnmn, ks > 0);
         ptx::mma_commit(d3);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -823,8 +885,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         tmem_ld_pair16(dD1 + lane_base, c0, d);
         if (r < 64) {
           const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128 + c0 * 4);
-          const float rs = scs[128 + r];
-          float vn[16], vs[16];
+          float vn[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float4 u = u4[q];
@@ -833,9 +894,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
             vn[4 * q + 2] = u.z + d[4 * q + 2];
             vn[4 * q + 3] = u.w + d[4 * q + 3];
           }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) vs[j] = rs * vn[j];
-          store_pair16(VSi, r, c0, 1024, vs);
           store_pair16(VN, r, c0, 1024, vn);
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
@@ -846,6 +904,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
           for (int j = 0; j < 16; ++j) qh[j] = d[j];
         }
       }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp no longer reads stage s
       ok = ptx::mbar_wait_bounded(d3, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
       {
@@ -882,8 +942,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&empty[s]);
     }
     if (!ok) {
       if (lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
