@@ -325,6 +325,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   const int row0 = cp.b * p.T + s0;  // token row in the [B*T] flattening
   unsigned char *blk = p.blocks + ((size_t)blockIdx.x * p.H + h) * p.block;
 
+  // Loads first: the gate inputs into registers (warp 3: g, warps 4-5: beta)
+  // and the TMA of k, q, v, so their latency overlaps the set-up below.
+  float ga0 = 0.f, ga1 = 0.f, gbe = 0.f;
+  if (!KDA && warp == 3) {
+    ga0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
+    ga1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+  }
+  if (warp == 4 || warp == 5) {
+    const int i = tid - 128;
+    gbe = i < L ? p.beta[(size_t)(row0 + i) * p.H + h] : 0.f;
+  }
   if (tid == 0) {
     ptx::mbar_init(&bars[0], 1);
     ptx::mbar_init(&bars[1], 1);
@@ -332,13 +343,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::mbar_arrive_expect_tx(&bars[0], 32768 + (uint32_t)V * 128 + (KDA ? 32768u : 0u));
     flags[0] = 1;
   }
-  if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  // three issuing threads, one per tensor
+  // three issuing threads, one per tensor, once warp 0 has set the barrier up
+  if (warp < 3) asm volatile("bar.sync 1, 96;" ::: "memory");
   if (lane == 0 && warp < 3) {
     if (warp == 0) {
 #pragma unroll 1
@@ -354,16 +360,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       if (KDA) ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
     }
   }
+  if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
   // ---- gates: gamma (chunk-local inclusive cumsum), beta, scales
-  if (warp == 4 || warp == 5) {
-    const int i = tid - 128;
-    bet[i] = i < L ? p.beta[(size_t)(row0 + i) * p.H + h] : 0.f;
-  }
+  if (warp == 4 || warp == 5) bet[tid - 128] = gbe;
   if (!KDA) {
     if (warp == 3) {
-      const float a0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
-      const float a1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+      const float a0 = ga0, a1 = ga1;
       float c0, c1;
       if (p.g_is_cumsum) {
         c0 = a0;
@@ -676,7 +683,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   if (tid == 0) {
     ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
     ptx::bulk_commit();
-    ptx::bulk_wait<0>();
+    ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   }
   if (!(ok1 && ok2) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
   __syncthreads();
