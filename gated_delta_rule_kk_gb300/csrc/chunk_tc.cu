@@ -302,6 +302,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   unsigned char *AQ = smem + I_AQ;   // Aqk pair, later Tu hi, Tu lo
   unsigned char *KB = smem + I_KB;
   unsigned char *KTs = smem + I_KT;
+  // staging for the row-major k | q | v tiles (48 KB): regions first written
+  // by the gating (GDN: R1 + AQ; KDA, whose gate tile takes R1: AQ + KB + KT)
+  unsigned char *STG = smem + (KDA ? I_AQ : I_R1);
   float *sc = reinterpret_cast<float *>(smem + IntraLayout<KDA>::SMALL);  // decay, rs, qs
   float *gam = sc + 256;                                   // [64]
   float *bet = gam + 64;                                   // [64]
@@ -345,17 +348,20 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
   // three issuing threads, one per tensor, once warp 0 has set the barrier up
   if (warp < 3) asm volatile("bar.sync 1, 96;" ::: "memory");
+  // k, q and v arrive row-major (128-byte, resp. 64-byte rows: few large
+  // requests) in a staging area that is free until the gating, and are
+  // rearranged into the operand images once they land
   if (lane == 0 && warp < 3) {
     if (warp == 0) {
-#pragma unroll 1
-      for (int j = 0; j < 16; ++j) ptx::tma_load_3d(KQ + j * 2048, &tm_k, 8 * j, hk, row0, &bars[0]);
+      ptx::tma_load_3d(STG, &tm_k, 0, hk, row0, &bars[0]);
+      ptx::tma_load_3d(STG + 8192, &tm_k, 64, hk, row0, &bars[0]);
     } else if (warp == 1) {
-#pragma unroll 1
-      for (int j = 0; j < 16; ++j)
-        ptx::tma_load_3d(KQ + j * 2048 + 1024, &tm_q, 8 * j, hk, row0, &bars[0]);
+      ptx::tma_load_3d(STG + 16384, &tm_q, 0, hk, row0, &bars[0]);
+      ptx::tma_load_3d(STG + 24576, &tm_q, 64, hk, row0, &bars[0]);
     } else {
 #pragma unroll 1
-      for (int j = 0; j < V / 8; ++j) ptx::tma_load_3d(VS + j * 1024, &tm_v, 8 * j, h, row0, &bars[0]);
+      for (int j = 0; j < V / 32; ++j)
+        ptx::tma_load_3d(STG + 32768 + j * 4096, &tm_v, 32 * j, h, row0, &bars[0]);
       // KDA: the fp32 gate tile (64 tokens x 128 channels, row-major) into R1
       if (KDA) ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
     }
@@ -421,6 +427,27 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     if (warp == 0) ptx::tmem_dealloc<256>(tmem);
     return;
   }
+  // staging -> operand images, 16 bytes at a time.  Eight consecutive lanes
+  // take eight rows and eight different 16-byte columns (a rotation), so both
+  // the row-major reads and the column-group writes are free of bank conflicts.
+  for (int idx = tid; idx < 2048; idx += INTRA_THREADS) {
+    const int which = idx >> 10, j = idx & 7, grp = (idx >> 3) & 127;
+    const int r = (grp & 7) * 8 + j, cgp = grp >> 3;
+    const int c8 = (cgp & 8) | ((j + cgp) & 7);
+    const uint4 x = *reinterpret_cast<const uint4 *>(STG + which * 16384 + (c8 >> 3) * 8192 +
+                                                     r * 128 + (c8 & 7) * 16);
+    *reinterpret_cast<uint4 *>(KQ + c8 * 2048 + (which * 64 + r) * 16) = x;
+  }
+  for (int idx = tid; idx < 8 * V; idx += INTRA_THREADS) {
+    const int j = idx & 7, grp = idx >> 3;
+    const int r = (grp & 7) * 8 + j, cg = grp >> 3;
+    const int c8 = (cg & ~3) | ((j + cg) & 3);
+    const uint4 x = *reinterpret_cast<const uint4 *>(STG + 32768 + (c8 >> 2) * 4096 + r * 64 +
+                                                     (c8 & 3) * 16);
+    *reinterpret_cast<uint4 *>(VS + c8 * 1024 + r * 16) = x;
+  }
+  ptx::fence_proxy_async_smem();  // the images feed the tensor cores
+  __syncthreads();
   if (KDA) {
     // thread c < 128 owns key channel c: running cumsum down the TMA-loaded
     // gate tile in place (rows >= L repeat row L - 1)
@@ -993,13 +1020,14 @@ bool make_gate_map(CUtensorMap *m, const float *base, int heads, long long rows)
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][heads][dim] bf16 tensor, boxes of 8 x 1 x 64 (16-byte rows).
-bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long rows) {
+// [rows][heads][dim] bf16 tensor, boxes of `width` x 1 x 64 (64 rows of
+// `width` contiguous elements each, row-major in shared memory).
+bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long rows, int width) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)heads * dim * 2};
-  cuuint32_t box[3] = {8, 1, 64};
+  cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1030,8 +1058,8 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const bool varlen = cp.cu_seqlens != nullptr;
   CUtensorMap mk, mq, mv, mg;
   const long long rows = (long long)cp.B * cp.T;
-  if (!make_map(&mk, cp.k, KD, cp.Hk, rows) || !make_map(&mq, cp.q, KD, cp.Hk, rows) ||
-      !make_map(&mv, cp.v, cp.V, cp.H, rows))
+  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, 64) || !make_map(&mq, cp.q, KD, cp.Hk, rows, 64) ||
+      !make_map(&mv, cp.v, cp.V, cp.H, rows, 32))
     return cudaErrorInvalidValue;
   if (kda) {
     if (!make_gate_map(&mg, cp.g, cp.H, rows)) return cudaErrorInvalidValue;
