@@ -1,4 +1,5 @@
-// Decode step (T = 1..4 tokens) against a pooled bf16 state, HBM-streaming.
+// Decode step against a pooled bf16 state, HBM-streaming: the kernel for
+// T = 1, 2 tokens (T = 3, 4 run on the warp-level tensor cores, decode_tc.cu).
 //
 // FlashInfer gdn_decode_bf16_state.py (compute_single_gate,
 // normalize_and_store_qk_to_smem, the per-token helpers and the public
@@ -543,12 +544,13 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
 
 }  // namespace
 
+// T <= 2 is HBM-bound on this kernel; at T = 3, 4 the packed-FMA work per
+// item outgrows the state stream and the tensor-core kernel is faster.
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
+  if (p.T >= 3) return launch_decode_tc(p, stream);
   switch (p.T) {
     case 1: return launch_t<1>(p, stream);
     case 2: return launch_t<2>(p, stream);
-    case 3: return launch_t<3>(p, stream);
-    case 4: return launch_t<4>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,552 @@
+// Decode step for T = 3, 4 tokens on the warp-level tensor cores (mma.sync
+// m16n8k16, bf16 in, fp32 accumulate): same arithmetic and item schedule as
+// decode.cu, with the state tile held as MMA accumulator fragments.  (The
+// kernel is written for any T <= 4; at T = 1, 2 decode.cu is HBM-bound and
+// faster, so it serves those.)
+//
+// FlashInfer gdn_decode_bf16_state.py (compute_single_gate,
+// normalize_and_store_qk_to_smem, the per-token helpers and gated_delta_rule)
+// defines the step; the T tokens of an item are taken in the chunk (WY) form
+// (G_t cumulative decay, R_ts = G_t / G_s):
+//   y_t = S0 k^_t,  z_t = S0 q^_t
+//   delta_t = beta_t v_t - beta_t G_t y_t - sum_{s<t} beta_t R_ts (k^_s.k^_t) delta_s
+//   o_t = G_t z_t + sum_{s<=t} R_ts (k^_s.q^_t) delta_s
+//   S_T = G_{T-1} S0 + sum_s R_{T-1,s} delta_s k^_s^T
+//
+// Warp w owns rows 16 w .. 16 w + 15 of the [V, K] state of the item.  The
+// state slot arrives by TMA in the 128-byte-swizzled layout; ldmatrix gives
+// each warp its rows as bf16 A fragments, which are exactly the fp32
+// accumulator fragments of the update once converted (lossless: the state is
+// bf16).  The 2T dot products are one M16 x N(8 or 16) x K128 product with
+// B = [k^_0 hi, k^_0 lo, k^_1 hi, ...] (bf16 pairs, so the vectors keep
+// fp32-grade accuracy); the update is one K = 16 product per 8 columns with
+// A = [c delta hi | c delta lo | c delta hi] and B = [k^ hi; k^ hi; k^ lo].
+// The updated rows go back through stmatrix into the stage and one TMA store
+// per warp.  Per item the first warp to finish the previous item prepares the
+// stage (normalised q/k as the bf16 operand images, gates, coefficients); the
+// last warp out refills it; no block-wide barrier in the item loop.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "ptx.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int DK = 128, DV = 128;
+constexpr int NWARPS = 8, NTHREADS = NWARPS * 32;
+constexpr int NSTAGE = 2;     // two CTAs per SM: two 46 KB stages each
+constexpr int PREP_AHEAD = 1;  // the first warp out of item i prepares item i + 1
+constexpr uint32_t SLOT_BYTES = DK * DV * 2;  // 32 KB bf16 state slot
+constexpr uint32_t ROW_BYTES = DK * 2;        // one bf16 q/k/v row
+constexpr uint32_t BD_PITCH = 272, BU_PITCH = 48;
+
+// stage layout (bytes; stages 1024-aligned for the 128-byte swizzle)
+//   SW   [0, 32768)       state slot, two 64-column halves, each 128 rows x 128 B
+//   BD   [32768, 37120)   dot operand: 16 rows (k^_t hi/lo, then q^_t hi/lo) x 128
+//   BU   [37120, 43264)   update operand: 128 rows (state columns) x 16 (pitch 48 B)
+//   RAW  [43264, 46336)   q, k, v rows as copied (T <= 4)
+//   HDR  [46336, 46592)   slot index and coefficients
+constexpr uint32_t O_SW = 0, O_BD = 32768, O_BU = 37120, O_RAW = 43264, O_HDR = 46336;
+constexpr uint32_t STAGE_BYTES = 47104;
+constexpr size_t SMEM_BYTES = (size_t)NSTAGE * STAGE_BYTES + NSTAGE * 16 + NSTAGE * 4 + 1024;
+
+// header words
+constexpr int H_SLOT = 0, H_GT = 1, H_BG = 4, H_BE = 8, H_GAM = 12, H_C = 16, H_A = 20, H_B = 36;
+
+__device__ __forceinline__ float softplus_f(float x, float beta, float thr) {
+  const float bx = beta * x;
+  return bx <= thr ? log1pf(expf(bx)) / beta : x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+}
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Address of the 16-byte row piece lane `lane` supplies to ldmatrix/stmatrix
+// for the 16 x 16 block (rows r0 .. r0 + 15, columns 16 j .. 16 j + 15) of a
+// swizzled state tile.
+__device__ __forceinline__ unsigned char *sw_addr(unsigned char *sw, int r0, int j, int lane) {
+  const int r = r0 + (lane & 15);
+  const int c = (j & 3) * 2 + (lane >> 4);  // 16-byte chunk within the 128-byte row
+  return sw + (j >> 2) * 16384 + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ int slot_of(const DecodeParams &p, int item) {
+  const int bi = item / p.HV;
+  return p.slot_indices ? p.slot_indices[bi] : bi;
+}
+
+template <int T>
+__device__ __forceinline__ void issue(const DecodeParams &p, const CUtensorMap *tm_ld,
+                                      unsigned char *st, uint64_t *full, int item, int slot) {
+  const int HV = p.HV;
+  const int bi = item / HV, hv = item % HV, hk = hv / (HV / p.H);
+  int *hdr = reinterpret_cast<int *>(st + O_HDR);
+  if (slot < 0 || slot >= p.pool) {
+    hdr[H_SLOT] = -1;
+    ptx::mbar_arrive(full);
+    return;
+  }
+  hdr[H_SLOT] = slot;
+  ptx::fence_proxy_async_smem();
+  ptx::mbar_arrive_expect_tx(full, SLOT_BYTES + 3 * T * ROW_BYTES);
+  const int row0 = (slot * HV + hv) * DV;
+  ptx::tma_load_2d(st + O_SW, tm_ld, 0, row0, full);
+  ptx::tma_load_2d(st + O_SW + 16384, tm_ld, 64, row0, full);
+  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const size_t qk_off = (((size_t)bi * T + t) * p.H + hk) * DK;
+    const size_t v_off = (((size_t)bi * T + t) * HV + hv) * DV;
+    ptx::bulk_g2s(st + O_RAW + t * ROW_BYTES, k + qk_off, ROW_BYTES, full);
+    ptx::bulk_g2s(st + O_RAW + (T + t) * ROW_BYTES, q + qk_off, ROW_BYTES, full);
+    ptx::bulk_g2s(st + O_RAW + (2 * T + t) * ROW_BYTES, v + v_off, ROW_BYTES, full);
+  }
+}
+
+struct GateIn {
+  float a, b, A_log, dt_bias;
+};
+
+__device__ __forceinline__ GateIn load_gate_in(const DecodeParams &p, int item, int lane, int T) {
+  GateIn g{0.f, 0.f, 0.f, 0.f};
+  if (lane < T) {
+    const int bi = item / p.HV, hv = item % p.HV;
+    const size_t gi = ((size_t)bi * T + lane) * p.HV + hv;
+    g.a = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.a)[gi]);
+    g.b = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.b)[gi]);
+    g.A_log = p.A_log[hv];
+    g.dt_bias = p.dt_bias[hv];
+  }
+  return g;
+}
+
+// Prepare a landed stage (one warp): operand images of the normalised q/k,
+// gates and coefficients; every lane then arrives on `prep`.  Lane l handles
+// columns 4 l .. 4 l + 3 of every vector.
+template <int T>
+__device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, uint64_t *full,
+                                     uint64_t *prep, uint32_t parity, GateIn gin, int lane) {
+  if (!ptx::mbar_wait_bounded(full, parity)) record_error(p.err, GDN_ERR_TIMEOUT);
+  float *hdr = reinterpret_cast<float *>(st + O_HDR);
+  if (*reinterpret_cast<const int *>(hdr) >= 0) {
+    float x[2 * T][4];
+#pragma unroll
+    for (int n = 0; n < 2 * T; ++n) {
+      const uint2 raw = *reinterpret_cast<const uint2 *>(st + O_RAW + n * ROW_BYTES + lane * 8);
+      const float2 a = unpack2(raw.x), b = unpack2(raw.y);
+      x[n][0] = a.x; x[n][1] = a.y; x[n][2] = b.x; x[n][3] = b.y;
+    }
+#pragma unroll
+    for (int n = 0; n < 2 * T; ++n) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = fmaf(x[n][e], x[n][e], ss);
+      ss = warp_sum(ss);
+      float f = p.use_qk_l2norm ? rsqrtf(ss + p.eps) : 1.f;
+      if (n >= T) f *= p.scale;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[n][e] *= f;
+    }
+    float gk[T][T], gq[T][T];
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int s = 0; s < T; ++s) {
+        float dk = 0.f, dq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dk = fmaf(x[s][e], x[t][e], dk);
+          dq = fmaf(x[s][e], x[T + t][e], dq);
+        }
+        gk[t][s] = s < t ? warp_sum(dk) : 0.f;
+        gq[t][s] = s <= t ? warp_sum(dq) : 0.f;
+      }
+    // BD: row 2 n = hi, row 2 n + 1 = lo of vector n (k^_0.., then q^_0..)
+    unsigned char *bd = st + O_BD;
+    float hi[2 * T][4], lo[2 * T][4];
+#pragma unroll
+    for (int n = 0; n < 2 * T; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[n][e] = bf16_round(x[n][e]);
+        lo[n][e] = x[n][e] - hi[n][e];
+      }
+      *reinterpret_cast<uint2 *>(bd + (2 * n) * BD_PITCH + lane * 8) =
+          make_uint2(pack2(hi[n][0], hi[n][1]), pack2(hi[n][2], hi[n][3]));
+      *reinterpret_cast<uint2 *>(bd + (2 * n + 1) * BD_PITCH + lane * 8) =
+          make_uint2(pack2(lo[n][0], lo[n][1]), pack2(lo[n][2], lo[n][3]));
+    }
+    // BU: row = state column c, k index t: k^_t hi, T + t: k^_t hi, 2T + t: k^_t lo
+    unsigned char *bu = st + O_BU;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float row[16];
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) row[kk] = 0.f;
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        row[t] = hi[t][e];
+        row[T + t] = hi[t][e];
+        row[2 * T + t] = lo[t][e];
+      }
+      uint4 w0, w1;
+      w0.x = pack2(row[0], row[1]); w0.y = pack2(row[2], row[3]);
+      w0.z = pack2(row[4], row[5]); w0.w = pack2(row[6], row[7]);
+      w1.x = pack2(row[8], row[9]); w1.y = pack2(row[10], row[11]);
+      w1.z = pack2(row[12], row[13]); w1.w = pack2(row[14], row[15]);
+      *reinterpret_cast<uint4 *>(bu + (4 * lane + e) * BU_PITCH) = w0;
+      *reinterpret_cast<uint4 *>(bu + (4 * lane + e) * BU_PITCH + 16) = w1;
+    }
+    // gates (lane t for token t), then the coefficients (uniform over lanes)
+    float gl = 1.f, bl = 0.f;
+    if (lane < T) {
+      gl = expf(-expf(gin.A_log) *
+                softplus_f(gin.a + gin.dt_bias, p.softplus_beta, p.softplus_threshold));
+      bl = 1.f / (1.f + expf(-gin.b));
+    }
+    float gam[T], be[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      gam[t] = __shfl_sync(0xffffffffu, gl, t);
+      be[t] = __shfl_sync(0xffffffffu, bl, t);
+    }
+    float G[T], R[T][T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      G[t] = t == 0 ? gam[0] : G[t - 1] * gam[t];
+      R[t][t] = 1.f;
+#pragma unroll
+      for (int s = t - 1; s >= 0; --s) R[t][s] = R[t][s + 1] * gam[s + 1];
+    }
+    if (lane == 0) {
+      hdr[H_GT] = G[T - 1];
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        hdr[H_BG + t] = be[t] * G[t];
+        hdr[H_BE + t] = be[t];
+        hdr[H_GAM + t] = G[t];
+        hdr[H_C + t] = R[T - 1][t];
+#pragma unroll
+        for (int s = 0; s < T; ++s) {
+          hdr[H_A + 4 * t + s] = s < t ? be[t] * R[t][s] * gk[t][s] : 0.f;
+          hdr[H_B + 4 * t + s] = s <= t ? R[t][s] * gq[t][s] : 0.f;
+        }
+      }
+    }
+  }
+  ptx::mbar_arrive(prep);  // each lane releases its own writes
+}
+
+template <int T>
+__global__ void __launch_bounds__(NTHREADS, 2)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constant__ CUtensorMap tm_st,
+                 DecodeParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  // stages on a 1024-byte boundary (the 128-byte swizzle repeats every 1 KB)
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * STAGE_BYTES);
+  uint64_t *prep = full + NSTAGE;
+  int *done = reinterpret_cast<int *>(prep + NSTAGE);
+  constexpr int NT_DOT = (2 * T + 3) / 4;  // 8-column tiles of the dot product
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tig = lane & 3;
+  const int HV = p.HV, nitems = p.B * HV, stride = gridDim.x;
+  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&prep[s], 32);
+      done[s] = 0;
+    }
+    ptx::fence_mbar_init();
+  }
+  // BD rows past the 2T vectors stay zero
+  for (int s = 0; s < NSTAGE; ++s)
+    for (int i = tid; i < (16 - 4 * T) * (int)BD_PITCH / 16; i += NTHREADS)
+      reinterpret_cast<uint4 *>(smem + s * STAGE_BYTES + O_BD + 4 * T * BD_PITCH)[i] =
+          make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid == 0) {
+    ptx::prefetch_tmap(&tm_ld);
+    ptx::prefetch_tmap(&tm_st);
+    for (int s = 0; s < NSTAGE; ++s) {
+      const int item = blockIdx.x + s * stride;
+      if (item < nitems) issue<T>(p, &tm_ld, smem + s * STAGE_BYTES, &full[s], item, slot_of(p, item));
+    }
+  }
+  if (warp < PREP_AHEAD) {
+    const int item = blockIdx.x + warp * stride;
+    if (item < nitems)
+      prepare<T>(p, smem + warp * STAGE_BYTES, &full[warp], &prep[warp], 0u,
+                 load_gate_in(p, item, lane, T), lane);
+  }
+
+#pragma unroll 1
+  for (int it = 0;; ++it) {
+    const int item = blockIdx.x + it * stride;
+    if (item >= nitems) break;
+    const int s = it % NSTAGE;
+    const uint32_t parity = (uint32_t)((it / NSTAGE) & 1);
+    const int bi = item / HV, hv = item % HV;
+    const int refill = item + NSTAGE * stride;
+    const int ahead = item + PREP_AHEAD * stride;
+    unsigned char *st = smem + s * STAGE_BYTES;
+    unsigned char *sw = st + O_SW;
+    const float *hdr = reinterpret_cast<const float *>(st + O_HDR);
+
+    if (!ptx::mbar_wait_bounded(&full[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
+    const int slot = *reinterpret_cast<const int *>(hdr);
+    const int r0 = 16 * warp;  // this warp's first state row
+
+    if (slot >= 0) {
+      if (!ptx::mbar_wait_bounded(&prep[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
+      // ---- S0 rows as A fragments; the same values seed the fp32 accumulators
+      float C[16][4];
+      float D[NT_DOT][4];
+#pragma unroll
+      for (int n = 0; n < NT_DOT; ++n) D[n][0] = D[n][1] = D[n][2] = D[n][3] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t a[4];
+        ptx::ldmatrix_x4(sw_addr(sw, r0, j, lane), a[0], a[1], a[2], a[3]);
+        const float2 c00 = unpack2(a[0]), c01 = unpack2(a[1]), c10 = unpack2(a[2]),
+                     c11 = unpack2(a[3]);
+        C[2 * j][0] = c00.x; C[2 * j][1] = c00.y; C[2 * j][2] = c01.x; C[2 * j][3] = c01.y;
+        C[2 * j + 1][0] = c10.x; C[2 * j + 1][1] = c10.y;
+        C[2 * j + 1][2] = c11.x; C[2 * j + 1][3] = c11.y;
+        // dot products: B rows n (vectors' hi/lo), k = 16 j .. 16 j + 15
+        uint32_t b[4];
+        const int n = (lane & 7) + ((lane >> 4) << 3);
+        ptx::ldmatrix_x4(st + O_BD + n * BD_PITCH + (16 * j + 8 * ((lane >> 3) & 1)) * 2, b[0],
+                         b[1], b[2], b[3]);
+        ptx::mma_16816_bf16(D[0], a, b[0], b[1]);
+        if (NT_DOT > 1) ptx::mma_16816_bf16(D[NT_DOT - 1], a, b[2], b[3]);
+      }
+      // vector 4 nt + tig on this lane: rows g (hi + lo) and g + 8
+      float vg[NT_DOT], vg8[NT_DOT];
+#pragma unroll
+      for (int n = 0; n < NT_DOT; ++n) {
+        vg[n] = D[n][0] + D[n][1];
+        vg8[n] = D[n][2] + D[n][3];
+      }
+      // all 2T values of rows g and g + 8 on every lane of the quad
+      float y[2][T], z[2][T];
+#pragma unroll
+      for (int jv = 0; jv < 2 * T; ++jv) {
+        const int src = (lane & ~3) | (jv & 3);
+        const float a0 = __shfl_sync(0xffffffffu, vg[jv >> 2], src);
+        const float a1 = __shfl_sync(0xffffffffu, vg8[jv >> 2], src);
+        if (jv < T) {
+          y[0][jv] = a0;
+          y[1][jv] = a1;
+        } else {
+          z[0][jv - T] = a0;
+          z[1][jv - T] = a1;
+        }
+      }
+      // ---- deltas and outputs of rows r0 + g and r0 + g + 8
+      const __nv_bfloat16 *vraw = reinterpret_cast<const __nv_bfloat16 *>(st + O_RAW + 2 * T * ROW_BYTES);
+      float dl[2][T];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = r0 + g + 8 * h;
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float vv = __bfloat162float(vraw[t * DV + row]);
+          float d = fmaf(hdr[H_BE + t], vv, -hdr[H_BG + t] * y[h][t]);
+#pragma unroll
+          for (int s2 = 0; s2 < t; ++s2) d = fmaf(-hdr[H_A + 4 * t + s2], dl[h][s2], d);
+          dl[h][t] = d;
+        }
+        if (tig < T) {
+          // lane tig writes token tig
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            if (t != tig) continue;
+            float ov = hdr[H_GAM + t] * z[h][t];
+#pragma unroll
+            for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[h][s2], ov);
+            o[(((size_t)bi * T + t) * HV + hv) * DV + row] = __float2bfloat16_rn(ov);
+          }
+        }
+      }
+      // ---- update: C = G_{T-1} C + A B with A = [c d hi | c d lo | c d hi]
+      const float gt = hdr[H_GT];
+#pragma unroll
+      for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) C[n][e] *= gt;
+      uint32_t ua[4];
+      {
+        float dh[2][T], dlo[2][T];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            const float d = hdr[H_C + t] * dl[h][t];
+            dh[h][t] = bf16_round(d);
+            dlo[h][t] = d - dh[h][t];
+          }
+        auto kval = [&](int h, int kk) {
+          float r = 0.f;
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            if (kk == t) r = dh[h][t];
+            if (kk == T + t) r = dlo[h][t];
+            if (kk == 2 * T + t) r = dh[h][t];
+          }
+          return r;
+        };
+        ua[0] = pack2(kval(0, 2 * tig), kval(0, 2 * tig + 1));
+        ua[1] = pack2(kval(1, 2 * tig), kval(1, 2 * tig + 1));
+        ua[2] = pack2(kval(0, 2 * tig + 8), kval(0, 2 * tig + 9));
+        ua[3] = pack2(kval(1, 2 * tig + 8), kval(1, 2 * tig + 9));
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t b[4];
+        const int n = 16 * j + (lane & 7) + ((lane >> 4) << 3);
+        ptx::ldmatrix_x4(st + O_BU + n * BU_PITCH + ((lane >> 3) & 1) * 16, b[0], b[1], b[2], b[3]);
+        ptx::mma_16816_bf16(C[2 * j], ua, b[0], b[1]);
+        ptx::mma_16816_bf16(C[2 * j + 1], ua, b[2], b[3]);
+      }
+      // ---- write back: bf16 fragments -> this warp's rows of the stage -> TMA store
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        ptx::stmatrix_x4(sw_addr(sw, r0, j, lane), pack2(C[2 * j][0], C[2 * j][1]),
+                         pack2(C[2 * j][2], C[2 * j][3]), pack2(C[2 * j + 1][0], C[2 * j + 1][1]),
+                         pack2(C[2 * j + 1][2], C[2 * j + 1][3]));
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int grow = (slot * HV + hv) * DV + r0;
+        ptx::tma_store_2d(&tm_st, 0, grow, sw + r0 * 128);
+        ptx::tma_store_2d(&tm_st, 64, grow, sw + 16384 + r0 * 128);
+        ptx::bulk_commit();
+        ptx::bulk_wait_read<0>();  // the stage may be refilled only after this
+      }
+    }
+
+    // This warp is done with stage s: the last warp out refills it, the first
+    // prepares the next item.
+    __syncwarp();
+    int order = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      order = atomicAdd(&done[s], 1);
+      if (order == NWARPS - 1) {
+        done[s] = 0;
+        __threadfence_block();
+        if (refill < nitems) issue<T>(p, &tm_ld, st, &full[s], refill, slot_of(p, refill));
+      }
+    }
+    order = __shfl_sync(0xffffffffu, order, 0);
+    if (slot < 0) {
+      if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
+      for (int idx = tid; idx < T * DV; idx += NTHREADS)
+        o[(((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV] = __float2bfloat16_rn(0.f);
+    }
+    if (order == 0 && ahead < nitems) {
+      const int sa = (it + PREP_AHEAD) % NSTAGE;
+      prepare<T>(p, smem + sa * STAGE_BYTES, &full[sa], &prep[sa],
+                 (uint32_t)(((it + PREP_AHEAD) / NSTAGE) & 1), load_gate_in(p, ahead, lane, T), lane);
+    }
+  }
+  // the last stores must have left shared memory before the block exits
+  if (lane == 0) ptx::bulk_wait<0>();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// The pool as a 2-D bf16 tensor [pool * HV * V rows][K], boxes of 64 columns x
+// `rows` rows, 128-byte swizzle.
+bool make_state_map(CUtensorMap *m, void *base, long long rows, int box_rows) {
+  auto fn = encoder();
+  if (!fn) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)DK, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)DK * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int T>
+cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
+  CUtensorMap ld, stm;
+  const long long rows = (long long)p.pool * p.HV * DV;
+  if (!make_state_map(&ld, p.state, rows, 128) || !make_state_map(&stm, p.state, rows, 16))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel<T>, NTHREADS,
+                                                    SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int items = p.B * p.HV;
+  const int cap = per_sm * sm_count();
+  const int grid = items < cap ? items : cap;
+  decode_tc_kernel<T><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ld, stm, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
+  switch (p.T) {
+    case 3: return launch_t<3>(p, stream);
+    case 4: return launch_t<4>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

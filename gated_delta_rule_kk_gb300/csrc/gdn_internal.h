@@ -39,6 +39,8 @@ struct DecodeParams {
 cudaError_t launch_chunk_simt(const ChunkParams &p, bool bf16, bool per_channel_gate,
                               cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
+// The decode step on the warp-level tensor cores (K = V = 128).
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 
 // Tensor-core chunked forward (bf16, K = 128, V % 32 == 0): whether it serves
 // these arguments, the workspace it needs, and the launch.

@@ -112,6 +112,27 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
+// 2-D tiled load of one box into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, int c0, int c1,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 2-D tiled store of one box from shared memory (bulk async-group; wait with
+// bulk_wait_read / bulk_wait after bulk_commit).  Coordinates must be >= 0.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int c0, int c1,
+                                             const void *smem_src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          tmap),
+      "r"(c0), "r"(c1), "r"(smem_u32(smem_src))
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -215,6 +236,38 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+
+// ---- warp-level matrix fragments (ldmatrix / stmatrix / mma.sync) --------
+
+// Four 8x8 b16 matrices; lane i supplies the address of row i % 8 of matrix
+// i / 8, and register j of every lane receives its share of matrix j.
+__device__ __forceinline__ void ldmatrix_x4(const void *row_addr, uint32_t &r0, uint32_t &r1,
+                                            uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(row_addr))
+               : "memory");
+}
+
+__device__ __forceinline__ void stmatrix_x4(void *row_addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                   smem_u32(row_addr)),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// D (16x8, fp32) += A (16x16, bf16, row-major fragment) * B (16x8, bf16,
+// column-major fragment).
+__device__ __forceinline__ void mma_16816_bf16(float *d, const uint32_t *a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 }  // namespace ptx
