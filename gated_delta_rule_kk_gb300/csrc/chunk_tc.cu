@@ -271,20 +271,22 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
 //   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys), cs 2048;
 //                          at the end [-w ; q], the chain's A operand
 //   VS   [32768, 49152)    v (64 tokens x V), cs 1024
+//                          (KDA: first k e^-g, the B operand of S; v is loaded
+//                          once S is done)
 //   R1   [49152, 83968)    KDA gamma (fp32 64 x 128); then A | T (fp32, 64 x 68
 //                          each); after the solve Tw hi | Tw lo (64 x 64, cs
 //                          1024) over A
 //   AQ   [83968, 100352)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
 //                          Tu hi | Tu lo
-//   KB   [100352, 116736)  KDA: k e^-g (64 x 128, cs 1024)
-//   KT   [116736, 133120)  KDA: k e^{gamma_L - g} (64 x 128, cs 1024)
 //   small                  scales, gamma, factors, merge scratch, barriers
-constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 83968, I_KB = 100352,
-                   I_KT = 116736;
+// GDN stages the row-major k | q | v tiles in R1 + AQ before the gating; KDA
+// loads k and q straight into KQ (its gate tile takes R1).  Both fit two CTAs
+// per SM.
+constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 83968, I_SMALL = 100352;
 constexpr int INTRA_THREADS = 256;
 template <bool KDA>
 struct IntraLayout {
-  static constexpr uint32_t SMALL = KDA ? I_KT + 16384 : I_KB;
+  static constexpr uint32_t SMALL = I_SMALL;
   static constexpr uint32_t SMEM = SMALL + 8192;
 };
 
@@ -300,11 +302,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   float *Tsm = Asm + 64 * SLD;
   unsigned char *TW = smem + I_R1;   // Tw hi, Tw lo (after the solve)
   unsigned char *AQ = smem + I_AQ;   // Aqk pair, later Tu hi, Tu lo
-  unsigned char *KB = smem + I_KB;
-  unsigned char *KTs = smem + I_KT;
-  // staging for the row-major k | q | v tiles (48 KB): regions first written
-  // by the gating (GDN: R1 + AQ; KDA, whose gate tile takes R1: AQ + KB + KT)
-  unsigned char *STG = smem + (KDA ? I_AQ : I_R1);
+  unsigned char *KB = VS;  // KDA: k e^-g, until the S GEMM is done
+  // GDN staging for the row-major k | q | v tiles (48 KB): R1 + AQ, first
+  // written by the gating
+  unsigned char *STG = smem + I_R1;
   float *sc = reinterpret_cast<float *>(smem + IntraLayout<KDA>::SMALL);  // decay, rs, qs
   float *gam = sc + 256;                                   // [64]
   float *bet = gam + 64;                                   // [64]
@@ -343,7 +344,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::mbar_init(&bars[0], 1);
     ptx::mbar_init(&bars[1], 1);
     ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(&bars[0], 32768 + (uint32_t)V * 128 + (KDA ? 32768u : 0u));
+    // KDA: k, q and the gate tile now, v after the S GEMM (second phase)
+    ptx::mbar_arrive_expect_tx(&bars[0], KDA ? 65536u : 32768u + (uint32_t)V * 128);
     flags[0] = 1;
   }
   // three issuing threads, one per tensor, once warp 0 has set the barrier up
@@ -351,7 +353,20 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   // k, q and v arrive row-major (128-byte, resp. 64-byte rows: few large
   // requests) in a staging area that is free until the gating, and are
   // rearranged into the operand images once they land
-  if (lane == 0 && warp < 3) {
+  if (KDA && lane == 0 && warp < 3) {
+    // canonical operand-image boxes (16-byte rows) straight into KQ
+    if (warp == 0) {
+#pragma unroll 1
+      for (int j = 0; j < 16; ++j) ptx::tma_load_3d(KQ + j * 2048, &tm_k, 8 * j, hk, row0, &bars[0]);
+    } else if (warp == 1) {
+#pragma unroll 1
+      for (int j = 0; j < 16; ++j)
+        ptx::tma_load_3d(KQ + j * 2048 + 1024, &tm_q, 8 * j, hk, row0, &bars[0]);
+    } else {
+      // the fp32 gate tile (64 tokens x 128 channels, row-major) into R1
+      ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
+    }
+  } else if (!KDA && lane == 0 && warp < 3) {
     if (warp == 0) {
       ptx::tma_load_3d(STG, &tm_k, 0, hk, row0, &bars[0]);
       ptx::tma_load_3d(STG + 8192, &tm_k, 64, hk, row0, &bars[0]);
@@ -362,8 +377,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 #pragma unroll 1
       for (int j = 0; j < V / 32; ++j)
         ptx::tma_load_3d(STG + 32768 + j * 4096, &tm_v, 32 * j, h, row0, &bars[0]);
-      // KDA: the fp32 gate tile (64 tokens x 128 channels, row-major) into R1
-      if (KDA) ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
     }
   }
   if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
@@ -430,7 +443,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   // staging -> operand images, 16 bytes at a time.  Eight consecutive lanes
   // take eight rows and eight different 16-byte columns (a rotation), so both
   // the row-major reads and the column-group writes are free of bank conflicts.
-  for (int idx = tid; idx < 2048; idx += INTRA_THREADS) {
+  for (int idx = tid; idx < (KDA ? 0 : 2048); idx += INTRA_THREADS) {
     const int which = idx >> 10, j = idx & 7, grp = (idx >> 3) & 127;
     const int r = (grp & 7) * 8 + j, cgp = grp >> 3;
     const int c8 = (cgp & 8) | ((j + cgp) & 7);
@@ -438,7 +451,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
                                                      r * 128 + (c8 & 7) * 16);
     *reinterpret_cast<uint4 *>(KQ + c8 * 2048 + (which * 64 + r) * 16) = x;
   }
-  for (int idx = tid; idx < 8 * V; idx += INTRA_THREADS) {
+  for (int idx = tid; idx < (KDA ? 0 : 8 * V); idx += INTRA_THREADS) {
     const int j = idx & 7, grp = idx >> 3;
     const int r = (grp & 7) * 8 + j, cg = grp >> 3;
     const int c8 = (cg & ~3) | ((j + cg) & 3);
@@ -474,7 +487,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 
   if (KDA) {
     // KQ <- [k e^g ; q e^g] (bounded by |k|, |q| for gates <= 0),
-    // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g}
+    // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g} (to the block)
     const float *G = Asm;
     for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
       const int i = pc & 63, cg = pc >> 6;
@@ -498,7 +511,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       *kp = pack8(a);
       *qp = pack8(b);
       *reinterpret_cast<uint4 *>(KB + img_off(i, 8 * cg, 1024)) = pack8(c);
-      *reinterpret_cast<uint4 *>(KTs + img_off(i, 8 * cg, 1024)) = pack8(t);
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 1024)) = pack8(t);
     }
     ptx::fence_proxy_async_smem();
     __syncthreads();
@@ -537,6 +550,11 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   const bool ok1 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
   mma_phase ^= 1;
   ptx::tc_fence_after();
+  if (KDA && tid == 0) {
+    // S is done with KB: v into VS, counted on the second phase of bars[0]
+    ptx::mbar_arrive_expect_tx(&bars[0], (uint32_t)V * 128);
+    for (int j = 0; j < V / 8; ++j) ptx::tma_load_3d(VS + j * 1024, &tm_v, 8 * j, h, row0, &bars[0]);
+  }
 
   // ---- gating: thread (qd, hf, lane) holds row r = 32 qd + lane of S,
   //      columns 32 hf .. 32 hf + 31 (r < 64: kk, r >= 64: qk)
@@ -607,7 +625,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   __syncthreads();
   if (tid == 0) {
     ptx::bulk_s2g(blk + OFF_AQ, AQ, 16384);
-    if (KDA) ptx::bulk_s2g(blk + OFF_KT, KTs, 16384);
     ptx::bulk_commit();
   }
 
@@ -649,7 +666,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   // ---- w = Tw k (N = 128 keys) and u = Tu v (N = V), M = 64, K = 64 tokens,
   //      each as hi + lo passes accumulating in TMEM
   const uint32_t dW = tmem, dU = tmem + 128;
+  bool ok_v = true;
   if (tid == 0) {
+    if (KDA) ok_v = ptx::mbar_wait_bounded(&bars[0], 1);  // v has landed
     ptx::tc_fence_after();
     const uint32_t idw = ptx::idesc_bf16(64, 128, 0, 1);
     const uint32_t idu = ptx::idesc_bf16(64, V, 0, 1);
@@ -712,7 +731,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::bulk_commit();
     ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   }
-  if (!(ok1 && ok2) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+  if (!(ok1 && ok2 && ok_v) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
   __syncthreads();
   if (warp == 0) ptx::tmem_dealloc<256>(tmem);
 }
@@ -1058,8 +1077,10 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const bool varlen = cp.cu_seqlens != nullptr;
   CUtensorMap mk, mq, mv, mg;
   const long long rows = (long long)cp.B * cp.T;
-  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, 64) || !make_map(&mq, cp.q, KD, cp.Hk, rows, 64) ||
-      !make_map(&mv, cp.v, cp.V, cp.H, rows, 32))
+  // GDN: row-major tiles into staging; KDA: canonical 16-byte-row boxes
+  const int wkq = kda ? 8 : 64, wv = kda ? 8 : 32;
+  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, wkq) || !make_map(&mq, cp.q, KD, cp.Hk, rows, wkq) ||
+      !make_map(&mv, cp.v, cp.V, cp.H, rows, wv))
     return cudaErrorInvalidValue;
   if (kda) {
     if (!make_gate_map(&mg, cp.g, cp.H, rows)) return cudaErrorInvalidValue;
