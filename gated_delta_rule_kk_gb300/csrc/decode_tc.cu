@@ -21,10 +21,10 @@
 // B = [k^_0 hi, k^_0 lo, k^_1 hi, ...] (bf16 pairs, so the vectors keep
 // fp32-grade accuracy); the update is one K = 16 product per 8 columns with
 // A = [c delta hi | c delta lo | c delta hi] and B = [k^ hi; k^ hi; k^ lo].
-// The updated rows go back through stmatrix into the stage and one TMA store
-// per warp.  Per item the first warp to finish the previous item prepares the
-// stage (normalised q/k as the bf16 operand images, gates, coefficients); the
-// last warp out refills it; no block-wide barrier in the item loop.
+// The updated rows go back through stmatrix into the slot and one TMA store
+// per warp.  Per item the first warp to finish item i - 2 prepares it
+// (normalised q/k as the bf16 operand images, gates, coefficients); the last
+// warp out of a ring entry refills it; no block-wide barrier in the item loop.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,21 +37,22 @@ namespace {
 
 constexpr int DK = 128, DV = 128;
 constexpr int NWARPS = 8, NTHREADS = NWARPS * 32;
-constexpr int NSTAGE = 2;     // two CTAs per SM: two 46 KB stages each
-constexpr int PREP_AHEAD = 1;  // the first warp out of item i prepares item i + 1
+// Two rings per CTA (two CTAs per SM): the 32 KB state slots (NSW deep,
+// each slot two 64-column halves of 128 rows x 128 B, swizzled, 1024-aligned)
+// and small per-item entries (NAUX deep) holding
+//   RAW  [0, 3072)       q, k, v rows as copied (T <= 4)
+//   BD   [3072, 7424)    dot operand: 16 rows (k^_t hi/lo, then q^_t hi/lo) x 128
+//   BU   [7424, 13568)   update operand: 128 rows (state columns) x 16 (pitch 48 B)
+//   HDR  [13568, 13824)  slot index and coefficients
+// The per-item ring is deeper, so an item is prepared two items ahead of its
+// use, off the critical path.
+constexpr int NSW = 2, NAUX = 3, PREP_AHEAD = 2;
 constexpr uint32_t SLOT_BYTES = DK * DV * 2;  // 32 KB bf16 state slot
 constexpr uint32_t ROW_BYTES = DK * 2;        // one bf16 q/k/v row
 constexpr uint32_t BD_PITCH = 272, BU_PITCH = 48;
-
-// stage layout (bytes; stages 1024-aligned for the 128-byte swizzle)
-//   SW   [0, 32768)       state slot, two 64-column halves, each 128 rows x 128 B
-//   BD   [32768, 37120)   dot operand: 16 rows (k^_t hi/lo, then q^_t hi/lo) x 128
-//   BU   [37120, 43264)   update operand: 128 rows (state columns) x 16 (pitch 48 B)
-//   RAW  [43264, 46336)   q, k, v rows as copied (T <= 4)
-//   HDR  [46336, 46592)   slot index and coefficients
-constexpr uint32_t O_SW = 0, O_BD = 32768, O_BU = 37120, O_RAW = 43264, O_HDR = 46336;
-constexpr uint32_t STAGE_BYTES = 47104;
-constexpr size_t SMEM_BYTES = (size_t)NSTAGE * STAGE_BYTES + NSTAGE * 16 + NSTAGE * 4 + 1024;
+constexpr uint32_t A_RAW = 0, A_BD = 3072, A_BU = 7424, A_HDR = 13568, AUX_BYTES = 13824;
+constexpr uint32_t O_AUX = NSW * SLOT_BYTES, O_BARS = O_AUX + NAUX * AUX_BYTES;
+constexpr size_t SMEM_BYTES = O_BARS + (NSW + 2 * NAUX) * 8 + (NSW + NAUX) * 4 + 1024;
 
 // header words
 constexpr int H_SLOT = 0, H_GT = 1, H_BG = 4, H_BE = 8, H_GAM = 12, H_C = 16, H_A = 20, H_B = 36;
@@ -92,12 +93,28 @@ __device__ __forceinline__ int slot_of(const DecodeParams &p, int item) {
   return p.slot_indices ? p.slot_indices[bi] : bi;
 }
 
+// Fill a state-slot stage (one thread); an out-of-range slot completes the
+// barrier with no copies.
+__device__ __forceinline__ void issue_sw(const DecodeParams &p, const CUtensorMap *tm_ld,
+                                         unsigned char *sw, uint64_t *full, int item, int slot) {
+  if (slot < 0 || slot >= p.pool) {
+    ptx::mbar_arrive(full);
+    return;
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::mbar_arrive_expect_tx(full, SLOT_BYTES);
+  const int row0 = (slot * p.HV + item % p.HV) * DV;
+  ptx::tma_load_2d(sw, tm_ld, 0, row0, full);
+  ptx::tma_load_2d(sw + 16384, tm_ld, 64, row0, full);
+}
+
+// Fill a per-item entry with the item's q, k, v rows and its slot index.
 template <int T>
-__device__ __forceinline__ void issue(const DecodeParams &p, const CUtensorMap *tm_ld,
-                                      unsigned char *st, uint64_t *full, int item, int slot) {
+__device__ __forceinline__ void issue_aux(const DecodeParams &p, unsigned char *aux,
+                                          uint64_t *full, int item, int slot) {
   const int HV = p.HV;
   const int bi = item / HV, hv = item % HV, hk = hv / (HV / p.H);
-  int *hdr = reinterpret_cast<int *>(st + O_HDR);
+  int *hdr = reinterpret_cast<int *>(aux + A_HDR);
   if (slot < 0 || slot >= p.pool) {
     hdr[H_SLOT] = -1;
     ptx::mbar_arrive(full);
@@ -105,10 +122,7 @@ __device__ __forceinline__ void issue(const DecodeParams &p, const CUtensorMap *
   }
   hdr[H_SLOT] = slot;
   ptx::fence_proxy_async_smem();
-  ptx::mbar_arrive_expect_tx(full, SLOT_BYTES + 3 * T * ROW_BYTES);
-  const int row0 = (slot * HV + hv) * DV;
-  ptx::tma_load_2d(st + O_SW, tm_ld, 0, row0, full);
-  ptx::tma_load_2d(st + O_SW + 16384, tm_ld, 64, row0, full);
+  ptx::mbar_arrive_expect_tx(full, 3 * T * ROW_BYTES);
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
   const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
@@ -116,9 +130,9 @@ __device__ __forceinline__ void issue(const DecodeParams &p, const CUtensorMap *
   for (int t = 0; t < T; ++t) {
     const size_t qk_off = (((size_t)bi * T + t) * p.H + hk) * DK;
     const size_t v_off = (((size_t)bi * T + t) * HV + hv) * DV;
-    ptx::bulk_g2s(st + O_RAW + t * ROW_BYTES, k + qk_off, ROW_BYTES, full);
-    ptx::bulk_g2s(st + O_RAW + (T + t) * ROW_BYTES, q + qk_off, ROW_BYTES, full);
-    ptx::bulk_g2s(st + O_RAW + (2 * T + t) * ROW_BYTES, v + v_off, ROW_BYTES, full);
+    ptx::bulk_g2s(aux + A_RAW + t * ROW_BYTES, k + qk_off, ROW_BYTES, full);
+    ptx::bulk_g2s(aux + A_RAW + (T + t) * ROW_BYTES, q + qk_off, ROW_BYTES, full);
+    ptx::bulk_g2s(aux + A_RAW + (2 * T + t) * ROW_BYTES, v + v_off, ROW_BYTES, full);
   }
 }
 
@@ -139,19 +153,19 @@ __device__ __forceinline__ GateIn load_gate_in(const DecodeParams &p, int item, 
   return g;
 }
 
-// Prepare a landed stage (one warp): operand images of the normalised q/k,
-// gates and coefficients; every lane then arrives on `prep`.  Lane l handles
-// columns 4 l .. 4 l + 3 of every vector.
+// Prepare a landed per-item entry (one warp): operand images of the
+// normalised q/k, gates and coefficients; every lane then arrives on `prep`.
+// Lane l handles columns 4 l .. 4 l + 3 of every vector.
 template <int T>
 __device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, uint64_t *full,
                                      uint64_t *prep, uint32_t parity, GateIn gin, int lane) {
   if (!ptx::mbar_wait_bounded(full, parity)) record_error(p.err, GDN_ERR_TIMEOUT);
-  float *hdr = reinterpret_cast<float *>(st + O_HDR);
+  float *hdr = reinterpret_cast<float *>(st + A_HDR);
   if (*reinterpret_cast<const int *>(hdr) >= 0) {
     float x[2 * T][4];
 #pragma unroll
     for (int n = 0; n < 2 * T; ++n) {
-      const uint2 raw = *reinterpret_cast<const uint2 *>(st + O_RAW + n * ROW_BYTES + lane * 8);
+      const uint2 raw = *reinterpret_cast<const uint2 *>(st + A_RAW + n * ROW_BYTES + lane * 8);
       const float2 a = unpack2(raw.x), b = unpack2(raw.y);
       x[n][0] = a.x; x[n][1] = a.y; x[n][2] = b.x; x[n][3] = b.y;
     }
@@ -181,7 +195,7 @@ __device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, u
         gq[t][s] = s <= t ? warp_sum(dq) : 0.f;
       }
     // BD: row 2 n = hi, row 2 n + 1 = lo of vector n (k^_0.., then q^_0..)
-    unsigned char *bd = st + O_BD;
+    unsigned char *bd = st + A_BD;
     float hi[2 * T][4], lo[2 * T][4];
 #pragma unroll
     for (int n = 0; n < 2 * T; ++n) {
@@ -196,7 +210,7 @@ __device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, u
           make_uint2(pack2(lo[n][0], lo[n][1]), pack2(lo[n][2], lo[n][3]));
     }
     // BU: row = state column c, k index t: k^_t hi, T + t: k^_t hi, 2T + t: k^_t lo
-    unsigned char *bu = st + O_BU;
+    unsigned char *bu = st + A_BU;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float row[16];
@@ -261,12 +275,14 @@ __global__ void __launch_bounds__(NTHREADS, 2)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constant__ CUtensorMap tm_st,
                  DecodeParams p) {
   extern __shared__ unsigned char smem_raw[];
-  // stages on a 1024-byte boundary (the 128-byte swizzle repeats every 1 KB)
+  // slots on a 1024-byte boundary (the 128-byte swizzle repeats every 1 KB)
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NSTAGE * STAGE_BYTES);
-  uint64_t *prep = full + NSTAGE;
-  int *done = reinterpret_cast<int *>(prep + NSTAGE);
+  uint64_t *sw_full = reinterpret_cast<uint64_t *>(smem + O_BARS);
+  uint64_t *aux_full = sw_full + NSW, *prep = aux_full + NAUX;
+  int *sw_done = reinterpret_cast<int *>(prep + NAUX), *aux_done = sw_done + NSW;
+  auto sw_at = [&](int s) { return smem + s * SLOT_BYTES; };
+  auto aux_at = [&](int a) { return smem + O_AUX + a * AUX_BYTES; };
   constexpr int NT_DOT = (2 * T + 3) / 4;  // 8-column tiles of the dot product
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -275,74 +291,78 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
   __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
 
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&prep[s], 32);
-      done[s] = 0;
+    for (int s = 0; s < NSW; ++s) {
+      ptx::mbar_init(&sw_full[s], 1);
+      sw_done[s] = 0;
+    }
+    for (int a = 0; a < NAUX; ++a) {
+      ptx::mbar_init(&aux_full[a], 1);
+      ptx::mbar_init(&prep[a], 32);
+      aux_done[a] = 0;
     }
     ptx::fence_mbar_init();
   }
   // BD rows past the 2T vectors stay zero
-  for (int s = 0; s < NSTAGE; ++s)
+  for (int a = 0; a < NAUX; ++a)
     for (int i = tid; i < (16 - 4 * T) * (int)BD_PITCH / 16; i += NTHREADS)
-      reinterpret_cast<uint4 *>(smem + s * STAGE_BYTES + O_BD + 4 * T * BD_PITCH)[i] =
-          make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4 *>(aux_at(a) + A_BD + 4 * T * BD_PITCH)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   if (tid == 0) {
     ptx::prefetch_tmap(&tm_ld);
     ptx::prefetch_tmap(&tm_st);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NSW; ++s) {
       const int item = blockIdx.x + s * stride;
-      if (item < nitems) issue<T>(p, &tm_ld, smem + s * STAGE_BYTES, &full[s], item, slot_of(p, item));
+      if (item < nitems) issue_sw(p, &tm_ld, sw_at(s), &sw_full[s], item, slot_of(p, item));
+    }
+    for (int a = 0; a < NAUX; ++a) {
+      const int item = blockIdx.x + a * stride;
+      if (item < nitems) issue_aux<T>(p, aux_at(a), &aux_full[a], item, slot_of(p, item));
     }
   }
   if (warp < PREP_AHEAD) {
     const int item = blockIdx.x + warp * stride;
     if (item < nitems)
-      prepare<T>(p, smem + warp * STAGE_BYTES, &full[warp], &prep[warp], 0u,
-                 load_gate_in(p, item, lane, T), lane);
+      prepare<T>(p, aux_at(warp), &aux_full[warp], &prep[warp], 0u, load_gate_in(p, item, lane, T),
+                 lane);
   }
 
 #pragma unroll 1
   for (int it = 0;; ++it) {
     const int item = blockIdx.x + it * stride;
     if (item >= nitems) break;
-    const int s = it % NSTAGE;
-    const uint32_t parity = (uint32_t)((it / NSTAGE) & 1);
+    const int s = it % NSW, a = it % NAUX;
+    const uint32_t sp = (uint32_t)((it / NSW) & 1), ap = (uint32_t)((it / NAUX) & 1);
     const int bi = item / HV, hv = item % HV;
-    const int refill = item + NSTAGE * stride;
-    const int ahead = item + PREP_AHEAD * stride;
-    unsigned char *st = smem + s * STAGE_BYTES;
-    unsigned char *sw = st + O_SW;
-    const float *hdr = reinterpret_cast<const float *>(st + O_HDR);
-
-    if (!ptx::mbar_wait_bounded(&full[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
-    const int slot = *reinterpret_cast<const int *>(hdr);
+    unsigned char *sw = sw_at(s);
+    unsigned char *aux = aux_at(a);
+    const float *hdr = reinterpret_cast<const float *>(aux + A_HDR);
     const int r0 = 16 * warp;  // this warp's first state row
 
+    if (!ptx::mbar_wait_bounded(&prep[a], ap)) record_error(p.err, GDN_ERR_TIMEOUT);
+    const int slot = *reinterpret_cast<const int *>(hdr);
+    float C[16][4];
     if (slot >= 0) {
-      if (!ptx::mbar_wait_bounded(&prep[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
+      if (!ptx::mbar_wait_bounded(&sw_full[s], sp)) record_error(p.err, GDN_ERR_TIMEOUT);
       // ---- S0 rows as A fragments; the same values seed the fp32 accumulators
-      float C[16][4];
       float D[NT_DOT][4];
 #pragma unroll
       for (int n = 0; n < NT_DOT; ++n) D[n][0] = D[n][1] = D[n][2] = D[n][3] = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint32_t a[4];
-        ptx::ldmatrix_x4(sw_addr(sw, r0, j, lane), a[0], a[1], a[2], a[3]);
-        const float2 c00 = unpack2(a[0]), c01 = unpack2(a[1]), c10 = unpack2(a[2]),
-                     c11 = unpack2(a[3]);
+        uint32_t af[4];
+        ptx::ldmatrix_x4(sw_addr(sw, r0, j, lane), af[0], af[1], af[2], af[3]);
+        const float2 c00 = unpack2(af[0]), c01 = unpack2(af[1]), c10 = unpack2(af[2]),
+                     c11 = unpack2(af[3]);
         C[2 * j][0] = c00.x; C[2 * j][1] = c00.y; C[2 * j][2] = c01.x; C[2 * j][3] = c01.y;
         C[2 * j + 1][0] = c10.x; C[2 * j + 1][1] = c10.y;
         C[2 * j + 1][2] = c11.x; C[2 * j + 1][3] = c11.y;
         // dot products: B rows n (vectors' hi/lo), k = 16 j .. 16 j + 15
         uint32_t b[4];
         const int n = (lane & 7) + ((lane >> 4) << 3);
-        ptx::ldmatrix_x4(st + O_BD + n * BD_PITCH + (16 * j + 8 * ((lane >> 3) & 1)) * 2, b[0],
+        ptx::ldmatrix_x4(aux + A_BD + n * BD_PITCH + (16 * j + 8 * ((lane >> 3) & 1)) * 2, b[0],
                          b[1], b[2], b[3]);
-        ptx::mma_16816_bf16(D[0], a, b[0], b[1]);
-        if (NT_DOT > 1) ptx::mma_16816_bf16(D[NT_DOT - 1], a, b[2], b[3]);
+        ptx::mma_16816_bf16(D[0], af, b[0], b[1]);
+        if (NT_DOT > 1) ptx::mma_16816_bf16(D[NT_DOT - 1], af, b[2], b[3]);
       }
       // vector 4 nt + tig on this lane: rows g (hi + lo) and g + 8
       float vg[NT_DOT], vg8[NT_DOT];
@@ -367,7 +387,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
         }
       }
       // ---- deltas and outputs of rows r0 + g and r0 + g + 8
-      const __nv_bfloat16 *vraw = reinterpret_cast<const __nv_bfloat16 *>(st + O_RAW + 2 * T * ROW_BYTES);
+      const __nv_bfloat16 *vraw =
+          reinterpret_cast<const __nv_bfloat16 *>(aux + A_RAW + 2 * T * ROW_BYTES);
       float dl[2][T];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -428,11 +449,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
       for (int j = 0; j < 8; ++j) {
         uint32_t b[4];
         const int n = 16 * j + (lane & 7) + ((lane >> 4) << 3);
-        ptx::ldmatrix_x4(st + O_BU + n * BU_PITCH + ((lane >> 3) & 1) * 16, b[0], b[1], b[2], b[3]);
+        ptx::ldmatrix_x4(aux + A_BU + n * BU_PITCH + ((lane >> 3) & 1) * 16, b[0], b[1], b[2], b[3]);
         ptx::mma_16816_bf16(C[2 * j], ua, b[0], b[1]);
         ptx::mma_16816_bf16(C[2 * j + 1], ua, b[2], b[3]);
       }
-      // ---- write back: bf16 fragments -> this warp's rows of the stage -> TMA store
+    }
+
+    // Done with the per-item entry: the last warp out refills it with the
+    // item NAUX ahead; the first prepares the item PREP_AHEAD ahead (below).
+    __syncwarp();
+    int order = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      order = atomicAdd(&aux_done[a], 1);
+      if (order == NWARPS - 1) {
+        aux_done[a] = 0;
+        __threadfence_block();
+        const int refill = item + NAUX * stride;
+        if (refill < nitems) issue_aux<T>(p, aux, &aux_full[a], refill, slot_of(p, refill));
+      }
+    }
+    order = __shfl_sync(0xffffffffu, order, 0);
+
+    if (slot >= 0) {
+      // ---- write back: bf16 fragments -> this warp's rows of the slot -> TMA store
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         ptx::stmatrix_x4(sw_addr(sw, r0, j, lane), pack2(C[2 * j][0], C[2 * j][1]),
@@ -445,33 +485,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
         ptx::tma_store_2d(&tm_st, 0, grow, sw + r0 * 128);
         ptx::tma_store_2d(&tm_st, 64, grow, sw + 16384 + r0 * 128);
         ptx::bulk_commit();
-        ptx::bulk_wait_read<0>();  // the stage may be refilled only after this
+        ptx::bulk_wait_read<0>();  // the slot may be refilled only after this
       }
-    }
-
-    // This warp is done with stage s: the last warp out refills it, the first
-    // prepares the next item.
-    __syncwarp();
-    int order = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      order = atomicAdd(&done[s], 1);
-      if (order == NWARPS - 1) {
-        done[s] = 0;
-        __threadfence_block();
-        if (refill < nitems) issue<T>(p, &tm_ld, st, &full[s], refill, slot_of(p, refill));
-      }
-    }
-    order = __shfl_sync(0xffffffffu, order, 0);
-    if (slot < 0) {
+    } else {
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
       for (int idx = tid; idx < T * DV; idx += NTHREADS)
         o[(((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV] = __float2bfloat16_rn(0.f);
     }
+    // done with the state slot: the last warp out refills it
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&sw_done[s], 1) == NWARPS - 1) {
+        sw_done[s] = 0;
+        __threadfence_block();
+        const int refill = item + NSW * stride;
+        if (refill < nitems) issue_sw(p, &tm_ld, sw, &sw_full[s], refill, slot_of(p, refill));
+      }
+    }
+    const int ahead = item + PREP_AHEAD * stride;
     if (order == 0 && ahead < nitems) {
-      const int sa = (it + PREP_AHEAD) % NSTAGE;
-      prepare<T>(p, smem + sa * STAGE_BYTES, &full[sa], &prep[sa],
-                 (uint32_t)(((it + PREP_AHEAD) / NSTAGE) & 1), load_gate_in(p, ahead, lane, T), lane);
+      const int pa = (it + PREP_AHEAD) % NAUX;
+      prepare<T>(p, aux_at(pa), &aux_full[pa], &prep[pa], (uint32_t)(((it + PREP_AHEAD) / NAUX) & 1),
+                 load_gate_in(p, ahead, lane, T), lane);
     }
   }
   // the last stores must have left shared memory before the block exits
