@@ -184,6 +184,22 @@ def time_steps(fn, steps, warmup, flush, stream):
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's `x` (the whole job takes as long as its
+    slowest replica); `x` itself on one rank.  Works with gloo (CPU tensors)
+    and NCCL (device tensors)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_step, steps, world, total_ms):
+    """Units all `world` replicas processed per second over the timed region."""
+    return units_per_step * steps * world / (total_ms / 1e3)
+
+
 def to_dev(inp, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
@@ -222,14 +238,10 @@ def run_ours(args, rank, world, dev):
     status = gdn.gdn_check_device_error()
     if status != gdn.Status.OK:
         raise RuntimeError(f"device error during bench: {status.name}")
-    tot_ms = sum(ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(ms), world, dev)
     ms_step = tot_ms / args.steps
     tokens = dm["B"] * dm["T"]
-    value = tokens * args.steps * world / (tot_ms / 1e3)
+    value = replica_throughput(tokens, args.steps, world, tot_ms)
     nbytes = gdn_bytes(dm["B"], dm["T"], dm["H"], dm["Hg"], dm["K"], dm["V"], dm["N"])
     flops = chunk_flops(dm["B"], dm["T"], dm["H"], dm["K"], dm["V"])
     achieved_gbs = nbytes / (ms_step / 1e3) / 1e9
@@ -269,12 +281,8 @@ def run_ours(args, rank, world, dev):
         ht_h.copy_(ht, non_blocking=True)
 
     e2e_ms = time_steps(e2e_step, min(args.steps, 10), 2, flush, stream)
-    e2e_tot = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_tot], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_tot = float(t.item())
-    result["e2e"] = {"value": tokens * len(e2e_ms) * world / (e2e_tot / 1e3), "unit": UNIT,
+    e2e_tot = max_over_ranks(sum(e2e_ms), world, dev)
+    result["e2e"] = {"value": replica_throughput(tokens, len(e2e_ms), world, e2e_tot), "unit": UNIT,
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     del d, o, ht, pin
 

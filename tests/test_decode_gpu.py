@@ -41,9 +41,10 @@ def test_small_batch(T):
     assert_close(state, st_ref, TOL_BF16, "state")
 
 
-def test_permuted_slots_pool_larger_than_batch():
+@pytest.mark.parametrize("T", [2, 4])
+def test_permuted_slots_pool_larger_than_batch(T):
     slots = [5, 0, 3]
-    inp = synth.decode_inputs(311, 3, 2, 1, 2, 128, 128, pool=7, slots=slots)
+    inp = synth.decode_inputs(311, 3, T, 1, 2, 128, 128, pool=7, slots=slots)
     o, state = run_gpu(inp)
     assert gdn_check_device_error() == Status.OK
     o_ref, st_ref = oracle_for(inp, range(3))
@@ -65,8 +66,9 @@ def test_without_l2norm_and_custom_gate_params():
     assert_close(state, st_ref, TOL_BF16, "state")
 
 
-def test_bad_slot_is_reported_and_skipped():
-    inp = synth.decode_inputs(313, 3, 1, 1, 1, 128, 128, pool=3, slots=[0, 9, 2])
+@pytest.mark.parametrize("T", [1, 3])
+def test_bad_slot_is_reported_and_skipped(T):
+    inp = synth.decode_inputs(313, 3, T, 1, 1, 128, 128, pool=3, slots=[0, 9, 2])
     o, state = run_gpu(inp)
     assert gdn_check_device_error() == Status.BAD_SLOT
     assert torch.count_nonzero(o[1]).item() == 0
