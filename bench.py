@@ -264,27 +264,33 @@ def run_ours(args, rank, world, dev):
         "wall_s_timed_region": t_wall,
     }
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the C-ABI host entry point: pinned host buffers in
+    # and out, every host<->device copy inside the timed region (the library
+    # overlaps them with the kernels piece by piece)
     pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
     keys = ("q", "k", "v", "g", "beta", "h0")
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in keys)
     d2h = o_h.numel() * o_h.element_size() + ht_h.numel() * ht_h.element_size()
+    del d, o, ht
+    ws = torch.empty(gdn.gdn_chunk_host_workspace_bytes(pin["q"], pin["v"]), dtype=torch.uint8,
+                     device=dev)
 
     def e2e_step():
-        for k in keys:
-            d[k].copy_(pin[k], non_blocking=True)
-        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
-                          initial_state=d["h0"], out=o, final_state=ht)
-        o_h.copy_(o, non_blocking=True)
-        ht_h.copy_(ht, non_blocking=True)
+        gdn.gdn_chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"],
+                               scale=pin["scale"], initial_state=pin["h0"], out=o_h,
+                               final_state=ht_h, workspace=ws, stream=stream)
 
-    e2e_ms = time_steps(e2e_step, min(args.steps, 10), 2, flush, stream)
+    e2e_ms = time_steps(e2e_step, min(args.steps, 10), 3, flush, stream)
     e2e_tot = max_over_ranks(sum(e2e_ms), world, dev)
+    status = gdn.gdn_check_device_error()
+    if status != gdn.Status.OK:
+        raise RuntimeError(f"device error during the end-to-end run: {status.name}")
     result["e2e"] = {"value": replica_throughput(tokens, len(e2e_ms), world, e2e_tot), "unit": UNIT,
-                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    del d, o, ht, pin
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                     "entry_point": "gdn_chunk_fwd_host (host buffers, pinned)"}
+    del pin, ws
 
     # ---- the other rows of the hot path, same timing rules
     rows = {}

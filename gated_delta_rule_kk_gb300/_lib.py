@@ -78,6 +78,9 @@ class GdnDecodeArgs(ctypes.Structure):
 SIGNATURES = {
     "gdn_chunk_workspace_size": ([ctypes.POINTER(GdnChunkArgs), ctypes.POINTER(c_size_t)], c_int32),
     "gdn_chunk_fwd": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
+    "gdn_chunk_fwd_host": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
+    "gdn_chunk_host_workspace_size": ([ctypes.POINTER(GdnChunkArgs), ctypes.POINTER(c_size_t)],
+                                      c_int32),
     "kda_chunk_workspace_size": ([ctypes.POINTER(KdaChunkArgs), ctypes.POINTER(c_size_t)], c_int32),
     "kda_chunk_fwd": ([ctypes.POINTER(KdaChunkArgs), c_void_p], c_int32),
     "gdn_decode": ([ctypes.POINTER(GdnDecodeArgs), c_void_p], c_int32),

@@ -119,6 +119,97 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     return out, ht
 
 
+def _need_host(t, name, dtypes):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def gdn_chunk_fwd_host(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                       output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
+                       workspace=None, stream=None, device=None):
+    """``gdn_chunk_fwd`` from and to host memory, copies included.
+
+    Every tensor is a CPU tensor (pinned ones copy asynchronously and fastest);
+    the library copies them to ``workspace`` (a CUDA uint8 tensor, allocated on
+    ``device`` if not passed), runs the forward and copies ``o`` and ``ht``
+    back, piece by piece so that copies overlap the kernels.  Everything is
+    enqueued on ``stream``; the host outputs are complete once it has
+    completed.  Returns ``(o, ht)`` as CPU tensors.
+    """
+    dt, dts = _io_dtype(q)
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _need_host(t, name, dts)
+    _need_host(g, "g", (torch.float32,))
+    _need_host(beta, "beta", (torch.float32,))
+    B, T, Hg, K = q.shape
+    H, V = v.shape[2], v.shape[3]
+    if k.shape != q.shape or v.shape[:2] != (B, T):
+        raise ValueError("q, k must be [B,T,Hg,K] and v [B,T,H,V]")
+    N = B
+    if cu_seqlens is not None:
+        _need_host(cu_seqlens, "cu_seqlens", (torch.int32,))
+        N = cu_seqlens.numel() - 1
+    if initial_state is not None:
+        _need_host(initial_state, "initial_state", (torch.float32,))
+        if tuple(initial_state.shape) != (N, H, K, V):
+            raise ValueError(f"initial_state must be [{N},{H},{K},{V}]")
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=q.dtype, pin_memory=True)
+    else:
+        _need_host(out, "out", dts)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, pin_memory=True)
+    elif final_state is not None:
+        _need_host(final_state, "final_state", (torch.float32,))
+    a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
+                     h0=_ptr(initial_state), ht=_ptr(final_state), o=_ptr(out),
+                     cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N,
+                     chunk_size=CHUNK, g_is_cumsum=int(bool(g_is_cumsum)),
+                     scale=float(scale) if scale is not None else 0.0,
+                     workspace=None, workspace_bytes=0)
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    _lib.check(lib.gdn_chunk_host_workspace_size(ctypes.byref(a), ctypes.byref(n)),
+               "gdn_chunk_host_workspace_size")
+    if device is None:
+        device = stream.device if stream is not None else torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        workspace = torch.empty(n.value, dtype=torch.uint8, device=device)
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < n.value:
+        raise ValueError(f"workspace needs {n.value} bytes on the GPU")
+    a.workspace = ctypes.c_void_p(workspace.data_ptr())
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(workspace.device):
+        _lib.check(lib.gdn_chunk_fwd_host(ctypes.byref(a), _stream(stream)), "gdn_chunk_fwd_host")
+    del workspace  # the caching allocator keeps it valid for work already on `stream`
+    return out, final_state
+
+
+def gdn_chunk_host_workspace_bytes(q, v, cu_seqlens=None, Hg=None):
+    """Device workspace ``gdn_chunk_fwd_host`` needs for q [B,T,Hg,K] and
+    v [B,T,H,V] (CPU tensors; only their shapes and dtype are read) and, with
+    packed sequences, the CPU int32 ``cu_seqlens``."""
+    dt, _ = _io_dtype(q)
+    B, T, hg, K = q.shape
+    H, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    a = GdnChunkArgs(dtype=int(dt), q=None, k=None, v=None, g=None, beta=None, h0=None, ht=None,
+                     o=None, cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, Hg=Hg or hg, K=K, V=V,
+                     N=N, chunk_size=CHUNK, g_is_cumsum=0, scale=0.0, workspace=None,
+                     workspace_bytes=0)
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.load().gdn_chunk_host_workspace_size(ctypes.byref(a), ctypes.byref(n)),
+               "gdn_chunk_host_workspace_size")
+    return n.value
+
+
 def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                           output_final_state=True, g_is_cumsum=False, out=None,
                           final_state=None, stream=None):

@@ -55,7 +55,7 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
                          const float *g, const float *beta, const float *h0, const float *ht,
                          const void *o, const int32_t *cu, int B, int T, int Hk, int Hv, int K,
                          int V, int N, int chunk_size, int g_is_cumsum, float scale,
-                         const char *hk_name) {
+                         const char *hk_name, bool sizes_only = false) {
   REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG, "dtype %d is not GDN_F32/GDN_BF16", dtype);
   REQUIRE(B >= 1 && T >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1 && N >= 1,
           GDN_ERR_INVALID_ARG, "sizes must be positive (B=%d T=%d heads=%d/%d K=%d V=%d N=%d)", B,
@@ -71,6 +71,7 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
   } else {
     REQUIRE(B == 1, GDN_ERR_INVALID_ARG, "with cu_seqlens B must be 1 (got %d)", B);
   }
+  if (sizes_only) return GDN_OK;
   REQUIRE_PTR(q, "q");
   REQUIRE_PTR(k, "k");
   REQUIRE_PTR(v, "v");
@@ -128,6 +129,13 @@ gdn_status_t run_chunk(ChunkParams &p, bool bf16, bool kda, void *ws, size_t ws_
 }
 
 }  // namespace
+
+gdn_status_t check_gdn_chunk_sizes(const gdn_chunk_args &a) {
+  g_msg[0] = '\0';
+  return check_chunk(a.dtype, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                     nullptr, a.cu_seqlens, a.B, a.T, a.Hg, a.H, a.K, a.V,
+                     a.N, a.chunk_size, a.g_is_cumsum, a.scale, "Hg", true);
+}
 
 gdn_status_t set_host_error(gdn_status_t st, const char *msg) { return fail(st, "%s", msg); }
 

@@ -49,6 +49,10 @@ size_t chunk_tc_workspace(const ChunkParams &p, bool per_channel_gate);
 cudaError_t launch_chunk_tc(const ChunkParams &p, bool per_channel_gate, void *workspace,
                             cudaStream_t stream);
 
+// The checks of gdn_chunk_fwd that read only sizes, dtype and flags (no
+// pointer is dereferenced; cu_seqlens only counts as given or NULL).
+gdn_status_t check_gdn_chunk_sizes(const gdn_chunk_args &a);
+
 // Record `msg` as the calling thread's last host-side error; returns `st`.
 gdn_status_t set_host_error(gdn_status_t st, const char *msg);
 

@@ -117,6 +117,40 @@ gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *args, size_t *bytes)
 gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *args, gdn_stream_t stream);
 
 /*
+ * The same forward end to end from HOST memory: q, k, v, g, beta, h0,
+ * cu_seqlens are read from and o, ht written to host buffers (pinned memory
+ * lets the copies run asynchronously and at full speed; pageable memory is
+ * accepted).  Shapes, limits and NULL rules are those of gdn_chunk_fwd.
+ * `workspace` is a DEVICE buffer on the current device, 256-byte aligned,
+ * caller-owned, of at least gdn_chunk_host_workspace_size() bytes: it takes
+ * device copies of the inputs and outputs and the kernels' scratch.
+ * The call enqueues everything behind the work already on `stream` and
+ * returns; o and ht are complete in host memory when `stream` has completed
+ * (e.g. cudaStreamSynchronize).  Host buffers must stay valid and unchanged
+ * until then.  Inside, the problem is cut into pieces of whole 64-token
+ * chunks along time (sequences of at least two pieces of 1024 tokens) or into
+ * ranges of whole sequences, and each piece's host->device copies, kernels
+ * and device->host copies run on an internal copy-in stream, `stream` and an
+ * internal copy-out stream, so the copies of one piece overlap the kernels of
+ * its neighbours.  The results equal gdn_chunk_fwd's bit for bit: a time cut
+ * hands the fp32 state of the chunkwise recurrence (Gated Delta Networks,
+ * section 3) from one piece to the next exactly as the kernels carry it
+ * between chunks.
+ * Errors: argument errors as gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG when an
+ * input or output pointer is device memory, GDN_ERR_WORKSPACE when the
+ * workspace is missing, too small or not device memory, GDN_ERR_BAD_SEQLENS
+ * (returned by the call itself) when cu_seqlens does not rise from 0 to T.
+ * With cu_seqlens the call copies offsets rebased per piece from pageable
+ * memory, so it cannot be captured into a CUDA graph; without, it can.
+ * Calls from several host threads are serialised inside the library.
+ */
+gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *args, gdn_stream_t stream);
+
+/* Bytes of device workspace gdn_chunk_fwd_host needs for these arguments.
+ * Reads sizes, dtype and, when given, the host array cu_seqlens. */
+gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *bytes);
+
+/*
  * Chunked forward with one log-gate per token, value head and key channel
  * (KDA).  Shapes follow chunk_kda_fwd_kernel_inter_solve_fused (vLLM kimi_k3
  * kda/chunk_intra page):
