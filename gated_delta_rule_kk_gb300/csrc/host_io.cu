@@ -3,9 +3,10 @@
 // The caller passes host buffers for every input and output and one device
 // buffer (the workspace) that receives device copies of them and the scratch
 // of the tensor-core kernels.  The problem is cut into pieces:
-//   * time pieces (fixed-length batches whose sequences span at least two
-//     pieces of PIECE_CHUNKS 64-token chunks): piece j holds tokens
-//     t0_j .. t1_j of every sequence, t0_j a multiple of 64;
+//   * time pieces (fixed-length batches of sequences of more than 10
+//     64-token chunks): piece j holds tokens t0_j .. t1_j of every sequence,
+//     t0_j a multiple of 64, and the pieces shrink geometrically towards the
+//     end (see time_pieces);
 //   * sequence pieces (shorter fixed-length sequences, or cu_seqlens): piece
 //     j holds whole sequences n0_j .. n1_j, cut so that the pieces carry
 //     about the same number of tokens.
@@ -24,6 +25,7 @@
 // after a chunk depends on the tokens before it only through the state
 // entering it (Gated Delta Networks, section 3, chunkwise form).
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 #include <vector>
@@ -37,7 +39,8 @@ namespace gdn {
 namespace {
 
 constexpr int MAX_PIECES = 8;
-constexpr int PIECE_CHUNKS = 16;          // time piece: >= 16 chunks of each sequence
+constexpr int MIN_PIECE_CHUNKS = 4;       // the last (shortest) time piece, in chunks
+constexpr double PIECE_GROWTH = 1.6;      // each time piece is this much longer than the next
 constexpr int64_t PIECE_TOKENS = 2048;    // sequence piece: >= 2048 tokens
 constexpr int CHUNK = 64;
 constexpr int MAX_DEVICES = 64;
@@ -100,6 +103,33 @@ gdn_chunk_args piece_args(const gdn_chunk_args &a, const Plan &L, int j, unsigne
   return d;
 }
 
+// Chunk boundaries c[0..P] of the time pieces of a sequence of nc chunks.
+// What is left once the last copy-in has landed (the last piece's kernels and
+// its copy-out) is short because the last piece is short; earlier pieces grow
+// by PIECE_GROWTH each, so that every piece's kernels finish while the next,
+// shorter piece is still being copied in.  P is the largest count whose
+// smallest piece still holds MIN_PIECE_CHUNKS chunks; 1 = no time cut.
+int time_pieces(int nc, int *c) {
+  int P = 0;
+  double sum = 0.0, w = MIN_PIECE_CHUNKS;
+  while (P < MAX_PIECES && sum + w <= nc) {
+    sum += w;
+    w *= PIECE_GROWTH;
+    ++P;
+  }
+  if (P < 2) return 1;
+  double W = 0.0;
+  for (int j = 0; j < P; ++j) W += std::pow(PIECE_GROWTH, j);
+  double acc = 0.0;
+  c[0] = 0;
+  for (int j = 0; j < P; ++j) {
+    acc += std::pow(PIECE_GROWTH, P - 1 - j);
+    c[j + 1] = (int)std::llround(nc * acc / W);
+  }
+  c[P] = nc;
+  return P;
+}
+
 gdn_status_t make_plan(const gdn_chunk_args &a, Plan *L) {
   gdn_status_t st = check_gdn_chunk_sizes(a);
   if (st != GDN_OK) return st;
@@ -141,15 +171,16 @@ gdn_status_t make_plan(const gdn_chunk_args &a, Plan *L) {
   } else {
     L->rows_per_seq = a.T;
     const int nc = (a.T + CHUNK - 1) / CHUNK;
-    const int Pt = std::min(MAX_PIECES, nc / PIECE_CHUNKS);
+    int cb[MAX_PIECES + 1];
+    const int Pt = time_pieces(nc, cb);
     if (Pt >= 2) {
       L->time_cut = true;
       L->P = Pt;
       for (int j = 0; j < Pt; ++j) {
         Piece &p = L->pc[j];
         p.n0 = 0; p.n1 = a.B; p.cu_off = 0;
-        p.t0 = std::min<int64_t>((int64_t)CHUNK * (nc * (int64_t)j / Pt), a.T);
-        p.t1 = std::min<int64_t>((int64_t)CHUNK * (nc * (int64_t)(j + 1) / Pt), a.T);
+        p.t0 = std::min<int64_t>((int64_t)CHUNK * cb[j], a.T);
+        p.t1 = std::min<int64_t>((int64_t)CHUNK * cb[j + 1], a.T);
       }
     } else {
       const int64_t tokens = (int64_t)a.B * a.T;

@@ -39,22 +39,50 @@ def ws_size(lib, a):
 
 
 def test_time_cut_layout(lib):
-    # B=2, T=4096: four time pieces of 1024 tokens per sequence (2048 rows each);
-    # q, k, v, o, g, beta slices per piece, two whole fp32 states, and the
-    # tensor-core scratch of one piece (B=2, T=1024: 16 chunks x 16 heads each).
+    # B=2, T=4096 (64 chunks): five time pieces shrinking by about 1.6 each
+    # towards a last piece of 4 chunks -> 27, 16, 10, 7, 4 chunks.  Each piece
+    # has its own q, k, v, o, g, beta slices; two whole fp32 states; and the
+    # tensor-core scratch of the largest piece (B=2, 27 chunks x 16 heads).
     st, n = ws_size(lib, args())
     assert st == Status.OK
-    rows = 2048
-    qk = 4 * a256(rows * 16 * 128 * 2)
-    vo = 4 * a256(rows * 16 * 128 * 2)
-    gb = 4 * a256(rows * 16 * 4)
+    chunks = (27, 16, 10, 7, 4)
+    rows = [2 * 64 * c for c in chunks]
+    qk = sum(a256(r * 16 * 128 * 2) for r in rows)
+    vo = sum(a256(r * 16 * 128 * 2) for r in rows)
+    gb = sum(a256(r * 16 * 4) for r in rows)
     state = a256(2 * 16 * 128 * 128 * 4)
-    scratch = 256 + 2 * 16 * 16 * BLK128
+    scratch = 256 + 2 * 27 * 16 * BLK128
     assert n == 2 * qk + 2 * vo + 2 * gb + 2 * state + scratch
 
 
+@pytest.mark.parametrize("T,chunks", [
+    (641, (7, 4)),             # 11 chunks: the shortest sequence that is cut in time
+    (2100, (16, 11, 6)),       # ragged tail inside the last piece
+    (64 * 1000, None),         # at most 8 pieces
+])
+def test_time_cut_piece_counts(lib, T, chunks):
+    st, n = ws_size(lib, args(B=1, N=1, T=T, dtype=0, H=1, Hg=1, K=16, V=16))
+    assert st == Status.OK
+    if chunks is not None:
+        tok = [64 * c for c in chunks]
+        tok[-1] -= 64 * sum(chunks) - T
+        per = sum(2 * a256(t * 16 * 4) * 2 + 2 * a256(t * 4) for t in tok)
+        assert n == per + 2 * a256(16 * 16 * 4)
+    else:
+        # eight pieces: 8 slices of each of the six per-row regions, each
+        # padded to 256 bytes, so the total sits within 6*8*256 of the tight sum
+        tight = 2 * (T * 64) * 2 + 2 * T * 4 + 2 * a256(16 * 16 * 4)
+        assert tight <= n <= tight + 6 * 8 * 256
+
+
+def test_640_tokens_are_cut_by_sequence(lib):
+    st, n = ws_size(lib, args(B=1, N=1, T=640, dtype=0, H=1, Hg=1, K=16, V=16))
+    assert st == Status.OK
+    assert n == 2 * a256(640 * 64) * 2 + 2 * a256(640 * 4) + 2 * a256(16 * 16 * 4)
+
+
 def test_short_sequences_cut_by_batch(lib):
-    # T=512 is below two 1024-token pieces: cut the 16 sequences into
+    # T=512 (8 chunks) is too short to cut in time: cut the 16 sequences into
     # 16*512/2048 = 4 pieces of 4 whole sequences.
     st, n = ws_size(lib, args(B=16, N=16, T=512))
     assert st == Status.OK
