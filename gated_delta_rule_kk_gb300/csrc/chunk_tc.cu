@@ -66,7 +66,7 @@ constexpr float GATE_FACTOR_LIMIT = 80.f;  // |gamma| bound for split exponentia
 // per (chunk, head) block in the workspace: the chain's operand images
 //   AW  [-w ; q~] (128 x 128 bf16, cs 2048)   KT  k~ (64 x 128 bf16, cs 1024)
 //   AQ  [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048) SC  decay[128], rs[64], qs[64]
-//   U   u, fp32 [V / 32 tiles][64][32]
+//   U   u, fp32 [V / 32 tiles][64][32], 16-byte group q of row i at q ^ (i & 7)
 constexpr uint32_t OFF_AW = 0, OFF_KT = 32768, OFF_AQ = 49152, OFF_SC = 65536, OFF_U = 66560;
 __host__ __device__ constexpr uint32_t block_bytes(int V, bool) {
   return OFF_U + (uint32_t)V * 256u;
@@ -715,10 +715,13 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       float v[32];
       ptx::tmem_ld32(dU + lane_base + t * 32, v);
       if (lane < 16) {
+        // 16-byte group q of row i sits at group q ^ (i & 7), so that the
+        // chain's per-row loads (one row per lane) hit eight different groups
+        // in every quarter warp: no shared-memory bank conflicts
         float4 *dst = reinterpret_cast<float4 *>(blk + OFF_U + t * 8192 + i * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          dst[q ^ (i & 7)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
     }
   }
@@ -744,11 +747,12 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 //   KT  [32768, 49152)   k~ (64 tokens x 128 keys, cs 1024)
 //   AQ  [49152, 65536)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
 //   SC  [65536, 66560)   decay[128], rs[64], qs[64]
-//   U   [66560, 74752)   u tile, fp32 64 x 32
+//   U   [66560, 74752)   u tile, fp32 64 x 32 (row-swizzled 16-byte groups)
 // then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo]
-// (64 tokens x 64, cs 1024) and the fp32 exchange X.  The epilogue warps are
-// done with a stage once v_new is formed (SC and U read), so they release it
-// then, not after the output: the next block streams in a step earlier.
+// (64 tokens x 64, cs 1024) and the fp32 exchange X.  A stage is filled and
+// released in two halves: AW, SC and U are free once D1 has run and v_new is
+// formed, KT and AQ only after the output GEMM, so the first half of the next
+// block but one streams in half a step earlier.
 // Every bf16 pair rides in the N dimension of one GEMM (N = 64), so the
 // split costs no extra tcgen05 instructions; each accumulator holds the two
 // halves side by side and the epilogue adds them.
@@ -758,6 +762,20 @@ constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_X = C_VN + 8192,
                    C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
 constexpr int CHAIN_THREADS = 320;
 constexpr int EPI_WARPS = 8;
+// Named barriers of the chain kernel (1 is the epilogue warps' own).  The
+// epilogue warps arrive (without waiting) once h, or v_new, is in shared
+// memory; the MMA warp waits on them.  Each phase's arrivals depend on MMAs
+// the MMA warp issues only after it passed the previous phase, so phases
+// never overlap; every role runs every chunk, so every phase completes.
+constexpr int BAR_HREADY = 2, BAR_HREADY_THREADS = 32 * (EPI_WARPS + 1);
+constexpr int BAR_VNREADY = 3, BAR_VNREADY_THREADS = 32 * (4 + 1);  // warps 0, 1, 4, 5 + MMA
+
+__device__ __forceinline__ void bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // start-address field of a shared-memory descriptor advanced by `bytes`
 __device__ __forceinline__ uint64_t adv(uint64_t desc, uint32_t bytes) {
@@ -793,10 +811,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   unsigned char *VN = smem + C_VN;
   float *X = reinterpret_cast<float *>(smem + C_X);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C_BAR);
-  uint64_t *full = bar, *empty = bar + 2, *d1 = bar + 4, *d3 = bar + 5, *d5 = bar + 6,
-           *vnready = bar + 7, *hready = bar + 8;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 9);
-  volatile int *abort_flag = reinterpret_cast<int *>(bar + 10);
+  // each stage has two halves with their own barriers: A = AW, SC, U (read
+  // by D1 and the v_new epilogue), B = KT, AQ (read by DH and D5), so that A
+  // is refilled as soon as v_new is formed, half a step before B
+  uint64_t *fullA = bar, *emptyA = bar + 2, *fullB = bar + 4, *emptyB = bar + 6;
+  uint64_t *d1 = bar + 8, *d3 = bar + 9, *d5 = bar + 10;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 11);
+  volatile int *abort_flag = reinterpret_cast<int *>(bar + 12);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int vt = blockIdx.x;
@@ -819,15 +840,15 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   const int nch = (eos - bos + BT - 1) / BT;
 
   if (tid == 0) {
-    ptx::mbar_init(&full[0], 1);
-    ptx::mbar_init(&full[1], 1);
-    ptx::mbar_init(&empty[0], 1 + EPI_WARPS);
-    ptx::mbar_init(&empty[1], 1 + EPI_WARPS);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&fullA[i], 1);
+      ptx::mbar_init(&emptyA[i], 1 + EPI_WARPS);
+      ptx::mbar_init(&fullB[i], 1);
+      ptx::mbar_init(&emptyB[i], 1);
+    }
     ptx::mbar_init(d1, 1);
     ptx::mbar_init(d3, 1);
     ptx::mbar_init(d5, 1);
-    ptx::mbar_init(vnready, 4);
-    ptx::mbar_init(hready, EPI_WARPS);
     ptx::fence_mbar_init();
     *abort_flag = 0;
   }
@@ -839,47 +860,65 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   const uint32_t dD1 = tmem, dDH = tmem + 64, dD5 = tmem + 128;
 
   if (warp == EPI_WARPS) {
-    // ---------------- producer: one operand block per chunk, five bulk copies
+    // ---------------- producer: one operand block per chunk, in two halves.
+    // Half A of chunk c + 1 is released (v_new of chunk c - 1) before half B
+    // of chunk c (output GEMM of chunk c - 2), so waiting in the order
+    // A(c), B(c), A(c + 1), ... never holds a release back.
     if (lane == 0) {
+      constexpr uint32_t A_BYTES = 32768 + 1024 + 8192, B_BYTES = 32768;
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1, k = c >> 1;
-        if (k > 0 && !ptx::mbar_wait_bounded(&empty[s], (uint32_t)((k - 1) & 1))) {
+        unsigned char *st = smem + s * STAGE_BYTES;
+        const unsigned char *src = p.blocks + ((size_t)(base + c) * p.H + h) * p.block;
+        if (k > 0 && !ptx::mbar_wait_bounded(&emptyA[s], (uint32_t)((k - 1) & 1))) {
           record_error(p.err, GDN_ERR_TIMEOUT);  // keep going: no role may stall the others
           *abort_flag = 1;
         }
-        unsigned char *st = smem + s * STAGE_BYTES;
-        const unsigned char *src = p.blocks + ((size_t)(base + c) * p.H + h) * p.block;
-        ptx::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-        ptx::bulk_g2s(st + S_AW, src + OFF_AW, OFF_SC + 1024, &full[s]);  // AW, KT, AQ, SC
-        ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &full[s]);
+        ptx::mbar_arrive_expect_tx(&fullA[s], A_BYTES);
+        ptx::bulk_g2s(st + S_AW, src + OFF_AW, 32768, &fullA[s]);
+        ptx::bulk_g2s(st + S_SC, src + OFF_SC, 1024, &fullA[s]);
+        ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &fullA[s]);
+        if (k > 0 && !ptx::mbar_wait_bounded(&emptyB[s], (uint32_t)((k - 1) & 1))) {
+          record_error(p.err, GDN_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        ptx::mbar_arrive_expect_tx(&fullB[s], B_BYTES);
+        ptx::bulk_g2s(st + S_KT, src + OFF_KT, B_BYTES, &fullB[s]);  // KT, AQ
       }
     }
   } else if (warp == EPI_WARPS + 1) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t id_kmn = ptx::idesc_bf16(128, 2 * VTILE, 0, 1);   // A K-major, B MN-major
-      const uint32_t id_mnmn = ptx::idesc_bf16(128, 2 * VTILE, 1, 1);  // both MN-major
-      const uint64_t dH0 = ptx::sdesc(Himg, 128, 2048);
-      const uint64_t dVN0 = ptx::sdesc(VN, 128, 1024);
-      bool ok = true;
+    // ---------------- MMA issuer (lane 0 issues; the whole warp takes part in
+    // the named barriers that hand over h and v_new)
+    const uint32_t id_kmn = ptx::idesc_bf16(128, 2 * VTILE, 0, 1);   // A K-major, B MN-major
+    const uint32_t id_mnmn = ptx::idesc_bf16(128, 2 * VTILE, 1, 1);  // both MN-major
+    const uint64_t dH0 = ptx::sdesc(Himg, 128, 2048);
+    const uint64_t dVN0 = ptx::sdesc(VN, 128, 1024);
+    bool ok = true;
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c) {
-        const int s = c & 1, k = c >> 1;
-        unsigned char *st = smem + s * STAGE_BYTES;
-        const uint64_t aw = ptx::sdesc(st + S_AW, 2048, 128);
-        const uint64_t kt = ptx::sdesc(st + S_KT, 128, 1024);
-        const uint64_t aq = ptx::sdesc(st + S_AQ, 2048, 128);
-        ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)(k & 1)) && ok;
-        ok = ptx::mbar_wait_bounded(hready, (uint32_t)(c & 1)) && ok;
-        ptx::tc_fence_after();
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & 1, k = c >> 1;
+      unsigned char *st = smem + s * STAGE_BYTES;
+      const uint64_t aw = ptx::sdesc(st + S_AW, 2048, 128);
+      const uint64_t kt = ptx::sdesc(st + S_KT, 128, 1024);
+      const uint64_t aq = ptx::sdesc(st + S_AQ, 2048, 128);
+      ok = ptx::mbar_wait_bounded(&fullA[s], (uint32_t)(k & 1)) && ok;
+      __syncwarp();
+      bar_sync(BAR_HREADY, BAR_HREADY_THREADS);  // h of this chunk is in H
+      ptx::tc_fence_after();
+      if (lane == 0) {
         // D1 = [-w ; q~] [h_hi | h_lo]
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           ptx::mma_bf16(dD1, adv(aw, ks * 4096), adv(dH0, ks * 256), id_kmn, ks > 0);
         ptx::mma_commit(d1);
-        ok = ptx::mbar_wait_bounded(vnready, (uint32_t)(c & 1)) && ok;
-        ptx::tc_fence_after();
+        ptx::mma_commit(&emptyA[s]);  // D1 no longer reads AW
+      }
+      ok = ptx::mbar_wait_bounded(&fullB[s], (uint32_t)(k & 1)) && ok;
+      __syncwarp();
+      bar_sync(BAR_VNREADY, BAR_VNREADY_THREADS);  // v_new is in VN
+      ptx::tc_fence_after();
+      if (lane == 0) {
         // DH = k~^T [vn_hi | vn_lo]  (critical path), then D5 = AQ [vn_hi | vn_lo]
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -889,12 +928,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         for (int ks = 0; ks < 4; ++ks)
           ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN0, ks * 256), id_kmn, ks > 0);
         ptx::mma_commit(d5);
-        ptx::mma_commit(&empty[s]);
+        ptx::mma_commit(&emptyB[s]);
       }
-      if (!ok) {
-        record_error(p.err, GDN_ERR_TIMEOUT);
-        *abort_flag = 1;
-      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      record_error(p.err, GDN_ERR_TIMEOUT);
+      *abort_flag = 1;
     }
   } else {
     // ---------------- epilogue warps 0-7: row r = TMEM lane, columns c0..c0+15
@@ -918,7 +958,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     store_pair16(Himg, r, c0, 2048, hs);
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(hready);
+    bar_arrive(BAR_HREADY, BAR_HREADY_THREADS);
 
     bool ok = true;
 #pragma unroll 1
@@ -926,7 +966,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       const int s = c & 1, k = c >> 1;
       const unsigned char *st = smem + s * STAGE_BYTES;
       const int L = min(BT, eos - bos - c * BT);
-      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)(k & 1)) && ok;
+      ok = ptx::mbar_wait_bounded(&fullA[s], (uint32_t)(k & 1)) && ok;
       const float *scs = reinterpret_cast<const float *>(st + S_SC);
       const float decay = scs[r];
       const float qs = r >= 64 ? scs[192 + r - 64] : 0.f;
@@ -937,11 +977,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         float d[16];
         tmem_ld_pair16(dD1 + lane_base, c0, d);
         if (r < 64) {
-          const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128 + c0 * 4);
+          const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128);
           float vn[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 u = u4[q];
+            const float4 u = u4[((c0 >> 2) + q) ^ (r & 7)];  // row-swizzled groups
             vn[4 * q] = u.x + d[4 * q];
             vn[4 * q + 1] = u.y + d[4 * q + 1];
             vn[4 * q + 2] = u.z + d[4 * q + 2];
@@ -951,14 +991,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(vnready);
+          bar_arrive(BAR_VNREADY, BAR_VNREADY_THREADS);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) qh[j] = d[j];
         }
       }
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp no longer reads stage s
+      if (lane == 0) ptx::mbar_arrive(&emptyA[s]);  // this warp no longer reads SC, U
       ok = ptx::mbar_wait_bounded(d3, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
       {
@@ -970,7 +1010,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(hready);
+        bar_arrive(BAR_HREADY, BAR_HREADY_THREADS);
       }
       ok = ptx::mbar_wait_bounded(d5, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
