@@ -300,8 +300,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   unsigned char *VS = smem + I_VS;
   float *Asm = reinterpret_cast<float *>(smem + I_R1);
   float *Tsm = Asm + 64 * SLD;
-  unsigned char *TW = smem + I_R1;   // Tw hi, Tw lo (after the solve)
-  unsigned char *AQ = smem + I_AQ;   // Aqk pair, later Tu hi, Tu lo
+  unsigned char *TH = smem + I_R1;   // [Tw ; Tu] hi (after the solve, 128 x 64, cs 2048)
+  unsigned char *AQ = smem + I_AQ;   // Aqk pair, later [Tw ; Tu] lo
   unsigned char *KB = VS;  // KDA: k e^-g, until the S GEMM is done
   // GDN staging for the row-major k | q | v tiles (48 KB): R1 + AQ, first
   // written by the gating
@@ -633,8 +633,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   if (tid == 0) ptx::bulk_wait_read<0>();
   __syncthreads();  // AQ and the k rows may be overwritten now
 
-  // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) -> TW hi | lo;
-  //      Tu = T diag(beta) -> AQ region hi | lo  (64 x 64 each, cs 1024)
+  // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) in rows 0..63 and
+  //      Tu = T diag(beta) in rows 64..127 of one 128 x 64 image per bf16 half
+  //      (hi in TH, lo in the AQ region; cs 2048), so that one M = 128 GEMM per
+  //      operand puts w and u in all four TMEM lane quarters
   for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
     const int i = pc & 63, cg = pc >> 6;
     const bool is_u = cg >= 8;
@@ -655,33 +657,34 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     }
     uint4 hi, lo;
     split8(v8, hi, lo);
-    unsigned char *dst = is_u ? AQ : TW;
-    *reinterpret_cast<uint4 *>(dst + img_off(i, j0, 1024)) = hi;
-    *reinterpret_cast<uint4 *>(dst + 8192 + img_off(i, j0, 1024)) = lo;
+    const int row = is_u ? 64 + i : i;
+    *reinterpret_cast<uint4 *>(TH + img_off(row, j0, 2048)) = hi;
+    *reinterpret_cast<uint4 *>(AQ + img_off(row, j0, 2048)) = lo;
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
 
-  // ---- w = Tw k (N = 128 keys) and u = Tu v (N = V), M = 64, K = 64 tokens,
-  //      each as hi + lo passes accumulating in TMEM
+  // ---- [Tw ; Tu] k (N = 128 keys) and [Tw ; Tu] v (N = V), M = 128, K = 64
+  //      tokens, hi + lo passes accumulating in TMEM: w = rows 0..63 of the
+  //      first, u = rows 64..127 of the second (the other halves are unused)
   const uint32_t dW = tmem, dU = tmem + 128;
   bool ok_v = true;
   if (tid == 0) {
     if (KDA) ok_v = ptx::mbar_wait_bounded(&bars[0], 1);  // v has landed
     ptx::tc_fence_after();
-    const uint32_t idw = ptx::idesc_bf16(64, 128, 0, 1);
-    const uint32_t idu = ptx::idesc_bf16(64, V, 0, 1);
+    const uint32_t idw = ptx::idesc_bf16(128, 128, 0, 1);
+    const uint32_t idu = ptx::idesc_bf16(128, V, 0, 1);
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
+      unsigned char *img = part ? AQ : TH;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t a = ptx::sdesc(img + ks * 4096, 2048, 128);
         const uint64_t b = ptx::sdesc(KQ + ks * 256, 128, 2048);
-        ptx::mma_bf16(dW, ptx::sdesc(TW + part * 8192 + ks * 2048, 1024, 128), b, idw,
-                      part > 0 || ks > 0);
+        ptx::mma_bf16(dW, a, b, idw, part > 0 || ks > 0);
         const uint64_t bv = ptx::sdesc(VS + ks * 256, 128, 1024);
-        ptx::mma_bf16(dU, ptx::sdesc(AQ + part * 8192 + ks * 2048, 1024, 128), bv, idu,
-                      part > 0 || ks > 0);
+        ptx::mma_bf16(dU, a, bv, idu, part > 0 || ks > 0);
       }
     }
     ptx::mma_commit(&bars[1]);
@@ -692,15 +695,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   mma_phase ^= 1;
   ptx::tc_fence_after();
   {
-    // M = 64 layout: row 16 qd + l lives in TMEM lane 32 qd + l (l < 16);
-    // -w replaces k in rows 0..63 of KQ (the WY GEMM has finished with it)
+    // M = 128 layout: row r lives in TMEM lane r.  Lane quarters 0-1 hold the
+    // w rows (keys split between the two warps of a quarter), quarters 2-3
+    // the u rows (value tiles split likewise).  -w replaces k in rows 0..63
+    // of KQ (the WY GEMM has finished with it).
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    const int i = qd * 16 + (lane & 15);
+    if (qd < 2) {
+      const int i = qd * 32 + lane;
 #pragma unroll 1
-    for (int q4 = 2 * hf; q4 < 2 * hf + 2; ++q4) {
-      float v[32];
-      ptx::tmem_ld32(dW + lane_base + q4 * 32, v);
-      if (lane < 16) {
+      for (int q4 = 2 * hf; q4 < 2 * hf + 2; ++q4) {
+        float v[32];
+        ptx::tmem_ld32(dW + lane_base + q4 * 32, v);
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           float out[8];
@@ -709,12 +714,12 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
           *reinterpret_cast<uint4 *>(KQ + img_off(i, q4 * 32 + q8 * 8, 2048)) = pack8(out);
         }
       }
-    }
+    } else {
+      const int i = (qd - 2) * 32 + lane;
 #pragma unroll 1
-    for (int t = hf; t < V / 32; t += 2) {
-      float v[32];
-      ptx::tmem_ld32(dU + lane_base + t * 32, v);
-      if (lane < 16) {
+      for (int t = hf; t < V / 32; t += 2) {
+        float v[32];
+        ptx::tmem_ld32(dU + lane_base + t * 32, v);
         // 16-byte group q of row i sits at group q ^ (i & 7), so that the
         // chain's per-row loads (one row per lane) hit eight different groups
         // in every quarter warp: no shared-memory bank conflicts
