@@ -730,18 +730,19 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
   }
-  // KQ is now the chain's A operand [-w ; q] (cs 2048)
+  // KQ is now the chain's A operand [-w ; q] (cs 2048).  The tensor memory is
+  // no longer read: free it before waiting on the store, so that the next
+  // CTA on this SM can allocate it while this one drains.
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc<256>(tmem);
   if (tid == 0) {
     ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
     ptx::bulk_commit();
     ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   }
   if (!(ok1 && ok2 && ok_v) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc<256>(tmem);
 }
 
 // ---------------------------------------------------------------------------
