@@ -3,7 +3,7 @@
 // The caller passes host buffers for every input and output and one device
 // buffer (the workspace) that receives device copies of them and the scratch
 // of the tensor-core kernels.  The problem is cut into pieces:
-//   * time pieces (fixed-length batches of sequences of more than 10
+//   * time pieces (fixed-length batches of sequences of more than 11
 //     64-token chunks): piece j holds tokens t0_j .. t1_j of every sequence,
 //     t0_j a multiple of 64, and the pieces shrink geometrically towards the
 //     end (see time_pieces);
@@ -40,7 +40,7 @@ namespace {
 
 constexpr int MAX_PIECES = 8;
 constexpr int MIN_PIECE_CHUNKS = 4;       // the last (shortest) time piece, in chunks
-constexpr double PIECE_GROWTH = 1.6;      // each time piece is this much longer than the next
+constexpr double PIECE_GROWTH = 2.0;      // each time piece is this much longer than the next
 constexpr int64_t PIECE_TOKENS = 2048;    // sequence piece: >= 2048 tokens
 constexpr int CHUNK = 64;
 constexpr int MAX_DEVICES = 64;

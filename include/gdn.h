@@ -128,7 +128,7 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *args, gdn_stream_t stream);
  * returns; o and ht are complete in host memory when `stream` has completed
  * (e.g. cudaStreamSynchronize).  Host buffers must stay valid and unchanged
  * until then.  Inside, the problem is cut into pieces of whole 64-token
- * chunks along time (sequences of more than 640 tokens; the pieces shrink
+ * chunks along time (sequences of more than 704 tokens; the pieces shrink
  * towards the end) or into ranges of whole sequences, and each piece's host->device copies, kernels
  * and device->host copies run on an internal copy-in stream, `stream` and an
  * internal copy-out stream, so the copies of one piece overlap the kernels of

@@ -39,25 +39,25 @@ def ws_size(lib, a):
 
 
 def test_time_cut_layout(lib):
-    # B=2, T=4096 (64 chunks): five time pieces shrinking by about 1.6 each
-    # towards a last piece of 4 chunks -> 27, 16, 10, 7, 4 chunks.  Each piece
-    # has its own q, k, v, o, g, beta slices; two whole fp32 states; and the
-    # tensor-core scratch of the largest piece (B=2, 27 chunks x 16 heads).
+    # B=2, T=4096 (64 chunks): four time pieces halving towards a last piece
+    # of 4 chunks -> 34, 17, 9, 4 chunks.  Each piece has its own q, k, v, o,
+    # g, beta slices; two whole fp32 states; and the tensor-core scratch of the
+    # largest piece (B=2, 34 chunks x 16 heads).
     st, n = ws_size(lib, args())
     assert st == Status.OK
-    chunks = (27, 16, 10, 7, 4)
+    chunks = (34, 17, 9, 4)
     rows = [2 * 64 * c for c in chunks]
     qk = sum(a256(r * 16 * 128 * 2) for r in rows)
     vo = sum(a256(r * 16 * 128 * 2) for r in rows)
     gb = sum(a256(r * 16 * 4) for r in rows)
     state = a256(2 * 16 * 128 * 128 * 4)
-    scratch = 256 + 2 * 27 * 16 * BLK128
+    scratch = 256 + 2 * 34 * 16 * BLK128
     assert n == 2 * qk + 2 * vo + 2 * gb + 2 * state + scratch
 
 
 @pytest.mark.parametrize("T,chunks", [
-    (641, (7, 4)),             # 11 chunks: the shortest sequence that is cut in time
-    (2100, (16, 11, 6)),       # ragged tail inside the last piece
+    (705, (8, 4)),             # 12 chunks: the shortest sequence that is cut in time
+    (2100, (19, 9, 5)),        # ragged tail inside the last piece
     (64 * 1000, None),         # at most 8 pieces
 ])
 def test_time_cut_piece_counts(lib, T, chunks):
@@ -75,10 +75,10 @@ def test_time_cut_piece_counts(lib, T, chunks):
         assert tight <= n <= tight + 6 * 8 * 256
 
 
-def test_640_tokens_are_cut_by_sequence(lib):
-    st, n = ws_size(lib, args(B=1, N=1, T=640, dtype=0, H=1, Hg=1, K=16, V=16))
+def test_704_tokens_are_cut_by_sequence(lib):
+    st, n = ws_size(lib, args(B=1, N=1, T=704, dtype=0, H=1, Hg=1, K=16, V=16))
     assert st == Status.OK
-    assert n == 2 * a256(640 * 64) * 2 + 2 * a256(640 * 4) + 2 * a256(16 * 16 * 4)
+    assert n == 2 * a256(704 * 64) * 2 + 2 * a256(704 * 4) + 2 * a256(16 * 16 * 4)
 
 
 def test_short_sequences_cut_by_batch(lib):

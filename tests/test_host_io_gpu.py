@@ -52,9 +52,9 @@ def _same(a, b, what):
 
 
 CASES = {
-    # B=2, T=4096: four time pieces, state handed on between them
+    # B=2, T=4096: four time pieces (34, 17, 9, 4 chunks), state handed on
     "time_cut_bench_shape": lambda: synth.prefill_inputs(61, 2, 4096, 16, 16, 128, 128, h0_std=0.1),
-    # T=2100 = 32 full chunks + a ragged tail of 52 tokens: two time pieces
+    # T=2100 = 32 full chunks + a ragged tail of 52 tokens: three time pieces
     "time_cut_ragged": lambda: synth.prefill_inputs(62, 1, 2100, 4, 2, 128, 64, h0_std=0.1),
     # 16 short sequences: four pieces of four whole sequences
     "batch_cut": lambda: synth.prefill_inputs(63, 16, 512, 8, 4, 128, 128, h0_std=0.1),
