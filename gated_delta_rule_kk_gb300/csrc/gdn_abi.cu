@@ -72,12 +72,21 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
     REQUIRE(B == 1, GDN_ERR_INVALID_ARG, "with cu_seqlens B must be 1 (got %d)", B);
   }
   if (sizes_only) return GDN_OK;
-  REQUIRE_PTR(q, "q");
-  REQUIRE_PTR(k, "k");
-  REQUIRE_PTR(v, "v");
-  REQUIRE_PTR(g, "g");
-  REQUIRE_PTR(beta, "beta");
-  REQUIRE_PTR(o, "o");
+  if (T > 0) {
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(g, "g");
+    REQUIRE_PTR(beta, "beta");
+    REQUIRE_PTR(o, "o");
+  } else {  // no token is read or written: the per-token arrays may be NULL
+    REQUIRE_OPT_PTR(q, "q");
+    REQUIRE_OPT_PTR(k, "k");
+    REQUIRE_OPT_PTR(v, "v");
+    REQUIRE_OPT_PTR(g, "g");
+    REQUIRE_OPT_PTR(beta, "beta");
+    REQUIRE_OPT_PTR(o, "o");
+  }
   REQUIRE_OPT_PTR(h0, "h0");
   REQUIRE_OPT_PTR(ht, "ht");
   REQUIRE_OPT_PTR(cu, "cu_seqlens");

@@ -325,7 +325,7 @@ extern "C" gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *a, gdn_stream_t
       {a->cu_seqlens, "cu_seqlens", false}};
   char msg[96];
   for (const auto &h : host) {
-    if (h.p == nullptr && h.required) {
+    if (h.p == nullptr && h.required && a->T > 0) {  // T = 0: no token array is touched
       snprintf(msg, sizeof(msg), "%s must not be NULL", h.name);
       return set_host_error(GDN_ERR_INVALID_ARG, msg);
     }

@@ -82,7 +82,9 @@ typedef enum gdn_dtype {
  *                                     tokens cu_seqlens[n] .. cu_seqlens[n+1]
  *                                     (0 = cu_seqlens[0] <= ... <= cu_seqlens[N]
  *                                     = T, checked on the device)
- * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, H % Hg == 0.
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, H % Hg == 0.  With T == 0
+ * nothing per token is read or written, so q, k, v, g, beta and o may be NULL
+ * (ht = h0, or zeros).
  * scale <= 0 selects 1/sqrt(K).
  * Workspace: bf16 inputs with K == 128 and V a multiple of 32 up to 128 run on
  * the tensor cores and need `workspace` (device, 256-byte aligned,
@@ -163,7 +165,8 @@ gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *b
  *   beta   [B, T, HV]     float32
  *   h0, ht [N, HV, K, V]  float32     as for GDN
  *   cu_seqlens            as for GDN
- * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0.
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0.  With T == 0
+ * q, k, v, g, beta and o may be NULL (ht = h0, or zeros).
  * Workspace: as for GDN (tensor cores for bf16, K == 128, V % 32 == 0,
  * V <= 128; kda_chunk_workspace_size() bytes).
  */

@@ -121,3 +121,28 @@ def test_varlen_gqa_workload_sampled():
         s, e = cu[n], cu[n + 1]
         assert_close(o[0, s:e, h], o_ref[0, s:e, h], TOL_BF16, f"o seq {n} head {h}")
         assert_close(ht[n, h], ht_ref[n, h], TOL_BF16, f"ht seq {n} head {h}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_zero_length_batch_returns_the_initial_state(dtype):
+    # T = 0: no token is read or written (the empty tensors' pointers are NULL);
+    # the final state is the initial state, or zeros without one
+    import gated_delta_rule_kk_gb300 as gdn
+    B, H, Hg, K, V = 3, 4, 2, 128, 128
+    q = torch.empty((B, 0, Hg, K), dtype=dtype, device="cuda")
+    v = torch.empty((B, 0, H, V), dtype=dtype, device="cuda")
+    g = torch.empty((B, 0, H), dtype=torch.float32, device="cuda")
+    h0 = torch.randn((B, H, K, V), generator=torch.Generator().manual_seed(5)).cuda()
+    o, ht = gdn_chunk_fwd(q, q, v, g, g, initial_state=h0)
+    torch.cuda.synchronize()
+    assert gdn_check_device_error() == Status.OK
+    assert tuple(o.shape) == (B, 0, H, V)
+    assert torch.equal(ht, h0)
+    _, ht0 = gdn_chunk_fwd(q, q, v, g, g)
+    torch.cuda.synchronize()
+    assert torch.equal(ht0, torch.zeros_like(h0))
+    o_h, ht_h = gdn.gdn_chunk_fwd_host(q.cpu(), q.cpu(), v.cpu(), g.cpu(), g.cpu(),
+                                       initial_state=h0.cpu())
+    torch.cuda.synchronize()
+    assert tuple(o_h.shape) == (B, 0, H, V)
+    assert torch.equal(ht_h, h0.cpu())

@@ -84,3 +84,17 @@ def test_kda_prefill_workload_sampled():
         o_ref, ht_ref = run_oracle(inp, heads=[h], seqs=[0])
         assert_close(o[0, :, h], o_ref[0, :, h], TOL_BF16, f"o head {h}")
         assert_close(ht[0, h], ht_ref[0, h], TOL_BF16, f"ht head {h}")
+
+
+def test_zero_length_batch_returns_the_initial_state():
+    B, H, K, V = 2, 4, 128, 64
+    q = torch.empty((B, 0, H, K), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((B, 0, H, V), dtype=torch.bfloat16, device="cuda")
+    g = torch.empty((B, 0, H, K), dtype=torch.float32, device="cuda")
+    beta = torch.empty((B, 0, H), dtype=torch.float32, device="cuda")
+    h0 = torch.randn((B, H, K, V), generator=torch.Generator().manual_seed(6)).cuda()
+    o, ht = kda_chunk_fwd(q, q, v, g, beta, initial_state=h0)
+    torch.cuda.synchronize()
+    assert gdn_check_device_error() == Status.OK
+    assert tuple(o.shape) == (B, 0, H, V)
+    assert torch.equal(ht, h0)
