@@ -316,7 +316,7 @@ def run_ours(args, rank, world, dev):
                          "algorithmic_bytes": kb, "algorithmic_flops": kf,
                          "traffic": traffic_record("kda_chunk")}}
         del kd, ko, kht, kin
-        for T in (1, 2, 4):
+        for T in (1, 2, 3, 4):
             din = synth.decode(T)
             dd = to_dev(din, dev)
             m = din["dims"]
