@@ -316,6 +316,29 @@ def run_ours(args, rank, world, dev):
                          "algorithmic_bytes": kb, "algorithmic_flops": kf,
                          "traffic": traffic_record("kda_chunk")}}
         del kd, ko, kht, kin
+        # packed sequences with grouped heads: 8 lengths in [64, 8192], Hg=4, H=16
+        vin = synth.varlen_gqa()
+        vm = vin["dims"]
+        vd = to_dev(vin, dev)
+        vo = torch.empty_like(vd["v"])
+        vht = torch.empty((vm["N"], vm["H"], vm["K"], vm["V"]), dtype=torch.float32, device=dev)
+        vms = time_steps(lambda: gdn.gdn_chunk_fwd(vd["q"], vd["k"], vd["v"], vd["g"], vd["beta"],
+                                                   scale=vd["scale"], cu_seqlens=vd["cu_seqlens"],
+                                                   out=vo, final_state=vht),
+                         rsteps, max(3, args.warmup // 2), flush, stream)
+        vt = statistics.mean(vms)
+        vtok = vm["B"] * vm["T"]
+        vb = gdn_bytes(vm["B"], vm["T"], vm["H"], vm["Hg"], vm["K"], vm["V"], vm["N"], h0=False)
+        vf = chunk_flops(vm["B"], vm["T"], vm["H"], vm["K"], vm["V"])
+        lens = (vd["cu_seqlens"][1:] - vd["cu_seqlens"][:-1]).tolist()
+        rows["gdn_varlen"] = {
+            "workload": f"GDN varlen GQA prefill: {vm['N']} packed sequences, lengths {lens} "
+                        f"(sum {vtok}), Hg=4, H=16, K=V=128, bf16, h0=0, ht returned",
+            "tokens_per_s": vtok / (vt / 1e3), "ms_per_call": vt,
+            "roofline": {"bound": "hbm", "achieved": vb / (vt / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": vb / (vt / 1e3) / 1e9 / hbm,
+                         "algorithmic_bytes": vb, "algorithmic_flops": vf, "traffic": None}}
+        del vd, vo, vht, vin
         for T in (1, 2, 3, 4):
             din = synth.decode(T)
             dd = to_dev(din, dev)

@@ -49,3 +49,34 @@ def chain_outputs(S0, g, beta, q, k, v, scale):
     for t in range(1, T + 1):
         o[t - 1] = scale * state_after(S0, g, beta, k, v, t) @ q[t - 1]
     return o, state_after(S0, g, beta, k, v, T)
+
+
+def linear_state_after(h0, decay_k, decay_v, k, v, t):
+    """State of the gated linear-attention recurrence h <- Dk_s h Dv_s + k_s v_s^T
+    after tokens ``0..t-1``, multiplied out (no stepping):
+
+        h_t = (Dk_t ... Dk_1) h0 (Dv_1 ... Dv_t)
+              + sum_{j<t} (Dk_t ... Dk_{j+1}) k_j v_j^T (Dv_{j+1} ... Dv_t)
+
+    ``decay_k[s]`` (K) and ``decay_v[s]`` (V) are the diagonals of token s's
+    key-side and value-side decay (the scalar and per-head gates put the same
+    factor on every key channel and ones on the value side).
+    """
+    K, V = h0.shape
+
+    def left(a, b):  # Dk_{b-1} ... Dk_a
+        P = np.eye(K)
+        for s in range(a, b):
+            P = np.diag(decay_k[s]) @ P
+        return P
+
+    def right(a, b):  # Dv_a ... Dv_{b-1}
+        P = np.eye(V)
+        for s in range(a, b):
+            P = P @ np.diag(decay_v[s])
+        return P
+
+    h = left(0, t) @ h0 @ right(0, t)
+    for j in range(t):
+        h = h + left(j + 1, t) @ np.outer(k[j], v[j]) @ right(j + 1, t)
+    return h

@@ -1,0 +1,91 @@
+"""Chunk state pass of gated linear attention, token by token, fp64.
+
+This module is part of the oracle, which is test infrastructure: only tests,
+the smoke check and the CPU legs of the benchmark use it.  It shares no code
+with the CUDA library.
+
+The KDA ``_fla/ops/common/chunk_h.py`` page (``chunk_fwd_kernel_h`` and its
+host wrapper ``chunk_fwd_h``) computes, for every sequence and head, the state
+``h`` (``[K, V]``) at the start of every chunk of ``chunk_size`` tokens and,
+optionally, the final state, for the gated linear-attention recurrence
+
+    h <- decay_t(h) + k_t v_t^T          (token t, after the decay)
+
+with one of these decays (the page's kernel works in base 2; the gates here
+are natural logarithms, as everywhere in this library):
+
+    "g"        e^{r_t} h            r_t per token and head
+    "g_gamma"  e^{gamma_h} h        one rate per head, the same for every token
+    "gk"       diag(e^{r_t}) h      r_t per token, head and key channel
+    "gv"       h diag(e^{r_t})      r_t per token, head and value channel
+    None       h                    no decay
+
+The per-token gates ``g``, ``gk``, ``gv`` are taken the way the page's kernel
+takes them: as inclusive cumulative sums inside each chunk (chunks counted
+from each sequence's first token); the raw per-token rate ``r_t`` is recovered
+by differencing inside a chunk.  ``g_gamma`` is the raw rate itself (the
+page's kernel forms the in-chunk cumulative sum ``gamma * (i + 1)``).
+
+Output layout: the chunk states of all sequences one after another, sequence
+n contributing ceil(len_n / chunk_size) entries -- for B equal sequences of T
+tokens that is ``[B, NT, H, K, V]`` flattened over (B, NT).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .recurrence import _f64, raw_gate_from_chunk_cumsum, sequence_bounds
+
+GATES = (None, "g", "g_gamma", "gk", "gv")
+
+
+def chunk_counts(B: int, T: int, cu_seqlens=None, chunk_size: int = 64):
+    """Number of chunks of every sequence (0 for an empty one)."""
+    return [-(-(eos - bos) // chunk_size) for _, bos, eos in sequence_bounds(B, T, cu_seqlens)]
+
+
+def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None,
+                     chunk_size: int = 64):
+    """Chunk-start states ``hs`` ``[sum NT_n, H, K, V]`` and final states
+    ``ht`` ``[N, H, K, V]`` of the gated linear-attention recurrence.
+
+    k ``[B, T, H, K]``, v ``[B, T, H, V]``; gate_values: ``g`` ``[B, T, H]``,
+    ``g_gamma`` ``[H]``, ``gk`` ``[B, T, H, K]``, ``gv`` ``[B, T, H, V]``
+    (chunk-local cumulative sums except ``g_gamma``); h0 ``[N, H, K, V]`` or
+    None (zeros).
+    """
+    if gate not in GATES:
+        raise ValueError(f"unknown gate {gate!r}")
+    k, v = _f64(k), _f64(v)
+    B, T, H, K = k.shape
+    V = v.shape[3]
+    gv_ = _f64(gate_values)
+    seqs = sequence_bounds(B, T, cu_seqlens)
+    N = len(seqs)
+    h0 = np.zeros((N, H, K, V)) if h0 is None else _f64(h0)
+    counts = chunk_counts(B, T, cu_seqlens, chunk_size)
+    hs = np.zeros((sum(counts), H, K, V))
+    ht = np.zeros((N, H, K, V))
+    first = 0
+    for n, (b, bos, eos) in enumerate(seqs):
+        raw = None
+        if gate in ("g", "gk", "gv"):
+            raw = raw_gate_from_chunk_cumsum(gv_[b], bos, eos, chunk_size)
+        for h in range(H):
+            S = h0[n, h].copy()
+            for t in range(bos, eos):
+                i = t - bos
+                if i % chunk_size == 0:
+                    hs[first + i // chunk_size, h] = S
+                if gate == "g":
+                    S = np.exp(raw[t, h]) * S
+                elif gate == "g_gamma":
+                    S = np.exp(gv_[h]) * S
+                elif gate == "gk":
+                    S = np.exp(raw[t, h])[:, None] * S
+                elif gate == "gv":
+                    S = S * np.exp(raw[t, h])[None, :]
+                S = S + np.outer(k[b, t, h], v[b, t, h])
+            ht[n, h] = S
+        first += counts[n]
+    return hs, ht

@@ -1,0 +1,122 @@
+"""Pins of the chunk-state-pass oracle (gated linear attention, chunk_h page).
+
+The oracle steps the recurrence token by token; these tests tie it to things
+it does not compute that way: the multiplied-out closed form of the state,
+the reductions between gate kinds (a per-head constant rate is a per-token
+gate with equal values; a per-channel gate constant across its channels is the
+scalar gate), and what the chunk-start states mean (the first is h0, a
+sequence resumed from a chunk-start state continues the same run).
+"""
+import numpy as np
+import pytest
+
+from oracle import brute
+from oracle import state_pass as SP
+
+
+
+def _inputs(seed, B, T, H, K, V):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((B, T, H, K))
+    v = rng.standard_normal((B, T, H, V))
+    raw_g = -np.abs(rng.standard_normal((B, T, H))) * 0.3
+    raw_gk = -np.abs(rng.standard_normal((B, T, H, K))) * 0.3
+    raw_gv = -np.abs(rng.standard_normal((B, T, H, V))) * 0.3
+    h0 = rng.standard_normal((B, H, K, V))
+    return k, v, raw_g, raw_gk, raw_gv, h0
+
+
+def _chunk_cumsum(raw, chunk):
+    out = np.empty_like(raw)
+    T = raw.shape[1]
+    for c in range(0, T, chunk):
+        out[:, c:c + chunk] = np.cumsum(raw[:, c:c + chunk], axis=1)
+    return out
+
+
+@pytest.mark.parametrize("gate", SP.GATES)
+def test_final_state_matches_closed_form(gate):
+    B, T, H, K, V, chunk = 1, 7, 2, 3, 4, 3
+    k, v, rg, rgk, rgv, h0 = _inputs(1, B, T, H, K, V)
+    gamma = np.array([-0.2, -0.05])
+    vals = {None: None, "g": _chunk_cumsum(rg, chunk), "g_gamma": gamma,
+            "gk": _chunk_cumsum(rgk, chunk), "gv": _chunk_cumsum(rgv, chunk)}[gate]
+    hs, ht = SP.chunk_state_pass(k, v, gate, vals, h0=h0, chunk_size=chunk)
+    for h in range(H):
+        dk = np.ones((T, K))
+        dv = np.ones((T, V))
+        if gate == "g":
+            dk = np.repeat(np.exp(rg[0, :, h])[:, None], K, axis=1)
+        elif gate == "g_gamma":
+            dk = np.full((T, K), np.exp(gamma[h]))
+        elif gate == "gk":
+            dk = np.exp(rgk[0, :, h])
+        elif gate == "gv":
+            dv = np.exp(rgv[0, :, h])
+        ref_t = brute.linear_state_after(h0[0, h], dk, dv, k[0, :, h], v[0, :, h], T)
+        np.testing.assert_allclose(ht[0, h], ref_t, rtol=1e-12, atol=1e-12)
+        for c in range(hs.shape[0]):  # chunk starts at tokens 0, 3, 6
+            ref_c = brute.linear_state_after(h0[0, h], dk, dv, k[0, :, h], v[0, :, h], c * chunk)
+            np.testing.assert_allclose(hs[c, h], ref_c, rtol=1e-12, atol=1e-12)
+
+
+def test_gate_kinds_reduce_to_each_other():
+    B, T, H, K, V, chunk = 2, 13, 3, 4, 5, 4
+    k, v, rg, _, _, h0 = _inputs(2, B, T, H, K, V)
+    g = _chunk_cumsum(rg, chunk)
+    ref = SP.chunk_state_pass(k, v, "g", g, h0=h0, chunk_size=chunk)
+    gk = np.repeat(g[..., None], K, axis=3)
+    gv = np.repeat(g[..., None], V, axis=3)
+    for gate, vals in (("gk", gk), ("gv", gv)):
+        got = SP.chunk_state_pass(k, v, gate, vals, h0=h0, chunk_size=chunk)
+        np.testing.assert_allclose(got[0], ref[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(got[1], ref[1], rtol=1e-12, atol=1e-12)
+    # a per-head constant rate is the per-token gate with that value everywhere
+    gamma = np.array([-0.3, -0.01, 0.0])
+    const = _chunk_cumsum(np.broadcast_to(gamma, (B, T, H)).copy(), chunk)
+    a = SP.chunk_state_pass(k, v, "g_gamma", gamma, h0=h0, chunk_size=chunk)
+    b = SP.chunk_state_pass(k, v, "g", const, h0=h0, chunk_size=chunk)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12, atol=1e-12)
+    # no gate is a zero gate
+    a = SP.chunk_state_pass(k, v, None, None, h0=h0, chunk_size=chunk)
+    b = SP.chunk_state_pass(k, v, "g", np.zeros_like(g), h0=h0, chunk_size=chunk)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12, atol=1e-12)
+
+
+def test_chunk_starts_resume_the_run_and_packed_sequences_are_separate_runs():
+    B, T, H, K, V, chunk = 1, 20, 2, 3, 3, 4
+    k, v, _, rgk, _, h0 = _inputs(3, B, T, H, K, V)
+    gk = _chunk_cumsum(rgk, chunk)
+    hs, ht = SP.chunk_state_pass(k, v, "gk", gk, h0=h0, chunk_size=chunk)
+    assert hs.shape == (5, H, K, V)
+    np.testing.assert_array_equal(hs[0], h0[0])
+    # resuming at chunk 3 (token 12) from its chunk-start state gives the same end
+    rs, rt = SP.chunk_state_pass(k[:, 12:], v[:, 12:], "gk", gk[:, 12:], h0=hs[3][None],
+                                 chunk_size=chunk)
+    np.testing.assert_allclose(rt, ht, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(rs, hs[3:], rtol=1e-12, atol=1e-12)
+    # packed sequences (one empty) = separate runs, chunk states one after another
+    lens = [6, 0, 9, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    rng = np.random.default_rng(4)
+    kk = rng.standard_normal((1, cu[-1], H, K))
+    vv = rng.standard_normal((1, cu[-1], H, V))
+    raw = -np.abs(rng.standard_normal((1, cu[-1], H)))
+    gg = np.empty_like(raw)
+    for n in range(len(lens)):
+        for c in range(cu[n], cu[n + 1], chunk):
+            e = min(c + chunk, cu[n + 1])
+            gg[:, c:e] = np.cumsum(raw[:, c:e], axis=1)
+    hh0 = rng.standard_normal((len(lens), H, K, V))
+    hs_p, ht_p = SP.chunk_state_pass(kk, vv, "g", gg, h0=hh0, cu_seqlens=cu, chunk_size=chunk)
+    assert hs_p.shape[0] == sum(-(-n // chunk) for n in lens)
+    first = 0
+    for n in range(len(lens)):
+        a, b = cu[n], cu[n + 1]
+        s_n, t_n = SP.chunk_state_pass(kk[:, a:b], vv[:, a:b], "g", gg[:, a:b], h0=hh0[n][None],
+                                       chunk_size=chunk)
+        np.testing.assert_allclose(ht_p[n], t_n[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(hs_p[first:first + s_n.shape[0]], s_n, rtol=1e-12, atol=1e-12)
+        first += s_n.shape[0]
+    np.testing.assert_array_equal(ht_p[1], hh0[1])  # the empty sequence keeps its state
