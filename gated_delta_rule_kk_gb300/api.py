@@ -11,7 +11,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import DType, GdnChunkArgs, GdnDecodeArgs, KdaChunkArgs
+from ._lib import DType, GateKind, GdnChunkArgs, GdnDecodeArgs, GdnStateArgs, KdaChunkArgs
 
 CHUNK = 64
 
@@ -301,3 +301,68 @@ def gdn_check_device_error(stream=None):
     _lib.check(lib.gdn_check_device_error(_stream(stream), ctypes.byref(code)),
                "gdn_check_device_error")
     return _lib.Status(code.value)
+
+
+_GATES = {None: GateKind.NONE, "g": GateKind.G, "g_gamma": GateKind.G_GAMMA, "gk": GateKind.GK,
+          "gv": GateKind.GV}
+
+
+def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, cu_seqlens=None,
+                        output_final_state=True, output_states=True,
+                        states_dtype=torch.float32, out_states=None, final_state=None,
+                        num_chunks=None, stream=None):
+    """Chunk state pass of gated linear attention.  Returns ``(hs, ht)``.
+
+    k [B,T,H,K], v [B,T,H,V] (float32 or bfloat16); gate one of None, "g"
+    ([B,T,H]), "g_gamma" ([H]), "gk" ([B,T,H,K]), "gv" ([B,T,H,V]) with
+    ``gate_values`` float32 (chunk-local cumulative sums except g_gamma);
+    initial_state [N,H,K,V] float32.  hs holds the state at the start of every
+    64-token chunk, sequence after sequence ([C,H,K,V]); with ``cu_seqlens``
+    and no ``num_chunks``, C is read from the lengths (a device sync).
+    """
+    dev = k.device
+    dt, dts = _io_dtype(k)
+    _need(k, "k", dts, dev)
+    _need(v, "v", dts, dev)
+    if gate not in _GATES:
+        raise ValueError(f"gate must be one of {list(_GATES)}")
+    if gate is not None:
+        _need(gate_values, "gate_values", (torch.float32,), dev)
+    B, T, H, K = k.shape
+    V = v.shape[3]
+    if v.shape[:3] != (B, T, H):
+        raise ValueError("k must be [B,T,H,K] and v [B,T,H,V]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+        N = cu_seqlens.numel() - 1
+        if num_chunks is None and (output_states or out_states is not None):
+            lens = (cu_seqlens[1:] - cu_seqlens[:-1]).clamp(min=0).to(torch.int64)
+            num_chunks = int(((lens + CHUNK - 1) // CHUNK).sum().item())
+    else:
+        N = B
+        if num_chunks is None:
+            num_chunks = B * ((T + CHUNK - 1) // CHUNK)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", (torch.float32,), dev)
+        if tuple(initial_state.shape) != (N, H, K, V):
+            raise ValueError(f"initial_state must be [{N},{H},{K},{V}]")
+    hs = out_states
+    if hs is None and output_states:
+        hs = torch.empty((num_chunks, H, K, V), dtype=states_dtype, device=dev)
+    if hs is not None:
+        _need(hs, "out_states", (torch.float32, torch.bfloat16), dev)
+    ht = final_state
+    if ht is None and output_final_state:
+        ht = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+    elif ht is not None:
+        _need(ht, "final_state", (torch.float32,), dev)
+    a = GdnStateArgs(dtype=int(dt), k=_ptr(k), v=_ptr(v), gate=int(_GATES[gate]),
+                     gate_values=_ptr(gate_values) if gate is not None else None,
+                     h0=_ptr(initial_state), ht=_ptr(ht), hs=_ptr(hs),
+                     hs_dtype=int(DType.BF16 if hs is not None and hs.dtype == torch.bfloat16
+                                  else DType.F32),
+                     cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, K=K, V=V, N=N,
+                     chunk_size=CHUNK, num_chunks=int(num_chunks or 0))
+    lib = _lib.load()
+    _lib.check(lib.gdn_chunk_state_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_fwd")
+    return hs, ht

@@ -35,10 +35,26 @@ struct DecodeParams {
   float scale, softplus_beta, softplus_threshold, eps;
 };
 
+// One chunk-state-pass problem (gated linear attention), already validated.
+struct StateParams {
+  const void *k, *v;
+  int gate;                   // gdn_gate_kind_t
+  const float *gate_values;
+  const float *h0;
+  float *ht;
+  void *hs;                   // chunk-start states or NULL
+  int hs_bf16;
+  const int32_t *cu_seqlens;
+  int *err;
+  int B, T, H, K, V, N;
+  long long num_chunks;       // capacity of hs in chunks
+};
+
 // Each launcher enqueues its kernel(s) and returns the launch status.
 cudaError_t launch_chunk_simt(const ChunkParams &p, bool bf16, bool per_channel_gate,
                               cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_state_pass(const StateParams &p, bool bf16, cudaStream_t stream);
 // The decode step on the warp-level tensor cores (K = V = 128).
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 

@@ -135,6 +135,48 @@ def decode_inputs(seed, B, T, H, HV, K, V, pool=None, state_std=0.05,
     }
 
 
+def state_pass_inputs(seed, B, T, H, K, V, gate, dtype=torch.bfloat16, lengths=None,
+                      h0_std=None, chunk=64):
+    """Inputs of one chunk state pass (gated linear attention).
+
+    k ~ N(0, 1) L2-normalised per token, v ~ N(0, 1); the gate's per-token
+    rates are logsigmoid(N(0, 1) + 3) ("g": per token and head, "gk": per key
+    channel, "gv": per value channel), given as chunk-local inclusive
+    cumulative sums (chunks of ``chunk`` tokens from each sequence start);
+    "g_gamma" is one logsigmoid(N(0, 1) + 3) per head; None draws no gate.
+    Draw order: k, v, gate, h0.
+    """
+    rng = np.random.default_rng(seed)
+    if lengths is not None:
+        assert B == 1 and sum(lengths) == T
+    k = _unit_rows(rng.standard_normal((B, T, H, K)))
+    v = rng.standard_normal((B, T, H, V))
+    shape = {"g": (B, T, H), "gk": (B, T, H, K), "gv": (B, T, H, V), "g_gamma": (H,)}
+    gv = None
+    if gate is not None:
+        raw = _logsigmoid(rng.standard_normal(shape[gate]) + GATE_SHIFT_SCALAR)
+        if gate == "g_gamma":
+            gv = raw
+        else:
+            cu = np.concatenate([[0], np.cumsum(lengths)]) if lengths is not None else [0, T]
+            raw = raw.astype(np.float32)
+            gv = np.empty_like(raw)
+            for s0, e0 in zip(cu[:-1], cu[1:]):
+                for c in range(int(s0), int(e0), chunk):
+                    ce = min(c + chunk, int(e0))
+                    gv[:, c:ce] = np.cumsum(raw[:, c:ce], axis=1, dtype=np.float32)
+    N = len(lengths) if lengths is not None else B
+    h0 = None if h0_std is None else rng.standard_normal((N, H, K, V)) * h0_std
+    return {
+        "k": _t(k, dtype), "v": _t(v, dtype), "gate": gate,
+        "gate_values": None if gv is None else _t(gv, torch.float32),
+        "h0": None if h0 is None else _t(h0, torch.float32),
+        "cu_seqlens": None if lengths is None else torch.from_numpy(
+            np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)),
+        "dims": dict(B=B, T=T, H=H, K=K, V=V, N=N),
+    }
+
+
 # ---- the named workloads -------------------------------------------------
 
 def tiny():

@@ -148,6 +148,60 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *args, gdn_stream_t stream);
  */
 gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *args, gdn_stream_t stream);
 
+/*
+ * Chunk state pass of gated linear attention (KDA _fla/ops/common/chunk_h.py:
+ * chunk_fwd_kernel_h / chunk_fwd_h, "h += k^T v" with an optional decay).
+ * For every sequence n and head h the state h [K, V] starts at h0 (or zeros)
+ * and takes, token by token,
+ *     h <- Dk_t h Dv_t + k_t v_t^T
+ * where the decay depends on `gate` (natural-log gates):
+ *   GDN_GATE_NONE      Dk = Dv = I                       gate_values NULL
+ *   GDN_GATE_G         Dk = e^{r_t} I                    gate_values [B,T,H]
+ *   GDN_GATE_G_GAMMA   Dk = e^{gamma_h} I, every token   gate_values [H]
+ *   GDN_GATE_GK        Dk = diag(e^{r_t[:]}) (keys)      gate_values [B,T,H,K]
+ *   GDN_GATE_GV        Dv = diag(e^{r_t[:]}) (values)    gate_values [B,T,H,V]
+ * The per-token gates are given as the page's kernel takes them: inclusive
+ * cumulative sums of r_t inside each 64-token chunk (chunks counted from each
+ * sequence's first token); g_gamma is the per-token rate itself.
+ *   k [B,T,H,K], v [B,T,H,V]   dtype (GDN_F32 or GDN_BF16)
+ *   h0, ht [N,H,K,V]           float32, NULL = zeros / not returned
+ *   hs [C,H,K,V]               hs_dtype (GDN_F32 or GDN_BF16): the state at the
+ *                              start of every chunk, sequence after sequence
+ *                              (sequence n contributes ceil(len_n / 64)
+ *                              entries; B equal sequences: [B, ceil(T/64), ...]);
+ *                              NULL = not returned; num_chunks = C, its capacity
+ *   cu_seqlens [N + 1] int32   as gdn_chunk_fwd (device memory; checked on the
+ *                              device, GDN_ERR_BAD_SEQLENS also when the chunks
+ *                              do not fit num_chunks)
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64.  Arithmetic in fp32 (bf16
+ * inputs are widened).  Nothing is allocated; no workspace.
+ */
+typedef enum gdn_gate_kind {
+  GDN_GATE_NONE = 0,
+  GDN_GATE_G = 1,
+  GDN_GATE_G_GAMMA = 2,
+  GDN_GATE_GK = 3,
+  GDN_GATE_GV = 4
+} gdn_gate_kind_t;
+
+typedef struct gdn_state_args {
+  int32_t dtype;               /* gdn_dtype_t of k, v */
+  const void *k, *v;
+  int32_t gate;                /* gdn_gate_kind_t */
+  const float *gate_values;
+  const float *h0;
+  float *ht;
+  void *hs;
+  int32_t hs_dtype;            /* gdn_dtype_t of hs */
+  const int32_t *cu_seqlens;
+  int32_t B, T, H, K, V, N;
+  int32_t chunk_size;
+  int64_t num_chunks;
+} gdn_state_args;
+
+/* Enqueue the chunk state pass on `stream`. */
+gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *args, gdn_stream_t stream);
+
 /* Bytes of device workspace gdn_chunk_fwd_host needs for these arguments.
  * Reads sizes, dtype and, when given, the host array cu_seqlens. */
 gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *bytes);

@@ -15,7 +15,7 @@ import tempfile
 import pytest
 
 from gated_delta_rule_kk_gb300 import _lib, build_lib
-from gated_delta_rule_kk_gb300._lib import GdnChunkArgs, GdnDecodeArgs, KdaChunkArgs, Status
+from gated_delta_rule_kk_gb300._lib import GdnChunkArgs, GdnDecodeArgs, GdnStateArgs, KdaChunkArgs, Status
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
@@ -65,13 +65,14 @@ int main(void) {
   printf("gdn_chunk_args size %zu\n", sizeof(gdn_chunk_args));
   printf("kda_chunk_args size %zu\n", sizeof(kda_chunk_args));
   printf("gdn_decode_args size %zu\n", sizeof(gdn_decode_args));
+  printf("gdn_state_args size %zu\n", sizeof(gdn_state_args));
   %FIELDS%
   return 0;
 }
 """
     lines = []
     for cname, cls in (("gdn_chunk_args", GdnChunkArgs), ("kda_chunk_args", KdaChunkArgs),
-                       ("gdn_decode_args", GdnDecodeArgs)):
+                       ("gdn_decode_args", GdnDecodeArgs), ("gdn_state_args", GdnStateArgs)):
         for fname, _ in cls._fields_:
             lines.append(f"F({cname}, {fname})")
     src = probe.replace("%FIELDS%", "\n  ".join(lines))
@@ -87,7 +88,7 @@ int main(void) {
             s, f, v = ln.split()
             got[(s, f)] = int(v)
     for cname, cls in (("gdn_chunk_args", GdnChunkArgs), ("kda_chunk_args", KdaChunkArgs),
-                       ("gdn_decode_args", GdnDecodeArgs)):
+                       ("gdn_decode_args", GdnDecodeArgs), ("gdn_state_args", GdnStateArgs)):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for fname, _ in cls._fields_:
             assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
@@ -201,3 +202,32 @@ def test_workspace_errors_found_on_host(lib):
     assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.WORKSPACE
     a = good_chunk(workspace=FAKE + 16, workspace_bytes=1 << 30)
     assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.MISALIGNED
+
+
+def good_state(**kw):
+    a = dict(dtype=1, k=FAKE, v=FAKE, gate=1, gate_values=FAKE, h0=None, ht=None, hs=FAKE,
+             hs_dtype=0, cu_seqlens=None, B=2, T=130, H=4, K=128, V=64, N=2, chunk_size=64,
+             num_chunks=6)
+    a.update(kw)
+    return GdnStateArgs(**a)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(dtype=5), Status.INVALID_ARG),
+    (dict(gate=7), Status.INVALID_ARG),
+    (dict(gate=0), Status.INVALID_ARG),            # gate values without a gate
+    (dict(gate_values=None), Status.INVALID_ARG),   # a gate without values
+    (dict(k=None), Status.INVALID_ARG),
+    (dict(v=FAKE + 4), Status.MISALIGNED),
+    (dict(K=256), Status.UNSUPPORTED),
+    (dict(chunk_size=32), Status.UNSUPPORTED),
+    (dict(N=3), Status.INVALID_ARG),
+    (dict(cu_seqlens=FAKE), Status.INVALID_ARG),    # B=2 with cu_seqlens
+    (dict(num_chunks=5), Status.INVALID_ARG),       # 2 sequences x 3 chunks do not fit
+    (dict(hs_dtype=3), Status.INVALID_ARG),
+    (dict(h0=FAKE + 8), Status.MISALIGNED),
+])
+def test_state_pass_argument_errors(lib, change, expect):
+    a = good_state(**change)
+    assert lib.gdn_chunk_state_fwd(ctypes.byref(a), None) == expect
+    assert lib.gdn_last_error_message().decode() != ""

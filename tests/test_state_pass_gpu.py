@@ -1,0 +1,101 @@
+"""gdn_chunk_state_fwd (gated linear-attention chunk state pass) against the oracle.
+
+Every gate kind on fp32 and bf16 inputs, ragged tails and a partial value
+tile, packed sequences with empty ones, bf16 chunk states, no outputs but the
+final state, an empty batch, and a bad cu_seqlens reported on the device.
+The kernel computes in fp32 from the inputs as stored, so the fp32 bound
+(1e-4 RMS) applies to both input dtypes; bf16-stored chunk states get the
+half-ulp storage allowance.
+"""
+import pytest
+import torch
+
+import gated_delta_rule_kk_gb300 as gdn
+from gated_delta_rule_kk_gb300 import Status, synth
+from oracle import state_pass as SP
+
+from _util import TOL_F32, assert_close
+
+pytestmark = pytest.mark.gpu
+
+GATES = [None, "g", "g_gamma", "gk", "gv"]
+
+
+def _dev(x):
+    return None if x is None else x.cuda()
+
+
+def run(inp, states_dtype=torch.float32, output_states=True):
+    hs, ht = gdn.gdn_chunk_state_fwd(
+        inp["k"].cuda(), inp["v"].cuda(), gate=inp["gate"], gate_values=_dev(inp["gate_values"]),
+        initial_state=_dev(inp["h0"]), cu_seqlens=_dev(inp["cu_seqlens"]),
+        states_dtype=states_dtype, output_states=output_states)
+    torch.cuda.synchronize()
+    assert gdn.gdn_check_device_error() == Status.OK
+    return hs, ht
+
+
+def oracle(inp):
+    return SP.chunk_state_pass(inp["k"], inp["v"], inp["gate"], inp["gate_values"], h0=inp["h0"],
+                               cu_seqlens=inp["cu_seqlens"])
+
+
+@pytest.mark.parametrize("gate", GATES)
+def test_fp32_every_gate(gate):
+    # T = 150: two full chunks and a 22-token tail; V = 48: one full and one half tile
+    inp = synth.state_pass_inputs(70, 2, 150, 3, 32, 48, gate, dtype=torch.float32, h0_std=0.3)
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert tuple(hs.shape) == hs_ref.shape
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate})")
+
+
+@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+def test_bf16_inputs_full_width(gate):
+    inp = synth.state_pass_inputs(71, 1, 300, 2, 128, 128, gate, h0_std=0.1)
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate})")
+
+
+def test_bf16_chunk_states_and_no_states():
+    inp = synth.state_pass_inputs(72, 2, 200, 2, 64, 64, "g", h0_std=0.2)
+    hs, ht = run(inp, states_dtype=torch.bfloat16)
+    hs_ref, ht_ref = oracle(inp)
+    assert hs.dtype == torch.bfloat16
+    assert_close(hs, hs_ref, TOL_F32, "hs (bf16)")
+    assert_close(ht, ht_ref, TOL_F32, "ht")
+    none, ht2 = run(inp, output_states=False)
+    assert none is None
+    assert torch.equal(ht2, ht)
+
+
+def test_packed_sequences_with_empty_ones():
+    lengths = [70, 0, 130, 1, 64]
+    inp = synth.state_pass_inputs(73, 1, sum(lengths), 2, 32, 32, "gk", dtype=torch.float32,
+                                  lengths=lengths, h0_std=0.5)
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert hs.shape[0] == 2 + 0 + 3 + 1 + 1
+    assert_close(hs, hs_ref, TOL_F32, "hs")
+    assert_close(ht, ht_ref, TOL_F32, "ht")
+    assert torch.equal(ht[1].cpu(), inp["h0"][1])  # the empty sequence keeps its state
+
+
+def test_empty_batch_returns_the_initial_state():
+    inp = synth.state_pass_inputs(74, 2, 0, 2, 32, 32, "g", dtype=torch.float32, h0_std=1.0)
+    hs, ht = run(inp)
+    assert hs.shape[0] == 0
+    assert torch.equal(ht.cpu(), inp["h0"])
+
+
+def test_bad_seqlens_is_reported():
+    k = torch.randn(1, 100, 2, 32, device="cuda")
+    v = torch.randn(1, 100, 2, 32, device="cuda")
+    cu = torch.tensor([0, 60, 40, 100], dtype=torch.int32, device="cuda")
+    gdn.gdn_chunk_state_fwd(k, v, cu_seqlens=cu, num_chunks=8)
+    torch.cuda.synchronize()
+    assert gdn.gdn_check_device_error() == Status.BAD_SEQLENS
+    assert gdn.gdn_check_device_error() == Status.OK  # reading clears it
