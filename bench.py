@@ -339,6 +339,32 @@ def run_ours(args, rank, world, dev):
                          "unit": "GB/s", "frac": vb / (vt / 1e3) / 1e9 / hbm,
                          "algorithmic_bytes": vb, "algorithmic_flops": vf, "traffic": None}}
         del vd, vo, vht, vin
+        # chunk state pass (gated linear attention), per-token gate and per-key gate
+        for sgate in ("g", "gk"):
+            sin = synth.state_pass_inputs(5, 2, 4096, 16, 128, 128, sgate, h0_std=0.1)
+            sm = sin["dims"]
+            sk, sv = sin["k"].to(dev), sin["v"].to(dev)
+            sg, sh0 = sin["gate_values"].to(dev), sin["h0"].to(dev)
+            nchunk = sm["B"] * ((sm["T"] + 63) // 64)
+            shs = torch.empty((nchunk, sm["H"], sm["K"], sm["V"]), dtype=torch.float32, device=dev)
+            sht = torch.empty((sm["N"], sm["H"], sm["K"], sm["V"]), dtype=torch.float32, device=dev)
+            sms = time_steps(lambda: gdn.gdn_chunk_state_fwd(sk, sv, gate=sgate, gate_values=sg,
+                                                             initial_state=sh0, out_states=shs,
+                                                             final_state=sht),
+                             rsteps, max(3, args.warmup // 2), flush, stream)
+            st_ = statistics.mean(sms)
+            per_tok = sm["H"] * (sm["K"] + sm["V"]) * 2 + sg.numel() * 4 // (sm["B"] * sm["T"])
+            sbytes = (sm["B"] * sm["T"] * per_tok + shs.numel() * 4
+                      + 2 * sm["N"] * sm["H"] * sm["K"] * sm["V"] * 4)
+            rows[f"state_pass_{sgate}"] = {
+                "workload": f"chunk state pass (gated linear attention): B=2, T=4096, H=16, "
+                            f"K=V=128, bf16 k/v, gate {sgate}, h0 given, fp32 chunk states "
+                            f"[{nchunk},16,128,128] and final state",
+                "tokens_per_s": sm["B"] * sm["T"] / (st_ / 1e3), "ms_per_call": st_,
+                "roofline": {"bound": "hbm", "achieved": sbytes / (st_ / 1e3) / 1e9, "peak": hbm,
+                             "unit": "GB/s", "frac": sbytes / (st_ / 1e3) / 1e9 / hbm,
+                             "algorithmic_bytes": sbytes, "traffic": None}}
+            del sk, sv, sg, sh0, shs, sht, sin
         for T in (1, 2, 3, 4):
             din = synth.decode(T)
             dd = to_dev(din, dev)

@@ -222,6 +222,8 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
           GDN_ERR_INVALID_ARG, "sizes must be positive (B=%d T=%d H=%d K=%d V=%d N=%d)", a->B,
           a->T, a->H, a->K, a->V, a->N);
   REQUIRE(a->K <= KMAX, GDN_ERR_UNSUPPORTED, "K=%d exceeds %d", a->K, KMAX);
+  REQUIRE(a->K % 8 == 0 && a->V % 8 == 0, GDN_ERR_UNSUPPORTED,
+          "K (%d) and V (%d) must be multiples of 8", a->K, a->V);
   REQUIRE(a->chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT,
           a->chunk_size);
   if (a->cu_seqlens == nullptr) {

@@ -11,8 +11,10 @@
 //
 // Exact fp32 CUDA-core kernel: one CTA per (32-column tile of V, head,
 // sequence); each of its 256 threads keeps 16 state values (one key row, 16
-// columns) in registers across the chunks, and each chunk's gated k~ and v~
-// are staged in shared memory first.
+// columns) in registers across the chunks.  A chunk's k, v and gates are
+// loaded into registers (16-byte loads; K and V are multiples of 8) while the
+// previous chunk is computed, then written to shared memory with the gate
+// factors applied.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -20,6 +22,32 @@ namespace gdn {
 namespace {
 
 constexpr int SP_THREADS = 256, SP_VT = 32;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {  // RNE, a in the low half
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// 8 consecutive elements (16-byte aligned) widened to fp32; zeros if !ok.
+__device__ __forceinline__ void load8(const float *src, bool ok, float *out) {
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (ok) {
+    a = reinterpret_cast<const float4 *>(src)[0];
+    b = reinterpret_cast<const float4 *>(src)[1];
+  }
+  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *src, bool ok, float *out) {
+  uint4 u = make_uint4(0u, 0u, 0u, 0u);
+  if (ok) u = *reinterpret_cast<const uint4 *>(src);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[2 * q] = __uint_as_float(w[q] << 16);
+    out[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
@@ -78,79 +106,113 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
     hv[j] = (p.h0 && row_ok && col < V) ? p.h0[sbase + col] : 0.f;
   }
 
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
+  // Each thread's share of a chunk's inputs, loaded into registers one chunk
+  // ahead (16-byte loads, all independent, so their latency overlaps the
+  // current chunk's arithmetic): 8 consecutive keys of rows (tid >> 4) + 16 p,
+  // p = 0..3, of the [64, K] k tile (keys 8 (tid & 15) ..), and 8 consecutive
+  // columns of row tid >> 2 of the [64, 32] v tile (columns 8 (tid & 3) ..),
+  // with the matching gates.
+  float kx[4][8], gkx[4][8], vx[8], gvx[8];
+  float gtok = 0.f, glast = 0.f;
+  const bool gk = p.gate == GDN_GATE_GK, gvg = p.gate == GDN_GATE_GV;
+  const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
+  const int kq = (tid & 15) * 8, vi = tid >> 2, vq = (tid & 3) * 8;
+  const bool kq_ok = kq < K, vq_ok = v0 + vq < V;
+  auto load = [&](int c) {
     const int t0 = bos + c * BT;
     const int L = min(BT, eos - t0);
-    const size_t row0 = (size_t)b * p.T + t0;  // global token row of the chunk's first token
-
-    // chunk-start state
-    if (write_hs && row_ok) {
-      const size_t o = (((size_t)(first + c) * H + h) * K + r) * V;
+    const size_t row0 = (size_t)b * p.T + t0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int col = v0 + c0 + j;
-        if (col < V) {
-          if (p.hs_bf16)
-            static_cast<__nv_bfloat16 *>(p.hs)[o + col] = __float2bfloat16_rn(hv[j]);
-          else
-            static_cast<float *>(p.hs)[o + col] = hv[j];
+    for (int pp = 0; pp < 4; ++pp) {
+      const int i = (tid >> 4) + 16 * pp;
+      const bool ok = i < L && kq_ok;
+      const size_t e = (row0 + i) * H * K + (size_t)h * K + kq;
+      load8(k + e, ok, kx[pp]);
+      load8(p.gate_values + e, ok && gk, gkx[pp]);
+    }
+    {
+      const bool ok = vi < L && vq_ok;
+      const size_t e = (row0 + vi) * H * V + (size_t)h * V + v0 + vq;
+      load8(v + e, ok, vx);
+      load8(p.gate_values + e, ok && gvg, gvx);
+    }
+    gtok = 0.f;
+    if (p.gate == GDN_GATE_G && tid < L) gtok = p.gate_values[(row0 + tid) * H + h];
+    if (p.gate == GDN_GATE_G_GAMMA && tid < L) gtok = p.gate_values[h] * (float)(tid + 1);
+    glast = 0.f;
+    if (gk && tid < K) glast = p.gate_values[((row0 + L - 1) * H + h) * K + tid];
+    if (gvg && tid < SP_VT && v0 + tid < V)
+      glast = p.gate_values[((row0 + L - 1) * H + h) * V + v0 + tid];
+  };
+
+  if (nch > 0) load(0);
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const int L = min(BT, eos - (bos + c * BT));
+
+    // chunk-start state, 8 columns (16 or 32 bytes) per store
+    if (write_hs && row_ok) {
+      const size_t o = (((size_t)(first + c) * H + h) * K + r) * V + v0 + c0;
+#pragma unroll
+      for (int g8 = 0; g8 < 2; ++g8) {
+        if (v0 + c0 + 8 * g8 >= V) continue;  // V is a multiple of 8
+        const float *x = hv + 8 * g8;
+        if (p.hs_bf16) {
+          __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.hs) + o + 8 * g8;
+          uint4 w;
+          w.x = pack_bf16x2(x[0], x[1]); w.y = pack_bf16x2(x[2], x[3]);
+          w.z = pack_bf16x2(x[4], x[5]); w.w = pack_bf16x2(x[6], x[7]);
+          *reinterpret_cast<uint4 *>(dst) = w;
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.hs) + o + 8 * g8);
+          dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+          dst[1] = make_float4(x[4], x[5], x[6], x[7]);
         }
       }
     }
 
-    // gates of the chunk
-    if (p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA) {
-      if (tid < BT) {
-        float x = 0.f;
-        if (tid < L)
-          x = p.gate == GDN_GATE_G ? p.gate_values[(row0 + tid) * H + h]
-                                   : p.gate_values[h] * (float)(tid + 1);
-        gam[tid] = x;
-      }
-    } else if (p.gate == GDN_GATE_GK) {
-      if (tid < K) gkl[tid] = p.gate_values[((row0 + L - 1) * H + h) * K + tid];
-    } else if (p.gate == GDN_GATE_GV) {
-      if (tid < SP_VT) {
-        const int col = v0 + tid;
-        gvl[tid] = col < V ? p.gate_values[((row0 + L - 1) * H + h) * V + col] : 0.f;
-      }
-    }
+    // this chunk's gates, then k~ and v~, from the registers (rows past the
+    // chunk's last one hold zeros and take no factor)
+    if (scalar_gate && tid < BT) gam[tid] = gtok;
+    if (gk && tid < K) gkl[tid] = glast;
+    if (gvg && tid < SP_VT) gvl[tid] = glast;
     __syncthreads();
-    const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
     const float gL = scalar_gate ? gam[L - 1] : 0.f;
-
-    // stage k~ (per-key gate applied) and v~ (scalar and per-column gates)
-    for (int idx = tid; idx < BT * K; idx += SP_THREADS) {
-      const int i = idx / K, kk = idx % K;
-      float x = 0.f;
-      if (i < L) {
-        x = to_f32(k[(row0 + i) * H * K + (size_t)h * K + kk]);
-        if (p.gate == GDN_GATE_GK)
-          x *= expf(gkl[kk] - p.gate_values[((row0 + i) * H + h) * K + kk]);
+    if (kq_ok) {
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const int i = (tid >> 4) + 16 * pp;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          x[e] = (gk && i < L) ? kx[pp][e] * expf(gkl[kq + e] - gkx[pp][e]) : kx[pp][e];
+        float4 *dst = reinterpret_cast<float4 *>(&ks[i][kq]);
+        dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+        dst[1] = make_float4(x[4], x[5], x[6], x[7]);
       }
-      ks[i][kk] = x;
     }
-    for (int idx = tid; idx < BT * SP_VT; idx += SP_THREADS) {
-      const int i = idx / SP_VT, cc = idx % SP_VT, col = v0 + cc;
-      float x = 0.f;
-      if (i < L && col < V) {
-        x = to_f32(v[(row0 + i) * H * V + (size_t)h * V + col]);
-        if (scalar_gate) x *= expf(gL - gam[i]);
-        if (p.gate == GDN_GATE_GV)
-          x *= expf(gvl[cc] - p.gate_values[((row0 + i) * H + h) * V + col]);
+    {
+      float x[8];
+      const float sf = (scalar_gate && vi < L) ? expf(gL - gam[vi]) : 1.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[e] = vx[e] * sf;
+        if (gvg && vi < L) x[e] *= expf(gvl[vq + e] - gvx[e]);
       }
-      vs[i][cc] = x;
+      float4 *dst = reinterpret_cast<float4 *>(&vs[vi][vq]);
+      dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+      dst[1] = make_float4(x[4], x[5], x[6], x[7]);
     }
     __syncthreads();
+    if (c + 1 < nch) load(c + 1);  // in flight during the update below
 
     // h <- decay(h) + k~^T v~
     float dk = 1.f;
     if (scalar_gate) dk = expf(gL);
-    if (p.gate == GDN_GATE_GK && row_ok) dk = expf(gkl[r]);
+    if (gk && row_ok) dk = expf(gkl[r]);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float dv = p.gate == GDN_GATE_GV ? expf(gvl[c0 + j]) : 1.f;
+      const float dv = gvg ? expf(gvl[c0 + j]) : 1.f;
       hv[j] *= dk * dv;
     }
     if (row_ok) {

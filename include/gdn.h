@@ -173,8 +173,9 @@ gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *args, gdn_stream_t stream)
  *   cu_seqlens [N + 1] int32   as gdn_chunk_fwd (device memory; checked on the
  *                              device, GDN_ERR_BAD_SEQLENS also when the chunks
  *                              do not fit num_chunks)
- * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64.  Arithmetic in fp32 (bf16
- * inputs are widened).  Nothing is allocated; no workspace.
+ * Limits: 1 <= K <= 128, K and V multiples of 8, chunk_size == 64.
+ * Arithmetic in fp32 (bf16 inputs are widened).  Nothing is allocated; no
+ * workspace.
  */
 typedef enum gdn_gate_kind {
   GDN_GATE_NONE = 0,

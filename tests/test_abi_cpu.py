@@ -220,6 +220,8 @@ def good_state(**kw):
     (dict(k=None), Status.INVALID_ARG),
     (dict(v=FAKE + 4), Status.MISALIGNED),
     (dict(K=256), Status.UNSUPPORTED),
+    (dict(V=60), Status.UNSUPPORTED),
+    (dict(K=36), Status.UNSUPPORTED),
     (dict(chunk_size=32), Status.UNSUPPORTED),
     (dict(N=3), Status.INVALID_ARG),
     (dict(cu_seqlens=FAKE), Status.INVALID_ARG),    # B=2 with cu_seqlens
