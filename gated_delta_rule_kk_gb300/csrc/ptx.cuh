@@ -251,6 +251,16 @@ __device__ __forceinline__ void ldmatrix_x4(const void *row_addr, uint32_t &r0, 
                : "memory");
 }
 
+// As ldmatrix_x4, each 8x8 matrix transposed (lane i supplies row i % 8 of
+// matrix i / 8 as stored; a register holds two elements of one stored column).
+__device__ __forceinline__ void ldmatrix_x4_trans(const void *row_addr, uint32_t &r0,
+                                                  uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(row_addr))
+               : "memory");
+}
+
 __device__ __forceinline__ void stmatrix_x4(void *row_addr, uint32_t r0, uint32_t r1, uint32_t r2,
                                             uint32_t r3) {
   asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
