@@ -363,7 +363,8 @@ def run_ours(args, rank, world, dev):
                 "tokens_per_s": sm["B"] * sm["T"] / (st_ / 1e3), "ms_per_call": st_,
                 "roofline": {"bound": "hbm", "achieved": sbytes / (st_ / 1e3) / 1e9, "peak": hbm,
                              "unit": "GB/s", "frac": sbytes / (st_ / 1e3) / 1e9 / hbm,
-                             "algorithmic_bytes": sbytes, "traffic": None}}
+                             "algorithmic_bytes": sbytes,
+                             "traffic": traffic_record(f"state_pass_{sgate}")}}
             del sk, sv, sg, sh0, shs, sht, sin
         for T in (1, 2, 3, 4):
             din = synth.decode(T)
