@@ -89,3 +89,67 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
             ht[n, h] = S
         first += counts[n]
     return hs, ht
+
+
+def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=None,
+                     scale=None, chunk_size: int = 64):
+    """Backward state pass (the chunk_h page's ``chunk_bwd_kernel_dh``).
+
+    For the gated linear attention above with outputs o_t = scale S_t^T q_t
+    (S_t the state after token t), the gradient G_t = dL/dS_t of a loss with
+    dL/do_t = do_t obeys, going backwards,
+
+        G <- G + scale q_t do_t^T      (token t's output)
+        G <- decay_t^T(G)              (to the state before token t)
+
+    starting from G = dht after the last token.  Returns ``dh``
+    ``[sum NT_n, HQ, K, V]``, the gradient with respect to the state at the
+    end of every chunk (taken before that chunk's tokens are folded in), and
+    ``dh0`` ``[N, HQ, K, V]``.  q ``[B, T, HQ, K]``, do ``[B, T, HQ, V]``;
+    the gate has H heads (HQ a multiple of H, query head hq uses gate head
+    hq // (HQ / H)), given as in :func:`chunk_state_pass`.
+    """
+    if gate not in GATES:
+        raise ValueError(f"unknown gate {gate!r}")
+    q, do = _f64(q), _f64(do)
+    B, T, HQ, K = q.shape
+    V = do.shape[3]
+    scale = 1.0 / np.sqrt(K) if scale is None else float(scale)
+    gv_ = _f64(gate_values)
+    if gate is None:
+        H = HQ
+    elif gate == "g_gamma":
+        H = gv_.shape[0]
+    else:
+        H = gv_.shape[2]
+    group = HQ // H
+    seqs = sequence_bounds(B, T, cu_seqlens)
+    N = len(seqs)
+    dht = np.zeros((N, HQ, K, V)) if dht is None else _f64(dht)
+    counts = chunk_counts(B, T, cu_seqlens, chunk_size)
+    dh = np.zeros((sum(counts), HQ, K, V))
+    dh0 = np.zeros((N, HQ, K, V))
+    first = 0
+    for n, (b, bos, eos) in enumerate(seqs):
+        raw = None
+        if gate in ("g", "gk", "gv"):
+            raw = raw_gate_from_chunk_cumsum(gv_[b], bos, eos, chunk_size)
+        for hq in range(HQ):
+            h = hq // group
+            G = dht[n, hq].copy()
+            for t in range(eos - 1, bos - 1, -1):
+                i = t - bos
+                if i % chunk_size == chunk_size - 1 or t == eos - 1:
+                    dh[first + i // chunk_size, hq] = G
+                G = G + scale * np.outer(q[b, t, hq], do[b, t, hq])
+                if gate == "g":
+                    G = np.exp(raw[t, h]) * G
+                elif gate == "g_gamma":
+                    G = np.exp(gv_[h]) * G
+                elif gate == "gk":
+                    G = np.exp(raw[t, h])[:, None] * G
+                elif gate == "gv":
+                    G = G * np.exp(raw[t, h])[None, :]
+            dh0[n, hq] = G
+        first += counts[n]
+    return dh, dh0

@@ -120,3 +120,78 @@ def test_chunk_starts_resume_the_run_and_packed_sequences_are_separate_runs():
         np.testing.assert_allclose(hs_p[first:first + s_n.shape[0]], s_n, rtol=1e-12, atol=1e-12)
         first += s_n.shape[0]
     np.testing.assert_array_equal(ht_p[1], hh0[1])  # the empty sequence keeps its state
+
+
+def _outputs(k, v, q, gate, raw, gamma, h0, scale):
+    """o_t = scale S_t^T q_t of one (sequence, head) chain, by stepping the
+    forward recurrence (the loss below is linear in h0 and dht)."""
+    S = h0.copy()
+    outs = []
+    for t in range(k.shape[0]):
+        if gate == "g":
+            S = np.exp(raw[t]) * S
+        elif gate == "g_gamma":
+            S = np.exp(gamma) * S
+        elif gate == "gk":
+            S = np.exp(raw[t])[:, None] * S
+        elif gate == "gv":
+            S = S * np.exp(raw[t])[None, :]
+        S = S + np.outer(k[t], v[t])
+        outs.append(scale * S.T @ q[t])
+    return np.array(outs), S
+
+
+@pytest.mark.parametrize("gate", SP.GATES)
+def test_state_gradient_is_the_adjoint_of_the_forward_pass(gate):
+    # L(h0) = sum_t <do_t, o_t> + <dht, S_T> is affine in h0, so for any
+    # direction E: L(h0 + E) - L(h0) = <dh0, E>; and dh[c] is the gradient with
+    # respect to the state at the end of chunk c (resume the forward run there).
+    T, K, V, chunk, scale = 11, 3, 4, 4, 0.7
+    rng = np.random.default_rng(7)
+    k, v, q, do = (rng.standard_normal((T, K)), rng.standard_normal((T, V)),
+                   rng.standard_normal((T, K)), rng.standard_normal((T, V)))
+    raw = {None: None, "g": -np.abs(rng.standard_normal(T)) * 0.4, "g_gamma": None,
+           "gk": -np.abs(rng.standard_normal((T, K))) * 0.4,
+           "gv": -np.abs(rng.standard_normal((T, V))) * 0.4}[gate]
+    gamma = -0.3
+    h0, dht = rng.standard_normal((K, V)), rng.standard_normal((K, V))
+    vals = None
+    if gate == "g_gamma":
+        vals = np.array([gamma])
+    elif gate is not None:
+        vals = _chunk_cumsum(raw[None, :, None], chunk)[0, :, 0]
+        vals = vals[None, :, None] if raw.ndim == 1 else vals[None, :, None, :]
+    dh, dh0 = SP.chunk_state_grad(q[None, :, None], do[None, :, None], gate, vals,
+                                  dht=dht[None, None], scale=scale, chunk_size=chunk)
+
+    def loss(start_state, t0):
+        o, S = _outputs(k[t0:], v[t0:], q[t0:], gate, None if raw is None else raw[t0:],
+                        gamma, start_state, scale)
+        return float(np.sum(o * do[t0:]) + np.sum(S * dht))
+
+    E = rng.standard_normal((K, V))
+    np.testing.assert_allclose(loss(h0 + E, 0) - loss(h0, 0), np.sum(dh0[0, 0] * E),
+                               rtol=1e-10, atol=1e-10)
+    for c in range(dh.shape[0]):
+        t_end = min((c + 1) * chunk, T)  # the state after token t_end - 1
+        if t_end == T:
+            np.testing.assert_allclose(dh[c, 0], dht, rtol=1e-12, atol=1e-12)
+            continue
+        _, S_end = _outputs(k[:t_end], v[:t_end], q[:t_end], gate,
+                            None if raw is None else raw[:t_end], gamma, h0, scale)
+        np.testing.assert_allclose(loss(S_end + E, t_end) - loss(S_end, t_end),
+                                   np.sum(dh[c, 0] * E), rtol=1e-10, atol=1e-10)
+
+
+def test_state_gradient_grouped_query_heads_share_the_gate():
+    B, T, HQ, H, K, V, chunk = 1, 9, 4, 2, 3, 2, 4
+    rng = np.random.default_rng(8)
+    q, do = rng.standard_normal((B, T, HQ, K)), rng.standard_normal((B, T, HQ, V))
+    raw = -np.abs(rng.standard_normal((B, T, H, K))) * 0.3
+    gk = _chunk_cumsum(raw, chunk)
+    dht = rng.standard_normal((B, HQ, K, V))
+    a = SP.chunk_state_grad(q, do, "gk", gk, dht=dht, scale=0.5, chunk_size=chunk)
+    b = SP.chunk_state_grad(q, do, "gk", np.repeat(gk, HQ // H, axis=2), dht=dht, scale=0.5,
+                            chunk_size=chunk)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-12, atol=1e-12)
