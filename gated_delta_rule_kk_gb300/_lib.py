@@ -96,6 +96,21 @@ class GdnStateArgs(ctypes.Structure):
     ]
 
 
+class GdnStateBwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("dtype", c_int32),
+        ("q", c_void_p), ("do_", c_void_p),
+        ("gate", c_int32), ("gate_values", c_void_p),
+        ("dht", c_void_p), ("dh0", c_void_p),
+        ("dh", c_void_p), ("dh_dtype", c_int32),
+        ("cu_seqlens", c_void_p),
+        ("B", c_int32), ("T", c_int32), ("HQ", c_int32), ("H", c_int32), ("K", c_int32),
+        ("V", c_int32), ("N", c_int32), ("chunk_size", c_int32),
+        ("num_chunks", ctypes.c_int64),
+        ("scale", c_float),
+    ]
+
+
 # name -> (argtypes, restype); exactly the functions include/gdn.h declares
 SIGNATURES = {
     "gdn_chunk_workspace_size": ([ctypes.POINTER(GdnChunkArgs), ctypes.POINTER(c_size_t)], c_int32),
@@ -107,6 +122,7 @@ SIGNATURES = {
     "kda_chunk_fwd": ([ctypes.POINTER(KdaChunkArgs), c_void_p], c_int32),
     "gdn_decode": ([ctypes.POINTER(GdnDecodeArgs), c_void_p], c_int32),
     "gdn_chunk_state_fwd": ([ctypes.POINTER(GdnStateArgs), c_void_p], c_int32),
+    "gdn_chunk_state_bwd": ([ctypes.POINTER(GdnStateBwdArgs), c_void_p], c_int32),
     "gdn_chunk_fwd_noalloc": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
     "gdn_noalloc_scratch_bytes": ([], c_size_t),
     "gdn_check_device_error": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),

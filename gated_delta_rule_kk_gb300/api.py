@@ -11,7 +11,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import DType, GateKind, GdnChunkArgs, GdnDecodeArgs, GdnStateArgs, KdaChunkArgs
+from ._lib import (DType, GateKind, GdnChunkArgs, GdnDecodeArgs, GdnStateArgs, GdnStateBwdArgs,
+                   KdaChunkArgs)
 
 CHUNK = 64
 
@@ -366,3 +367,64 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_state_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_fwd")
     return hs, ht
+
+
+def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=None,
+                        scale=None, output_dh0=True, output_states=True,
+                        states_dtype=torch.float32, out_states=None, dh0=None,
+                        num_chunks=None, stream=None):
+    """Backward state pass (dh recurrence).  Returns ``(dh, dh0)``.
+
+    q [B,T,HQ,K], do [B,T,HQ,V] (float32 or bfloat16); gate and gate_values
+    as :func:`gdn_chunk_state_fwd` with H gate heads (HQ % H == 0); dht
+    [N,HQ,K,V] float32.  dh [C,HQ,K,V] is the gradient at the end of every
+    64-token chunk, sequence after sequence.
+    """
+    dev = q.device
+    dt, dts = _io_dtype(q)
+    _need(q, "q", dts, dev)
+    _need(do, "do", dts, dev)
+    if gate not in _GATES:
+        raise ValueError(f"gate must be one of {list(_GATES)}")
+    B, T, HQ, K = q.shape
+    V = do.shape[3]
+    if do.shape[:3] != (B, T, HQ):
+        raise ValueError("q must be [B,T,HQ,K] and do [B,T,HQ,V]")
+    H = HQ
+    if gate is not None:
+        _need(gate_values, "gate_values", (torch.float32,), dev)
+        H = gate_values.shape[0] if gate == "g_gamma" else gate_values.shape[2]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+        N = cu_seqlens.numel() - 1
+        if num_chunks is None and (output_states or out_states is not None):
+            lens = (cu_seqlens[1:] - cu_seqlens[:-1]).clamp(min=0).to(torch.int64)
+            num_chunks = int(((lens + CHUNK - 1) // CHUNK).sum().item())
+    else:
+        N = B
+        if num_chunks is None:
+            num_chunks = B * ((T + CHUNK - 1) // CHUNK)
+    if dht is not None:
+        _need(dht, "dht", (torch.float32,), dev)
+        if tuple(dht.shape) != (N, HQ, K, V):
+            raise ValueError(f"dht must be [{N},{HQ},{K},{V}]")
+    dh = out_states
+    if dh is None and output_states:
+        dh = torch.empty((num_chunks, HQ, K, V), dtype=states_dtype, device=dev)
+    if dh is not None:
+        _need(dh, "out_states", (torch.float32, torch.bfloat16), dev)
+    if dh0 is None and output_dh0:
+        dh0 = torch.empty((N, HQ, K, V), dtype=torch.float32, device=dev)
+    elif dh0 is not None:
+        _need(dh0, "dh0", (torch.float32,), dev)
+    a = GdnStateBwdArgs(dtype=int(dt), q=_ptr(q), do_=_ptr(do), gate=int(_GATES[gate]),
+                        gate_values=_ptr(gate_values) if gate is not None else None,
+                        dht=_ptr(dht), dh0=_ptr(dh0), dh=_ptr(dh),
+                        dh_dtype=int(DType.BF16 if dh is not None and dh.dtype == torch.bfloat16
+                                     else DType.F32),
+                        cu_seqlens=_ptr(cu_seqlens), B=B, T=T, HQ=HQ, H=H, K=K, V=V, N=N,
+                        chunk_size=CHUNK, num_chunks=int(num_chunks or 0),
+                        scale=float(scale) if scale is not None else 0.0)
+    lib = _lib.load()
+    _lib.check(lib.gdn_chunk_state_bwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_bwd")
+    return dh, dh0

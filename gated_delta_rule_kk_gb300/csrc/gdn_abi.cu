@@ -259,12 +259,78 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
   p.h0 = a->h0; p.ht = a->ht; p.hs = a->hs; p.hs_bf16 = a->hs_dtype == GDN_BF16;
   p.cu_seqlens = a->cu_seqlens;
   p.B = a->B; p.T = a->T; p.H = a->H; p.K = a->K; p.V = a->V; p.N = a->N;
+  p.HG = a->H;
   p.num_chunks = a->hs ? a->num_chunks : 0;
+  p.reverse = 0;
+  p.scale = 1.f;
   p.err = device_error_word();
   if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
   return cuda_status(launch_state_pass(p, a->dtype == GDN_BF16,
                                        reinterpret_cast<cudaStream_t>(stream)),
                      "state pass launch");
+}
+
+gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t stream) {
+  g_msg[0] = '\0';
+  if (a == nullptr) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
+  REQUIRE(a->dtype == GDN_F32 || a->dtype == GDN_BF16, GDN_ERR_INVALID_ARG,
+          "dtype %d is not GDN_F32/GDN_BF16", a->dtype);
+  REQUIRE(a->gate >= GDN_GATE_NONE && a->gate <= GDN_GATE_GV, GDN_ERR_INVALID_ARG,
+          "gate %d is not a gdn_gate_kind_t", a->gate);
+  REQUIRE(a->B >= 1 && a->T >= 0 && a->HQ >= 1 && a->H >= 1 && a->K >= 1 && a->V >= 1 &&
+              a->N >= 1,
+          GDN_ERR_INVALID_ARG, "sizes must be positive (B=%d T=%d HQ=%d H=%d K=%d V=%d N=%d)",
+          a->B, a->T, a->HQ, a->H, a->K, a->V, a->N);
+  REQUIRE(a->HQ % a->H == 0, GDN_ERR_UNSUPPORTED, "HQ (%d) must be a multiple of H (%d)", a->HQ,
+          a->H);
+  REQUIRE(a->K <= KMAX, GDN_ERR_UNSUPPORTED, "K=%d exceeds %d", a->K, KMAX);
+  REQUIRE(a->K % 8 == 0 && a->V % 8 == 0, GDN_ERR_UNSUPPORTED,
+          "K (%d) and V (%d) must be multiples of 8", a->K, a->V);
+  REQUIRE(a->chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT,
+          a->chunk_size);
+  REQUIRE(isfinite(a->scale), GDN_ERR_INVALID_ARG, "scale must be finite");
+  if (a->cu_seqlens == nullptr) {
+    REQUIRE(a->N == a->B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)",
+            a->N, a->B);
+  } else {
+    REQUIRE(a->B == 1, GDN_ERR_INVALID_ARG, "with cu_seqlens B must be 1 (got %d)", a->B);
+  }
+  if (a->T > 0) {
+    REQUIRE_PTR(a->q, "q");
+    REQUIRE_PTR(a->do_, "do");
+  }
+  if (a->gate == GDN_GATE_NONE) {
+    REQUIRE(a->gate_values == nullptr, GDN_ERR_INVALID_ARG, "gate_values given without a gate");
+  } else if (a->T > 0 || a->gate == GDN_GATE_G_GAMMA) {
+    REQUIRE_PTR(a->gate_values, "gate_values");
+  }
+  REQUIRE_OPT_PTR(a->dht, "dht");
+  REQUIRE_OPT_PTR(a->dh0, "dh0");
+  REQUIRE_OPT_PTR(a->cu_seqlens, "cu_seqlens");
+  if (a->dh != nullptr) {
+    REQUIRE_PTR(a->dh, "dh");
+    REQUIRE(a->dh_dtype == GDN_F32 || a->dh_dtype == GDN_BF16, GDN_ERR_INVALID_ARG,
+            "dh_dtype %d is not GDN_F32/GDN_BF16", a->dh_dtype);
+    if (a->cu_seqlens == nullptr) {
+      const long long need = (long long)a->B * ((a->T + BT - 1) / BT);
+      REQUIRE(a->num_chunks >= need, GDN_ERR_INVALID_ARG,
+              "dh holds %lld chunks, %lld needed", (long long)a->num_chunks, need);
+    }
+  }
+  StateParams p{};
+  p.k = a->q; p.v = a->do_; p.gate = a->gate; p.gate_values = a->gate_values;
+  p.h0 = a->dht; p.ht = a->dh0; p.hs = a->dh; p.hs_bf16 = a->dh_dtype == GDN_BF16;
+  p.cu_seqlens = a->cu_seqlens;
+  p.B = a->B; p.T = a->T; p.H = a->HQ; p.K = a->K; p.V = a->V; p.N = a->N;
+  p.HG = a->H;
+  p.num_chunks = a->dh ? a->num_chunks : 0;
+  p.reverse = 1;
+  p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)a->K);
+  p.err = device_error_word();
+  if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
+  return cuda_status(launch_state_pass(p, a->dtype == GDN_BF16,
+                                       reinterpret_cast<cudaStream_t>(stream)),
+                     "state backward launch");
 }
 
 gdn_status_t gdn_decode(const gdn_decode_args *a, gdn_stream_t stream) {

@@ -47,7 +47,13 @@ struct StateParams {
   const int32_t *cu_seqlens;
   int *err;
   int B, T, H, K, V, N;
+  int HG;                     // gate heads (H % HG == 0; head h uses gate head h / (H / HG))
   long long num_chunks;       // capacity of hs in chunks
+  // Backward (dh) pass: chunks from last to first, k = q scaled by `scale`,
+  // v = do, gate factors taken from the chunk start instead of its end,
+  // h0 = dht, ht = dh0, hs = dh (the gradient at the end of every chunk).
+  int reverse;
+  float scale;
 };
 
 // Each launcher enqueues its kernel(s) and returns the launch status.

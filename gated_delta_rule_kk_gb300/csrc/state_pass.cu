@@ -7,7 +7,10 @@
 //   h_{c+1} = e^{g_L} diag(e^{gk_L}) h_c diag(e^{gv_L}) + sum_i k~_i v~_i^T,
 //   k~_i = k_i e^{gk_L - gk_i},   v~_i = v_i e^{g_L - g_i} e^{gv_L - gv_i}
 // (each factor present only for its gate kind; the per-head rate g_gamma has
-// g_i = g_gamma (i + 1)).
+// g_i = g_gamma (i + 1)).  The backward pass (chunk_bwd_kernel_dh) runs the
+// same steps from the last chunk to the first with q (scaled) for k, do for v
+// and the factors e^{gamma_i} measured from the chunk's start:
+//   dh_{c} = e^{g_L} diag(e^{gk_L}) dh_{c+1} diag(e^{gv_L}) + sum_i q~_i do~_i^T.
 //
 // Two kernels, one CTA per (32-column tile of V, head, sequence), 256 threads,
 // the fp32 state in registers across the chunks.  A chunk's k, v and gates are
@@ -109,7 +112,7 @@ struct ChunkRegs {
 template <typename T>
 __device__ __forceinline__ void load_chunk(const StateParams &p, const SeqInfo &sq, int c, int h,
                                            int v0, int tid, ChunkRegs &R) {
-  const int H = p.H, K = p.K, V = p.V;
+  const int H = p.H, K = p.K, V = p.V, HG = p.HG, hg = h / (H / HG);
   const T *k = static_cast<const T *>(p.k);
   const T *v = static_cast<const T *>(p.v);
   const bool gk = p.gate == GDN_GATE_GK, gvg = p.gate == GDN_GATE_GV;
@@ -123,43 +126,50 @@ __device__ __forceinline__ void load_chunk(const StateParams &p, const SeqInfo &
     const bool ok = i < L && kq < K;
     const size_t e = (row0 + i) * H * K + (size_t)h * K + kq;
     load8(k + e, ok, R.kx[pp]);
-    load8(p.gate_values + e, ok && gk, R.gkx[pp]);
+    load8(p.gate_values + ((row0 + i) * HG + hg) * K + kq, ok && gk, R.gkx[pp]);
   }
   {
     const bool ok = vi < L && v0 + vq < V;
     const size_t e = (row0 + vi) * H * V + (size_t)h * V + v0 + vq;
     load8(v + e, ok, R.vx);
-    load8(p.gate_values + e, ok && gvg, R.gvx);
+    load8(p.gate_values + ((row0 + vi) * HG + hg) * V + v0 + vq, ok && gvg, R.gvx);
   }
   R.gtok = 0.f;
-  if (p.gate == GDN_GATE_G && tid < L) R.gtok = p.gate_values[(row0 + tid) * H + h];
-  if (p.gate == GDN_GATE_G_GAMMA && tid < L) R.gtok = p.gate_values[h] * (float)(tid + 1);
+  if (p.gate == GDN_GATE_G && tid < L) R.gtok = p.gate_values[(row0 + tid) * HG + hg];
+  if (p.gate == GDN_GATE_G_GAMMA && tid < L) R.gtok = p.gate_values[hg] * (float)(tid + 1);
   R.glast = 0.f;
-  if (gk && tid < K) R.glast = p.gate_values[((row0 + L - 1) * H + h) * K + tid];
+  if (gk && tid < K) R.glast = p.gate_values[((row0 + L - 1) * HG + hg) * K + tid];
   if (gvg && tid < SP_VT && v0 + tid < V)
-    R.glast = p.gate_values[((row0 + L - 1) * H + h) * V + v0 + tid];
+    R.glast = p.gate_values[((row0 + L - 1) * HG + hg) * V + v0 + tid];
 }
 
 // The gated k~ (8 values of row (tid >> 4) + 16 pp) and v~ (8 values of row
-// tid >> 2) of a chunk, once its gate vectors are in shared memory.  Rows past
-// the chunk's last one hold zeros and take no factor.
+// tid >> 2) of a chunk, once its gate vectors are in shared memory.  Forward:
+// factors e^{gamma_L - gamma_i} (from token i to the chunk's end); backward:
+// e^{gamma_i} (from the chunk's start to token i) and the scale on q.  Rows
+// past the chunk's last one hold zeros and take no factor.
 __device__ __forceinline__ void gated_k(const StateParams &p, const ChunkRegs &R, int pp, int tid,
                                         int L, const float *gkl, float *x) {
   const int i = (tid >> 4) + 16 * pp, kq = (tid & 15) * 8;
   const bool apply = p.gate == GDN_GATE_GK && i < L;
+  const float s = p.reverse ? p.scale : 1.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e)
-    x[e] = apply ? R.kx[pp][e] * expf(gkl[kq + e] - R.gkx[pp][e]) : R.kx[pp][e];
+  for (int e = 0; e < 8; ++e) {
+    const float f = p.reverse ? R.gkx[pp][e] : gkl[kq + e] - R.gkx[pp][e];
+    x[e] = s * (apply ? R.kx[pp][e] * expf(f) : R.kx[pp][e]);
+  }
 }
 __device__ __forceinline__ void gated_v(const StateParams &p, const ChunkRegs &R, int tid, int L,
                                         float gL, const float *gam, const float *gvl, float *x) {
   const int vi = tid >> 2, vq = (tid & 3) * 8;
   const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
-  const float sf = (scalar_gate && vi < L) ? expf(gL - gam[vi]) : 1.f;
+  float sf = 1.f;
+  if (scalar_gate && vi < L) sf = expf(p.reverse ? gam[vi] : gL - gam[vi]);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     x[e] = R.vx[e] * sf;
-    if (p.gate == GDN_GATE_GV && vi < L) x[e] *= expf(gvl[vq + e] - R.gvx[e]);
+    if (p.gate == GDN_GATE_GV && vi < L)
+      x[e] *= expf(p.reverse ? R.gvx[e] : gvl[vq + e] - R.gvx[e]);
   }
 }
 
@@ -205,10 +215,13 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
     hv[j] = (p.h0 && row_ok && col < V) ? p.h0[sbase + col] : 0.f;
   }
 
+  // chunk of the it-th step: forward from the first, backward from the last
+  auto chunk_at = [&](int it) { return p.reverse ? sq.nch - 1 - it : it; };
   ChunkRegs R;
-  if (sq.nch > 0) load_chunk<T>(p, sq, 0, h, v0, tid, R);
+  if (sq.nch > 0) load_chunk<T>(p, sq, chunk_at(0), h, v0, tid, R);
 #pragma unroll 1
-  for (int c = 0; c < sq.nch; ++c) {
+  for (int it = 0; it < sq.nch; ++it) {
+    const int c = chunk_at(it);
     const int L = min(BT, sq.eos - (sq.bos + c * BT));
 
     // chunk-start state, 8 columns (16 or 32 bytes) per store
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
       dst[1] = make_float4(x[4], x[5], x[6], x[7]);
     }
     __syncthreads();
-    if (c + 1 < sq.nch) load_chunk<T>(p, sq, c + 1, h, v0, tid, R);  // in flight below
+    if (it + 1 < sq.nch) load_chunk<T>(p, sq, chunk_at(it + 1), h, v0, tid, R);  // in flight below
 
     // h <- decay(h) + k~^T v~
     float dk = 1.f;
@@ -331,10 +344,12 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_tc_kernel(StateParams p
     C[nt][3] = ok ? p.h0[sB + col + 1] : 0.f;
   }
 
+  auto chunk_at = [&](int it) { return p.reverse ? sq.nch - 1 - it : it; };
   ChunkRegs R;
-  if (sq.nch > 0) load_chunk<__nv_bfloat16>(p, sq, 0, h, v0, tid, R);
+  if (sq.nch > 0) load_chunk<__nv_bfloat16>(p, sq, chunk_at(0), h, v0, tid, R);
 #pragma unroll 1
-  for (int c = 0; c < sq.nch; ++c) {
+  for (int it = 0; it < sq.nch; ++it) {
+    const int c = chunk_at(it);
     const int L = min(BT, sq.eos - (sq.bos + c * BT));
 
     // chunk-start state: two columns per 8-column tile and row
@@ -382,7 +397,7 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_tc_kernel(StateParams p
       *reinterpret_cast<uint4 *>(&vsl[vi][vq]) = lo;
     }
     __syncthreads();
-    if (c + 1 < sq.nch) load_chunk<__nv_bfloat16>(p, sq, c + 1, h, v0, tid, R);
+    if (it + 1 < sq.nch) load_chunk<__nv_bfloat16>(p, sq, chunk_at(it + 1), h, v0, tid, R);
 
     // decay: rows by e^{g_L} e^{gk_L[row]}, columns by e^{gv_L[col]}
     float dA = 1.f, dB = 1.f;

@@ -135,6 +135,25 @@ def decode_inputs(seed, B, T, H, HV, K, V, pool=None, state_std=0.05,
     }
 
 
+def _chunk_cumsum_gate(rng, gate, B, T, H, K, V, lengths, chunk):
+    """Gate values of the state passes: logsigmoid(N(0, 1) + 3) rates, as
+    chunk-local inclusive cumulative sums (fp32) except g_gamma."""
+    if gate is None:
+        return None
+    shape = {"g": (B, T, H), "gk": (B, T, H, K), "gv": (B, T, H, V), "g_gamma": (H,)}
+    raw = _logsigmoid(rng.standard_normal(shape[gate]) + GATE_SHIFT_SCALAR)
+    if gate == "g_gamma":
+        return raw
+    cu = np.concatenate([[0], np.cumsum(lengths)]) if lengths is not None else [0, T]
+    raw = raw.astype(np.float32)
+    gv = np.empty_like(raw)
+    for s0, e0 in zip(cu[:-1], cu[1:]):
+        for c in range(int(s0), int(e0), chunk):
+            ce = min(c + chunk, int(e0))
+            gv[:, c:ce] = np.cumsum(raw[:, c:ce], axis=1, dtype=np.float32)
+    return gv
+
+
 def state_pass_inputs(seed, B, T, H, K, V, gate, dtype=torch.bfloat16, lengths=None,
                       h0_std=None, chunk=64):
     """Inputs of one chunk state pass (gated linear attention).
@@ -151,20 +170,7 @@ def state_pass_inputs(seed, B, T, H, K, V, gate, dtype=torch.bfloat16, lengths=N
         assert B == 1 and sum(lengths) == T
     k = _unit_rows(rng.standard_normal((B, T, H, K)))
     v = rng.standard_normal((B, T, H, V))
-    shape = {"g": (B, T, H), "gk": (B, T, H, K), "gv": (B, T, H, V), "g_gamma": (H,)}
-    gv = None
-    if gate is not None:
-        raw = _logsigmoid(rng.standard_normal(shape[gate]) + GATE_SHIFT_SCALAR)
-        if gate == "g_gamma":
-            gv = raw
-        else:
-            cu = np.concatenate([[0], np.cumsum(lengths)]) if lengths is not None else [0, T]
-            raw = raw.astype(np.float32)
-            gv = np.empty_like(raw)
-            for s0, e0 in zip(cu[:-1], cu[1:]):
-                for c in range(int(s0), int(e0), chunk):
-                    ce = min(c + chunk, int(e0))
-                    gv[:, c:ce] = np.cumsum(raw[:, c:ce], axis=1, dtype=np.float32)
+    gv = _chunk_cumsum_gate(rng, gate, B, T, H, K, V, lengths, chunk)
     N = len(lengths) if lengths is not None else B
     h0 = None if h0_std is None else rng.standard_normal((N, H, K, V)) * h0_std
     return {
@@ -204,3 +210,29 @@ def decode(T=1):
 WORKLOADS = {
     "tiny": tiny, "gdn": gdn_prefill, "varlen": varlen_gqa, "kda": kda_prefill,
 }
+
+
+def state_grad_inputs(seed, B, T, HQ, H, K, V, gate, dtype=torch.bfloat16, lengths=None,
+                      dht_std=None, chunk=64):
+    """Inputs of one backward state pass: q ~ N(0, 1) L2-normalised per token
+    and do ~ N(0, 1) with HQ heads, the gate (as :func:`state_pass_inputs`)
+    with H heads, dht ~ N(0, dht_std) [N, HQ, K, V] or None.
+    Draw order: q, do, gate, dht.
+    """
+    rng = np.random.default_rng(seed)
+    if lengths is not None:
+        assert B == 1 and sum(lengths) == T
+    q = _unit_rows(rng.standard_normal((B, T, HQ, K)))
+    do = rng.standard_normal((B, T, HQ, V))
+    gv = _chunk_cumsum_gate(rng, gate, B, T, H, K, V, lengths, chunk)
+    N = len(lengths) if lengths is not None else B
+    dht = None if dht_std is None else rng.standard_normal((N, HQ, K, V)) * dht_std
+    return {
+        "q": _t(q, dtype), "do": _t(do, dtype), "gate": gate,
+        "gate_values": None if gv is None else _t(gv, torch.float32),
+        "dht": None if dht is None else _t(dht, torch.float32),
+        "cu_seqlens": None if lengths is None else torch.from_numpy(
+            np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)),
+        "scale": K ** -0.5,
+        "dims": dict(B=B, T=T, HQ=HQ, H=H, K=K, V=V, N=N),
+    }

@@ -203,6 +203,42 @@ typedef struct gdn_state_args {
 /* Enqueue the chunk state pass on `stream`. */
 gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *args, gdn_stream_t stream);
 
+/*
+ * Backward state pass (KDA _fla/ops/common/chunk_h.py: chunk_bwd_kernel_dh /
+ * chunk_bwd_dh): for the recurrence of gdn_chunk_state_fwd with outputs
+ * o_t = scale S_t^T q_t (S_t the state after token t), the gradient
+ * G = dL/dS of a loss with dL/do_t = do_t, going from the last token back:
+ *     G <- G + scale q_t do_t^T,   then   G <- decay_t^T(G)
+ * starting from dht (or zeros).  Per query head hq (gate head hq / (HQ / H)):
+ *   q [B,T,HQ,K], do [B,T,HQ,V]  dtype (GDN_F32 or GDN_BF16)
+ *   gate, gate_values            as gdn_chunk_state_fwd, with H heads
+ *   dht, dh0 [N,HQ,K,V]          float32, NULL = zeros / not returned
+ *   dh [C,HQ,K,V]                dh_dtype: the gradient with respect to the
+ *                                state at the end of every chunk (before that
+ *                                chunk's tokens are folded in), sequence after
+ *                                sequence; NULL = not returned; num_chunks = C
+ *   scale                        <= 0 selects 1/sqrt(K)
+ * Limits, errors and the rest as gdn_chunk_state_fwd; HQ % H == 0.
+ */
+typedef struct gdn_state_bwd_args {
+  int32_t dtype;               /* gdn_dtype_t of q, do */
+  const void *q, *do_;
+  int32_t gate;                /* gdn_gate_kind_t */
+  const float *gate_values;
+  const float *dht;
+  float *dh0;
+  void *dh;
+  int32_t dh_dtype;            /* gdn_dtype_t of dh */
+  const int32_t *cu_seqlens;
+  int32_t B, T, HQ, H, K, V, N;
+  int32_t chunk_size;
+  int64_t num_chunks;
+  float scale;
+} gdn_state_bwd_args;
+
+/* Enqueue the backward state pass on `stream`. */
+gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *args, gdn_stream_t stream);
+
 /* Bytes of device workspace gdn_chunk_fwd_host needs for these arguments.
  * Reads sizes, dtype and, when given, the host array cu_seqlens. */
 gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *bytes);

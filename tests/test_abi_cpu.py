@@ -15,7 +15,8 @@ import tempfile
 import pytest
 
 from gated_delta_rule_kk_gb300 import _lib, build_lib
-from gated_delta_rule_kk_gb300._lib import GdnChunkArgs, GdnDecodeArgs, GdnStateArgs, KdaChunkArgs, Status
+from gated_delta_rule_kk_gb300._lib import (GdnChunkArgs, GdnDecodeArgs, GdnStateArgs,
+                                            GdnStateBwdArgs, KdaChunkArgs, Status)
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
@@ -66,13 +67,15 @@ int main(void) {
   printf("kda_chunk_args size %zu\n", sizeof(kda_chunk_args));
   printf("gdn_decode_args size %zu\n", sizeof(gdn_decode_args));
   printf("gdn_state_args size %zu\n", sizeof(gdn_state_args));
+  printf("gdn_state_bwd_args size %zu\n", sizeof(gdn_state_bwd_args));
   %FIELDS%
   return 0;
 }
 """
     lines = []
     for cname, cls in (("gdn_chunk_args", GdnChunkArgs), ("kda_chunk_args", KdaChunkArgs),
-                       ("gdn_decode_args", GdnDecodeArgs), ("gdn_state_args", GdnStateArgs)):
+                       ("gdn_decode_args", GdnDecodeArgs), ("gdn_state_args", GdnStateArgs),
+                       ("gdn_state_bwd_args", GdnStateBwdArgs)):
         for fname, _ in cls._fields_:
             lines.append(f"F({cname}, {fname})")
     src = probe.replace("%FIELDS%", "\n  ".join(lines))
@@ -88,7 +91,8 @@ int main(void) {
             s, f, v = ln.split()
             got[(s, f)] = int(v)
     for cname, cls in (("gdn_chunk_args", GdnChunkArgs), ("kda_chunk_args", KdaChunkArgs),
-                       ("gdn_decode_args", GdnDecodeArgs), ("gdn_state_args", GdnStateArgs)):
+                       ("gdn_decode_args", GdnDecodeArgs), ("gdn_state_args", GdnStateArgs),
+                       ("gdn_state_bwd_args", GdnStateBwdArgs)):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for fname, _ in cls._fields_:
             assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
@@ -233,3 +237,20 @@ def test_state_pass_argument_errors(lib, change, expect):
     a = good_state(**change)
     assert lib.gdn_chunk_state_fwd(ctypes.byref(a), None) == expect
     assert lib.gdn_last_error_message().decode() != ""
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(H=3), Status.UNSUPPORTED),               # HQ = 4 not a multiple
+    (dict(do_=None), Status.INVALID_ARG),
+    (dict(scale=float("inf")), Status.INVALID_ARG),
+    (dict(K=20), Status.UNSUPPORTED),
+    (dict(num_chunks=1), Status.INVALID_ARG),
+    (dict(gate=1, gate_values=None), Status.INVALID_ARG),
+])
+def test_state_bwd_argument_errors(lib, change, expect):
+    a = dict(dtype=1, q=FAKE, do_=FAKE, gate=0, gate_values=None, dht=None, dh0=None, dh=FAKE,
+             dh_dtype=0, cu_seqlens=None, B=1, T=100, HQ=4, H=2, K=64, V=64, N=1, chunk_size=64,
+             num_chunks=2, scale=0.0)
+    a.update(change)
+    st = lib.gdn_chunk_state_bwd(ctypes.byref(GdnStateBwdArgs(**a)), None)
+    assert st == expect, (change, Status(st))

@@ -1,0 +1,107 @@
+"""gdn_chunk_state_bwd (backward state pass, the dh recurrence) against the oracle.
+
+Every gate kind on fp32 and bf16 inputs with ragged tails and a partial value
+tile, grouped query heads sharing a gate head, packed sequences with empty
+ones, bf16 chunk gradients, the default and an explicit scale, and an empty
+batch.  Like the forward pass the kernel computes in fp32 from the inputs as
+stored, so the fp32 bound (1e-4 RMS) applies to both input dtypes.
+"""
+import pytest
+import torch
+
+import gated_delta_rule_kk_gb300 as gdn
+from gated_delta_rule_kk_gb300 import Status, synth
+from oracle import state_pass as SP
+
+from _util import TOL_F32, assert_close
+
+pytestmark = pytest.mark.gpu
+
+GATES = [None, "g", "g_gamma", "gk", "gv"]
+
+
+def _dev(x):
+    return None if x is None else x.cuda()
+
+
+def run(inp, states_dtype=torch.float32, output_states=True, scale="inp"):
+    dh, dh0 = gdn.gdn_chunk_state_bwd(
+        inp["q"].cuda(), inp["do"].cuda(), gate=inp["gate"], gate_values=_dev(inp["gate_values"]),
+        dht=_dev(inp["dht"]), cu_seqlens=_dev(inp["cu_seqlens"]),
+        scale=inp["scale"] if scale == "inp" else scale, states_dtype=states_dtype,
+        output_states=output_states)
+    torch.cuda.synchronize()
+    assert gdn.gdn_check_device_error() == Status.OK
+    return dh, dh0
+
+
+def oracle(inp, scale="inp"):
+    return SP.chunk_state_grad(inp["q"], inp["do"], inp["gate"], inp["gate_values"],
+                               dht=inp["dht"], cu_seqlens=inp["cu_seqlens"],
+                               scale=inp["scale"] if scale == "inp" else scale)
+
+
+@pytest.mark.parametrize("gate", GATES)
+def test_fp32_every_gate(gate):
+    # T = 150: two full chunks and a 22-token tail; V = 48: one full and one half tile
+    inp = synth.state_grad_inputs(80, 2, 150, 3, 3, 32, 48, gate, dtype=torch.float32,
+                                  dht_std=0.3)
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert tuple(dh.shape) == dh_ref.shape
+    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate})")
+
+
+@pytest.mark.parametrize("gate", GATES)
+def test_bf16_inputs_full_width_grouped_heads(gate):
+    # K = 128 bf16 takes the tensor-core kernel; 4 query heads over 2 gate heads
+    inp = synth.state_grad_inputs(81, 1, 300, 4, 2, 128, 128, gate, dht_std=0.1)
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate})")
+
+
+def test_fp32_grouped_heads_and_default_scale():
+    inp = synth.state_grad_inputs(82, 2, 100, 6, 2, 64, 32, "gk", dtype=torch.float32,
+                                  dht_std=0.2)
+    dh, dh0 = run(inp, scale=None)
+    dh_ref, dh0_ref = oracle(inp, scale=None)
+    assert_close(dh, dh_ref, TOL_F32, "dh")
+    assert_close(dh0, dh0_ref, TOL_F32, "dh0")
+    dh2, _ = run(inp, scale=0.37)
+    dh2_ref, _ = oracle(inp, scale=0.37)
+    assert_close(dh2, dh2_ref, TOL_F32, "dh (scale 0.37)")
+
+
+def test_bf16_chunk_gradients_and_no_chunk_output():
+    inp = synth.state_grad_inputs(83, 2, 200, 2, 2, 64, 64, "g", dht_std=0.2)
+    dh, dh0 = run(inp, states_dtype=torch.bfloat16)
+    dh_ref, dh0_ref = oracle(inp)
+    assert dh.dtype == torch.bfloat16
+    assert_close(dh, dh_ref, TOL_F32, "dh (bf16)")
+    assert_close(dh0, dh0_ref, TOL_F32, "dh0")
+    none, dh0b = run(inp, output_states=False)
+    assert none is None
+    assert torch.equal(dh0b, dh0)
+
+
+@pytest.mark.parametrize("K,dtype", [(32, torch.float32), (128, torch.bfloat16)])
+def test_packed_sequences_with_empty_ones(K, dtype):
+    lengths = [70, 0, 130, 1, 64]
+    inp = synth.state_grad_inputs(84, 1, sum(lengths), 4, 2, K, 32, "gv", dtype=dtype,
+                                  lengths=lengths, dht_std=0.5)
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert dh.shape[0] == 2 + 0 + 3 + 1 + 1
+    assert_close(dh, dh_ref, TOL_F32, "dh")
+    assert_close(dh0, dh0_ref, TOL_F32, "dh0")
+    assert torch.equal(dh0[1].cpu(), inp["dht"][1])  # the empty sequence passes dht through
+
+
+def test_empty_batch_returns_dht():
+    inp = synth.state_grad_inputs(85, 2, 0, 2, 2, 32, 32, "g", dtype=torch.float32, dht_std=1.0)
+    dh, dh0 = run(inp)
+    assert dh.shape[0] == 0
+    assert torch.equal(dh0.cpu(), inp["dht"])
