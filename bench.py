@@ -366,6 +366,31 @@ def run_ours(args, rank, world, dev):
                              "algorithmic_bytes": sbytes,
                              "traffic": traffic_record(f"state_pass_{sgate}")}}
             del sk, sv, sg, sh0, shs, sht, sin
+        # backward state pass (dh recurrence), per-token gate
+        gin = synth.state_grad_inputs(6, 2, 4096, 16, 16, 128, 128, "g", dht_std=0.1)
+        gm = gin["dims"]
+        gq, gdo = gin["q"].to(dev), gin["do"].to(dev)
+        gg, gdht = gin["gate_values"].to(dev), gin["dht"].to(dev)
+        nchunk = gm["B"] * ((gm["T"] + 63) // 64)
+        gdh = torch.empty((nchunk, gm["HQ"], gm["K"], gm["V"]), dtype=torch.float32, device=dev)
+        gdh0 = torch.empty((gm["N"], gm["HQ"], gm["K"], gm["V"]), dtype=torch.float32, device=dev)
+        gms = time_steps(lambda: gdn.gdn_chunk_state_bwd(gq, gdo, gate="g", gate_values=gg,
+                                                         dht=gdht, scale=gin["scale"],
+                                                         out_states=gdh, dh0=gdh0),
+                         rsteps, max(3, args.warmup // 2), flush, stream)
+        gt_ = statistics.mean(gms)
+        per_tok = gm["HQ"] * (gm["K"] + gm["V"]) * 2 + gg.numel() * 4 // (gm["B"] * gm["T"])
+        gbytes = (gm["B"] * gm["T"] * per_tok + gdh.numel() * 4
+                  + 2 * gm["N"] * gm["HQ"] * gm["K"] * gm["V"] * 4)
+        rows["state_grad_g"] = {
+            "workload": "backward chunk state pass (dh recurrence): B=2, T=4096, HQ=H=16, "
+                        f"K=V=128, bf16 q/do, gate g, dht given, fp32 chunk gradients "
+                        f"[{nchunk},16,128,128] and dh0",
+            "tokens_per_s": gm["B"] * gm["T"] / (gt_ / 1e3), "ms_per_call": gt_,
+            "roofline": {"bound": "hbm", "achieved": gbytes / (gt_ / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": gbytes / (gt_ / 1e3) / 1e9 / hbm,
+                         "algorithmic_bytes": gbytes, "traffic": traffic_record("state_grad_g")}}
+        del gq, gdo, gg, gdht, gdh, gdh0, gin
         for T in (1, 2, 3, 4):
             din = synth.decode(T)
             dd = to_dev(din, dev)
