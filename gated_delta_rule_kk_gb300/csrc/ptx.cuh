@@ -253,6 +253,26 @@ __device__ __forceinline__ void ldmatrix_x4(const void *row_addr, uint32_t &r0, 
 
 // As ldmatrix_x4, each 8x8 matrix transposed (lane i supplies row i % 8 of
 // matrix i / 8 as stored; a register holds two elements of one stored column).
+// Asynchronous global -> shared copies of 16 or 4 bytes; with ok = false the
+// destination is zero-filled and nothing is read.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(gsrc), "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(gsrc), "r"(ok ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void ldmatrix_x4_trans(const void *row_addr, uint32_t &r0,
                                                   uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"

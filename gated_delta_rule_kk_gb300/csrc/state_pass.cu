@@ -12,17 +12,18 @@
 // and the factors e^{gamma_i} measured from the chunk's start:
 //   dh_{c} = e^{g_L} diag(e^{gk_L}) dh_{c+1} diag(e^{gv_L}) + sum_i q~_i do~_i^T.
 //
-// Two kernels, one CTA per (32-column tile of V, head, sequence), 256 threads,
-// the fp32 state in registers across the chunks.  A chunk's k, v and gates are
+// Two kernels, one CTA per (32-column tile of V, head, sequence), the fp32
+// state in registers across the chunks.  A chunk's k, v and gates are
 // loaded into registers (16-byte loads; K and V are multiples of 8) while the
 // previous chunk is computed, then staged in shared memory with the gate
 // factors applied.
 //   state_pass_kernel     exact fp32 FMAs; every thread holds one key row x
 //                         16 columns (any K <= 128, fp32 or bf16 inputs)
-//   state_pass_tc_kernel  bf16 inputs with K = 128: warp w holds key rows
-//                         16 w .. 16 w + 15 as m16n8k16 accumulators and adds
-//                         k~^T v~ on the tensor cores from bf16 hi/lo pairs of
-//                         k~ and v~ (hi.hi + hi.lo + lo.hi: fp32-grade products)
+//   state_pass_tc_kernel  bf16 inputs with K = 128, 512 threads: each warp
+//                         holds 16 key rows x 16 columns as m16n8k16
+//                         accumulators and adds k~^T v~ on the tensor cores
+//                         from bf16 hi/lo pairs of k~ and v~ (hi.hi + hi.lo +
+//                         lo.hi: fp32-grade products), operands double-buffered
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "ptx.cuh"
@@ -309,34 +310,216 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
 
 // ---------------------------------------------------------------------------
 // tensor-core kernel (bf16 inputs, K = 128)
+//
+// 512 threads.  Warp w holds key rows 16 (w & 7) .. + 15 and columns
+// 16 (w >> 3) .. + 15 of the 32-column tile as two m16n8k16 accumulators.
+// Raw chunks (k, v and the gate rows) stream into a ring of RING slots by
+// asynchronous copies issued several steps ahead.  In the step of chunk c
+// every thread stages chunk c+1 from the ring into the other operand buffer,
+// refills a free ring slot, then runs the MMAs of chunk c, so staging and
+// tensor-core work of different warps overlap and a step needs one barrier.
+//
+// The token-dependent gate factors and the backward scale go on v~ (staged
+// as a bf16 hi/lo pair).  k then stays exact in bf16 and is read by the MMAs
+// straight from the ring (C += k^T (v~hi + v~lo)), except with the per-key
+// gate (KSTAGE), whose factor e^{gk_L - gk_i} depends on key and token: there
+// k~ is staged as a hi/lo pair too (C += k~hi^T v~hi + k~hi^T v~lo + k~lo^T v~hi).
 
-// Row pitches of the staged operands (bf16): 272 B and 80 B, so the eight
-// 16-byte rows an ldmatrix reads fall in eight different bank quads.
+constexpr int TC_THREADS = 512;
+// Row pitches of the operands (bf16): 272 B and 80 B, so the eight 16-byte
+// rows an ldmatrix reads fall in eight different bank quads.
 constexpr int TC_KP = 136;
 constexpr int TC_VP = 40;
+constexpr uint32_t TC_KS = BT * TC_KP * 2, TC_VS = BT * TC_VP * 2;  // one tile, bytes
+// Operand buffer: [k~ hi, k~ lo] (KSTAGE only), then v~ hi, v~ lo.
+__host__ __device__ constexpr uint32_t tc_buf_bytes(bool kstage) {
+  return (kstage ? 2 * TC_KS : 0) + 2 * TC_VS;
+}
+// A ring slot: raw k [64][TC_KP] bf16 (rows padded like the operands), raw v
+// [64][32] bf16, then the gate rows (g: [64] fp32, gk: [64][128] fp32,
+// gv: [64][32] fp32; none for g_gamma).
+constexpr uint32_t RS_K = 0, RS_V = TC_KS, RS_G = RS_V + BT * SP_VT * 2;
+__host__ __device__ constexpr uint32_t ring_slot_bytes(int gate) {
+  return RS_G + (gate == GDN_GATE_G    ? BT * 4
+                 : gate == GDN_GATE_GK ? BT * KMAX * 4
+                 : gate == GDN_GATE_GV ? BT * SP_VT * 4
+                                       : 0);
+}
 
-__global__ void __launch_bounds__(SP_THREADS) state_pass_tc_kernel(StateParams p) {
-  __shared__ __align__(16) __nv_bfloat16 ksh[BT][TC_KP], ksl[BT][TC_KP];  // k~ hi, lo
-  __shared__ __align__(16) __nv_bfloat16 vsh[BT][TC_VP], vsl[BT][TC_VP];  // v~ hi, lo
-  __shared__ float gam[BT], gkl[KMAX], gvl[SP_VT];
+// Issue the copies of chunk c into a ring slot (rows past the chunk's end and
+// columns past V are zero-filled).
+__device__ __forceinline__ void tc_fetch(const StateParams &p, const SeqInfo &sq, int c, int h,
+                                         int v0, int tid, unsigned char *slot) {
+  const int H = p.H, V = p.V, HG = p.HG, hg = h / (H / HG);
+  constexpr int K = KMAX;
+  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+  const float *gvals = p.gate_values;
+  const int t0 = sq.bos + c * BT;
+  const int L = min(BT, sq.eos - t0);
+  const size_t row0 = (size_t)sq.b * p.T + t0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {  // k: 64 rows x 16 pieces
+    const int piece = tid + TC_THREADS * j, i = piece >> 4, q = piece & 15;
+    const bool ok = i < L;
+    ptx::cp_async16(slot + RS_K + (i * TC_KP + 8 * q) * 2,
+                    k + ((row0 + (ok ? i : 0)) * H + h) * K + 8 * q, ok);
+  }
+  if (tid < 4 * BT) {  // v: 64 rows x 4 pieces
+    const int i = tid >> 2, q = tid & 3;
+    const bool ok = i < L && v0 + 8 * q < V;
+    ptx::cp_async16(slot + RS_V + (i * SP_VT + 8 * q) * 2,
+                    v + ((row0 + (ok ? i : 0)) * H + h) * V + (ok ? v0 + 8 * q : 0), ok);
+  }
+  if (p.gate == GDN_GATE_G) {
+    if (tid < BT) {
+      const bool ok = tid < L;
+      ptx::cp_async4(slot + RS_G + tid * 4, gvals + (row0 + (ok ? tid : 0)) * HG + hg, ok);
+    }
+  } else if (p.gate == GDN_GATE_GK) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // 64 rows x 32 pieces
+      const int piece = tid + TC_THREADS * j, i = piece >> 5, q = piece & 31;
+      const bool ok = i < L;
+      ptx::cp_async16(slot + RS_G + (i * K + 4 * q) * 4,
+                      gvals + ((row0 + (ok ? i : 0)) * HG + hg) * K + 4 * q, ok);
+    }
+  } else if (p.gate == GDN_GATE_GV) {  // 64 rows x 8 pieces
+    const int i = tid >> 3, q = tid & 7;
+    const bool ok = i < L && v0 + 4 * q < V;  // V, v0 multiples of 8: the piece is whole
+    ptx::cp_async16(slot + RS_G + (i * SP_VT + 4 * q) * 4,
+                    gvals + ((row0 + (ok ? i : 0)) * HG + hg) * V + (ok ? v0 + 4 * q : 0), ok);
+  }
+}
+
+// Decay of the accumulators over one chunk (rows rA, rA + 8; columns of the
+// two n-tiles, two each) and the chunk's valid row count.
+struct TcDecay {
+  float r[2], c[4];
+  int L;
+};
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 &u, float *out) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    out[2 * q] = __uint_as_float(w[q] << 16);
+    out[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void ld8_shared(const float *src, float *out) {
+  const float4 a = reinterpret_cast<const float4 *>(src)[0];
+  const float4 b = reinterpret_cast<const float4 *>(src)[1];
+  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+
+// Stage a chunk (L valid rows) from a ring slot into an operand buffer and
+// return its accumulator decay.  Forward: v~ = v e^{g_L - g_i} e^{gv_L - gv_i}
+// (and k~ = k e^{gk_L - gk_i}); backward: v~ = scale do e^{g_i} e^{gv_i} (and
+// k~ = q e^{gk_i}).  Rows past the chunk's end are zeros and take no factor.
+template <bool KSTAGE>
+__device__ __forceinline__ void tc_stage(const StateParams &p, const unsigned char *slot, int L,
+                                         float gamma, unsigned char *buf, int tid, int rA, int cl,
+                                         TcDecay &d) {
+  constexpr int K = KMAX;
+  const bool gvg = p.gate == GDN_GATE_GV;
+  const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
+  const float *gr = reinterpret_cast<const float *>(slot + RS_G);
+  if (KSTAGE) {  // per-key gate
+    const int kq = (tid & 15) * 8;
+    __nv_bfloat16(*ksh)[TC_KP] = reinterpret_cast<__nv_bfloat16(*)[TC_KP]>(buf);
+    __nv_bfloat16(*ksl)[TC_KP] = reinterpret_cast<__nv_bfloat16(*)[TC_KP]>(buf + TC_KS);
+    float gkl[8];
+    if (!p.reverse) ld8_shared(gr + (L - 1) * K + kq, gkl);
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+      const int i = (tid >> 4) + 32 * pp;
+      float x[8];
+      unpack8_bf16(*reinterpret_cast<const uint4 *>(slot + RS_K + (i * TC_KP + kq) * 2), x);
+      if (i < L) {
+        float gi[8];
+        ld8_shared(gr + i * K + kq, gi);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= expf(p.reverse ? gi[e] : gkl[e] - gi[e]);
+      }
+      uint4 hi, lo;
+      split8_bf16(x, hi, lo);
+      *reinterpret_cast<uint4 *>(&ksh[i][kq]) = hi;
+      *reinterpret_cast<uint4 *>(&ksl[i][kq]) = lo;
+    }
+  }
+  float glast = 0.f;
+  if (p.gate == GDN_GATE_G) glast = gr[L - 1];
+  if (p.gate == GDN_GATE_G_GAMMA) glast = gamma * (float)L;
+  if (tid < 4 * BT) {
+    const int vi = tid >> 2, vq = (tid & 3) * 8;
+    unsigned char *vb = buf + (KSTAGE ? 2 * TC_KS : 0);
+    __nv_bfloat16(*vsh)[TC_VP] = reinterpret_cast<__nv_bfloat16(*)[TC_VP]>(vb);
+    __nv_bfloat16(*vsl)[TC_VP] = reinterpret_cast<__nv_bfloat16(*)[TC_VP]>(vb + TC_VS);
+    float x[8];
+    unpack8_bf16(*reinterpret_cast<const uint4 *>(slot + RS_V + (vi * SP_VT + vq) * 2), x);
+    float sf = p.reverse ? p.scale : 1.f;
+    if (scalar_gate && vi < L) {
+      const float gi = p.gate == GDN_GATE_G ? gr[vi] : gamma * (float)(vi + 1);
+      sf *= expf(p.reverse ? gi : glast - gi);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] *= sf;
+    if (gvg && vi < L) {
+      float gi[8], gl[8];
+      ld8_shared(gr + vi * SP_VT + vq, gi);
+      ld8_shared(gr + (L - 1) * SP_VT + vq, gl);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= expf(p.reverse ? gi[e] : gl[e] - gi[e]);
+    }
+    uint4 hi, lo;
+    split8_bf16(x, hi, lo);
+    *reinterpret_cast<uint4 *>(&vsh[vi][vq]) = hi;
+    *reinterpret_cast<uint4 *>(&vsl[vi][vq]) = lo;
+  }
+  d.L = L;
+  d.r[0] = d.r[1] = scalar_gate ? expf(glast) : 1.f;
+  if (KSTAGE) {
+    d.r[0] = expf(gr[(L - 1) * K + rA]);
+    d.r[1] = expf(gr[(L - 1) * K + rA + 8]);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    d.c[j] = gvg ? expf(gr[(L - 1) * SP_VT + cl + 8 * (j >> 1) + (j & 1)]) : 1.f;
+}
+
+// RING slots; KSTAGE: the per-key gate (k~ staged; RING = 2 for its 32 KB gate
+// rows).  Without KSTAGE the MMAs of a step read k from its ring slot, so a
+// slot is refilled one step later (LAG = 1) than when only staging reads it.
+template <int RING, bool KSTAGE>
+__global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParams p) {
+  constexpr int LAG = KSTAGE ? 0 : 1;
+  static_assert(RING >= 2 + LAG, "the ring must hold the staged, the computed and a refilled slot");
+  extern __shared__ __align__(16) unsigned char tc_smem[];
   __shared__ long long seq_info[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tig = lane & 3;
+  const int kb = warp & 7, ch = warp >> 3;  // key block, column half
   const int v0 = blockIdx.x * SP_VT, h = blockIdx.y, n = blockIdx.z;
   const int H = p.H, V = p.V;
   constexpr int K = KMAX;
-  const bool gk = p.gate == GDN_GATE_GK, gvg = p.gate == GDN_GATE_GV;
-  const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
+  constexpr uint32_t BUF = tc_buf_bytes(KSTAGE);
+  // g_gamma: the block's per-head rate (gamma_i = rate (i + 1))
+  const float gamma = p.gate == GDN_GATE_G_GAMMA ? p.gate_values[h / (H / p.HG)] : 0.f;
   const SeqInfo sq = sequence_of(p, n, tid, seq_info);
+  unsigned char *ring = tc_smem + 2 * BUF;
+  const uint32_t slot_bytes = ring_slot_bytes(p.gate);
+  auto slot_of = [&](int it) { return ring + (uint32_t)(it % RING) * slot_bytes; };
 
-  // accumulator rows rA = 16 warp + g and rA + 8, columns v0 + 8 nt + 2 tig (+ 1)
-  const int rA = 16 * warp + g;
-  float C[4][4];
+  // accumulator rows rA = 16 kb + g and rA + 8, columns v0 + cl + 8 nt (+ 1)
+  const int rA = 16 * kb + g, cl = 16 * ch + 2 * tig, cB = v0 + cl;
+  float C[2][4];
   const size_t sA = (((size_t)n * H + h) * K + rA) * V, sB = sA + (size_t)8 * V;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    const int col = v0 + 8 * nt + 2 * tig;
+  for (int nt = 0; nt < 2; ++nt) {
+    const int col = cB + 8 * nt;
     const bool ok = p.h0 && col < V;  // V is a multiple of 8, so col + 1 < V too
     C[nt][0] = ok ? p.h0[sA + col] : 0.f;
     C[nt][1] = ok ? p.h0[sA + col + 1] : 0.f;
@@ -344,20 +527,33 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_tc_kernel(StateParams p
     C[nt][3] = ok ? p.h0[sB + col + 1] : 0.f;
   }
 
+  // chunk of the it-th step: forward from the first, backward from the last
   auto chunk_at = [&](int it) { return p.reverse ? sq.nch - 1 - it : it; };
-  ChunkRegs R;
-  if (sq.nch > 0) load_chunk<__nv_bfloat16>(p, sq, chunk_at(0), h, v0, tid, R);
+  auto rows_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
+  // The ring starts with steps 0 .. RING-1, one copy group each (empty past
+  // the end); step it commits one more group, holding step it - LAG + RING.
+#pragma unroll
+  for (int j = 0; j < RING; ++j) {
+    if (j < sq.nch) tc_fetch(p, sq, chunk_at(j), h, v0, tid, slot_of(j));
+    ptx::cp_async_commit();
+  }
+  TcDecay dec;
+  if (sq.nch > 0) {
+    ptx::cp_async_wait<RING - 2>();  // steps 0 and 1 have landed
+    __syncthreads();
+    tc_stage<KSTAGE>(p, slot_of(0), rows_of(0), gamma, tc_smem, tid, rA, cl, dec);
+  }
+  __syncthreads();
 #pragma unroll 1
   for (int it = 0; it < sq.nch; ++it) {
     const int c = chunk_at(it);
-    const int L = min(BT, sq.eos - (sq.bos + c * BT));
 
     // chunk-start state: two columns per 8-column tile and row
     if (sq.write_hs) {
       const size_t oA = (((size_t)(sq.first + c) * H + h) * K + rA) * V, oB = oA + (size_t)8 * V;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = v0 + 8 * nt + 2 * tig;
+      for (int nt = 0; nt < 2; ++nt) {
+        const int col = cB + 8 * nt;
         if (col >= V) continue;
         if (p.hs_bf16) {
           __nv_bfloat16 *hb = static_cast<__nv_bfloat16 *>(p.hs);
@@ -371,89 +567,67 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_tc_kernel(StateParams p
       }
     }
 
-    // stage k~ and v~ as bf16 hi/lo pairs
-    if (scalar_gate && tid < BT) gam[tid] = R.gtok;
-    if (gk && tid < K) gkl[tid] = R.glast;
-    if (gvg && tid < SP_VT) gvl[tid] = R.glast;
-    __syncthreads();
-    const float gL = scalar_gate ? gam[L - 1] : 0.f;
-#pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      float x[8];
-      gated_k(p, R, pp, tid, L, gkl, x);
-      uint4 hi, lo;
-      split8_bf16(x, hi, lo);
-      const int i = (tid >> 4) + 16 * pp, kq = (tid & 15) * 8;
-      *reinterpret_cast<uint4 *>(&ksh[i][kq]) = hi;
-      *reinterpret_cast<uint4 *>(&ksl[i][kq]) = lo;
-    }
-    {
-      float x[8];
-      gated_v(p, R, tid, L, gL, gam, gvl, x);
-      uint4 hi, lo;
-      split8_bf16(x, hi, lo);
-      const int vi = tid >> 2, vq = (tid & 3) * 8;
-      *reinterpret_cast<uint4 *>(&vsh[vi][vq]) = hi;
-      *reinterpret_cast<uint4 *>(&vsl[vi][vq]) = lo;
-    }
-    __syncthreads();
-    if (it + 1 < sq.nch) load_chunk<__nv_bfloat16>(p, sq, chunk_at(it + 1), h, v0, tid, R);
-
     // decay: rows by e^{g_L} e^{gk_L[row]}, columns by e^{gv_L[col]}
-    float dA = 1.f, dB = 1.f;
-    if (scalar_gate) dA = dB = expf(gL);
-    if (gk) {
-      dA = expf(gkl[rA]);
-      dB = expf(gkl[rA + 8]);
-    }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      float d0 = 1.f, d1 = 1.f;
-      if (gvg) {
-        d0 = expf(gvl[8 * nt + 2 * tig]);
-        d1 = expf(gvl[8 * nt + 2 * tig + 1]);
-      }
-      C[nt][0] *= dA * d0;
-      C[nt][1] *= dA * d1;
-      C[nt][2] *= dB * d0;
-      C[nt][3] *= dB * d1;
+    for (int nt = 0; nt < 2; ++nt) {
+      C[nt][0] *= dec.r[0] * dec.c[2 * nt];
+      C[nt][1] *= dec.r[0] * dec.c[2 * nt + 1];
+      C[nt][2] *= dec.r[1] * dec.c[2 * nt];
+      C[nt][3] *= dec.r[1] * dec.c[2 * nt + 1];
     }
+    const int L = dec.L;
 
-    // C += k~^T v~ over the chunk's tokens, 16 at a time.  A = k~^T (this
-    // warp's 16 keys x 16 tokens) and B = v~ (16 tokens x 16 columns) come
-    // from the token-major tiles by transposing ldmatrix.
+    // the next step's operands into the other buffer; the slot of step
+    // it - LAG (read out before the last barrier) takes step it - LAG + RING
+    if (it + 1 < sq.nch)
+      tc_stage<KSTAGE>(p, slot_of(it + 1), rows_of(it + 1), gamma,
+                       tc_smem + ((it + 1) & 1) * BUF, tid, rA, cl, dec);
+    if (it >= LAG && it - LAG + RING < sq.nch)
+      tc_fetch(p, sq, chunk_at(it - LAG + RING), h, v0, tid, slot_of(it - LAG));
+    ptx::cp_async_commit();
+
+    // C += k~^T v~ over this chunk's tokens, 16 at a time.  A = k~^T (16 keys
+    // x 16 tokens) and B = v~ (16 tokens x 16 columns) come from token-major
+    // tiles by transposing ldmatrix.
+    const unsigned char *buf = tc_smem + (it & 1) * BUF;
+    const __nv_bfloat16(*ksh)[TC_KP] = reinterpret_cast<const __nv_bfloat16(*)[TC_KP]>(
+        KSTAGE ? buf : slot_of(it) + RS_K);
+    const __nv_bfloat16(*ksl)[TC_KP] = reinterpret_cast<const __nv_bfloat16(*)[TC_KP]>(buf + TC_KS);
+    const unsigned char *vb = buf + (KSTAGE ? 2 * TC_KS : 0);
+    const __nv_bfloat16(*vsh)[TC_VP] = reinterpret_cast<const __nv_bfloat16(*)[TC_VP]>(vb);
+    const __nv_bfloat16(*vsl)[TC_VP] = reinterpret_cast<const __nv_bfloat16(*)[TC_VP]>(vb + TC_VS);
 #pragma unroll
     for (int kt = 0; kt < 4; ++kt) {
       if (16 * kt >= L) break;
-      uint32_t ah[4], al[4];
-      {
-        const int row = 16 * kt + (lane & 7) + ((lane >> 4) << 3);
-        const int key = 16 * warp + ((lane >> 3) & 1) * 8;
-        ptx::ldmatrix_x4_trans(&ksh[row][key], ah[0], ah[1], ah[2], ah[3]);
-        ptx::ldmatrix_x4_trans(&ksl[row][key], al[0], al[1], al[2], al[3]);
-      }
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t bh[4], bl[4];
-        const int row = 16 * kt + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int col = 16 * np + ((lane >> 4) << 3);
-        ptx::ldmatrix_x4_trans(&vsh[row][col], bh[0], bh[1], bh[2], bh[3]);
-        ptx::ldmatrix_x4_trans(&vsl[row][col], bl[0], bl[1], bl[2], bl[3]);
-        ptx::mma_16816_bf16(C[2 * np], ah, bh[0], bh[1]);
-        ptx::mma_16816_bf16(C[2 * np], ah, bl[0], bl[1]);
-        ptx::mma_16816_bf16(C[2 * np], al, bh[0], bh[1]);
-        ptx::mma_16816_bf16(C[2 * np + 1], ah, bh[2], bh[3]);
-        ptx::mma_16816_bf16(C[2 * np + 1], ah, bl[2], bl[3]);
-        ptx::mma_16816_bf16(C[2 * np + 1], al, bh[2], bh[3]);
+      uint32_t ah[4], al[4], bh[4], bl[4];
+      const int arow = 16 * kt + (lane & 7) + ((lane >> 4) << 3);
+      const int key = 16 * kb + ((lane >> 3) & 1) * 8;
+      ptx::ldmatrix_x4_trans(&ksh[arow][key], ah[0], ah[1], ah[2], ah[3]);
+      if (KSTAGE) ptx::ldmatrix_x4_trans(&ksl[arow][key], al[0], al[1], al[2], al[3]);
+      const int brow = 16 * kt + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int col = 16 * ch + ((lane >> 4) << 3);
+      ptx::ldmatrix_x4_trans(&vsh[brow][col], bh[0], bh[1], bh[2], bh[3]);
+      ptx::ldmatrix_x4_trans(&vsl[brow][col], bl[0], bl[1], bl[2], bl[3]);
+      ptx::mma_16816_bf16(C[0], ah, bh[0], bh[1]);
+      ptx::mma_16816_bf16(C[1], ah, bh[2], bh[3]);
+      ptx::mma_16816_bf16(C[0], ah, bl[0], bl[1]);
+      ptx::mma_16816_bf16(C[1], ah, bl[2], bl[3]);
+      if (KSTAGE) {
+        ptx::mma_16816_bf16(C[0], al, bh[0], bh[1]);
+        ptx::mma_16816_bf16(C[1], al, bh[2], bh[3]);
       }
     }
-    __syncthreads();  // the next chunk restages the operands and the gates
+    // step it + 2's copies have landed (this thread's); the barrier makes them
+    // and the staged buffer visible and frees this step's buffer and slot
+    ptx::cp_async_wait<RING - 2 - LAG>();
+    __syncthreads();
   }
+  ptx::cp_async_wait<0>();  // no copy outlives the block
 
   if (p.ht) {
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = v0 + 8 * nt + 2 * tig;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = cB + 8 * nt;
       if (col >= V) continue;
       p.ht[sA + col] = C[nt][0];
       p.ht[sA + col + 1] = C[nt][1];
@@ -467,12 +641,22 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_tc_kernel(StateParams p
 
 cudaError_t launch_state_pass(const StateParams &p, bool bf16, cudaStream_t stream) {
   const dim3 grid((unsigned)((p.V + SP_VT - 1) / SP_VT), (unsigned)p.H, (unsigned)p.N);
-  if (bf16 && p.K == KMAX)
-    state_pass_tc_kernel<<<grid, SP_THREADS, 0, stream>>>(p);
-  else if (bf16)
+  if (bf16 && p.K == KMAX) {
+    // per-key gate: k~ staged, two ring slots (its gate rows are 32 KB a
+    // chunk); otherwise six slots, four steps of copies in flight
+    const bool kstage = p.gate == GDN_GATE_GK;
+    const int ring = kstage ? 2 : 6;
+    const int smem = (int)(2 * tc_buf_bytes(kstage) + ring * ring_slot_bytes(p.gate));
+    auto kern = kstage ? state_pass_tc_kernel<2, true> : state_pass_tc_kernel<6, false>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, TC_THREADS, smem, stream>>>(p);
+  } else if (bf16) {
     state_pass_kernel<__nv_bfloat16><<<grid, SP_THREADS, 0, stream>>>(p);
-  else
+  } else {
     state_pass_kernel<float><<<grid, SP_THREADS, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
