@@ -96,6 +96,10 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
 
 gdn_status_t cuda_status(cudaError_t e, const char *what) {
   if (e == cudaSuccess) return GDN_OK;
+  // The status carries the error; take it out of the runtime's last-error
+  // slot so that the caller's next, unrelated CUDA call does not report it
+  // (a sticky error stays in the context whatever this does).
+  (void)cudaGetLastError();
   return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 

@@ -297,6 +297,7 @@ bool is_device_memory(const void *p) {
 }
 
 gdn_status_t cuda_fail(cudaError_t e, const char *what) {
+  (void)cudaGetLastError();  // reported here, not by the caller's next CUDA call
   char msg[200];
   snprintf(msg, sizeof(msg), "%s: %s", what, cudaGetErrorString(e));
   return set_host_error(GDN_ERR_CUDA, msg);

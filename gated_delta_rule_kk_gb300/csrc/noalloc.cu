@@ -41,12 +41,14 @@ void *g_scratch_ptr[MAX_DEVICES] = {nullptr};
 void *scratch_address(gdn_status_t *st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+    (void)cudaGetLastError();
     *st = GDN_ERR_CUDA;
     return nullptr;
   }
   if (g_scratch_ptr[dev] == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
       *st = GDN_ERR_CUDA;
       return nullptr;
     }

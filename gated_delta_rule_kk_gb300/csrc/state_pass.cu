@@ -393,10 +393,9 @@ __device__ __forceinline__ void tc_fetch(const StateParams &p, const SeqInfo &sq
 }
 
 // Decay of the accumulators over one chunk (rows rA, rA + 8; columns of the
-// two n-tiles, two each) and the chunk's valid row count.
+// two n-tiles, two each).
 struct TcDecay {
   float r[2], c[4];
-  int L;
 };
 
 __device__ __forceinline__ void unpack8_bf16(const uint4 &u, float *out) {
@@ -478,7 +477,6 @@ __device__ __forceinline__ void tc_stage(const StateParams &p, const unsigned ch
     *reinterpret_cast<uint4 *>(&vsh[vi][vq]) = hi;
     *reinterpret_cast<uint4 *>(&vsl[vi][vq]) = lo;
   }
-  d.L = L;
   d.r[0] = d.r[1] = scalar_gate ? expf(glast) : 1.f;
   if (KSTAGE) {
     d.r[0] = expf(gr[(L - 1) * K + rA]);
@@ -575,7 +573,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
       C[nt][2] *= dec.r[1] * dec.c[2 * nt];
       C[nt][3] *= dec.r[1] * dec.c[2 * nt + 1];
     }
-    const int L = dec.L;
 
     // the next step's operands into the other buffer; the slot of step
     // it - LAG (read out before the last barrier) takes step it - LAG + RING
@@ -586,9 +583,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
       tc_fetch(p, sq, chunk_at(it - LAG + RING), h, v0, tid, slot_of(it - LAG));
     ptx::cp_async_commit();
 
-    // C += k~^T v~ over this chunk's tokens, 16 at a time.  A = k~^T (16 keys
-    // x 16 tokens) and B = v~ (16 tokens x 16 columns) come from token-major
-    // tiles by transposing ldmatrix.
+    // C += k~^T v~ over the chunk's 64 rows, 16 at a time (rows past its end
+    // are zeros).  A = k~^T (16 keys x 16 tokens) and B = v~ (16 tokens x 16
+    // columns) come from token-major tiles by transposing ldmatrix.
     const unsigned char *buf = tc_smem + (it & 1) * BUF;
     const __nv_bfloat16(*ksh)[TC_KP] = reinterpret_cast<const __nv_bfloat16(*)[TC_KP]>(
         KSTAGE ? buf : slot_of(it) + RS_K);
@@ -598,7 +595,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
     const __nv_bfloat16(*vsl)[TC_VP] = reinterpret_cast<const __nv_bfloat16(*)[TC_VP]>(vb + TC_VS);
 #pragma unroll
     for (int kt = 0; kt < 4; ++kt) {
-      if (16 * kt >= L) break;
       uint32_t ah[4], al[4], bh[4], bl[4];
       const int arow = 16 * kt + (lane & 7) + ((lane >> 4) << 3);
       const int key = 16 * kb + ((lane >> 3) & 1) * 8;
