@@ -2,7 +2,7 @@
 // accumulators, TMA and bulk copies), bf16 inputs, K = 128, V in {32..128}
 // a multiple of 32.
 //
-// Two kernels per call (plus a one-thread chunk-table kernel for packed
+// Two kernels per call (plus a small chunk-table kernel for packed
 // sequences):
 //
 // 1. intra: one CTA per (chunk, value head), all chunks in parallel.  With
@@ -115,7 +115,7 @@ struct TcParams {
   float *ht;
   __nv_bfloat16 *o;
   const int32_t *cu_seqlens;
-  int32_t *table;          // [N + 1] chunk offsets (packed sequences)
+  int32_t *table;          // [N + 1] chunk offsets, then [N] chain order (packed sequences)
   unsigned char *blocks;   // per (chunk, head) operand blocks
   const void *kraw, *qraw;  // KDA exact fallback reads raw k/q
   int *err;
@@ -126,18 +126,43 @@ struct TcParams {
 };
 
 // ---------------------------------------------------------------------------
-// chunk table for packed sequences: table[n] = sum_{m<n} ceil(len_m / 64)
-__global__ void chunk_table_kernel(const int32_t *cu, int N, int T, int32_t *table, int *err) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  bool ok = cu[0] == 0 && cu[N] == T;
-  for (int n = 0; n < N && ok; ++n) ok = cu[n + 1] >= cu[n];
-  if (!ok) record_error(err, GDN_ERR_BAD_SEQLENS);
-  int acc = 0;
-  for (int n = 0; n < N; ++n) {
-    table[n] = acc;
-    if (ok) acc += (cu[n + 1] - cu[n] + BT - 1) / BT;
+// Chunk table for packed sequences: table[n] = sum_{m<n} ceil(len_m / 64)
+// for n = 0..N, then the order in which the chain kernel takes the sequences:
+// by decreasing chunk count (ties by index) when N <= ORDER_MAX, else by
+// index.  The chain CTAs are dispatched in that order, so the longest chains,
+// which set the call's length, start first.
+constexpr int TABLE_THREADS = 512, ORDER_MAX = 1024;
+__global__ void __launch_bounds__(TABLE_THREADS)
+    chunk_table_kernel(const int32_t *cu, int N, int T, int32_t *table, int *err) {
+  __shared__ int cnt[ORDER_MAX];
+  __shared__ int valid;
+  const int tid = threadIdx.x;
+  int32_t *order = table + N + 1;
+  if (tid == 0) {
+    bool ok = cu[0] == 0 && cu[N] == T;
+    for (int n = 0; n < N && ok; ++n) ok = cu[n + 1] >= cu[n];
+    if (!ok) record_error(err, GDN_ERR_BAD_SEQLENS);
+    int acc = 0;
+    for (int n = 0; n < N; ++n) {
+      table[n] = acc;
+      if (ok) acc += (cu[n + 1] - cu[n] + BT - 1) / BT;
+    }
+    table[N] = acc;
+    valid = ok ? 1 : 0;
   }
-  table[N] = acc;
+  __syncthreads();
+  if (!valid || N > ORDER_MAX) {
+    for (int n = tid; n < N; n += TABLE_THREADS) order[n] = n;
+    return;
+  }
+  for (int n = tid; n < N; n += TABLE_THREADS) cnt[n] = (cu[n + 1] - cu[n] + BT - 1) / BT;
+  __syncthreads();
+  for (int n = tid; n < N; n += TABLE_THREADS) {
+    const int c = cnt[n];
+    int rank = 0;  // position of n under (count descending, index ascending)
+    for (int m = 0; m < N; ++m) rank += (cnt[m] > c) || (cnt[m] == c && m < n);
+    order[rank] = n;
+  }
 }
 
 // Map a global chunk id to (sequence, chunk-in-sequence, token bounds).
@@ -829,7 +854,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   const int vt = blockIdx.x;
   const int v0 = vt * VTILE;
   const int h = blockIdx.y;
-  const int n = blockIdx.z;
+  const int n = p.cu_seqlens ? p.table[p.N + 1 + blockIdx.z] : (int)blockIdx.z;
   int bos, eos, b, base;
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
@@ -1099,7 +1124,7 @@ bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long ro
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t table_bytes(int N) { return (((size_t)N + 1) * 4 + 255) / 256 * 256; }
+size_t table_bytes(int N) { return ((2 * (size_t)N + 1) * 4 + 255) / 256 * 256; }
 
 size_t max_chunks(int B, int T, int N, bool varlen) {
   const size_t nt = ((size_t)T + BT - 1) / BT;
@@ -1147,7 +1172,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   p.scale = cp.scale;
   p.block = block_bytes(cp.V, kda);
   if (varlen) {
-    chunk_table_kernel<<<1, 32, 0, stream>>>(cp.cu_seqlens, cp.N, cp.T, p.table, cp.err);
+    chunk_table_kernel<<<1, TABLE_THREADS, 0, stream>>>(cp.cu_seqlens, cp.N, cp.T, p.table, cp.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

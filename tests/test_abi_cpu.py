@@ -175,8 +175,8 @@ def test_decode_argument_errors(lib, change, expect):
 
 def test_workspace_size(lib):
     # the tensor-core path (bf16, K = 128, V % 32 == 0, V <= 128) needs per
-    # (chunk, head) operand blocks of 66560 + 256 V bytes plus a 256-byte
-    # chunk table
+    # (chunk, head) operand blocks of 66560 + 256 V bytes plus the chunk table
+    # (N + 1 offsets and N sequence indices, int32, rounded up to 256 bytes)
     blk = 66560 + 256 * 128
     a = good_chunk()
     n = ctypes.c_size_t(123)
@@ -186,6 +186,9 @@ def test_workspace_size(lib):
     a = good_chunk(B=1, N=3, cu_seqlens=FAKE, T=200)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
     assert n.value == 256 + (4 + 3) * 4 * blk
+    a = good_chunk(B=1, N=100, cu_seqlens=FAKE, T=6400)
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
+    assert n.value == 1024 + (100 + 100) * 4 * blk
     # V beyond 128 takes the CUDA-core path
     a = good_chunk(V=160)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK

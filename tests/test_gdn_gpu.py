@@ -82,6 +82,24 @@ def test_varlen_with_empty_and_short_sequences():
     assert torch.equal(ht[5].cpu(), inp["h0"][5])
 
 
+@pytest.mark.parametrize("lengths", [
+    [70, 0, 300, 1, 129, 64, 65, 250],   # the chain takes them longest first
+    [int(x) for x in np.random.default_rng(17).integers(0, 5, 1100)],  # past the ordering limit
+], ids=["mixed", "1100_short"])
+def test_varlen_tensor_core_path(lengths):
+    T = sum(lengths)
+    H, Hg, V = (4, 2, 64) if len(lengths) < 100 else (1, 1, 32)
+    inp = synth.prefill_inputs(10, 1, T, H, Hg, 128, V, dtype=torch.bfloat16, h0_std=None,
+                               lengths=lengths)
+    inp["h0"] = 0.1 * torch.randn(len(lengths), H, 128, V, generator=torch.Generator().manual_seed(4))
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
+    for n in (i for i, x in enumerate(lengths) if x == 0):
+        assert torch.equal(ht[n].cpu(), inp["h0"][n])
+
+
 def test_no_final_state_and_deterministic():
     inp = synth.prefill_inputs(21, 1, 300, 2, 1, 128, 128, dtype=torch.bfloat16)
     d = to_dev(inp)

@@ -2,8 +2,8 @@
 
 Every gate kind on fp32 and bf16 inputs with ragged tails and a partial value
 tile, grouped query heads sharing a gate head, packed sequences with empty
-ones, bf16 chunk gradients, the default and an explicit scale, and an empty
-batch.  Like the forward pass the kernel computes in fp32 from the inputs as
+ones, bf16 chunk gradients, the default and an explicit scale, an empty
+batch, and the benchmarked shape on sampled chains.  Like the forward pass the kernel computes in fp32 from the inputs as
 stored, so the fp32 bound (1e-4 RMS) applies to both input dtypes.
 """
 import pytest
@@ -105,3 +105,21 @@ def test_empty_batch_returns_dht():
     dh, dh0 = run(inp)
     assert dh.shape[0] == 0
     assert torch.equal(dh0.cpu(), inp["dht"])
+
+
+@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+def test_benchmark_workload_sampled(gate):
+    # the benchmarked shape and launch (B=2, T=4096, HQ=H=16, K=V=128, bf16,
+    # fp32 chunk gradients); the oracle runs three sampled (sequence, head) chains
+    inp = synth.state_grad_inputs(6, 2, 4096, 16, 16, 128, 128, gate, dht_std=0.1)
+    dh, dh0 = run(inp)
+    nt = 4096 // 64
+    for b, h in ((0, 0), (1, 7), (1, 15)):
+        one = {"q": inp["q"][b:b + 1, :, h:h + 1], "do": inp["do"][b:b + 1, :, h:h + 1],
+               "gate": gate, "gate_values": inp["gate_values"][b:b + 1, :, h:h + 1],
+               "dht": inp["dht"][b:b + 1, h:h + 1],
+               "cu_seqlens": None, "scale": inp["scale"]}
+        dh_ref, dh0_ref = oracle(one)
+        what = f"({gate}) seq {b} head {h}"
+        assert_close(dh[b * nt:(b + 1) * nt, h], dh_ref[:, 0], TOL_F32, f"dh {what}")
+        assert_close(dh0[b, h], dh0_ref[0, 0], TOL_F32, f"dh0 {what}")

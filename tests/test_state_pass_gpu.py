@@ -2,7 +2,8 @@
 
 Every gate kind on fp32 and bf16 inputs, ragged tails and a partial value
 tile, packed sequences with empty ones, bf16 chunk states, no outputs but the
-final state, an empty batch, and a bad cu_seqlens reported on the device.
+final state, an empty batch, a bad cu_seqlens reported on the device, and the
+benchmarked shape on sampled chains.
 The kernel computes in fp32 from the inputs as stored, so the fp32 bound
 (1e-4 RMS) applies to both input dtypes; bf16-stored chunk states get the
 half-ulp storage allowance.
@@ -99,3 +100,28 @@ def test_bad_seqlens_is_reported():
     torch.cuda.synchronize()
     assert gdn.gdn_check_device_error() == Status.BAD_SEQLENS
     assert gdn.gdn_check_device_error() == Status.OK  # reading clears it
+
+
+def _head_slice(inp, b, h):
+    """The inputs of one (sequence, head) chain of a fixed-length batch."""
+    gv = inp["gate_values"]
+    if gv is not None:
+        gv = gv[h:h + 1] if inp["gate"] == "g_gamma" else gv[b:b + 1, :, h:h + 1]
+    return {"k": inp["k"][b:b + 1, :, h:h + 1], "v": inp["v"][b:b + 1, :, h:h + 1],
+            "gate": inp["gate"], "gate_values": gv,
+            "h0": None if inp["h0"] is None else inp["h0"][b:b + 1, h:h + 1],
+            "cu_seqlens": None}
+
+
+@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+def test_benchmark_workload_sampled(gate):
+    # the benchmarked shape and launch (B=2, T=4096, H=16, K=V=128, bf16, fp32
+    # chunk states); the oracle runs three sampled (sequence, head) chains
+    inp = synth.state_pass_inputs(5, 2, 4096, 16, 128, 128, gate, h0_std=0.1)
+    hs, ht = run(inp)
+    nt = 4096 // 64
+    for b, h in ((0, 0), (1, 7), (1, 15)):
+        hs_ref, ht_ref = oracle(_head_slice(inp, b, h))
+        what = f"({gate}) seq {b} head {h}"
+        assert_close(hs[b * nt:(b + 1) * nt, h], hs_ref[:, 0], TOL_F32, f"hs {what}")
+        assert_close(ht[b, h], ht_ref[0, 0], TOL_F32, f"ht {what}")
