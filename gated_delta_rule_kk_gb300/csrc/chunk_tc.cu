@@ -81,6 +81,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// hi = RNE(x), lo = RNE(x - hi), two values each (x0 in the low halves)
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = pack_bf16x2(x0 - hf.x, x1 - hf.y);
+}
+
 __device__ __forceinline__ void unpack8(uint4 u, float *f) {
   const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
@@ -197,15 +205,14 @@ __device__ __forceinline__ bool locate_chunk(const TcParams &p, int id, ChunkPos
 
 // ---------------------------------------------------------------------------
 // (I + A)^-1 for strictly lower-triangular 64x64 A (fp32, row stride SLD, rows
-// 16-byte aligned) by 16x16 diagonal-block forward substitution and a
-// three-level block merge (T_ij = -T_ii sum_{j<=m<i} A_im T_mj).  NT threads;
-// X is scratch for 3 x 16 x XLD floats.  Only the lower block triangle of T
-// is written.  The merges run as 2 x 2 register tiles fed by 16-byte row
-// loads of A and 8-byte row loads of T, so shared-memory traffic is one load
-// per two FMAs or better.
-constexpr int SLD = 68, XLD = 18;
+// 16-byte aligned) by 16x16 diagonal-block forward substitution (fp32, CUDA
+// cores) and a three-level block merge T_ij = -T_ii sum_{j<=m<i} A_im T_mj
+// (warp-level tensor cores).  NT threads; only the lower block triangle of T
+// is written.
+constexpr int SLD = 68, XLD = 18;  // XLD: the small region keeps 3 x 16 x XLD floats free
 template <int NT>
-__device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int tid) {
+__device__ void unit_lower_inverse_64(const float *A, float *Tm, int tid) {
+  static_assert(NT >= 96, "the merge takes warps 0..2");
   if (tid < 64) {
     // thread (o, j): column j of diagonal block o
     const int o = (tid >> 4) * 16, j = tid & 15;
@@ -232,57 +239,65 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, float *X, int t
     for (int i = 0; i < 16; ++i) Tm[(o + i) * SLD + o + j] = x[i];
   }
   __syncthreads();
-  // level d: blocks (b + d, b) for b = 0 .. 3 - d; 64 two-by-two tiles per block
+  // level d: blocks (b + d, b) for b = 0 .. 3 - d, warp b each, on the tensor
+  // cores (m16n8k16 with bf16 hi/lo operands: hi.hi + hi.lo + lo.hi, fp32
+  // accumulation).  The warp forms X^T = sum_m T_{m,b}^T A_{b+d,m}^T, then
+  // T_{b+d,b}^T = -X^T T_{b+d,b+d}^T with X^T's accumulators serving directly
+  // as the second product's A fragments.
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll 1
   for (int d = 1; d <= 3; ++d) {
-    const int ntile = (4 - d) * 64;
-    // X_b = sum_{m = b .. b+d-1} A_{b+d, m} T_{m, b}
-    for (int e = tid; e < ntile; e += NT) {
-      const int b = e >> 6, rr = ((e >> 3) & 7) * 2, cc = (e & 7) * 2;
-      const float *a0 = A + ((b + d) * 16 + rr) * SLD;
-      const float *a1 = a0 + SLD;
-      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-#pragma unroll 2
-      for (int k = b * 16; k < (b + d) * 16; k += 4) {
-        const float4 x0 = *reinterpret_cast<const float4 *>(a0 + k);
-        const float4 x1 = *reinterpret_cast<const float4 *>(a1 + k);
-        const float r0[4] = {x0.x, x0.y, x0.z, x0.w}, r1[4] = {x1.x, x1.y, x1.z, x1.w};
+    if (warp <= 3 - d) {
+      const int b = warp, r = (b + d) * 16, c = b * 16;
+      float xt[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+      for (int m = b; m < b + d; ++m) {
+        // A = T_{m,b}^T: element (i, k) = T[16 m + k][c + i]
+        const float *Tb = Tm + (16 * m) * SLD + c;
+        uint32_t ah[4], al[4];
+        split_bf16x2(Tb[(2 * t) * SLD + g], Tb[(2 * t + 1) * SLD + g], ah[0], al[0]);
+        split_bf16x2(Tb[(2 * t) * SLD + g + 8], Tb[(2 * t + 1) * SLD + g + 8], ah[1], al[1]);
+        split_bf16x2(Tb[(2 * t + 8) * SLD + g], Tb[(2 * t + 9) * SLD + g], ah[2], al[2]);
+        split_bf16x2(Tb[(2 * t + 8) * SLD + g + 8], Tb[(2 * t + 9) * SLD + g + 8], ah[3], al[3]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float2 t = *reinterpret_cast<const float2 *>(Tm + (k + kk) * SLD + b * 16 + cc);
-          s00 = fmaf(r0[kk], t.x, s00);
-          s01 = fmaf(r0[kk], t.y, s01);
-          s10 = fmaf(r1[kk], t.x, s10);
-          s11 = fmaf(r1[kk], t.y, s11);
+        for (int nt = 0; nt < 2; ++nt) {
+          // B = A_{b+d,m}^T: element (k, n) = A[r + 8 nt + n][16 m + k]
+          const float *Ar = A + (r + 8 * nt + g) * SLD + 16 * m;
+          const float2 p0 = *reinterpret_cast<const float2 *>(Ar + 2 * t);
+          const float2 p1 = *reinterpret_cast<const float2 *>(Ar + 2 * t + 8);
+          uint32_t bh0, bl0, bh1, bl1;
+          split_bf16x2(p0.x, p0.y, bh0, bl0);
+          split_bf16x2(p1.x, p1.y, bh1, bl1);
+          ptx::mma_16816_bf16(xt[nt], ah, bh0, bh1);
+          ptx::mma_16816_bf16(xt[nt], ah, bl0, bl1);
+          ptx::mma_16816_bf16(xt[nt], al, bh0, bh1);
         }
       }
-      *reinterpret_cast<float2 *>(X + (b * 16 + rr) * XLD + cc) = make_float2(s00, s01);
-      *reinterpret_cast<float2 *>(X + (b * 16 + rr + 1) * XLD + cc) = make_float2(s10, s11);
-    }
-    __syncthreads();
-    // T_{b+d, b} = -T_{b+d, b+d} X_b
-    for (int e = tid; e < ntile; e += NT) {
-      const int b = e >> 6, rr = ((e >> 3) & 7) * 2, cc = (e & 7) * 2;
-      const int o = (b + d) * 16;
-      const float *t0 = Tm + (o + rr) * SLD + o;
-      const float *t1 = t0 + SLD;
-      float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+      uint32_t xh[4], xl[4];
+      split_bf16x2(xt[0][0], xt[0][1], xh[0], xl[0]);
+      split_bf16x2(xt[0][2], xt[0][3], xh[1], xl[1]);
+      split_bf16x2(xt[1][0], xt[1][1], xh[2], xl[2]);
+      split_bf16x2(xt[1][2], xt[1][3], xh[3], xl[3]);
+      float *Tw = Tm + r * SLD + c;  // T_{b+d,b}
 #pragma unroll
-      for (int k = 0; k < 16; k += 4) {
-        const float4 x0 = *reinterpret_cast<const float4 *>(t0 + k);
-        const float4 x1 = *reinterpret_cast<const float4 *>(t1 + k);
-        const float r0[4] = {x0.x, x0.y, x0.z, x0.w}, r1[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float2 xv = *reinterpret_cast<const float2 *>(X + (b * 16 + k + kk) * XLD + cc);
-          s00 = fmaf(r0[kk], xv.x, s00);
-          s01 = fmaf(r0[kk], xv.y, s01);
-          s10 = fmaf(r1[kk], xv.x, s10);
-          s11 = fmaf(r1[kk], xv.y, s11);
-        }
+      for (int nt = 0; nt < 2; ++nt) {
+        // B = T_{b+d,b+d}^T: element (k, n) = T[r + 8 nt + n][r + k]
+        const float *Tr = Tm + (r + 8 * nt + g) * SLD + r;
+        const float2 p0 = *reinterpret_cast<const float2 *>(Tr + 2 * t);
+        const float2 p1 = *reinterpret_cast<const float2 *>(Tr + 2 * t + 8);
+        uint32_t bh0, bl0, bh1, bl1;
+        split_bf16x2(p0.x, p0.y, bh0, bl0);
+        split_bf16x2(p1.x, p1.y, bh1, bl1);
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        ptx::mma_16816_bf16(o, xh, bh0, bh1);
+        ptx::mma_16816_bf16(o, xh, bl0, bl1);
+        ptx::mma_16816_bf16(o, xl, bh0, bh1);
+        // o: T_{b+d,b}^T rows g, g + 8 and columns 8 nt + 2 t (+ 1)
+        Tw[(8 * nt + 2 * t) * SLD + g] = -o[0];
+        Tw[(8 * nt + 2 * t + 1) * SLD + g] = -o[1];
+        Tw[(8 * nt + 2 * t) * SLD + g + 8] = -o[2];
+        Tw[(8 * nt + 2 * t + 1) * SLD + g + 8] = -o[3];
       }
-      *reinterpret_cast<float2 *>(Tm + (o + rr) * SLD + b * 16 + cc) = make_float2(-s00, -s01);
-      *reinterpret_cast<float2 *>(Tm + (o + rr + 1) * SLD + b * 16 + cc) = make_float2(-s10, -s11);
     }
     __syncthreads();
   }
@@ -337,8 +352,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   float *eg = bet + 64;                                    // [64] e^{gamma}
   float *eng = eg + 64;                                    // [64] e^{-gamma}
   float *gl = eng + 64;                                    // [128] KDA gamma_L
-  float *Xs = gl + 128;                                    // merge scratch 3 x 16 x XLD
-  uint64_t *bars = reinterpret_cast<uint64_t *>(Xs + 3 * 16 * XLD + 4);  // tma, mma
+  uint64_t *bars = reinterpret_cast<uint64_t *>(gl + 128 + 3 * 16 * XLD + 4);  // tma, mma
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
   int *flags = reinterpret_cast<int *>(tmem_slot + 1);     // [0]: split exps ok
 
@@ -654,7 +668,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
 
   // ---- T = (I + A)^-1 (fp32)
-  unit_lower_inverse_64<INTRA_THREADS>(Asm, Tsm, Xs, tid);
+  unit_lower_inverse_64<INTRA_THREADS>(Asm, Tsm, tid);
   if (tid == 0) ptx::bulk_wait_read<0>();
   __syncthreads();  // AQ and the k rows may be overwritten now
 
