@@ -75,6 +75,18 @@ def test_fp32_grouped_heads_and_default_scale():
     assert_close(dh2, dh2_ref, TOL_F32, "dh (scale 0.37)")
 
 
+@pytest.mark.parametrize("gate", ["g_gamma", "gk"])
+def test_tensor_core_path_partial_tile_and_bf16_gradients(gate):
+    # K = 128 bf16 (tensor-core kernel), V = 48, T = 190, 6 query heads over 3
+    # gate heads, chunk gradients in bf16
+    inp = synth.state_grad_inputs(86, 2, 190, 6, 3, 128, 48, gate, dht_std=0.2)
+    dh, dh0 = run(inp, states_dtype=torch.bfloat16)
+    dh_ref, dh0_ref = oracle(inp)
+    assert dh.dtype == torch.bfloat16
+    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate})")
+
+
 def test_bf16_chunk_gradients_and_no_chunk_output():
     inp = synth.state_grad_inputs(83, 2, 200, 2, 2, 64, 64, "g", dht_std=0.2)
     dh, dh0 = run(inp, states_dtype=torch.bfloat16)

@@ -52,13 +52,28 @@ def test_fp32_every_gate(gate):
     assert_close(ht, ht_ref, TOL_F32, f"ht ({gate})")
 
 
-@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+@pytest.mark.parametrize("gate", GATES)
 def test_bf16_inputs_full_width(gate):
     inp = synth.state_pass_inputs(71, 1, 300, 2, 128, 128, gate, h0_std=0.1)
     hs, ht = run(inp)
     hs_ref, ht_ref = oracle(inp)
     assert_close(hs, hs_ref, TOL_F32, f"hs ({gate})")
     assert_close(ht, ht_ref, TOL_F32, f"ht ({gate})")
+
+
+@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+def test_tensor_core_path_partial_tile_and_bf16_states(gate):
+    # K = 128 bf16 (tensor-core kernel), V = 48: one full and one half 32-column
+    # tile; T = 190: two full chunks and a 62-token tail; chunk states in bf16
+    inp = synth.state_pass_inputs(75, 2, 190, 3, 128, 48, gate, h0_std=0.2)
+    hs, ht = run(inp, states_dtype=torch.bfloat16)
+    hs_ref, ht_ref = oracle(inp)
+    assert hs.dtype == torch.bfloat16
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate})")
+    hs32, ht32 = run(inp)
+    assert_close(hs32, hs_ref, TOL_F32, f"hs fp32 ({gate})")
+    assert torch.equal(ht32, ht)
 
 
 def test_bf16_chunk_states_and_no_states():
