@@ -257,3 +257,14 @@ def test_state_bwd_argument_errors(lib, change, expect):
     a.update(change)
     st = lib.gdn_chunk_state_bwd(ctypes.byref(GdnStateBwdArgs(**a)), None)
     assert st == expect, (change, Status(st))
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_plain_c_caller_compiles(tmp_path):
+    # tests/c_abi_program.c, the plain C caller the GPU tests run, builds
+    # against include/gdn.h with -Wall -Werror
+    from c_program import compile_program
+    try:
+        compile_program(str(tmp_path), link=False)
+    except subprocess.CalledProcessError as e:
+        raise AssertionError(e.stderr)
