@@ -10,8 +10,9 @@
 //    tcgen05 GEMM; sglang fla/chunk_fwd.py, fused KK^T + solve kernel):
 //      A   = beta_i S_kk[i,j] exp(gamma_i - gamma_j), i > j       (Steps 1-2)
 //      Aqk = scale S_qk[i,j] exp(gamma_i - gamma_j),  i >= j
-//      T   = (I + A)^-1 in fp32: 16 x 16 diagonal blocks by forward
-//            substitution, then the block merge                     (Steps 3-4)
+//      T   = (I + A)^-1: 16 x 16 diagonal blocks by forward substitution
+//            (fp32), then the block merge on the warp-level tensor
+//            cores (bf16 hi/lo operands, fp32 accumulation)     (Steps 3-4)
 //      w   = T diag(beta e^gamma) k,  u = T diag(beta) v         (WY recompute)
 //    T enters the two WY GEMMs as a hi + lo pair of bf16 matrices, so w and u
 //    carry fp32-grade accuracy.  Per (chunk, head) the kernel stores a block
@@ -33,7 +34,7 @@
 //    quarter w % 4 and split its 32 columns; each thread keeps 16 columns of
 //    one key row of the fp32 state tile h[128, 32] in registers for the
 //    whole sequence).  Per chunk
-//      D1  = [-w ; q~] bf16(h)            rows 0..63: -w h, rows 64..127: q h
+//      D1  = [-w ; q~] [h_hi | h_lo]      rows 0..63: -w h, rows 64..127: q h
 //      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
 //      DH  = k~^T v_new                  (k~ = k e^{gamma_L - gamma}, from KT)
 //      D5  = [Aqk_lo ; Aqk_hi] v_new

@@ -13,17 +13,20 @@
 //   dh_{c} = e^{g_L} diag(e^{gk_L}) dh_{c+1} diag(e^{gv_L}) + sum_i q~_i do~_i^T.
 //
 // Two kernels, one CTA per (32-column tile of V, head, sequence), the fp32
-// state in registers across the chunks.  A chunk's k, v and gates are
-// loaded into registers (16-byte loads; K and V are multiples of 8) while the
-// previous chunk is computed, then staged in shared memory with the gate
-// factors applied.
-//   state_pass_kernel     exact fp32 FMAs; every thread holds one key row x
-//                         16 columns (any K <= 128, fp32 or bf16 inputs)
+// state in registers across the chunks (K and V are multiples of 8, so every
+// row piece is a 16-byte load or copy).
+//   state_pass_kernel     256 threads, exact fp32 FMAs; every thread holds one
+//                         key row x 16 columns (any K <= 128, fp32 or bf16
+//                         inputs); a chunk's k, v and gates are loaded into
+//                         registers while the previous chunk is computed, then
+//                         staged in shared memory with the gate factors applied
 //   state_pass_tc_kernel  bf16 inputs with K = 128, 512 threads: each warp
 //                         holds 16 key rows x 16 columns as m16n8k16
-//                         accumulators and adds k~^T v~ on the tensor cores
-//                         from bf16 hi/lo pairs of k~ and v~ (hi.hi + hi.lo +
-//                         lo.hi: fp32-grade products), operands double-buffered
+//                         accumulators; raw chunks stream into a shared-memory
+//                         ring by cp.async several steps ahead, v~ (and with
+//                         the per-key gate k~) is staged as a bf16 hi/lo pair
+//                         into double-buffered operands, and the tensor-core
+//                         update takes fp32-grade products (below)
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "ptx.cuh"
