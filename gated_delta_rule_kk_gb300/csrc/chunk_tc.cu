@@ -545,8 +545,11 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         const float ep = __expf(gv);
         a[e] = kf[e] * ep;
         b[e] = qf[e] * ep;
-        c[e] = split ? kf[e] * __expf(-gv) : 0.f;
-        t[e] = i < L ? kf[e] * __expf(gl[8 * cg + e] - gv) : 0.f;
+        // split range (|gamma| bounded): e^{gamma_L - g} = e^{gamma_L} e^{-g}
+        const float en = split ? __expf(-gv) : 0.f;
+        c[e] = kf[e] * en;
+        const float fl = split ? sc[8 * cg + e] * en : __expf(gl[8 * cg + e] - gv);
+        t[e] = i < L ? kf[e] * fl : 0.f;
       }
       *kp = pack8(a);
       *qp = pack8(b);
