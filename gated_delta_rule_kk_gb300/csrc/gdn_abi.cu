@@ -62,6 +62,8 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
           T, Hk, Hv, K, V, N);
   REQUIRE(Hv % Hk == 0, GDN_ERR_UNSUPPORTED, "value heads (%d) must be a multiple of %s (%d)", Hv,
           hk_name, Hk);
+  REQUIRE(N <= MAX_GRID_YZ && Hv <= MAX_GRID_YZ, GDN_ERR_UNSUPPORTED,
+          "N (%d) and the value heads (%d) must be at most %d", N, Hv, MAX_GRID_YZ);
   REQUIRE(K <= KMAX, GDN_ERR_UNSUPPORTED, "K=%d exceeds %d", K, KMAX);
   REQUIRE(chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT, chunk_size);
   REQUIRE(g_is_cumsum == 0 || g_is_cumsum == 1, GDN_ERR_INVALID_ARG, "g_is_cumsum must be 0 or 1");
@@ -225,9 +227,13 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
   REQUIRE(a->B >= 1 && a->T >= 0 && a->H >= 1 && a->K >= 1 && a->V >= 1 && a->N >= 1,
           GDN_ERR_INVALID_ARG, "sizes must be positive (B=%d T=%d H=%d K=%d V=%d N=%d)", a->B,
           a->T, a->H, a->K, a->V, a->N);
+  REQUIRE(a->H <= MAX_GRID_YZ, GDN_ERR_UNSUPPORTED, "H (%d) must be at most %d", a->H,
+          MAX_GRID_YZ);
   REQUIRE(a->K <= KMAX, GDN_ERR_UNSUPPORTED, "K=%d exceeds %d", a->K, KMAX);
   REQUIRE(a->K % 8 == 0 && a->V % 8 == 0, GDN_ERR_UNSUPPORTED,
           "K (%d) and V (%d) must be multiples of 8", a->K, a->V);
+  REQUIRE(a->N <= MAX_GRID_YZ, GDN_ERR_UNSUPPORTED, "N (%d) must be at most %d", a->N,
+          MAX_GRID_YZ);
   REQUIRE(a->chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT,
           a->chunk_size);
   if (a->cu_seqlens == nullptr) {
@@ -287,9 +293,13 @@ gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t strea
           a->B, a->T, a->HQ, a->H, a->K, a->V, a->N);
   REQUIRE(a->HQ % a->H == 0, GDN_ERR_UNSUPPORTED, "HQ (%d) must be a multiple of H (%d)", a->HQ,
           a->H);
+  REQUIRE(a->HQ <= MAX_GRID_YZ, GDN_ERR_UNSUPPORTED, "HQ (%d) must be at most %d", a->HQ,
+          MAX_GRID_YZ);
   REQUIRE(a->K <= KMAX, GDN_ERR_UNSUPPORTED, "K=%d exceeds %d", a->K, KMAX);
   REQUIRE(a->K % 8 == 0 && a->V % 8 == 0, GDN_ERR_UNSUPPORTED,
           "K (%d) and V (%d) must be multiples of 8", a->K, a->V);
+  REQUIRE(a->N <= MAX_GRID_YZ, GDN_ERR_UNSUPPORTED, "N (%d) must be at most %d", a->N,
+          MAX_GRID_YZ);
   REQUIRE(a->chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT,
           a->chunk_size);
   REQUIRE(isfinite(a->scale), GDN_ERR_INVALID_ARG, "scale must be finite");

@@ -82,7 +82,8 @@ typedef enum gdn_dtype {
  *                                     tokens cu_seqlens[n] .. cu_seqlens[n+1]
  *                                     (0 = cu_seqlens[0] <= ... <= cu_seqlens[N]
  *                                     = T, checked on the device)
- * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, H % Hg == 0.  With T == 0
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, H % Hg == 0, N and H at
+ * most 65535 (GDN_ERR_UNSUPPORTED otherwise).  With T == 0
  * nothing per token is read or written, so q, k, v, g, beta and o may be NULL
  * (ht = h0, or zeros).
  * scale <= 0 selects 1/sqrt(K).
@@ -173,7 +174,8 @@ gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *args, gdn_stream_t stream)
  *   cu_seqlens [N + 1] int32   as gdn_chunk_fwd (device memory; checked on the
  *                              device, GDN_ERR_BAD_SEQLENS also when the chunks
  *                              do not fit num_chunks)
- * Limits: 1 <= K <= 128, K and V multiples of 8, chunk_size == 64.
+ * Limits: 1 <= K <= 128, K and V multiples of 8, chunk_size == 64, N and H at
+ * most 65535.
  * Arithmetic in fp32 (bf16 inputs are widened).  Nothing is allocated; no
  * workspace.
  */
@@ -256,7 +258,8 @@ gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *b
  *   beta   [B, T, HV]     float32
  *   h0, ht [N, HV, K, V]  float32     as for GDN
  *   cu_seqlens            as for GDN
- * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0.  With T == 0
+ * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0, N and HV at
+ * most 65535.  With T == 0
  * q, k, v, g, beta and o may be NULL (ht = h0, or zeros).
  * Workspace: as for GDN (tensor cores for bf16, K == 128, V % 32 == 0,
  * V <= 128; kda_chunk_workspace_size() bytes).

@@ -268,3 +268,16 @@ def test_plain_c_caller_compiles(tmp_path):
         compile_program(str(tmp_path), link=False)
     except subprocess.CalledProcessError as e:
         raise AssertionError(e.stderr)
+
+
+def test_grid_limits_are_rejected_up_front(lib):
+    # sequences and heads index grid dimensions y and z (at most 65535)
+    a = good_chunk(B=1, N=70000, cu_seqlens=FAKE, T=70000)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.UNSUPPORTED
+    assert "65535" in lib.gdn_last_error_message().decode()
+    st = GdnStateArgs(dtype=1, k=FAKE, v=FAKE, gate=0, B=1, T=70000, H=2, K=64, V=64, N=70000,
+                      chunk_size=64, cu_seqlens=FAKE)
+    assert lib.gdn_chunk_state_fwd(ctypes.byref(st), None) == Status.UNSUPPORTED
+    bw = GdnStateBwdArgs(dtype=1, q=FAKE, do_=FAKE, gate=0, B=1, T=100, HQ=70000, H=70000, K=64,
+                         V=64, N=1, chunk_size=64)
+    assert lib.gdn_chunk_state_bwd(ctypes.byref(bw), None) == Status.UNSUPPORTED
