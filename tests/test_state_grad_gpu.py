@@ -135,3 +135,14 @@ def test_benchmark_workload_sampled(gate):
         what = f"({gate}) seq {b} head {h}"
         assert_close(dh[b * nt:(b + 1) * nt, h], dh_ref[:, 0], TOL_F32, f"dh {what}")
         assert_close(dh0[b, h], dh0_ref[0, 0], TOL_F32, f"dh0 {what}")
+
+
+@pytest.mark.parametrize("T", [1, 64, 65])
+@pytest.mark.parametrize("gate", ["g", "gk"])
+def test_tensor_core_path_chunk_boundaries(T, gate):
+    inp = synth.state_grad_inputs(87, 2, T, 2, 2, 128, 64, gate, dht_std=0.3)
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert tuple(dh.shape) == dh_ref.shape
+    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate}, T={T})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate}, T={T})")

@@ -140,3 +140,16 @@ def test_benchmark_workload_sampled(gate):
         what = f"({gate}) seq {b} head {h}"
         assert_close(hs[b * nt:(b + 1) * nt, h], hs_ref[:, 0], TOL_F32, f"hs {what}")
         assert_close(ht[b, h], ht_ref[0, 0], TOL_F32, f"ht {what}")
+
+
+@pytest.mark.parametrize("T", [1, 64, 65])
+@pytest.mark.parametrize("gate", ["g", "gk"])
+def test_tensor_core_path_chunk_boundaries(T, gate):
+    # one token, exactly one chunk, one chunk and one token (both variants of
+    # the tensor-core kernel: k from the ring, and k~ staged for gk)
+    inp = synth.state_pass_inputs(76, 2, T, 2, 128, 64, gate, h0_std=0.3)
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert tuple(hs.shape) == hs_ref.shape
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate}, T={T})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate}, T={T})")
