@@ -28,7 +28,10 @@ page's kernel forms the in-chunk cumulative sum ``gamma * (i + 1)``).
 
 Output layout: the chunk states of all sequences one after another, sequence
 n contributing ceil(len_n / chunk_size) entries -- for B equal sequences of T
-tokens that is ``[B, NT, H, K, V]`` flattened over (B, NT).
+tokens that is ``[B, NT, H, K, V]`` flattened over (B, NT).  With the page's
+``split_size`` (a multiple of the chunk size) only the chunks whose index is
+a multiple of split_size / chunk_size are stored, at index chunk // (split_size
+/ chunk_size): ceil(len_n / split_size) entries per sequence.
 """
 from __future__ import annotations
 
@@ -39,21 +42,32 @@ from .recurrence import _f64, raw_gate_from_chunk_cumsum, sequence_bounds
 GATES = (None, "g", "g_gamma", "gk", "gv")
 
 
-def chunk_counts(B: int, T: int, cu_seqlens=None, chunk_size: int = 64):
-    """Number of chunks of every sequence (0 for an empty one)."""
-    return [-(-(eos - bos) // chunk_size) for _, bos, eos in sequence_bounds(B, T, cu_seqlens)]
+def chunk_counts(B: int, T: int, cu_seqlens=None, chunk_size: int = 64, split_size=None):
+    """Number of stored states of every sequence (0 for an empty one): one per
+    chunk, or one per split of ``split_size`` tokens."""
+    span = chunk_size if split_size is None else split_size
+    return [-(-(eos - bos) // span) for _, bos, eos in sequence_bounds(B, T, cu_seqlens)]
+
+
+def _split(chunk_size, split_size):
+    if split_size is None:
+        return 1
+    if split_size <= 0 or split_size % chunk_size:
+        raise ValueError("split_size must be a positive multiple of chunk_size")
+    return split_size // chunk_size
 
 
 def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None,
-                     chunk_size: int = 64):
+                     chunk_size: int = 64, split_size=None):
     """Chunk-start states ``hs`` ``[sum NT_n, H, K, V]`` and final states
     ``ht`` ``[N, H, K, V]`` of the gated linear-attention recurrence.
 
     k ``[B, T, H, K]``, v ``[B, T, H, V]``; gate_values: ``g`` ``[B, T, H]``,
     ``g_gamma`` ``[H]``, ``gk`` ``[B, T, H, K]``, ``gv`` ``[B, T, H, V]``
     (chunk-local cumulative sums except ``g_gamma``); h0 ``[N, H, K, V]`` or
-    None (zeros).
+    None (zeros); split_size stores every (split_size / chunk_size)-th chunk.
     """
+    NTS = _split(chunk_size, split_size)
     if gate not in GATES:
         raise ValueError(f"unknown gate {gate!r}")
     k, v = _f64(k), _f64(v)
@@ -63,7 +77,7 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
     seqs = sequence_bounds(B, T, cu_seqlens)
     N = len(seqs)
     h0 = np.zeros((N, H, K, V)) if h0 is None else _f64(h0)
-    counts = chunk_counts(B, T, cu_seqlens, chunk_size)
+    counts = chunk_counts(B, T, cu_seqlens, chunk_size, split_size)
     hs = np.zeros((sum(counts), H, K, V))
     ht = np.zeros((N, H, K, V))
     first = 0
@@ -75,8 +89,8 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
             S = h0[n, h].copy()
             for t in range(bos, eos):
                 i = t - bos
-                if i % chunk_size == 0:
-                    hs[first + i // chunk_size, h] = S
+                if i % chunk_size == 0 and (i // chunk_size) % NTS == 0:
+                    hs[first + i // chunk_size // NTS, h] = S
                 if gate == "g":
                     S = np.exp(raw[t, h]) * S
                 elif gate == "g_gamma":
@@ -92,7 +106,7 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
 
 
 def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=None,
-                     scale=None, chunk_size: int = 64):
+                     scale=None, chunk_size: int = 64, split_size=None):
     """Backward state pass (the chunk_h page's ``chunk_bwd_kernel_dh``).
 
     For the gated linear attention above with outputs o_t = scale S_t^T q_t
@@ -107,8 +121,11 @@ def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=No
     end of every chunk (taken before that chunk's tokens are folded in), and
     ``dh0`` ``[N, HQ, K, V]``.  q ``[B, T, HQ, K]``, do ``[B, T, HQ, V]``;
     the gate has H heads (HQ a multiple of H, query head hq uses gate head
-    hq // (HQ / H)), given as in :func:`chunk_state_pass`.
+    hq // (HQ / H)), given as in :func:`chunk_state_pass`.  With split_size
+    only chunks whose index is a multiple of split_size / chunk_size are
+    stored, at index chunk // (split_size / chunk_size).
     """
+    NTS = _split(chunk_size, split_size)
     if gate not in GATES:
         raise ValueError(f"unknown gate {gate!r}")
     q, do = _f64(q), _f64(do)
@@ -126,7 +143,7 @@ def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=No
     seqs = sequence_bounds(B, T, cu_seqlens)
     N = len(seqs)
     dht = np.zeros((N, HQ, K, V)) if dht is None else _f64(dht)
-    counts = chunk_counts(B, T, cu_seqlens, chunk_size)
+    counts = chunk_counts(B, T, cu_seqlens, chunk_size, split_size)
     dh = np.zeros((sum(counts), HQ, K, V))
     dh0 = np.zeros((N, HQ, K, V))
     first = 0
@@ -139,8 +156,9 @@ def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=No
             G = dht[n, hq].copy()
             for t in range(eos - 1, bos - 1, -1):
                 i = t - bos
-                if i % chunk_size == chunk_size - 1 or t == eos - 1:
-                    dh[first + i // chunk_size, hq] = G
+                if ((i % chunk_size == chunk_size - 1 or t == eos - 1)
+                        and (i // chunk_size) % NTS == 0):
+                    dh[first + i // chunk_size // NTS, hq] = G
                 G = G + scale * np.outer(q[b, t, hq], do[b, t, hq])
                 if gate == "g":
                     G = np.exp(raw[t, h]) * G

@@ -195,3 +195,35 @@ def test_state_gradient_grouped_query_heads_share_the_gate():
                             chunk_size=chunk)
     np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(a[1], b[1], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("split", [128, 192])
+def test_split_size_keeps_every_split_chunk(split):
+    # the chunk_h page's split_size: the stored states are those of the chunks
+    # whose index is a multiple of split / 64, in order, per sequence
+    lengths = [300, 0, 64, 129, 200]
+    T, H, K, V = sum(lengths), 2, 8, 4
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((1, T, H, K))
+    v = rng.standard_normal((1, T, H, V))
+    raw = -0.05 * np.abs(rng.standard_normal((1, T, H, K)))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    gk = np.empty_like(raw)
+    for s0, e0 in zip(cu[:-1], cu[1:]):
+        for c in range(s0, e0, 64):
+            gk[:, c:min(c + 64, e0)] = np.cumsum(raw[:, c:min(c + 64, e0)], axis=1)
+    h0 = rng.standard_normal((len(lengths), H, K, V))
+    hs1, ht1 = SP.chunk_state_pass(k, v, "gk", gk, h0=h0, cu_seqlens=cu)
+    hsS, htS = SP.chunk_state_pass(k, v, "gk", gk, h0=h0, cu_seqlens=cu, split_size=split)
+    S = split // 64
+    keep, first = [], 0
+    for n_chunks in SP.chunk_counts(1, T, cu):
+        keep += [first + c for c in range(0, n_chunks, S)]
+        first += n_chunks
+    assert SP.chunk_counts(1, T, cu, split_size=split) == [-(-x // split) for x in lengths]
+    np.testing.assert_array_equal(hsS, hs1[keep])
+    np.testing.assert_array_equal(htS, ht1)
+    dh1, dh01 = SP.chunk_state_grad(k, v, "gk", gk, dht=h0, cu_seqlens=cu)
+    dhS, dh0S = SP.chunk_state_grad(k, v, "gk", gk, dht=h0, cu_seqlens=cu, split_size=split)
+    np.testing.assert_array_equal(dhS, dh1[keep])
+    np.testing.assert_array_equal(dh0S, dh01)
