@@ -93,6 +93,7 @@ class GdnStateArgs(ctypes.Structure):
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("K", c_int32), ("V", c_int32),
         ("N", c_int32), ("chunk_size", c_int32),
         ("num_chunks", ctypes.c_int64),
+        ("split_size", c_int32),
     ]
 
 
@@ -108,6 +109,7 @@ class GdnStateBwdArgs(ctypes.Structure):
         ("V", c_int32), ("N", c_int32), ("chunk_size", c_int32),
         ("num_chunks", ctypes.c_int64),
         ("scale", c_float),
+        ("split_size", c_int32),
     ]
 
 

@@ -308,19 +308,37 @@ _GATES = {None: GateKind.NONE, "g": GateKind.G, "g_gamma": GateKind.G_GAMMA, "gk
           "gv": GateKind.GV}
 
 
+def _stored_states(B, T, cu_seqlens, split):
+    """Number of stored states: ceil(len / split) per sequence (a device sync
+    with cu_seqlens)."""
+    if cu_seqlens is None:
+        return B * ((T + split - 1) // split)
+    lens = (cu_seqlens[1:] - cu_seqlens[:-1]).clamp(min=0).to(torch.int64)
+    return int(((lens + split - 1) // split).sum().item())
+
+
+def _split_tokens(split_size):
+    split = CHUNK if not split_size else int(split_size)
+    if split <= 0 or split % CHUNK:
+        raise ValueError(f"split_size must be a positive multiple of {CHUNK}")
+    return split
+
+
 def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, cu_seqlens=None,
                         output_final_state=True, output_states=True,
                         states_dtype=torch.float32, out_states=None, final_state=None,
-                        num_chunks=None, stream=None):
+                        num_chunks=None, split_size=None, stream=None):
     """Chunk state pass of gated linear attention.  Returns ``(hs, ht)``.
 
     k [B,T,H,K], v [B,T,H,V] (float32 or bfloat16); gate one of None, "g"
     ([B,T,H]), "g_gamma" ([H]), "gk" ([B,T,H,K]), "gv" ([B,T,H,V]) with
     ``gate_values`` float32 (chunk-local cumulative sums except g_gamma);
     initial_state [N,H,K,V] float32.  hs holds the state at the start of every
-    64-token chunk, sequence after sequence ([C,H,K,V]); with ``cu_seqlens``
-    and no ``num_chunks``, C is read from the lengths (a device sync).
+    split of ``split_size`` tokens (a multiple of 64; default 64: every
+    chunk), sequence after sequence ([C,H,K,V]); with ``cu_seqlens`` and no
+    ``num_chunks``, C is read from the lengths (a device sync).
     """
+    split = _split_tokens(split_size)
     dev = k.device
     dt, dts = _io_dtype(k)
     _need(k, "k", dts, dev)
@@ -336,13 +354,10 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
         N = cu_seqlens.numel() - 1
-        if num_chunks is None and (output_states or out_states is not None):
-            lens = (cu_seqlens[1:] - cu_seqlens[:-1]).clamp(min=0).to(torch.int64)
-            num_chunks = int(((lens + CHUNK - 1) // CHUNK).sum().item())
     else:
         N = B
-        if num_chunks is None:
-            num_chunks = B * ((T + CHUNK - 1) // CHUNK)
+    if num_chunks is None and (output_states or out_states is not None or cu_seqlens is None):
+        num_chunks = _stored_states(B, T, cu_seqlens, split)
     if initial_state is not None:
         _need(initial_state, "initial_state", (torch.float32,), dev)
         if tuple(initial_state.shape) != (N, H, K, V):
@@ -363,7 +378,7 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
                      hs_dtype=int(DType.BF16 if hs is not None and hs.dtype == torch.bfloat16
                                   else DType.F32),
                      cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, K=K, V=V, N=N,
-                     chunk_size=CHUNK, num_chunks=int(num_chunks or 0))
+                     chunk_size=CHUNK, num_chunks=int(num_chunks or 0), split_size=split)
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_state_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_fwd")
     return hs, ht
@@ -372,14 +387,16 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
 def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=None,
                         scale=None, output_dh0=True, output_states=True,
                         states_dtype=torch.float32, out_states=None, dh0=None,
-                        num_chunks=None, stream=None):
+                        num_chunks=None, split_size=None, stream=None):
     """Backward state pass (dh recurrence).  Returns ``(dh, dh0)``.
 
     q [B,T,HQ,K], do [B,T,HQ,V] (float32 or bfloat16); gate and gate_values
     as :func:`gdn_chunk_state_fwd` with H gate heads (HQ % H == 0); dht
-    [N,HQ,K,V] float32.  dh [C,HQ,K,V] is the gradient at the end of every
-    64-token chunk, sequence after sequence.
+    [N,HQ,K,V] float32.  dh [C,HQ,K,V] is the gradient at the end of the
+    first 64-token chunk of every split of ``split_size`` tokens (default 64:
+    every chunk), sequence after sequence.
     """
+    split = _split_tokens(split_size)
     dev = q.device
     dt, dts = _io_dtype(q)
     _need(q, "q", dts, dev)
@@ -397,13 +414,10 @@ def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
         N = cu_seqlens.numel() - 1
-        if num_chunks is None and (output_states or out_states is not None):
-            lens = (cu_seqlens[1:] - cu_seqlens[:-1]).clamp(min=0).to(torch.int64)
-            num_chunks = int(((lens + CHUNK - 1) // CHUNK).sum().item())
     else:
         N = B
-        if num_chunks is None:
-            num_chunks = B * ((T + CHUNK - 1) // CHUNK)
+    if num_chunks is None and (output_states or out_states is not None or cu_seqlens is None):
+        num_chunks = _stored_states(B, T, cu_seqlens, split)
     if dht is not None:
         _need(dht, "dht", (torch.float32,), dev)
         if tuple(dht.shape) != (N, HQ, K, V):
@@ -424,7 +438,7 @@ def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens
                                      else DType.F32),
                         cu_seqlens=_ptr(cu_seqlens), B=B, T=T, HQ=HQ, H=H, K=K, V=V, N=N,
                         chunk_size=CHUNK, num_chunks=int(num_chunks or 0),
-                        scale=float(scale) if scale is not None else 0.0)
+                        scale=float(scale) if scale is not None else 0.0, split_size=split)
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_state_bwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_bwd")
     return dh, dh0

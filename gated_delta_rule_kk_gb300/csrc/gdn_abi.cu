@@ -236,6 +236,9 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
           MAX_GRID_YZ);
   REQUIRE(a->chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT,
           a->chunk_size);
+  REQUIRE(a->split_size >= 0 && a->split_size % BT == 0, GDN_ERR_INVALID_ARG,
+          "split_size (%d) must be 0 or a positive multiple of %d", a->split_size, BT);
+  const int split = a->split_size > 0 ? a->split_size / BT : 1;
   if (a->cu_seqlens == nullptr) {
     REQUIRE(a->N == a->B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)",
             a->N, a->B);
@@ -259,7 +262,8 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
     REQUIRE(a->hs_dtype == GDN_F32 || a->hs_dtype == GDN_BF16, GDN_ERR_INVALID_ARG,
             "hs_dtype %d is not GDN_F32/GDN_BF16", a->hs_dtype);
     if (a->cu_seqlens == nullptr) {
-      const long long need = (long long)a->B * ((a->T + BT - 1) / BT);
+      const long long split_tokens = (long long)BT * split;
+      const long long need = (long long)a->B * ((a->T + split_tokens - 1) / split_tokens);
       REQUIRE(a->num_chunks >= need, GDN_ERR_INVALID_ARG,
               "hs holds %lld chunks, %lld needed", (long long)a->num_chunks, need);
     }
@@ -273,6 +277,7 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
   p.num_chunks = a->hs ? a->num_chunks : 0;
   p.reverse = 0;
   p.scale = 1.f;
+  p.split = split;
   p.err = device_error_word();
   if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
   return cuda_status(launch_state_pass(p, a->dtype == GDN_BF16,
@@ -302,6 +307,9 @@ gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t strea
           MAX_GRID_YZ);
   REQUIRE(a->chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT,
           a->chunk_size);
+  REQUIRE(a->split_size >= 0 && a->split_size % BT == 0, GDN_ERR_INVALID_ARG,
+          "split_size (%d) must be 0 or a positive multiple of %d", a->split_size, BT);
+  const int split = a->split_size > 0 ? a->split_size / BT : 1;
   REQUIRE(isfinite(a->scale), GDN_ERR_INVALID_ARG, "scale must be finite");
   if (a->cu_seqlens == nullptr) {
     REQUIRE(a->N == a->B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)",
@@ -326,7 +334,8 @@ gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t strea
     REQUIRE(a->dh_dtype == GDN_F32 || a->dh_dtype == GDN_BF16, GDN_ERR_INVALID_ARG,
             "dh_dtype %d is not GDN_F32/GDN_BF16", a->dh_dtype);
     if (a->cu_seqlens == nullptr) {
-      const long long need = (long long)a->B * ((a->T + BT - 1) / BT);
+      const long long split_tokens = (long long)BT * split;
+      const long long need = (long long)a->B * ((a->T + split_tokens - 1) / split_tokens);
       REQUIRE(a->num_chunks >= need, GDN_ERR_INVALID_ARG,
               "dh holds %lld chunks, %lld needed", (long long)a->num_chunks, need);
     }
@@ -340,6 +349,7 @@ gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t strea
   p.num_chunks = a->dh ? a->num_chunks : 0;
   p.reverse = 1;
   p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)a->K);
+  p.split = split;
   p.err = device_error_word();
   if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
   return cuda_status(launch_state_pass(p, a->dtype == GDN_BF16,

@@ -54,6 +54,7 @@ struct StateParams {
   // h0 = dht, ht = dh0, hs = dh (the gradient at the end of every chunk).
   int reverse;
   float scale;
+  int split;                  // chunks per stored state (>= 1): hs holds chunks 0, split, ..
 };
 
 // Each launcher enqueues its kernel(s) and returns the launch status.

@@ -12,6 +12,9 @@
 // and the factors e^{gamma_i} measured from the chunk's start:
 //   dh_{c} = e^{g_L} diag(e^{gk_L}) dh_{c+1} diag(e^{gv_L}) + sum_i q~_i do~_i^T.
 //
+// The state (or gradient) is stored at chunks c = 0, S, 2 S, .. of each
+// sequence for a split of S chunks (the page's split_size / chunk_size).
+//
 // Two kernels, one CTA per (32-column tile of V, head, sequence), the fp32
 // state in registers across the chunks (K and V are multiples of 8, so every
 // row piece is a 16-byte load or copy).
@@ -62,9 +65,9 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *src, bool ok, float *
   }
 }
 
-// Bounds of sequence n and the index of its first chunk in hs (every thread
-// calls it; it synchronises the block).  A bad cu_seqlens is recorded and
-// leaves the sequence empty.
+// Bounds of sequence n and the index of its first stored state in hs (one
+// per split of p.split chunks; every thread calls it; it synchronises the
+// block).  A bad cu_seqlens is recorded and leaves the sequence empty.
 struct SeqInfo {
   int bos, eos, b, nch;
   long long first;
@@ -84,7 +87,7 @@ __device__ SeqInfo sequence_of(const StateParams &p, int n, int tid, long long *
       for (int m = 0; m < n && ok; ++m) {
         const int len = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
         if (len < 0) ok = false;
-        first += (len + BT - 1) / BT;
+        first += (len + BT * p.split - 1) / (BT * p.split);
       }
       shared_info[0] = first;
       shared_info[1] = ok ? 1 : 0;
@@ -93,13 +96,14 @@ __device__ SeqInfo sequence_of(const StateParams &p, int n, int tid, long long *
     __syncthreads();
     if (shared_info[1] == 0) s.bos = s.eos = 0;  // nothing read, no chunk written
   } else if (tid == 0) {
-    shared_info[0] = (long long)n * ((p.T + BT - 1) / BT);
+    shared_info[0] = (long long)n * ((p.T + BT * p.split - 1) / (BT * p.split));
     shared_info[1] = 1;
   }
   __syncthreads();
   s.nch = (s.eos - s.bos + BT - 1) / BT;
   s.first = shared_info[0];
-  s.write_hs = p.hs && shared_info[1] && s.first + s.nch <= p.num_chunks;
+  s.write_hs =
+      p.hs && shared_info[1] && s.first + (s.nch + p.split - 1) / p.split <= p.num_chunks;
   if (p.hs && shared_info[1] && !s.write_hs && tid == 0) record_error(p.err, GDN_ERR_BAD_SEQLENS);
   return s;
 }
@@ -194,7 +198,7 @@ __device__ __forceinline__ void split8_bf16(const float *x, uint4 &hi, uint4 &lo
 // exact fp32 kernel
 
 template <typename T>
-__global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
+__global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(StateParams p) {
   __shared__ float ks[BT][KMAX];                 // k~ of the chunk, token-major
   __shared__ __align__(16) float vs[BT][SP_VT];  // v~ of the chunk's column tile
   __shared__ float gam[BT];                      // per-token cumulative gate (g, g_gamma)
@@ -221,16 +225,25 @@ __global__ void __launch_bounds__(SP_THREADS) state_pass_kernel(StateParams p) {
 
   // chunk of the it-th step: forward from the first, backward from the last
   auto chunk_at = [&](int it) { return p.reverse ? sq.nch - 1 - it : it; };
+  // stored chunks 0, split, 2 split, ..; the reverse pass meets them last first
+  int store_i = p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
+  int store_c = store_i * p.split;
   ChunkRegs R;
   if (sq.nch > 0) load_chunk<T>(p, sq, chunk_at(0), h, v0, tid, R);
 #pragma unroll 1
   for (int it = 0; it < sq.nch; ++it) {
     const int c = chunk_at(it);
     const int L = min(BT, sq.eos - (sq.bos + c * BT));
+    const bool store = c == store_c;
+    const long long slot = sq.first + store_i;
+    if (store) {
+      store_c += p.reverse ? -p.split : p.split;
+      store_i += p.reverse ? -1 : 1;
+    }
 
     // chunk-start state, 8 columns (16 or 32 bytes) per store
-    if (sq.write_hs && row_ok) {
-      const size_t o = (((size_t)(sq.first + c) * H + h) * K + r) * V + v0 + c0;
+    if (sq.write_hs && row_ok && store) {
+      const size_t o = (((size_t)slot * H + h) * K + r) * V + v0 + c0;
 #pragma unroll
       for (int g8 = 0; g8 < 2; ++g8) {
         if (v0 + c0 + 8 * g8 >= V) continue;  // V is a multiple of 8
@@ -538,6 +551,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
     if (j < sq.nch) tc_fetch(p, sq, chunk_at(j), h, v0, tid, slot_of(j));
     ptx::cp_async_commit();
   }
+  // stored chunks 0, split, 2 split, ..; the reverse pass meets them last first
+  int store_i = p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
+  int store_c = store_i * p.split;
   TcDecay dec;
   if (sq.nch > 0) {
     ptx::cp_async_wait<RING - 2>();  // steps 0 and 1 have landed
@@ -548,10 +564,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
 #pragma unroll 1
   for (int it = 0; it < sq.nch; ++it) {
     const int c = chunk_at(it);
+    const bool store = c == store_c;
+    const long long slot = sq.first + store_i;
+    if (store) {
+      store_c += p.reverse ? -p.split : p.split;
+      store_i += p.reverse ? -1 : 1;
+    }
 
     // chunk-start state: two columns per 8-column tile and row
-    if (sq.write_hs) {
-      const size_t oA = (((size_t)(sq.first + c) * H + h) * K + rA) * V, oB = oA + (size_t)8 * V;
+    if (sq.write_hs && store) {
+      const size_t oA = (((size_t)slot * H + h) * K + rA) * V, oB = oA + (size_t)8 * V;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int col = cB + 8 * nt;

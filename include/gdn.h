@@ -167,9 +167,11 @@ gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *args, gdn_stream_t stream)
  *   k [B,T,H,K], v [B,T,H,V]   dtype (GDN_F32 or GDN_BF16)
  *   h0, ht [N,H,K,V]           float32, NULL = zeros / not returned
  *   hs [C,H,K,V]               hs_dtype (GDN_F32 or GDN_BF16): the state at the
- *                              start of every chunk, sequence after sequence
- *                              (sequence n contributes ceil(len_n / 64)
- *                              entries; B equal sequences: [B, ceil(T/64), ...]);
+ *                              start of every split (split_size tokens, a
+ *                              multiple of 64; 0 = 64: every chunk), sequence
+ *                              after sequence (sequence n contributes
+ *                              ceil(len_n / split_size) entries; B equal
+ *                              sequences: [B, ceil(T/split_size), ...]);
  *                              NULL = not returned; num_chunks = C, its capacity
  *   cu_seqlens [N + 1] int32   as gdn_chunk_fwd (device memory; checked on the
  *                              device, GDN_ERR_BAD_SEQLENS also when the chunks
@@ -200,6 +202,7 @@ typedef struct gdn_state_args {
   int32_t B, T, H, K, V, N;
   int32_t chunk_size;
   int64_t num_chunks;
+  int32_t split_size;          /* tokens between stored states; 0 = chunk_size */
 } gdn_state_args;
 
 /* Enqueue the chunk state pass on `stream`. */
@@ -216,9 +219,11 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *args, gdn_stream_t stream
  *   gate, gate_values            as gdn_chunk_state_fwd, with H heads
  *   dht, dh0 [N,HQ,K,V]          float32, NULL = zeros / not returned
  *   dh [C,HQ,K,V]                dh_dtype: the gradient with respect to the
- *                                state at the end of every chunk (before that
- *                                chunk's tokens are folded in), sequence after
- *                                sequence; NULL = not returned; num_chunks = C
+ *                                state at the end of the first chunk of every
+ *                                split (before that chunk's tokens are folded
+ *                                in; split_size as gdn_chunk_state_fwd, 0 = every
+ *                                chunk), sequence after sequence; NULL = not
+ *                                returned; num_chunks = C
  *   scale                        <= 0 selects 1/sqrt(K)
  * Limits, errors and the rest as gdn_chunk_state_fwd; HQ % H == 0.
  */
@@ -236,6 +241,7 @@ typedef struct gdn_state_bwd_args {
   int32_t chunk_size;
   int64_t num_chunks;
   float scale;
+  int32_t split_size;          /* tokens between stored gradients; 0 = chunk_size */
 } gdn_state_bwd_args;
 
 /* Enqueue the backward state pass on `stream`. */

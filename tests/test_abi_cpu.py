@@ -281,3 +281,21 @@ def test_grid_limits_are_rejected_up_front(lib):
     bw = GdnStateBwdArgs(dtype=1, q=FAKE, do_=FAKE, gate=0, B=1, T=100, HQ=70000, H=70000, K=64,
                          V=64, N=1, chunk_size=64)
     assert lib.gdn_chunk_state_bwd(ctypes.byref(bw), None) == Status.UNSUPPORTED
+
+
+@pytest.mark.parametrize("split,expect", [(100, Status.INVALID_ARG), (-64, Status.INVALID_ARG),
+                                          (128, Status.OK)])
+def test_state_split_size(lib, split, expect):
+    # split_size: 0 or a positive multiple of 64; the stored states then number
+    # ceil(T / split_size) per sequence (T = 300, split 128: 3 per sequence)
+    a = GdnStateArgs(dtype=1, k=FAKE, v=FAKE, gate=0, hs=FAKE, hs_dtype=0, B=2, T=300, H=2,
+                     K=64, V=64, N=2, chunk_size=64, num_chunks=6, split_size=split)
+    st = lib.gdn_chunk_state_fwd(ctypes.byref(a), None)
+    if expect == Status.OK:
+        # the sizes pass; the first CUDA call then fails without a GPU
+        assert st != Status.INVALID_ARG, lib.gdn_last_error_message()
+        a.num_chunks = 5
+        assert lib.gdn_chunk_state_fwd(ctypes.byref(a), None) == Status.INVALID_ARG
+        assert "needed" in lib.gdn_last_error_message().decode()
+    else:
+        assert st == expect

@@ -24,21 +24,22 @@ def _dev(x):
     return None if x is None else x.cuda()
 
 
-def run(inp, states_dtype=torch.float32, output_states=True, scale="inp"):
+def run(inp, states_dtype=torch.float32, output_states=True, scale="inp", split_size=None):
     dh, dh0 = gdn.gdn_chunk_state_bwd(
         inp["q"].cuda(), inp["do"].cuda(), gate=inp["gate"], gate_values=_dev(inp["gate_values"]),
         dht=_dev(inp["dht"]), cu_seqlens=_dev(inp["cu_seqlens"]),
         scale=inp["scale"] if scale == "inp" else scale, states_dtype=states_dtype,
-        output_states=output_states)
+        output_states=output_states, split_size=split_size)
     torch.cuda.synchronize()
     assert gdn.gdn_check_device_error() == Status.OK
     return dh, dh0
 
 
-def oracle(inp, scale="inp"):
+def oracle(inp, scale="inp", split_size=None):
     return SP.chunk_state_grad(inp["q"], inp["do"], inp["gate"], inp["gate_values"],
                                dht=inp["dht"], cu_seqlens=inp["cu_seqlens"],
-                               scale=inp["scale"] if scale == "inp" else scale)
+                               scale=inp["scale"] if scale == "inp" else scale,
+                               split_size=split_size)
 
 
 @pytest.mark.parametrize("gate", GATES)
@@ -146,3 +147,22 @@ def test_tensor_core_path_chunk_boundaries(T, gate):
     assert tuple(dh.shape) == dh_ref.shape
     assert_close(dh, dh_ref, TOL_F32, f"dh ({gate}, T={T})")
     assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate}, T={T})")
+
+
+@pytest.mark.parametrize("split", [128, 192])
+@pytest.mark.parametrize("K,dtype", [(128, torch.bfloat16), (32, torch.float32)])
+def test_split_size(split, K, dtype):
+    inp = synth.state_grad_inputs(88, 2, 333, 2, 2, K, 64, "gk", dtype=dtype, dht_std=0.3)
+    dh, dh0 = run(inp, split_size=split)
+    dh_ref, dh0_ref = oracle(inp, split_size=split)
+    assert tuple(dh.shape) == dh_ref.shape
+    assert_close(dh, dh_ref, TOL_F32, f"dh (split {split})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 (split {split})")
+    lengths = [200, 0, 64, 260]
+    inp = synth.state_grad_inputs(89, 1, sum(lengths), 2, 2, K, 64, "g", dtype=dtype,
+                                  lengths=lengths, dht_std=0.3)
+    dh, dh0 = run(inp, split_size=split)
+    dh_ref, dh0_ref = oracle(inp, split_size=split)
+    assert tuple(dh.shape) == dh_ref.shape
+    assert_close(dh, dh_ref, TOL_F32, f"dh packed (split {split})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 packed (split {split})")

@@ -26,19 +26,19 @@ def _dev(x):
     return None if x is None else x.cuda()
 
 
-def run(inp, states_dtype=torch.float32, output_states=True):
+def run(inp, states_dtype=torch.float32, output_states=True, split_size=None):
     hs, ht = gdn.gdn_chunk_state_fwd(
         inp["k"].cuda(), inp["v"].cuda(), gate=inp["gate"], gate_values=_dev(inp["gate_values"]),
         initial_state=_dev(inp["h0"]), cu_seqlens=_dev(inp["cu_seqlens"]),
-        states_dtype=states_dtype, output_states=output_states)
+        states_dtype=states_dtype, output_states=output_states, split_size=split_size)
     torch.cuda.synchronize()
     assert gdn.gdn_check_device_error() == Status.OK
     return hs, ht
 
 
-def oracle(inp):
+def oracle(inp, split_size=None):
     return SP.chunk_state_pass(inp["k"], inp["v"], inp["gate"], inp["gate_values"], h0=inp["h0"],
-                               cu_seqlens=inp["cu_seqlens"])
+                               cu_seqlens=inp["cu_seqlens"], split_size=split_size)
 
 
 @pytest.mark.parametrize("gate", GATES)
@@ -153,3 +153,24 @@ def test_tensor_core_path_chunk_boundaries(T, gate):
     assert tuple(hs.shape) == hs_ref.shape
     assert_close(hs, hs_ref, TOL_F32, f"hs ({gate}, T={T})")
     assert_close(ht, ht_ref, TOL_F32, f"ht ({gate}, T={T})")
+
+
+@pytest.mark.parametrize("split", [128, 192])
+@pytest.mark.parametrize("K,dtype", [(128, torch.bfloat16), (32, torch.float32)])
+def test_split_size(split, K, dtype):
+    # states stored every split / 64 chunks, fixed-length and packed sequences,
+    # tensor-core (K = 128 bf16) and exact kernels
+    inp = synth.state_pass_inputs(77, 2, 333, 2, K, 64, "g", dtype=dtype, h0_std=0.3)
+    hs, ht = run(inp, split_size=split)
+    hs_ref, ht_ref = oracle(inp, split_size=split)
+    assert tuple(hs.shape) == hs_ref.shape
+    assert_close(hs, hs_ref, TOL_F32, f"hs (split {split})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht (split {split})")
+    lengths = [200, 0, 64, 260]
+    inp = synth.state_pass_inputs(78, 1, sum(lengths), 2, K, 64, "gv", dtype=dtype,
+                                  lengths=lengths, h0_std=0.3)
+    hs, ht = run(inp, split_size=split)
+    hs_ref, ht_ref = oracle(inp, split_size=split)
+    assert tuple(hs.shape) == hs_ref.shape
+    assert_close(hs, hs_ref, TOL_F32, f"hs packed (split {split})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht packed (split {split})")
