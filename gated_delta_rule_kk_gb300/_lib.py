@@ -94,6 +94,7 @@ class GdnStateArgs(ctypes.Structure):
         ("N", c_int32), ("chunk_size", c_int32),
         ("num_chunks", ctypes.c_int64),
         ("split_size", c_int32),
+        ("state_v_first", c_int32),
     ]
 
 
@@ -110,6 +111,7 @@ class GdnStateBwdArgs(ctypes.Structure):
         ("num_chunks", ctypes.c_int64),
         ("scale", c_float),
         ("split_size", c_int32),
+        ("state_v_first", c_int32),
     ]
 
 

@@ -327,7 +327,7 @@ def _split_tokens(split_size):
 def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, cu_seqlens=None,
                         output_final_state=True, output_states=True,
                         states_dtype=torch.float32, out_states=None, final_state=None,
-                        num_chunks=None, split_size=None, stream=None):
+                        num_chunks=None, split_size=None, state_v_first=False, stream=None):
     """Chunk state pass of gated linear attention.  Returns ``(hs, ht)``.
 
     k [B,T,H,K], v [B,T,H,V] (float32 or bfloat16); gate one of None, "g"
@@ -336,7 +336,8 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
     initial_state [N,H,K,V] float32.  hs holds the state at the start of every
     split of ``split_size`` tokens (a multiple of 64; default 64: every
     chunk), sequence after sequence ([C,H,K,V]); with ``cu_seqlens`` and no
-    ``num_chunks``, C is read from the lengths (a device sync).
+    ``num_chunks``, C is read from the lengths (a device sync).  With
+    ``state_v_first`` every state (initial_state, hs, ht) is [.., V, K].
     """
     split = _split_tokens(split_size)
     dev = k.device
@@ -358,18 +359,19 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
         N = B
     if num_chunks is None and (output_states or out_states is not None or cu_seqlens is None):
         num_chunks = _stored_states(B, T, cu_seqlens, split)
+    SK, SV = (V, K) if state_v_first else (K, V)
     if initial_state is not None:
         _need(initial_state, "initial_state", (torch.float32,), dev)
-        if tuple(initial_state.shape) != (N, H, K, V):
-            raise ValueError(f"initial_state must be [{N},{H},{K},{V}]")
+        if tuple(initial_state.shape) != (N, H, SK, SV):
+            raise ValueError(f"initial_state must be [{N},{H},{SK},{SV}]")
     hs = out_states
     if hs is None and output_states:
-        hs = torch.empty((num_chunks, H, K, V), dtype=states_dtype, device=dev)
+        hs = torch.empty((num_chunks, H, SK, SV), dtype=states_dtype, device=dev)
     if hs is not None:
         _need(hs, "out_states", (torch.float32, torch.bfloat16), dev)
     ht = final_state
     if ht is None and output_final_state:
-        ht = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+        ht = torch.empty((N, H, SK, SV), dtype=torch.float32, device=dev)
     elif ht is not None:
         _need(ht, "final_state", (torch.float32,), dev)
     a = GdnStateArgs(dtype=int(dt), k=_ptr(k), v=_ptr(v), gate=int(_GATES[gate]),
@@ -378,7 +380,8 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
                      hs_dtype=int(DType.BF16 if hs is not None and hs.dtype == torch.bfloat16
                                   else DType.F32),
                      cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, K=K, V=V, N=N,
-                     chunk_size=CHUNK, num_chunks=int(num_chunks or 0), split_size=split)
+                     chunk_size=CHUNK, num_chunks=int(num_chunks or 0), split_size=split,
+                     state_v_first=int(bool(state_v_first)))
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_state_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_fwd")
     return hs, ht
@@ -387,14 +390,15 @@ def gdn_chunk_state_fwd(k, v, gate=None, gate_values=None, initial_state=None, c
 def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=None,
                         scale=None, output_dh0=True, output_states=True,
                         states_dtype=torch.float32, out_states=None, dh0=None,
-                        num_chunks=None, split_size=None, stream=None):
+                        num_chunks=None, split_size=None, state_v_first=False, stream=None):
     """Backward state pass (dh recurrence).  Returns ``(dh, dh0)``.
 
     q [B,T,HQ,K], do [B,T,HQ,V] (float32 or bfloat16); gate and gate_values
     as :func:`gdn_chunk_state_fwd` with H gate heads (HQ % H == 0); dht
     [N,HQ,K,V] float32.  dh [C,HQ,K,V] is the gradient at the end of the
     first 64-token chunk of every split of ``split_size`` tokens (default 64:
-    every chunk), sequence after sequence.
+    every chunk), sequence after sequence.  With ``state_v_first`` every
+    state gradient (dht, dh, dh0) is [.., V, K].
     """
     split = _split_tokens(split_size)
     dev = q.device
@@ -418,17 +422,18 @@ def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens
         N = B
     if num_chunks is None and (output_states or out_states is not None or cu_seqlens is None):
         num_chunks = _stored_states(B, T, cu_seqlens, split)
+    SK, SV = (V, K) if state_v_first else (K, V)
     if dht is not None:
         _need(dht, "dht", (torch.float32,), dev)
-        if tuple(dht.shape) != (N, HQ, K, V):
-            raise ValueError(f"dht must be [{N},{HQ},{K},{V}]")
+        if tuple(dht.shape) != (N, HQ, SK, SV):
+            raise ValueError(f"dht must be [{N},{HQ},{SK},{SV}]")
     dh = out_states
     if dh is None and output_states:
-        dh = torch.empty((num_chunks, HQ, K, V), dtype=states_dtype, device=dev)
+        dh = torch.empty((num_chunks, HQ, SK, SV), dtype=states_dtype, device=dev)
     if dh is not None:
         _need(dh, "out_states", (torch.float32, torch.bfloat16), dev)
     if dh0 is None and output_dh0:
-        dh0 = torch.empty((N, HQ, K, V), dtype=torch.float32, device=dev)
+        dh0 = torch.empty((N, HQ, SK, SV), dtype=torch.float32, device=dev)
     elif dh0 is not None:
         _need(dh0, "dh0", (torch.float32,), dev)
     a = GdnStateBwdArgs(dtype=int(dt), q=_ptr(q), do_=_ptr(do), gate=int(_GATES[gate]),
@@ -438,7 +443,8 @@ def gdn_chunk_state_bwd(q, do, gate=None, gate_values=None, dht=None, cu_seqlens
                                      else DType.F32),
                         cu_seqlens=_ptr(cu_seqlens), B=B, T=T, HQ=HQ, H=H, K=K, V=V, N=N,
                         chunk_size=CHUNK, num_chunks=int(num_chunks or 0),
-                        scale=float(scale) if scale is not None else 0.0, split_size=split)
+                        scale=float(scale) if scale is not None else 0.0, split_size=split,
+                        state_v_first=int(bool(state_v_first)))
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_state_bwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_state_bwd")
     return dh, dh0

@@ -239,6 +239,8 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
   REQUIRE(a->split_size >= 0 && a->split_size % BT == 0, GDN_ERR_INVALID_ARG,
           "split_size (%d) must be 0 or a positive multiple of %d", a->split_size, BT);
   const int split = a->split_size > 0 ? a->split_size / BT : 1;
+  REQUIRE(a->state_v_first == 0 || a->state_v_first == 1, GDN_ERR_INVALID_ARG,
+          "state_v_first must be 0 or 1");
   if (a->cu_seqlens == nullptr) {
     REQUIRE(a->N == a->B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)",
             a->N, a->B);
@@ -278,6 +280,7 @@ gdn_status_t gdn_chunk_state_fwd(const gdn_state_args *a, gdn_stream_t stream) {
   p.reverse = 0;
   p.scale = 1.f;
   p.split = split;
+  p.v_first = a->state_v_first;
   p.err = device_error_word();
   if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
   return cuda_status(launch_state_pass(p, a->dtype == GDN_BF16,
@@ -310,6 +313,8 @@ gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t strea
   REQUIRE(a->split_size >= 0 && a->split_size % BT == 0, GDN_ERR_INVALID_ARG,
           "split_size (%d) must be 0 or a positive multiple of %d", a->split_size, BT);
   const int split = a->split_size > 0 ? a->split_size / BT : 1;
+  REQUIRE(a->state_v_first == 0 || a->state_v_first == 1, GDN_ERR_INVALID_ARG,
+          "state_v_first must be 0 or 1");
   REQUIRE(isfinite(a->scale), GDN_ERR_INVALID_ARG, "scale must be finite");
   if (a->cu_seqlens == nullptr) {
     REQUIRE(a->N == a->B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)",
@@ -350,6 +355,7 @@ gdn_status_t gdn_chunk_state_bwd(const gdn_state_bwd_args *a, gdn_stream_t strea
   p.reverse = 1;
   p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)a->K);
   p.split = split;
+  p.v_first = a->state_v_first;
   p.err = device_error_word();
   if (p.err == nullptr) return cuda_status(cudaGetLastError(), "device error word");
   return cuda_status(launch_state_pass(p, a->dtype == GDN_BF16,

@@ -55,6 +55,7 @@ struct StateParams {
   int reverse;
   float scale;
   int split;                  // chunks per stored state (>= 1): hs holds chunks 0, split, ..
+  int v_first;                // h0, ht, hs as [V, K] instead of [K, V]
 };
 
 // Each launcher enqueues its kernel(s) and returns the launch status.

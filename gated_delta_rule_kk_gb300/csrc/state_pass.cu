@@ -216,11 +216,13 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(StateParams p
   const SeqInfo sq = sequence_of(p, n, tid, seq_info);
 
   float hv[16];
-  const size_t sbase = (((size_t)n * H + h) * K + r) * V;
+  // element (key r, column col) of a [K, V] state (or [V, K] with v_first)
+  const size_t hbase = ((size_t)n * H + h) * K * V;
+  auto at = [&](int col) { return p.v_first ? (size_t)col * K + r : (size_t)r * V + col; };
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = v0 + c0 + j;
-    hv[j] = (p.h0 && row_ok && col < V) ? p.h0[sbase + col] : 0.f;
+    hv[j] = (p.h0 && row_ok && col < V) ? p.h0[hbase + at(col)] : 0.f;
   }
 
   // chunk of the it-th step: forward from the first, backward from the last
@@ -241,8 +243,20 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(StateParams p
       store_i += p.reverse ? -1 : 1;
     }
 
-    // chunk-start state, 8 columns (16 or 32 bytes) per store
-    if (sq.write_hs && row_ok && store) {
+    // chunk-start state, 8 columns (16 or 32 bytes) per store; one element
+    // at a time in the [V, K] layout
+    if (sq.write_hs && row_ok && store && p.v_first) {
+      const size_t sb = ((size_t)slot * H + h) * K * V;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int col = v0 + c0 + j;
+        if (col >= V) continue;
+        if (p.hs_bf16)
+          static_cast<__nv_bfloat16 *>(p.hs)[sb + at(col)] = __float2bfloat16_rn(hv[j]);
+        else
+          static_cast<float *>(p.hs)[sb + at(col)] = hv[j];
+      }
+    } else if (sq.write_hs && row_ok && store) {
       const size_t o = (((size_t)slot * H + h) * K + r) * V + v0 + c0;
 #pragma unroll
       for (int g8 = 0; g8 < 2; ++g8) {
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(StateParams p
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int col = v0 + c0 + j;
-      if (col < V) p.ht[sbase + col] = hv[j];
+      if (col < V) p.ht[hbase + at(col)] = hv[j];
     }
   }
 }
@@ -504,9 +518,10 @@ __device__ __forceinline__ void tc_stage(const StateParams &p, const unsigned ch
 }
 
 // RING slots; KSTAGE: the per-key gate (k~ staged; RING = 2 for its 32 KB gate
-// rows).  Without KSTAGE the MMAs of a step read k from its ring slot, so a
-// slot is refilled one step later (LAG = 1) than when only staging reads it.
-template <int RING, bool KSTAGE>
+// rows); VF: states in the [V, K] layout.  Without KSTAGE the MMAs of a step
+// read k from its ring slot, so a slot is refilled one step later (LAG = 1)
+// than when only staging reads it.
+template <int RING, bool KSTAGE, bool VF>
 __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParams p) {
   constexpr int LAG = KSTAGE ? 0 : 1;
   static_assert(RING >= 2 + LAG, "the ring must hold the staged, the computed and a refilled slot");
@@ -530,15 +545,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
   // accumulator rows rA = 16 kb + g and rA + 8, columns v0 + cl + 8 nt (+ 1)
   const int rA = 16 * kb + g, cl = 16 * ch + 2 * tig, cB = v0 + cl;
   float C[2][4];
-  const size_t sA = (((size_t)n * H + h) * K + rA) * V, sB = sA + (size_t)8 * V;
+  // element (key, column) of a [K, V] state (or [V, K] with v_first); the
+  // accumulator element e of n-tile nt is (rA + 8 (e >> 1), cB + 8 nt + (e & 1))
+  const size_t hbase = ((size_t)n * H + h) * K * V;
+  auto at = [&](int key, int col) { return VF ? (size_t)col * K + key : (size_t)key * V + col; };
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const int col = cB + 8 * nt;
     const bool ok = p.h0 && col < V;  // V is a multiple of 8, so col + 1 < V too
-    C[nt][0] = ok ? p.h0[sA + col] : 0.f;
-    C[nt][1] = ok ? p.h0[sA + col + 1] : 0.f;
-    C[nt][2] = ok ? p.h0[sB + col] : 0.f;
-    C[nt][3] = ok ? p.h0[sB + col + 1] : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      C[nt][e] = ok ? p.h0[hbase + at(rA + 8 * (e >> 1), col + (e & 1))] : 0.f;
   }
 
   // chunk of the it-th step: forward from the first, backward from the last
@@ -571,8 +588,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
       store_i += p.reverse ? -1 : 1;
     }
 
-    // chunk-start state: two columns per 8-column tile and row
-    if (sq.write_hs && store) {
+    // chunk-start state: two columns per 8-column tile and row; one element
+    // at a time in the [V, K] layout
+    if (VF && sq.write_hs && store) {
+      const size_t sb = ((size_t)slot * H + h) * K * V;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int col = cB + 8 * nt;
+        if (col >= V) continue;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const size_t o = sb + at(rA + 8 * (e >> 1), col + (e & 1));
+          if (p.hs_bf16)
+            static_cast<__nv_bfloat16 *>(p.hs)[o] = __float2bfloat16_rn(C[nt][e]);
+          else
+            static_cast<float *>(p.hs)[o] = C[nt][e];
+        }
+      }
+    } else if (!VF && sq.write_hs && store) {
       const size_t oA = (((size_t)slot * H + h) * K + rA) * V, oB = oA + (size_t)8 * V;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -650,10 +683,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
     for (int nt = 0; nt < 2; ++nt) {
       const int col = cB + 8 * nt;
       if (col >= V) continue;
-      p.ht[sA + col] = C[nt][0];
-      p.ht[sA + col + 1] = C[nt][1];
-      p.ht[sB + col] = C[nt][2];
-      p.ht[sB + col + 1] = C[nt][3];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p.ht[hbase + at(rA + 8 * (e >> 1), col + (e & 1))] = C[nt][e];
     }
   }
 }
@@ -668,7 +699,10 @@ cudaError_t launch_state_pass(const StateParams &p, bool bf16, cudaStream_t stre
     const bool kstage = p.gate == GDN_GATE_GK;
     const int ring = kstage ? 2 : 6;
     const int smem = (int)(2 * tc_buf_bytes(kstage) + ring * ring_slot_bytes(p.gate));
-    auto kern = kstage ? state_pass_tc_kernel<2, true> : state_pass_tc_kernel<6, false>;
+    auto kern = kstage ? (p.v_first ? state_pass_tc_kernel<2, true, true>
+                                    : state_pass_tc_kernel<2, true, false>)
+                       : (p.v_first ? state_pass_tc_kernel<6, false, true>
+                                    : state_pass_tc_kernel<6, false, false>);
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -176,6 +176,9 @@ gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *args, gdn_stream_t stream)
  *   cu_seqlens [N + 1] int32   as gdn_chunk_fwd (device memory; checked on the
  *                              device, GDN_ERR_BAD_SEQLENS also when the chunks
  *                              do not fit num_chunks)
+ *   state_v_first = 1          every state tensor (h0, ht, hs) holds each
+ *                              state transposed, [V, K] (the page's
+ *                              state_v_first); the arithmetic is unchanged
  * Limits: 1 <= K <= 128, K and V multiples of 8, chunk_size == 64, N and H at
  * most 65535.
  * Arithmetic in fp32 (bf16 inputs are widened).  Nothing is allocated; no
@@ -203,6 +206,7 @@ typedef struct gdn_state_args {
   int32_t chunk_size;
   int64_t num_chunks;
   int32_t split_size;          /* tokens between stored states; 0 = chunk_size */
+  int32_t state_v_first;       /* 1: h0, ht, hs are [.., V, K] instead of [.., K, V] */
 } gdn_state_args;
 
 /* Enqueue the chunk state pass on `stream`. */
@@ -242,6 +246,7 @@ typedef struct gdn_state_bwd_args {
   int64_t num_chunks;
   float scale;
   int32_t split_size;          /* tokens between stored gradients; 0 = chunk_size */
+  int32_t state_v_first;       /* 1: dht, dh0, dh are [.., V, K] instead of [.., K, V] */
 } gdn_state_bwd_args;
 
 /* Enqueue the backward state pass on `stream`. */

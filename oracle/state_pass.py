@@ -58,7 +58,7 @@ def _split(chunk_size, split_size):
 
 
 def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None,
-                     chunk_size: int = 64, split_size=None):
+                     chunk_size: int = 64, split_size=None, state_v_first: bool = False):
     """Chunk-start states ``hs`` ``[sum NT_n, H, K, V]`` and final states
     ``ht`` ``[N, H, K, V]`` of the gated linear-attention recurrence.
 
@@ -66,6 +66,8 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
     ``g_gamma`` ``[H]``, ``gk`` ``[B, T, H, K]``, ``gv`` ``[B, T, H, V]``
     (chunk-local cumulative sums except ``g_gamma``); h0 ``[N, H, K, V]`` or
     None (zeros); split_size stores every (split_size / chunk_size)-th chunk.
+    With state_v_first every state (h0 in, hs and ht out) is [.., V, K]: the
+    page's layout flag, which transposes the stored states and nothing else.
     """
     NTS = _split(chunk_size, split_size)
     if gate not in GATES:
@@ -77,6 +79,8 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
     seqs = sequence_bounds(B, T, cu_seqlens)
     N = len(seqs)
     h0 = np.zeros((N, H, K, V)) if h0 is None else _f64(h0)
+    if state_v_first:
+        h0 = h0.swapaxes(-1, -2)
     counts = chunk_counts(B, T, cu_seqlens, chunk_size, split_size)
     hs = np.zeros((sum(counts), H, K, V))
     ht = np.zeros((N, H, K, V))
@@ -102,11 +106,14 @@ def chunk_state_pass(k, v, gate=None, gate_values=None, h0=None, cu_seqlens=None
                 S = S + np.outer(k[b, t, h], v[b, t, h])
             ht[n, h] = S
         first += counts[n]
+    if state_v_first:
+        return hs.swapaxes(-1, -2), ht.swapaxes(-1, -2)
     return hs, ht
 
 
 def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=None,
-                     scale=None, chunk_size: int = 64, split_size=None):
+                     scale=None, chunk_size: int = 64, split_size=None,
+                     state_v_first: bool = False):
     """Backward state pass (the chunk_h page's ``chunk_bwd_kernel_dh``).
 
     For the gated linear attention above with outputs o_t = scale S_t^T q_t
@@ -123,7 +130,8 @@ def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=No
     the gate has H heads (HQ a multiple of H, query head hq uses gate head
     hq // (HQ / H)), given as in :func:`chunk_state_pass`.  With split_size
     only chunks whose index is a multiple of split_size / chunk_size are
-    stored, at index chunk // (split_size / chunk_size).
+    stored, at index chunk // (split_size / chunk_size).  state_v_first: dht,
+    dh and dh0 are [.., V, K], as in :func:`chunk_state_pass`.
     """
     NTS = _split(chunk_size, split_size)
     if gate not in GATES:
@@ -143,6 +151,8 @@ def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=No
     seqs = sequence_bounds(B, T, cu_seqlens)
     N = len(seqs)
     dht = np.zeros((N, HQ, K, V)) if dht is None else _f64(dht)
+    if state_v_first:
+        dht = dht.swapaxes(-1, -2)
     counts = chunk_counts(B, T, cu_seqlens, chunk_size, split_size)
     dh = np.zeros((sum(counts), HQ, K, V))
     dh0 = np.zeros((N, HQ, K, V))
@@ -170,4 +180,6 @@ def chunk_state_grad(q, do, gate=None, gate_values=None, dht=None, cu_seqlens=No
                     G = G * np.exp(raw[t, h])[None, :]
             dh0[n, hq] = G
         first += counts[n]
+    if state_v_first:
+        return dh.swapaxes(-1, -2), dh0.swapaxes(-1, -2)
     return dh, dh0

@@ -166,3 +166,18 @@ def test_split_size(split, K, dtype):
     assert tuple(dh.shape) == dh_ref.shape
     assert_close(dh, dh_ref, TOL_F32, f"dh packed (split {split})")
     assert_close(dh0, dh0_ref, TOL_F32, f"dh0 packed (split {split})")
+
+
+@pytest.mark.parametrize("K,dtype", [(128, torch.bfloat16), (32, torch.float32)])
+def test_state_v_first(K, dtype):
+    inp = synth.state_grad_inputs(90, 2, 200, 4, 2, K, 48, "gv", dtype=dtype, dht_std=0.3)
+    dh_ref, dh0_ref = oracle(inp)
+    dh, dh0 = gdn.gdn_chunk_state_bwd(
+        inp["q"].cuda(), inp["do"].cuda(), gate="gv", gate_values=inp["gate_values"].cuda(),
+        dht=inp["dht"].transpose(-1, -2).contiguous().cuda(), scale=inp["scale"],
+        state_v_first=True)
+    torch.cuda.synchronize()
+    assert gdn.gdn_check_device_error() == Status.OK
+    assert tuple(dh.shape) == (8, 4, 48, K)
+    assert_close(dh, dh_ref.swapaxes(-1, -2), TOL_F32, "dh [V, K]")
+    assert_close(dh0, dh0_ref.swapaxes(-1, -2), TOL_F32, "dh0 [V, K]")

@@ -174,3 +174,21 @@ def test_split_size(split, K, dtype):
     assert tuple(hs.shape) == hs_ref.shape
     assert_close(hs, hs_ref, TOL_F32, f"hs packed (split {split})")
     assert_close(ht, ht_ref, TOL_F32, f"ht packed (split {split})")
+
+
+@pytest.mark.parametrize("K,dtype,states_dtype", [(128, torch.bfloat16, torch.float32),
+                                                  (128, torch.bfloat16, torch.bfloat16),
+                                                  (32, torch.float32, torch.float32)])
+def test_state_v_first(K, dtype, states_dtype):
+    # every state [V, K]: h0 in, hs and ht out (a partial value tile, a split)
+    inp = synth.state_pass_inputs(79, 2, 200, 2, K, 48, "gk", dtype=dtype, h0_std=0.3)
+    hs_ref, ht_ref = oracle(inp, split_size=128)
+    hs, ht = gdn.gdn_chunk_state_fwd(
+        inp["k"].cuda(), inp["v"].cuda(), gate="gk", gate_values=inp["gate_values"].cuda(),
+        initial_state=inp["h0"].transpose(-1, -2).contiguous().cuda(), split_size=128,
+        states_dtype=states_dtype, state_v_first=True)
+    torch.cuda.synchronize()
+    assert gdn.gdn_check_device_error() == Status.OK
+    assert tuple(hs.shape) == (4, 2, 48, K) and tuple(ht.shape) == (2, 2, 48, K)
+    assert_close(hs, hs_ref.swapaxes(-1, -2), TOL_F32, "hs [V, K]")
+    assert_close(ht, ht_ref.swapaxes(-1, -2), TOL_F32, "ht [V, K]")

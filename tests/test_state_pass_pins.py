@@ -227,3 +227,22 @@ def test_split_size_keeps_every_split_chunk(split):
     dhS, dh0S = SP.chunk_state_grad(k, v, "gk", gk, dht=h0, cu_seqlens=cu, split_size=split)
     np.testing.assert_array_equal(dhS, dh1[keep])
     np.testing.assert_array_equal(dh0S, dh01)
+
+
+def test_state_v_first_transposes_every_state():
+    # the page's state_v_first: h0 in and every state out are [V, K]; the
+    # recurrence is unchanged
+    rng = np.random.default_rng(22)
+    B, T, H, K, V = 2, 150, 2, 8, 4
+    k, v = rng.standard_normal((B, T, H, K)), rng.standard_normal((B, T, H, V))
+    raw = -0.05 * np.abs(rng.standard_normal((B, T, H)))
+    g = np.concatenate([np.cumsum(raw[:, c:c + 64], axis=1) for c in range(0, T, 64)], axis=1)
+    h0 = rng.standard_normal((B, H, K, V))
+    hs, ht = SP.chunk_state_pass(k, v, "g", g, h0=h0)
+    hsT, htT = SP.chunk_state_pass(k, v, "g", g, h0=h0.swapaxes(-1, -2), state_v_first=True)
+    np.testing.assert_array_equal(hsT, hs.swapaxes(-1, -2))
+    np.testing.assert_array_equal(htT, ht.swapaxes(-1, -2))
+    dh, dh0 = SP.chunk_state_grad(k, v, "g", g, dht=h0)
+    dhT, dh0T = SP.chunk_state_grad(k, v, "g", g, dht=h0.swapaxes(-1, -2), state_v_first=True)
+    np.testing.assert_array_equal(dhT, dh.swapaxes(-1, -2))
+    np.testing.assert_array_equal(dh0T, dh0.swapaxes(-1, -2))
