@@ -518,10 +518,11 @@ __device__ __forceinline__ void tc_stage(const StateParams &p, const unsigned ch
 }
 
 // RING slots; KSTAGE: the per-key gate (k~ staged; RING = 2 for its 32 KB gate
-// rows); VF: states in the [V, K] layout.  Without KSTAGE the MMAs of a step
+// rows); VF: states in the [V, K] layout; SPLIT: a state stored every p.split
+// > 1 chunks (else every chunk).  Without KSTAGE the MMAs of a step
 // read k from its ring slot, so a slot is refilled one step later (LAG = 1)
 // than when only staging reads it.
-template <int RING, bool KSTAGE, bool VF>
+template <int RING, bool KSTAGE, bool VF, bool SPLIT>
 __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParams p) {
   constexpr int LAG = KSTAGE ? 0 : 1;
   static_assert(RING >= 2 + LAG, "the ring must hold the staged, the computed and a refilled slot");
@@ -549,13 +550,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
   // accumulator element e of n-tile nt is (rA + 8 (e >> 1), cB + 8 nt + (e & 1))
   const size_t hbase = ((size_t)n * H + h) * K * V;
   auto at = [&](int key, int col) { return VF ? (size_t)col * K + key : (size_t)key * V + col; };
+  const size_t sA = hbase + (size_t)rA * V, sB = sA + (size_t)8 * V;  // [K, V] rows rA, rA + 8
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const int col = cB + 8 * nt;
     const bool ok = p.h0 && col < V;  // V is a multiple of 8, so col + 1 < V too
+    if (VF) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      C[nt][e] = ok ? p.h0[hbase + at(rA + 8 * (e >> 1), col + (e & 1))] : 0.f;
+      for (int e = 0; e < 4; ++e)
+        C[nt][e] = ok ? p.h0[hbase + at(rA + 8 * (e >> 1), col + (e & 1))] : 0.f;
+    } else {
+      C[nt][0] = ok ? p.h0[sA + col] : 0.f;
+      C[nt][1] = ok ? p.h0[sA + col + 1] : 0.f;
+      C[nt][2] = ok ? p.h0[sB + col] : 0.f;
+      C[nt][3] = ok ? p.h0[sB + col + 1] : 0.f;
+    }
   }
 
   // chunk of the it-th step: forward from the first, backward from the last
@@ -569,7 +578,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
     ptx::cp_async_commit();
   }
   // stored chunks 0, split, 2 split, ..; the reverse pass meets them last first
-  int store_i = p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
+  int store_i = SPLIT && p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
   int store_c = store_i * p.split;
   TcDecay dec;
   if (sq.nch > 0) {
@@ -581,11 +590,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
 #pragma unroll 1
   for (int it = 0; it < sq.nch; ++it) {
     const int c = chunk_at(it);
-    const bool store = c == store_c;
-    const long long slot = sq.first + store_i;
-    if (store) {
-      store_c += p.reverse ? -p.split : p.split;
-      store_i += p.reverse ? -1 : 1;
+    bool store = true;
+    long long slot = sq.first + c;
+    if (SPLIT) {
+      store = c == store_c;
+      slot = sq.first + store_i;
+      if (store) {
+        store_c += p.reverse ? -p.split : p.split;
+        store_i += p.reverse ? -1 : 1;
+      }
     }
 
     // chunk-start state: two columns per 8-column tile and row; one element
@@ -683,8 +696,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
     for (int nt = 0; nt < 2; ++nt) {
       const int col = cB + 8 * nt;
       if (col >= V) continue;
+      if (VF) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) p.ht[hbase + at(rA + 8 * (e >> 1), col + (e & 1))] = C[nt][e];
+        for (int e = 0; e < 4; ++e) p.ht[hbase + at(rA + 8 * (e >> 1), col + (e & 1))] = C[nt][e];
+      } else {
+        p.ht[sA + col] = C[nt][0];
+        p.ht[sA + col + 1] = C[nt][1];
+        p.ht[sB + col] = C[nt][2];
+        p.ht[sB + col + 1] = C[nt][3];
+      }
     }
   }
 }
@@ -699,10 +719,18 @@ cudaError_t launch_state_pass(const StateParams &p, bool bf16, cudaStream_t stre
     const bool kstage = p.gate == GDN_GATE_GK;
     const int ring = kstage ? 2 : 6;
     const int smem = (int)(2 * tc_buf_bytes(kstage) + ring * ring_slot_bytes(p.gate));
-    auto kern = kstage ? (p.v_first ? state_pass_tc_kernel<2, true, true>
-                                    : state_pass_tc_kernel<2, true, false>)
-                       : (p.v_first ? state_pass_tc_kernel<6, false, true>
-                                    : state_pass_tc_kernel<6, false, false>);
+    const bool split = p.split > 1;
+    auto pick = [&](auto k00, auto k01, auto k10, auto k11) {
+      return p.v_first ? (split ? k11 : k10) : (split ? k01 : k00);
+    };
+    auto kern = kstage ? pick(state_pass_tc_kernel<2, true, false, false>,
+                              state_pass_tc_kernel<2, true, false, true>,
+                              state_pass_tc_kernel<2, true, true, false>,
+                              state_pass_tc_kernel<2, true, true, true>)
+                       : pick(state_pass_tc_kernel<6, false, false, false>,
+                              state_pass_tc_kernel<6, false, false, true>,
+                              state_pass_tc_kernel<6, false, true, false>,
+                              state_pass_tc_kernel<6, false, true, true>);
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
