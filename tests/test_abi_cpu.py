@@ -299,3 +299,17 @@ def test_state_split_size(lib, split, expect):
         assert "needed" in lib.gdn_last_error_message().decode()
     else:
         assert st == expect
+
+
+def test_state_pass_binding_rejects_bad_split_before_any_call():
+    # the binding checks split_size first, so no library call (or GPU) is
+    # needed to see the error
+    import torch
+    import gated_delta_rule_kk_gb300 as gdn
+    k = torch.zeros(1, 64, 2, 64)
+    v = torch.zeros(1, 64, 2, 64)
+    for bad in (100, -64, 32):
+        with pytest.raises(ValueError, match="multiple of 64"):
+            gdn.gdn_chunk_state_fwd(k, v, split_size=bad)
+        with pytest.raises(ValueError, match="multiple of 64"):
+            gdn.gdn_chunk_state_bwd(k, v, split_size=bad)
