@@ -249,7 +249,8 @@ def run_ours(args, rank, world, dev):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (bf16 inputs; hi/lo bf16 tensor-core products, fp32 accumulation and state)",
         "data": "synthetic (seeded numpy draws, see gated_delta_rule_kk_gb300/synth.py)",
         "config": {"workload": WORKLOAD, "global_batch": dm["B"] * world, "seq_len": dm["T"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -421,55 +422,88 @@ def run_ours(args, rank, world, dev):
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_sample(target_s):
-    """Time the fp64 oracle on whole (sequence, head) chains of the headline
-    workload until about `target_s` seconds have passed.  Returns
-    (token-equivalents per second, seconds, chains)."""
+def _headline_chain_specs():
+    """One oracle call per (sequence, head) chain of the headline workload, its
+    inputs sliced to that chain (the chains are independent)."""
     from gated_delta_rule_kk_gb300 import synth
-    from oracle import recurrence as R
     inp = synth.gdn_prefill()
     dm = inp["dims"]
+    f = {k: inp[k].float().numpy() for k in ("q", "k", "v", "g", "beta", "h0")}
+    specs = []
+    for i in range(dm["B"] * dm["H"]):
+        n, h = i % dm["B"], (i // dm["B"]) % dm["H"]
+        hk = h // (dm["H"] // dm["Hg"])
+        args = (f["q"][n:n + 1, :, hk:hk + 1], f["k"][n:n + 1, :, hk:hk + 1],
+                f["v"][n:n + 1, :, h:h + 1], f["g"][n:n + 1, :, h:h + 1],
+                f["beta"][n:n + 1, :, h:h + 1])
+        specs.append(("gdn_recurrent", args,
+                      dict(scale=inp["scale"], h0=f["h0"][n:n + 1, h:h + 1])))
+    return specs, dm
+
+
+def tiny_single_thread_s():
+    """Seconds the oracle takes on the tiny fp32 workload (B=1, T=128, K=V=32)
+    in this process, one thread."""
+    from gated_delta_rule_kk_gb300 import synth
+    from oracle import recurrence as R
+    inp = synth.tiny()
     t0 = time.perf_counter()
-    chains = 0
-    while True:
-        n, h = chains % dm["B"], (chains // dm["B"]) % dm["H"]
-        R.gdn_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
-                        h0=inp["h0"], heads=[h], seqs=[n])
-        chains += 1
-        el = time.perf_counter() - t0
-        if el >= target_s:
-            break
+    R.gdn_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"])
+    return time.perf_counter() - t0
+
+
+def oracle_sample(target_s):
+    """Time the fp64 oracle on whole (sequence, head) chains of the headline
+    workload, one chain per host core at a time, until about `target_s`
+    seconds have passed.  Returns (token-equivalents per second, seconds,
+    chains, cores)."""
+    from oracle import parallel
+    specs, dm = _headline_chain_specs()
+    cores = parallel.default_workers()
+    with parallel.ChainPool(cores) as pool:
+        pool.map(specs[:cores])  # start the workers (not timed)
+        t0 = time.perf_counter()
+        chains = 0
+        while True:
+            batch = [specs[(chains + j) % len(specs)] for j in range(cores)]
+            pool.map(batch)
+            chains += cores
+            el = time.perf_counter() - t0
+            if el >= target_s:
+                break
     # one chain is T tokens of one of H value heads: T / H token-equivalents
     tok = chains * dm["T"] / dm["H"]
-    return tok / el, el, chains
+    return tok / el, el, chains, cores
 
 
 def run_reference(args):
-    """The oracle on the host cores, as the reference arm."""
-    from gated_delta_rule_kk_gb300 import synth
-    from oracle import recurrence as R
-    inp = synth.gdn_prefill()
-    dm = inp["dims"]
+    """The oracle on the host cores, as the reference arm: each step runs one
+    whole (sequence, head) chain of the headline workload on every core."""
+    from oracle import parallel
+    specs, dm = _headline_chain_specs()
+    cores = parallel.default_workers()
     times = []
-    for i in range(args.warmup + args.steps):
-        n, h = i % dm["B"], (i // dm["B"]) % dm["H"]
-        t0 = time.perf_counter()
-        R.gdn_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
-                        h0=inp["h0"], heads=[h], seqs=[n])
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
-    tok = dm["T"] / dm["H"]
+    with parallel.ChainPool(cores) as pool:
+        pool.map(specs[:cores])  # start the workers (not timed)
+        for i in range(args.warmup + args.steps):
+            batch = [specs[(i * cores + j) % len(specs)] for j in range(cores)]
+            t0 = time.perf_counter()
+            pool.map(batch)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+    tok = cores * dm["T"] / dm["H"]
     value = tok / statistics.mean(times)
-    sample = (f"one whole (sequence, head) chain of the headline workload per step "
-              f"({dm['T']} tokens x 1 of {dm['H']} heads = {tok:.0f} token-equivalents)")
+    sample = (f"per step one whole (sequence, head) chain of the headline workload on each of "
+              f"{cores} host cores ({cores} x {dm['T']} tokens x 1 of {dm['H']} heads = "
+              f"{tok:.0f} token-equivalents), fp64 numpy token recurrence")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "global_batch": dm["B"],
                                         "seq_len": dm["T"], "parallelism": "host CPU"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample, "tiny_single_thread_s": tiny_single_thread_s()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -509,11 +543,13 @@ def main():
 
     result = run_ours(args, rank, world, dev)
     if rank == 0:
-        v, el, chains = oracle_sample(args.cpu_baseline_s)
+        v, el, chains, cores = oracle_sample(args.cpu_baseline_s)
         result["cpu_baseline"] = {
-            "value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{chains} whole (sequence, head) chains of the headline workload "
-                      f"({el:.1f} s, fp64 numpy token recurrence, one thread)"}
+            "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{chains} whole (sequence, head) chains of the headline workload, one "
+                      f"per core at a time on {cores} cores ({el:.1f} s, fp64 numpy token "
+                      f"recurrence)",
+            "tiny_single_thread_s": tiny_single_thread_s()}
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.barrier()

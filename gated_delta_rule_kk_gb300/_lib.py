@@ -42,7 +42,8 @@ class GdnChunkArgs(ctypes.Structure):
         ("o", c_void_p), ("cu_seqlens", c_void_p),
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("Hg", c_int32),
         ("K", c_int32), ("V", c_int32), ("N", c_int32),
-        ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("scale", c_float),
+        ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("state_v_first", c_int32),
+        ("scale", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -55,7 +56,8 @@ class KdaChunkArgs(ctypes.Structure):
         ("o", c_void_p), ("cu_seqlens", c_void_p),
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("HV", c_int32),
         ("K", c_int32), ("V", c_int32), ("N", c_int32),
-        ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("scale", c_float),
+        ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("state_v_first", c_int32),
+        ("scale", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -129,6 +131,7 @@ SIGNATURES = {
     "gdn_chunk_state_bwd": ([ctypes.POINTER(GdnStateBwdArgs), c_void_p], c_int32),
     "gdn_chunk_fwd_noalloc": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
     "gdn_noalloc_scratch_bytes": ([], c_size_t),
+    "gdn_self_test_wait": ([c_int32, c_int32, c_void_p], c_int32),
     "gdn_check_device_error": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),
     "gdn_status_string": ([c_int32], ctypes.c_char_p),
     "gdn_last_error_message": ([], ctypes.c_char_p),

@@ -48,7 +48,7 @@ def _io_dtype(q):
 
 
 def _chunk_common(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out,
-                  final_state, value_heads_name):
+                  final_state, value_heads_name, state_v_first=False):
     dev = q.device
     dt, dts = _io_dtype(q)
     _need(q, "q", dts, dev)
@@ -65,16 +65,17 @@ def _chunk_common(q, k, v, g, beta, initial_state, cu_seqlens, output_final_stat
         N = cu_seqlens.numel() - 1
     else:
         N = B
+    SK, SV = (V, K) if state_v_first else (K, V)
     if initial_state is not None:
         _need(initial_state, "initial_state", (torch.float32,), dev)
-        if tuple(initial_state.shape) != (N, Hv, K, V):
-            raise ValueError(f"initial_state must be [{N},{Hv},{K},{V}]")
+        if tuple(initial_state.shape) != (N, Hv, SK, SV):
+            raise ValueError(f"initial_state must be [{N},{Hv},{SK},{SV}]")
     if out is None:
         out = torch.empty((B, T, Hv, V), dtype=q.dtype, device=dev)
     else:
         _need(out, "out", dts, dev)
     if output_final_state and final_state is None:
-        final_state = torch.empty((N, Hv, K, V), dtype=torch.float32, device=dev)
+        final_state = torch.empty((N, Hv, SK, SV), dtype=torch.float32, device=dev)
     elif final_state is not None:
         _need(final_state, "final_state", (torch.float32,), dev)
     return dt, (B, T, Hk, Hv, K, V, N), out, final_state
@@ -99,18 +100,20 @@ def _attach_workspace(args, size_fn, workspace, device):
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, state_v_first=False):
     """GDN chunked forward.  Returns ``(o, ht)`` (``ht`` None if not requested).
 
     q, k [B,T,Hg,K]; v [B,T,H,V]; g, beta [B,T,H] float32; initial_state
-    [N,H,K,V] float32; cu_seqlens [N+1] int32 (then B == 1).
+    [N,H,K,V] float32 ([N,H,V,K] with ``state_v_first``, as ``ht``);
+    cu_seqlens [N+1] int32 (then B == 1).
     """
     dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
-        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H")
+        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H",
+        state_v_first)
     a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
-                     g_is_cumsum=int(bool(g_is_cumsum)),
+                     g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     ws = _attach_workspace(a, lambda lib: lib.gdn_chunk_workspace_size, workspace, q.device)
@@ -134,7 +137,7 @@ def _need_host(t, name, dtypes):
 
 def gdn_chunk_fwd_host(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                        output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
-                       workspace=None, stream=None, device=None):
+                       workspace=None, stream=None, device=None, state_v_first=False):
     """``gdn_chunk_fwd`` from and to host memory, copies included.
 
     Every tensor is a CPU tensor (pinned ones copy asynchronously and fastest);
@@ -157,22 +160,24 @@ def gdn_chunk_fwd_host(q, k, v, g, beta, scale=None, initial_state=None, cu_seql
     if cu_seqlens is not None:
         _need_host(cu_seqlens, "cu_seqlens", (torch.int32,))
         N = cu_seqlens.numel() - 1
+    SK, SV = (V, K) if state_v_first else (K, V)
     if initial_state is not None:
         _need_host(initial_state, "initial_state", (torch.float32,))
-        if tuple(initial_state.shape) != (N, H, K, V):
-            raise ValueError(f"initial_state must be [{N},{H},{K},{V}]")
+        if tuple(initial_state.shape) != (N, H, SK, SV):
+            raise ValueError(f"initial_state must be [{N},{H},{SK},{SV}]")
     if out is None:
         out = torch.empty((B, T, H, V), dtype=q.dtype, pin_memory=True)
     else:
         _need_host(out, "out", dts)
     if output_final_state and final_state is None:
-        final_state = torch.empty((N, H, K, V), dtype=torch.float32, pin_memory=True)
+        final_state = torch.empty((N, H, SK, SV), dtype=torch.float32, pin_memory=True)
     elif final_state is not None:
         _need_host(final_state, "final_state", (torch.float32,))
     a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(final_state), o=_ptr(out),
                      cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N,
                      chunk_size=CHUNK, g_is_cumsum=int(bool(g_is_cumsum)),
+                     state_v_first=int(bool(state_v_first)),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     lib = _lib.load()
@@ -213,7 +218,7 @@ def gdn_chunk_host_workspace_bytes(q, v, cu_seqlens=None, Hg=None):
 
 def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                           output_final_state=True, g_is_cumsum=False, out=None,
-                          final_state=None, stream=None):
+                          final_state=None, stream=None, state_v_first=False):
     """``gdn_chunk_fwd`` for callers that cannot allocate device memory.
 
     No workspace is requested or allocated: the library uses a fixed device
@@ -222,11 +227,12 @@ def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale=None, initial_state=None, cu_s
     allocated here only when ``out`` / ``final_state`` are not passed.
     """
     dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
-        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H")
+        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H",
+        state_v_first)
     a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
-                     g_is_cumsum=int(bool(g_is_cumsum)),
+                     g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     lib = _lib.load()
@@ -242,18 +248,20 @@ def gdn_noalloc_scratch_bytes():
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=True, out=None, final_state=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, state_v_first=False):
     """KDA chunked forward.  Returns ``(o, ht)``.
 
     q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV,K] float32 (chunk-local cumsum
-    when g_is_cumsum); beta [B,T,HV]; initial_state [N,HV,K,V] float32.
+    when g_is_cumsum); beta [B,T,HV]; initial_state [N,HV,K,V] float32
+    ([N,HV,V,K] with ``state_v_first``, as ``ht``).
     """
     dt, (B, T, H, HV, K, V, N), out, ht = _chunk_common(
-        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "HV")
+        q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "HV",
+        state_v_first)
     a = KdaChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, HV=HV, K=K, V=V, N=N, chunk_size=CHUNK,
-                     g_is_cumsum=int(bool(g_is_cumsum)),
+                     g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     ws = _attach_workspace(a, lambda lib: lib.kda_chunk_workspace_size, workspace, q.device)

@@ -92,7 +92,9 @@ __global__ void __launch_bounds__(THREADS, 1) chunk_fwd_simt_kernel(ChunkParams 
   for (int idx = tid; idx < K * VT; idx += THREADS) {
     const int c = idx / VT, j = idx % VT;
     float x = 0.f;
-    if (p.h0 && v0 + j < V) x = p.h0[(((size_t)n * H + h) * K + c) * V + v0 + j];
+    if (p.h0 && v0 + j < V)
+      x = p.v_first ? p.h0[(((size_t)n * H + h) * V + v0 + j) * K + c]
+                    : p.h0[(((size_t)n * H + h) * K + c) * V + v0 + j];
     hS[c * VS + j] = x;
   }
 
@@ -304,7 +306,10 @@ __global__ void __launch_bounds__(THREADS, 1) chunk_fwd_simt_kernel(ChunkParams 
   if (p.ht) {
     for (int idx = tid; idx < K * VT; idx += THREADS) {
       const int c = idx / VT, j = idx % VT;
-      if (v0 + j < V) p.ht[(((size_t)n * H + h) * K + c) * V + v0 + j] = hS[c * VS + j];
+      if (v0 + j >= V) continue;
+      const size_t at = p.v_first ? (((size_t)n * H + h) * V + v0 + j) * K + c
+                                  : (((size_t)n * H + h) * K + c) * V + v0 + j;
+      p.ht[at] = hS[c * VS + j];
     }
   }
 }

@@ -130,6 +130,7 @@ struct TcParams {
   int *err;
   int B, T, H, Hk, V, N, NT;  // NT: chunks per sequence without cu_seqlens
   int g_is_cumsum;
+  int v_first;             // h0, ht stored [V, K] per (sequence, head) instead of [K, V]
   float scale;
   uint32_t block;          // bytes per (chunk, head) block
 };
@@ -992,7 +993,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     const int r = qd * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     float hs[16];
-    if (p.h0) {
+    if (p.h0 && p.v_first) {
+      // [V, K]: the lanes of a warp read 32 consecutive keys of one value row
+      const float *src = p.h0 + ((size_t)n * p.H + h) * KD * p.V + (size_t)(v0 + c0) * KD + r;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hs[j] = src[(size_t)j * KD];
+    } else if (p.h0) {
       const float4 *src = reinterpret_cast<const float4 *>(
           p.h0 + (((size_t)n * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
@@ -1087,6 +1093,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     }
     if (!ok) {
       if (lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+    } else if (p.ht && *abort_flag == 0 && p.v_first) {
+      float *dst = p.ht + ((size_t)n * p.H + h) * KD * p.V + (size_t)(v0 + c0) * KD + r;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dst[(size_t)j * KD] = hs[j];
     } else if (p.ht && *abort_flag == 0) {
       float4 *dst = reinterpret_cast<float4 *>(p.ht + (((size_t)n * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
@@ -1187,6 +1197,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   p.B = cp.B; p.T = cp.T; p.H = cp.H; p.Hk = cp.Hk; p.V = cp.V; p.N = cp.N;
   p.NT = (cp.T + BT - 1) / BT;
   p.g_is_cumsum = cp.g_is_cumsum;
+  p.v_first = cp.v_first;
   p.scale = cp.scale;
   p.block = block_bytes(cp.V, kda);
   if (varlen) {

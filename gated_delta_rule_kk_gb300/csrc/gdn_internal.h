@@ -20,6 +20,7 @@ struct ChunkParams {
   int *err;
   int B, T, H, Hk, K, V, N;
   int g_is_cumsum;
+  int v_first;                // h0, ht as [V, K] instead of [K, V]
   float scale;
 };
 

@@ -26,6 +26,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gdn_internal.h"
 
 namespace {
@@ -35,7 +37,10 @@ constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
-void *g_scratch_ptr[MAX_DEVICES] = {nullptr};
+// Per-device address of the array, resolved once per device.  Host threads
+// may make their first call on a device at the same time: the slot is an
+// atomic, so concurrent first calls at worst both resolve the (same) address.
+std::atomic<void *> g_scratch_ptr[MAX_DEVICES];
 
 // Device address of the scratch array on the current device (set up once).
 void *scratch_address(gdn_status_t *st) {
@@ -45,17 +50,17 @@ void *scratch_address(gdn_status_t *st) {
     *st = GDN_ERR_CUDA;
     return nullptr;
   }
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
+  void *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       (void)cudaGetLastError();
       *st = GDN_ERR_CUDA;
       return nullptr;
     }
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
   }
   *st = GDN_OK;
-  return g_scratch_ptr[dev];
+  return p;
 }
 
 }  // namespace

@@ -77,6 +77,9 @@ typedef enum gdn_dtype {
  *   beta   [B, T, H]      float32
  *   h0     [N, H, K, V]   float32     initial state h = S^T, NULL = zeros
  *   ht     [N, H, K, V]   float32     final state, NULL = not returned
+ *   state_v_first = 1     h0 and ht hold every state transposed,
+ *                                     [N, H, V, K] (S itself; the chunk_h
+ *                                     page's state_v_first); 0 = [K, V]
  *   cu_seqlens [N + 1]    int32       NULL: N = B sequences of T tokens.
  *                                     Else B must be 1 and sequence n is
  *                                     tokens cu_seqlens[n] .. cu_seqlens[n+1]
@@ -104,6 +107,7 @@ typedef struct gdn_chunk_args {
   int32_t B, T, H, Hg, K, V, N;
   int32_t chunk_size;
   int32_t g_is_cumsum;
+  int32_t state_v_first;       /* 1: h0, ht are [N, H, V, K] instead of [N, H, K, V] */
   float scale;
   void *workspace;
   size_t workspace_bytes;
@@ -267,7 +271,8 @@ gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *b
  *                                     g_is_cumsum = 1 (as that kernel takes
  *                                     it), raw per-token log-gates when 0
  *   beta   [B, T, HV]     float32
- *   h0, ht [N, HV, K, V]  float32     as for GDN
+ *   h0, ht [N, HV, K, V]  float32     as for GDN ([N, HV, V, K] with
+ *                                     state_v_first = 1)
  *   cu_seqlens            as for GDN
  * Limits: 1 <= K <= 128, V >= 1, chunk_size == 64, HV % H == 0, N and HV at
  * most 65535.  With T == 0
@@ -286,6 +291,7 @@ typedef struct kda_chunk_args {
   int32_t B, T, H, HV, K, V, N;
   int32_t chunk_size;
   int32_t g_is_cumsum;
+  int32_t state_v_first;       /* 1: h0, ht are [N, HV, V, K] instead of [N, HV, K, V] */
   float scale;
   void *workspace;
   size_t workspace_bytes;
@@ -354,6 +360,22 @@ gdn_status_t gdn_chunk_fwd_noalloc(const gdn_chunk_args *args, gdn_stream_t stre
 
 /* Size in bytes of the fixed scratch array used by gdn_chunk_fwd_noalloc. */
 size_t gdn_noalloc_scratch_bytes(void);
+
+/*
+ * Self-test of the failure path shared by every kernel that waits on an
+ * asynchronous copy or tensor-core operation: each such wait polls an
+ * mbarrier a bounded number of times and, if the phase has not completed by
+ * then, records GDN_ERR_TIMEOUT in the device error word and lets the kernel
+ * finish instead of hanging.  This call runs that same wait once, in a
+ * one-thread kernel, on a barrier of its own: with arrive = 0 nothing ever
+ * arrives, so the wait gives up after max_polls polls (1 .. 2^22; the kernels
+ * use 2^22) and GDN_ERR_TIMEOUT is recorded; with arrive = 1 the kernel
+ * completes the phase itself first and nothing is recorded.  No copy or
+ * tensor-core operation is in flight, so giving up leaves nothing behind.
+ * Read the outcome with gdn_check_device_error().  GDN_ERR_INVALID_ARG for
+ * arguments outside those ranges.
+ */
+gdn_status_t gdn_self_test_wait(int32_t arrive, int32_t max_polls, gdn_stream_t stream);
 
 /* Wait for `stream`, then read and clear the device error word of the current
  * device into *code (a gdn_status_t value, GDN_OK if nothing was recorded).

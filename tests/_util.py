@@ -2,18 +2,21 @@
 
 Tolerance: max |gpu - oracle| <= TOL * RMS(oracle), separately for o and for
 the state, with TOL = 1e-4 for fp32 inputs and 2e-2 for bf16 inputs with fp32
-accumulation.  A result that the method stores in bf16 (o for bf16 inputs,
-the decode state pool) cannot be closer to the exact value than half a bf16
-unit in the last place, so for those results that storage rounding,
-2^(floor(log2 |x|) - 8) per element, is taken off each element's error before
-the bound is applied.  fp32 results (the prefill final state) get no such
-allowance.
+accumulation.  The bound is applied to the raw element-wise error, storage
+rounding included.  As a diagnostic only, each check also computes the error
+left once every bf16-stored element's own storage rounding (half a bf16 unit
+in the last place) is taken off; both figures are recorded and printed in the
+session summary (tests/conftest.py), the bound never uses the second one.
 """
 import numpy as np
 import torch
 
 TOL_F32 = 1e-4
 TOL_BF16 = 2e-2
+
+# (test id, what, raw error / RMS, storage-adjusted error / RMS, tolerance)
+RECORDS = []
+CURRENT_TEST = [""]
 
 
 def _np(x):
@@ -29,27 +32,43 @@ def bf16_half_ulp(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def rel_max_err(got, ref, bf16_out=None):
-    """max over elements of (|got - ref| - storage rounding) / RMS(ref)."""
+def _rms(r):
+    return float(np.sqrt(np.mean(r * r))) if r.size else 0.0
+
+
+def rel_max_err(got, ref):
+    """max over elements of |got - ref| / RMS(ref): the bound's quantity."""
     g = _np(got)
     r = np.asarray(ref, dtype=np.float64)
-    if bf16_out is None:
-        bf16_out = hasattr(got, "dtype") and got.dtype == torch.bfloat16
+    if not g.size:
+        return 0.0
+    err = float(np.max(np.abs(g - r)))
+    rms = _rms(r)
+    return err / rms if rms > 0.0 else err
+
+
+def storage_adjusted_err(got, ref):
+    """Diagnostic: the error left once each bf16 element's storage rounding is
+    taken off (a bf16 number cannot be closer to the exact value than that)."""
+    g = _np(got)
+    r = np.asarray(ref, dtype=np.float64)
+    if not g.size:
+        return 0.0
     err = np.abs(g - r)
-    if bf16_out:
+    if hasattr(got, "dtype") and got.dtype == torch.bfloat16:
         err = np.maximum(err - bf16_half_ulp(np.maximum(np.abs(g), np.abs(r))), 0.0)
-    rms = float(np.sqrt(np.mean(r * r)))
-    if rms == 0.0:
-        return float(np.max(err)) if err.size else 0.0
-    return float(np.max(err) / rms) if err.size else 0.0
+    rms = _rms(r)
+    return float(np.max(err)) / rms if rms > 0.0 else float(np.max(err))
 
 
 def assert_close(got, ref, tol, what):
-    e = rel_max_err(got, ref)
-    raw = rel_max_err(got, ref, bf16_out=False)
-    assert np.isfinite(e) and e <= tol, (
-        f"{what}: error {e:.3e} x RMS exceeds {tol:.1e} (raw max-abs {raw:.3e} x RMS)")
-    return e
+    raw = rel_max_err(got, ref)
+    adj = storage_adjusted_err(got, ref)
+    RECORDS.append((CURRENT_TEST[0], what, raw, adj, tol))
+    assert np.isfinite(raw) and raw <= tol, (
+        f"{what}: max-abs error {raw:.3e} x RMS exceeds {tol:.1e} "
+        f"(storage-adjusted diagnostic {adj:.3e})")
+    return raw
 
 
 def to_dev(inp, device="cuda"):

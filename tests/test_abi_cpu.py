@@ -313,3 +313,20 @@ def test_state_pass_binding_rejects_bad_split_before_any_call():
             gdn.gdn_chunk_state_fwd(k, v, split_size=bad)
         with pytest.raises(ValueError, match="multiple of 64"):
             gdn.gdn_chunk_state_bwd(k, v, split_size=bad)
+
+
+def test_self_test_wait_rejects_bad_arguments(lib):
+    for arrive, polls in ((2, 1), (0, 0), (0, -5), (1, (1 << 22) + 1)):
+        assert lib.gdn_self_test_wait(arrive, polls, None) == Status.INVALID_ARG
+
+
+def test_chunk_state_v_first_flag_is_checked(lib):
+    for cls, fn in ((GdnChunkArgs, "gdn_chunk_fwd"), (KdaChunkArgs, "kda_chunk_fwd")):
+        a = cls(dtype=1, q=0x10000, k=0x10000, v=0x10000, g=0x10000, beta=0x10000, o=0x10000,
+                B=1, T=64, K=128, V=128, N=1, chunk_size=64, state_v_first=2)
+        if cls is GdnChunkArgs:
+            a.H, a.Hg = 1, 1
+        else:
+            a.H, a.HV = 1, 1
+        assert getattr(lib, fn)(ctypes.byref(a), None) == Status.INVALID_ARG
+        assert b"state_v_first" in lib.gdn_last_error_message()

@@ -7,6 +7,7 @@ from gated_delta_rule_kk_gb300 import Status, gdn_check_device_error, gdn_decode
 from gated_delta_rule_kk_gb300 import synth
 from oracle import recurrence as R
 
+from _fullsize import decode_all_entries
 from _util import TOL_BF16, assert_close, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -104,15 +105,15 @@ def test_chained_single_token_calls():
     assert_close(st, ref_state.double().numpy(), TOL_BF16, "chained state")
 
 
-@pytest.mark.parametrize("T", [1, 2, 4])
-def test_decode_workload_sampled(T):
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_decode_workload_all_entries(T):
+    """B=pool=256, H=16, HV=32, K=V=128: all 8192 (batch entry, value head) states."""
     inp = synth.decode(T)
     o, state = run_gpu(inp)
     assert gdn_check_device_error() == Status.OK
-    sample = [0, 1, 77, 128, 200, 255]
-    o_ref, st_ref = oracle_for(inp, sample)
-    assert_close(o[sample], o_ref, TOL_BF16, "o")
-    assert_close(state[sample], st_ref, TOL_BF16, "state")
+    o_ref, st_ref = decode_all_entries(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(state, st_ref, TOL_BF16, "state")
 
 
 @pytest.mark.parametrize("T", [2, 4])

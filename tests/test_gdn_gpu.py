@@ -7,6 +7,7 @@ from gated_delta_rule_kk_gb300 import Status, gdn_check_device_error, gdn_chunk_
 from gated_delta_rule_kk_gb300 import synth
 from oracle import recurrence as R
 
+from _fullsize import prefill_all_chains
 from _util import TOL_BF16, TOL_F32, assert_close, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -118,27 +119,67 @@ def test_bad_cu_seqlens_reported_on_device():
     assert gdn_check_device_error() == Status.OK  # reading clears it
 
 
-# ---- the named workloads at full size, oracle on sampled chains -------------
+# ---- the named workloads at full size, every chain against the oracle ------
 
-def test_gdn_prefill_workload_sampled():
+def test_gdn_prefill_workload_all_chains():
+    """B=2, T=4096, H=Hg=16, K=V=128, bf16: all 32 (sequence, head) chains."""
     inp = synth.gdn_prefill()
     o, ht = run_gpu(inp)
-    for n, h in ((0, 0), (1, 9), (1, 15)):
-        o_ref, ht_ref = run_oracle(inp, heads=[h], seqs=[n])
-        assert_close(o[n, :, h], o_ref[n, :, h], TOL_BF16, f"o seq {n} head {h}")
-        assert_close(ht[n, h], ht_ref[n, h], TOL_BF16, f"ht seq {n} head {h}")
+    o_ref, ht_ref = prefill_all_chains(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
 
 
-def test_varlen_gqa_workload_sampled():
+def test_varlen_gqa_workload_all_chains():
+    """8 packed sequences (32,068 tokens), Hg=4 key heads for H=16 value heads:
+    all 128 (sequence, head) chains."""
     inp = synth.varlen_gqa()
     o, ht = run_gpu(inp)
-    cu = inp["cu_seqlens"].numpy()
-    longest = int(np.argmax(np.diff(cu)))
-    for n, h in ((longest, 5), (0, 0), (7, 15)):
-        o_ref, ht_ref = run_oracle(inp, heads=[h], seqs=[n])
-        s, e = cu[n], cu[n + 1]
-        assert_close(o[0, s:e, h], o_ref[0, s:e, h], TOL_BF16, f"o seq {n} head {h}")
-        assert_close(ht[n, h], ht_ref[n, h], TOL_BF16, f"ht seq {n} head {h}")
+    o_ref, ht_ref = prefill_all_chains(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
+
+
+# ---- gates the synthetic workloads never reach, on the tensor-core path ----
+
+def _tc_problem(seed, T=256, H=2, Hg=1):
+    return synth.prefill_inputs(seed, 1, T, H, Hg, 128, 128, dtype=torch.bfloat16, h0_std=0.1)
+
+
+def _check(inp):
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
+
+
+def test_strong_gates_inside_a_chunk_take_the_exact_exponentials():
+    """A chunk whose cumulative gate falls below -80 (tokens 64..127 at -2.5
+    each) is gated with exact per-element exponentials; its neighbours keep
+    the split form.  Head 1 is strong in the tail chunk instead."""
+    inp = _tc_problem(51, T=230)
+    g = inp["g"].clone()
+    g[:, 64:128, 0] = -2.5
+    g[:, 192:, 1] = -3.0
+    _check(dict(inp, g=g))
+
+
+def test_positive_log_gates():
+    """Log-gates above zero (a growing state), mixed with negative ones."""
+    inp = _tc_problem(52, T=200)
+    r = torch.Generator().manual_seed(7)
+    g = 0.02 + 0.05 * torch.randn(inp["g"].shape, generator=r)
+    _check(dict(inp, g=g.float()))
+
+
+def test_gate_reset_mid_chunk_and_at_a_chunk_start():
+    """g = -1000 (exp underflows to exactly zero in fp32) wipes the state: at a
+    token inside a chunk for head 0 and at a chunk's first token for head 1."""
+    inp = _tc_problem(53, T=200)
+    g = inp["g"].clone()
+    g[:, 90, 0] = -1000.0
+    g[:, 128, 1] = -1000.0
+    _check(dict(inp, g=g))
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -164,3 +205,50 @@ def test_zero_length_batch_returns_the_initial_state(dtype):
     torch.cuda.synchronize()
     assert tuple(o_h.shape) == (B, 0, H, V)
     assert torch.equal(ht_h, h0.cpu())
+
+
+# ---- state_v_first: h0 / ht as [V, K] (the chunk_h page's layout flag) -----
+
+@pytest.mark.parametrize("dtype,K,V,lengths", [
+    (torch.bfloat16, 128, 128, None),       # tensor cores
+    (torch.bfloat16, 128, 64, [70, 0, 130]),  # tensor cores, packed, an empty sequence
+    (torch.float32, 64, 48, [1, 0, 99]),     # exact fp32 kernel
+])
+def test_state_v_first_layout(dtype, K, V, lengths):
+    T = 150 if lengths is None else sum(lengths)
+    B = 2 if lengths is None else 1
+    inp = synth.prefill_inputs(81, B, T, 4, 2, K, V, dtype=dtype, h0_std=0.1, lengths=lengths)
+    d = to_dev(inp)
+    kw = dict(scale=d["scale"], cu_seqlens=d["cu_seqlens"])
+    o1, ht1 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"], **kw)
+    h0t = d["h0"].transpose(-1, -2).contiguous()
+    o2, ht2 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=h0t,
+                            state_v_first=True, **kw)
+    assert gdn_check_device_error() == Status.OK
+    assert tuple(ht2.shape) == tuple(h0t.shape)
+    # the layout changes where states live, not the arithmetic
+    assert torch.equal(o1, o2)
+    assert torch.equal(ht2, ht1.transpose(-1, -2))
+    o_ref, ht_ref = run_oracle(inp)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert_close(o2, o_ref, tol, "o")
+    assert_close(ht2.transpose(-1, -2), ht_ref, tol, "ht")
+    if lengths is not None:
+        for n in (i for i, x in enumerate(lengths) if x == 0):
+            assert torch.equal(ht2[n], h0t[n])
+
+
+def test_state_v_first_host_entry_point():
+    import gated_delta_rule_kk_gb300 as gdn
+    inp = synth.prefill_inputs(82, 1, 1000, 2, 1, 128, 128, h0_std=0.1)
+    d = to_dev(inp)
+    h0t = inp["h0"].transpose(-1, -2).contiguous()
+    o1, ht1 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                            initial_state=h0t.cuda(), state_v_first=True)
+    o2, ht2 = gdn.gdn_chunk_fwd_host(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     scale=inp["scale"], initial_state=h0t.pin_memory(),
+                                     state_v_first=True)
+    torch.cuda.synchronize()
+    assert gdn_check_device_error() == Status.OK
+    assert torch.equal(o2, o1.cpu())
+    assert torch.equal(ht2, ht1.cpu())

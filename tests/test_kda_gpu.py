@@ -6,6 +6,7 @@ from gated_delta_rule_kk_gb300 import Status, gdn_check_device_error, gdn_chunk_
 from gated_delta_rule_kk_gb300 import synth
 from oracle import recurrence as R
 
+from _fullsize import prefill_all_chains
 from _util import TOL_BF16, TOL_F32, assert_close, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -77,13 +78,58 @@ def test_channel_constant_gate_equals_gdn():
     assert_close(ht2, ht1.cpu().double().numpy(), 1e-5, "ht")
 
 
-def test_kda_prefill_workload_sampled():
+def test_kda_prefill_workload_all_heads():
+    """B=1, T=8192, H=HV=32, K=V=128, bf16, chunk-local cumsum gate: all 32 heads."""
     inp = synth.kda_prefill()
     o, ht = run_gpu(inp)
-    for h in (0, 17, 31):
-        o_ref, ht_ref = run_oracle(inp, heads=[h], seqs=[0])
-        assert_close(o[0, :, h], o_ref[0, :, h], TOL_BF16, f"o head {h}")
-        assert_close(ht[0, h], ht_ref[0, h], TOL_BF16, f"ht head {h}")
+    o_ref, ht_ref = prefill_all_chains(inp, kda=True)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
+
+
+# ---- per-channel gates the synthetic workload never reaches (tensor cores) --
+
+def _raw_problem(seed, T=200):
+    inp = synth.prefill_inputs(seed, 1, T, 2, 1, 128, 128, dtype=torch.bfloat16, h0_std=0.1,
+                               per_channel=True)
+    # hand the gates over raw so the edits below are per-token rates
+    r = torch.Generator().manual_seed(seed)
+    g = -torch.rand(inp["g"].shape, generator=r) * 0.05
+    return dict(inp, g=g, g_is_cumsum=False)
+
+
+def _check(inp):
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
+
+
+def test_strong_channel_gates_take_the_exact_exponentials():
+    """Channels 0..15 of head 0 fall below -80 inside chunk 1 (-2.5 per token):
+    that chunk is gated with exact per-element exponentials."""
+    inp = _raw_problem(61)
+    g = inp["g"].clone()
+    g[:, 64:128, 0, :16] = -2.5
+    g[:, 128:, 1, 100:] = -4.0
+    _check(dict(inp, g=g))
+
+
+def test_positive_channel_gates():
+    inp = _raw_problem(62)
+    r = torch.Generator().manual_seed(8)
+    g = 0.02 + 0.05 * torch.randn(inp["g"].shape, generator=r)
+    _check(dict(inp, g=g.float()))
+
+
+def test_channel_gate_reset():
+    """A -1000 rate zeroes the decay: every channel of head 0 at token 90, and
+    half the channels of head 1 at a chunk's first token (128)."""
+    inp = _raw_problem(63)
+    g = inp["g"].clone()
+    g[:, 90, 0, :] = -1000.0
+    g[:, 128, 1, :64] = -1000.0
+    _check(dict(inp, g=g))
 
 
 def test_zero_length_batch_returns_the_initial_state():
@@ -98,3 +144,20 @@ def test_zero_length_batch_returns_the_initial_state():
     assert gdn_check_device_error() == Status.OK
     assert tuple(o.shape) == (B, 0, H, V)
     assert torch.equal(ht, h0)
+
+
+@pytest.mark.parametrize("dtype,K", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_state_v_first_layout(dtype, K):
+    inp = synth.prefill_inputs(83, 1, 140, 4, 2, K, 64, dtype=dtype, h0_std=0.1,
+                               per_channel=True)
+    d = to_dev(inp)
+    o1, ht1 = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"])
+    h0t = d["h0"].transpose(-1, -2).contiguous()
+    o2, ht2 = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=h0t,
+                            state_v_first=True)
+    assert gdn_check_device_error() == Status.OK
+    assert torch.equal(o1, o2)
+    assert torch.equal(ht2, ht1.transpose(-1, -2))
+    o_ref, ht_ref = run_oracle(inp)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert_close(ht2.transpose(-1, -2), ht_ref, tol, "ht")

@@ -265,3 +265,102 @@ def test_l2_normalize_eps_inside_root():
     x = np.array([3.0, 4.0])
     np.testing.assert_allclose(R.l2_normalize(x, eps=0.0), [0.6, 0.8], atol=1e-16)
     np.testing.assert_allclose(R.l2_normalize(x, eps=11.0), [0.5, 2.0 / 3.0], atol=1e-16)
+
+
+# ---------------------------------------------------------------- gate given as a chunk-local cumsum
+
+def _chunk_cumsum_by_hand(g_raw, cu, chunk):
+    """Inclusive running sums of the raw gates, restarted at every chunk of
+    `chunk` tokens counted from each sequence's first token (token axis 1)."""
+    out = np.zeros_like(g_raw)
+    for n in range(len(cu) - 1):
+        acc = None
+        for t in range(cu[n], cu[n + 1]):
+            if (t - cu[n]) % chunk == 0:
+                acc = np.zeros_like(g_raw[:, t])
+            acc = acc + g_raw[:, t]
+            out[:, t] = acc
+    return out
+
+
+@pytest.mark.parametrize("chunk", [64, 4])
+def test_kda_cumsum_gate_input_equals_raw_and_transition_product(chunk):
+    """kda_recurrent's default input form: per-channel gates as chunk-local
+    cumulative sums.  Packed sequences whose starts are not chunk-aligned
+    (70, 71) and that span several chunks; grouped value heads; K != V."""
+    rng = np.random.default_rng(21)
+    lengths = [70, 1, 130]
+    T = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    H, HV, K, V = 1, 2, 3, 2
+    q, k, v, g_raw, beta, _ = _rand_problem(rng, 1, T, H, HV, K, V, per_channel=True,
+                                            with_h0=False, gate_scale=0.2)
+    h0 = rng.standard_normal((3, HV, K, V))
+    g_cum = _chunk_cumsum_by_hand(g_raw, cu, chunk)
+    o1, ht1 = R.kda_recurrent(q, k, v, g_cum, beta, scale=0.6, h0=h0, cu_seqlens=cu,
+                              g_is_cumsum=True, chunk_size=chunk)
+    o2, ht2 = R.kda_recurrent(q, k, v, g_raw, beta, scale=0.6, h0=h0, cu_seqlens=cu,
+                              g_is_cumsum=False)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(ht1, ht2, atol=1e-12)
+    for n in range(3):
+        s, e = cu[n], cu[n + 1]
+        for hv in range(HV):
+            hk = hv // (HV // H)
+            ob, Sb = brute.chain_outputs(h0[n, hv].T, g_raw[0, s:e, hv, :], beta[0, s:e, hv],
+                                         q[0, s:e, hk], k[0, s:e, hk], v[0, s:e, hv], 0.6)
+            np.testing.assert_allclose(o1[0, s:e, hv], ob, rtol=1e-10, atol=1e-10)
+            np.testing.assert_allclose(ht1[n, hv], Sb.T, rtol=1e-10, atol=1e-10)
+
+
+def test_kda_cumsum_gate_reset_counts_chunks_from_each_sequence_start():
+    """Counting chunks from the packed row's first token instead (a plausible
+    slip) changes the result whenever a sequence starts off a chunk boundary."""
+    rng = np.random.default_rng(22)
+    lengths = [5, 9]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    q, k, v, g_raw, beta, _ = _rand_problem(rng, 1, 14, 1, 1, 2, 2, per_channel=True,
+                                            with_h0=False)
+    right = _chunk_cumsum_by_hand(g_raw, cu, 4)
+    wrong = _chunk_cumsum_by_hand(g_raw, np.array([0, 14]), 4)
+    o_r, _ = R.kda_recurrent(q, k, v, right, beta, scale=1.0, cu_seqlens=cu, chunk_size=4)
+    o_w, _ = R.kda_recurrent(q, k, v, wrong, beta, scale=1.0, cu_seqlens=cu, chunk_size=4)
+    o_raw, _ = R.kda_recurrent(q, k, v, g_raw, beta, scale=1.0, cu_seqlens=cu, g_is_cumsum=False)
+    np.testing.assert_allclose(o_r, o_raw, atol=1e-12)
+    assert np.max(np.abs(o_w - o_raw)) > 1e-3
+
+
+# ---------------------------------------------------------------- decode without the L2 norm
+
+def test_decode_without_l2norm_matches_transition_product():
+    """use_qk_l2norm = 0: q and k enter as given (q times scale), so the state
+    and outputs are the product of the transitions with the raw keys."""
+    rng = np.random.default_rng(23)
+    B, T, H, HV, K, V = 2, 3, 1, 2, 4, 3
+    q = rng.standard_normal((B, T, H, K)) * 0.4
+    k = rng.standard_normal((B, T, H, K)) * 0.4     # not unit length
+    v = rng.standard_normal((B, T, HV, V))
+    a = rng.standard_normal((B, T, HV))
+    b = rng.standard_normal((B, T, HV))
+    A_log = rng.standard_normal(HV)
+    dt = rng.standard_normal(HV)
+    state = rng.standard_normal((3, HV, V, K))
+    slots = np.array([1, 2])
+    o, ns = R.gdn_decode(q, k, v, a, b, A_log, dt, state, slots, scale=0.3, use_qk_l2norm=False)
+    g, beta = R.decode_gates(a, b, A_log, dt)
+    for bi in range(B):
+        for hv in range(HV):
+            hk = hv // (HV // H)
+            ob, Sb = brute.chain_outputs(state[slots[bi], hv], g[bi, :, hv], beta[bi, :, hv],
+                                         q[bi, :, hk], k[bi, :, hk], v[bi, :, hv], 0.3)
+            np.testing.assert_allclose(o[bi, :, hv], ob, rtol=1e-11, atol=1e-11)
+            np.testing.assert_allclose(ns[bi, hv], Sb, rtol=1e-11, atol=1e-11)
+    # and with the norm on, the same product on the normalised keys and queries
+    o_n, ns_n = R.gdn_decode(q, k, v, a, b, A_log, dt, state, slots, scale=0.3)
+    assert np.max(np.abs(o_n - o)) > 1e-3
+    kn = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + 1e-6)
+    qn = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + 1e-6)
+    ob, Sb = brute.chain_outputs(state[slots[0], 0], g[0, :, 0], beta[0, :, 0], qn[0, :, 0],
+                                 kn[0, :, 0], v[0, :, 0], 0.3)
+    np.testing.assert_allclose(o_n[0, :, 0], ob, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(ns_n[0, 0], Sb, rtol=1e-11, atol=1e-11)
