@@ -43,7 +43,7 @@ class GdnChunkArgs(ctypes.Structure):
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("Hg", c_int32),
         ("K", c_int32), ("V", c_int32), ("N", c_int32),
         ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("state_v_first", c_int32),
-        ("scale", c_float),
+        ("o_fp32", c_int32), ("scale", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -57,7 +57,7 @@ class KdaChunkArgs(ctypes.Structure):
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("HV", c_int32),
         ("K", c_int32), ("V", c_int32), ("N", c_int32),
         ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("state_v_first", c_int32),
-        ("scale", c_float),
+        ("o_fp32", c_int32), ("scale", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -68,9 +68,10 @@ class GdnDecodeArgs(ctypes.Structure):
         ("a", c_void_p), ("b", c_void_p),
         ("A_log", c_void_p), ("dt_bias", c_void_p),
         ("state", c_void_p), ("slot_indices", c_void_p), ("o", c_void_p),
+        ("new_state_f32", c_void_p),
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("HV", c_int32),
         ("K", c_int32), ("V", c_int32), ("pool", c_int32),
-        ("use_qk_l2norm", c_int32),
+        ("use_qk_l2norm", c_int32), ("o_fp32", c_int32),
         ("scale", c_float), ("softplus_beta", c_float), ("softplus_threshold", c_float),
         ("eps", c_float),
     ]

@@ -47,8 +47,17 @@ def _io_dtype(q):
     raise ValueError(f"q/k/v must be float32 or bfloat16, got {q.dtype}")
 
 
+def _out_fp32(q, out_dtype):
+    """Whether o is written as float32: out_dtype None means q's dtype."""
+    if out_dtype is None or out_dtype == q.dtype:
+        return q.dtype == torch.float32
+    if out_dtype == torch.float32:
+        return True
+    raise ValueError(f"out_dtype must be None, {q.dtype} or torch.float32")
+
+
 def _chunk_common(q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out,
-                  final_state, value_heads_name, state_v_first=False):
+                  final_state, value_heads_name, state_v_first=False, out_dtype=None):
     dev = q.device
     dt, dts = _io_dtype(q)
     _need(q, "q", dts, dev)
@@ -70,10 +79,11 @@ def _chunk_common(q, k, v, g, beta, initial_state, cu_seqlens, output_final_stat
         _need(initial_state, "initial_state", (torch.float32,), dev)
         if tuple(initial_state.shape) != (N, Hv, SK, SV):
             raise ValueError(f"initial_state must be [{N},{Hv},{SK},{SV}]")
+    odt = torch.float32 if _out_fp32(q, out_dtype) else q.dtype
     if out is None:
-        out = torch.empty((B, T, Hv, V), dtype=q.dtype, device=dev)
+        out = torch.empty((B, T, Hv, V), dtype=odt, device=dev)
     else:
-        _need(out, "out", dts, dev)
+        _need(out, "out", (odt,), dev)
     if output_final_state and final_state is None:
         final_state = torch.empty((N, Hv, SK, SV), dtype=torch.float32, device=dev)
     elif final_state is not None:
@@ -100,20 +110,22 @@ def _attach_workspace(args, size_fn, workspace, device):
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
-                  workspace=None, stream=None, state_v_first=False):
+                  workspace=None, stream=None, state_v_first=False, out_dtype=None):
     """GDN chunked forward.  Returns ``(o, ht)`` (``ht`` None if not requested).
 
     q, k [B,T,Hg,K]; v [B,T,H,V]; g, beta [B,T,H] float32; initial_state
     [N,H,K,V] float32 ([N,H,V,K] with ``state_v_first``, as ``ht``);
-    cu_seqlens [N+1] int32 (then B == 1).
+    cu_seqlens [N+1] int32 (then B == 1).  ``out_dtype=torch.float32`` writes
+    o in float32 (the value a bf16 o is the round-to-nearest-even of).
     """
     dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
         q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H",
-        state_v_first)
+        state_v_first, out_dtype)
     a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
                      g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
+                     o_fp32=int(out.dtype == torch.float32),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     ws = _attach_workspace(a, lambda lib: lib.gdn_chunk_workspace_size, workspace, q.device)
@@ -137,7 +149,8 @@ def _need_host(t, name, dtypes):
 
 def gdn_chunk_fwd_host(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                        output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
-                       workspace=None, stream=None, device=None, state_v_first=False):
+                       workspace=None, stream=None, device=None, state_v_first=False,
+                       out_dtype=None):
     """``gdn_chunk_fwd`` from and to host memory, copies included.
 
     Every tensor is a CPU tensor (pinned ones copy asynchronously and fastest);
@@ -165,10 +178,11 @@ def gdn_chunk_fwd_host(q, k, v, g, beta, scale=None, initial_state=None, cu_seql
         _need_host(initial_state, "initial_state", (torch.float32,))
         if tuple(initial_state.shape) != (N, H, SK, SV):
             raise ValueError(f"initial_state must be [{N},{H},{SK},{SV}]")
+    odt = torch.float32 if _out_fp32(q, out_dtype) else q.dtype
     if out is None:
-        out = torch.empty((B, T, H, V), dtype=q.dtype, pin_memory=True)
+        out = torch.empty((B, T, H, V), dtype=odt, pin_memory=True)
     else:
-        _need_host(out, "out", dts)
+        _need_host(out, "out", (odt,))
     if output_final_state and final_state is None:
         final_state = torch.empty((N, H, SK, SV), dtype=torch.float32, pin_memory=True)
     elif final_state is not None:
@@ -177,7 +191,7 @@ def gdn_chunk_fwd_host(q, k, v, g, beta, scale=None, initial_state=None, cu_seql
                      h0=_ptr(initial_state), ht=_ptr(final_state), o=_ptr(out),
                      cu_seqlens=_ptr(cu_seqlens), B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N,
                      chunk_size=CHUNK, g_is_cumsum=int(bool(g_is_cumsum)),
-                     state_v_first=int(bool(state_v_first)),
+                     state_v_first=int(bool(state_v_first)), o_fp32=int(odt == torch.float32),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     lib = _lib.load()
@@ -218,7 +232,7 @@ def gdn_chunk_host_workspace_bytes(q, v, cu_seqlens=None, Hg=None):
 
 def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                           output_final_state=True, g_is_cumsum=False, out=None,
-                          final_state=None, stream=None, state_v_first=False):
+                          final_state=None, stream=None, state_v_first=False, out_dtype=None):
     """``gdn_chunk_fwd`` for callers that cannot allocate device memory.
 
     No workspace is requested or allocated: the library uses a fixed device
@@ -228,12 +242,12 @@ def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale=None, initial_state=None, cu_s
     """
     dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
         q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H",
-        state_v_first)
+        state_v_first, out_dtype)
     a = GdnChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
                      g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
-                     scale=float(scale) if scale is not None else 0.0,
+                     o_fp32=int(out.dtype == torch.float32), scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     lib = _lib.load()
     _lib.check(lib.gdn_chunk_fwd_noalloc(ctypes.byref(a), _stream(stream)),
@@ -248,7 +262,7 @@ def gdn_noalloc_scratch_bytes():
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=True, out=None, final_state=None,
-                  workspace=None, stream=None, state_v_first=False):
+                  workspace=None, stream=None, state_v_first=False, out_dtype=None):
     """KDA chunked forward.  Returns ``(o, ht)``.
 
     q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV,K] float32 (chunk-local cumsum
@@ -257,11 +271,12 @@ def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     """
     dt, (B, T, H, HV, K, V, N), out, ht = _chunk_common(
         q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "HV",
-        state_v_first)
+        state_v_first, out_dtype)
     a = KdaChunkArgs(dtype=int(dt), q=_ptr(q), k=_ptr(k), v=_ptr(v), g=_ptr(g), beta=_ptr(beta),
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, HV=HV, K=K, V=V, N=N, chunk_size=CHUNK,
                      g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
+                     o_fp32=int(out.dtype == torch.float32),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     ws = _attach_workspace(a, lambda lib: lib.kda_chunk_workspace_size, workspace, q.device)
@@ -273,8 +288,13 @@ def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
 
 def gdn_decode(q, k, v, a, b, A_log, dt_bias, state, slot_indices=None, scale=None,
                softplus_beta=1.0, softplus_threshold=20.0, eps=1e-6, use_qk_l2norm=True,
-               out=None, stream=None):
-    """Decode T = 1..4 tokens; ``state`` [pool,HV,V,K] bf16 is updated in place.  Returns o."""
+               out=None, stream=None, out_dtype=None, new_state_f32=None):
+    """Decode T = 1..4 tokens; ``state`` [pool,HV,V,K] bf16 is updated in place.  Returns o.
+
+    ``out_dtype=torch.float32`` writes o in float32; ``new_state_f32`` (a
+    [B,HV,V,K] float32 tensor) receives each entry's updated state before its
+    rounding into the bf16 pool.
+    """
     dev = q.device
     bf = (torch.bfloat16,)
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (a, "a"), (b, "b"), (state, "state")):
@@ -286,15 +306,22 @@ def gdn_decode(q, k, v, a, b, A_log, dt_bias, state, slot_indices=None, scale=No
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     pool = state.shape[0]
+    odt = torch.float32 if _out_fp32(q, out_dtype) else torch.bfloat16
     if out is None:
-        out = torch.empty((B, T, HV, V), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((B, T, HV, V), dtype=odt, device=dev)
     else:
-        _need(out, "out", bf, dev)
+        _need(out, "out", (odt,), dev)
+    if new_state_f32 is not None:
+        _need(new_state_f32, "new_state_f32", (torch.float32,), dev)
+        if tuple(new_state_f32.shape) != (B, HV, V, K):
+            raise ValueError(f"new_state_f32 must be [{B},{HV},{V},{K}]")
     args = GdnDecodeArgs(q=_ptr(q), k=_ptr(k), v=_ptr(v), a=_ptr(a), b=_ptr(b),
                          A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), state=_ptr(state),
                          slot_indices=_ptr(slot_indices), o=_ptr(out),
+                         new_state_f32=_ptr(new_state_f32),
                          B=B, T=T, H=H, HV=HV, K=K, V=V, pool=pool,
                          use_qk_l2norm=int(bool(use_qk_l2norm)),
+                         o_fp32=int(odt == torch.float32),
                          scale=float(scale) if scale is not None else 0.0,
                          softplus_beta=float(softplus_beta),
                          softplus_threshold=float(softplus_threshold), eps=float(eps))

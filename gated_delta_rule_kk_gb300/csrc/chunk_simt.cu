@@ -279,7 +279,11 @@ __global__ void __launch_bounds__(THREADS, 1) chunk_fwd_simt_kernel(ChunkParams 
         float acc = 0.f;
         for (int c = 0; c < K; ++c) acc = fmaf(qS[i * KS + c], hS[c * VS + j], acc);
         for (int m = 0; m <= i; ++m) acc = fmaf(QS[i * LDA + m], uS[m * VS + j], acc);
-        o[((row0 + i) * H + h) * V + v0 + j] = from_f32<T>(acc);
+        const size_t oi = ((row0 + i) * H + h) * V + v0 + j;
+        if (p.o_f32)
+          static_cast<float *>(p.o)[oi] = acc;
+        else
+          o[oi] = from_f32<T>(acc);
       }
     }
     float hn[(KMAX * VT) / THREADS];

@@ -18,9 +18,9 @@
 //    carry fp32-grade accuracy.  Per (chunk, head) the kernel stores a block
 //    of ready-made operand images the sequential pass consumes directly:
 //      AW  [-w ; q] (bf16)                U   u (fp32, per 32-wide V tile)
-//      KT  k e^{gamma_L - gamma} (bf16)   SC  exp(gamma_L) per key row,
-//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)      exp(gamma_L - gamma_i) and
-//                                              scale exp(gamma_i) per token
+//      KT  [k~_hi ; k~_lo] (bf16 pair,    SC  exp(gamma_L) per key row,
+//          k~ = k e^{gamma_L - gamma})        exp(gamma_L - gamma_i) and
+//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)      scale exp(gamma_i) per token
 //    For the per-channel gate (KDA, vLLM kimi_k3 kda/chunk_intra,
 //    chunk_kda_fwd_kernel_inter_solve_fused) the exponentials move into the
 //    operands: S = [k e^g; q e^g] (k e^-g)^T with the chunk start as the
@@ -36,7 +36,9 @@
 //    whole sequence).  Per chunk
 //      D1  = [-w ; q~] [h_hi | h_lo]      rows 0..63: -w h, rows 64..127: q h
 //      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
-//      DH  = k~^T v_new                  (k~ = k e^{gamma_L - gamma}, from KT)
+//      DH  = k~^T v_new                  (k~ = k e^{gamma_L - gamma} as a hi + lo
+//                                         pair, from KT: the state update keeps
+//                                         fp32-grade accuracy over long memories)
 //      D5  = [Aqk_lo ; Aqk_hi] v_new
 //      h   = exp(gamma_L) h + DH
 //      o   = scale e^gamma (q h) + Aqk v_new
@@ -65,10 +67,11 @@ constexpr int VMAX = 128;
 constexpr float GATE_FACTOR_LIMIT = 80.f;  // |gamma| bound for split exponentials
 
 // per (chunk, head) block in the workspace: the chain's operand images
-//   AW  [-w ; q~] (128 x 128 bf16, cs 2048)   KT  k~ (64 x 128 bf16, cs 1024)
+//   AW  [-w ; q~] (128 x 128 bf16, cs 2048)
+//   KT  [k~_hi ; k~_lo] (128 token rows x 128 keys bf16, cs 2048)
 //   AQ  [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048) SC  decay[128], rs[64], qs[64]
 //   U   u, fp32 [V / 32 tiles][64][32], 16-byte group q of row i at q ^ (i & 7)
-constexpr uint32_t OFF_AW = 0, OFF_KT = 32768, OFF_AQ = 49152, OFF_SC = 65536, OFF_U = 66560;
+constexpr uint32_t OFF_AW = 0, OFF_KT = 32768, OFF_AQ = 65536, OFF_SC = 81920, OFF_U = 82944;
 __host__ __device__ constexpr uint32_t block_bytes(int V, bool) {
   return OFF_U + (uint32_t)V * 256u;
 }
@@ -122,7 +125,7 @@ __device__ __forceinline__ void split8(const float *f, uint4 &hi, uint4 &lo) {
 struct TcParams {
   const float *g, *beta, *h0;
   float *ht;
-  __nv_bfloat16 *o;
+  void *o;                 // bf16, or fp32 with o_f32
   const int32_t *cu_seqlens;
   int32_t *table;          // [N + 1] chunk offsets, then [N] chain order (packed sequences)
   unsigned char *blocks;   // per (chunk, head) operand blocks
@@ -131,6 +134,7 @@ struct TcParams {
   int B, T, H, Hk, V, N, NT;  // NT: chunks per sequence without cu_seqlens
   int g_is_cumsum;
   int v_first;             // h0, ht stored [V, K] per (sequence, head) instead of [K, V]
+  int o_f32;               // o written as fp32 instead of bf16
   float scale;
   uint32_t block;          // bytes per (chunk, head) block
 };
@@ -555,7 +559,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       *kp = pack8(a);
       *qp = pack8(b);
       *reinterpret_cast<uint4 *>(KB + img_off(i, 8 * cg, 1024)) = pack8(c);
-      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 1024)) = pack8(t);
+      uint4 thi, tlo;
+      split8(t, thi, tlo);
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 2048)) = thi;
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(64 + i, 8 * cg, 2048)) = tlo;
     }
     ptx::fence_proxy_async_smem();
     __syncthreads();
@@ -579,8 +586,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::mma_commit(&bars[1]);
   }
   if (!KDA) {
-    // KT = k e^{gamma_L - gamma_i} (zero on padding rows), straight into the
-    // block while the GEMM runs; the chain's state update takes it as is
+    // KT = k e^{gamma_L - gamma_i} (zero on padding rows) as a hi + lo pair,
+    // straight into the block while the GEMM runs; the chain's state update
+    // takes it as is
     for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
       const int i = pc & 63, cg = pc >> 6;
       float kf[8];
@@ -588,7 +596,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       const float r = sc[128 + i];
 #pragma unroll
       for (int e = 0; e < 8; ++e) kf[e] *= r;
-      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 1024)) = pack8(kf);
+      uint4 hi, lo;
+      split8(kf, hi, lo);
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 2048)) = hi;
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(64 + i, 8 * cg, 2048)) = lo;
     }
   }
   const bool ok1 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
@@ -794,10 +805,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 //
 // shared memory: two stages holding one operand block each
 //   AW  [0, 32768)       [-w ; q~] (128 x 128, cs 2048)
-//   KT  [32768, 49152)   k~ (64 tokens x 128 keys, cs 1024)
-//   AQ  [49152, 65536)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
-//   SC  [65536, 66560)   decay[128], rs[64], qs[64]
-//   U   [66560, 74752)   u tile, fp32 64 x 32 (row-swizzled 16-byte groups)
+//   KT  [32768, 65536)   [k~_hi ; k~_lo] (128 token rows x 128 keys, cs 2048)
+//   AQ  [65536, 81920)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
+//   SC  [81920, 82944)   decay[128], rs[64], qs[64]
+//   U   [82944, 91136)   u tile, fp32 64 x 32 (row-swizzled 16-byte groups)
 // then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo]
 // (64 tokens x 64, cs 1024) and the fp32 exchange X.  A stage is filled and
 // released in two halves: AW, SC and U are free once D1 has run and v_new is
@@ -806,8 +817,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 // Every bf16 pair rides in the N dimension of one GEMM (N = 64), so the
 // split costs no extra tcgen05 instructions; each accumulator holds the two
 // halves side by side and the epilogue adds them.
-constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 49152, S_SC = 65536, S_U = 66560,
-                   STAGE_BYTES = 74752;
+constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 65536, S_SC = 81920, S_U = 82944,
+                   STAGE_BYTES = 91136;
 constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_X = C_VN + 8192,
                    C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
 constexpr int CHAIN_THREADS = 320;
@@ -915,7 +926,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     // of chunk c (output GEMM of chunk c - 2), so waiting in the order
     // A(c), B(c), A(c + 1), ... never holds a release back.
     if (lane == 0) {
-      constexpr uint32_t A_BYTES = 32768 + 1024 + 8192, B_BYTES = 32768;
+      constexpr uint32_t A_BYTES = 32768 + 1024 + 8192, B_BYTES = 49152;
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1, k = c >> 1;
@@ -950,7 +961,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       const int s = c & 1, k = c >> 1;
       unsigned char *st = smem + s * STAGE_BYTES;
       const uint64_t aw = ptx::sdesc(st + S_AW, 2048, 128);
-      const uint64_t kt = ptx::sdesc(st + S_KT, 128, 1024);
+      const uint64_t kt = ptx::sdesc(st + S_KT, 128, 2048);
       const uint64_t aq = ptx::sdesc(st + S_AQ, 2048, 128);
       ok = ptx::mbar_wait_bounded(&fullA[s], (uint32_t)(k & 1)) && ok;
       __syncwarp();
@@ -969,10 +980,12 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       bar_sync(BAR_VNREADY, BAR_VNREADY_THREADS);  // v_new is in VN
       ptx::tc_fence_after();
       if (lane == 0) {
-        // DH = k~^T [vn_hi | vn_lo]  (critical path), then D5 = AQ [vn_hi | vn_lo]
+        // DH = [k~_hi ; k~_lo]^T [vn_hi | vn_lo ; vn_hi | vn_lo] (K = 128: the
+        // token rows once with each half of k~; critical path), then
+        // D5 = AQ [vn_hi | vn_lo]
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, ks * 256), id_mnmn, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 256), id_mnmn, ks > 0);
         ptx::mma_commit(d3);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1083,10 +1096,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
           float ov[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) ov[j] = fmaf(qs, qh[j], d5v[j] + X[i * 33 + c0 + j]);
-          uint4 *dst = reinterpret_cast<uint4 *>(
-              p.o + ((size_t)(b * p.T + bos + c * BT + i) * p.H + h) * p.V + v0 + c0);
-          dst[0] = pack8(ov);
-          dst[1] = pack8(ov + 8);
+          const size_t oi = ((size_t)(b * p.T + bos + c * BT + i) * p.H + h) * p.V + v0 + c0;
+          if (p.o_f32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + oi);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + oi);
+            dst[0] = pack8(ov);
+            dst[1] = pack8(ov + 8);
+          }
         }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -1189,7 +1209,8 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   TcParams p{};
   p.g = cp.g; p.beta = cp.beta; p.h0 = cp.h0; p.ht = cp.ht;
   p.kraw = cp.k; p.qraw = cp.q;
-  p.o = static_cast<__nv_bfloat16 *>(cp.o);
+  p.o = cp.o;
+  p.o_f32 = cp.o_f32;
   p.cu_seqlens = cp.cu_seqlens;
   p.table = static_cast<int32_t *>(ws);
   p.blocks = static_cast<unsigned char *>(ws) + table_bytes(cp.N);

@@ -432,7 +432,11 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
           float ov = hdr[H_GAM + t] * z[t];
 #pragma unroll
           for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[s2], ov);
-          o[(((size_t)bi * T + t) * HV + hv) * DV + rg + 32 * rsel] = __float2bfloat16_rn(ov);
+          const size_t oi = (((size_t)bi * T + t) * HV + hv) * DV + rg + 32 * rsel;
+          if (p.o_f32)
+            static_cast<float *>(p.o)[oi] = ov;
+          else
+            o[oi] = __float2bfloat16_rn(ov);
         }
       }
 
@@ -485,10 +489,31 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
 
     if (slot < 0) {
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
-      for (int idx = tid; idx < T * DV; idx += DTHREADS)
-        o[(((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV] = __float2bfloat16_rn(0.f);
+      for (int idx = tid; idx < T * DV; idx += DTHREADS) {
+        const size_t oi = (((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV;
+        if (p.o_f32)
+          static_cast<float *>(p.o)[oi] = 0.f;
+        else
+          o[oi] = __float2bfloat16_rn(0.f);
+      }
     } else {
       __nv_bfloat16 *dst = state + ((size_t)slot * HV + hv) * DV * DK;
+      if (p.state_f32) {
+        // the fp32 values the bf16 write-back rounds (entry bi, not its slot)
+        float *d32 = p.state_f32 + ((size_t)bi * HV + hv) * DV * DK;
+#pragma unroll
+        for (int i = 0; i < ROWS_PER_THREAD; ++i) {
+          const int row = rg + 32 * i;
+#pragma unroll
+          for (int pc = 0; pc < 2; ++pc) {
+            float4 *q4 = reinterpret_cast<float4 *>(d32 + row * DK + (cs + 8 * pc) * 8);
+            q4[0] = make_float4(S[i][pc * 4].x, S[i][pc * 4].y, S[i][pc * 4 + 1].x,
+                                S[i][pc * 4 + 1].y);
+            q4[1] = make_float4(S[i][pc * 4 + 2].x, S[i][pc * 4 + 2].y, S[i][pc * 4 + 3].x,
+                                S[i][pc * 4 + 3].y);
+          }
+        }
+      }
 #pragma unroll
       for (int i = 0; i < ROWS_PER_THREAD; ++i) {
         const int row = rg + 32 * i;

@@ -409,7 +409,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
             float ov = hdr[H_GAM + t] * z[h][t];
 #pragma unroll
             for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[h][s2], ov);
-            o[(((size_t)bi * T + t) * HV + hv) * DV + row] = __float2bfloat16_rn(ov);
+            const size_t oi = (((size_t)bi * T + t) * HV + hv) * DV + row;
+            if (p.o_f32)
+              static_cast<float *>(p.o)[oi] = ov;
+            else
+              o[oi] = __float2bfloat16_rn(ov);
           }
         }
       }
@@ -471,6 +475,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
     }
     order = __shfl_sync(0xffffffffu, order, 0);
 
+    if (slot >= 0 && p.state_f32) {
+      // the fp32 values the bf16 write-back rounds (entry bi, not its slot):
+      // rows r0 + g and r0 + g + 8, columns 8 n + 2 tig (+ 1)
+      float *d32 = p.state_f32 + ((size_t)bi * HV + hv) * DV * DK;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const int col = 8 * n + 2 * tig;
+        *reinterpret_cast<float2 *>(d32 + (r0 + g) * DK + col) = make_float2(C[n][0], C[n][1]);
+        *reinterpret_cast<float2 *>(d32 + (r0 + g + 8) * DK + col) = make_float2(C[n][2], C[n][3]);
+      }
+    }
     if (slot >= 0) {
       // ---- write back: bf16 fragments -> this warp's rows of the slot -> TMA store
 #pragma unroll
@@ -489,8 +504,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
       }
     } else {
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
-      for (int idx = tid; idx < T * DV; idx += NTHREADS)
-        o[(((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV] = __float2bfloat16_rn(0.f);
+      for (int idx = tid; idx < T * DV; idx += NTHREADS) {
+        const size_t oi = (((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV;
+        if (p.o_f32)
+          static_cast<float *>(p.o)[oi] = 0.f;
+        else
+          o[oi] = __float2bfloat16_rn(0.f);
+      }
     }
     // done with the state slot: the last warp out refills it
     __syncwarp();

@@ -55,7 +55,8 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
                          const float *g, const float *beta, const float *h0, const float *ht,
                          const void *o, const int32_t *cu, int B, int T, int Hk, int Hv, int K,
                          int V, int N, int chunk_size, int g_is_cumsum, int v_first,
-                         float scale, const char *hk_name, bool sizes_only = false) {
+                         int o_f32, float scale, const char *hk_name,
+                         bool sizes_only = false) {
   REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG, "dtype %d is not GDN_F32/GDN_BF16", dtype);
   REQUIRE(B >= 1 && T >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1 && N >= 1,
           GDN_ERR_INVALID_ARG, "sizes must be positive (B=%d T=%d heads=%d/%d K=%d V=%d N=%d)", B,
@@ -68,6 +69,7 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
   REQUIRE(chunk_size == BT, GDN_ERR_UNSUPPORTED, "chunk_size must be %d (got %d)", BT, chunk_size);
   REQUIRE(g_is_cumsum == 0 || g_is_cumsum == 1, GDN_ERR_INVALID_ARG, "g_is_cumsum must be 0 or 1");
   REQUIRE(v_first == 0 || v_first == 1, GDN_ERR_INVALID_ARG, "state_v_first must be 0 or 1");
+  REQUIRE(o_f32 == 0 || o_f32 == 1, GDN_ERR_INVALID_ARG, "o_fp32 must be 0 or 1");
   REQUIRE(isfinite(scale), GDN_ERR_INVALID_ARG, "scale must be finite");
   if (cu == nullptr) {
     REQUIRE(N == B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)", N, B);
@@ -113,6 +115,7 @@ ChunkParams gdn_params(const gdn_chunk_args &a) {
   p.B = a.B; p.T = a.T; p.H = a.H; p.Hk = a.Hg; p.K = a.K; p.V = a.V; p.N = a.N;
   p.g_is_cumsum = a.g_is_cumsum;
   p.v_first = a.state_v_first;
+  p.o_f32 = a.o_fp32 || a.dtype == GDN_F32;
   p.scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)(a.K > 0 ? a.K : 1));
   return p;
 }
@@ -124,6 +127,7 @@ ChunkParams kda_params(const kda_chunk_args &a) {
   p.B = a.B; p.T = a.T; p.H = a.HV; p.Hk = a.H; p.K = a.K; p.V = a.V; p.N = a.N;
   p.g_is_cumsum = a.g_is_cumsum;
   p.v_first = a.state_v_first;
+  p.o_f32 = a.o_fp32 || a.dtype == GDN_F32;
   p.scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)(a.K > 0 ? a.K : 1));
   return p;
 }
@@ -152,7 +156,8 @@ gdn_status_t check_gdn_chunk_sizes(const gdn_chunk_args &a) {
   g_msg[0] = '\0';
   return check_chunk(a.dtype, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                      nullptr, a.cu_seqlens, a.B, a.T, a.Hg, a.H, a.K, a.V,
-                     a.N, a.chunk_size, a.g_is_cumsum, a.state_v_first, a.scale, "Hg", true);
+                     a.N, a.chunk_size, a.g_is_cumsum, a.state_v_first, a.o_fp32, a.scale, "Hg",
+                     true);
 }
 
 gdn_status_t set_host_error(gdn_status_t st, const char *msg) { return fail(st, "%s", msg); }
@@ -201,7 +206,8 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *a, gdn_stream_t stream) {
   if (a == nullptr) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
   gdn_status_t st = check_chunk(a->dtype, a->q, a->k, a->v, a->g, a->beta, a->h0, a->ht, a->o,
                                 a->cu_seqlens, a->B, a->T, a->Hg, a->H, a->K, a->V, a->N,
-                                a->chunk_size, a->g_is_cumsum, a->state_v_first, a->scale, "Hg");
+                                a->chunk_size, a->g_is_cumsum, a->state_v_first, a->o_fp32,
+                                a->scale, "Hg");
   if (st != GDN_OK) return st;
   ChunkParams p = gdn_params(*a);
   return run_chunk(p, a->dtype == GDN_BF16, false, a->workspace, a->workspace_bytes,
@@ -213,7 +219,8 @@ gdn_status_t kda_chunk_fwd(const kda_chunk_args *a, gdn_stream_t stream) {
   if (a == nullptr) return fail(GDN_ERR_INVALID_ARG, "args is NULL");
   gdn_status_t st = check_chunk(a->dtype, a->q, a->k, a->v, a->g, a->beta, a->h0, a->ht, a->o,
                                 a->cu_seqlens, a->B, a->T, a->H, a->HV, a->K, a->V, a->N,
-                                a->chunk_size, a->g_is_cumsum, a->state_v_first, a->scale, "H");
+                                a->chunk_size, a->g_is_cumsum, a->state_v_first, a->o_fp32,
+                                a->scale, "H");
   if (st != GDN_OK) return st;
   ChunkParams p = kda_params(*a);
   return run_chunk(p, a->dtype == GDN_BF16, true, a->workspace, a->workspace_bytes,
@@ -379,6 +386,7 @@ gdn_status_t gdn_decode(const gdn_decode_args *a, gdn_stream_t stream) {
           "identity slots need pool (%d) >= B (%d)", a->pool, a->B);
   REQUIRE(a->use_qk_l2norm == 0 || a->use_qk_l2norm == 1, GDN_ERR_INVALID_ARG,
           "use_qk_l2norm must be 0 or 1");
+  REQUIRE(a->o_fp32 == 0 || a->o_fp32 == 1, GDN_ERR_INVALID_ARG, "o_fp32 must be 0 or 1");
   REQUIRE(isfinite(a->scale) && isfinite(a->softplus_beta) && isfinite(a->softplus_threshold) &&
               isfinite(a->eps),
           GDN_ERR_INVALID_ARG, "scalar arguments must be finite");
@@ -392,10 +400,12 @@ gdn_status_t gdn_decode(const gdn_decode_args *a, gdn_stream_t stream) {
   REQUIRE_PTR(a->state, "state");
   REQUIRE_PTR(a->o, "o");
   REQUIRE_OPT_PTR(a->slot_indices, "slot_indices");
+  REQUIRE_OPT_PTR(a->new_state_f32, "new_state_f32");
   DecodeParams p{};
   p.q = a->q; p.k = a->k; p.v = a->v; p.a = a->a; p.b = a->b;
   p.A_log = a->A_log; p.dt_bias = a->dt_bias; p.state = a->state;
-  p.slot_indices = a->slot_indices; p.o = a->o;
+  p.slot_indices = a->slot_indices; p.o = a->o; p.state_f32 = a->new_state_f32;
+  p.o_f32 = a->o_fp32;
   p.B = a->B; p.T = a->T; p.H = a->H; p.HV = a->HV; p.K = a->K; p.V = a->V; p.pool = a->pool;
   p.use_qk_l2norm = a->use_qk_l2norm;
   p.scale = a->scale > 0.f ? a->scale : 1.0f / sqrtf((float)a->K);

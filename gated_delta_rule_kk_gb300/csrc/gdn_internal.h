@@ -21,6 +21,7 @@ struct ChunkParams {
   int B, T, H, Hk, K, V, N;
   int g_is_cumsum;
   int v_first;                // h0, ht as [V, K] instead of [K, V]
+  int o_f32;                  // o written as float32 (else in the input dtype)
   float scale;
 };
 
@@ -30,9 +31,11 @@ struct DecodeParams {
   void *state;
   const int32_t *slot_indices;
   void *o;
+  float *state_f32;           // updated states in fp32 [B, HV, V, K] or NULL
   int *err;
   int B, T, H, HV, K, V, pool;
   int use_qk_l2norm;
+  int o_f32;                  // o written as float32 (else bf16)
   float scale, softplus_beta, softplus_threshold, eps;
 };
 

@@ -59,10 +59,10 @@ struct Plan {
   int P = 0;
   Piece pc[MAX_PIECES];
   int64_t rows_per_seq = 0;                           // T (fixed-length batches)
-  size_t rq = 0, rv = 0, rg = 0, state_seq = 0;       // bytes per row / per sequence state
-  size_t q[MAX_PIECES], v[MAX_PIECES], g[MAX_PIECES]; // piece offsets inside a region
+  size_t rq = 0, rv = 0, ro = 0, rg = 0, state_seq = 0;  // bytes per row / sequence state
+  size_t q[MAX_PIECES], v[MAX_PIECES], o[MAX_PIECES], g[MAX_PIECES];  // piece offsets
   size_t s[MAX_PIECES];                               // sequence pieces: state slice offset
-  size_t reg_q = 0, reg_v = 0, reg_g = 0, reg_s = 0, reg_cu = 0;
+  size_t reg_q = 0, reg_v = 0, reg_o = 0, reg_g = 0, reg_s = 0, reg_cu = 0;
   size_t off_q = 0, off_k = 0, off_v = 0, off_g = 0, off_beta = 0, off_o = 0;
   size_t off_s0 = 0, off_s1 = 0, off_cu = 0, off_ws = 0, ws_bytes = 0, total = 0;
   std::vector<int32_t> cu;                            // varlen: rebased offsets, all pieces
@@ -85,7 +85,7 @@ gdn_chunk_args piece_args(const gdn_chunk_args &a, const Plan &L, int j, unsigne
   d.q = base + L.off_q + L.q[j];
   d.k = base + L.off_k + L.q[j];
   d.v = base + L.off_v + L.v[j];
-  d.o = base + L.off_o + L.v[j];
+  d.o = base + L.off_o + L.o[j];
   d.g = reinterpret_cast<const float *>(base + L.off_g + L.g[j]);
   d.beta = reinterpret_cast<const float *>(base + L.off_beta + L.g[j]);
   float *s0 = reinterpret_cast<float *>(base + L.off_s0);
@@ -136,6 +136,7 @@ gdn_status_t make_plan(const gdn_chunk_args &a, Plan *L) {
   const size_t elt = a.dtype == GDN_BF16 ? 2 : 4;
   L->rq = size_t(a.Hg) * a.K * elt;
   L->rv = size_t(a.H) * a.V * elt;
+  L->ro = size_t(a.H) * a.V * (a.o_fp32 ? 4 : elt);
   L->rg = size_t(a.H) * 4;
   L->state_seq = size_t(a.H) * a.K * a.V * 4;
   L->varlen = a.cu_seqlens != nullptr;
@@ -197,11 +198,12 @@ gdn_status_t make_plan(const gdn_chunk_args &a, Plan *L) {
   }
 
   // regions: each piece's slice starts on a 256-byte boundary
-  L->reg_q = L->reg_v = L->reg_g = L->reg_s = 0;
+  L->reg_q = L->reg_v = L->reg_o = L->reg_g = L->reg_s = 0;
   for (int j = 0; j < L->P; ++j) {
     const int64_t rows = piece_rows(*L, L->pc[j]);
     L->q[j] = L->reg_q; L->reg_q += align256(rows * L->rq);
     L->v[j] = L->reg_v; L->reg_v += align256(rows * L->rv);
+    L->o[j] = L->reg_o; L->reg_o += align256(rows * L->ro);
     L->g[j] = L->reg_g; L->reg_g += align256(rows * L->rg);
     L->s[j] = L->reg_s; L->reg_s += align256(size_t(L->pc[j].n1 - L->pc[j].n0) * L->state_seq);
   }
@@ -211,7 +213,7 @@ gdn_status_t make_plan(const gdn_chunk_args &a, Plan *L) {
   L->off_q = off; off += L->reg_q;
   L->off_k = off; off += L->reg_q;
   L->off_v = off; off += L->reg_v;
-  L->off_o = off; off += L->reg_v;
+  L->off_o = off; off += L->reg_o;
   L->off_g = off; off += L->reg_g;
   L->off_beta = off; off += L->reg_g;
   L->off_s0 = off; off += L->reg_s;
@@ -416,7 +418,7 @@ extern "C" gdn_status_t gdn_chunk_fwd_host(const gdn_chunk_args *a, gdn_stream_t
 
     ok(cudaEventRecord(dq->computed[j], s), "event record");
     ok(cudaStreamWaitEvent(dq->out, dq->computed[j], 0), "stream wait");
-    ok(copy_rows(ho + first * L.rv, T * L.rv, base + L.off_o + L.v[j], len * L.rv, len * L.rv,
+    ok(copy_rows(ho + first * L.ro, T * L.ro, base + L.off_o + L.o[j], len * L.ro, len * L.ro,
                  height, D2H, dq->out, mp), "o copy");
     if (!L.time_cut && a->ht)
       ok(cudaMemcpyAsync(reinterpret_cast<char *>(a->ht) + size_t(p.n0) * L.state_seq,

@@ -68,7 +68,11 @@ typedef enum gdn_dtype {
  * and chunk_fwd_h (KDA _fla/ops/common/chunk_h.py):
  *   q, k   [B, T, Hg, K]  dtype       key/query heads; value head h reads
  *                                     key head h / (H / Hg)
- *   v, o   [B, T, H, V]   dtype       o is written
+ *   v, o   [B, T, H, V]   dtype       o is written, in float32 instead
+ *                                     when o_fp32 = 1 (the same result
+ *                                     before its rounding to dtype: with
+ *                                     o_fp32 = 0 and bf16, o is exactly the
+ *                                     round-to-nearest-even of that value)
  *   g      [B, T, H]      float32     natural-log gate per token; with
  *                                     g_is_cumsum = 1 it is instead the
  *                                     inclusive cumulative sum inside each
@@ -108,6 +112,7 @@ typedef struct gdn_chunk_args {
   int32_t chunk_size;
   int32_t g_is_cumsum;
   int32_t state_v_first;       /* 1: h0, ht are [N, H, V, K] instead of [N, H, K, V] */
+  int32_t o_fp32;              /* 1: o is float32 whatever dtype is; 0: o has dtype */
   float scale;
   void *workspace;
   size_t workspace_bytes;
@@ -265,7 +270,7 @@ gdn_status_t gdn_chunk_host_workspace_size(const gdn_chunk_args *args, size_t *b
  * (KDA).  Shapes follow chunk_kda_fwd_kernel_inter_solve_fused (vLLM kimi_k3
  * kda/chunk_intra page):
  *   q, k   [B, T, H, K]   dtype       value head hv reads key head hv / (HV / H)
- *   v, o   [B, T, HV, V]  dtype
+ *   v, o   [B, T, HV, V]  dtype       (o float32 with o_fp32 = 1, as for GDN)
  *   g      [B, T, HV, K]  float32     chunk-local inclusive cumulative sum of
  *                                     the per-channel log-gates when
  *                                     g_is_cumsum = 1 (as that kernel takes
@@ -292,6 +297,7 @@ typedef struct kda_chunk_args {
   int32_t chunk_size;
   int32_t g_is_cumsum;
   int32_t state_v_first;       /* 1: h0, ht are [N, HV, V, K] instead of [N, HV, K, V] */
+  int32_t o_fp32;              /* 1: o is float32 whatever dtype is; 0: o has dtype */
   float scale;
   void *workspace;
   size_t workspace_bytes;
@@ -318,7 +324,12 @@ gdn_status_t kda_chunk_fwd(const kda_chunk_args *args, gdn_stream_t stream);
  *                                       outside [0, pool) records
  *                                       GDN_ERR_BAD_SLOT and that entry's o
  *                                       is written as zeros.
- *   o        [B, T, HV, V]    bf16
+ *   o        [B, T, HV, V]    bf16      (float32 when o_fp32 = 1: the same
+ *                                       value before its rounding to bf16)
+ *   new_state_f32 [B, HV, V, K] float32 or NULL: when given, entry b's
+ *                                       updated state in float32, the value
+ *                                       whose round-to-nearest-even the pool
+ *                                       receives (NULL = not written)
  * Per token: g = -exp(A_log) * softplus(a + dt_bias) with
  *   softplus(x) = log(1 + exp(beta_sp x)) / beta_sp if beta_sp x <= threshold
  *   else x; beta = sigmoid(b); if use_qk_l2norm, q and k are divided by
@@ -333,8 +344,10 @@ typedef struct gdn_decode_args {
   void *state;
   const int32_t *slot_indices;
   void *o;
+  float *new_state_f32;
   int32_t B, T, H, HV, K, V, pool;
   int32_t use_qk_l2norm;
+  int32_t o_fp32;
   float scale, softplus_beta, softplus_threshold, eps;
 } gdn_decode_args;
 

@@ -175,9 +175,9 @@ def test_decode_argument_errors(lib, change, expect):
 
 def test_workspace_size(lib):
     # the tensor-core path (bf16, K = 128, V % 32 == 0, V <= 128) needs per
-    # (chunk, head) operand blocks of 66560 + 256 V bytes plus the chunk table
+    # (chunk, head) operand blocks of 82944 + 256 V bytes plus the chunk table
     # (N + 1 offsets and N sequence indices, int32, rounded up to 256 bytes)
-    blk = 66560 + 256 * 128
+    blk = 82944 + 256 * 128
     a = good_chunk()
     n = ctypes.c_size_t(123)
     assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n)) == Status.OK
@@ -199,7 +199,7 @@ def test_workspace_size(lib):
     assert n.value == 0
     k = KdaChunkArgs(dtype=1, B=1, T=64, H=2, HV=2, K=128, V=64, N=1, chunk_size=64)
     assert lib.kda_chunk_workspace_size(ctypes.byref(k), ctypes.byref(n)) == Status.OK
-    assert n.value == 256 + 1 * 2 * (66560 + 256 * 64)
+    assert n.value == 256 + 1 * 2 * (82944 + 256 * 64)
 
 
 def test_workspace_errors_found_on_host(lib):

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from gated_delta_rule_kk_gb300 import synth
+from gated_delta_rule_kk_gb300 import gdn_chunk_fwd, synth
 from oracle import recurrence as R
 
 from _util import TOL_BF16, assert_close
@@ -52,5 +52,13 @@ def test_plain_c_caller(tmp_path):
     assert np.array_equal(raw_d, raw_h), "host entry point differs from the device entry point"
     o_ref, ht_ref = R.gdn_recurrent(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                     scale=inp["scale"], h0=inp["h0"])
-    assert_close(torch.from_numpy(o_d.copy()).to(torch.bfloat16), o_ref, TOL_BF16, "o")
+    # the same call with o in fp32 (through the binding): the C caller's bf16 o
+    # is its round-to-nearest-even bit for bit, and the fp32 o meets the bound
+    d = {k2: (v2.cuda() if isinstance(v2, torch.Tensor) else v2) for k2, v2 in inp.items()}
+    o32, ht32 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                              initial_state=d["h0"], out_dtype=torch.float32)
+    o16 = torch.from_numpy(o_d.copy()).to(torch.bfloat16)
+    assert torch.equal(o16, o32.cpu().to(torch.bfloat16))
+    assert np.array_equal(ht_d, ht32.cpu().numpy())
+    assert_close(o32, o_ref, TOL_BF16, "o")
     assert_close(ht_d, ht_ref, TOL_BF16, "ht")

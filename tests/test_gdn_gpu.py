@@ -14,10 +14,17 @@ pytestmark = pytest.mark.gpu
 
 
 def run_gpu(inp):
+    """o in fp32 (the value the bound applies to) and ht; for bf16 inputs the
+    default bf16 o must be that value rounded to nearest even, bit for bit."""
     d = to_dev(inp)
-    o, ht = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
-                          initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
-                          g_is_cumsum=d["g_is_cumsum"])
+    kw = dict(scale=d["scale"], initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+              g_is_cumsum=d["g_is_cumsum"])
+    o, ht = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], out_dtype=torch.float32, **kw)
+    if d["q"].dtype == torch.bfloat16:
+        o16, ht16 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
+        assert o16.dtype == torch.bfloat16
+        assert torch.equal(o16, o.to(torch.bfloat16)), "bf16 o is not the RNE of the fp32 o"
+        assert torch.equal(ht16, ht)
     assert gdn_check_device_error() == Status.OK
     return o, ht
 
@@ -219,7 +226,7 @@ def test_state_v_first_layout(dtype, K, V, lengths):
     B = 2 if lengths is None else 1
     inp = synth.prefill_inputs(81, B, T, 4, 2, K, V, dtype=dtype, h0_std=0.1, lengths=lengths)
     d = to_dev(inp)
-    kw = dict(scale=d["scale"], cu_seqlens=d["cu_seqlens"])
+    kw = dict(scale=d["scale"], cu_seqlens=d["cu_seqlens"], out_dtype=torch.float32)
     o1, ht1 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"], **kw)
     h0t = d["h0"].transpose(-1, -2).contiguous()
     o2, ht2 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=h0t,

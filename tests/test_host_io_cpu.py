@@ -11,7 +11,7 @@ import pytest
 from gated_delta_rule_kk_gb300 import _lib, build_lib
 from gated_delta_rule_kk_gb300._lib import GdnChunkArgs, Status
 
-BLK128 = 66560 + 256 * 128  # tensor-core operand block per (chunk, head), V = 128
+BLK128 = 82944 + 256 * 128  # tensor-core operand block per (chunk, head), V = 128
 
 
 def a256(x):

@@ -129,3 +129,18 @@ def test_device_pointers_are_rejected():
     torch.cuda.synchronize()
     o_d, _ = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"])
     _same(host_o, o_d.cpu(), "o")
+
+
+def test_fp32_output_from_host_buffers_equals_device_entry_point():
+    """o in fp32 (twice the bytes per row of bf16 o) through time pieces."""
+    inp = synth.prefill_inputs(97, 2, 1500, 2, 1, 128, 128, h0_std=0.1)
+    d = to_dev(inp)
+    o_d, ht_d = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
+                                  initial_state=d["h0"], out_dtype=torch.float32)
+    o_h, ht_h = gdn.gdn_chunk_fwd_host(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                       scale=inp["scale"], initial_state=inp["h0"],
+                                       out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert o_h.dtype == torch.float32
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(ht_h, ht_d.cpu())

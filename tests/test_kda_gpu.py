@@ -13,10 +13,16 @@ pytestmark = pytest.mark.gpu
 
 
 def run_gpu(inp):
+    """o in fp32 (the value the bound applies to) and ht; for bf16 inputs the
+    default bf16 o must be that value rounded to nearest even, bit for bit."""
     d = to_dev(inp)
-    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
-                          initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
-                          g_is_cumsum=d["g_is_cumsum"])
+    kw = dict(scale=d["scale"], initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+              g_is_cumsum=d["g_is_cumsum"])
+    o, ht = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], out_dtype=torch.float32, **kw)
+    if d["q"].dtype == torch.bfloat16:
+        o16, ht16 = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
+        assert torch.equal(o16, o.to(torch.bfloat16)), "bf16 o is not the RNE of the fp32 o"
+        assert torch.equal(ht16, ht)
     assert gdn_check_device_error() == Status.OK
     return o, ht
 
@@ -151,13 +157,15 @@ def test_state_v_first_layout(dtype, K):
     inp = synth.prefill_inputs(83, 1, 140, 4, 2, K, 64, dtype=dtype, h0_std=0.1,
                                per_channel=True)
     d = to_dev(inp)
-    o1, ht1 = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"])
+    o1, ht1 = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"],
+                            out_dtype=torch.float32)
     h0t = d["h0"].transpose(-1, -2).contiguous()
     o2, ht2 = kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=h0t,
-                            state_v_first=True)
+                            state_v_first=True, out_dtype=torch.float32)
     assert gdn_check_device_error() == Status.OK
     assert torch.equal(o1, o2)
     assert torch.equal(ht2, ht1.transpose(-1, -2))
     o_ref, ht_ref = run_oracle(inp)
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    assert_close(o2, o_ref, tol, "o")
     assert_close(ht2.transpose(-1, -2), ht_ref, tol, "ht")

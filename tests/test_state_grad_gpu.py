@@ -13,7 +13,7 @@ import gated_delta_rule_kk_gb300 as gdn
 from gated_delta_rule_kk_gb300 import Status, synth
 from oracle import state_pass as SP
 
-from _util import TOL_F32, assert_close
+from _util import TOL_BF16, TOL_F32, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -84,7 +84,11 @@ def test_tensor_core_path_partial_tile_and_bf16_gradients(gate):
     dh, dh0 = run(inp, states_dtype=torch.bfloat16)
     dh_ref, dh0_ref = oracle(inp)
     assert dh.dtype == torch.bfloat16
-    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate})")
+    # bf16 chunk gradients: bit for bit the RNE of the fp32 ones of the same call
+    dh32, _ = run(inp)
+    assert torch.equal(dh, dh32.to(torch.bfloat16))
+    assert_close(dh32, dh_ref, TOL_F32, f"dh fp32 ({gate})")
+    assert_close(dh, dh_ref, TOL_BF16, f"dh bf16 ({gate})")
     assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate})")
 
 
@@ -93,7 +97,10 @@ def test_bf16_chunk_gradients_and_no_chunk_output():
     dh, dh0 = run(inp, states_dtype=torch.bfloat16)
     dh_ref, dh0_ref = oracle(inp)
     assert dh.dtype == torch.bfloat16
-    assert_close(dh, dh_ref, TOL_F32, "dh (bf16)")
+    dh32, _ = run(inp)
+    assert torch.equal(dh, dh32.to(torch.bfloat16))
+    assert_close(dh32, dh_ref, TOL_F32, "dh (fp32)")
+    assert_close(dh, dh_ref, TOL_BF16, "dh (bf16)")
     assert_close(dh0, dh0_ref, TOL_F32, "dh0")
     none, dh0b = run(inp, output_states=False)
     assert none is None
