@@ -340,6 +340,32 @@ def run_ours(args, rank, world, dev):
                          "unit": "GB/s", "frac": vb / (vt / 1e3) / 1e9 / hbm,
                          "algorithmic_bytes": vb, "algorithmic_flops": vf, "traffic": None}}
         del vd, vo, vht, vin
+        # few long chains: one sequence of 8192 tokens, two heads (8 chains of
+        # 32 value columns on 152 SMs): the library's segment-parallel state
+        # pass against one sequential chain per sequence
+        fin = synth.prefill_inputs(7, 1, 8192, 2, 2, 128, 128, h0_std=0.1)
+        fm = fin["dims"]
+        fd = to_dev(fin, dev)
+        fo = torch.empty_like(fd["v"])
+        fht = torch.empty((1, 2, 128, 128), dtype=torch.float32, device=dev)
+        nseg = gdn.gdn_chunk_segment_count(1, 8192, 2, 2, 128, 128)
+        ftimes = {}
+        for segs in (1, 0):
+            fms = time_steps(lambda: gdn.gdn_chunk_fwd(fd["q"], fd["k"], fd["v"], fd["g"], fd["beta"],
+                                                       scale=fd["scale"], initial_state=fd["h0"],
+                                                       out=fo, final_state=fht, segments=segs),
+                             rsteps, max(3, args.warmup // 2), flush, stream)
+            ftimes[segs] = statistics.mean(fms)
+        fb = gdn_bytes(1, 8192, 2, 2, 128, 128, 1)
+        rows["gdn_few_chains"] = {
+            "workload": "GDN chunked prefill with few long chains: B=1, T=8192, H=Hg=2, "
+                        "K=V=128, bf16, h0 ~ N(0,0.1), ht returned",
+            "segments_chosen": nseg, "ms_per_call": ftimes[0], "ms_one_chain": ftimes[1],
+            "tokens_per_s": 8192 / (ftimes[0] / 1e3),
+            "roofline": {"bound": "hbm", "achieved": fb / (ftimes[0] / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": fb / (ftimes[0] / 1e3) / 1e9 / hbm,
+                         "algorithmic_bytes": fb, "traffic": None}}
+        del fd, fo, fht, fin
         # chunk state pass (gated linear attention), per-token gate and per-key gate
         for sgate in ("g", "gk"):
             sin = synth.state_pass_inputs(5, 2, 4096, 16, 128, 128, sgate, h0_std=0.1)

@@ -43,7 +43,7 @@ class GdnChunkArgs(ctypes.Structure):
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("Hg", c_int32),
         ("K", c_int32), ("V", c_int32), ("N", c_int32),
         ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("state_v_first", c_int32),
-        ("o_fp32", c_int32), ("scale", c_float),
+        ("o_fp32", c_int32), ("segments", c_int32), ("scale", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -57,7 +57,7 @@ class KdaChunkArgs(ctypes.Structure):
         ("B", c_int32), ("T", c_int32), ("H", c_int32), ("HV", c_int32),
         ("K", c_int32), ("V", c_int32), ("N", c_int32),
         ("chunk_size", c_int32), ("g_is_cumsum", c_int32), ("state_v_first", c_int32),
-        ("o_fp32", c_int32), ("scale", c_float),
+        ("o_fp32", c_int32), ("segments", c_int32), ("scale", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -122,6 +122,7 @@ class GdnStateBwdArgs(ctypes.Structure):
 SIGNATURES = {
     "gdn_chunk_workspace_size": ([ctypes.POINTER(GdnChunkArgs), ctypes.POINTER(c_size_t)], c_int32),
     "gdn_chunk_fwd": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
+    "gdn_chunk_segment_count": ([ctypes.POINTER(GdnChunkArgs), ctypes.POINTER(c_int32)], c_int32),
     "gdn_chunk_fwd_host": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
     "gdn_chunk_host_workspace_size": ([ctypes.POINTER(GdnChunkArgs), ctypes.POINTER(c_size_t)],
                                       c_int32),

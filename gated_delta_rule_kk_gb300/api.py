@@ -110,13 +110,15 @@ def _attach_workspace(args, size_fn, workspace, device):
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=False, out=None, final_state=None,
-                  workspace=None, stream=None, state_v_first=False, out_dtype=None):
+                  workspace=None, stream=None, state_v_first=False, out_dtype=None, segments=0):
     """GDN chunked forward.  Returns ``(o, ht)`` (``ht`` None if not requested).
 
     q, k [B,T,Hg,K]; v [B,T,H,V]; g, beta [B,T,H] float32; initial_state
     [N,H,K,V] float32 ([N,H,V,K] with ``state_v_first``, as ``ht``);
     cu_seqlens [N+1] int32 (then B == 1).  ``out_dtype=torch.float32`` writes
     o in float32 (the value a bf16 o is the round-to-nearest-even of).
+    ``segments``: the state pass's segment count (0 = the library's choice,
+    1 = one sequential chain per sequence, >= 2 = segment-parallel).
     """
     dt, (B, T, Hg, H, K, V, N), out, ht = _chunk_common(
         q, k, v, g, beta, initial_state, cu_seqlens, output_final_state, out, final_state, "H",
@@ -125,7 +127,7 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N, chunk_size=CHUNK,
                      g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
-                     o_fp32=int(out.dtype == torch.float32),
+                     o_fp32=int(out.dtype == torch.float32), segments=int(segments),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     ws = _attach_workspace(a, lambda lib: lib.gdn_chunk_workspace_size, workspace, q.device)
@@ -133,6 +135,20 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
     _lib.check(lib.gdn_chunk_fwd(ctypes.byref(a), _stream(stream)), "gdn_chunk_fwd")
     del ws  # the caching allocator keeps it valid for work already on `stream`
     return out, ht
+
+
+def gdn_chunk_segment_count(B, T, H, Hg, K, V, N=None, dtype=torch.bfloat16, varlen=False,
+                            segments=0):
+    """Segments per sequence the state pass of ``gdn_chunk_fwd`` uses for
+    these sizes (1: one sequential chain per sequence)."""
+    dt = DType.BF16 if dtype == torch.bfloat16 else DType.F32
+    a = GdnChunkArgs(dtype=int(dt), B=B, T=T, H=H, Hg=Hg, K=K, V=V, N=N or B, chunk_size=CHUNK,
+                     segments=int(segments),
+                     cu_seqlens=ctypes.c_void_p(16) if varlen else None)
+    n = ctypes.c_int32(0)
+    _lib.check(_lib.load().gdn_chunk_segment_count(ctypes.byref(a), ctypes.byref(n)),
+               "gdn_chunk_segment_count")
+    return n.value
 
 
 def _need_host(t, name, dtypes):
@@ -262,7 +278,7 @@ def gdn_noalloc_scratch_bytes():
 
 def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                   output_final_state=True, g_is_cumsum=True, out=None, final_state=None,
-                  workspace=None, stream=None, state_v_first=False, out_dtype=None):
+                  workspace=None, stream=None, state_v_first=False, out_dtype=None, segments=0):
     """KDA chunked forward.  Returns ``(o, ht)``.
 
     q, k [B,T,H,K]; v [B,T,HV,V]; g [B,T,HV,K] float32 (chunk-local cumsum
@@ -276,7 +292,7 @@ def kda_chunk_fwd(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=N
                      h0=_ptr(initial_state), ht=_ptr(ht), o=_ptr(out), cu_seqlens=_ptr(cu_seqlens),
                      B=B, T=T, H=H, HV=HV, K=K, V=V, N=N, chunk_size=CHUNK,
                      g_is_cumsum=int(bool(g_is_cumsum)), state_v_first=int(bool(state_v_first)),
-                     o_fp32=int(out.dtype == torch.float32),
+                     o_fp32=int(out.dtype == torch.float32), segments=int(segments),
                      scale=float(scale) if scale is not None else 0.0,
                      workspace=None, workspace_bytes=0)
     ws = _attach_workspace(a, lambda lib: lib.kda_chunk_workspace_size, workspace, q.device)

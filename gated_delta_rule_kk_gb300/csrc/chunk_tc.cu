@@ -54,6 +54,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "ptx.cuh"
@@ -137,6 +139,12 @@ struct TcParams {
   int o_f32;               // o written as fp32 instead of bf16
   float scale;
   uint32_t block;          // bytes per (chunk, head) block
+  // segment-parallel state pass (seg_count >= 2; see chain_kernel)
+  int seg_count;           // segments per sequence
+  int seg_phase;           // 0: whole sequences; 1: every segment from zero / identity;
+                           // 2: segments 1 .. seg_count-1 again from their true start
+  float *seg_state;        // [N][seg_count][H][K][K + V]: phase-1 ends, [M_s | B_s]
+  float *seg_start;        // [N][seg_count][H][K][V]: combined start states (s >= 1)
 };
 
 // ---------------------------------------------------------------------------
@@ -337,7 +345,7 @@ struct IntraLayout {
 };
 
 template <bool KDA>
-__global__ void __launch_bounds__(INTRA_THREADS, 1)
+__global__ void __launch_bounds__(INTRA_THREADS, 2)
 intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
              TcParams p) {
@@ -530,11 +538,21 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
   const bool split = flags[0] != 0;
 
+  // KDA, split range: the lo halves of the gated operands, for the S GEMM's
+  // hi.lo and lo.hi passes (KQ_lo where the gate tile was, KB_lo in the AQ
+  // staging area, both dead until the gating)
+  unsigned char *KQL = smem + I_R1;
+  unsigned char *KBL = AQ;
   if (KDA) {
     // KQ <- [k e^g ; q e^g] (bounded by |k|, |q| for gates <= 0),
-    // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g} (to the block)
+    // KB <- k e^-g (split path only), KT <- k e^{gamma_L - g} (to the block);
+    // each a hi + lo pair in the split path (the per-channel gate sits inside
+    // the products, so its operands carry the rounding)
     const float *G = Asm;
-    for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
+    uint4 klo[4], qlo[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int pc = tid + it * INTRA_THREADS;
       const int i = pc & 63, cg = pc >> 6;
       uint4 *kp = reinterpret_cast<uint4 *>(KQ + img_off(i, 8 * cg, 2048));
       uint4 *qp = reinterpret_cast<uint4 *>(KQ + img_off(64 + i, 8 * cg, 2048));
@@ -556,13 +574,27 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         const float fl = split ? sc[8 * cg + e] * en : __expf(gl[8 * cg + e] - gv);
         t[e] = i < L ? kf[e] * fl : 0.f;
       }
-      *kp = pack8(a);
-      *qp = pack8(b);
-      *reinterpret_cast<uint4 *>(KB + img_off(i, 8 * cg, 1024)) = pack8(c);
-      uint4 thi, tlo;
-      split8(t, thi, tlo);
-      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 2048)) = thi;
-      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(64 + i, 8 * cg, 2048)) = tlo;
+      uint4 hi, lo;
+      split8(a, hi, klo[it]);
+      *kp = hi;
+      split8(b, hi, qlo[it]);
+      *qp = hi;
+      split8(c, hi, lo);
+      *reinterpret_cast<uint4 *>(KB + img_off(i, 8 * cg, 1024)) = hi;
+      if (split) *reinterpret_cast<uint4 *>(KBL + img_off(i, 8 * cg, 1024)) = lo;
+      split8(t, hi, lo);
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 2048)) = hi;
+      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(64 + i, 8 * cg, 2048)) = lo;
+    }
+    if (split) {
+      __syncthreads();  // every thread is done reading the gate tile
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int pc = tid + it * INTRA_THREADS;
+        const int i = pc & 63, cg = pc >> 6;
+        *reinterpret_cast<uint4 *>(KQL + img_off(i, 8 * cg, 2048)) = klo[it];
+        *reinterpret_cast<uint4 *>(KQL + img_off(64 + i, 8 * cg, 2048)) = qlo[it];
+      }
     }
     ptx::fence_proxy_async_smem();
     __syncthreads();
@@ -570,7 +602,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     ptx::fence_proxy_async_smem();
   }
 
-  // ---- S = [k; q] k^T  (M = 128, N = 64, K = 128)
+  // ---- S = [k; q] k^T  (M = 128, N = 64, K = 128); KDA split range: three
+  //      passes hi.hi + hi.lo + lo.hi of the gated operands
   uint32_t mma_phase = 0;
   if (tid == 0) {
     ptx::tc_fence_after();
@@ -582,6 +615,15 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       const uint64_t a = ptx::sdesc(KQ + ks * 2 * 2048, 2048, 128);
       const uint64_t b = ptx::sdesc(Bop + ks * 2 * b_cs, b_cs, 128);
       ptx::mma_bf16(tmem, a, b, id, ks > 0);
+    }
+    if (KDA && split) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        ptx::mma_bf16(tmem, ptx::sdesc(KQ + ks * 2 * 2048, 2048, 128),
+                      ptx::sdesc(KBL + ks * 2 * 1024, 1024, 128), id, 1);
+        ptx::mma_bf16(tmem, ptx::sdesc(KQL + ks * 2 * 2048, 2048, 128),
+                      ptx::sdesc(KB + ks * 2 * 1024, 1024, 128), id, 1);
+      }
     }
     ptx::mma_commit(&bars[1]);
   }
@@ -881,10 +923,38 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   volatile int *abort_flag = reinterpret_cast<int *>(bar + 12);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int vt = blockIdx.x;
+  // The CTA's chain.  Phase 0: value tile blockIdx.x of sequence blockIdx.z,
+  // all its chunks.  Segment-parallel pass (every sequence cut into
+  // seg_count segments of equal chunk counts): phase 1 runs every segment
+  // at once, grid x over K / 32 transition tiles then V / 32 value tiles --
+  // a transition tile starts from 32 columns of the identity with u = 0, so
+  // it ends on those columns of the segment's linear map M_s; a value tile
+  // starts from zero (segment 0: from h0, writing o), ending on B_s -- both
+  // stored to seg_state; phase 2 reruns segments 1.. from the start states
+  // the combine kernel formed (start_{s+1} = M_s start_s + B_s), writing o
+  // and, for the last segment, ht.
+  constexpr int KTILES = KD / VTILE;
+  int zz = blockIdx.z, seg = 0;
+  if (p.seg_phase == 1) {
+    seg = zz % p.seg_count;
+    zz /= p.seg_count;
+  } else if (p.seg_phase == 2) {
+    seg = zz % (p.seg_count - 1) + 1;
+    zz /= p.seg_count - 1;
+  }
+  bool trans = false;  // transition tile (phase 1)
+  int vt = blockIdx.x;
+  if (p.seg_phase == 1) {
+    if (vt < KTILES) {
+      if (seg == 0) return;  // segment 0 starts from h0: no map needed
+      trans = true;
+    } else {
+      vt -= KTILES;
+    }
+  }
   const int v0 = vt * VTILE;
   const int h = blockIdx.y;
-  const int n = p.cu_seqlens ? p.table[p.N + 1 + blockIdx.z] : (int)blockIdx.z;
+  const int n = p.cu_seqlens ? p.table[p.N + 1 + zz] : zz;
   int bos, eos, b, base;
   if (p.cu_seqlens) {
     bos = p.cu_seqlens[n];
@@ -898,7 +968,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     b = n;
     base = n * p.NT;
   }
-  const int nch = (eos - bos + BT - 1) / BT;
+  int cfirst = 0, nch = (eos - bos + BT - 1) / BT;
+  if (p.seg_phase != 0) {
+    const int per = (nch + p.seg_count - 1) / p.seg_count;
+    cfirst = min(seg * per, nch);
+    nch = min(per, nch - cfirst);
+  }
+  const bool write_o = p.seg_phase != 1 || seg == 0;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -926,12 +1002,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     // of chunk c (output GEMM of chunk c - 2), so waiting in the order
     // A(c), B(c), A(c + 1), ... never holds a release back.
     if (lane == 0) {
-      constexpr uint32_t A_BYTES = 32768 + 1024 + 8192, B_BYTES = 49152;
+      // a transition tile's u is zero: its U tile is not loaded
+      const uint32_t A_BYTES = 32768 + 1024 + (trans ? 0 : 8192), B_BYTES = 49152;
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1, k = c >> 1;
         unsigned char *st = smem + s * STAGE_BYTES;
-        const unsigned char *src = p.blocks + ((size_t)(base + c) * p.H + h) * p.block;
+        const unsigned char *src =
+            p.blocks + ((size_t)(base + cfirst + c) * p.H + h) * p.block;
         if (k > 0 && !ptx::mbar_wait_bounded(&emptyA[s], (uint32_t)((k - 1) & 1))) {
           record_error(p.err, GDN_ERR_TIMEOUT);  // keep going: no role may stall the others
           *abort_flag = 1;
@@ -939,7 +1017,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         ptx::mbar_arrive_expect_tx(&fullA[s], A_BYTES);
         ptx::bulk_g2s(st + S_AW, src + OFF_AW, 32768, &fullA[s]);
         ptx::bulk_g2s(st + S_SC, src + OFF_SC, 1024, &fullA[s]);
-        ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &fullA[s]);
+        if (!trans) ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &fullA[s]);
         if (k > 0 && !ptx::mbar_wait_bounded(&emptyB[s], (uint32_t)((k - 1) & 1))) {
           record_error(p.err, GDN_ERR_TIMEOUT);
           *abort_flag = 1;
@@ -1006,7 +1084,23 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     const int r = qd * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     float hs[16];
-    if (p.h0 && p.v_first) {
+    const bool from_h0 = p.seg_phase == 0 || (p.seg_phase == 1 && seg == 0);
+    if (trans) {
+      // columns v0 + c0 .. of the identity (key index = column)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hs[j] = (r == v0 + c0 + j) ? 1.f : 0.f;
+    } else if (p.seg_phase == 2) {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          p.seg_start + ((((size_t)n * p.seg_count + seg) * p.H + h) * KD + r) * p.V + v0 + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = src[q];
+        hs[4 * q] = x.x; hs[4 * q + 1] = x.y; hs[4 * q + 2] = x.z; hs[4 * q + 3] = x.w;
+      }
+    } else if (!from_h0) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hs[j] = 0.f;
+    } else if (p.h0 && p.v_first) {
       // [V, K]: the lanes of a warp read 32 consecutive keys of one value row
       const float *src = p.h0 + ((size_t)n * p.H + h) * KD * p.V + (size_t)(v0 + c0) * KD + r;
 #pragma unroll
@@ -1033,7 +1127,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     for (int c = 0; c < nch; ++c) {
       const int s = c & 1, k = c >> 1;
       const unsigned char *st = smem + s * STAGE_BYTES;
-      const int L = min(BT, eos - bos - c * BT);
+      const int L = min(BT, eos - bos - (cfirst + c) * BT);
       ok = ptx::mbar_wait_bounded(&fullA[s], (uint32_t)(k & 1)) && ok;
       const float *scs = reinterpret_cast<const float *>(st + S_SC);
       const float decay = scs[r];
@@ -1049,7 +1143,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
           float vn[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float4 u = u4[((c0 >> 2) + q) ^ (r & 7)];  // row-swizzled groups
+            const float4 u = trans ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                   : u4[((c0 >> 2) + q) ^ (r & 7)];  // row-swizzled groups
             vn[4 * q] = u.x + d[4 * q];
             vn[4 * q + 1] = u.y + d[4 * q + 1];
             vn[4 * q + 2] = u.z + d[4 * q + 2];
@@ -1090,13 +1185,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         for (int j = 0; j < 16; ++j) X[r * 33 + c0 + j] = d5v[j];
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (r >= 64) {
+      if (r >= 64 && write_o) {
         const int i = r - 64;
         if (i < L) {
           float ov[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) ov[j] = fmaf(qs, qh[j], d5v[j] + X[i * 33 + c0 + j]);
-          const size_t oi = ((size_t)(b * p.T + bos + c * BT + i) * p.H + h) * p.V + v0 + c0;
+          const size_t oi =
+              ((size_t)(b * p.T + bos + (cfirst + c) * BT + i) * p.H + h) * p.V + v0 + c0;
           if (p.o_f32) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + oi);
 #pragma unroll
@@ -1113,6 +1209,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     }
     if (!ok) {
       if (lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+    } else if (p.seg_phase == 1 && *abort_flag == 0) {
+      // row r of [M_s | B_s]: transition tiles fill columns 0 .. K - 1,
+      // value tiles columns K + v0 ..
+      const int W = KD + p.V, col = (trans ? v0 : KD + v0) + c0;
+      float4 *dst = reinterpret_cast<float4 *>(
+          p.seg_state + ((((size_t)n * p.seg_count + seg) * p.H + h) * KD + r) * W + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
+    } else if (p.seg_phase == 2 && seg != p.seg_count - 1) {
+      // an inner segment's end is the next one's start: already formed
     } else if (p.ht && *abort_flag == 0 && p.v_first) {
       float *dst = p.ht + ((size_t)n * p.H + h) * KD * p.V + (size_t)(v0 + c0) * KD + r;
 #pragma unroll
@@ -1127,6 +1234,65 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) ptx::tmem_dealloc<256>(tmem);
+}
+
+// ---------------------------------------------------------------------------
+// Segment combine (between the two phases of the segment-parallel pass): the
+// affine map of segment s takes its start state to M_s start + B_s, so
+//   start_1 = B_0 (segment 0's end, run from h0),
+//   start_{s+1} = M_s start_s + B_s          for s = 1 .. seg_count - 2,
+// in fp32 on the CUDA cores.  One CTA per (32-column value tile, head,
+// sequence), M_s staged in shared memory; thread t holds row t / 4, columns
+// 8 (t % 4) .. + 7 of the running start state.
+constexpr int COMB_THREADS = 512, COMB_LDM = KD + 1, COMB_LDC = VTILE + 1;
+constexpr uint32_t COMB_SMEM = (KD * COMB_LDM + KD * COMB_LDC) * 4;
+__global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(TcParams p) {
+  extern __shared__ float csm[];
+  float *Msm = csm;                  // M_s, [KD][COMB_LDM]
+  float *cur = csm + KD * COMB_LDM;  // start_s tile, [KD][COMB_LDC]
+  const int vt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int S = p.seg_count, W = KD + p.V, tid = threadIdx.x;
+  const int r = tid >> 2, cb = (tid & 3) * 8;
+  auto state = [&](int sg) {
+    return p.seg_state + (((size_t)n * S + sg) * p.H + h) * KD * W;
+  };
+  float acc[8];
+  {
+    const float4 *e0 = reinterpret_cast<const float4 *>(state(0) + (size_t)r * W + KD +
+                                                        vt * VTILE + cb);
+    const float4 a = e0[0], b = e0[1];
+    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+  }
+#pragma unroll 1
+  for (int sg = 1; sg < S; ++sg) {
+    float4 *dst = reinterpret_cast<float4 *>(
+        p.seg_start + ((((size_t)n * S + sg) * p.H + h) * KD + r) * p.V + vt * VTILE + cb);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (sg == S - 1) break;
+    __syncthreads();  // the previous step's readers are done
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cur[r * COMB_LDC + cb + j] = acc[j];
+    const float *Ms = state(sg);
+    for (int idx = tid; idx < KD * KD / 4; idx += COMB_THREADS) {
+      const int rr = idx / (KD / 4), c4 = idx % (KD / 4);
+      const float4 x = *reinterpret_cast<const float4 *>(Ms + (size_t)rr * W + 4 * c4);
+      float *m = Msm + rr * COMB_LDM + 4 * c4;
+      m[0] = x.x; m[1] = x.y; m[2] = x.z; m[3] = x.w;
+    }
+    __syncthreads();
+    const float4 *bs = reinterpret_cast<const float4 *>(Ms + (size_t)r * W + KD + vt * VTILE + cb);
+    const float4 b0 = bs[0], b1 = bs[1];
+    acc[0] = b0.x; acc[1] = b0.y; acc[2] = b0.z; acc[3] = b0.w;
+    acc[4] = b1.x; acc[5] = b1.y; acc[6] = b1.z; acc[7] = b1.w;
+#pragma unroll 4
+    for (int m = 0; m < KD; ++m) {
+      const float a = Msm[r * COMB_LDM + m];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(a, cur[m * COMB_LDC + cb + j], acc[j]);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1174,6 +1340,56 @@ bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long ro
 
 size_t table_bytes(int N) { return ((2 * (size_t)N + 1) * 4 + 255) / 256 * 256; }
 
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = 148;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Segments per sequence for the state pass: `requested` if given (>= 1),
+// else the count that shortens the sequential chain most while the first
+// phase's CTAs (one per SM) still fit on the GPU at once.  Cost in chain
+// steps: 2 ceil(nc / S) for the two phases, about one per combine step and
+// four for the two extra launches; taken only when it beats nc, so never
+// when the sequences' own chains already fill half the SMs.
+int segment_count(const ChunkParams &cp, bool varlen) {
+  if (cp.segments >= 1) return cp.segments;
+  const long long vtiles = cp.V / VTILE, ktiles = KD / VTILE;
+  const long long chains = vtiles * cp.H * cp.N;
+  const double nc = varlen ? (double)cp.T / cp.N / BT : (double)((cp.T + BT - 1) / BT);
+  const long long sms = sm_count();
+  if (2 * chains > sms || nc < 16.0) return 1;
+  int best = 1;
+  double best_cost = nc;
+  for (int S = 2; S <= 16; ++S) {
+    if ((long long)cp.H * cp.N * (vtiles + (S - 1) * (ktiles + vtiles)) > sms) break;
+    const double cost = 2.0 * std::ceil(nc / S) + (S - 2) + 4.0;
+    if (cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+size_t segment_bytes(const ChunkParams &cp, int S) {
+  if (S <= 1) return 0;
+  const size_t per = (size_t)cp.N * S * cp.H * KD;
+  return (per * (KD + cp.V) * 4 + 255) / 256 * 256 + (per * cp.V * 4 + 255) / 256 * 256;
+}
+
 size_t max_chunks(int B, int T, int N, bool varlen) {
   const size_t nt = ((size_t)T + BT - 1) / BT;
   return varlen ? nt + (size_t)N : (size_t)B * nt;
@@ -1185,10 +1401,15 @@ bool chunk_tc_supported(const ChunkParams &p, bool bf16) {
   return bf16 && p.K == tc::KD && p.V % tc::VTILE == 0 && p.V <= tc::VMAX && p.T > 0;
 }
 
+int chunk_tc_segments(const ChunkParams &p) {
+  return tc::segment_count(p, p.cu_seqlens != nullptr);
+}
+
 size_t chunk_tc_workspace(const ChunkParams &p, bool kda) {
   const bool varlen = p.cu_seqlens != nullptr;
   return tc::table_bytes(p.N) +
-         tc::max_chunks(p.B, p.T, p.N, varlen) * (size_t)p.H * tc::block_bytes(p.V, kda);
+         tc::max_chunks(p.B, p.T, p.N, varlen) * (size_t)p.H * tc::block_bytes(p.V, kda) +
+         tc::segment_bytes(p, tc::segment_count(p, varlen));
 }
 
 cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStream_t stream) {
@@ -1221,6 +1442,16 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   p.v_first = cp.v_first;
   p.scale = cp.scale;
   p.block = block_bytes(cp.V, kda);
+  const int S = segment_count(cp, varlen);
+  p.seg_count = S;
+  p.seg_phase = 0;
+  if (S > 1) {
+    const size_t nchunks_all = max_chunks(cp.B, cp.T, cp.N, varlen);
+    unsigned char *seg = p.blocks + nchunks_all * (size_t)cp.H * p.block;
+    const size_t per = (size_t)cp.N * S * cp.H * KD;
+    p.seg_state = reinterpret_cast<float *>(seg);
+    p.seg_start = reinterpret_cast<float *>(seg + (per * (KD + cp.V) * 4 + 255) / 256 * 256);
+  }
   if (varlen) {
     chunk_table_kernel<<<1, TABLE_THREADS, 0, stream>>>(cp.cu_seqlens, cp.N, cp.T, p.table, cp.err);
     cudaError_t e = cudaGetLastError();
@@ -1236,7 +1467,22 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(p);
+  if (S <= 1) {
+    chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // segment-parallel: every segment at once (transition and value tiles),
+  // the combine, then segments 1.. again from their true start states
+  p.seg_phase = 1;
+  chain_kernel<<<dim3(KD / VTILE + cp.V / VTILE, cp.H, cp.N * S), CHAIN_THREADS, C_SMEM, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)COMB_SMEM);
+  if (e != cudaSuccess) return e;
+  segment_combine_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), COMB_THREADS, COMB_SMEM, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  p.seg_phase = 2;
+  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N * (S - 1)), CHAIN_THREADS, C_SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -299,7 +299,9 @@ __device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, u
   ptx::mbar_arrive(prep);  // each lane releases its own writes
 }
 
-template <int T>
+// F32: the variant that writes o in fp32 (p.o_f32) and/or the fp32 updated
+// states (p.state_f32); the default variant is compiled without either.
+template <int T, bool F32>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
   using L = DecodeSmem<T>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
 #pragma unroll
           for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[s2], ov);
           const size_t oi = (((size_t)bi * T + t) * HV + hv) * DV + rg + 32 * rsel;
-          if (p.o_f32)
+          if (F32 && p.o_f32)
             static_cast<float *>(p.o)[oi] = ov;
           else
             o[oi] = __float2bfloat16_rn(ov);
@@ -491,14 +493,14 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
       for (int idx = tid; idx < T * DV; idx += DTHREADS) {
         const size_t oi = (((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV;
-        if (p.o_f32)
+        if (F32 && p.o_f32)
           static_cast<float *>(p.o)[oi] = 0.f;
         else
           o[oi] = __float2bfloat16_rn(0.f);
       }
     } else {
       __nv_bfloat16 *dst = state + ((size_t)slot * HV + hv) * DV * DK;
-      if (p.state_f32) {
+      if (F32 && p.state_f32) {
         // the fp32 values the bf16 write-back rounds (entry bi, not its slot)
         float *d32 = p.state_f32 + ((size_t)bi * HV + hv) * DV * DK;
 #pragma unroll
@@ -549,22 +551,28 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int T>
-cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
+template <int T, bool F32>
+cudaError_t launch_tf(const DecodeParams &p, cudaStream_t stream) {
   const size_t bytes = DecodeSmem<T>::BYTES;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, F32>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   // persistent grid: as many CTAs as are resident at once (two per SM)
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T>, DTHREADS, bytes);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T, F32>, DTHREADS,
+                                                    bytes);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int items = p.B * p.HV;
   const int cap = per_sm * sm_count();
   const int grid = items < cap ? items : cap;
-  decode_kernel<T><<<grid, DTHREADS, bytes, stream>>>(p);
+  decode_kernel<T, F32><<<grid, DTHREADS, bytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int T>
+cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
+  return (p.o_f32 || p.state_f32) ? launch_tf<T, true>(p, stream) : launch_tf<T, false>(p, stream);
 }
 
 }  // namespace

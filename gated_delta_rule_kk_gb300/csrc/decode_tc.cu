@@ -270,7 +270,9 @@ __device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, u
   ptx::mbar_arrive(prep);  // each lane releases its own writes
 }
 
-template <int T>
+// F32: the variant that writes o in fp32 (p.o_f32) and/or the fp32 updated
+// states (p.state_f32); the default variant is compiled without either.
+template <int T, bool F32>
 __global__ void __launch_bounds__(NTHREADS, 2)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constant__ CUtensorMap tm_st,
                  DecodeParams p) {
@@ -410,7 +412,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
 #pragma unroll
             for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[h][s2], ov);
             const size_t oi = (((size_t)bi * T + t) * HV + hv) * DV + row;
-            if (p.o_f32)
+            if (F32 && p.o_f32)
               static_cast<float *>(p.o)[oi] = ov;
             else
               o[oi] = __float2bfloat16_rn(ov);
@@ -475,7 +477,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
     }
     order = __shfl_sync(0xffffffffu, order, 0);
 
-    if (slot >= 0 && p.state_f32) {
+    if (F32 && slot >= 0 && p.state_f32) {
       // the fp32 values the bf16 write-back rounds (entry bi, not its slot):
       // rows r0 + g and r0 + g + 8, columns 8 n + 2 tig (+ 1)
       float *d32 = p.state_f32 + ((size_t)bi * HV + hv) * DV * DK;
@@ -506,7 +508,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
       for (int idx = tid; idx < T * DV; idx += NTHREADS) {
         const size_t oi = (((size_t)bi * T + idx / DV) * HV + hv) * DV + idx % DV;
-        if (p.o_f32)
+        if (F32 && p.o_f32)
           static_cast<float *>(p.o)[oi] = 0.f;
         else
           o[oi] = __float2bfloat16_rn(0.f);
@@ -574,25 +576,30 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int T>
-cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
+template <int T, bool F32>
+cudaError_t launch_tf(const DecodeParams &p, cudaStream_t stream) {
   CUtensorMap ld, stm;
   const long long rows = (long long)p.pool * p.HV * DV;
   if (!make_state_map(&ld, p.state, rows, 128) || !make_state_map(&stm, p.state, rows, 16))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T>,
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, F32>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel<T>, NTHREADS,
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel<T, F32>, NTHREADS,
                                                     SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int items = p.B * p.HV;
   const int cap = per_sm * sm_count();
   const int grid = items < cap ? items : cap;
-  decode_tc_kernel<T><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ld, stm, p);
+  decode_tc_kernel<T, F32><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ld, stm, p);
   return cudaGetLastError();
+}
+
+template <int T>
+cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
+  return (p.o_f32 || p.state_f32) ? launch_tf<T, true>(p, stream) : launch_tf<T, false>(p, stream);
 }
 
 }  // namespace

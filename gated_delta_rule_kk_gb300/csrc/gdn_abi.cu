@@ -55,7 +55,7 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
                          const float *g, const float *beta, const float *h0, const float *ht,
                          const void *o, const int32_t *cu, int B, int T, int Hk, int Hv, int K,
                          int V, int N, int chunk_size, int g_is_cumsum, int v_first,
-                         int o_f32, float scale, const char *hk_name,
+                         int o_f32, int segments, float scale, const char *hk_name,
                          bool sizes_only = false) {
   REQUIRE(dtype == GDN_F32 || dtype == GDN_BF16, GDN_ERR_INVALID_ARG, "dtype %d is not GDN_F32/GDN_BF16", dtype);
   REQUIRE(B >= 1 && T >= 0 && Hk >= 1 && Hv >= 1 && K >= 1 && V >= 1 && N >= 1,
@@ -70,6 +70,10 @@ gdn_status_t check_chunk(int32_t dtype, const void *q, const void *k, const void
   REQUIRE(g_is_cumsum == 0 || g_is_cumsum == 1, GDN_ERR_INVALID_ARG, "g_is_cumsum must be 0 or 1");
   REQUIRE(v_first == 0 || v_first == 1, GDN_ERR_INVALID_ARG, "state_v_first must be 0 or 1");
   REQUIRE(o_f32 == 0 || o_f32 == 1, GDN_ERR_INVALID_ARG, "o_fp32 must be 0 or 1");
+  REQUIRE(segments >= 0, GDN_ERR_INVALID_ARG, "segments must not be negative");
+  REQUIRE(segments <= MAX_SEGMENTS && (long long)N * (segments > 0 ? segments : 1) <= MAX_GRID_YZ,
+          GDN_ERR_UNSUPPORTED, "segments (%d) must be at most %d and N * segments at most %d",
+          segments, MAX_SEGMENTS, MAX_GRID_YZ);
   REQUIRE(isfinite(scale), GDN_ERR_INVALID_ARG, "scale must be finite");
   if (cu == nullptr) {
     REQUIRE(N == B, GDN_ERR_INVALID_ARG, "without cu_seqlens N (%d) must equal B (%d)", N, B);
@@ -116,6 +120,7 @@ ChunkParams gdn_params(const gdn_chunk_args &a) {
   p.g_is_cumsum = a.g_is_cumsum;
   p.v_first = a.state_v_first;
   p.o_f32 = a.o_fp32 || a.dtype == GDN_F32;
+  p.segments = a.segments;
   p.scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)(a.K > 0 ? a.K : 1));
   return p;
 }
@@ -128,6 +133,7 @@ ChunkParams kda_params(const kda_chunk_args &a) {
   p.g_is_cumsum = a.g_is_cumsum;
   p.v_first = a.state_v_first;
   p.o_f32 = a.o_fp32 || a.dtype == GDN_F32;
+  p.segments = a.segments;
   p.scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)(a.K > 0 ? a.K : 1));
   return p;
 }
@@ -156,8 +162,8 @@ gdn_status_t check_gdn_chunk_sizes(const gdn_chunk_args &a) {
   g_msg[0] = '\0';
   return check_chunk(a.dtype, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                      nullptr, a.cu_seqlens, a.B, a.T, a.Hg, a.H, a.K, a.V,
-                     a.N, a.chunk_size, a.g_is_cumsum, a.state_v_first, a.o_fp32, a.scale, "Hg",
-                     true);
+                     a.N, a.chunk_size, a.g_is_cumsum, a.state_v_first, a.o_fp32, a.segments,
+                     a.scale, "Hg", true);
 }
 
 gdn_status_t set_host_error(gdn_status_t st, const char *msg) { return fail(st, "%s", msg); }
@@ -193,6 +199,16 @@ gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *a, size_t *bytes) {
   return GDN_OK;
 }
 
+gdn_status_t gdn_chunk_segment_count(const gdn_chunk_args *a, int32_t *segments) {
+  if (a == nullptr || segments == nullptr) return fail(GDN_ERR_INVALID_ARG, "NULL argument");
+  *segments = 1;
+  gdn_status_t st = check_gdn_chunk_sizes(*a);
+  if (st != GDN_OK) return st;
+  ChunkParams p = gdn_params(*a);
+  if (chunk_tc_supported(p, a->dtype == GDN_BF16)) *segments = chunk_tc_segments(p);
+  return GDN_OK;
+}
+
 gdn_status_t kda_chunk_workspace_size(const kda_chunk_args *a, size_t *bytes) {
   if (a == nullptr || bytes == nullptr) return fail(GDN_ERR_INVALID_ARG, "NULL argument");
   *bytes = 0;
@@ -207,7 +223,7 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *a, gdn_stream_t stream) {
   gdn_status_t st = check_chunk(a->dtype, a->q, a->k, a->v, a->g, a->beta, a->h0, a->ht, a->o,
                                 a->cu_seqlens, a->B, a->T, a->Hg, a->H, a->K, a->V, a->N,
                                 a->chunk_size, a->g_is_cumsum, a->state_v_first, a->o_fp32,
-                                a->scale, "Hg");
+                                a->segments, a->scale, "Hg");
   if (st != GDN_OK) return st;
   ChunkParams p = gdn_params(*a);
   return run_chunk(p, a->dtype == GDN_BF16, false, a->workspace, a->workspace_bytes,
@@ -220,7 +236,7 @@ gdn_status_t kda_chunk_fwd(const kda_chunk_args *a, gdn_stream_t stream) {
   gdn_status_t st = check_chunk(a->dtype, a->q, a->k, a->v, a->g, a->beta, a->h0, a->ht, a->o,
                                 a->cu_seqlens, a->B, a->T, a->H, a->HV, a->K, a->V, a->N,
                                 a->chunk_size, a->g_is_cumsum, a->state_v_first, a->o_fp32,
-                                a->scale, "H");
+                                a->segments, a->scale, "H");
   if (st != GDN_OK) return st;
   ChunkParams p = kda_params(*a);
   return run_chunk(p, a->dtype == GDN_BF16, true, a->workspace, a->workspace_bytes,

@@ -15,6 +15,8 @@ constexpr int BT = 64;
 constexpr int KMAX = 128;
 // Largest grid y / z dimension of a launch: heads and sequences index them.
 constexpr int MAX_GRID_YZ = 65535;
+// Most segments per sequence of the segment-parallel state pass.
+constexpr int MAX_SEGMENTS = 64;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

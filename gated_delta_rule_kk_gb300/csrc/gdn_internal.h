@@ -22,6 +22,7 @@ struct ChunkParams {
   int g_is_cumsum;
   int v_first;                // h0, ht as [V, K] instead of [K, V]
   int o_f32;                  // o written as float32 (else in the input dtype)
+  int segments;               // state pass segments: 0 = choose, 1 = none, >= 2
   float scale;
 };
 
@@ -76,6 +77,8 @@ bool chunk_tc_supported(const ChunkParams &p, bool bf16);
 size_t chunk_tc_workspace(const ChunkParams &p, bool per_channel_gate);
 cudaError_t launch_chunk_tc(const ChunkParams &p, bool per_channel_gate, void *workspace,
                             cudaStream_t stream);
+// Segments per sequence the tensor-core state pass uses for these arguments.
+int chunk_tc_segments(const ChunkParams &p);
 
 // The checks of gdn_chunk_fwd that read only sizes, dtype and flags (no
 // pointer is dereferenced; cu_seqlens only counts as given or NULL).

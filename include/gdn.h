@@ -99,6 +99,17 @@ typedef enum gdn_dtype {
  * caller-owned, contents irrelevant before and after the call) of at least
  * gdn_chunk_workspace_size() bytes, else GDN_ERR_WORKSPACE.  Every other
  * shape runs the exact fp32 CUDA-core kernel and needs none.
+ * Segment-parallel state pass (tensor-core path; `segments`): the chunk
+ * recurrence h <- M_c h + B_c is affine in h, so with S >= 2 every sequence
+ * is cut into S runs of ceil(chunks / S) chunks that are all processed at
+ * once -- each from a zero state and on the identity, which gives the run's
+ * map (M, B) -- then combined in order (start of run s + 1 = M start_s + B)
+ * and run again from their true starts, writing o.  The sequential part
+ * shrinks from `chunks` to about 2 chunks / S steps, at about three times
+ * the work; it pays when the sequences' own chains (V / 32 per head and
+ * sequence) leave most SMs idle.  0 lets the library choose (1 unless that
+ * holds); the fp32 CUDA-core kernel ignores it.  1 <= segments <= 64 and
+ * N * segments <= 65535, else GDN_ERR_UNSUPPORTED.
  */
 typedef struct gdn_chunk_args {
   int32_t dtype;               /* gdn_dtype_t of q, k, v, o */
@@ -113,6 +124,8 @@ typedef struct gdn_chunk_args {
   int32_t g_is_cumsum;
   int32_t state_v_first;       /* 1: h0, ht are [N, H, V, K] instead of [N, H, K, V] */
   int32_t o_fp32;              /* 1: o is float32 whatever dtype is; 0: o has dtype */
+  int32_t segments;            /* state pass: 0 = library's choice, 1 = one chain per
+                                  sequence, 2..64 = segment-parallel (see above) */
   float scale;
   void *workspace;
   size_t workspace_bytes;
@@ -122,6 +135,12 @@ typedef struct gdn_chunk_args {
  * CUDA-core kernel serves them).  Reads only sizes, dtype and whether
  * cu_seqlens is NULL. */
 gdn_status_t gdn_chunk_workspace_size(const gdn_chunk_args *args, size_t *bytes);
+
+/* The segment count gdn_chunk_fwd would use for the state pass with these
+ * arguments (args->segments, or the library's choice when it is 0; 1 when
+ * the exact fp32 CUDA-core kernel serves them).  Reads only sizes, dtype,
+ * segments and whether cu_seqlens is NULL. */
+gdn_status_t gdn_chunk_segment_count(const gdn_chunk_args *args, int32_t *segments);
 
 /* Enqueue the GDN chunked forward (gate cumsum, intra-chunk (I+A)^-1 with the
  * WY vectors w, u, the sequential inter-chunk state pass and the output) on
@@ -298,6 +317,7 @@ typedef struct kda_chunk_args {
   int32_t g_is_cumsum;
   int32_t state_v_first;       /* 1: h0, ht are [N, HV, V, K] instead of [N, HV, K, V] */
   int32_t o_fp32;              /* 1: o is float32 whatever dtype is; 0: o has dtype */
+  int32_t segments;            /* as gdn_chunk_args.segments */
   float scale;
   void *workspace;
   size_t workspace_bytes;

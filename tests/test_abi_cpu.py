@@ -13,6 +13,7 @@ import subprocess
 import tempfile
 
 import pytest
+import torch
 
 from gated_delta_rule_kk_gb300 import _lib, build_lib
 from gated_delta_rule_kk_gb300._lib import (GdnChunkArgs, GdnDecodeArgs, GdnStateArgs,
@@ -330,3 +331,32 @@ def test_chunk_state_v_first_flag_is_checked(lib):
             a.H, a.HV = 1, 1
         assert getattr(lib, fn)(ctypes.byref(a), None) == Status.INVALID_ARG
         assert b"state_v_first" in lib.gdn_last_error_message()
+
+
+def test_segments_range_is_checked(lib):
+    base = dict(dtype=1, q=0x10000, k=0x10000, v=0x10000, g=0x10000, beta=0x10000, o=0x10000,
+                B=1, T=64, H=1, Hg=1, K=128, V=128, N=1, chunk_size=64)
+    a = GdnChunkArgs(segments=-1, **base)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.INVALID_ARG
+    a = GdnChunkArgs(segments=65, **base)
+    assert lib.gdn_chunk_fwd(ctypes.byref(a), None) == Status.UNSUPPORTED
+    a = GdnChunkArgs(segments=4, **base)
+    n4, n1 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n4)) == Status.OK
+    a.segments = 1
+    assert lib.gdn_chunk_workspace_size(ctypes.byref(a), ctypes.byref(n1)) == Status.OK
+    # the segment scratch: per (sequence, segment, head) a [K, K + V] and a [K, V] fp32 state
+    assert n4.value - n1.value == 4 * 128 * (256 + 128) * 4
+
+
+def test_segment_count_choice(lib):
+    """The library's own choice: none for the benchmarked shapes (their chains
+    already fill the SMs), the segment-parallel pass for one long sequence
+    with few heads; an explicit count is returned as given."""
+    import gated_delta_rule_kk_gb300 as gdn
+    assert gdn.gdn_chunk_segment_count(2, 4096, 16, 16, 128, 128) == 1
+    assert gdn.gdn_chunk_segment_count(1, 8192, 32, 32, 128, 128) == 1
+    assert gdn.gdn_chunk_segment_count(1, 8192, 1, 1, 128, 128) > 1
+    assert gdn.gdn_chunk_segment_count(1, 8192, 2, 2, 128, 128, segments=3) == 3
+    assert gdn.gdn_chunk_segment_count(1, 8192, 1, 1, 64, 64, dtype=torch.float32) == 1
+    assert gdn.gdn_chunk_segment_count(1, 300, 1, 1, 128, 128) == 1  # too few chunks
