@@ -77,6 +77,10 @@ int64_t piece_rows(const Plan &L, const Piece &p) {
 gdn_chunk_args piece_args(const gdn_chunk_args &a, const Plan &L, int j, unsigned char *base) {
   const Piece &p = L.pc[j];
   gdn_chunk_args d = a;
+  // the pieces' state passes run one chain per sequence, as gdn_chunk_fwd
+  // with segments = 1 does: a time cut hands the state on exactly as a chunk
+  // boundary inside one chain does
+  d.segments = 1;
   d.B = L.varlen ? 1 : p.n1 - p.n0;
   d.T = (int32_t)(p.t1 - p.t0);
   d.N = p.n1 - p.n0;

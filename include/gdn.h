@@ -163,10 +163,11 @@ gdn_status_t gdn_chunk_fwd(const gdn_chunk_args *args, gdn_stream_t stream);
  * towards the end) or into ranges of whole sequences, and each piece's host->device copies, kernels
  * and device->host copies run on an internal copy-in stream, `stream` and an
  * internal copy-out stream, so the copies of one piece overlap the kernels of
- * its neighbours.  The results equal gdn_chunk_fwd's bit for bit: a time cut
- * hands the fp32 state of the chunkwise recurrence (Gated Delta Networks,
- * section 3) from one piece to the next exactly as the kernels carry it
- * between chunks.
+ * its neighbours.  The state pass runs one chain per sequence (`segments`
+ * is ignored), and the results equal gdn_chunk_fwd's with segments = 1 bit
+ * for bit: a time cut hands the fp32 state of the chunkwise recurrence (Gated
+ * Delta Networks, section 3) from one piece to the next exactly as the
+ * kernels carry it between chunks.
  * Errors: argument errors as gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG when an
  * input or output pointer is device memory, GDN_ERR_WORKSPACE when the
  * workspace is missing, too small or not device memory, GDN_ERR_BAD_SEQLENS

@@ -99,6 +99,7 @@ int main(int argc, char **argv) {
   a.chunk_size = 64;
   a.g_is_cumsum = 0;
   a.scale = scale;
+  a.segments = 1; /* one chain per sequence, as the host entry point runs it */
   size_t ws_bytes = 0;
   GDN_OK_OR_FAIL(gdn_chunk_workspace_size(&a, &ws_bytes));
   if (ws_bytes) CUDA_OK(cudaMalloc(&ws, ws_bytes));

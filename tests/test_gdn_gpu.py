@@ -251,7 +251,7 @@ def test_state_v_first_host_entry_point():
     d = to_dev(inp)
     h0t = inp["h0"].transpose(-1, -2).contiguous()
     o1, ht1 = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
-                            initial_state=h0t.cuda(), state_v_first=True)
+                            initial_state=h0t.cuda(), state_v_first=True, segments=1)
     o2, ht2 = gdn.gdn_chunk_fwd_host(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                      scale=inp["scale"], initial_state=h0t.pin_memory(),
                                      state_v_first=True)

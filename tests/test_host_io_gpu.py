@@ -26,7 +26,7 @@ def _device(inp, h0=True):
     d = to_dev(inp)
     o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
                               initial_state=d["h0"] if h0 else None, cu_seqlens=d["cu_seqlens"],
-                              g_is_cumsum=d["g_is_cumsum"])
+                              g_is_cumsum=d["g_is_cumsum"], segments=1)
     torch.cuda.synchronize()
     assert gdn.gdn_check_device_error() == Status.OK
     return o.cpu(), ht.cpu()
@@ -127,7 +127,7 @@ def test_device_pointers_are_rejected():
     a.workspace = vp(ws)
     assert lib.gdn_chunk_fwd_host(ctypes.byref(a), None) == Status.OK
     torch.cuda.synchronize()
-    o_d, _ = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"])
+    o_d, _ = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], segments=1)
     _same(host_o, o_d.cpu(), "o")
 
 
@@ -136,7 +136,7 @@ def test_fp32_output_from_host_buffers_equals_device_entry_point():
     inp = synth.prefill_inputs(97, 2, 1500, 2, 1, 128, 128, h0_std=0.1)
     d = to_dev(inp)
     o_d, ht_d = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d["scale"],
-                                  initial_state=d["h0"], out_dtype=torch.float32)
+                                  initial_state=d["h0"], out_dtype=torch.float32, segments=1)
     o_h, ht_h = gdn.gdn_chunk_fwd_host(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                        scale=inp["scale"], initial_state=inp["h0"],
                                        out_dtype=torch.float32)
