@@ -1270,57 +1270,69 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
 // affine map of segment s takes its start state to M_s start + B_s, so
 //   start_1 = B_0 (segment 0's end, run from h0),
 //   start_{s+1} = M_s start_s + B_s          for s = 1 .. seg_count - 2,
-// in fp32 on the CUDA cores.  One CTA per (32-column value tile, head,
-// sequence), M_s staged in shared memory; thread t holds row t / 4, columns
-// 8 (t % 4) .. + 7 of the running start state.
-constexpr int COMB_THREADS = 512, COMB_LDM = KD + 1, COMB_LDC = VTILE + 1;
-constexpr uint32_t COMB_SMEM = (KD * COMB_LDM + KD * COMB_LDC) * 4;
+// in fp32 on the CUDA cores.  Every M_s and B_s is known when the kernel
+// starts, so only the running state is sequential: one CTA per (8-column
+// value tile, head, sequence), thread t holding row t / 2, columns
+// 4 (t % 2) .. + 3 of it; M_{s+1} streams into the other of two shared-memory
+// buffers (cp.async) while step s computes.
+constexpr int COMB_THREADS = 256, COMB_COLS = 8, COMB_LDM = KD + 4;
+constexpr uint32_t COMB_SMEM = (2 * KD * COMB_LDM + KD * COMB_COLS) * 4;
 __global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(TcParams p) {
-  extern __shared__ float csm[];
-  float *Msm = csm;                  // M_s, [KD][COMB_LDM]
-  float *cur = csm + KD * COMB_LDM;  // start_s tile, [KD][COMB_LDC]
-  const int vt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  extern __shared__ __align__(16) float csm[];
+  float *X = csm + 2 * KD * COMB_LDM;  // the running state's tile, [KD][COMB_COLS]
+  const int h = blockIdx.y, n = blockIdx.z;
   const int S = p.seg_count, W = KD + p.V, tid = threadIdx.x;
-  const int r = tid >> 2, cb = (tid & 3) * 8;
+  const int r = tid >> 1, cq = (tid & 1) * 4, col = blockIdx.x * COMB_COLS + cq;
   auto state = [&](int sg) {
     return p.seg_state + (((size_t)n * S + sg) * p.H + h) * KD * W;
   };
-  float acc[8];
-  {
-    const float4 *e0 = reinterpret_cast<const float4 *>(state(0) + (size_t)r * W + KD +
-                                                        vt * VTILE + cb);
-    const float4 a = e0[0], b = e0[1];
-    acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-    acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+  auto stage_m = [&](int sg) {  // M_sg into buffer sg & 1
+    const float *Ms = state(sg);
+    float *dst = csm + (sg & 1) * KD * COMB_LDM;
+    for (int idx = tid; idx < KD * KD / 4; idx += COMB_THREADS) {
+      const int rr = idx >> 5, c4 = idx & 31;
+      ptx::cp_async16(dst + rr * COMB_LDM + 4 * c4, Ms + (size_t)rr * W + 4 * c4, true);
+    }
+    ptx::cp_async_commit();
+  };
+  float4 acc = *reinterpret_cast<const float4 *>(state(0) + (size_t)r * W + KD + col);
+  float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (S > 2) {
+    stage_m(1);
+    bnext = *reinterpret_cast<const float4 *>(state(1) + (size_t)r * W + KD + col);
   }
 #pragma unroll 1
   for (int sg = 1; sg < S; ++sg) {
-    float4 *dst = reinterpret_cast<float4 *>(
-        p.seg_start + ((((size_t)n * S + sg) * p.H + h) * KD + r) * p.V + vt * VTILE + cb);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    *reinterpret_cast<float4 *>(
+        p.seg_start + ((((size_t)n * S + sg) * p.H + h) * KD + r) * p.V + col) = acc;
     if (sg == S - 1) break;
-    __syncthreads();  // the previous step's readers are done
-#pragma unroll
-    for (int j = 0; j < 8; ++j) cur[r * COMB_LDC + cb + j] = acc[j];
-    const float *Ms = state(sg);
-    for (int idx = tid; idx < KD * KD / 4; idx += COMB_THREADS) {
-      const int rr = idx / (KD / 4), c4 = idx % (KD / 4);
-      const float4 x = *reinterpret_cast<const float4 *>(Ms + (size_t)rr * W + 4 * c4);
-      float *m = Msm + rr * COMB_LDM + 4 * c4;
-      m[0] = x.x; m[1] = x.y; m[2] = x.z; m[3] = x.w;
+    const float4 b = bnext;
+    __syncthreads();  // the previous step is done with X and with the buffer refilled next
+    *reinterpret_cast<float4 *>(X + r * COMB_COLS + cq) = acc;
+    if (sg + 1 < S - 1) {
+      stage_m(sg + 1);
+      bnext = *reinterpret_cast<const float4 *>(state(sg + 1) + (size_t)r * W + KD + col);
+      ptx::cp_async_wait<1>();  // M_sg has landed
+    } else {
+      ptx::cp_async_wait<0>();
     }
     __syncthreads();
-    const float4 *bs = reinterpret_cast<const float4 *>(Ms + (size_t)r * W + KD + vt * VTILE + cb);
-    const float4 b0 = bs[0], b1 = bs[1];
-    acc[0] = b0.x; acc[1] = b0.y; acc[2] = b0.z; acc[3] = b0.w;
-    acc[4] = b1.x; acc[5] = b1.y; acc[6] = b1.z; acc[7] = b1.w;
+    const float *mrow = csm + (sg & 1) * KD * COMB_LDM + r * COMB_LDM;
+    float a0 = b.x, a1 = b.y, a2 = b.z, a3 = b.w;
 #pragma unroll 4
-    for (int m = 0; m < KD; ++m) {
-      const float a = Msm[r * COMB_LDM + m];
+    for (int m = 0; m < KD; m += 4) {
+      const float4 mv = *reinterpret_cast<const float4 *>(mrow + m);
+      const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(a, cur[m * COMB_LDC + cb + j], acc[j]);
+      for (int e = 0; e < 4; ++e) {
+        const float4 x = *reinterpret_cast<const float4 *>(X + (m + e) * COMB_COLS + cq);
+        a0 = fmaf(mm[e], x.x, a0);
+        a1 = fmaf(mm[e], x.y, a1);
+        a2 = fmaf(mm[e], x.z, a2);
+        a3 = fmaf(mm[e], x.w, a3);
+      }
     }
+    acc = make_float4(a0, a1, a2, a3);
   }
 }
 
@@ -1390,9 +1402,9 @@ int sm_count() {
 // Segments per sequence for the state pass: `requested` if given (>= 1),
 // else the count that shortens the sequential chain most while the first
 // phase's CTAs (one per SM) still fit on the GPU at once.  Cost in chain
-// steps: 2 ceil(nc / S) for the two phases, about one per combine step and
-// four for the two extra launches; taken only when it beats nc, so never
-// when the sequences' own chains already fill half the SMs.
+// steps: 2 ceil(nc / S) for the two phases, about half a step per combine
+// step and four for the two extra launches; taken only when it beats nc, so
+// never when the sequences' own chains already fill half the SMs.
 int segment_count(const ChunkParams &cp, bool varlen) {
   if (cp.segments >= 1) return cp.segments;
   const long long vtiles = cp.V / VTILE, ktiles = KD / VTILE;
@@ -1404,7 +1416,7 @@ int segment_count(const ChunkParams &cp, bool varlen) {
   double best_cost = nc;
   for (int S = 2; S <= 16; ++S) {
     if ((long long)cp.H * cp.N * (vtiles + (S - 1) * (ktiles + vtiles)) > sms) break;
-    const double cost = 2.0 * std::ceil(nc / S) + (S - 2) + 4.0;
+    const double cost = 2.0 * std::ceil(nc / S) + 0.5 * (S - 2) + 4.0;
     if (cost < best_cost) {
       best = S;
       best_cost = cost;
@@ -1508,7 +1520,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)COMB_SMEM);
   if (e != cudaSuccess) return e;
-  segment_combine_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), COMB_THREADS, COMB_SMEM, stream>>>(p);
+  segment_combine_kernel<<<dim3(cp.V / COMB_COLS, cp.H, cp.N), COMB_THREADS, COMB_SMEM, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.seg_phase = 2;
   chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N * (S - 1)), CHAIN_THREADS, C_SMEM, stream>>>(p);
