@@ -863,20 +863,15 @@ constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 65536, S_SC = 81920, S_U = 829
                    STAGE_BYTES = 91136;
 constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_X = C_VN + 8192,
                    C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
-// The critical-path GEMMs' K slices are split between MMA_ISSUERS warps, each
-// into its own accumulator (tcgen05.mma costs about as much to issue as to
-// run at these sizes, so issuing from two warps shortens the step).
-constexpr int MMA_ISSUERS = 2;
+constexpr int CHAIN_THREADS = 320;
 constexpr int EPI_WARPS = 8;
-constexpr int CHAIN_THREADS = 32 * (EPI_WARPS + 1 + MMA_ISSUERS);
 // Named barriers of the chain kernel (1 is the epilogue warps' own).  The
 // epilogue warps arrive (without waiting) once h, or v_new, is in shared
 // memory; the MMA warp waits on them.  Each phase's arrivals depend on MMAs
 // the MMA warp issues only after it passed the previous phase, so phases
 // never overlap; every role runs every chunk, so every phase completes.
-constexpr int BAR_HREADY = 2, BAR_HREADY_THREADS = 32 * (EPI_WARPS + MMA_ISSUERS);
-// warps 0, 1, 4, 5 (the v_new rows) + the MMA warps
-constexpr int BAR_VNREADY = 3, BAR_VNREADY_THREADS = 32 * (4 + MMA_ISSUERS);
+constexpr int BAR_HREADY = 2, BAR_HREADY_THREADS = 32 * (EPI_WARPS + 1);
+constexpr int BAR_VNREADY = 3, BAR_VNREADY_THREADS = 32 * (4 + 1);  // warps 0, 1, 4, 5 + MMA
 
 __device__ __forceinline__ void bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -891,23 +886,13 @@ __device__ __forceinline__ uint64_t adv(uint64_t desc, uint32_t bytes) {
 }
 
 // columns [c0, c0 + 16) of a 64-column accumulator holding the hi product in
-// columns 0..31 and the lo product in 32..63, summed (both loads in flight
-// together)
+// columns 0..31 and the lo product in 32..63, summed
 __device__ __forceinline__ void tmem_ld_pair16(uint32_t taddr, int c0, float *v) {
   float lo[16];
-  ptx::tmem_ld16x2(taddr + c0, taddr + 32 + c0, v, lo);
+  ptx::tmem_ld16(taddr + c0, v);
+  ptx::tmem_ld16(taddr + 32 + c0, lo);
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] += lo[j];
-}
-
-// the same for the sum of two such accumulators (the halves of a product
-// whose K slices two MMA warps issued)
-__device__ __forceinline__ void tmem_ld_pair16_2(uint32_t ta, uint32_t tb, int c0, float *v) {
-  float v1[16], v2[16], v3[16];
-  ptx::tmem_ld16x2(ta + c0, ta + 32 + c0, v, v1);
-  ptx::tmem_ld16x2(tb + c0, tb + 32 + c0, v2, v3);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] += v1[j] + (v2[j] + v3[j]);
 }
 
 // 16 values -> hi/lo bf16 halves of an image with column-group stride cs
@@ -994,24 +979,22 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&fullA[i], 1);
-      ptx::mbar_init(&emptyA[i], MMA_ISSUERS + EPI_WARPS);
+      ptx::mbar_init(&emptyA[i], 1 + EPI_WARPS);
       ptx::mbar_init(&fullB[i], 1);
-      ptx::mbar_init(&emptyB[i], MMA_ISSUERS);
+      ptx::mbar_init(&emptyB[i], 1);
     }
-    ptx::mbar_init(d1, MMA_ISSUERS);
-    ptx::mbar_init(d3, MMA_ISSUERS);
+    ptx::mbar_init(d1, 1);
+    ptx::mbar_init(d3, 1);
     ptx::mbar_init(d5, 1);
     ptx::fence_mbar_init();
     *abort_flag = 0;
   }
-  constexpr int CHAIN_TMEM_COLS = MMA_ISSUERS > 1 ? 512 : 256;
-  if (warp == 0) ptx::tmem_alloc<CHAIN_TMEM_COLS>(tmem_slot);
+  if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // D1 and DH per issuer (64 columns each), then D5
-  const uint32_t dD1 = tmem, dDH = tmem + 64 * MMA_ISSUERS, dD5 = tmem + 128 * MMA_ISSUERS;
+  const uint32_t dD1 = tmem, dDH = tmem + 64, dD5 = tmem + 128;
 
   if (warp == EPI_WARPS) {
     // ---------------- producer: one operand block per chunk, in two halves.
@@ -1043,12 +1026,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         ptx::bulk_g2s(st + S_KT, src + OFF_KT, B_BYTES, &fullB[s]);  // KT, AQ
       }
     }
-  } else if (warp > EPI_WARPS) {
-    // ---------------- MMA issuers (lane 0 issues; the whole warp takes part in
-    // the named barriers that hand over h and v_new).  Issuer m takes K slices
-    // m, m + MMA_ISSUERS, ... of D1 and DH into its own accumulators; issuer 0
-    // also the output GEMM D5.
-    const int mi = warp - (EPI_WARPS + 1);
+  } else if (warp == EPI_WARPS + 1) {
+    // ---------------- MMA issuer (lane 0 issues; the whole warp takes part in
+    // the named barriers that hand over h and v_new)
     const uint32_t id_kmn = ptx::idesc_bf16(128, 2 * VTILE, 0, 1);   // A K-major, B MN-major
     const uint32_t id_mnmn = ptx::idesc_bf16(128, 2 * VTILE, 1, 1);  // both MN-major
     const uint64_t dH0 = ptx::sdesc(Himg, 128, 2048);
@@ -1068,8 +1048,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       if (lane == 0) {
         // D1 = [-w ; q~] [h_hi | h_lo]
 #pragma unroll
-        for (int ks = mi; ks < 8; ks += MMA_ISSUERS)
-          ptx::mma_bf16(dD1 + 64 * mi, adv(aw, ks * 4096), adv(dH0, ks * 256), id_kmn, ks > mi);
+        for (int ks = 0; ks < 8; ++ks)
+          ptx::mma_bf16(dD1, adv(aw, ks * 4096), adv(dH0, ks * 256), id_kmn, ks > 0);
         ptx::mma_commit(d1);
         ptx::mma_commit(&emptyA[s]);  // D1 no longer reads AW
       }
@@ -1082,16 +1062,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
         // token rows once with each half of k~; critical path), then
         // D5 = AQ [vn_hi | vn_lo]
 #pragma unroll
-        for (int ks = mi; ks < 8; ks += MMA_ISSUERS)
-          ptx::mma_bf16(dDH + 64 * mi, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 256), id_mnmn,
-                        ks > mi);
+        for (int ks = 0; ks < 8; ++ks)
+          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 256), id_mnmn, ks > 0);
         ptx::mma_commit(d3);
-        if (mi == 0) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN0, ks * 256), id_kmn, ks > 0);
-          ptx::mma_commit(d5);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN0, ks * 256), id_kmn, ks > 0);
+        ptx::mma_commit(d5);
         ptx::mma_commit(&emptyB[s]);
       }
       __syncwarp();
@@ -1160,10 +1137,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       float qh[16];
       {
         float d[16];
-        if (MMA_ISSUERS > 1)
-          tmem_ld_pair16_2(dD1 + lane_base, dD1 + 64 + lane_base, c0, d);
-        else
-          tmem_ld_pair16(dD1 + lane_base, c0, d);
+        tmem_ld_pair16(dD1 + lane_base, c0, d);
         if (r < 64) {
           const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128);
           float vn[16];
@@ -1192,10 +1166,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       ptx::tc_fence_after();
       {
         float d[16];
-        if (MMA_ISSUERS > 1)
-          tmem_ld_pair16_2(dDH + lane_base, dDH + 64 + lane_base, c0, d);
-        else
-          tmem_ld_pair16(dDH + lane_base, c0, d);
+        tmem_ld_pair16(dDH + lane_base, c0, d);
 #pragma unroll
         for (int j = 0; j < 16; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
         store_pair16(Himg, r, c0, 2048, hs);
@@ -1262,7 +1233,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc<CHAIN_TMEM_COLS>(tmem);
+  if (warp == 0) ptx::tmem_dealloc<256>(tmem);
 }
 
 // ---------------------------------------------------------------------------
