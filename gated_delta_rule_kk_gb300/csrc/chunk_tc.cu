@@ -1289,21 +1289,25 @@ __global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(TcParams 
     }
     __syncthreads();
     const float *mrow = csm + (sg & 1) * KD * COMB_LDM + r * COMB_LDM;
-    float a0 = b.x, a1 = b.y, a2 = b.z, a3 = b.w;
-#pragma unroll 4
+    // four partial sums per output (k = m mod 4) keep sixteen FMA chains in flight
+    float part[4][4] = {{b.x, b.y, b.z, b.w}};
+#pragma unroll 2
     for (int m = 0; m < KD; m += 4) {
       const float4 mv = *reinterpret_cast<const float4 *>(mrow + m);
       const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float4 x = *reinterpret_cast<const float4 *>(X + (m + e) * COMB_COLS + cq);
-        a0 = fmaf(mm[e], x.x, a0);
-        a1 = fmaf(mm[e], x.y, a1);
-        a2 = fmaf(mm[e], x.z, a2);
-        a3 = fmaf(mm[e], x.w, a3);
+        part[e][0] = fmaf(mm[e], x.x, part[e][0]);
+        part[e][1] = fmaf(mm[e], x.y, part[e][1]);
+        part[e][2] = fmaf(mm[e], x.z, part[e][2]);
+        part[e][3] = fmaf(mm[e], x.w, part[e][3]);
       }
     }
-    acc = make_float4(a0, a1, a2, a3);
+    acc = make_float4((part[0][0] + part[1][0]) + (part[2][0] + part[3][0]),
+                      (part[0][1] + part[1][1]) + (part[2][1] + part[3][1]),
+                      (part[0][2] + part[1][2]) + (part[2][2] + part[3][2]),
+                      (part[0][3] + part[1][3]) + (part[2][3] + part[3][3]));
   }
 }
 

@@ -37,25 +37,21 @@ namespace {
 
 constexpr int DK = 128, DV = 128;
 constexpr int NWARPS = 8, NTHREADS = NWARPS * 32;
-// Per CTA (two CTAs per SM): the 32 KB state slot (NSW deep, two 64-column
-// halves of 128 rows x 128 B, swizzled, 1024-aligned), a write-back buffer of
-// the same layout, and a ring of small per-item entries (NAUX deep) holding
+// Two rings per CTA (two CTAs per SM): the 32 KB state slots (NSW deep,
+// each slot two 64-column halves of 128 rows x 128 B, swizzled, 1024-aligned)
+// and small per-item entries (NAUX deep) holding
 //   RAW  [0, 3072)       q, k, v rows as copied (T <= 4)
 //   BD   [3072, 7424)    dot operand: 16 rows (k^_t hi/lo, then q^_t hi/lo) x 128
 //   BU   [7424, 13568)   update operand: 128 rows (state columns) x 16 (pitch 48 B)
 //   HDR  [13568, 13824)  slot index and coefficients
 // The per-item ring is deeper, so an item is prepared two items ahead of its
-// use, off the critical path.  The slot is released as soon as every warp has
-// its rows in registers, so the next item's state streams in during this
-// item's whole compute; updated rows leave through the write-back buffer,
-// whose previous store a warp waits on only when it writes it again.
-constexpr int NSW = 1, NAUX = 3, PREP_AHEAD = 2;
+// use, off the critical path.
+constexpr int NSW = 2, NAUX = 3, PREP_AHEAD = 2;
 constexpr uint32_t SLOT_BYTES = DK * DV * 2;  // 32 KB bf16 state slot
 constexpr uint32_t ROW_BYTES = DK * 2;        // one bf16 q/k/v row
 constexpr uint32_t BD_PITCH = 272, BU_PITCH = 48;
 constexpr uint32_t A_RAW = 0, A_BD = 3072, A_BU = 7424, A_HDR = 13568, AUX_BYTES = 13824;
-constexpr uint32_t O_OUT = NSW * SLOT_BYTES, O_AUX = O_OUT + SLOT_BYTES,
-                   O_BARS = O_AUX + NAUX * AUX_BYTES;
+constexpr uint32_t O_AUX = NSW * SLOT_BYTES, O_BARS = O_AUX + NAUX * AUX_BYTES;
 constexpr size_t SMEM_BYTES = O_BARS + (NSW + 2 * NAUX) * 8 + (NSW + NAUX) * 4 + 1024;
 
 // header words
@@ -288,7 +284,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
   uint64_t *aux_full = sw_full + NSW, *prep = aux_full + NAUX;
   int *sw_done = reinterpret_cast<int *>(prep + NAUX), *aux_done = sw_done + NSW;
   auto sw_at = [&](int s) { return smem + s * SLOT_BYTES; };
-  unsigned char *wb = smem + O_OUT;  // write-back buffer
   auto aux_at = [&](int a) { return smem + O_AUX + a * AUX_BYTES; };
   constexpr int NT_DOT = (2 * T + 3) / 4;  // 8-column tiles of the dot product
 
@@ -347,22 +342,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
 
     if (!ptx::mbar_wait_bounded(&prep[a], ap)) record_error(p.err, GDN_ERR_TIMEOUT);
     const int slot = *reinterpret_cast<const int *>(hdr);
-    // done with the state slot (rows loaded, or nothing to load): the last
-    // warp out refills it with this CTA's next item
-    auto release_slot = [&]() {
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        if (atomicAdd(&sw_done[s], 1) == NWARPS - 1) {
-          sw_done[s] = 0;
-          __threadfence_block();
-          const int refill = item + NSW * stride;
-          if (refill < nitems) issue_sw(p, &tm_ld, sw, &sw_full[s], refill, slot_of(p, refill));
-        }
-      }
-    };
     float C[16][4];
-    if (slot < 0) release_slot();
     if (slot >= 0) {
       if (!ptx::mbar_wait_bounded(&sw_full[s], sp)) record_error(p.err, GDN_ERR_TIMEOUT);
       // ---- S0 rows as A fragments; the same values seed the fp32 accumulators
@@ -386,7 +366,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
         ptx::mma_16816_bf16(D[0], af, b[0], b[1]);
         if (NT_DOT > 1) ptx::mma_16816_bf16(D[NT_DOT - 1], af, b[2], b[3]);
       }
-      release_slot();  // this warp's rows are in registers
       // vector 4 nt + tig on this lane: rows g (hi + lo) and g + 8
       float vg[NT_DOT], vg8[NT_DOT];
 #pragma unroll
@@ -510,22 +489,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
       }
     }
     if (slot >= 0) {
-      // ---- write back: bf16 fragments -> this warp's rows of the write-back
-      // buffer -> TMA store; the rows' previous store has to be read out first
-      if (lane == 0) ptx::bulk_wait_read<0>();
-      __syncwarp();
+      // ---- write back: bf16 fragments -> this warp's rows of the slot -> TMA store
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        ptx::stmatrix_x4(sw_addr(wb, r0, j, lane), pack2(C[2 * j][0], C[2 * j][1]),
+        ptx::stmatrix_x4(sw_addr(sw, r0, j, lane), pack2(C[2 * j][0], C[2 * j][1]),
                          pack2(C[2 * j][2], C[2 * j][3]), pack2(C[2 * j + 1][0], C[2 * j + 1][1]),
                          pack2(C[2 * j + 1][2], C[2 * j + 1][3]));
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         const int grow = (slot * HV + hv) * DV + r0;
-        ptx::tma_store_2d(&tm_st, 0, grow, wb + r0 * 128);
-        ptx::tma_store_2d(&tm_st, 64, grow, wb + 16384 + r0 * 128);
+        ptx::tma_store_2d(&tm_st, 0, grow, sw + r0 * 128);
+        ptx::tma_store_2d(&tm_st, 64, grow, sw + 16384 + r0 * 128);
         ptx::bulk_commit();
+        ptx::bulk_wait_read<0>();  // the slot may be refilled only after this
       }
     } else {
       if (tid == 0) record_error(p.err, GDN_ERR_BAD_SLOT);
@@ -535,6 +512,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
           static_cast<float *>(p.o)[oi] = 0.f;
         else
           o[oi] = __float2bfloat16_rn(0.f);
+      }
+    }
+    // done with the state slot: the last warp out refills it
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&sw_done[s], 1) == NWARPS - 1) {
+        sw_done[s] = 0;
+        __threadfence_block();
+        const int refill = item + NSW * stride;
+        if (refill < nitems) issue_sw(p, &tm_ld, sw, &sw_full[s], refill, slot_of(p, refill));
       }
     }
     const int ahead = item + PREP_AHEAD * stride;
