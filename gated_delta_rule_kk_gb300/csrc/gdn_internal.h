@@ -68,6 +68,10 @@ cudaError_t launch_chunk_simt(const ChunkParams &p, bool bf16, bool per_channel_
                               cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_state_pass(const StateParams &p, bool bf16, cudaStream_t stream);
+// The state pass on tcgen05 + TMA (bf16, K = 128, V % 32 == 0, gates whose
+// chunk factors ride on the value side): whether it serves p, and its launch.
+bool state_pass_tc5_supported(const StateParams &p, bool bf16);
+cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream);
 // The decode step on the warp-level tensor cores (K = V = 128).
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 

@@ -712,6 +712,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
 }  // namespace
 
 cudaError_t launch_state_pass(const StateParams &p, bool bf16, cudaStream_t stream) {
+  if (state_pass_tc5_supported(p, bf16)) return launch_state_pass_tc5(p, stream);
   const dim3 grid((unsigned)((p.V + SP_VT - 1) / SP_VT), (unsigned)p.H, (unsigned)p.N);
   if (bf16 && p.K == KMAX) {
     // per-key gate: k~ staged, two ring slots (its gate rows are 32 KB a

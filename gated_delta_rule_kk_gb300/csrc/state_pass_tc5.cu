@@ -1,0 +1,462 @@
+// Chunk state pass on the 5th-generation tensor cores (tcgen05 + TMA), bf16
+// inputs with K = 128, V a multiple of 32, gates none / g / g_gamma / gv (the
+// gates whose chunk factors ride on the value side).  The recurrence is that
+// of state_pass.cu (KDA _fla/ops/common/chunk_h.py, chunk_fwd_kernel_h and
+// chunk_bwd_kernel_dh):
+//   h_{c+1} = decay_c o h_c + Delta_c,   Delta_c = k_c^T v~_c,
+// where decay_c is e^{g_L} (per column e^{gv_L}) and v~ carries every token
+// factor (forward e^{g_L - g_i} e^{gv_L - gv_i}, backward scale e^{g_i} e^{gv_i}).
+// Delta_c does not depend on h, so the tensor core computes it for chunks
+// ahead of the state: only the element-wise update is sequential.
+//
+// One CTA per (32-column V tile, head, sequence), 256 threads:
+//   warp 6      producer: TMA of the chunk's k tile (16 boxes of 8 keys x 64
+//               tokens, which land as the column groups of the MN-major
+//               operand image), its v tile and, for gv, its gate tile, into a
+//               ring of NS slots
+//   warps 4-5   stagers: thread i forms row i of v~ = v x factor as a bf16
+//               hi/lo pair (zero past the chunk's end) into one of two
+//               operand images
+//   warp 7      MMA: Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64,
+//               K = 64 tokens) into one of two TMEM accumulators
+//   warps 0-3   state: thread r holds key row r, 32 columns, of the fp32
+//               state; per chunk it stores the chunk-start state (when that
+//               chunk is stored) and applies h = decay o h + Delta_hi + Delta_lo
+// Every wait is bounded (GDN_ERR_TIMEOUT, then every role still runs every
+// chunk so no barrier is left short of arrivals).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "ptx.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int T5_THREADS = 256, T5_VT = 32, T5_KD = 128, T5_NS = 4;
+// ring slot: k image (16 KB, column group stride 1024), v tile (64 x 32 bf16,
+// row-major), gv tile (64 x 32 fp32, row-major)
+constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
+constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 20480u; }
+// v~ image: 64 token rows x 64 columns (hi 0..31, lo 32..63), group stride 1024
+constexpr uint32_t T5_VTB = 8192;
+
+struct T5Seq {
+  int bos, eos, b, nch;
+  long long first;
+  bool write_hs;
+};
+
+// Sequence n's token range and first stored-state index (one thread reads the
+// offsets; bad cu_seqlens or too small a num_chunks are recorded).
+__device__ T5Seq t5_sequence(const StateParams &p, int n, int tid, long long *sh) {
+  T5Seq s;
+  s.bos = 0; s.eos = p.T; s.b = n;
+  if (p.cu_seqlens) {
+    s.b = 0;
+    s.bos = p.cu_seqlens[n];
+    s.eos = p.cu_seqlens[n + 1];
+    if (tid == 0) {
+      bool ok = s.bos >= 0 && s.eos >= s.bos && s.eos <= p.T && p.cu_seqlens[0] == 0 &&
+                p.cu_seqlens[p.N] == p.T;
+      long long first = 0;
+      for (int m = 0; m < n && ok; ++m) {
+        const int len = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
+        if (len < 0) ok = false;
+        first += (len + BT * p.split - 1) / (BT * p.split);
+      }
+      sh[0] = first;
+      sh[1] = ok ? 1 : 0;
+      if (!ok) record_error(p.err, GDN_ERR_BAD_SEQLENS);
+    }
+    __syncthreads();
+    if (sh[1] == 0) s.bos = s.eos = 0;
+  } else if (tid == 0) {
+    sh[0] = (long long)n * ((p.T + BT * p.split - 1) / (BT * p.split));
+    sh[1] = 1;
+  }
+  __syncthreads();
+  s.nch = (s.eos - s.bos + BT - 1) / BT;
+  s.first = sh[0];
+  s.write_hs = p.hs && sh[1] && s.first + (s.nch + p.split - 1) / p.split <= p.num_chunks;
+  if (p.hs && sh[1] && !s.write_hs && tid == 0) record_error(p.err, GDN_ERR_BAD_SEQLENS);
+  return s;
+}
+
+__device__ __forceinline__ void t5_split8(const float *f, uint4 &hi, uint4 &lo) {
+  __nv_bfloat162 h2[4];
+  float r[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    h2[e] = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+    const float2 b = __bfloat1622float2(h2[e]);
+    r[2 * e] = f[2 * e] - b.x;
+    r[2 * e + 1] = f[2 * e + 1] - b.y;
+  }
+  hi = *reinterpret_cast<const uint4 *>(h2);
+  __nv_bfloat162 l2[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) l2[e] = __floats2bfloat162_rn(r[2 * e], r[2 * e + 1]);
+  lo = *reinterpret_cast<const uint4 *>(l2);
+}
+
+template <bool GV, bool VF, bool SPLIT>
+__global__ void __launch_bounds__(T5_THREADS, 1)
+state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_g, StateParams p) {
+  extern __shared__ __align__(1024) unsigned char sm5[];
+  constexpr int K = T5_KD;
+  constexpr uint32_t SLOT = t5_slot_bytes(GV);
+  unsigned char *ring = sm5;
+  unsigned char *vimg = sm5 + T5_NS * SLOT;  // two v~ images
+  uint64_t *bars = reinterpret_cast<uint64_t *>(vimg + 2 * T5_VTB);
+  uint64_t *full = bars, *empty = bars + T5_NS;
+  uint64_t *vready = bars + 2 * T5_NS, *vfree = vready + 2, *afull = vfree + 2, *afree = afull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(afree + 2);
+  __shared__ long long seq_sh[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int v0 = blockIdx.x * T5_VT, h = blockIdx.y, n = blockIdx.z;
+  const int H = p.H, V = p.V, HG = p.HG, hg = h / (H / HG);
+  const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
+  const float gamma = p.gate == GDN_GATE_G_GAMMA ? p.gate_values[hg] : 0.f;
+  const T5Seq sq = t5_sequence(p, n, tid, seq_sh);
+  auto chunk_at = [&](int it) { return p.reverse ? sq.nch - 1 - it : it; };
+
+  if (tid == 0) {
+    for (int s = 0; s < T5_NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 3);  // two stager warps + the MMA's commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&vready[b], 2);
+      ptx::mbar_init(&vfree[b], 1);
+      ptx::mbar_init(&afull[b], 1);
+      ptx::mbar_init(&afree[b], 4);
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) ptx::tmem_alloc<128>(tmem_slot);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 6) {
+    // ---------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_k);
+      ptx::prefetch_tmap(&tm_v);
+      if (GV) ptx::prefetch_tmap(&tm_g);
+      const uint32_t bytes = 16384u + 4096u + (GV ? 8192u : 0u);
+#pragma unroll 1
+      for (int it = 0; it < sq.nch; ++it) {
+        const int s = it % T5_NS;
+        if (it >= T5_NS) ok = ptx::mbar_wait_bounded(&empty[s], (uint32_t)((it / T5_NS - 1) & 1)) && ok;
+        unsigned char *slot = ring + s * SLOT;
+        const int row0 = sq.b * p.T + sq.bos + chunk_at(it) * BT;
+        ptx::mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll 1
+        for (int j = 0; j < K / 8; ++j)
+          ptx::tma_load_3d(slot + T5_RK + j * 1024, &tm_k, 8 * j, h, row0, &full[s]);
+        ptx::tma_load_3d(slot + T5_RV, &tm_v, v0, h, row0, &full[s]);
+        if (GV) ptx::tma_load_3d(slot + T5_RG, &tm_g, v0, hg, row0, &full[s]);
+      }
+    }
+  } else if (warp == 4 || warp == 5) {
+    // ---------------- stagers: thread i = token row i of the chunk
+    const int i = tid - 128;
+    const float *g = p.gate_values;
+    auto gate_at = [&](int it, int row) {  // g of the chunk's row (row < its length)
+      const size_t t = (size_t)sq.b * p.T + sq.bos + (size_t)chunk_at(it) * BT + row;
+      return g[t * HG + hg];
+    };
+    auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
+    float gi = 0.f, gl = 0.f;
+    if (p.gate == GDN_GATE_G && sq.nch > 0) {
+      const int L0 = len_of(0);
+      gi = i < L0 ? gate_at(0, i) : 0.f;
+      gl = gate_at(0, L0 - 1);
+    }
+#pragma unroll 1
+    for (int it = 0; it < sq.nch; ++it) {
+      const int s = it % T5_NS, b = it & 1;
+      const int L = len_of(it);
+      // the next chunk's gates now: their latency overlaps this chunk
+      float gin = 0.f, gln = 0.f;
+      if (p.gate == GDN_GATE_G && it + 1 < sq.nch) {
+        const int L1 = len_of(it + 1);
+        gin = i < L1 ? gate_at(it + 1, i) : 0.f;
+        gln = gate_at(it + 1, L1 - 1);
+      }
+      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
+      const unsigned char *slot = ring + s * SLOT;
+      float f = 0.f;
+      if (i < L) {
+        f = p.reverse ? p.scale : 1.f;
+        if (scalar_gate) {
+          const float g_i = p.gate == GDN_GATE_G ? gi : gamma * (float)(i + 1);
+          const float g_l = p.gate == GDN_GATE_G ? gl : gamma * (float)L;
+          f *= expf(p.reverse ? g_i : g_l - g_i);
+        }
+      }
+      float x[T5_VT];
+      {
+        const uint4 *vr = reinterpret_cast<const uint4 *>(slot + T5_RV + i * 64);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = vr[q];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[8 * q + 2 * e] = __uint_as_float(w[e] << 16) * f;
+            x[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * f;
+          }
+        }
+      }
+      if (GV && i < L) {
+        const float *gr = reinterpret_cast<const float *>(slot + T5_RG);
+#pragma unroll
+        for (int j = 0; j < T5_VT; ++j)
+          x[j] *= expf(p.reverse ? gr[i * T5_VT + j] : gr[(L - 1) * T5_VT + j] - gr[i * T5_VT + j]);
+      }
+      if (it >= 2) ok = ptx::mbar_wait_bounded(&vfree[b], (uint32_t)(((it >> 1) - 1) & 1)) && ok;
+      unsigned char *img = vimg + b * T5_VTB;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 hi, lo;
+        t5_split8(x + 8 * q, hi, lo);
+        *reinterpret_cast<uint4 *>(img + q * 1024 + i * 16) = hi;
+        *reinterpret_cast<uint4 *>(img + (4 + q) * 1024 + i * 16) = lo;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&vready[b]);
+        ptx::mbar_arrive(&empty[s]);  // this warp has read the slot's v (and gate) tile
+      }
+      gi = gin;
+      gl = gln;
+    }
+  } else if (warp == 7) {
+    // ---------------- MMA issuer
+    const uint32_t id = ptx::idesc_bf16(128, 2 * T5_VT, 1, 1);  // A and B MN-major
+#pragma unroll 1
+    for (int it = 0; it < sq.nch; ++it) {
+      const int s = it % T5_NS, b = it & 1;
+      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
+      ok = ptx::mbar_wait_bounded(&vready[b], (uint32_t)((it >> 1) & 1)) && ok;
+      if (it >= 2) ok = ptx::mbar_wait_bounded(&afree[b], (uint32_t)(((it >> 1) - 1) & 1)) && ok;
+      __syncwarp();
+      ptx::tc_fence_after();
+      if (lane == 0) {
+        const uint64_t a = ptx::sdesc(ring + s * SLOT + T5_RK, 128, 1024);
+        const uint64_t bv = ptx::sdesc(vimg + b * T5_VTB, 128, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          ptx::mma_bf16(tmem + 64 * b, a + (uint64_t)(ks * 256 >> 4), bv + (uint64_t)(ks * 256 >> 4),
+                        id, ks > 0);
+        ptx::mma_commit(&afull[b]);
+        ptx::mma_commit(&vfree[b]);
+        ptx::mma_commit(&empty[s]);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---------------- state warps 0-3: key row r, columns v0 .. v0 + 31
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const size_t hbase = ((size_t)n * H + h) * K * V;
+    auto at = [&](int col) { return VF ? (size_t)(v0 + col) * K + r : (size_t)r * V + v0 + col; };
+    float hs[T5_VT];
+    if (p.h0) {
+      if (VF) {
+#pragma unroll
+        for (int j = 0; j < T5_VT; ++j) hs[j] = p.h0[hbase + at(j)];
+      } else {
+        const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hbase + at(0));
+#pragma unroll
+        for (int q = 0; q < T5_VT / 4; ++q) {
+          const float4 x = src[q];
+          hs[4 * q] = x.x; hs[4 * q + 1] = x.y; hs[4 * q + 2] = x.z; hs[4 * q + 3] = x.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < T5_VT; ++j) hs[j] = 0.f;
+    }
+    // decay of chunk it (prefetched one chunk ahead)
+    auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
+    auto last_row = [&](int it) {
+      return (size_t)sq.b * p.T + sq.bos + (size_t)chunk_at(it) * BT + len_of(it) - 1;
+    };
+    float dsc = 1.f, dsn = 1.f;
+    float dv[T5_VT], dvn[T5_VT];
+#pragma unroll
+    for (int j = 0; j < T5_VT; ++j) dv[j] = dvn[j] = 1.f;
+    auto load_decay = [&](int it, float &ds, float *dvv) {
+      if (p.gate == GDN_GATE_G) ds = p.gate_values[last_row(it) * HG + hg];
+      if (p.gate == GDN_GATE_G_GAMMA) ds = gamma * (float)len_of(it);
+      if (GV) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            p.gate_values + (last_row(it) * HG + hg) * V + v0);
+#pragma unroll
+        for (int q = 0; q < T5_VT / 4; ++q) {
+          const float4 x = src[q];
+          dvv[4 * q] = x.x; dvv[4 * q + 1] = x.y; dvv[4 * q + 2] = x.z; dvv[4 * q + 3] = x.w;
+        }
+      }
+    };
+    if (sq.nch > 0) load_decay(0, dsc, dv);
+    int store_i = SPLIT && p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
+    int store_c = store_i * p.split;
+#pragma unroll 1
+    for (int it = 0; it < sq.nch; ++it) {
+      const int c = chunk_at(it), b = it & 1;
+      if (it + 1 < sq.nch) load_decay(it + 1, dsn, dvn);
+      bool store = true;
+      long long slot = sq.first + c;
+      if (SPLIT) {
+        store = c == store_c;
+        slot = sq.first + store_i;
+        if (store) {
+          store_c += p.reverse ? -p.split : p.split;
+          store_i += p.reverse ? -1 : 1;
+        }
+      }
+      if (sq.write_hs && store) {
+        const size_t sb = ((size_t)slot * H + h) * K * V;
+        if (VF) {
+#pragma unroll
+          for (int j = 0; j < T5_VT; ++j) {
+            if (p.hs_bf16)
+              static_cast<__nv_bfloat16 *>(p.hs)[sb + at(j)] = __float2bfloat16_rn(hs[j]);
+            else
+              static_cast<float *>(p.hs)[sb + at(j)] = hs[j];
+          }
+        } else if (p.hs_bf16) {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.hs) + sb + at(0));
+#pragma unroll
+          for (int q = 0; q < T5_VT / 8; ++q) {
+            __nv_bfloat162 w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = __floats2bfloat162_rn(hs[8 * q + 2 * e], hs[8 * q + 2 * e + 1]);
+            dst[q] = *reinterpret_cast<const uint4 *>(w);
+          }
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.hs) + sb + at(0));
+#pragma unroll
+          for (int q = 0; q < T5_VT / 4; ++q)
+            dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
+        }
+      }
+      ok = ptx::mbar_wait_bounded(&afull[b], (uint32_t)((it >> 1) & 1)) && ok;
+      ptx::tc_fence_after();
+      float dh[T5_VT], dl[T5_VT];
+      ptx::tmem_ld32(tmem + 64 * b + lane_base, dh);
+      ptx::tmem_ld32(tmem + 64 * b + 32 + lane_base, dl);
+      const float ds = scalar_gate ? expf(dsc) : 1.f;
+#pragma unroll
+      for (int j = 0; j < T5_VT; ++j) {
+        const float d = GV ? expf(dv[j]) * ds : ds;
+        hs[j] = fmaf(d, hs[j], dh[j] + dl[j]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&afree[b]);
+      dsc = dsn;
+#pragma unroll
+      for (int j = 0; j < T5_VT; ++j) dv[j] = dvn[j];
+    }
+    if (p.ht && ok) {
+      if (VF) {
+#pragma unroll
+        for (int j = 0; j < T5_VT; ++j) p.ht[hbase + at(j)] = hs[j];
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(p.ht + hbase + at(0));
+#pragma unroll
+        for (int q = 0; q < T5_VT / 4; ++q)
+          dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
+      }
+    }
+  }
+  if (!ok && lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc<128>(tmem);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 t5_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [rows][heads][dim] tensor of `elt`-byte elements, boxes of width x 1 x 64.
+bool t5_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elt, int dim,
+            int heads, long long rows, int width) {
+  auto fn = t5_encoder();
+  if (!fn) return false;
+  cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t gstride[2] = {(cuuint64_t)dim * elt, (cuuint64_t)heads * dim * elt};
+  cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, type, 3, const_cast<void *>(base), gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool state_pass_tc5_supported(const StateParams &p, bool bf16) {
+  return bf16 && p.K == T5_KD && p.V % T5_VT == 0 && p.T > 0 &&
+         (p.gate == GDN_GATE_NONE || p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA ||
+          p.gate == GDN_GATE_GV);
+}
+
+cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
+  const bool gv = p.gate == GDN_GATE_GV;
+  CUtensorMap mk, mv, mg;
+  const long long rows = (long long)p.B * p.T;
+  if (!t5_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T5_KD, p.H, rows, 8) ||
+      !t5_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.V, p.H, rows, T5_VT))
+    return cudaErrorInvalidValue;
+  if (gv) {
+    if (!t5_map(&mg, p.gate_values, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.V, p.HG, rows, T5_VT))
+      return cudaErrorInvalidValue;
+  } else {
+    mg = mv;  // unused
+  }
+  const size_t smem = T5_NS * t5_slot_bytes(gv) + 2 * T5_VTB + 256;  // + barriers, TMEM slot
+  const bool split = p.split > 1, vf = p.v_first != 0;
+  auto pick = [&](auto k000, auto k001, auto k010, auto k011, auto k100, auto k101, auto k110,
+                  auto k111) {
+    return gv ? (vf ? (split ? k111 : k110) : (split ? k101 : k100))
+              : (vf ? (split ? k011 : k010) : (split ? k001 : k000));
+  };
+  auto kern = pick(state_pass_tc5_kernel<false, false, false>,
+                   state_pass_tc5_kernel<false, false, true>,
+                   state_pass_tc5_kernel<false, true, false>,
+                   state_pass_tc5_kernel<false, true, true>,
+                   state_pass_tc5_kernel<true, false, false>,
+                   state_pass_tc5_kernel<true, false, true>,
+                   state_pass_tc5_kernel<true, true, false>,
+                   state_pass_tc5_kernel<true, true, true>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)(p.V / T5_VT), (unsigned)p.H, (unsigned)p.N);
+  kern<<<grid, T5_THREADS, smem, stream>>>(mk, mv, mg, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
