@@ -265,6 +265,13 @@ __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc, bool
                "l"(gsrc), "r"(ok ? 4 : 0)
                : "memory");
 }
+// Make the mbarrier track completion of this thread's earlier cp.async
+// copies: it receives one arrival (counted in its expected count) when they
+// have all landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -13,7 +13,9 @@
 //   warp 6      producer: TMA of the chunk's k tile (16 boxes of 8 keys x 64
 //               tokens, which land as the column groups of the MN-major
 //               operand image), its v tile and, for gv, its gate tile, into a
-//               ring of NS slots
+//               ring of NS slots; the per-token gate g by cp.async from every
+//               lane (counted on the slot's barrier), so no consumer ever
+//               waits on a global load
 //   warps 4-5   stagers: thread i forms row i of v~ = v x factor as a bf16
 //               hi/lo pair (zero past the chunk's end) into one of two
 //               operand images
@@ -21,7 +23,8 @@
 //               K = 64 tokens) into one of two TMEM accumulators
 //   warps 0-3   state: thread r holds key row r, 32 columns, of the fp32
 //               state; per chunk it stores the chunk-start state (when that
-//               chunk is stored) and applies h = decay o h + Delta_hi + Delta_lo
+//               chunk is stored) and applies h = decay o h + Delta_hi + Delta_lo,
+//               the decay read from the chunk's ring slot
 // Every wait is bounded (GDN_ERR_TIMEOUT, then every role still runs every
 // chunk so no barrier is left short of arrivals).
 #include <cuda.h>
@@ -36,7 +39,8 @@ namespace {
 
 constexpr int T5_THREADS = 256, T5_VT = 32, T5_KD = 128, T5_NS = 4;
 // ring slot: k image (16 KB, column group stride 1024), v tile (64 x 32 bf16,
-// row-major), gv tile (64 x 32 fp32, row-major)
+// row-major), gate: g per token (64 fp32) or the gv tile (64 x 32 fp32,
+// row-major)
 constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
 constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 20480u; }
 // v~ image: 64 token rows x 64 columns (hi 0..31, lo 32..63), group stride 1024
@@ -127,8 +131,10 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   if (tid == 0) {
     for (int s = 0; s < T5_NS; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 3);  // two stager warps + the MMA's commit
+      // the producer's expect-tx arrival + one cp.async arrival per lane
+      ptx::mbar_init(&full[s], 1 + 32);
+      // two stager warps + the MMA's commit + four state warps
+      ptx::mbar_init(&empty[s], 3 + 4);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&vready[b], 2);
@@ -151,13 +157,18 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       ptx::prefetch_tmap(&tm_k);
       ptx::prefetch_tmap(&tm_v);
       if (GV) ptx::prefetch_tmap(&tm_g);
-      const uint32_t bytes = 16384u + 4096u + (GV ? 8192u : 0u);
+    }
+    const uint32_t bytes = 16384u + 4096u + (GV ? 8192u : 0u);
+    const long long rows = (long long)p.B * p.T;
 #pragma unroll 1
-      for (int it = 0; it < sq.nch; ++it) {
-        const int s = it % T5_NS;
-        if (it >= T5_NS) ok = ptx::mbar_wait_bounded(&empty[s], (uint32_t)((it / T5_NS - 1) & 1)) && ok;
-        unsigned char *slot = ring + s * SLOT;
-        const int row0 = sq.b * p.T + sq.bos + chunk_at(it) * BT;
+    for (int it = 0; it < sq.nch; ++it) {
+      const int s = it % T5_NS;
+      if (it >= T5_NS)
+        ok = ptx::mbar_wait_bounded(&empty[s], (uint32_t)((it / T5_NS - 1) & 1)) && ok;
+      __syncwarp();
+      unsigned char *slot = ring + s * SLOT;
+      const int row0 = sq.b * p.T + sq.bos + chunk_at(it) * BT;
+      if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll 1
         for (int j = 0; j < K / 8; ++j)
@@ -165,41 +176,35 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::tma_load_3d(slot + T5_RV, &tm_v, v0, h, row0, &full[s]);
         if (GV) ptx::tma_load_3d(slot + T5_RG, &tm_g, v0, hg, row0, &full[s]);
       }
+      if (p.gate == GDN_GATE_G) {
+        // g of the chunk's 64 rows (rows past the tensor read as zero)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const long long r = (long long)row0 + lane + 32 * q;
+          const bool in = r < rows;
+          ptx::cp_async4(slot + T5_RG + (lane + 32 * q) * 4,
+                         p.gate_values + (in ? r : 0) * HG + hg, in);
+        }
+      }
+      ptx::cp_async_mbar_arrive(&full[s]);
     }
   } else if (warp == 4 || warp == 5) {
     // ---------------- stagers: thread i = token row i of the chunk
     const int i = tid - 128;
-    const float *g = p.gate_values;
-    auto gate_at = [&](int it, int row) {  // g of the chunk's row (row < its length)
-      const size_t t = (size_t)sq.b * p.T + sq.bos + (size_t)chunk_at(it) * BT + row;
-      return g[t * HG + hg];
-    };
     auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
-    float gi = 0.f, gl = 0.f;
-    if (p.gate == GDN_GATE_G && sq.nch > 0) {
-      const int L0 = len_of(0);
-      gi = i < L0 ? gate_at(0, i) : 0.f;
-      gl = gate_at(0, L0 - 1);
-    }
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
       const int s = it % T5_NS, b = it & 1;
       const int L = len_of(it);
-      // the next chunk's gates now: their latency overlaps this chunk
-      float gin = 0.f, gln = 0.f;
-      if (p.gate == GDN_GATE_G && it + 1 < sq.nch) {
-        const int L1 = len_of(it + 1);
-        gin = i < L1 ? gate_at(it + 1, i) : 0.f;
-        gln = gate_at(it + 1, L1 - 1);
-      }
       ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
       const unsigned char *slot = ring + s * SLOT;
+      const float *gslot = reinterpret_cast<const float *>(slot + T5_RG);
       float f = 0.f;
       if (i < L) {
         f = p.reverse ? p.scale : 1.f;
         if (scalar_gate) {
-          const float g_i = p.gate == GDN_GATE_G ? gi : gamma * (float)(i + 1);
-          const float g_l = p.gate == GDN_GATE_G ? gl : gamma * (float)L;
+          const float g_i = p.gate == GDN_GATE_G ? gslot[i] : gamma * (float)(i + 1);
+          const float g_l = p.gate == GDN_GATE_G ? gslot[L - 1] : gamma * (float)L;
           f *= expf(p.reverse ? g_i : g_l - g_i);
         }
       }
@@ -238,8 +243,6 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_arrive(&vready[b]);
         ptx::mbar_arrive(&empty[s]);  // this warp has read the slot's v (and gate) tile
       }
-      gi = gin;
-      gl = gln;
     }
   } else if (warp == 7) {
     // ---------------- MMA issuer
@@ -288,35 +291,12 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
       for (int j = 0; j < T5_VT; ++j) hs[j] = 0.f;
     }
-    // decay of chunk it (prefetched one chunk ahead)
     auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
-    auto last_row = [&](int it) {
-      return (size_t)sq.b * p.T + sq.bos + (size_t)chunk_at(it) * BT + len_of(it) - 1;
-    };
-    float dsc = 1.f, dsn = 1.f;
-    float dv[T5_VT], dvn[T5_VT];
-#pragma unroll
-    for (int j = 0; j < T5_VT; ++j) dv[j] = dvn[j] = 1.f;
-    auto load_decay = [&](int it, float &ds, float *dvv) {
-      if (p.gate == GDN_GATE_G) ds = p.gate_values[last_row(it) * HG + hg];
-      if (p.gate == GDN_GATE_G_GAMMA) ds = gamma * (float)len_of(it);
-      if (GV) {
-        const float4 *src = reinterpret_cast<const float4 *>(
-            p.gate_values + (last_row(it) * HG + hg) * V + v0);
-#pragma unroll
-        for (int q = 0; q < T5_VT / 4; ++q) {
-          const float4 x = src[q];
-          dvv[4 * q] = x.x; dvv[4 * q + 1] = x.y; dvv[4 * q + 2] = x.z; dvv[4 * q + 3] = x.w;
-        }
-      }
-    };
-    if (sq.nch > 0) load_decay(0, dsc, dv);
     int store_i = SPLIT && p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
     int store_c = store_i * p.split;
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
-      const int c = chunk_at(it), b = it & 1;
-      if (it + 1 < sq.nch) load_decay(it + 1, dsn, dvn);
+      const int c = chunk_at(it), b = it & 1, s = it % T5_NS;
       bool store = true;
       long long slot = sq.first + c;
       if (SPLIT) {
@@ -353,23 +333,28 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
             dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
         }
       }
+      // the chunk's decay, from its ring slot
+      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
+      const int L = len_of(it);
+      const float *gslot = reinterpret_cast<const float *>(ring + s * SLOT + T5_RG);
+      float ds = 1.f;
+      if (p.gate == GDN_GATE_G) ds = expf(gslot[L - 1]);
+      if (p.gate == GDN_GATE_G_GAMMA) ds = expf(gamma * (float)L);
+      float dv[T5_VT];
+#pragma unroll
+      for (int j = 0; j < T5_VT; ++j) dv[j] = GV ? expf(gslot[(L - 1) * T5_VT + j]) : ds;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp is done with the slot
       ok = ptx::mbar_wait_bounded(&afull[b], (uint32_t)((it >> 1) & 1)) && ok;
       ptx::tc_fence_after();
       float dh[T5_VT], dl[T5_VT];
       ptx::tmem_ld32(tmem + 64 * b + lane_base, dh);
       ptx::tmem_ld32(tmem + 64 * b + 32 + lane_base, dl);
-      const float ds = scalar_gate ? expf(dsc) : 1.f;
 #pragma unroll
-      for (int j = 0; j < T5_VT; ++j) {
-        const float d = GV ? expf(dv[j]) * ds : ds;
-        hs[j] = fmaf(d, hs[j], dh[j] + dl[j]);
-      }
+      for (int j = 0; j < T5_VT; ++j) hs[j] = fmaf(dv[j], hs[j], dh[j] + dl[j]);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&afree[b]);
-      dsc = dsn;
-#pragma unroll
-      for (int j = 0; j < T5_VT; ++j) dv[j] = dvn[j];
     }
     if (p.ht && ok) {
       if (VF) {
