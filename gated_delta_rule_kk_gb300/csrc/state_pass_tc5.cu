@@ -40,9 +40,10 @@ namespace {
 constexpr int T5_THREADS = 256, T5_VT = 32, T5_KD = 128, T5_NS = 4;
 // ring slot: k image (16 KB, column group stride 1024), v tile (64 x 32 bf16,
 // row-major), gate: g per token (64 fp32) or the gv tile (64 x 32 fp32,
-// row-major)
+// row-major), all inside the slot
 constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
-constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 20480u; }
+// (1024-byte multiples, so every slot's k image stays 1024-aligned)
+constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 21504u; }
 // v~ image: 64 token rows x 64 columns (hi 0..31, lo 32..63), group stride 1024
 constexpr uint32_t T5_VTB = 8192;
 
