@@ -9,17 +9,19 @@
 // Delta_c does not depend on h, so the tensor core computes it for chunks
 // ahead of the state: only the element-wise update is sequential.
 //
-// One CTA per (32-column V tile, head, sequence), 256 threads:
-//   warp 6      producer: TMA of the chunk's k tile (16 boxes of 8 keys x 64
-//               tokens, which land as the column groups of the MN-major
-//               operand image), its v tile and, for gv, its gate tile, into a
-//               ring of NS slots; the per-token gate g by cp.async from every
-//               lane (counted on the slot's barrier), so no consumer ever
-//               waits on a global load
-//   warps 4-5   stagers: thread i forms row i of v~ = v x factor as a bf16
-//               hi/lo pair (zero past the chunk's end) into one of two
-//               operand images
-//   warp 7      MMA: Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64,
+// One CTA per (32-column V tile, head, sequence), 320 threads:
+//   warp 8      producer: one TMA each for the chunk's k tile, its v tile and,
+//               for gv, its gate tile, into a ring of NS slots, all with
+//               swizzled rows of 64 or 128 bytes (a TMA moves a box row by
+//               row, so narrow rows cost requests): k lands as two 128-byte
+//               swizzled MN-major atoms columns (keys 0-63 and 64-127) that
+//               the MMA reads directly; the per-token gate g by cp.async from
+//               every lane (counted on the slot's barrier), so no consumer
+//               ever waits on a global load
+//   warps 4-7   stagers: thread (i, half) forms row i, 16 columns, of
+//               v~ = v x factor as a bf16 hi/lo pair (zero past the chunk's
+//               end) into one of two operand images
+//   warp 9      MMA: Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64,
 //               K = 64 tokens) into one of two TMEM accumulators
 //   warps 0-3   state: thread r holds key row r, 32 columns, of the fp32
 //               state; per chunk it stores the chunk-start state (when that
@@ -37,10 +39,12 @@
 namespace gdn {
 namespace {
 
-constexpr int T5_THREADS = 256, T5_VT = 32, T5_KD = 128, T5_NS = 4;
-// ring slot: k image (16 KB, column group stride 1024), v tile (64 x 32 bf16,
-// row-major), gate: g per token (64 fp32) or the gv tile (64 x 32 fp32,
-// row-major), all inside the slot
+constexpr int T5_THREADS = 320, T5_VT = 32, T5_KD = 128, T5_NS = 4;
+constexpr int T5_STAGERS = 4, T5_WPROD = 8, T5_WMMA = 9;
+// ring slot: k image (two 8 KB halves of 64 keys: 64 token rows of 128 bytes,
+// 128-byte swizzle), v tile (64 token rows of 32 bf16, 64-byte swizzle),
+// gate: g per token (64 fp32) or the gv tile (64 token rows of 32 fp32,
+// 128-byte swizzle), all inside the slot
 constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
 // (1024-byte multiples, so every slot's k image stays 1024-aligned)
 constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 21504u; }
@@ -106,14 +110,33 @@ __device__ __forceinline__ void t5_split8(const float *f, uint4 &hi, uint4 &lo) 
   lo = *reinterpret_cast<const uint4 *>(l2);
 }
 
+__device__ __forceinline__ void t5_tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                               int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(ptx::smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(ptx::smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand (layout
+// field 2); lbo / sbo as for the MN-major swizzled layouts: the distance
+// between 64-element atoms columns along M or N, and between 8-row groups
+// along K.
+__device__ __forceinline__ uint64_t t5_sdesc_sw128(const void *smem, uint32_t lbo, uint32_t sbo) {
+  return ptx::sdesc(smem, lbo, sbo) | (2ull << 61);
+}
+
 template <bool GV, bool VF, bool SPLIT>
 __global__ void __launch_bounds__(T5_THREADS, 1)
 state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_g, StateParams p) {
-  extern __shared__ __align__(1024) unsigned char sm5[];
+  extern __shared__ __align__(1024) unsigned char sm5_raw[];
   constexpr int K = T5_KD;
   constexpr uint32_t SLOT = t5_slot_bytes(GV);
+  // the swizzle patterns follow address bits 4-9: slots start on 1024 bytes
+  unsigned char *sm5 = sm5_raw + ((1024u - (ptx::smem_u32(sm5_raw) & 1023u)) & 1023u);
   unsigned char *ring = sm5;
   unsigned char *vimg = sm5 + T5_NS * SLOT;  // two v~ images
   uint64_t *bars = reinterpret_cast<uint64_t *>(vimg + 2 * T5_VTB);
@@ -134,11 +157,11 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int s = 0; s < T5_NS; ++s) {
       // the producer's expect-tx arrival + one cp.async arrival per lane
       ptx::mbar_init(&full[s], 1 + 32);
-      // two stager warps + the MMA's commit + four state warps
-      ptx::mbar_init(&empty[s], 3 + 4);
+      // the stager warps + the MMA's commit + four state warps
+      ptx::mbar_init(&empty[s], T5_STAGERS + 1 + 4);
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&vready[b], 2);
+      ptx::mbar_init(&vready[b], T5_STAGERS);
       ptx::mbar_init(&vfree[b], 1);
       ptx::mbar_init(&afull[b], 1);
       ptx::mbar_init(&afree[b], 4);
@@ -152,7 +175,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
-  if (warp == 6) {
+  if (warp == T5_WPROD) {
     // ---------------- producer
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_k);
@@ -171,9 +194,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       const int row0 = sq.b * p.T + sq.bos + chunk_at(it) * BT;
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll 1
-        for (int j = 0; j < K / 8; ++j)
-          ptx::tma_load_3d(slot + T5_RK + j * 1024, &tm_k, 8 * j, h, row0, &full[s]);
+        t5_tma_load_4d(slot + T5_RK, &tm_k, 0, row0, 0, h, &full[s]);
         ptx::tma_load_3d(slot + T5_RV, &tm_v, v0, h, row0, &full[s]);
         if (GV) ptx::tma_load_3d(slot + T5_RG, &tm_g, v0, hg, row0, &full[s]);
       }
@@ -189,9 +210,9 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       ptx::cp_async_mbar_arrive(&full[s]);
     }
-  } else if (warp == 4 || warp == 5) {
-    // ---------------- stagers: thread i = token row i of the chunk
-    const int i = tid - 128;
+  } else if (warp >= 4 && warp < 4 + T5_STAGERS) {
+    // ---------------- stagers: thread (i, half) = token row i, columns 16 half ..
+    const int i = (tid - 128) & 63, half = (tid - 128) >> 6;
     auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
@@ -209,34 +230,43 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
           f *= expf(p.reverse ? g_i : g_l - g_i);
         }
       }
-      float x[T5_VT];
-      {
-        const uint4 *vr = reinterpret_cast<const uint4 *>(slot + T5_RV + i * 64);
+      // the thread's two 16-byte chunks of v row i (64-byte swizzle: chunk c
+      // of row i sits at chunk c ^ ((i >> 1) & 3))
+      float x[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 u = vr[q];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      for (int q = 0; q < 2; ++q) {
+        const int c = (2 * half + q) ^ ((i >> 1) & 3);
+        const uint4 u = *reinterpret_cast<const uint4 *>(slot + T5_RV + i * 64 + c * 16);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[8 * q + 2 * e] = __uint_as_float(w[e] << 16) * f;
-            x[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * f;
-          }
+        for (int e = 0; e < 4; ++e) {
+          x[8 * q + 2 * e] = __uint_as_float(w[e] << 16) * f;
+          x[8 * q + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * f;
         }
       }
       if (GV && i < L) {
-        const float *gr = reinterpret_cast<const float *>(slot + T5_RG);
+        // gv rows of 128 bytes, 128-byte swizzle (chunk c of row r at chunk
+        // c ^ (r & 7)): this thread's 16 columns are chunks 4 half .. 4 half + 3
+        const unsigned char *gt = slot + T5_RG;
 #pragma unroll
-        for (int j = 0; j < T5_VT; ++j)
-          x[j] *= expf(p.reverse ? gr[i * T5_VT + j] : gr[(L - 1) * T5_VT + j] - gr[i * T5_VT + j]);
+        for (int q = 0; q < 4; ++q) {
+          const int c = 4 * half + q;
+          const float4 gi4 = *reinterpret_cast<const float4 *>(gt + i * 128 + (c ^ (i & 7)) * 16);
+          const float4 gl4 = *reinterpret_cast<const float4 *>(gt + (L - 1) * 128 +
+                                                               (c ^ ((L - 1) & 7)) * 16);
+          const float gi[4] = {gi4.x, gi4.y, gi4.z, gi4.w}, gl[4] = {gl4.x, gl4.y, gl4.z, gl4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[4 * q + e] *= expf(p.reverse ? gi[e] : gl[e] - gi[e]);
+        }
       }
       if (it >= 2) ok = ptx::mbar_wait_bounded(&vfree[b], (uint32_t)(((it >> 1) - 1) & 1)) && ok;
       unsigned char *img = vimg + b * T5_VTB;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint4 hi, lo;
         t5_split8(x + 8 * q, hi, lo);
-        *reinterpret_cast<uint4 *>(img + q * 1024 + i * 16) = hi;
-        *reinterpret_cast<uint4 *>(img + (4 + q) * 1024 + i * 16) = lo;
+        *reinterpret_cast<uint4 *>(img + (2 * half + q) * 1024 + i * 16) = hi;
+        *reinterpret_cast<uint4 *>(img + (4 + 2 * half + q) * 1024 + i * 16) = lo;
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
@@ -245,7 +275,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
         ptx::mbar_arrive(&empty[s]);  // this warp has read the slot's v (and gate) tile
       }
     }
-  } else if (warp == 7) {
+  } else if (warp == T5_WMMA) {
     // ---------------- MMA issuer
     const uint32_t id = ptx::idesc_bf16(128, 2 * T5_VT, 1, 1);  // A and B MN-major
 #pragma unroll 1
@@ -257,12 +287,14 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       __syncwarp();
       ptx::tc_fence_after();
       if (lane == 0) {
-        const uint64_t a = ptx::sdesc(ring + s * SLOT + T5_RK, 128, 1024);
+        // A: MN-major, 128-byte swizzle, 64-key atoms columns 8 KB apart, 8-token
+        // groups 1 KB apart; a K step of 16 tokens is two groups (2 KB)
+        const uint64_t a = t5_sdesc_sw128(ring + s * SLOT + T5_RK, 8192, 1024);
         const uint64_t bv = ptx::sdesc(vimg + b * T5_VTB, 128, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(tmem + 64 * b, a + (uint64_t)(ks * 256 >> 4), bv + (uint64_t)(ks * 256 >> 4),
-                        id, ks > 0);
+          ptx::mma_bf16(tmem + 64 * b, a + (uint64_t)(ks * 2048 >> 4),
+                        bv + (uint64_t)(ks * 256 >> 4), id, ks > 0);
         ptx::mma_commit(&afull[b]);
         ptx::mma_commit(&vfree[b]);
         ptx::mma_commit(&empty[s]);
@@ -343,7 +375,8 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (p.gate == GDN_GATE_G_GAMMA) ds = expf(gamma * (float)L);
       float dv[T5_VT];
 #pragma unroll
-      for (int j = 0; j < T5_VT; ++j) dv[j] = GV ? expf(gslot[(L - 1) * T5_VT + j]) : ds;
+      for (int j = 0; j < T5_VT; ++j)  // gv row L - 1, 128-byte swizzle
+        dv[j] = GV ? expf(gslot[(L - 1) * 32 + (((j >> 2) ^ ((L - 1) & 7)) << 2) + (j & 3)]) : ds;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp is done with the slot
       ok = ptx::mbar_wait_bounded(&afull[b], (uint32_t)((it >> 1) & 1)) && ok;
@@ -388,9 +421,10 @@ PFN_cuTensorMapEncodeTiled_v12000 t5_encoder() {
   return fn;
 }
 
-// [rows][heads][dim] tensor of `elt`-byte elements, boxes of width x 1 x 64.
-bool t5_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elt, int dim,
-            int heads, long long rows, int width) {
+// A [rows][heads][dim] tensor of `elt`-byte elements, boxes of width x 1 x 64
+// rows with the given swizzle (width x elt = the swizzle span).
+bool t5_map3(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elt, int dim,
+             int heads, long long rows, int width, CUtensorMapSwizzle sw) {
   auto fn = t5_encoder();
   if (!fn) return false;
   cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows};
@@ -398,7 +432,22 @@ bool t5_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elt,
   cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, type, 3, const_cast<void *>(base), gdim, gstride, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// k ([rows][heads][128] bf16) seen as (64 keys, rows, 2 halves, heads): one
+// box of (64, 64 rows, 2, 1) lands as two 8 KB halves of 64 rows x 128 bytes,
+// 128-byte swizzle.
+bool t5_map_k(CUtensorMap *m, const void *base, int heads, long long rows) {
+  auto fn = t5_encoder();
+  if (!fn) return false;
+  cuuint64_t gdim[4] = {64, (cuuint64_t)rows, 2, (cuuint64_t)heads};
+  cuuint64_t gstride[3] = {(cuuint64_t)heads * T5_KD * 2, 128, T5_KD * 2};
+  cuuint32_t box[4] = {64, 64, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), gdim, gstride, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -414,16 +463,19 @@ cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
   const bool gv = p.gate == GDN_GATE_GV;
   CUtensorMap mk, mv, mg;
   const long long rows = (long long)p.B * p.T;
-  if (!t5_map(&mk, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T5_KD, p.H, rows, 8) ||
-      !t5_map(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.V, p.H, rows, T5_VT))
+  if (!t5_map_k(&mk, p.k, p.H, rows) ||
+      !t5_map3(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.V, p.H, rows, T5_VT,
+               CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   if (gv) {
-    if (!t5_map(&mg, p.gate_values, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.V, p.HG, rows, T5_VT))
+    if (!t5_map3(&mg, p.gate_values, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.V, p.HG, rows, T5_VT,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
     mg = mv;  // unused
   }
-  const size_t smem = T5_NS * t5_slot_bytes(gv) + 2 * T5_VTB + 256;  // + barriers, TMEM slot
+  // + barriers, TMEM slot, and up to 1 KB to align the ring
+  const size_t smem = T5_NS * t5_slot_bytes(gv) + 2 * T5_VTB + 256 + 1024;
   const bool split = p.split > 1, vf = p.v_first != 0;
   auto pick = [&](auto k000, auto k001, auto k010, auto k011, auto k100, auto k101, auto k110,
                   auto k111) {
