@@ -24,7 +24,10 @@
 //   warp 9      MMA: Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64,
 //               K = 64 tokens) into one of two TMEM accumulators
 //   warps 0-3   state: thread r holds key row r, 32 columns, of the fp32
-//               state; per chunk it stores the chunk-start state (when that
+//               state; per chunk each warp writes its 32 x 32 block of the
+//               chunk-start state to a staging tile and one lane stores the
+//               tile by TMA (so the stores leave in whole 64/128-byte rows);
+//               per chunk it stores the chunk-start state (when that
 //               chunk is stored) and applies h = decay o h + Delta_hi + Delta_lo,
 //               the decay read from the chunk's ring slot
 // Every wait is bounded (GDN_ERR_TIMEOUT, then every role still runs every
@@ -48,6 +51,8 @@ constexpr int T5_STAGERS = 4, T5_WPROD = 8, T5_WMMA = 9;
 constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
 // (1024-byte multiples, so every slot's k image stays 1024-aligned)
 constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 21504u; }
+// per state warp two staging tiles of 32 x 32 fp32 (4 KB, 1024-aligned)
+constexpr uint32_t T5_STAGE = 4 * 2 * 4096;
 // v~ image: 64 token rows x 64 columns (hi 0..31, lo 32..63), group stride 1024
 constexpr uint32_t T5_VTB = 8192;
 
@@ -131,7 +136,8 @@ template <bool GV, bool VF, bool SPLIT>
 __global__ void __launch_bounds__(T5_THREADS, 1)
 state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_g, StateParams p) {
+                      const __grid_constant__ CUtensorMap tm_g,
+                      const __grid_constant__ CUtensorMap tm_hs, StateParams p) {
   extern __shared__ __align__(1024) unsigned char sm5_raw[];
   constexpr int K = T5_KD;
   constexpr uint32_t SLOT = t5_slot_bytes(GV);
@@ -139,7 +145,8 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
   unsigned char *sm5 = sm5_raw + ((1024u - (ptx::smem_u32(sm5_raw) & 1023u)) & 1023u);
   unsigned char *ring = sm5;
   unsigned char *vimg = sm5 + T5_NS * SLOT;  // two v~ images
-  uint64_t *bars = reinterpret_cast<uint64_t *>(vimg + 2 * T5_VTB);
+  unsigned char *stage = vimg + 2 * T5_VTB;   // two state staging tiles per state warp
+  uint64_t *bars = reinterpret_cast<uint64_t *>(stage + T5_STAGE);
   uint64_t *full = bars, *empty = bars + T5_NS;
   uint64_t *vready = bars + 2 * T5_NS, *vfree = vready + 2, *afull = vfree + 2, *afree = afull + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(afree + 2);
@@ -325,6 +332,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       for (int j = 0; j < T5_VT; ++j) hs[j] = 0.f;
     }
     auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
+    int nst = 0;  // state tiles this warp has stored
     int store_i = SPLIT && p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
     int store_c = store_i * p.split;
 #pragma unroll 1
@@ -341,30 +349,43 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
       }
       if (sq.write_hs && store) {
-        const size_t sb = ((size_t)slot * H + h) * K * V;
+        // this warp's 32 x 32 block: [key row][column] with 128-byte (fp32) or
+        // 64-byte (bf16) swizzled rows, or [column][key] unswizzled for [V, K]
+        unsigned char *stg = stage + (warp * 2 + (nst & 1)) * 4096;
+        if (lane == 0 && nst >= 2) ptx::bulk_wait_read<1>();  // the tile's store of two stores ago
+        __syncwarp();
         if (VF) {
 #pragma unroll
           for (int j = 0; j < T5_VT; ++j) {
             if (p.hs_bf16)
-              static_cast<__nv_bfloat16 *>(p.hs)[sb + at(j)] = __float2bfloat16_rn(hs[j]);
+              reinterpret_cast<__nv_bfloat16 *>(stg)[j * 32 + lane] = __float2bfloat16_rn(hs[j]);
             else
-              static_cast<float *>(p.hs)[sb + at(j)] = hs[j];
+              reinterpret_cast<float *>(stg)[j * 32 + lane] = hs[j];
           }
         } else if (p.hs_bf16) {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.hs) + sb + at(0));
 #pragma unroll
           for (int q = 0; q < T5_VT / 8; ++q) {
             __nv_bfloat162 w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) w[e] = __floats2bfloat162_rn(hs[8 * q + 2 * e], hs[8 * q + 2 * e + 1]);
-            dst[q] = *reinterpret_cast<const uint4 *>(w);
+            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+                *reinterpret_cast<const uint4 *>(w);
           }
         } else {
-          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.hs) + sb + at(0));
 #pragma unroll
           for (int q = 0; q < T5_VT / 4; ++q)
-            dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
+            *reinterpret_cast<float4 *>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
         }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // hs seen as 2-D: [stored state, head, K or V rows][V or K columns]
+          const long long row0 = (slot * H + h) * (VF ? V : K) + (VF ? v0 : 32 * warp);
+          ptx::tma_store_2d(&tm_hs, VF ? 32 * warp : v0, (int)row0, stg);
+          ptx::bulk_commit();
+        }
+        ++nst;
       }
       // the chunk's decay, from its ring slot
       ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
@@ -390,6 +411,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&afree[b]);
     }
+    if (lane == 0) ptx::bulk_wait<0>();  // the last state tiles are written
     if (p.ht && ok) {
       if (VF) {
 #pragma unroll
@@ -436,6 +458,20 @@ bool t5_map3(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elt
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A [rows][cols] tensor of `elt`-byte elements, boxes of 32 x 32 with the
+// given swizzle (for the stored states).
+bool t5_map2(CUtensorMap *m, void *base, CUtensorMapDataType type, int elt, int cols,
+             long long rows, CUtensorMapSwizzle sw) {
+  auto fn = t5_encoder();
+  if (!fn) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols * elt};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, type, 2, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // k ([rows][heads][128] bf16) seen as (64 keys, rows, 2 halves, heads): one
 // box of (64, 64 rows, 2, 1) lands as two 8 KB halves of 64 rows x 128 bytes,
 // 128-byte swizzle.
@@ -454,7 +490,11 @@ bool t5_map_k(CUtensorMap *m, const void *base, int heads, long long rows) {
 }  // namespace
 
 bool state_pass_tc5_supported(const StateParams &p, bool bf16) {
-  return bf16 && p.K == T5_KD && p.V % T5_VT == 0 && p.T > 0 &&
+  const uintptr_t al = (uintptr_t)p.k | (uintptr_t)p.v | (uintptr_t)p.hs |
+                       (p.gate == GDN_GATE_GV ? (uintptr_t)p.gate_values : 0);
+  // (row coordinates of the stored states are 32-bit)
+  return bf16 && p.K == T5_KD && p.V % T5_VT == 0 && p.T > 0 && al % 16 == 0 &&
+         (!p.hs || p.num_chunks * p.H * (long long)(p.K > p.V ? p.K : p.V) < (1ll << 31)) &&
          (p.gate == GDN_GATE_NONE || p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA ||
           p.gate == GDN_GATE_GV);
 }
@@ -474,8 +514,20 @@ cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
   } else {
     mg = mv;  // unused
   }
-  // + barriers, TMEM slot, and up to 1 KB to align the ring
-  const size_t smem = T5_NS * t5_slot_bytes(gv) + 2 * T5_VTB + 256 + 1024;
+  CUtensorMap mh = mv;  // unused without hs
+  if (p.hs) {
+    const int elt = p.hs_bf16 ? 2 : 4;
+    const int cols = p.v_first ? p.K : p.V, rws = p.v_first ? p.V : p.K;
+    const CUtensorMapSwizzle sw = p.v_first ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                  : p.hs_bf16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!t5_map2(&mh, p.hs, p.hs_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                 elt, cols, (long long)p.num_chunks * p.H * rws, sw))
+      return cudaErrorInvalidValue;
+  }
+  // + state staging, barriers, TMEM slot, and up to 1 KB to align the ring
+  const size_t smem = T5_NS * t5_slot_bytes(gv) + 2 * T5_VTB + T5_STAGE + 256 + 1024;
   const bool split = p.split > 1, vf = p.v_first != 0;
   auto pick = [&](auto k000, auto k001, auto k010, auto k011, auto k100, auto k101, auto k110,
                   auto k111) {
@@ -493,7 +545,7 @@ cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.V / T5_VT), (unsigned)p.H, (unsigned)p.N);
-  kern<<<grid, T5_THREADS, smem, stream>>>(mk, mv, mg, p);
+  kern<<<grid, T5_THREADS, smem, stream>>>(mk, mv, mg, mh, p);
   return cudaGetLastError();
 }
 
