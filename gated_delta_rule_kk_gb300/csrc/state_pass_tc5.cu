@@ -23,11 +23,12 @@
 //               end) into one of two operand images
 //   warp 9      MMA: Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64,
 //               K = 64 tokens) into one of two TMEM accumulators
+//   warp 10     store: one TMA store per stored chunk state, from a ring of
+//               NB staging tiles the state warps fill (so the stores leave in
+//               whole rows and their issue and completion stay off the
+//               state's sequential path)
 //   warps 0-3   state: thread r holds key row r, 32 columns, of the fp32
-//               state; per chunk each warp writes its 32 x 32 block of the
-//               chunk-start state to a staging tile and one lane stores the
-//               tile by TMA (so the stores leave in whole 64/128-byte rows);
-//               per chunk it stores the chunk-start state (when that
+//               state; per chunk it writes the chunk-start state (when that
 //               chunk is stored) and applies h = decay o h + Delta_hi + Delta_lo,
 //               the decay read from the chunk's ring slot
 // Every wait is bounded (GDN_ERR_TIMEOUT, then every role still runs every
@@ -42,8 +43,12 @@
 namespace gdn {
 namespace {
 
-constexpr int T5_THREADS = 320, T5_VT = 32, T5_KD = 128, T5_NS = 4;
-constexpr int T5_STAGERS = 4, T5_WPROD = 8, T5_WMMA = 9;
+constexpr int T5_THREADS = 352, T5_VT = 32, T5_KD = 128, T5_NB = 2;
+// ring depth: the loads take ~2-3 K cycles under load, so the ring is as deep
+// as shared memory allows (a slot holds a chunk from its TMA issue until the
+// stagers and the MMA, and for gv the state warps, are done with it)
+constexpr int t5_ns(bool gv) { return gv ? 6 : 8; }
+constexpr int T5_STAGERS = 4, T5_WPROD = 8, T5_WMMA = 9, T5_WSTORE = 10;
 // ring slot: k image (two 8 KB halves of 64 keys: 64 token rows of 128 bytes,
 // 128-byte swizzle), v tile (64 token rows of 32 bf16, 64-byte swizzle),
 // gate: g per token (64 fp32) or the gv tile (64 token rows of 32 fp32,
@@ -51,8 +56,10 @@ constexpr int T5_STAGERS = 4, T5_WPROD = 8, T5_WMMA = 9;
 constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
 // (1024-byte multiples, so every slot's k image stays 1024-aligned)
 constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 21504u; }
-// per state warp two staging tiles of 32 x 32 fp32 (4 KB, 1024-aligned)
-constexpr uint32_t T5_STAGE = 4 * 2 * 4096;
+// NB staging tiles of one chunk state, 128 x 32 fp32 (16 KB): [key row][32
+// columns] in 128-byte (fp32) or 64-byte (bf16) swizzled rows, or [column]
+// [128 keys] unswizzled for states stored as [V, K]
+constexpr uint32_t T5_TILE = 16384, T5_STAGE = T5_NB * T5_TILE;
 // v~ image: 64 token rows x 64 columns (hi 0..31, lo 32..63), group stride 1024
 constexpr uint32_t T5_VTB = 8192;
 
@@ -115,6 +122,29 @@ __device__ __forceinline__ void t5_split8(const float *f, uint4 &hi, uint4 &lo) 
   lo = *reinterpret_cast<const uint4 *>(l2);
 }
 
+// The stored-state index of each chunk in processing order: every chunk, or
+// with `split` > 1 every split-th one (chunk 0, split, ..), numbered from the
+// sequence's first stored state; next() returns -1 for a chunk not stored.
+struct T5Stores {
+  long long first;
+  int split, step, store_i, store_c;
+  __device__ T5Stores(const StateParams &p, long long first_, int nch) : first(first_) {
+    split = p.split;
+    step = p.reverse ? -1 : 1;
+    store_i = split > 1 && p.reverse && nch > 0 ? (nch - 1) / split : 0;
+    store_c = store_i * split;
+  }
+  template <bool SPLIT>
+  __device__ long long next(int c) {
+    if (!SPLIT) return first + c;
+    if (c != store_c) return -1;
+    const long long slot = first + store_i;
+    store_c += step * split;
+    store_i += step;
+    return slot;
+  }
+};
+
 __device__ __forceinline__ void t5_tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2,
                                                int c3, uint64_t *bar) {
   asm volatile(
@@ -144,12 +174,14 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
   // the swizzle patterns follow address bits 4-9: slots start on 1024 bytes
   unsigned char *sm5 = sm5_raw + ((1024u - (ptx::smem_u32(sm5_raw) & 1023u)) & 1023u);
   unsigned char *ring = sm5;
+  constexpr int T5_NS = t5_ns(GV);
   unsigned char *vimg = sm5 + T5_NS * SLOT;  // two v~ images
-  unsigned char *stage = vimg + 2 * T5_VTB;   // two state staging tiles per state warp
+  unsigned char *stage = vimg + 2 * T5_VTB;   // NB state staging tiles
   uint64_t *bars = reinterpret_cast<uint64_t *>(stage + T5_STAGE);
   uint64_t *full = bars, *empty = bars + T5_NS;
   uint64_t *vready = bars + 2 * T5_NS, *vfree = vready + 2, *afull = vfree + 2, *afree = afull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(afree + 2);
+  uint64_t *staged = afree + 2, *stfree = staged + T5_NB;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(stfree + T5_NB);
   __shared__ long long seq_sh[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -164,14 +196,19 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int s = 0; s < T5_NS; ++s) {
       // the producer's expect-tx arrival + one cp.async arrival per lane
       ptx::mbar_init(&full[s], 1 + 32);
-      // the stager warps + the MMA's commit + four state warps
-      ptx::mbar_init(&empty[s], T5_STAGERS + 1 + 4);
+      // the stager warps + the MMA's commit (+ for gv the four state warps,
+      // which read the chunk's last gate row there)
+      ptx::mbar_init(&empty[s], T5_STAGERS + 1 + (GV ? 4 : 0));
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&vready[b], T5_STAGERS);
       ptx::mbar_init(&vfree[b], 1);
       ptx::mbar_init(&afull[b], 1);
       ptx::mbar_init(&afree[b], 4);
+    }
+    for (int b = 0; b < T5_NB; ++b) {
+      ptx::mbar_init(&staged[b], 4);  // the four state warps
+      ptx::mbar_init(&stfree[b], 1);  // the store warp
     }
     ptx::fence_mbar_init();
   }
@@ -308,6 +345,30 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       __syncwarp();
     }
+  } else if (warp == T5_WSTORE) {
+    // ---------------- store: one TMA store per staged chunk state
+    if (lane == 0 && sq.write_hs) {
+      ptx::prefetch_tmap(&tm_hs);
+      T5Stores stores(p, sq.first, sq.nch);
+      int nst = 0;
+#pragma unroll 1
+      for (int it = 0; it < sq.nch; ++it) {
+        const long long slot = stores.next<SPLIT>(chunk_at(it));
+        if (slot < 0) continue;
+        const int sb = nst % T5_NB;
+        ok = ptx::mbar_wait_bounded(&staged[sb], (uint32_t)((nst / T5_NB) & 1)) && ok;
+        // hs seen as 2-D: [stored state, head, K or V rows][V or K columns]
+        const long long row0 = (slot * H + h) * (VF ? V : K) + (VF ? v0 : 0);
+        ptx::tma_store_2d(&tm_hs, VF ? 0 : v0, (int)row0, stage + sb * T5_TILE);
+        ptx::bulk_commit();
+        if (nst > 0) {  // the previous tile has been read: hand it back
+          ptx::bulk_wait_read<1>();
+          ptx::mbar_arrive(&stfree[(nst - 1) % T5_NB]);
+        }
+        ++nst;
+      }
+      ptx::bulk_wait<0>();  // every chunk state is written
+    }
   } else {
     // ---------------- state warps 0-3: key row r, columns v0 .. v0 + 31
     const int r = warp * 32 + lane;
@@ -332,35 +393,30 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       for (int j = 0; j < T5_VT; ++j) hs[j] = 0.f;
     }
     auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
-    int nst = 0;  // state tiles this warp has stored
-    int store_i = SPLIT && p.reverse && sq.nch > 0 ? (sq.nch - 1) / p.split : 0;
-    int store_c = store_i * p.split;
+    int nst = 0;  // chunk states written to the staging ring
+    T5Stores stores(p, sq.first, sq.nch);
+    // gate g at the chunk's last row (chunk-local cumulative sum)
+    auto g_end = [&](int it) {
+      const long long row = (long long)sq.b * p.T + sq.bos + chunk_at(it) * BT + len_of(it) - 1;
+      return p.gate_values[row * HG + hg];
+    };
+    float g_next = p.gate == GDN_GATE_G && sq.nch > 0 ? g_end(0) : 0.f;
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
-      const int c = chunk_at(it), b = it & 1, s = it % T5_NS;
-      bool store = true;
-      long long slot = sq.first + c;
-      if (SPLIT) {
-        store = c == store_c;
-        slot = sq.first + store_i;
-        if (store) {
-          store_c += p.reverse ? -p.split : p.split;
-          store_i += p.reverse ? -1 : 1;
-        }
-      }
-      if (sq.write_hs && store) {
-        // this warp's 32 x 32 block: [key row][column] with 128-byte (fp32) or
-        // 64-byte (bf16) swizzled rows, or [column][key] unswizzled for [V, K]
-        unsigned char *stg = stage + (warp * 2 + (nst & 1)) * 4096;
-        if (lane == 0 && nst >= 2) ptx::bulk_wait_read<1>();  // the tile's store of two stores ago
-        __syncwarp();
+      const int b = it & 1, s = it % T5_NS;
+      const long long slot = stores.next<SPLIT>(chunk_at(it));
+      if (sq.write_hs && slot >= 0) {
+        const int sb = nst % T5_NB;
+        unsigned char *stg = stage + sb * T5_TILE;
+        if (nst >= T5_NB)  // the store warp has read the tile's previous state
+          ok = ptx::mbar_wait_bounded(&stfree[sb], (uint32_t)((nst / T5_NB - 1) & 1)) && ok;
         if (VF) {
 #pragma unroll
           for (int j = 0; j < T5_VT; ++j) {
             if (p.hs_bf16)
-              reinterpret_cast<__nv_bfloat16 *>(stg)[j * 32 + lane] = __float2bfloat16_rn(hs[j]);
+              reinterpret_cast<__nv_bfloat16 *>(stg)[j * K + r] = __float2bfloat16_rn(hs[j]);
             else
-              reinterpret_cast<float *>(stg)[j * 32 + lane] = hs[j];
+              reinterpret_cast<float *>(stg)[j * K + r] = hs[j];
           }
         } else if (p.hs_bf16) {
 #pragma unroll
@@ -368,38 +424,41 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
             __nv_bfloat162 w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) w[e] = __floats2bfloat162_rn(hs[8 * q + 2 * e], hs[8 * q + 2 * e + 1]);
-            *reinterpret_cast<uint4 *>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+            *reinterpret_cast<uint4 *>(stg + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) =
                 *reinterpret_cast<const uint4 *>(w);
           }
         } else {
 #pragma unroll
           for (int q = 0; q < T5_VT / 4; ++q)
-            *reinterpret_cast<float4 *>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<float4 *>(stg + r * 128 + ((q ^ (r & 7)) << 4)) =
                 make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          // hs seen as 2-D: [stored state, head, K or V rows][V or K columns]
-          const long long row0 = (slot * H + h) * (VF ? V : K) + (VF ? v0 : 32 * warp);
-          ptx::tma_store_2d(&tm_hs, VF ? 32 * warp : v0, (int)row0, stg);
-          ptx::bulk_commit();
-        }
+        if (lane == 0) ptx::mbar_arrive(&staged[sb]);
         ++nst;
       }
-      // the chunk's decay, from its ring slot
-      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
-      const int L = len_of(it);
-      const float *gslot = reinterpret_cast<const float *>(ring + s * SLOT + T5_RG);
-      float ds = 1.f;
-      if (p.gate == GDN_GATE_G) ds = expf(gslot[L - 1]);
-      if (p.gate == GDN_GATE_G_GAMMA) ds = expf(gamma * (float)L);
+      // the chunk's decay: for gv from its ring slot, for g from the gate
+      // value loaded one chunk ahead
+      const float g_cur = g_next;
+      if (p.gate == GDN_GATE_G && it + 1 < sq.nch) g_next = g_end(it + 1);
       float dv[T5_VT];
+      if (GV) {
+        ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
+        const int L = len_of(it);
+        const float *gslot = reinterpret_cast<const float *>(ring + s * SLOT + T5_RG);
 #pragma unroll
-      for (int j = 0; j < T5_VT; ++j)  // gv row L - 1, 128-byte swizzle
-        dv[j] = GV ? expf(gslot[(L - 1) * 32 + (((j >> 2) ^ ((L - 1) & 7)) << 2) + (j & 3)]) : ds;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp is done with the slot
+        for (int j = 0; j < T5_VT; ++j)  // gv row L - 1, 128-byte swizzle
+          dv[j] = expf(gslot[(L - 1) * 32 + (((j >> 2) ^ ((L - 1) & 7)) << 2) + (j & 3)]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp is done with the slot
+      } else {
+        float ds = 1.f;
+        if (p.gate == GDN_GATE_G) ds = expf(g_cur);
+        if (p.gate == GDN_GATE_G_GAMMA) ds = expf(gamma * (float)len_of(it));
+#pragma unroll
+        for (int j = 0; j < T5_VT; ++j) dv[j] = ds;
+      }
       ok = ptx::mbar_wait_bounded(&afull[b], (uint32_t)((it >> 1) & 1)) && ok;
       ptx::tc_fence_after();
       float dh[T5_VT], dl[T5_VT];
@@ -411,7 +470,6 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&afree[b]);
     }
-    if (lane == 0) ptx::bulk_wait<0>();  // the last state tiles are written
     if (p.ht && ok) {
       if (VF) {
 #pragma unroll
@@ -458,15 +516,15 @@ bool t5_map3(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elt
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A [rows][cols] tensor of `elt`-byte elements, boxes of 32 x 32 with the
+// A [rows][cols] tensor of `elt`-byte elements, boxes of bw x bh with the
 // given swizzle (for the stored states).
 bool t5_map2(CUtensorMap *m, void *base, CUtensorMapDataType type, int elt, int cols,
-             long long rows, CUtensorMapSwizzle sw) {
+             long long rows, int bw, int bh, CUtensorMapSwizzle sw) {
   auto fn = t5_encoder();
   if (!fn) return false;
   cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t gstride[1] = {(cuuint64_t)cols * elt};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {(cuuint32_t)bw, (cuuint32_t)bh};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, type, 2, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -523,11 +581,12 @@ cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
                                               : CU_TENSOR_MAP_SWIZZLE_128B;
     if (!t5_map2(&mh, p.hs, p.hs_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                 elt, cols, (long long)p.num_chunks * p.H * rws, sw))
+                 elt, cols, (long long)p.num_chunks * p.H * rws, p.v_first ? T5_KD : T5_VT,
+                 p.v_first ? T5_VT : T5_KD, sw))
       return cudaErrorInvalidValue;
   }
   // + state staging, barriers, TMEM slot, and up to 1 KB to align the ring
-  const size_t smem = T5_NS * t5_slot_bytes(gv) + 2 * T5_VTB + T5_STAGE + 256 + 1024;
+  const size_t smem = t5_ns(gv) * t5_slot_bytes(gv) + 2 * T5_VTB + T5_STAGE + 256 + 1024;
   const bool split = p.split > 1, vf = p.v_first != 0;
   auto pick = [&](auto k000, auto k001, auto k010, auto k011, auto k100, auto k101, auto k110,
                   auto k111) {
