@@ -19,8 +19,9 @@
 //    of ready-made operand images the sequential pass consumes directly:
 //      AW  [-w ; q] (bf16)                U   u (fp32, per 32-wide V tile)
 //      KT  [k~_hi ; k~_lo] (bf16 pair,    SC  exp(gamma_L) per key row,
-//          k~ = k e^{gamma_L - gamma})        exp(gamma_L - gamma_i) and
-//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)      scale exp(gamma_i) per token
+//          k~ = k e^{gamma_L - gamma};        exp(gamma_L - gamma_i) and
+//          per-channel gate only)             scale exp(gamma_i) per token
+//      AQ  [Aqk_lo ; Aqk_hi] (bf16 pair)
 //    For the per-channel gate (KDA, vLLM kimi_k3 kda/chunk_intra,
 //    chunk_kda_fwd_kernel_inter_solve_fused) the exponentials move into the
 //    operands: S = [k e^g; q e^g] (k e^-g)^T with the chunk start as the
@@ -36,8 +37,12 @@
 //    whole sequence).  Per chunk
 //      D1  = [-w ; q~] [h_hi | h_lo]      rows 0..63: -w h, rows 64..127: q h
 //      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
-//      DH  = k~^T v_new                  (k~ = k e^{gamma_L - gamma} as a hi + lo
-//                                         pair, from KT: the state update keeps
+//      DH  = k~^T v_new                  (scalar gate: k^T (e^{gamma_L - gamma} v_new),
+//                                         the factor on v_new's hi + lo pair and k
+//                                         read raw from the input by TMA, exact in
+//                                         bf16; per-channel gate: k~ = k
+//                                         e^{gamma_L - g} as a hi + lo pair from
+//                                         KT; either way the state update keeps
 //                                         fp32-grade accuracy over long memories)
 //      D5  = [Aqk_lo ; Aqk_hi] v_new
 //      h   = exp(gamma_L) h + DH
@@ -627,23 +632,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     }
     ptx::mma_commit(&bars[1]);
   }
-  if (!KDA) {
-    // KT = k e^{gamma_L - gamma_i} (zero on padding rows) as a hi + lo pair,
-    // straight into the block while the GEMM runs; the chain's state update
-    // takes it as is
-    for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
-      const int i = pc & 63, cg = pc >> 6;
-      float kf[8];
-      unpack8(*reinterpret_cast<const uint4 *>(KQ + img_off(i, 8 * cg, 2048)), kf);
-      const float r = sc[128 + i];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) kf[e] *= r;
-      uint4 hi, lo;
-      split8(kf, hi, lo);
-      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 2048)) = hi;
-      *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(64 + i, 8 * cg, 2048)) = lo;
-    }
-  }
+  // (scalar gate: no KT -- the chain reads k raw and puts e^{gamma_L - gamma_i}
+  // on v_new)
   const bool ok1 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
   mma_phase ^= 1;
   ptx::tc_fence_after();
@@ -847,12 +837,16 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 //
 // shared memory: two stages holding one operand block each
 //   AW  [0, 32768)       [-w ; q~] (128 x 128, cs 2048)
-//   KT  [32768, 65536)   [k~_hi ; k~_lo] (128 token rows x 128 keys, cs 2048)
+//   KT  [32768, 65536)   [k~_hi ; k~_lo] (128 token rows x 128 keys, cs 2048);
+//                        scalar gate: raw k of the chunk by TMA, two 8 KB halves
+//                        of 64 keys x 64 token rows (128-byte swizzle)
 //   AQ  [65536, 81920)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
 //   SC  [81920, 82944)   decay[128], rs[64], qs[64]
 //   U   [82944, 91136)   u tile, fp32 64 x 32 (row-swizzled 16-byte groups)
 // then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo]
-// (64 tokens x 64, cs 1024) and the fp32 exchange X.  A stage is filled and
+// (64 tokens x 64, cs 1024; scalar gate: e^{gamma_L - gamma_i} v_new, the
+// state update's operand, with v_new itself for the output GEMM in VN2) and
+// the fp32 exchange X.  A stage is filled and
 // released in two halves: AW, SC and U are free once D1 has run and v_new is
 // formed, KT and AQ only after the output GEMM, so the first half of the next
 // block but one streams in half a step earlier.
@@ -861,8 +855,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 // halves side by side and the epilogue adds them.
 constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 65536, S_SC = 81920, S_U = 82944,
                    STAGE_BYTES = 91136;
-constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_X = C_VN + 8192,
-                   C_BAR = C_X + 64 * 33 * 4, C_SMEM = C_BAR + 256;
+constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_VN2 = C_VN + 8192,
+                   C_X = C_VN2 + 8192, C_BAR = C_X + 64 * 33 * 4,
+                   C_SMEM = C_BAR + 256 + 1024;  // + up to 1 KB to align the base
 constexpr int CHAIN_THREADS = 320;
 constexpr int EPI_WARPS = 8;
 // Named barriers of the chain kernel (1 is the epilogue warps' own).  The
@@ -872,6 +867,7 @@ constexpr int EPI_WARPS = 8;
 // never overlap; every role runs every chunk, so every phase completes.
 constexpr int BAR_HREADY = 2, BAR_HREADY_THREADS = 32 * (EPI_WARPS + 1);
 constexpr int BAR_VNREADY = 3, BAR_VNREADY_THREADS = 32 * (4 + 1);  // warps 0, 1, 4, 5 + MMA
+constexpr int BAR_VN2READY = 4;  // (scalar gate) v_new for the output GEMM, same threads
 
 __device__ __forceinline__ void bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -908,10 +904,27 @@ __device__ __forceinline__ void store_pair16(unsigned char *img, int r, int c0, 
   }
 }
 
-__global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(ptx::smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(ptx::smem_u32(bar))
+      : "memory");
+}
+
+// RAWK (scalar gate): the state update reads k raw (tm_k: 4-D map of k as
+// (64 keys, rows, 2 halves, key heads), 128-byte swizzle) and the token
+// factors ride on v_new; otherwise (per-channel gate) it reads KT.
+template <bool RAWK>
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128-byte swizzle follows address bits 4-9: the stages start on 1 KB
+  unsigned char *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char *Himg = smem + C_H;
   unsigned char *VN = smem + C_VN;
+  unsigned char *VN2 = RAWK ? smem + C_VN2 : VN;
   float *X = reinterpret_cast<float *>(smem + C_X);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C_BAR);
   // each stage has two halves with their own barriers: A = AW, SC, U (read
@@ -1002,8 +1015,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
     // of chunk c (output GEMM of chunk c - 2), so waiting in the order
     // A(c), B(c), A(c + 1), ... never holds a release back.
     if (lane == 0) {
+      if (RAWK) ptx::prefetch_tmap(&tm_k);
+      const int hk = h / (p.H / p.Hk);
       // a transition tile's u is zero: its U tile is not loaded
-      const uint32_t A_BYTES = 32768 + 1024 + (trans ? 0 : 8192), B_BYTES = 49152;
+      const uint32_t A_BYTES = 32768 + 1024 + (trans ? 0 : 8192), B_BYTES = RAWK ? 32768 : 49152;
 #pragma unroll 1
       for (int c = 0; c < nch; ++c) {
         const int s = c & 1, k = c >> 1;
@@ -1023,7 +1038,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
           *abort_flag = 1;
         }
         ptx::mbar_arrive_expect_tx(&fullB[s], B_BYTES);
-        ptx::bulk_g2s(st + S_KT, src + OFF_KT, B_BYTES, &fullB[s]);  // KT, AQ
+        if (RAWK) {
+          // k rows of the chunk (rows past the tensor read as zero; rows
+          // past the sequence meet zero factors on v_new)
+          tma_load_4d(st + S_KT, &tm_k, 0, b * p.T + bos + (cfirst + c) * BT, 0, hk, &fullB[s]);
+          ptx::bulk_g2s(st + S_AQ, src + OFF_AQ, 16384, &fullB[s]);
+        } else {
+          ptx::bulk_g2s(st + S_KT, src + OFF_KT, B_BYTES, &fullB[s]);  // KT, AQ
+        }
       }
     }
   } else if (warp == EPI_WARPS + 1) {
@@ -1058,16 +1080,33 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
       bar_sync(BAR_VNREADY, BAR_VNREADY_THREADS);  // v_new is in VN
       ptx::tc_fence_after();
       if (lane == 0) {
-        // DH = [k~_hi ; k~_lo]^T [vn_hi | vn_lo ; vn_hi | vn_lo] (K = 128: the
-        // token rows once with each half of k~; critical path), then
-        // D5 = AQ [vn_hi | vn_lo]
+        if (RAWK) {
+          // DH = k^T [v~_hi | v~_lo] (K = 64 tokens; k MN-major, 128-byte
+          // swizzle: 64-key halves 8 KB apart, 8-token groups 1 KB apart)
+          const uint64_t kr = ptx::sdesc(st + S_KT, 8192, 1024) | (2ull << 61);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 256), id_mnmn, ks > 0);
+          for (int ks = 0; ks < 4; ++ks)
+            ptx::mma_bf16(dDH, adv(kr, ks * 2048), adv(dVN0, ks * 256), id_mnmn, ks > 0);
+        } else {
+          // DH = [k~_hi ; k~_lo]^T [vn_hi | vn_lo ; vn_hi | vn_lo] (K = 128:
+          // the token rows once with each half of k~; critical path)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 256), id_mnmn, ks > 0);
+        }
         ptx::mma_commit(d3);
+      }
+      if (RAWK) {
+        __syncwarp();
+        bar_sync(BAR_VN2READY, BAR_VNREADY_THREADS);  // v_new itself is in VN2
+        ptx::tc_fence_after();
+      }
+      if (lane == 0) {
+        // D5 = AQ [vn_hi | vn_lo]
+        const uint64_t dVN2 = ptx::sdesc(VN2, 128, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN0, ks * 256), id_kmn, ks > 0);
+          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN2, ks * 256), id_kmn, ks > 0);
         ptx::mma_commit(d5);
         ptx::mma_commit(&emptyB[s]);
       }
@@ -1150,11 +1189,27 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(TcParams p) {
             vn[4 * q + 2] = u.z + d[4 * q + 2];
             vn[4 * q + 3] = u.w + d[4 * q + 3];
           }
-          store_pair16(VN, r, c0, 1024, vn);
+          if (RAWK) {
+            // the state update's operand: e^{gamma_L - gamma_r} v_new (zero
+            // on padding rows), then v_new itself for the output GEMM
+            const float f = scs[128 + r];
+            float vt[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vt[j] = f * vn[j];
+            store_pair16(VN, r, c0, 1024, vt);
+          } else {
+            store_pair16(VN, r, c0, 1024, vn);
+          }
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
           __syncwarp();
           bar_arrive(BAR_VNREADY, BAR_VNREADY_THREADS);
+          if (RAWK) {
+            store_pair16(VN2, r, c0, 1024, vn);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            bar_arrive(BAR_VN2READY, BAR_VNREADY_THREADS);
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) qh[j] = d[j];
@@ -1354,6 +1409,21 @@ bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long ro
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// k ([rows][heads][128] bf16) seen as (64 keys, rows, 2 halves, heads): one
+// box of (64, 64 rows, 2, 1) lands as two 8 KB halves of 64 rows x 128 bytes,
+// 128-byte swizzle (the MN-major operand the state update reads).
+bool make_k_sw128_map(CUtensorMap *m, const void *base, int heads, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[4] = {64, (cuuint64_t)rows, 2, (cuuint64_t)heads};
+  cuuint64_t gstride[3] = {(cuuint64_t)heads * KD * 2, 128, KD * 2};
+  cuuint32_t box[4] = {64, 64, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), gdim, gstride, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t table_bytes(int N) { return ((2 * (size_t)N + 1) * 4 + 255) / 256 * 256; }
 
 int sm_count() {
@@ -1481,16 +1551,23 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   ik<<<dim3((unsigned)nchunks, cp.H), INTRA_THREADS, ismem, stream>>>(mk, mq, mv, mg, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+  CUtensorMap mkr;
+  if (kda) {
+    mkr = mk;  // unused: the per-channel chain reads KT
+  } else if (!make_k_sw128_map(&mkr, cp.k, cp.Hk, rows)) {
+    return cudaErrorInvalidValue;
+  }
+  auto chain = kda ? chain_kernel<false> : chain_kernel<true>;
+  e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
   if (S <= 1) {
-    chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(p);
+    chain<<<dim3(cp.V / VTILE, cp.H, cp.N), CHAIN_THREADS, C_SMEM, stream>>>(mkr, p);
     return cudaGetLastError();
   }
   // segment-parallel: every segment at once (transition and value tiles),
   // the combine, then segments 1.. again from their true start states
   p.seg_phase = 1;
-  chain_kernel<<<dim3(KD / VTILE + cp.V / VTILE, cp.H, cp.N * S), CHAIN_THREADS, C_SMEM, stream>>>(p);
+  chain<<<dim3(KD / VTILE + cp.V / VTILE, cp.H, cp.N * S), CHAIN_THREADS, C_SMEM, stream>>>(mkr, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)COMB_SMEM);
@@ -1498,7 +1575,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   segment_combine_kernel<<<dim3(cp.V / COMB_COLS, cp.H, cp.N), COMB_THREADS, COMB_SMEM, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.seg_phase = 2;
-  chain_kernel<<<dim3(cp.V / VTILE, cp.H, cp.N * (S - 1)), CHAIN_THREADS, C_SMEM, stream>>>(p);
+  chain<<<dim3(cp.V / VTILE, cp.H, cp.N * (S - 1)), CHAIN_THREADS, C_SMEM, stream>>>(mkr, p);
   return cudaGetLastError();
 }
 
