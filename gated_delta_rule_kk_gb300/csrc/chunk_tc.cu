@@ -1014,38 +1014,41 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
     // Half A of chunk c + 1 is released (v_new of chunk c - 1) before half B
     // of chunk c (output GEMM of chunk c - 2), so waiting in the order
     // A(c), B(c), A(c + 1), ... never holds a release back.
-    if (lane == 0) {
-      if (RAWK) ptx::prefetch_tmap(&tm_k);
-      const int hk = h / (p.H / p.Hk);
-      // a transition tile's u is zero: its U tile is not loaded
-      const uint32_t A_BYTES = 32768 + 1024 + (trans ? 0 : 8192), B_BYTES = RAWK ? 32768 : 49152;
+    // Each copy has its own lane: the copies one thread issues complete one
+    // after another, those of different threads overlap.
+    if (lane == 0 && RAWK) ptx::prefetch_tmap(&tm_k);
+    const int hk = h / (p.H / p.Hk);
+    // a transition tile's u is zero: its U tile is not loaded
+    const uint32_t A_BYTES = 32768 + 1024 + (trans ? 0 : 8192), B_BYTES = RAWK ? 32768 : 49152;
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c) {
-        const int s = c & 1, k = c >> 1;
-        unsigned char *st = smem + s * STAGE_BYTES;
-        const unsigned char *src =
-            p.blocks + ((size_t)(base + cfirst + c) * p.H + h) * p.block;
-        if (k > 0 && !ptx::mbar_wait_bounded(&emptyA[s], (uint32_t)((k - 1) & 1))) {
-          record_error(p.err, GDN_ERR_TIMEOUT);  // keep going: no role may stall the others
-          *abort_flag = 1;
-        }
-        ptx::mbar_arrive_expect_tx(&fullA[s], A_BYTES);
-        ptx::bulk_g2s(st + S_AW, src + OFF_AW, 32768, &fullA[s]);
-        ptx::bulk_g2s(st + S_SC, src + OFF_SC, 1024, &fullA[s]);
-        if (!trans) ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &fullA[s]);
-        if (k > 0 && !ptx::mbar_wait_bounded(&emptyB[s], (uint32_t)((k - 1) & 1))) {
-          record_error(p.err, GDN_ERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        ptx::mbar_arrive_expect_tx(&fullB[s], B_BYTES);
-        if (RAWK) {
-          // k rows of the chunk (rows past the tensor read as zero; rows
-          // past the sequence meet zero factors on v_new)
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & 1, k = c >> 1;
+      unsigned char *st = smem + s * STAGE_BYTES;
+      const unsigned char *src = p.blocks + ((size_t)(base + cfirst + c) * p.H + h) * p.block;
+      if (k > 0 && !ptx::mbar_wait_bounded(&emptyA[s], (uint32_t)((k - 1) & 1)) && lane == 0) {
+        record_error(p.err, GDN_ERR_TIMEOUT);  // keep going: no role may stall the others
+        *abort_flag = 1;
+      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&fullA[s], A_BYTES);
+      __syncwarp();
+      if (lane == 0) ptx::bulk_g2s(st + S_AW, src + OFF_AW, 32768, &fullA[s]);
+      if (lane == 1) ptx::bulk_g2s(st + S_SC, src + OFF_SC, 1024, &fullA[s]);
+      if (lane == 2 && !trans) ptx::bulk_g2s(st + S_U, src + OFF_U + vt * 8192, 8192, &fullA[s]);
+      if (k > 0 && !ptx::mbar_wait_bounded(&emptyB[s], (uint32_t)((k - 1) & 1)) && lane == 0) {
+        record_error(p.err, GDN_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&fullB[s], B_BYTES);
+      __syncwarp();
+      if (RAWK) {
+        // k rows of the chunk (rows past the tensor read as zero; rows past
+        // the sequence meet zero factors on v_new)
+        if (lane == 3)
           tma_load_4d(st + S_KT, &tm_k, 0, b * p.T + bos + (cfirst + c) * BT, 0, hk, &fullB[s]);
-          ptx::bulk_g2s(st + S_AQ, src + OFF_AQ, 16384, &fullB[s]);
-        } else {
-          ptx::bulk_g2s(st + S_KT, src + OFF_KT, B_BYTES, &fullB[s]);  // KT, AQ
-        }
+        if (lane == 4) ptx::bulk_g2s(st + S_AQ, src + OFF_AQ, 16384, &fullB[s]);
+      } else {
+        if (lane == 3) ptx::bulk_g2s(st + S_KT, src + OFF_KT, 32768, &fullB[s]);
+        if (lane == 4) ptx::bulk_g2s(st + S_AQ, src + OFF_AQ, 16384, &fullB[s]);
       }
     }
   } else if (warp == EPI_WARPS + 1) {

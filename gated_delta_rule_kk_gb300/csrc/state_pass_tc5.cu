@@ -10,8 +10,9 @@
 // ahead of the state: only the element-wise update is sequential.
 //
 // One CTA per (32-column V tile, head, sequence), 320 threads:
-//   warp 8      producer: one TMA each for the chunk's k tile, its v tile and,
-//               for gv, its gate tile, into a ring of NS slots, all with
+//   warp 8      producer: one TMA each (from lanes 0, 1, 2) for the chunk's k
+//               tile, its v tile and, for gv, its gate tile, into a ring of
+//               NS slots, all with
 //               swizzled rows of 64 or 128 bytes (a TMA moves a box row by
 //               row, so narrow rows cost requests): k lands as two 128-byte
 //               swizzled MN-major atoms columns (keys 0-63 and 64-127) that
@@ -236,12 +237,13 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       __syncwarp();
       unsigned char *slot = ring + s * SLOT;
       const int row0 = sq.b * p.T + sq.bos + chunk_at(it) * BT;
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&full[s], bytes);
-        t5_tma_load_4d(slot + T5_RK, &tm_k, 0, row0, 0, h, &full[s]);
-        ptx::tma_load_3d(slot + T5_RV, &tm_v, v0, h, row0, &full[s]);
-        if (GV) ptx::tma_load_3d(slot + T5_RG, &tm_g, v0, hg, row0, &full[s]);
-      }
+      // one copy per lane: the copies one thread issues complete one after
+      // another, those of different threads overlap
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&full[s], bytes);
+      __syncwarp();
+      if (lane == 0) t5_tma_load_4d(slot + T5_RK, &tm_k, 0, row0, 0, h, &full[s]);
+      if (lane == 1) ptx::tma_load_3d(slot + T5_RV, &tm_v, v0, h, row0, &full[s]);
+      if (GV && lane == 2) ptx::tma_load_3d(slot + T5_RG, &tm_g, v0, hg, row0, &full[s]);
       if (p.gate == GDN_GATE_G) {
         // g of the chunk's 64 rows (rows past the tensor read as zero)
 #pragma unroll
