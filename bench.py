@@ -338,7 +338,8 @@ def run_ours(args, rank, world, dev):
             "tokens_per_s": vtok / (vt / 1e3), "ms_per_call": vt,
             "roofline": {"bound": "hbm", "achieved": vb / (vt / 1e3) / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": vb / (vt / 1e3) / 1e9 / hbm,
-                         "algorithmic_bytes": vb, "algorithmic_flops": vf, "traffic": None}}
+                         "algorithmic_bytes": vb, "algorithmic_flops": vf,
+                         "traffic": traffic_record("gdn_varlen")}}
         del vd, vo, vht, vin
         # few long chains: one sequence of 8192 tokens, two heads (8 chains of
         # 32 value columns on 152 SMs): the library's segment-parallel state
@@ -364,7 +365,7 @@ def run_ours(args, rank, world, dev):
             "tokens_per_s": 8192 / (ftimes[0] / 1e3),
             "roofline": {"bound": "hbm", "achieved": fb / (ftimes[0] / 1e3) / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": fb / (ftimes[0] / 1e3) / 1e9 / hbm,
-                         "algorithmic_bytes": fb, "traffic": None}}
+                         "algorithmic_bytes": fb, "traffic": traffic_record("gdn_few_chains")}}
         del fd, fo, fht, fin
         # chunk state pass (gated linear attention), per-token gate and per-key gate
         for sgate in ("g", "gk"):
