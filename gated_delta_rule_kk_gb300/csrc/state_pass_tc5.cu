@@ -44,25 +44,35 @@
 namespace gdn {
 namespace {
 
-constexpr int T5_THREADS = 352, T5_VT = 32, T5_KD = 128, T5_NB = 2;
+constexpr int T5_VT = 32, T5_KD = 128, T5_NB = 2;
 // ring depth: the loads take ~2-3 K cycles under load, so the ring is as deep
 // as shared memory allows (a slot holds a chunk from its TMA issue until the
 // stagers and the MMA, and for gv the state warps, are done with it)
-constexpr int t5_ns(bool gv) { return gv ? 6 : 8; }
-constexpr int T5_STAGERS = 4, T5_WPROD = 8, T5_WMMA = 9, T5_WSTORE = 10;
+// gate modes: 0 = value-side scalar gates (g, g_gamma, none), 1 = gv, 2 = gk
+constexpr int t5_ns(int gm) { return gm == 1 ? 6 : gm == 2 ? 3 : 8; }
+// warps 0-3 state, then the stagers (8 for gk, whose k~ takes an exponential
+// per element, else 4), the producer, the MMA issuer and the store warp
+constexpr int t5_stagers(int gm) { return gm == 2 ? 8 : 4; }
+constexpr int t5_threads(int gm) { return 32 * (7 + t5_stagers(gm)); }
 // ring slot: k image (two 8 KB halves of 64 keys: 64 token rows of 128 bytes,
 // 128-byte swizzle), v tile (64 token rows of 32 bf16, 64-byte swizzle),
-// gate: g per token (64 fp32) or the gv tile (64 token rows of 32 fp32,
-// 128-byte swizzle), all inside the slot
+// gate: g per token (64 fp32), the gv tile (64 token rows of 32 fp32) or the
+// gk tile (four 8 KB boxes of 32 keys x 64 token rows fp32), 128-byte swizzle,
+// all inside the slot
 constexpr uint32_t T5_RK = 0, T5_RV = 16384, T5_RG = 20480;
 // (1024-byte multiples, so every slot's k image stays 1024-aligned)
-constexpr uint32_t t5_slot_bytes(bool gv) { return gv ? 28672u : 21504u; }
+constexpr uint32_t t5_slot_bytes(int gm) { return gm == 1 ? 28672u : gm == 2 ? 53248u : 21504u; }
 // NB staging tiles of one chunk state, 128 x 32 fp32 (16 KB): [key row][32
 // columns] in 128-byte (fp32) or 64-byte (bf16) swizzled rows, or [column]
 // [128 keys] unswizzled for states stored as [V, K]
 constexpr uint32_t T5_TILE = 16384, T5_STAGE = T5_NB * T5_TILE;
 // v~ image: 64 token rows x 64 columns (hi 0..31, lo 32..63), group stride 1024
 constexpr uint32_t T5_VTB = 8192;
+// operand images the stagers write, two buffers: v~ (8 KB each) or, for gk,
+// the lo half of k~ = k e^(gk_L - gk) in the raw k image's layout (16 KB
+// each; the hi half replaces the raw k image in its ring slot, which only
+// the stagers read)
+constexpr uint32_t t5_img_bytes(int gm) { return gm == 2 ? 2u * 16384u : 2u * T5_VTB; }
 
 struct T5Seq {
   int bos, eos, b, nch;
@@ -163,21 +173,24 @@ __device__ __forceinline__ uint64_t t5_sdesc_sw128(const void *smem, uint32_t lb
   return ptx::sdesc(smem, lbo, sbo) | (2ull << 61);
 }
 
-template <bool GV, bool VF, bool SPLIT>
-__global__ void __launch_bounds__(T5_THREADS, 1)
+template <int GM, bool VF, bool SPLIT>
+__global__ void __launch_bounds__(t5_threads(GM), 1)
 state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_g,
                       const __grid_constant__ CUtensorMap tm_hs, StateParams p) {
   extern __shared__ __align__(1024) unsigned char sm5_raw[];
+  constexpr bool GV = GM == 1, GK = GM == 2;
+  constexpr int T5_STAGERS = t5_stagers(GM), T5_WPROD = 4 + T5_STAGERS, T5_WMMA = T5_WPROD + 1,
+                T5_WSTORE = T5_WPROD + 2;
   constexpr int K = T5_KD;
-  constexpr uint32_t SLOT = t5_slot_bytes(GV);
+  constexpr uint32_t SLOT = t5_slot_bytes(GM);
   // the swizzle patterns follow address bits 4-9: slots start on 1024 bytes
   unsigned char *sm5 = sm5_raw + ((1024u - (ptx::smem_u32(sm5_raw) & 1023u)) & 1023u);
   unsigned char *ring = sm5;
-  constexpr int T5_NS = t5_ns(GV);
-  unsigned char *vimg = sm5 + T5_NS * SLOT;  // two v~ images
-  unsigned char *stage = vimg + 2 * T5_VTB;   // NB state staging tiles
+  constexpr int T5_NS = t5_ns(GM);
+  unsigned char *vimg = sm5 + T5_NS * SLOT;       // two operand images (v~, or k~ pairs)
+  unsigned char *stage = vimg + t5_img_bytes(GM);  // NB state staging tiles
   uint64_t *bars = reinterpret_cast<uint64_t *>(stage + T5_STAGE);
   uint64_t *full = bars, *empty = bars + T5_NS;
   uint64_t *vready = bars + 2 * T5_NS, *vfree = vready + 2, *afull = vfree + 2, *afree = afull + 2;
@@ -227,7 +240,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       ptx::prefetch_tmap(&tm_v);
       if (GV) ptx::prefetch_tmap(&tm_g);
     }
-    const uint32_t bytes = 16384u + 4096u + (GV ? 8192u : 0u);
+    const uint32_t bytes = 16384u + 4096u + (GV ? 8192u : 0u) + (GK ? 32768u : 0u);
     const long long rows = (long long)p.B * p.T;
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
@@ -244,6 +257,8 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (lane == 0) t5_tma_load_4d(slot + T5_RK, &tm_k, 0, row0, 0, h, &full[s]);
       if (lane == 1) ptx::tma_load_3d(slot + T5_RV, &tm_v, v0, h, row0, &full[s]);
       if (GV && lane == 2) ptx::tma_load_3d(slot + T5_RG, &tm_g, v0, hg, row0, &full[s]);
+      if (GK && lane >= 2 && lane < 6)
+        ptx::tma_load_3d(slot + T5_RG + (lane - 2) * 8192, &tm_g, 32 * (lane - 2), hg, row0, &full[s]);
       if (p.gate == GDN_GATE_G) {
         // g of the chunk's 64 rows (rows past the tensor read as zero)
 #pragma unroll
@@ -256,7 +271,75 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
       ptx::cp_async_mbar_arrive(&full[s]);
     }
-  } else if (warp >= 4 && warp < 4 + T5_STAGERS) {
+  } else if (GK && warp >= 4 && warp < 4 + T5_STAGERS) {
+    // ---------------- gk stagers: thread (i, part) = token row i, keys 32 part ..
+    // k~ = k e^(gk_L - gk_i) (backward: q e^(gk_i)), zero past the chunk's
+    // end, as a bf16 hi/lo pair in the raw k image's layout (hi in place)
+    constexpr int CPT = 8 * 4 / T5_STAGERS;  // 16-byte chunks (8 keys) per thread
+    const int i = (tid - 128) & 63, part = (tid - 128) >> 6;
+    const int half = part * CPT / 8, c0 = part * CPT % 8;
+    auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
+#pragma unroll 1
+    for (int it = 0; it < sq.nch; ++it) {
+      const int s = it % T5_NS, b = it & 1;
+      const int L = len_of(it);
+      ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
+      if (it >= 2) ok = ptx::mbar_wait_bounded(&vfree[b], (uint32_t)(((it >> 1) - 1) & 1)) && ok;
+      unsigned char *slot = ring + s * SLOT;
+      // k~_hi over the raw k it is formed from (each thread reads and writes
+      // the same 16-byte chunks), k~_lo into its own image
+      unsigned char *khi = slot + T5_RK + half * 8192;
+      unsigned char *klo = vimg + b * 16384 + half * 8192;
+      const unsigned char *kin = khi;
+#pragma unroll 2
+      for (int c = c0; c < c0 + CPT; ++c) {
+        // keys 64 half + 8 c .. + 7: 16-byte chunk c of row i (chunk c ^ (i & 7));
+        // in the gk tile, box 2 half + c / 4, chunks 2 (c % 4), + 1 of row i
+        const int cs = (c ^ (i & 7)) << 4;
+        float kf[8];
+        {
+          const uint4 u = *reinterpret_cast<const uint4 *>(kin + i * 128 + cs);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            kf[2 * e] = __uint_as_float(w[e] << 16);
+            kf[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        }
+        const unsigned char *gb = slot + T5_RG + (2 * half + (c >> 2)) * 8192;
+        const int g0 = 2 * (c & 3);
+        float x[8];
+        if (i < L) {
+          const float4 a0 = *reinterpret_cast<const float4 *>(gb + i * 128 + ((g0 ^ (i & 7)) << 4));
+          const float4 a1 = *reinterpret_cast<const float4 *>(gb + i * 128 + (((g0 + 1) ^ (i & 7)) << 4));
+          float gi[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          if (!p.reverse) {
+            const int l = L - 1;
+            const float4 b0 = *reinterpret_cast<const float4 *>(gb + l * 128 + ((g0 ^ (l & 7)) << 4));
+            const float4 b1 = *reinterpret_cast<const float4 *>(gb + l * 128 + (((g0 + 1) ^ (l & 7)) << 4));
+            const float gl[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) gi[e] = gl[e] - gi[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = kf[e] * expf(gi[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        uint4 hi, lo;
+        t5_split8(x, hi, lo);
+        *reinterpret_cast<uint4 *>(khi + i * 128 + cs) = hi;
+        *reinterpret_cast<uint4 *>(klo + i * 128 + cs) = lo;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&vready[b]);
+        ptx::mbar_arrive(&empty[s]);  // this warp has read the slot's k and gate tile
+      }
+    }
+  } else if (!GK && warp >= 4 && warp < 4 + T5_STAGERS) {
     // ---------------- stagers: thread (i, half) = token row i, columns 16 half ..
     const int i = (tid - 128) & 63, half = (tid - 128) >> 6;
     auto len_of = [&](int it) { return min(BT, sq.eos - (sq.bos + chunk_at(it) * BT)); };
@@ -323,7 +406,8 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
   } else if (warp == T5_WMMA) {
     // ---------------- MMA issuer
-    const uint32_t id = ptx::idesc_bf16(128, 2 * T5_VT, 1, 1);  // A and B MN-major
+    // A and B MN-major; gk: N = 32 (v raw), otherwise N = 64 (v~ hi | lo)
+    const uint32_t id = ptx::idesc_bf16(128, GK ? T5_VT : 2 * T5_VT, 1, 1);
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
       const int s = it % T5_NS, b = it & 1;
@@ -335,12 +419,29 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (lane == 0) {
         // A: MN-major, 128-byte swizzle, 64-key atoms columns 8 KB apart, 8-token
         // groups 1 KB apart; a K step of 16 tokens is two groups (2 KB)
-        const uint64_t a = t5_sdesc_sw128(ring + s * SLOT + T5_RK, 8192, 1024);
-        const uint64_t bv = ptx::sdesc(vimg + b * T5_VTB, 128, 1024);
+        if (GK) {
+          // D = k~_hi^T v + k~_lo^T v; B = the raw v tile, MN-major with
+          // 64-byte swizzle (one 32-column atom, 8-token groups 512 bytes
+          // apart; a K step is 1 KB)
+          const uint64_t ah = t5_sdesc_sw128(ring + s * SLOT + T5_RK, 8192, 1024);
+          const uint64_t al = t5_sdesc_sw128(vimg + b * 16384, 8192, 1024);
+          const uint64_t bv = ptx::sdesc(ring + s * SLOT + T5_RV, 512, 512) | (4ull << 61);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(tmem + 64 * b, a + (uint64_t)(ks * 2048 >> 4),
-                        bv + (uint64_t)(ks * 256 >> 4), id, ks > 0);
+          for (int ks = 0; ks < 4; ++ks)
+            ptx::mma_bf16(tmem + 64 * b, ah + (uint64_t)(ks * 2048 >> 4),
+                          bv + (uint64_t)(ks * 1024 >> 4), id, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            ptx::mma_bf16(tmem + 64 * b, al + (uint64_t)(ks * 2048 >> 4),
+                          bv + (uint64_t)(ks * 1024 >> 4), id, 1);
+        } else {
+          const uint64_t a = t5_sdesc_sw128(ring + s * SLOT + T5_RK, 8192, 1024);
+          const uint64_t bv = ptx::sdesc(vimg + b * T5_VTB, 128, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            ptx::mma_bf16(tmem + 64 * b, a + (uint64_t)(ks * 2048 >> 4),
+                          bv + (uint64_t)(ks * 256 >> 4), id, ks > 0);
+        }
         ptx::mma_commit(&afull[b]);
         ptx::mma_commit(&vfree[b]);
         ptx::mma_commit(&empty[s]);
@@ -398,11 +499,13 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
     int nst = 0;  // chunk states written to the staging ring
     T5Stores stores(p, sq.first, sq.nch);
     // gate g at the chunk's last row (chunk-local cumulative sum)
+    // (gk: this thread's key row r of the per-key gate there)
     auto g_end = [&](int it) {
       const long long row = (long long)sq.b * p.T + sq.bos + chunk_at(it) * BT + len_of(it) - 1;
-      return p.gate_values[row * HG + hg];
+      return GK ? p.gate_values[(row * HG + hg) * K + r] : p.gate_values[row * HG + hg];
     };
-    float g_next = p.gate == GDN_GATE_G && sq.nch > 0 ? g_end(0) : 0.f;
+    const bool row_gate = p.gate == GDN_GATE_G || GK;
+    float g_next = row_gate && sq.nch > 0 ? g_end(0) : 0.f;
 #pragma unroll 1
     for (int it = 0; it < sq.nch; ++it) {
       const int b = it & 1, s = it % T5_NS;
@@ -443,7 +546,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       // the chunk's decay: for gv from its ring slot, for g from the gate
       // value loaded one chunk ahead
       const float g_cur = g_next;
-      if (p.gate == GDN_GATE_G && it + 1 < sq.nch) g_next = g_end(it + 1);
+      if (row_gate && it + 1 < sq.nch) g_next = g_end(it + 1);
       float dv[T5_VT];
       if (GV) {
         ok = ptx::mbar_wait_bounded(&full[s], (uint32_t)((it / T5_NS) & 1)) && ok;
@@ -456,7 +559,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (lane == 0) ptx::mbar_arrive(&empty[s]);  // this warp is done with the slot
       } else {
         float ds = 1.f;
-        if (p.gate == GDN_GATE_G) ds = expf(g_cur);
+        if (p.gate == GDN_GATE_G || GK) ds = expf(g_cur);
         if (p.gate == GDN_GATE_G_GAMMA) ds = expf(gamma * (float)len_of(it));
 #pragma unroll
         for (int j = 0; j < T5_VT; ++j) dv[j] = ds;
@@ -465,9 +568,17 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       ptx::tc_fence_after();
       float dh[T5_VT], dl[T5_VT];
       ptx::tmem_ld32(tmem + 64 * b + lane_base, dh);
-      ptx::tmem_ld32(tmem + 64 * b + 32 + lane_base, dl);
+      if (GK) {
+        // one product (v raw); backward: times the scale, which v~ carries
+        // for the other gates
+        const float sc = p.reverse ? p.scale : 1.f;
 #pragma unroll
-      for (int j = 0; j < T5_VT; ++j) hs[j] = fmaf(dv[j], hs[j], dh[j] + dl[j]);
+        for (int j = 0; j < T5_VT; ++j) hs[j] = fmaf(dv[j], hs[j], sc * dh[j]);
+      } else {
+        ptx::tmem_ld32(tmem + 64 * b + 32 + lane_base, dl);
+#pragma unroll
+        for (int j = 0; j < T5_VT; ++j) hs[j] = fmaf(dv[j], hs[j], dh[j] + dl[j]);
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&afree[b]);
@@ -551,25 +662,26 @@ bool t5_map_k(CUtensorMap *m, const void *base, int heads, long long rows) {
 
 bool state_pass_tc5_supported(const StateParams &p, bool bf16) {
   const uintptr_t al = (uintptr_t)p.k | (uintptr_t)p.v | (uintptr_t)p.hs |
-                       (p.gate == GDN_GATE_GV ? (uintptr_t)p.gate_values : 0);
+                       (p.gate == GDN_GATE_GV || p.gate == GDN_GATE_GK ? (uintptr_t)p.gate_values : 0);
   // (row coordinates of the stored states are 32-bit)
   return bf16 && p.K == T5_KD && p.V % T5_VT == 0 && p.T > 0 && al % 16 == 0 &&
          (!p.hs || p.num_chunks * p.H * (long long)(p.K > p.V ? p.K : p.V) < (1ll << 31)) &&
          (p.gate == GDN_GATE_NONE || p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA ||
-          p.gate == GDN_GATE_GV);
+          p.gate == GDN_GATE_GV || p.gate == GDN_GATE_GK);
 }
 
 cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
-  const bool gv = p.gate == GDN_GATE_GV;
+  const int gm = p.gate == GDN_GATE_GV ? 1 : p.gate == GDN_GATE_GK ? 2 : 0;
   CUtensorMap mk, mv, mg;
   const long long rows = (long long)p.B * p.T;
   if (!t5_map_k(&mk, p.k, p.H, rows) ||
       !t5_map3(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.V, p.H, rows, T5_VT,
                CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  if (gv) {
-    if (!t5_map3(&mg, p.gate_values, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.V, p.HG, rows, T5_VT,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  if (gm != 0) {
+    // gv: [rows][HG][V], boxes of 32 values; gk: [rows][HG][K], boxes of 32 keys
+    if (!t5_map3(&mg, p.gate_values, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, gm == 1 ? p.V : T5_KD,
+                 p.HG, rows, 32, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
     mg = mv;  // unused
@@ -588,25 +700,21 @@ cudaError_t launch_state_pass_tc5(const StateParams &p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   // + state staging, barriers, TMEM slot, and up to 1 KB to align the ring
-  const size_t smem = t5_ns(gv) * t5_slot_bytes(gv) + 2 * T5_VTB + T5_STAGE + 256 + 1024;
+  const size_t smem = t5_ns(gm) * t5_slot_bytes(gm) + t5_img_bytes(gm) + T5_STAGE + 256 + 1024;
   const bool split = p.split > 1, vf = p.v_first != 0;
-  auto pick = [&](auto k000, auto k001, auto k010, auto k011, auto k100, auto k101, auto k110,
-                  auto k111) {
-    return gv ? (vf ? (split ? k111 : k110) : (split ? k101 : k100))
-              : (vf ? (split ? k011 : k010) : (split ? k001 : k000));
-  };
-  auto kern = pick(state_pass_tc5_kernel<false, false, false>,
-                   state_pass_tc5_kernel<false, false, true>,
-                   state_pass_tc5_kernel<false, true, false>,
-                   state_pass_tc5_kernel<false, true, true>,
-                   state_pass_tc5_kernel<true, false, false>,
-                   state_pass_tc5_kernel<true, false, true>,
-                   state_pass_tc5_kernel<true, true, false>,
-                   state_pass_tc5_kernel<true, true, true>);
+  using KernT = decltype(&state_pass_tc5_kernel<0, false, false>);
+  const KernT kernels[3][2][2] = {
+      {{state_pass_tc5_kernel<0, false, false>, state_pass_tc5_kernel<0, false, true>},
+       {state_pass_tc5_kernel<0, true, false>, state_pass_tc5_kernel<0, true, true>}},
+      {{state_pass_tc5_kernel<1, false, false>, state_pass_tc5_kernel<1, false, true>},
+       {state_pass_tc5_kernel<1, true, false>, state_pass_tc5_kernel<1, true, true>}},
+      {{state_pass_tc5_kernel<2, false, false>, state_pass_tc5_kernel<2, false, true>},
+       {state_pass_tc5_kernel<2, true, false>, state_pass_tc5_kernel<2, true, true>}}};
+  const KernT kern = kernels[gm][vf][split];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.V / T5_VT), (unsigned)p.H, (unsigned)p.N);
-  kern<<<grid, T5_THREADS, smem, stream>>>(mk, mv, mg, mh, p);
+  kern<<<grid, t5_threads(gm), smem, stream>>>(mk, mv, mg, mh, p);
   return cudaGetLastError();
 }
 
