@@ -291,8 +291,9 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
       unsigned char *khi = slot + T5_RK + half * 8192;
       unsigned char *klo = vimg + b * 16384 + half * 8192;
       const unsigned char *kin = khi;
-#pragma unroll 2
-      for (int c = c0; c < c0 + CPT; ++c) {
+#pragma unroll
+      for (int cc = 0; cc < CPT; ++cc) {
+        const int c = c0 + cc;
         // keys 64 half + 8 c .. + 7: 16-byte chunk c of row i (chunk c ^ (i & 7));
         // in the gk tile, box 2 half + c / 4, chunks 2 (c % 4), + 1 of row i
         const int cs = (c ^ (i & 7)) << 4;
@@ -322,7 +323,7 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
             for (int e = 0; e < 8; ++e) gi[e] = gl[e] - gi[e];
           }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = kf[e] * expf(gi[e]);
+          for (int e = 0; e < 8; ++e) x[e] = kf[e] * __expf(gi[e]);
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
