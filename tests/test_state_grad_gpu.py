@@ -120,6 +120,32 @@ def test_packed_sequences_with_empty_ones(K, dtype):
     assert torch.equal(dh0[1].cpu(), inp["dht"][1])  # the empty sequence passes dht through
 
 
+@pytest.mark.parametrize("gate", ["gk", "g"])
+def test_tensor_core_path_packed_sequences(gate):
+    """bf16 with K = 128 (the tcgen05 kernel, run backwards), packed sequences
+    with empty ones and grouped query heads."""
+    lengths = [70, 0, 130, 1, 64]
+    inp = synth.state_grad_inputs(86, 1, sum(lengths), 4, 2, 128, 64, gate, lengths=lengths,
+                                  dht_std=0.3)
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate})")
+    assert torch.equal(dh0[1].cpu(), inp["dht"][1])
+
+
+@pytest.mark.parametrize("factor", [40.0, -0.5])
+def test_tensor_core_path_strong_and_positive_gk(factor):
+    """The chunk-local cumulative per-key gates scaled by 40 (factors far below
+    fp32's range inside a chunk) and by -0.5 (factors above one)."""
+    inp = synth.state_grad_inputs(87, 2, 150, 2, 2, 128, 64, "gk", dht_std=0.3)
+    inp["gate_values"] = inp["gate_values"] * factor
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert_close(dh, dh_ref, TOL_F32, f"dh (gk, x{factor})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 (gk, x{factor})")
+
+
 def test_empty_batch_returns_dht():
     inp = synth.state_grad_inputs(85, 2, 0, 2, 2, 32, 32, "g", dtype=torch.float32, dht_std=1.0)
     dh, dh0 = run(inp)

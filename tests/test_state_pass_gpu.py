@@ -106,6 +106,36 @@ def test_packed_sequences_with_empty_ones():
     assert torch.equal(ht[1].cpu(), inp["h0"][1])  # the empty sequence keeps its state
 
 
+@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+def test_tensor_core_path_packed_sequences(gate):
+    """bf16 with K = 128 (the tcgen05 kernel), packed sequences with empty
+    ones: the TMA tiles of a sequence's last chunk hold the next sequence's
+    rows, which must take no part."""
+    lengths = [70, 0, 130, 1, 64]
+    inp = synth.state_pass_inputs(80, 1, sum(lengths), 2, 128, 64, gate, lengths=lengths,
+                                  h0_std=0.3)
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert hs.shape[0] == 2 + 0 + 3 + 1 + 1
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate})")
+    assert torch.equal(ht[1].cpu(), inp["h0"][1])
+
+
+@pytest.mark.parametrize("factor", [40.0, -0.5])
+@pytest.mark.parametrize("gate", ["gk", "gv", "g"])
+def test_tensor_core_path_strong_and_positive_gates(gate, factor):
+    """The chunk-local cumulative gates scaled: by 40 (about -2 per token, so
+    the in-chunk factors span e^0 .. far below fp32's range) and by -0.5
+    (growing states, factors above one)."""
+    inp = synth.state_pass_inputs(81, 2, 150, 2, 128, 64, gate, h0_std=0.3)
+    inp["gate_values"] = inp["gate_values"] * factor
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate}, x{factor})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate}, x{factor})")
+
+
 def test_empty_batch_returns_the_initial_state():
     inp = synth.state_pass_inputs(74, 2, 0, 2, 32, 32, "g", dtype=torch.float32, h0_std=1.0)
     hs, ht = run(inp)
