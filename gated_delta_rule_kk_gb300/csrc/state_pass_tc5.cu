@@ -116,15 +116,36 @@ __device__ T5Seq t5_sequence(const StateParams &p, int n, int tid, long long *sh
   return s;
 }
 
+// Packed fp32 pairs (sm_100: two lanes per instruction, each rounded to
+// nearest).
+__device__ __forceinline__ float2 t5_sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 t5_mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 __device__ __forceinline__ void t5_split8(const float *f, uint4 &hi, uint4 &lo) {
   __nv_bfloat162 h2[4];
   float r[8];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     h2[e] = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-    const float2 b = __bfloat1622float2(h2[e]);
-    r[2 * e] = f[2 * e] - b.x;
-    r[2 * e + 1] = f[2 * e + 1] - b.y;
+    const float2 d = t5_sub2(make_float2(f[2 * e], f[2 * e + 1]), __bfloat1622float2(h2[e]));
+    r[2 * e] = d.x;
+    r[2 * e + 1] = d.y;
   }
   hi = *reinterpret_cast<const uint4 *>(h2);
   __nv_bfloat162 l2[4];
@@ -313,17 +334,24 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (i < L) {
           const float4 a0 = *reinterpret_cast<const float4 *>(gb + i * 128 + ((g0 ^ (i & 7)) << 4));
           const float4 a1 = *reinterpret_cast<const float4 *>(gb + i * 128 + (((g0 + 1) ^ (i & 7)) << 4));
-          float gi[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          float2 gi[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                          make_float2(a1.z, a1.w)};
           if (!p.reverse) {
             const int l = L - 1;
             const float4 b0 = *reinterpret_cast<const float4 *>(gb + l * 128 + ((g0 ^ (l & 7)) << 4));
             const float4 b1 = *reinterpret_cast<const float4 *>(gb + l * 128 + (((g0 + 1) ^ (l & 7)) << 4));
-            const float gl[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) gi[e] = gl[e] - gi[e];
+            gi[0] = t5_sub2(make_float2(b0.x, b0.y), gi[0]);
+            gi[1] = t5_sub2(make_float2(b0.z, b0.w), gi[1]);
+            gi[2] = t5_sub2(make_float2(b1.x, b1.y), gi[2]);
+            gi[3] = t5_sub2(make_float2(b1.z, b1.w), gi[3]);
           }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = kf[e] * __expf(gi[e]);
+          for (int e = 0; e < 4; ++e) {
+            const float2 y = t5_mul2(make_float2(kf[2 * e], kf[2 * e + 1]),
+                                     make_float2(__expf(gi[e].x), __expf(gi[e].y)));
+            x[2 * e] = y.x;
+            x[2 * e + 1] = y.y;
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
