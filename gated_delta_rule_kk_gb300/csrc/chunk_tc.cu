@@ -524,12 +524,28 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     // gate tile in place (rows >= L repeat row L - 1)
     float *G = Asm;
     float mn = 0.f, mx = 0.f;
-    if (tid < KD) {
+    if (p.g_is_cumsum) {
+      // already the cumulative gate: thread (c, half) checks the range of 32
+      // rows of channel c and repeats row L - 1 over the padding rows
+      const int c = tid & (KD - 1), r0 = (tid >> 7) * 32;
+      const float last = G[(L - 1) * KD + c];
+#pragma unroll 8
+      for (int i = r0; i < r0 + 32; ++i) {
+        float x = last;
+        if (i < L) x = G[i * KD + c]; else G[i * KD + c] = last;
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      if (tid < KD) {
+        gl[c] = last;
+        sc[c] = __expf(last);
+      }
+    } else if (tid < KD) {
       const int c = tid;
       float acc = 0.f;
 #pragma unroll 8
       for (int i = 0; i < 64; ++i) {
-        if (i < L) acc = p.g_is_cumsum ? G[i * KD + c] : acc + G[i * KD + c];
+        if (i < L) acc += G[i * KD + c];
         G[i * KD + c] = acc;
         mn = fminf(mn, acc);
         mx = fmaxf(mx, acc);
