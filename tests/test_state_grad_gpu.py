@@ -146,6 +146,18 @@ def test_tensor_core_path_strong_and_positive_gk(factor):
     assert_close(dh0, dh0_ref, TOL_F32, f"dh0 (gk, x{factor})")
 
 
+@pytest.mark.parametrize("V", [32, 96])
+@pytest.mark.parametrize("gate", ["g", "gk", "gv"])
+def test_tensor_core_path_one_and_three_value_tiles(gate, V):
+    """The tcgen05 kernel run backwards at V = 32 and 96 (one and three value
+    tiles), grouped query heads."""
+    inp = synth.state_grad_inputs(88, 2, 150, 4, 2, 128, V, gate, dht_std=0.3)
+    dh, dh0 = run(inp)
+    dh_ref, dh0_ref = oracle(inp)
+    assert_close(dh, dh_ref, TOL_F32, f"dh ({gate}, V={V})")
+    assert_close(dh0, dh0_ref, TOL_F32, f"dh0 ({gate}, V={V})")
+
+
 def test_empty_batch_returns_dht():
     inp = synth.state_grad_inputs(85, 2, 0, 2, 2, 32, 32, "g", dtype=torch.float32, dht_std=1.0)
     dh, dh0 = run(inp)

@@ -136,6 +136,18 @@ def test_tensor_core_path_strong_and_positive_gates(gate, factor):
     assert_close(ht, ht_ref, TOL_F32, f"ht ({gate}, x{factor})")
 
 
+@pytest.mark.parametrize("V", [32, 96])
+@pytest.mark.parametrize("gate", ["g", "g_gamma", "gk", "gv", None])
+def test_tensor_core_path_one_and_three_value_tiles(gate, V):
+    """bf16 with K = 128 (the tcgen05 kernel) at V = 32 and 96: one and three
+    32-column value tiles per head; T = 150 leaves a 22-token tail."""
+    inp = synth.state_pass_inputs(82, 2, 150, 2, 128, V, gate, h0_std=0.3)
+    hs, ht = run(inp)
+    hs_ref, ht_ref = oracle(inp)
+    assert_close(hs, hs_ref, TOL_F32, f"hs ({gate}, V={V})")
+    assert_close(ht, ht_ref, TOL_F32, f"ht ({gate}, V={V})")
+
+
 def test_empty_batch_returns_the_initial_state():
     inp = synth.state_pass_inputs(74, 2, 0, 2, 32, 32, "g", dtype=torch.float32, h0_std=1.0)
     hs, ht = run(inp)
