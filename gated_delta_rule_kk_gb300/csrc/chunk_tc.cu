@@ -119,13 +119,38 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
   return u;
 }
 
+// Packed fp32 pairs (sm_100: two lanes per instruction, each rounded to
+// nearest, so the results equal the scalar operations').
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 16 significant bits.
 __device__ __forceinline__ void split8(const float *f, uint4 &hi, uint4 &lo) {
   float r[8];
   hi = pack8(f);
   unpack8(hi, r);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) r[e] = f[e] - r[e];
+  for (int e = 0; e < 4; ++e) {
+    const float2 d = sub2(make_float2(f[2 * e], f[2 * e + 1]), make_float2(r[2 * e], r[2 * e + 1]));
+    r[2 * e] = d.x;
+    r[2 * e + 1] = d.y;
+  }
   lo = pack8(r);
 }
 
@@ -583,17 +608,24 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       const float4 ga = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg);
       const float4 gb = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg + 4);
       const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+      // (fp32 pairs: two products per instruction)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float gv = gr[e];
-        const float ep = __expf(gv);
-        a[e] = kf[e] * ep;
-        b[e] = qf[e] * ep;
+      for (int e = 0; e < 8; e += 2) {
+        const float2 ep = make_float2(__expf(gr[e]), __expf(gr[e + 1]));
+        const float2 kk = make_float2(kf[e], kf[e + 1]), qq = make_float2(qf[e], qf[e + 1]);
+        const float2 ka = mul2(kk, ep), qb = mul2(qq, ep);
+        a[e] = ka.x; a[e + 1] = ka.y;
+        b[e] = qb.x; b[e + 1] = qb.y;
         // split range (|gamma| bounded): e^{gamma_L - g} = e^{gamma_L} e^{-g}
-        const float en = split ? __expf(-gv) : 0.f;
-        c[e] = kf[e] * en;
-        const float fl = split ? sc[8 * cg + e] * en : __expf(gl[8 * cg + e] - gv);
-        t[e] = i < L ? kf[e] * fl : 0.f;
+        const float2 en = split ? make_float2(__expf(-gr[e]), __expf(-gr[e + 1])) : make_float2(0.f, 0.f);
+        const float2 kc = mul2(kk, en);
+        c[e] = kc.x; c[e + 1] = kc.y;
+        const float2 fl = split ? mul2(make_float2(sc[8 * cg + e], sc[8 * cg + e + 1]), en)
+                                : make_float2(__expf(gl[8 * cg + e] - gr[e]),
+                                              __expf(gl[8 * cg + e + 1] - gr[e + 1]));
+        const float2 kt = mul2(kk, fl);
+        t[e] = i < L ? kt.x : 0.f;
+        t[e + 1] = i < L ? kt.y : 0.f;
       }
       uint4 hi, lo;
       split8(a, hi, klo[it]);

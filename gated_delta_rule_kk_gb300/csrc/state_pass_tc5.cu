@@ -1,37 +1,44 @@
 // Chunk state pass on the 5th-generation tensor cores (tcgen05 + TMA), bf16
-// inputs with K = 128, V a multiple of 32, gates none / g / g_gamma / gv (the
-// gates whose chunk factors ride on the value side).  The recurrence is that
-// of state_pass.cu (KDA _fla/ops/common/chunk_h.py, chunk_fwd_kernel_h and
+// inputs with K = 128, V a multiple of 32, every gate kind.  The recurrence is
+// that of state_pass.cu (KDA _fla/ops/common/chunk_h.py, chunk_fwd_kernel_h and
 // chunk_bwd_kernel_dh):
-//   h_{c+1} = decay_c o h_c + Delta_c,   Delta_c = k_c^T v~_c,
-// where decay_c is e^{g_L} (per column e^{gv_L}) and v~ carries every token
-// factor (forward e^{g_L - g_i} e^{gv_L - gv_i}, backward scale e^{g_i} e^{gv_i}).
-// Delta_c does not depend on h, so the tensor core computes it for chunks
-// ahead of the state: only the element-wise update is sequential.
+//   h_{c+1} = decay_c o h_c + Delta_c,   Delta_c = k~_c^T v~_c,
+// where decay_c is e^{g_L} (per column e^{gv_L}, per key row e^{gk_L}).  For
+// the value-side gates (none, g, g_gamma, gv) v~ carries every token factor
+// (forward e^{g_L - g_i} e^{gv_L - gv_i}, backward scale e^{g_i} e^{gv_i}) and
+// k~ = k; for the per-key gate gk, k~ = k e^{gk_L - gk_i} (backward q e^{gk_i})
+// and v~ = v (backward the scale on the product).  Delta_c does not depend on
+// h, so the tensor core computes it for chunks ahead of the state: only the
+// element-wise update is sequential.
 //
-// One CTA per (32-column V tile, head, sequence), 320 threads:
-//   warp 8      producer: one TMA each (from lanes 0, 1, 2) for the chunk's k
-//               tile, its v tile and, for gv, its gate tile, into a ring of
-//               NS slots, all with
-//               swizzled rows of 64 or 128 bytes (a TMA moves a box row by
-//               row, so narrow rows cost requests): k lands as two 128-byte
-//               swizzled MN-major atoms columns (keys 0-63 and 64-127) that
-//               the MMA reads directly; the per-token gate g by cp.async from
-//               every lane (counted on the slot's barrier), so no consumer
+// One CTA per (32-column V tile, head, sequence); warps 0-3 state, then the
+// stagers (4, or 8 for gk), the producer, the MMA issuer and the store warp:
+//   producer    one TMA each (from lanes 0, 1, 2..) for the chunk's k tile, its
+//               v tile and, for gv / gk, its gate tile, into a ring of NS
+//               slots, all with swizzled rows of 64 or 128 bytes (a TMA moves
+//               a box row by row, so narrow rows cost requests): k lands as two
+//               128-byte swizzled MN-major atoms columns (keys 0-63 and 64-127)
+//               that the MMA reads directly; the per-token gate g by cp.async
+//               from every lane (counted on the slot's barrier), so no consumer
 //               ever waits on a global load
-//   warps 4-7   stagers: thread (i, half) forms row i, 16 columns, of
+//   stagers     value-side gates: thread (i, half) forms row i, 16 columns, of
 //               v~ = v x factor as a bf16 hi/lo pair (zero past the chunk's
-//               end) into one of two operand images
-//   warp 9      MMA: Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64,
-//               K = 64 tokens) into one of two TMEM accumulators
-//   warp 10     store: one TMA store per stored chunk state, from a ring of
-//               NB staging tiles the state warps fill (so the stores leave in
+//               end) into one of two operand images; gk: thread (i, part)
+//               forms k~ for row i, 32 keys, as a bf16 hi/lo pair in the raw k
+//               image's layout (hi over the raw k in its slot, lo into one of
+//               two images)
+//   MMA         Delta_c = k^T [v~_hi | v~_lo] (M = 128 keys, N = 64, K = 64
+//               tokens; gk: k~_hi^T v + k~_lo^T v at N = 32, v raw from its
+//               64-byte-swizzled tile) into one of two TMEM accumulators
+//   store       one TMA store per stored chunk state, from a ring of NB
+//               staging tiles the state warps fill (so the stores leave in
 //               whole rows and their issue and completion stay off the
 //               state's sequential path)
-//   warps 0-3   state: thread r holds key row r, 32 columns, of the fp32
-//               state; per chunk it writes the chunk-start state (when that
-//               chunk is stored) and applies h = decay o h + Delta_hi + Delta_lo,
-//               the decay read from the chunk's ring slot
+//   state       thread r holds key row r, 32 columns, of the fp32 state; per
+//               chunk it writes the chunk-start state (when that chunk is
+//               stored) and applies h = decay o h + Delta, the scalar or
+//               per-key decay from a load issued one chunk ahead, gv's from
+//               the chunk's ring slot
 // Every wait is bounded (GDN_ERR_TIMEOUT, then every role still runs every
 // chunk so no barrier is left short of arrivals).
 #include <cuda.h>
