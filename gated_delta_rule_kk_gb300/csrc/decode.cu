@@ -577,13 +577,16 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
 
 }  // namespace
 
-// T <= 2 is HBM-bound on this kernel; at T = 3, 4 the packed-FMA work per
-// item outgrows the state stream and the tensor-core kernel is faster.
+// T <= 2 is HBM-bound on this kernel and T = 3 still faster here than on the
+// tensor-core kernel (112.7 against 116.9 us at B = 256, HV = 32); at T = 4
+// the packed-FMA work per item outgrows the state stream and the tensor-core
+// kernel is faster (134.6 against 159.5 us).
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
-  if (p.T >= 3) return launch_decode_tc(p, stream);
+  if (p.T >= 4) return launch_decode_tc(p, stream);
   switch (p.T) {
     case 1: return launch_t<1>(p, stream);
     case 2: return launch_t<2>(p, stream);
+    case 3: return launch_t<3>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,8 +1,8 @@
-// Decode step for T = 3, 4 tokens on the warp-level tensor cores (mma.sync
+// Decode step for T = 4 tokens on the warp-level tensor cores (mma.sync
 // m16n8k16, bf16 in, fp32 accumulate): same arithmetic and item schedule as
 // decode.cu, with the state tile held as MMA accumulator fragments.  (The
-// kernel is written for any T <= 4; at T = 1, 2 decode.cu is HBM-bound and
-// faster, so it serves those.)
+// kernel is written for any T <= 4; at T <= 3 decode.cu is faster, so it
+// serves those.)
 //
 // FlashInfer gdn_decode_bf16_state.py (compute_single_gate,
 // normalize_and_store_qk_to_smem, the per-token helpers and gated_delta_rule)
