@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
       }
       if (!ptx::mbar_wait_bounded(&prep[s], parity)) record_error(p.err, GDN_ERR_TIMEOUT);
 
-      // y_t = S0 k^_t and z_t = S0 q^_t of row rg + 32 rsel, two tokens at a time
+      // y_t = S0 k^_t and z_t = S0 q^_t of row rg + 32 rsel
       float y[T], z[T];
       auto dots = [&](auto n0_c, auto nt_c, float *out) {
         constexpr int N0 = decltype(n0_c)::value, NT = decltype(nt_c)::value;
@@ -403,19 +403,9 @@ __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
         for (int t = 0; t < NT; ++t) out[t] = r[t];
       };
       using C0 = std::integral_constant<int, 0>;
-      using C2 = std::integral_constant<int, 2>;
       using CT = std::integral_constant<int, T>;
-      using CT2 = std::integral_constant<int, T + 2>;
-      if constexpr (T <= 2) {
-        dots(C0{}, CT{}, y);
-        dots(CT{}, CT{}, z);
-      } else {
-        using CR = std::integral_constant<int, T - 2>;
-        dots(C0{}, C2{}, y);
-        dots(C2{}, CR{}, y + 2);
-        dots(CT{}, C2{}, z);
-        dots(CT2{}, CR{}, z + 2);
-      }
+      dots(C0{}, CT{}, y);
+      dots(CT{}, CT{}, z);
 
       // deltas and outputs of row rg + 32 rsel (the same on lanes cs and cs ^ 4)
       float dl[T];
@@ -577,16 +567,14 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream) {
 
 }  // namespace
 
-// T <= 2 is HBM-bound on this kernel and T = 3 still faster here than on the
-// tensor-core kernel (112.7 against 116.9 us at B = 256, HV = 32); at T = 4
-// the packed-FMA work per item outgrows the state stream and the tensor-core
-// kernel is faster (134.6 against 159.5 us).
+// T <= 2 is HBM-bound on this kernel; from T = 3 the packed-FMA work per item
+// outgrows the state stream and the tensor-core kernel is faster (at B = 256,
+// HV = 32: T = 3 107 against 112.6 us, T = 4 117 against 137 us).
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
-  if (p.T >= 4) return launch_decode_tc(p, stream);
+  if (p.T >= 3) return launch_decode_tc(p, stream);
   switch (p.T) {
     case 1: return launch_t<1>(p, stream);
     case 2: return launch_t<2>(p, stream);
-    case 3: return launch_t<3>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,8 +1,7 @@
-// Decode step for T = 4 tokens on the warp-level tensor cores (mma.sync
+// Decode step for T = 3, 4 tokens on the warp-level tensor cores (mma.sync
 // m16n8k16, bf16 in, fp32 accumulate): same arithmetic and item schedule as
-// decode.cu, with the state tile held as MMA accumulator fragments.  (The
-// kernel is written for any T <= 4; at T <= 3 decode.cu is faster, so it
-// serves those.)
+// decode.cu.  (The kernel is written for any T <= 4; at T <= 2 decode.cu is
+// HBM-bound and faster, so it serves those.)
 //
 // FlashInfer gdn_decode_bf16_state.py (compute_single_gate,
 // normalize_and_store_qk_to_smem, the per-token helpers and gated_delta_rule)
@@ -15,14 +14,16 @@
 //
 // Warp w owns rows 16 w .. 16 w + 15 of the [V, K] state of the item.  The
 // state slot arrives by TMA in the 128-byte-swizzled layout; ldmatrix gives
-// each warp its rows as bf16 A fragments, which are exactly the fp32
-// accumulator fragments of the update once converted (lossless: the state is
-// bf16).  The 2T dot products are one M16 x N(8 or 16) x K128 product with
-// B = [k^_0 hi, k^_0 lo, k^_1 hi, ...] (bf16 pairs, so the vectors keep
-// fp32-grade accuracy); the update is one K = 16 product per 8 columns with
-// A = [c delta hi | c delta lo | c delta hi] and B = [k^ hi; k^ hi; k^ lo].
-// The updated rows go back through stmatrix into the slot and one TMA store
-// per warp.  Per item the first warp to finish item i - 2 prepares it
+// each warp its rows as bf16 A fragments.  The 2T dot products are one
+// M16 x N(8 or 16) x K128 product with B = [k^_0 hi, k^_0 lo, k^_1 hi, ...]
+// (bf16 pairs, so the vectors keep fp32-grade accuracy).  The A fragments
+// stay in registers as bf16 for the update, which streams over 16-column
+// blocks: a block's fragments, converted and scaled by G_{T-1}, are exactly
+// the fp32 accumulator fragments (lossless: the state is bf16) of one K = 16
+// product per 8 columns with A = [c delta hi | c delta lo | c delta hi] and
+// B = [k^ hi; k^ hi; k^ lo]; the block goes back into the slot by stmatrix.
+// No fp32 copy of the whole tile is held in registers.  One TMA store per warp
+// writes its rows back.  Per item the first warp to finish item i - 2 prepares it
 // (normalised q/k as the bf16 operand images, gates, coefficients); the last
 // warp out of a ring entry refills it; no block-wide barrier in the item loop.
 #include <cuda.h>
@@ -342,22 +343,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
 
     if (!ptx::mbar_wait_bounded(&prep[a], ap)) record_error(p.err, GDN_ERR_TIMEOUT);
     const int slot = *reinterpret_cast<const int *>(hdr);
-    float C[16][4];
+    uint32_t S0f[8][4];  // this warp's rows of S0 as bf16 A fragments, block j = columns 16 j ..
     if (slot >= 0) {
       if (!ptx::mbar_wait_bounded(&sw_full[s], sp)) record_error(p.err, GDN_ERR_TIMEOUT);
-      // ---- S0 rows as A fragments; the same values seed the fp32 accumulators
+      // ---- dot products: S0 rows as A fragments
       float D[NT_DOT][4];
 #pragma unroll
       for (int n = 0; n < NT_DOT; ++n) D[n][0] = D[n][1] = D[n][2] = D[n][3] = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        uint32_t af[4];
+        uint32_t *af = S0f[j];
         ptx::ldmatrix_x4(sw_addr(sw, r0, j, lane), af[0], af[1], af[2], af[3]);
-        const float2 c00 = unpack2(af[0]), c01 = unpack2(af[1]), c10 = unpack2(af[2]),
-                     c11 = unpack2(af[3]);
-        C[2 * j][0] = c00.x; C[2 * j][1] = c00.y; C[2 * j][2] = c01.x; C[2 * j][3] = c01.y;
-        C[2 * j + 1][0] = c10.x; C[2 * j + 1][1] = c10.y;
-        C[2 * j + 1][2] = c11.x; C[2 * j + 1][3] = c11.y;
         // dot products: B rows n (vectors' hi/lo), k = 16 j .. 16 j + 15
         uint32_t b[4];
         const int n = (lane & 7) + ((lane >> 4) << 3);
@@ -391,6 +387,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
       // ---- deltas and outputs of rows r0 + g and r0 + g + 8
       const __nv_bfloat16 *vraw =
           reinterpret_cast<const __nv_bfloat16 *>(aux + A_RAW + 2 * T * ROW_BYTES);
+      // the coefficients, read as float4 groups (one broadcast load each)
+      const float4 *h4 = reinterpret_cast<const float4 *>(hdr);
+      auto el = [](const float4 &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; };
+      const float4 be4 = h4[H_BE / 4], bg4 = h4[H_BG / 4], gam4 = h4[H_GAM / 4], c4 = h4[H_C / 4];
+      float4 a4[T], b4[T];
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        a4[t] = h4[H_A / 4 + t];
+        b4[t] = h4[H_B / 4 + t];
+      }
       float dl[2][T];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -398,9 +404,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const float vv = __bfloat162float(vraw[t * DV + row]);
-          float d = fmaf(hdr[H_BE + t], vv, -hdr[H_BG + t] * y[h][t]);
+          float d = fmaf(el(be4, t), vv, -el(bg4, t) * y[h][t]);
 #pragma unroll
-          for (int s2 = 0; s2 < t; ++s2) d = fmaf(-hdr[H_A + 4 * t + s2], dl[h][s2], d);
+          for (int s2 = 0; s2 < t; ++s2) d = fmaf(-el(a4[t], s2), dl[h][s2], d);
           dl[h][t] = d;
         }
         if (tig < T) {
@@ -408,9 +414,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
 #pragma unroll
           for (int t = 0; t < T; ++t) {
             if (t != tig) continue;
-            float ov = hdr[H_GAM + t] * z[h][t];
+            float ov = el(gam4, t) * z[h][t];
 #pragma unroll
-            for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(hdr[H_B + 4 * t + s2], dl[h][s2], ov);
+            for (int s2 = 0; s2 <= t; ++s2) ov = fmaf(el(b4[t], s2), dl[h][s2], ov);
             const size_t oi = (((size_t)bi * T + t) * HV + hv) * DV + row;
             if (F32 && p.o_f32)
               static_cast<float *>(p.o)[oi] = ov;
@@ -419,12 +425,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
           }
         }
       }
-      // ---- update: C = G_{T-1} C + A B with A = [c d hi | c d lo | c d hi]
+      // ---- update: C = G_{T-1} S0 + A B with A = [c d hi | c d lo | c d hi]
       const float gt = hdr[H_GT];
-#pragma unroll
-      for (int n = 0; n < 16; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) C[n][e] *= gt;
       uint32_t ua[4];
       {
         float dh[2][T], dlo[2][T];
@@ -432,7 +434,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int t = 0; t < T; ++t) {
-            const float d = hdr[H_C + t] * dl[h][t];
+            const float d = el(c4, t) * dl[h][t];
             dh[h][t] = bf16_round(d);
             dlo[h][t] = d - dh[h][t];
           }
@@ -451,13 +453,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
         ua[2] = pack2(kval(0, 2 * tig + 8), kval(0, 2 * tig + 9));
         ua[3] = pack2(kval(1, 2 * tig + 8), kval(1, 2 * tig + 9));
       }
+      float *d32 = F32 && p.state_f32 ? p.state_f32 + ((size_t)bi * HV + hv) * DV * DK : nullptr;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        // block j of S0: af[0] / af[1] rows g / g + 8, columns 16 j + 2 tig (+1);
+        // af[2] / af[3] the same rows, columns + 8
+        unsigned char *blk = sw_addr(sw, r0, j, lane);
+        const uint32_t *af = S0f[j];
+        float C[2][4];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float2 rg = unpack2(af[2 * hf]), rg8 = unpack2(af[2 * hf + 1]);
+          C[hf][0] = gt * rg.x; C[hf][1] = gt * rg.y; C[hf][2] = gt * rg8.x; C[hf][3] = gt * rg8.y;
+        }
         uint32_t b[4];
         const int n = 16 * j + (lane & 7) + ((lane >> 4) << 3);
         ptx::ldmatrix_x4(aux + A_BU + n * BU_PITCH + ((lane >> 3) & 1) * 16, b[0], b[1], b[2], b[3]);
-        ptx::mma_16816_bf16(C[2 * j], ua, b[0], b[1]);
-        ptx::mma_16816_bf16(C[2 * j + 1], ua, b[2], b[3]);
+        ptx::mma_16816_bf16(C[0], ua, b[0], b[1]);
+        ptx::mma_16816_bf16(C[1], ua, b[2], b[3]);
+        if (F32 && d32) {
+          // the fp32 values the bf16 write-back rounds (entry bi, not its slot)
+          const int col = 16 * j + 2 * tig;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            *reinterpret_cast<float2 *>(d32 + (r0 + g) * DK + col + 8 * hf) =
+                make_float2(C[hf][0], C[hf][1]);
+            *reinterpret_cast<float2 *>(d32 + (r0 + g + 8) * DK + col + 8 * hf) =
+                make_float2(C[hf][2], C[hf][3]);
+          }
+        }
+        ptx::stmatrix_x4(blk, pack2(C[0][0], C[0][1]), pack2(C[0][2], C[0][3]),
+                         pack2(C[1][0], C[1][1]), pack2(C[1][2], C[1][3]));
       }
     }
 
@@ -477,24 +503,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_ld, const __grid_constan
     }
     order = __shfl_sync(0xffffffffu, order, 0);
 
-    if (F32 && slot >= 0 && p.state_f32) {
-      // the fp32 values the bf16 write-back rounds (entry bi, not its slot):
-      // rows r0 + g and r0 + g + 8, columns 8 n + 2 tig (+ 1)
-      float *d32 = p.state_f32 + ((size_t)bi * HV + hv) * DV * DK;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int col = 8 * n + 2 * tig;
-        *reinterpret_cast<float2 *>(d32 + (r0 + g) * DK + col) = make_float2(C[n][0], C[n][1]);
-        *reinterpret_cast<float2 *>(d32 + (r0 + g + 8) * DK + col) = make_float2(C[n][2], C[n][3]);
-      }
-    }
     if (slot >= 0) {
-      // ---- write back: bf16 fragments -> this warp's rows of the slot -> TMA store
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        ptx::stmatrix_x4(sw_addr(sw, r0, j, lane), pack2(C[2 * j][0], C[2 * j][1]),
-                         pack2(C[2 * j][2], C[2 * j][3]), pack2(C[2 * j + 1][0], C[2 * j + 1][1]),
-                         pack2(C[2 * j + 1][2], C[2 * j + 1][3]));
+      // ---- write back: this warp's updated rows of the slot -> TMA store
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {

@@ -84,7 +84,7 @@ def test_without_l2norm_and_custom_gate_params():
     assert_close(st32, st_ref, TOL_BF16, "state")
 
 
-@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("T", [1, 3, 4])
 def test_bad_slot_is_reported_and_skipped(T):
     inp = synth.decode_inputs(313, 3, T, 1, 1, 128, 128, pool=3, slots=[0, 9, 2])
     o, st32, pool = run_gpu(inp)
