@@ -364,14 +364,15 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, int tid) {
 //                          Tu hi | Tu lo
 //   small                  scales, gamma, factors, merge scratch, barriers
 // GDN stages the row-major k | q | v tiles in R1 + AQ before the gating; KDA
-// loads k and q straight into KQ (its gate tile takes R1).  Both fit two CTAs
-// per SM.
+// loads k and q as row-major tiles (128-byte rows, 128-byte swizzle) into KQ
+// itself (its gate tile takes R1), which the gating pass reads before it
+// writes the images there.  Both fit two CTAs per SM.
 constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 83968, I_SMALL = 100352;
 constexpr int INTRA_THREADS = 256;
 template <bool KDA>
 struct IntraLayout {
   static constexpr uint32_t SMALL = I_SMALL;
-  static constexpr uint32_t SMEM = SMALL + 8192;
+  static constexpr uint32_t SMEM = SMALL + 8192 + 1024;  // + up to 1 KB to align the base
 };
 
 template <bool KDA>
@@ -379,7 +380,9 @@ __global__ void __launch_bounds__(INTRA_THREADS, 2)
 intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
              TcParams p) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128-byte swizzle of the KDA k / q tiles follows address bits 4-9
+  unsigned char *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char *KQ = smem + I_KQ;
   unsigned char *VS = smem + I_VS;
   float *Asm = reinterpret_cast<float *>(smem + I_R1);
@@ -437,14 +440,13 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   // requests) in a staging area that is free until the gating, and are
   // rearranged into the operand images once they land
   if (KDA && lane == 0 && warp < 3) {
-    // canonical operand-image boxes (16-byte rows) straight into KQ
+    // row-major k | q tiles, two 8 KB halves of 64 keys each, into KQ
     if (warp == 0) {
-#pragma unroll 1
-      for (int j = 0; j < 16; ++j) ptx::tma_load_3d(KQ + j * 2048, &tm_k, 8 * j, hk, row0, &bars[0]);
+      ptx::tma_load_3d(KQ, &tm_k, 0, hk, row0, &bars[0]);
+      ptx::tma_load_3d(KQ + 8192, &tm_k, 64, hk, row0, &bars[0]);
     } else if (warp == 1) {
-#pragma unroll 1
-      for (int j = 0; j < 16; ++j)
-        ptx::tma_load_3d(KQ + j * 2048 + 1024, &tm_q, 8 * j, hk, row0, &bars[0]);
+      ptx::tma_load_3d(KQ + 16384, &tm_q, 0, hk, row0, &bars[0]);
+      ptx::tma_load_3d(KQ + 24576, &tm_q, 64, hk, row0, &bars[0]);
     } else {
       // the fp32 gate tile (64 tokens x 128 channels, row-major) into R1
       ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
@@ -595,6 +597,19 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     // each a hi + lo pair in the split path (the per-channel gate sits inside
     // the products, so its operands carry the rounding)
     const float *G = Asm;
+    // this thread's pieces of the row-major k and q tiles (16-byte piece cg of
+    // row i sits at piece cg ^ (i mod 8) of its 128-byte row), all read before
+    // the images overwrite the tiles
+    uint4 kraw[4], qraw[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int pc = tid + it * INTRA_THREADS;
+      const int i = pc & 63, cg = pc >> 6;
+      const uint32_t off = (cg >> 3) * 8192 + i * 128 + (((cg & 7) ^ (i & 7)) << 4);
+      kraw[it] = *reinterpret_cast<const uint4 *>(KQ + off);
+      qraw[it] = *reinterpret_cast<const uint4 *>(KQ + 16384 + off);
+    }
+    __syncthreads();
     uint4 klo[4], qlo[4];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
@@ -603,8 +618,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       uint4 *kp = reinterpret_cast<uint4 *>(KQ + img_off(i, 8 * cg, 2048));
       uint4 *qp = reinterpret_cast<uint4 *>(KQ + img_off(64 + i, 8 * cg, 2048));
       float kf[8], qf[8], a[8], b[8], c[8], t[8];
-      unpack8(*kp, kf);
-      unpack8(*qp, qf);
+      unpack8(kraw[it], kf);
+      unpack8(qraw[it], qf);
       const float4 ga = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg);
       const float4 gb = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg + 4);
       const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
@@ -1447,8 +1462,10 @@ bool make_gate_map(CUtensorMap *m, const float *base, int heads, long long rows)
 }
 
 // [rows][heads][dim] bf16 tensor, boxes of `width` x 1 x 64 (64 rows of
-// `width` contiguous elements each, row-major in shared memory).
-bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long rows, int width) {
+// `width` contiguous elements each, row-major in shared memory; with sw128,
+// 128-byte rows in the 128-byte swizzle).
+bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long rows, int width,
+              bool sw128 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows};
@@ -1456,7 +1473,8 @@ bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long ro
   cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1554,9 +1572,10 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const bool varlen = cp.cu_seqlens != nullptr;
   CUtensorMap mk, mq, mv, mg;
   const long long rows = (long long)cp.B * cp.T;
-  // GDN: row-major tiles into staging; KDA: canonical 16-byte-row boxes
-  const int wkq = kda ? 8 : 64, wv = kda ? 8 : 32;
-  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, wkq) || !make_map(&mq, cp.q, KD, cp.Hk, rows, wkq) ||
+  // k, q: row-major 64-key tiles (GDN into staging; KDA into KQ, 128-byte
+  // swizzle); v: GDN row-major 32-column tiles, KDA canonical 16-byte-row boxes
+  const int wv = kda ? 8 : 32;
+  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, 64, kda) || !make_map(&mq, cp.q, KD, cp.Hk, rows, 64, kda) ||
       !make_map(&mv, cp.v, cp.V, cp.H, rows, wv))
     return cudaErrorInvalidValue;
   if (kda) {
