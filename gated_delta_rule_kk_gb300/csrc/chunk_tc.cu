@@ -357,7 +357,7 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, int tid) {
 //   VS   [32768, 49152)    v (64 tokens x V), cs 1024
 //                          (KDA: first k e^-g, the B operand of S; v is loaded
 //                          once S is done)
-//   R1   [49152, 83968)    KDA gamma (fp32 64 x 128); then A | T (fp32, 64 x 68
+//   R1   [49152, 83968)    KDA gamma (fp32 64 x 128, swizzled: gidx); then A | T (fp32, 64 x 68
 //                          each); after the solve Tw hi | Tw lo (64 x 64, cs
 //                          1024) over A
 //   AQ   [83968, 100352)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
@@ -369,6 +369,14 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, int tid) {
 // writes the images there.  Both fit two CTAs per SM.
 constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 83968, I_SMALL = 100352;
 constexpr int INTRA_THREADS = 256;
+
+// KDA gate tile in R1: four TMA boxes of 32 channels x 64 rows (128-byte rows,
+// 128-byte swizzle), so that a warp reading one channel group of 32
+// consecutive rows, or one row of 32 channels, touches every bank once.
+// Index (in floats) of token row i, channel c.
+__device__ __forceinline__ int gidx(int i, int c) {
+  return (c >> 5) * 2048 + i * 32 + ((((c >> 2) & 7) ^ (i & 7)) << 2) + (c & 3);
+}
 template <bool KDA>
 struct IntraLayout {
   static constexpr uint32_t SMALL = I_SMALL;
@@ -448,8 +456,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       ptx::tma_load_3d(KQ + 16384, &tm_q, 0, hk, row0, &bars[0]);
       ptx::tma_load_3d(KQ + 24576, &tm_q, 64, hk, row0, &bars[0]);
     } else {
-      // the fp32 gate tile (64 tokens x 128 channels, row-major) into R1
-      ptx::tma_load_3d(Asm, &tm_g, 0, h, row0, &bars[0]);
+      // the fp32 gate tile (64 tokens x 128 channels) into R1, four boxes
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) ptx::tma_load_3d(Asm + j * 2048, &tm_g, 32 * j, h, row0, &bars[0]);
     }
   } else if (!KDA && lane == 0 && warp < 3) {
     if (warp == 0) {
@@ -555,11 +564,11 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       // already the cumulative gate: thread (c, half) checks the range of 32
       // rows of channel c and repeats row L - 1 over the padding rows
       const int c = tid & (KD - 1), r0 = (tid >> 7) * 32;
-      const float last = G[(L - 1) * KD + c];
+      const float last = G[gidx(L - 1, c)];
 #pragma unroll 8
       for (int i = r0; i < r0 + 32; ++i) {
         float x = last;
-        if (i < L) x = G[i * KD + c]; else G[i * KD + c] = last;
+        if (i < L) x = G[gidx(i, c)]; else G[gidx(i, c)] = last;
         mn = fminf(mn, x);
         mx = fmaxf(mx, x);
       }
@@ -572,8 +581,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       float acc = 0.f;
 #pragma unroll 8
       for (int i = 0; i < 64; ++i) {
-        if (i < L) acc += G[i * KD + c];
-        G[i * KD + c] = acc;
+        if (i < L) acc += G[gidx(i, c)];
+        G[gidx(i, c)] = acc;
         mn = fminf(mn, acc);
         mx = fmaxf(mx, acc);
       }
@@ -620,8 +629,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       float kf[8], qf[8], a[8], b[8], c[8], t[8];
       unpack8(kraw[it], kf);
       unpack8(qraw[it], qf);
-      const float4 ga = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg);
-      const float4 gb = *reinterpret_cast<const float4 *>(G + i * KD + 8 * cg + 4);
+      const float4 ga = *reinterpret_cast<const float4 *>(G + gidx(i, 8 * cg));
+      const float4 gb = *reinterpret_cast<const float4 *>(G + gidx(i, 8 * cg + 4));
       const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
       // (fp32 pairs: two products per instruction)
 #pragma unroll
@@ -729,7 +738,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
           const size_t oj = ((size_t)(row0 + j) * p.Hk + hk) * KD;
           for (int c = 0; c < KD; ++c)
             acc = fmaf(__bfloat162float(xg[oi + c]) * __bfloat162float(kg[oj + c]),
-                       __expf(G[i * KD + c] - G[j * KD + c]), acc);
+                       __expf(G[gidx(i, c)] - G[gidx(j, c)]), acc);
         }
         srow[jj] = acc;
       }
@@ -872,8 +881,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         ptx::tmem_ld32(dU + lane_base + t * 32, v);
         // 16-byte group q of row i sits at group q ^ (i & 7), so that the
         // chain's per-row loads (one row per lane) hit eight different groups
-        // in every quarter warp: no shared-memory bank conflicts
-        float4 *dst = reinterpret_cast<float4 *>(blk + OFF_U + t * 8192 + i * 128);
+        // in every quarter warp: no shared-memory bank conflicts.  The tile is
+        // staged in R1 (free once the WY GEMM is done) in the block's layout
+        // and leaves with the block's other parts in one bulk copy.
+        float4 *dst = reinterpret_cast<float4 *>(smem + I_R1 + t * 8192 + i * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           dst[q ^ (i & 7)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -889,6 +900,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   if (warp == 0) ptx::tmem_dealloc<256>(tmem);
   if (tid == 0) {
     ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
+    ptx::bulk_s2g(blk + OFF_U, smem + I_R1, (uint32_t)V * 256);
     ptx::bulk_commit();
     ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   }
@@ -1448,16 +1460,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [rows][heads][128] fp32 gate tensor, boxes of 128 x 1 x 64 (one tile).
+// [rows][heads][128] fp32 gate tensor, boxes of 32 x 1 x 64 (a quarter tile:
+// 64 rows of 128 bytes, 128-byte swizzle).
 bool make_gate_map(CUtensorMap *m, const float *base, int heads, long long rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3] = {(cuuint64_t)KD, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t gstride[2] = {(cuuint64_t)KD * 4, (cuuint64_t)heads * KD * 4};
-  cuuint32_t box[3] = {KD, 1, 64};
+  cuuint32_t box[3] = {32, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), gdim, gstride, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
