@@ -352,21 +352,24 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, int tid) {
 // and split the columns of every accumulator row)
 //
 // shared memory (bytes):
-//   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys), cs 2048;
-//                          at the end [-w ; q], the chain's A operand
-//   VS   [32768, 49152)    v (64 tokens x V), cs 1024
-//                          (KDA: first k e^-g, the B operand of S; v is loaded
-//                          once S is done)
+//   KQ   [0, 32768)        k rows 0..63 / q rows 64..127 (x 128 keys) as TMA
+//                          lands them: 128-byte swizzle, 64-key halves 16 KB
+//                          apart (swz_off); at the end [-w ; q], the chain's A
+//                          operand, in the same layout
+//   VS   [32768, 49152)    v (64 tokens x V) as TMA lands it: 64-byte swizzle,
+//                          32-column tiles 4 KB apart (the u GEMM's MN-major B)
+//                          (KDA: first k e^-g, the B operand of S, 128-byte
+//                          swizzle, halves 8 KB apart; v is loaded once S is
+//                          done)
 //   R1   [49152, 83968)    KDA gamma (fp32 64 x 128, swizzled: gidx); then A | T (fp32, 64 x 68
 //                          each); after the solve Tw hi | Tw lo (64 x 64, cs
 //                          1024) over A
 //   AQ   [83968, 100352)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
 //                          Tu hi | Tu lo
 //   small                  scales, gamma, factors, merge scratch, barriers
-// GDN stages the row-major k | q | v tiles in R1 + AQ before the gating; KDA
-// loads k and q as row-major tiles (128-byte rows, 128-byte swizzle) into KQ
-// itself (its gate tile takes R1), which the gating pass reads before it
-// writes the images there.  Both fit two CTAs per SM.
+// k, q and v land where the tensor cores read them, so there is no staging
+// copy; the KDA gating pass rewrites k and q in place.  Both fit two CTAs per
+// SM.
 constexpr uint32_t I_KQ = 0, I_VS = 32768, I_R1 = 49152, I_AQ = 83968, I_SMALL = 100352;
 constexpr int INTRA_THREADS = 256;
 
@@ -376,6 +379,19 @@ constexpr int INTRA_THREADS = 256;
 // Index (in floats) of token row i, channel c.
 __device__ __forceinline__ int gidx(int i, int c) {
   return (c >> 5) * 2048 + i * 32 + ((((c >> 2) & 7) ^ (i & 7)) << 2) + (c & 3);
+}
+
+// K-major image with a 128-byte swizzle (the layout TMA writes with 128-byte
+// rows): rows of 64 keys (128 bytes), the two 64-key halves `half` bytes
+// apart; the 16-byte piece cg (keys 8 cg ..) of row r sits at piece
+// (cg & 7) ^ (r & 7) of its row.  Offset of that piece:
+__device__ __forceinline__ uint32_t swz_off(int r, int cg, uint32_t half) {
+  return (uint32_t)(cg >> 3) * half + (uint32_t)r * 128u + ((uint32_t)((cg & 7) ^ (r & 7)) << 4);
+}
+// Descriptor of such an image as a K-major operand at key step ks (16 keys):
+// 32 bytes into the row inside a half, 8-row groups 1 KB apart.
+__device__ __forceinline__ uint64_t sw128_kmajor(const unsigned char *img, int ks, uint32_t half) {
+  return ptx::sdesc(img + (ks >> 2) * half + (ks & 3) * 32, 16, 1024) | (2ull << 61);
 }
 template <bool KDA>
 struct IntraLayout {
@@ -398,9 +414,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   unsigned char *TH = smem + I_R1;   // [Tw ; Tu] hi (after the solve, 128 x 64, cs 2048)
   unsigned char *AQ = smem + I_AQ;   // Aqk pair, later [Tw ; Tu] lo
   unsigned char *KB = VS;  // KDA: k e^-g, until the S GEMM is done
-  // GDN staging for the row-major k | q | v tiles (48 KB): R1 + AQ, first
-  // written by the gating
-  unsigned char *STG = smem + I_R1;
   float *sc = reinterpret_cast<float *>(smem + IntraLayout<KDA>::SMALL);  // decay, rs, qs
   float *gam = sc + 256;                                   // [64]
   float *bet = gam + 64;                                   // [64]
@@ -444,33 +457,26 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
   // three issuing threads, one per tensor, once warp 0 has set the barrier up
   if (warp < 3) asm volatile("bar.sync 1, 96;" ::: "memory");
-  // k, q and v arrive row-major (128-byte, resp. 64-byte rows: few large
-  // requests) in a staging area that is free until the gating, and are
-  // rearranged into the operand images once they land
-  if (KDA && lane == 0 && warp < 3) {
-    // row-major k | q tiles, two 8 KB halves of 64 keys each, into KQ
-    if (warp == 0) {
-      ptx::tma_load_3d(KQ, &tm_k, 0, hk, row0, &bars[0]);
-      ptx::tma_load_3d(KQ + 8192, &tm_k, 64, hk, row0, &bars[0]);
-    } else if (warp == 1) {
-      ptx::tma_load_3d(KQ + 16384, &tm_q, 0, hk, row0, &bars[0]);
-      ptx::tma_load_3d(KQ + 24576, &tm_q, 64, hk, row0, &bars[0]);
-    } else {
+  // k, q and v arrive in 128-byte (v: 64-byte) swizzled rows, few large
+  // requests, straight into the operand images
+  if (lane == 0 && warp == 0) {
+    // k rows 0..63 of each 64-key half of KQ
+    ptx::tma_load_3d(KQ, &tm_k, 0, hk, row0, &bars[0]);
+    ptx::tma_load_3d(KQ + 16384, &tm_k, 64, hk, row0, &bars[0]);
+  }
+  if (lane == 0 && warp == 1) {
+    // q rows 64..127
+    ptx::tma_load_3d(KQ + 8192, &tm_q, 0, hk, row0, &bars[0]);
+    ptx::tma_load_3d(KQ + 24576, &tm_q, 64, hk, row0, &bars[0]);
+  }
+  if (lane == 0 && warp == 2) {
+    if (KDA) {
       // the fp32 gate tile (64 tokens x 128 channels) into R1, four boxes
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) ptx::tma_load_3d(Asm + j * 2048, &tm_g, 32 * j, h, row0, &bars[0]);
-    }
-  } else if (!KDA && lane == 0 && warp < 3) {
-    if (warp == 0) {
-      ptx::tma_load_3d(STG, &tm_k, 0, hk, row0, &bars[0]);
-      ptx::tma_load_3d(STG + 8192, &tm_k, 64, hk, row0, &bars[0]);
-    } else if (warp == 1) {
-      ptx::tma_load_3d(STG + 16384, &tm_q, 0, hk, row0, &bars[0]);
-      ptx::tma_load_3d(STG + 24576, &tm_q, 64, hk, row0, &bars[0]);
     } else {
 #pragma unroll 1
-      for (int j = 0; j < V / 32; ++j)
-        ptx::tma_load_3d(STG + 32768 + j * 4096, &tm_v, 32 * j, h, row0, &bars[0]);
+      for (int j = 0; j < V / 32; ++j) ptx::tma_load_3d(VS + j * 4096, &tm_v, 32 * j, h, row0, &bars[0]);
     }
   }
   if (warp == 0) ptx::tmem_alloc<256>(tmem_slot);
@@ -534,25 +540,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     if (warp == 0) ptx::tmem_dealloc<256>(tmem);
     return;
   }
-  // staging -> operand images, 16 bytes at a time.  Eight consecutive lanes
-  // take eight rows and eight different 16-byte columns (a rotation), so both
-  // the row-major reads and the column-group writes are free of bank conflicts.
-  for (int idx = tid; idx < (KDA ? 0 : 2048); idx += INTRA_THREADS) {
-    const int which = idx >> 10, j = idx & 7, grp = (idx >> 3) & 127;
-    const int r = (grp & 7) * 8 + j, cgp = grp >> 3;
-    const int c8 = (cgp & 8) | ((j + cgp) & 7);
-    const uint4 x = *reinterpret_cast<const uint4 *>(STG + which * 16384 + (c8 >> 3) * 8192 +
-                                                     r * 128 + (c8 & 7) * 16);
-    *reinterpret_cast<uint4 *>(KQ + c8 * 2048 + (which * 64 + r) * 16) = x;
-  }
-  for (int idx = tid; idx < (KDA ? 0 : 8 * V); idx += INTRA_THREADS) {
-    const int j = idx & 7, grp = idx >> 3;
-    const int r = (grp & 7) * 8 + j, cg = grp >> 3;
-    const int c8 = (cg & ~3) | ((j + cg) & 3);
-    const uint4 x = *reinterpret_cast<const uint4 *>(STG + 32768 + (c8 >> 2) * 4096 + r * 64 +
-                                                     (c8 & 3) * 16);
-    *reinterpret_cast<uint4 *>(VS + c8 * 1024 + r * 16) = x;
-  }
   ptx::fence_proxy_async_smem();  // the images feed the tensor cores
   __syncthreads();
   if (KDA) {
@@ -606,29 +593,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     // each a hi + lo pair in the split path (the per-channel gate sits inside
     // the products, so its operands carry the rounding)
     const float *G = Asm;
-    // this thread's pieces of the row-major k and q tiles (16-byte piece cg of
-    // row i sits at piece cg ^ (i mod 8) of its 128-byte row), all read before
-    // the images overwrite the tiles
-    uint4 kraw[4], qraw[4];
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int pc = tid + it * INTRA_THREADS;
-      const int i = pc & 63, cg = pc >> 6;
-      const uint32_t off = (cg >> 3) * 8192 + i * 128 + (((cg & 7) ^ (i & 7)) << 4);
-      kraw[it] = *reinterpret_cast<const uint4 *>(KQ + off);
-      qraw[it] = *reinterpret_cast<const uint4 *>(KQ + 16384 + off);
-    }
-    __syncthreads();
     uint4 klo[4], qlo[4];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       const int pc = tid + it * INTRA_THREADS;
       const int i = pc & 63, cg = pc >> 6;
-      uint4 *kp = reinterpret_cast<uint4 *>(KQ + img_off(i, 8 * cg, 2048));
-      uint4 *qp = reinterpret_cast<uint4 *>(KQ + img_off(64 + i, 8 * cg, 2048));
+      // rewritten in place: each piece is read and written by its own thread
+      uint4 *kp = reinterpret_cast<uint4 *>(KQ + swz_off(i, cg, 16384));
+      uint4 *qp = reinterpret_cast<uint4 *>(KQ + swz_off(64 + i, cg, 16384));
       float kf[8], qf[8], a[8], b[8], c[8], t[8];
-      unpack8(kraw[it], kf);
-      unpack8(qraw[it], qf);
+      unpack8(*kp, kf);
+      unpack8(*qp, qf);
       const float4 ga = *reinterpret_cast<const float4 *>(G + gidx(i, 8 * cg));
       const float4 gb = *reinterpret_cast<const float4 *>(G + gidx(i, 8 * cg + 4));
       const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
@@ -657,8 +632,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       split8(b, hi, qlo[it]);
       *qp = hi;
       split8(c, hi, lo);
-      *reinterpret_cast<uint4 *>(KB + img_off(i, 8 * cg, 1024)) = hi;
-      if (split) *reinterpret_cast<uint4 *>(KBL + img_off(i, 8 * cg, 1024)) = lo;
+      *reinterpret_cast<uint4 *>(KB + swz_off(i, cg, 8192)) = hi;
+      if (split) *reinterpret_cast<uint4 *>(KBL + swz_off(i, cg, 8192)) = lo;
       split8(t, hi, lo);
       *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(i, 8 * cg, 2048)) = hi;
       *reinterpret_cast<uint4 *>(blk + OFF_KT + img_off(64 + i, 8 * cg, 2048)) = lo;
@@ -669,8 +644,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       for (int it = 0; it < 4; ++it) {
         const int pc = tid + it * INTRA_THREADS;
         const int i = pc & 63, cg = pc >> 6;
-        *reinterpret_cast<uint4 *>(KQL + img_off(i, 8 * cg, 2048)) = klo[it];
-        *reinterpret_cast<uint4 *>(KQL + img_off(64 + i, 8 * cg, 2048)) = qlo[it];
+        *reinterpret_cast<uint4 *>(KQL + swz_off(i, cg, 16384)) = klo[it];
+        *reinterpret_cast<uint4 *>(KQL + swz_off(64 + i, cg, 16384)) = qlo[it];
       }
     }
     ptx::fence_proxy_async_smem();
@@ -685,21 +660,18 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   if (tid == 0) {
     ptx::tc_fence_after();
     const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
-    const unsigned char *Bop = KDA ? KB : KQ;
-    const uint32_t b_cs = KDA ? 1024u : 2048u;
+    // (B: the k rows of KQ; KDA: KB, 64 rows a half)
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const uint64_t a = ptx::sdesc(KQ + ks * 2 * 2048, 2048, 128);
-      const uint64_t b = ptx::sdesc(Bop + ks * 2 * b_cs, b_cs, 128);
+      const uint64_t a = sw128_kmajor(KQ, ks, 16384);
+      const uint64_t b = KDA ? sw128_kmajor(KB, ks, 8192) : a;
       ptx::mma_bf16(tmem, a, b, id, ks > 0);
     }
     if (KDA && split) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        ptx::mma_bf16(tmem, ptx::sdesc(KQ + ks * 2 * 2048, 2048, 128),
-                      ptx::sdesc(KBL + ks * 2 * 1024, 1024, 128), id, 1);
-        ptx::mma_bf16(tmem, ptx::sdesc(KQL + ks * 2 * 2048, 2048, 128),
-                      ptx::sdesc(KB + ks * 2 * 1024, 1024, 128), id, 1);
+        ptx::mma_bf16(tmem, sw128_kmajor(KQ, ks, 16384), sw128_kmajor(KBL, ks, 8192), id, 1);
+        ptx::mma_bf16(tmem, sw128_kmajor(KQL, ks, 16384), sw128_kmajor(KB, ks, 8192), id, 1);
       }
     }
     ptx::mma_commit(&bars[1]);
@@ -712,7 +684,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   if (KDA && tid == 0) {
     // S is done with KB: v into VS, counted on the second phase of bars[0]
     ptx::mbar_arrive_expect_tx(&bars[0], (uint32_t)V * 128);
-    for (int j = 0; j < V / 8; ++j) ptx::tma_load_3d(VS + j * 1024, &tm_v, 8 * j, h, row0, &bars[0]);
+    for (int j = 0; j < V / 32; ++j) ptx::tma_load_3d(VS + j * 4096, &tm_v, 32 * j, h, row0, &bars[0]);
   }
 
   // ---- gating: thread (qd, hf, lane) holds row r = 32 qd + lane of S,
@@ -730,7 +702,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       const float *G = Asm;
       const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.kraw);
       const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(is_q ? p.qraw : p.kraw);
-      for (int jj = 0; jj < 32; ++jj) {
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {  // unrolled: srow stays in registers
         const int j = j0 + jj;
         float acc = 0.f;
         if (i < L && j <= i) {
@@ -840,9 +813,12 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const uint64_t a = ptx::sdesc(img + ks * 4096, 2048, 128);
-        const uint64_t b = ptx::sdesc(KQ + ks * 256, 128, 2048);
+        // k rows of KQ, MN-major: 64-key halves 16 KB apart, 8-token groups 1 KB
+        const uint64_t b = ptx::sdesc(KQ + ks * 2048, 16384, 1024) | (2ull << 61);
         ptx::mma_bf16(dW, a, b, idw, part > 0 || ks > 0);
-        const uint64_t bv = ptx::sdesc(VS + ks * 256, 128, 1024);
+        // v, MN-major with a 64-byte swizzle: 32-column tiles 4 KB apart,
+        // 8-token groups 512 bytes
+        const uint64_t bv = ptx::sdesc(VS + ks * 1024, 4096, 512) | (4ull << 61);
         ptx::mma_bf16(dU, a, bv, idu, part > 0 || ks > 0);
       }
     }
@@ -870,7 +846,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
           float out[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) out[e] = -v[q8 * 8 + e];
-          *reinterpret_cast<uint4 *>(KQ + img_off(i, q4 * 32 + q8 * 8, 2048)) = pack8(out);
+          *reinterpret_cast<uint4 *>(KQ + swz_off(i, q4 * 4 + q8, 16384)) = pack8(out);
         }
       }
     } else {
@@ -891,7 +867,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
   }
-  // KQ is now the chain's A operand [-w ; q] (cs 2048).  The tensor memory is
+  // KQ is now the chain's A operand [-w ; q] (swz_off layout).  The tensor memory is
   // no longer read: free it before waiting on the store, so that the next
   // CTA on this SM can allocate it while this one drains.
   ptx::fence_proxy_async_smem();
@@ -911,7 +887,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 // chain kernel (320 threads: warps 0-7 epilogue, warp 8 producer, warp 9 MMA)
 //
 // shared memory: two stages holding one operand block each
-//   AW  [0, 32768)       [-w ; q~] (128 x 128, cs 2048)
+//   AW  [0, 32768)       [-w ; q~] (128 x 128, 128-byte swizzle, halves 16 KB apart)
 //   KT  [32768, 65536)   [k~_hi ; k~_lo] (128 token rows x 128 keys, cs 2048);
 //                        scalar gate: raw k of the chunk by TMA, two 8 KB halves
 //                        of 64 keys x 64 token rows (128-byte swizzle)
@@ -1138,7 +1114,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
     for (int c = 0; c < nch; ++c) {
       const int s = c & 1, k = c >> 1;
       unsigned char *st = smem + s * STAGE_BYTES;
-      const uint64_t aw = ptx::sdesc(st + S_AW, 2048, 128);
       const uint64_t kt = ptx::sdesc(st + S_KT, 128, 2048);
       const uint64_t aq = ptx::sdesc(st + S_AQ, 2048, 128);
       ok = ptx::mbar_wait_bounded(&fullA[s], (uint32_t)(k & 1)) && ok;
@@ -1146,10 +1121,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       bar_sync(BAR_HREADY, BAR_HREADY_THREADS);  // h of this chunk is in H
       ptx::tc_fence_after();
       if (lane == 0) {
-        // D1 = [-w ; q~] [h_hi | h_lo]
+        // D1 = [-w ; q~] [h_hi | h_lo] (AW K-major, 128-byte swizzle: swz_off)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          ptx::mma_bf16(dD1, adv(aw, ks * 4096), adv(dH0, ks * 256), id_kmn, ks > 0);
+          ptx::mma_bf16(dD1, sw128_kmajor(st + S_AW, ks, 16384), adv(dH0, ks * 256), id_kmn, ks > 0);
         ptx::mma_commit(d1);
         ptx::mma_commit(&emptyA[s]);  // D1 no longer reads AW
       }
@@ -1475,10 +1450,10 @@ bool make_gate_map(CUtensorMap *m, const float *base, int heads, long long rows)
 }
 
 // [rows][heads][dim] bf16 tensor, boxes of `width` x 1 x 64 (64 rows of
-// `width` contiguous elements each, row-major in shared memory; with sw128,
-// 128-byte rows in the 128-byte swizzle).
+// `width` contiguous elements each, in the given swizzle: 128-byte rows with
+// the 128-byte swizzle, 64-byte rows with the 64-byte one).
 bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long rows, int width,
-              bool sw128 = false) {
+              CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)rows};
@@ -1486,8 +1461,7 @@ bool make_map(CUtensorMap *m, const void *base, int dim, int heads, long long ro
   cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1585,11 +1559,10 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const bool varlen = cp.cu_seqlens != nullptr;
   CUtensorMap mk, mq, mv, mg;
   const long long rows = (long long)cp.B * cp.T;
-  // k, q: row-major 64-key tiles (GDN into staging; KDA into KQ, 128-byte
-  // swizzle); v: GDN row-major 32-column tiles, KDA canonical 16-byte-row boxes
-  const int wv = kda ? 8 : 32;
-  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, 64, kda) || !make_map(&mq, cp.q, KD, cp.Hk, rows, 64, kda) ||
-      !make_map(&mv, cp.v, cp.V, cp.H, rows, wv))
+  // k, q: 64-key tiles, 128-byte swizzle; v: 32-column tiles, 64-byte swizzle
+  if (!make_map(&mk, cp.k, KD, cp.Hk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mq, cp.q, KD, cp.Hk, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mv, cp.v, cp.V, cp.H, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   if (kda) {
     if (!make_gate_map(&mg, cp.g, cp.H, rows)) return cudaErrorInvalidValue;
