@@ -894,8 +894,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 //   AQ  [65536, 81920)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
 //   SC  [81920, 82944)   decay[128], rs[64], qs[64]
 //   U   [82944, 91136)   u tile, fp32 64 x 32 (row-swizzled 16-byte groups)
-// then H = [h_hi | h_lo] (128 keys x 64, cs 2048), VN = [vn_hi | vn_lo]
-// (64 tokens x 64, cs 1024; scalar gate: e^{gamma_L - gamma_i} v_new, the
+// then H = [h_hi | h_lo] (128 keys x 64), VN = [vn_hi | vn_lo]
+// (64 tokens x 64; both in 128-byte swizzled rows; scalar gate: e^{gamma_L - gamma_i} v_new, the
 // state update's operand, with v_new itself for the output GEMM in VN2) and
 // the fp32 exchange X.  A stage is filled and
 // released in two halves: AW, SC and U are free once D1 has run and v_new is
@@ -942,16 +942,17 @@ __device__ __forceinline__ void tmem_ld_pair16(uint32_t taddr, int c0, float *v)
   for (int j = 0; j < 16; ++j) v[j] += lo[j];
 }
 
-// 16 values -> hi/lo bf16 halves of an image with column-group stride cs
-// (hi in columns c0.., lo in columns 32 + c0..)
-__device__ __forceinline__ void store_pair16(unsigned char *img, int r, int c0, uint32_t cs,
-                                             const float *v) {
+// 16 values -> hi/lo bf16 halves of row r of a 64-column image with 128-byte
+// rows in the 128-byte swizzle (hi in columns c0.., lo in columns 32 + c0..;
+// 16-byte piece j of row r at piece j ^ (r & 7))
+__device__ __forceinline__ void store_pair16(unsigned char *img, int r, int c0, const float *v) {
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     uint4 hi, lo;
     split8(v + 8 * g, hi, lo);
-    *reinterpret_cast<uint4 *>(img + img_off(r, c0 + 8 * g, cs)) = hi;
-    *reinterpret_cast<uint4 *>(img + img_off(r, 32 + c0 + 8 * g, cs)) = lo;
+    const int jh = (c0 >> 3) + g, jl = 4 + (c0 >> 3) + g;
+    *reinterpret_cast<uint4 *>(img + r * 128 + ((jh ^ (r & 7)) << 4)) = hi;
+    *reinterpret_cast<uint4 *>(img + r * 128 + ((jl ^ (r & 7)) << 4)) = lo;
   }
 }
 
@@ -1107,8 +1108,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
     // the named barriers that hand over h and v_new)
     const uint32_t id_kmn = ptx::idesc_bf16(128, 2 * VTILE, 0, 1);   // A K-major, B MN-major
     const uint32_t id_mnmn = ptx::idesc_bf16(128, 2 * VTILE, 1, 1);  // both MN-major
-    const uint64_t dH0 = ptx::sdesc(Himg, 128, 2048);
-    const uint64_t dVN0 = ptx::sdesc(VN, 128, 1024);
+    // H (128 key rows) and VN / VN2 (64 token rows) as MN-major B operands:
+    // 64 columns of 128-byte swizzled rows, 8-row groups 1 KB apart
+    const uint64_t dH0 = ptx::sdesc(Himg, 16384, 1024) | (2ull << 61);
+    const uint64_t dVN0 = ptx::sdesc(VN, 8192, 1024) | (2ull << 61);
     bool ok = true;
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
@@ -1124,7 +1127,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
         // D1 = [-w ; q~] [h_hi | h_lo] (AW K-major, 128-byte swizzle: swz_off)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          ptx::mma_bf16(dD1, sw128_kmajor(st + S_AW, ks, 16384), adv(dH0, ks * 256), id_kmn, ks > 0);
+          ptx::mma_bf16(dD1, sw128_kmajor(st + S_AW, ks, 16384), adv(dH0, ks * 2048), id_kmn, ks > 0);
         ptx::mma_commit(d1);
         ptx::mma_commit(&emptyA[s]);  // D1 no longer reads AW
       }
@@ -1139,13 +1142,13 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
           const uint64_t kr = ptx::sdesc(st + S_KT, 8192, 1024) | (2ull << 61);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            ptx::mma_bf16(dDH, adv(kr, ks * 2048), adv(dVN0, ks * 256), id_mnmn, ks > 0);
+            ptx::mma_bf16(dDH, adv(kr, ks * 2048), adv(dVN0, ks * 2048), id_mnmn, ks > 0);
         } else {
           // DH = [k~_hi ; k~_lo]^T [vn_hi | vn_lo ; vn_hi | vn_lo] (K = 128:
           // the token rows once with each half of k~; critical path)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 256), id_mnmn, ks > 0);
+            ptx::mma_bf16(dDH, adv(kt, ks * 256), adv(dVN0, (ks & 3) * 2048), id_mnmn, ks > 0);
         }
         ptx::mma_commit(d3);
       }
@@ -1156,10 +1159,10 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       }
       if (lane == 0) {
         // D5 = AQ [vn_hi | vn_lo]
-        const uint64_t dVN2 = ptx::sdesc(VN2, 128, 1024);
+        const uint64_t dVN2 = ptx::sdesc(VN2, 8192, 1024) | (2ull << 61);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN2, ks * 256), id_kmn, ks > 0);
+          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN2, ks * 2048), id_kmn, ks > 0);
         ptx::mma_commit(d5);
         ptx::mma_commit(&emptyB[s]);
       }
@@ -1209,7 +1212,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) hs[j] = 0.f;
     }
-    store_pair16(Himg, r, c0, 2048, hs);
+    store_pair16(Himg, r, c0, hs);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     bar_arrive(BAR_HREADY, BAR_HREADY_THREADS);
@@ -1249,16 +1252,16 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
             float vt[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) vt[j] = f * vn[j];
-            store_pair16(VN, r, c0, 1024, vt);
+            store_pair16(VN, r, c0, vt);
           } else {
-            store_pair16(VN, r, c0, 1024, vn);
+            store_pair16(VN, r, c0, vn);
           }
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
           __syncwarp();
           bar_arrive(BAR_VNREADY, BAR_VNREADY_THREADS);
           if (RAWK) {
-            store_pair16(VN2, r, c0, 1024, vn);
+            store_pair16(VN2, r, c0, vn);
             ptx::fence_proxy_async_smem();
             __syncwarp();
             bar_arrive(BAR_VN2READY, BAR_VNREADY_THREADS);
@@ -1277,7 +1280,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
         tmem_ld_pair16(dDH + lane_base, c0, d);
 #pragma unroll
         for (int j = 0; j < 16; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
-        store_pair16(Himg, r, c0, 2048, hs);
+        store_pair16(Himg, r, c0, hs);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
