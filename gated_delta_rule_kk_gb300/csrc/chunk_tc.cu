@@ -74,9 +74,9 @@ constexpr int VMAX = 128;
 constexpr float GATE_FACTOR_LIMIT = 80.f;  // |gamma| bound for split exponentials
 
 // per (chunk, head) block in the workspace: the chain's operand images
-//   AW  [-w ; q~] (128 x 128 bf16, cs 2048)
+//   AW  [-w ; q~] (128 x 128 bf16, 128-byte swizzled rows, 64-column halves 16 KB apart)
 //   KT  [k~_hi ; k~_lo] (128 token rows x 128 keys bf16, cs 2048)
-//   AQ  [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048) SC  decay[128], rs[64], qs[64]
+//   AQ  [Aqk_lo ; Aqk_hi] (128 x 64, 128-byte swizzled rows) SC  decay[128], rs[64], qs[64]
 //   U   u, fp32 [V / 32 tiles][64][32], 16-byte group q of row i at q ^ (i & 7)
 constexpr uint32_t OFF_AW = 0, OFF_KT = 32768, OFF_AQ = 65536, OFF_SC = 81920, OFF_U = 82944;
 __host__ __device__ constexpr uint32_t block_bytes(int V, bool) {
@@ -361,11 +361,12 @@ __device__ void unit_lower_inverse_64(const float *A, float *Tm, int tid) {
 //                          (KDA: first k e^-g, the B operand of S, 128-byte
 //                          swizzle, halves 8 KB apart; v is loaded once S is
 //                          done)
-//   R1   [49152, 83968)    KDA gamma (fp32 64 x 128, swizzled: gidx); then A | T (fp32, 64 x 68
-//                          each); after the solve Tw hi | Tw lo (64 x 64, cs
-//                          1024) over A
-//   AQ   [83968, 100352)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048); once stored,
-//                          Tu hi | Tu lo
+//   R1   [49152, 83968)    KDA gamma (fp32 64 x 128, swizzled: gidx); then A | T
+//                          (fp32, 64 x 68 each); after the solve [Tw ; Tu] hi
+//                          (128 x 64, 128-byte swizzled rows) over A; last, the
+//                          fp32 u tile for the block store
+//   AQ   [83968, 100352)   [Aqk_lo ; Aqk_hi] (128 x 64, 128-byte swizzled rows);
+//                          once stored, [Tw ; Tu] lo
 //   small                  scales, gamma, factors, merge scratch, barriers
 // k, q and v land where the tensor cores read them, so there is no staging
 // copy; the KDA gating pass rewrites k and q in place.  Both fit two CTAs per
@@ -387,6 +388,10 @@ __device__ __forceinline__ int gidx(int i, int c) {
 // (cg & 7) ^ (r & 7) of its row.  Offset of that piece:
 __device__ __forceinline__ uint32_t swz_off(int r, int cg, uint32_t half) {
   return (uint32_t)(cg >> 3) * half + (uint32_t)r * 128u + ((uint32_t)((cg & 7) ^ (r & 7)) << 4);
+}
+// Offset of 16-byte piece j of row r of a one-half image (64 columns).
+__device__ __forceinline__ uint32_t swz_row(int r, int j) {
+  return (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4);
 }
 // Descriptor of such an image as a K-major operand at key step ks (16 keys):
 // 32 bytes into the row inside a half, 8-row groups 1 KB apart.
@@ -411,7 +416,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   unsigned char *VS = smem + I_VS;
   float *Asm = reinterpret_cast<float *>(smem + I_R1);
   float *Tsm = Asm + 64 * SLD;
-  unsigned char *TH = smem + I_R1;   // [Tw ; Tu] hi (after the solve, 128 x 64, cs 2048)
+  unsigned char *TH = smem + I_R1;   // [Tw ; Tu] hi (after the solve, 128 x 64, swizzled rows)
   unsigned char *AQ = smem + I_AQ;   // Aqk pair, later [Tw ; Tu] lo
   unsigned char *KB = VS;  // KDA: k e^-g, until the S GEMM is done
   float *sc = reinterpret_cast<float *>(smem + IntraLayout<KDA>::SMALL);  // decay, rs, qs
@@ -747,8 +752,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         }
         uint4 hi, lo;
         split8(v8, hi, lo);
-        *reinterpret_cast<uint4 *>(AQ + img_off(64 + i, j0 + 8 * cg, 2048)) = hi;
-        *reinterpret_cast<uint4 *>(AQ + img_off(i, j0 + 8 * cg, 2048)) = lo;
+        *reinterpret_cast<uint4 *>(AQ + swz_row(64 + i, (j0 >> 3) + cg)) = hi;
+        *reinterpret_cast<uint4 *>(AQ + swz_row(i, (j0 >> 3) + cg)) = lo;
       }
     }
   }
@@ -767,7 +772,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 
   // ---- Tw = T diag(beta e^g) (GDN) / T diag(beta) (KDA) in rows 0..63 and
   //      Tu = T diag(beta) in rows 64..127 of one 128 x 64 image per bf16 half
-  //      (hi in TH, lo in the AQ region; cs 2048), so that one M = 128 GEMM per
+  //      (hi in TH, lo in the AQ region; 128-byte swizzled rows), so that one M = 128 GEMM per
   //      operand puts w and u in all four TMEM lane quarters
   for (int pc = tid; pc < 64 * 16; pc += INTRA_THREADS) {
     const int i = pc & 63, cg = pc >> 6;
@@ -790,8 +795,8 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     uint4 hi, lo;
     split8(v8, hi, lo);
     const int row = is_u ? 64 + i : i;
-    *reinterpret_cast<uint4 *>(TH + img_off(row, j0, 2048)) = hi;
-    *reinterpret_cast<uint4 *>(AQ + img_off(row, j0, 2048)) = lo;
+    *reinterpret_cast<uint4 *>(TH + swz_row(row, j0 >> 3)) = hi;
+    *reinterpret_cast<uint4 *>(AQ + swz_row(row, j0 >> 3)) = lo;
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
@@ -812,7 +817,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       unsigned char *img = part ? AQ : TH;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t a = ptx::sdesc(img + ks * 4096, 2048, 128);
+        const uint64_t a = sw128_kmajor(img, ks, 0);  // K = 64 tokens: one half
         // k rows of KQ, MN-major: 64-key halves 16 KB apart, 8-token groups 1 KB
         const uint64_t b = ptx::sdesc(KQ + ks * 2048, 16384, 1024) | (2ull << 61);
         ptx::mma_bf16(dW, a, b, idw, part > 0 || ks > 0);
@@ -891,7 +896,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 //   KT  [32768, 65536)   [k~_hi ; k~_lo] (128 token rows x 128 keys, cs 2048);
 //                        scalar gate: raw k of the chunk by TMA, two 8 KB halves
 //                        of 64 keys x 64 token rows (128-byte swizzle)
-//   AQ  [65536, 81920)   [Aqk_lo ; Aqk_hi] (128 x 64, cs 2048)
+//   AQ  [65536, 81920)   [Aqk_lo ; Aqk_hi] (128 x 64, 128-byte swizzled rows)
 //   SC  [81920, 82944)   decay[128], rs[64], qs[64]
 //   U   [82944, 91136)   u tile, fp32 64 x 32 (row-swizzled 16-byte groups)
 // then H = [h_hi | h_lo] (128 keys x 64), VN = [vn_hi | vn_lo]
@@ -1118,7 +1123,6 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       const int s = c & 1, k = c >> 1;
       unsigned char *st = smem + s * STAGE_BYTES;
       const uint64_t kt = ptx::sdesc(st + S_KT, 128, 2048);
-      const uint64_t aq = ptx::sdesc(st + S_AQ, 2048, 128);
       ok = ptx::mbar_wait_bounded(&fullA[s], (uint32_t)(k & 1)) && ok;
       __syncwarp();
       bar_sync(BAR_HREADY, BAR_HREADY_THREADS);  // h of this chunk is in H
@@ -1162,7 +1166,7 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
         const uint64_t dVN2 = ptx::sdesc(VN2, 8192, 1024) | (2ull << 61);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          ptx::mma_bf16(dD5, adv(aq, ks * 4096), adv(dVN2, ks * 2048), id_kmn, ks > 0);
+          ptx::mma_bf16(dD5, sw128_kmajor(st + S_AQ, ks, 0), adv(dVN2, ks * 2048), id_kmn, ks > 0);
         ptx::mma_commit(d5);
         ptx::mma_commit(&emptyB[s]);
       }
