@@ -239,6 +239,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 }
 
 
+// ---- programmatic dependent launch ----------------------------------------
+
+// In a grid launched with programmatic stream serialization: waits until the
+// grids it depends on have completed and their memory operations are visible
+// (returns at once otherwise).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- warp-level matrix fragments (ldmatrix / stmatrix / mma.sync) --------
 
 // Four 8x8 b16 matrices; lane i supplies the address of row i % 8 of matrix
