@@ -433,6 +433,9 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   const int qd = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
   const int h = blockIdx.y;
   ChunkPos cp;
+  // packed sequences: launched as a programmatic dependent of the chunk-table
+  // kernel, so the table is read once that kernel is done
+  if (p.cu_seqlens) ptx::griddep_wait();
   if (!locate_chunk(p, blockIdx.x, cp)) return;
   const int hk = h / (p.H / p.Hk);
   const int V = p.V;
@@ -1368,6 +1371,7 @@ constexpr int COMB_THREADS = 256, COMB_COLS = 8, COMB_LDM = KD + 4;
 constexpr uint32_t COMB_SMEM = (2 * KD * COMB_LDM + KD * COMB_COLS) * 4;
 __global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(TcParams p) {
   extern __shared__ __align__(16) float csm[];
+  ptx::griddep_wait();  // a programmatic dependent of the phase-1 chain grid
   float *X = csm + 2 * KD * COMB_LDM;  // the running state's tile, [KD][COMB_COLS]
   const int h = blockIdx.y, n = blockIdx.z;
   const int S = p.seg_count, W = KD + p.V, tid = threadIdx.x;
@@ -1614,9 +1618,22 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   const uint32_t ismem = kda ? IntraLayout<true>::SMEM : IntraLayout<false>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(ik, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ismem);
   if (e != cudaSuccess) return e;
-  ik<<<dim3((unsigned)nchunks, cp.H), INTRA_THREADS, ismem, stream>>>(mk, mq, mv, mg, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // Every kernel after the first is a programmatic dependent launch: its CTAs
+  // start as the previous grid's CTAs exit and wait (griddepcontrol.wait)
+  // for its results before reading them, which hides the launch gap (few long
+  // chains with segments: 82.9 -> 78 us).  The intra kernel is one only behind
+  // the chunk-table kernel: as the first kernel of a call it was 0.9 us slower.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t icfg = {};
+  icfg.gridDim = dim3((unsigned)nchunks, cp.H);
+  icfg.blockDim = dim3(INTRA_THREADS);
+  icfg.dynamicSmemBytes = ismem;
+  icfg.stream = stream;
+  icfg.attrs = pdl;
+  icfg.numAttrs = varlen ? 1 : 0;
+  if ((e = cudaLaunchKernelEx(&icfg, ik, mk, mq, mv, mg, p)) != cudaSuccess) return e;
   CUtensorMap mkr;
   if (kda) {
     mkr = mk;  // unused: the per-channel chain reads KT
@@ -1626,14 +1643,10 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   auto chain = kda ? chain_kernel<false> : chain_kernel<true>;
   e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  // The chain kernel right after the intra kernel is a programmatic
-  // dependent launch: its CTAs start as the intra kernel's CTAs exit, run
-  // their set-up and then wait for its results (GDN 170.2 -> 166.9 us).  An
-  // explicit early trigger in the intra kernel, which lets the chain grid be
-  // scheduled during the intra kernel's last wave, was slower (176.1 us).
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  // The chain kernel runs its set-up before it waits for the intra kernel's
+  // results (GDN 170.2 -> 166.9 us).  An explicit early trigger in the intra
+  // kernel, which lets the chain grid be scheduled during the intra kernel's
+  // last wave, was slower (176.1 us).
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(CHAIN_THREADS);
   cfg.dynamicSmemBytes = C_SMEM;
@@ -1652,11 +1665,14 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)COMB_SMEM);
   if (e != cudaSuccess) return e;
-  segment_combine_kernel<<<dim3(cp.V / COMB_COLS, cp.H, cp.N), COMB_THREADS, COMB_SMEM, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t ccfg = cfg;
+  ccfg.gridDim = dim3(cp.V / COMB_COLS, cp.H, cp.N);
+  ccfg.blockDim = dim3(COMB_THREADS);
+  ccfg.dynamicSmemBytes = COMB_SMEM;
+  if ((e = cudaLaunchKernelEx(&ccfg, segment_combine_kernel, p)) != cudaSuccess) return e;
   p.seg_phase = 2;
-  chain<<<dim3(cp.V / VTILE, cp.H, cp.N * (S - 1)), CHAIN_THREADS, C_SMEM, stream>>>(mkr, p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(cp.V / VTILE, cp.H, cp.N * (S - 1));
+  return cudaLaunchKernelEx(&cfg, chain, mkr, p);
 }
 
 }  // namespace gdn
