@@ -49,6 +49,8 @@ def test_tiny_fp32_workload():
     (1, 128, 128, 2, 2, torch.bfloat16, True),    # a single token
     (333, 128, 128, 4, 2, torch.bfloat16, True),  # several chunks + tail, GQA
     (130, 100, 72, 3, 3, torch.float32, True),    # K not a multiple of 32
+    (200, 128, 32, 2, 1, torch.bfloat16, True),   # tensor cores, one 32-column value tile
+    (150, 128, 96, 2, 2, torch.bfloat16, False),  # tensor cores, three value tiles
 ])
 def test_small_shapes(T, K, V, H, Hg, dtype, h0):
     inp = synth.prefill_inputs(100 + T, 2, T, H, Hg, K, V, dtype=dtype,

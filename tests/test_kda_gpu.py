@@ -38,6 +38,8 @@ def run_oracle(inp, heads=None, seqs=None):
     (64, 128, 64, 2, 2, torch.float32, False),
     (257, 128, 128, 2, 4, torch.bfloat16, True),
     (5, 48, 40, 1, 1, torch.float32, True),       # shorter than a sub-chunk
+    (200, 128, 32, 1, 2, torch.bfloat16, True),   # tensor cores, one 32-column value tile
+    (130, 128, 96, 2, 2, torch.bfloat16, False),  # tensor cores, three value tiles
 ])
 def test_small_shapes(T, K, V, H, HV, dtype, h0):
     inp = synth.prefill_inputs(200 + T, 1, T, HV, H, K, V, dtype=dtype,
