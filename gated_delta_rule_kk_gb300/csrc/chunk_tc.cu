@@ -431,13 +431,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
-  const int h = blockIdx.y;
+  // KDA: one head per CTA.  Scalar gate: one key head per CTA, whose R value
+  // heads share k, q and the S product; the CTA takes them in turn, loading
+  // k and q once and each head's v while the previous head finishes.
+  const int R = KDA ? 1 : p.H / p.Hk;
+  const int hk = KDA ? blockIdx.y / (p.H / p.Hk) : blockIdx.y;
+  int h = KDA ? blockIdx.y : blockIdx.y * R;
   ChunkPos cp;
   // packed sequences: launched as a programmatic dependent of the chunk-table
   // kernel, so the table is read once that kernel is done
   if (p.cu_seqlens) ptx::griddep_wait();
   if (!locate_chunk(p, blockIdx.x, cp)) return;
-  const int hk = h / (p.H / p.Hk);
   const int V = p.V;
   const int s0 = cp.bos + cp.c * BT;
   const int L = min(BT, cp.eos - s0);
@@ -447,14 +451,17 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   // Loads first: the gate inputs into registers (warp 3: g, warps 4-5: beta)
   // and the TMA of k, q, v, so their latency overlaps the set-up below.
   float ga0 = 0.f, ga1 = 0.f, gbe = 0.f;
-  if (!KDA && warp == 3) {
-    ga0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
-    ga1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
-  }
-  if (warp == 4 || warp == 5) {
-    const int i = tid - 128;
-    gbe = i < L ? p.beta[(size_t)(row0 + i) * p.H + h] : 0.f;
-  }
+  auto load_gates = [&](int hh) {
+    if (!KDA && warp == 3) {
+      ga0 = 2 * lane < L ? p.g[(size_t)(row0 + 2 * lane) * p.H + hh] : 0.f;
+      ga1 = 2 * lane + 1 < L ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + hh] : 0.f;
+    }
+    if (warp == 4 || warp == 5) {
+      const int i = tid - 128;
+      gbe = i < L ? p.beta[(size_t)(row0 + i) * p.H + hh] : 0.f;
+    }
+  };
+  load_gates(h);
   if (tid == 0) {
     ptx::mbar_init(&bars[0], 1);
     ptx::mbar_init(&bars[1], 1);
@@ -492,7 +499,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  uint32_t mma_phase = 0;
 
+#pragma unroll 1
+  for (int r = 0;; ++r) {
   // ---- gates: gamma (chunk-local inclusive cumsum), beta, scales
   if (warp == 4 || warp == 5) bet[tid - 128] = gbe;
   if (!KDA) {
@@ -540,7 +550,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
   __syncthreads();
 
-  const bool ok_tma = ptx::mbar_wait_bounded(&bars[0], 0);
+  const bool ok_tma = ptx::mbar_wait_bounded(&bars[0], (uint32_t)(r & 1));
   if (!__syncthreads_and(ok_tma)) {
     if (tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
     ptx::tc_fence_before();
@@ -664,7 +674,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 
   // ---- S = [k; q] k^T  (M = 128, N = 64, K = 128); KDA split range: three
   //      passes hi.hi + hi.lo + lo.hi of the gated operands
-  uint32_t mma_phase = 0;
   if (tid == 0) {
     ptx::tc_fence_after();
     const uint32_t id = ptx::idesc_bf16(128, 64, 0, 0);
@@ -837,11 +846,27 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   const bool ok2 = ptx::mbar_wait_bounded(&bars[1], mma_phase);
   mma_phase ^= 1;
   ptx::tc_fence_after();
+  if (r + 1 < R) {
+    // the next value head: its v into VS (the WY GEMM is done with it) and its
+    // gate inputs into registers, landing while this head finishes
+    if (tid == 0) {
+      ptx::mbar_arrive_expect_tx(&bars[0], (uint32_t)V * 128);
+#pragma unroll 1
+      for (int j = 0; j < V / 32; ++j)
+        ptx::tma_load_3d(VS + j * 4096, &tm_v, 32 * j, h + 1, row0, &bars[0]);
+    }
+    load_gates(h + 1);
+  }
+  const bool last = r + 1 == R;
+  // -w replaces k in KQ, which is then the chain's A operand [-w ; q]; while
+  // another value head follows, k stays and -w goes to the AQ region (the WY
+  // GEMM is done with it) with the key halves 8 KB apart
+  unsigned char *wimg = last ? KQ : AQ;
+  const uint32_t whalf = last ? 16384u : 8192u;
   {
     // M = 128 layout: row r lives in TMEM lane r.  Lane quarters 0-1 hold the
     // w rows (keys split between the two warps of a quarter), quarters 2-3
-    // the u rows (value tiles split likewise).  -w replaces k in rows 0..63
-    // of KQ (the WY GEMM has finished with it).
+    // the u rows (value tiles split likewise).
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     if (qd < 2) {
       const int i = qd * 32 + lane;
@@ -854,7 +879,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
           float out[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) out[e] = -v[q8 * 8 + e];
-          *reinterpret_cast<uint4 *>(KQ + swz_off(i, q4 * 4 + q8, 16384)) = pack8(out);
+          *reinterpret_cast<uint4 *>(wimg + swz_off(i, q4 * 4 + q8, whalf)) = pack8(out);
         }
       }
     } else {
@@ -875,20 +900,36 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       }
     }
   }
-  // KQ is now the chain's A operand [-w ; q] (swz_off layout).  The tensor memory is
-  // no longer read: free it before waiting on the store, so that the next
-  // CTA on this SM can allocate it while this one drains.
+  // The chain's A operand [-w ; q] leaves with the u tile (while another head
+  // follows, as four 8 KB pieces: -w from AQ, q from KQ).  After the last
+  // head the tensor memory is no longer read: free it before waiting on the
+  // store, so that the next CTA on this SM can allocate it while this one
+  // drains.
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc<256>(tmem);
+  if (last && warp == 0) ptx::tmem_dealloc<256>(tmem);
   if (tid == 0) {
-    ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
+    if (last) {
+      ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
+    } else {
+      ptx::bulk_s2g(blk + OFF_AW, AQ, 8192);
+      ptx::bulk_s2g(blk + OFF_AW + 8192, KQ + 8192, 8192);
+      ptx::bulk_s2g(blk + OFF_AW + 16384, AQ + 8192, 8192);
+      ptx::bulk_s2g(blk + OFF_AW + 24576, KQ + 24576, 8192);
+    }
     ptx::bulk_s2g(blk + OFF_U, smem + I_R1, (uint32_t)V * 256);
     ptx::bulk_commit();
     ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   }
   if (!(ok1 && ok2 && ok_v) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
+  if (last) break;
+  // next value head: the stores above have read AQ, R1 and the scales
+  ++h;
+  blk = p.blocks + ((size_t)blockIdx.x * p.H + h) * p.block;
+  if (tid == 0) flags[0] = 1;
+  __syncthreads();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1627,7 +1668,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t icfg = {};
-  icfg.gridDim = dim3((unsigned)nchunks, cp.H);
+  icfg.gridDim = dim3((unsigned)nchunks, kda ? cp.H : cp.Hk);  // scalar gate: one key head a CTA
   icfg.blockDim = dim3(INTRA_THREADS);
   icfg.dynamicSmemBytes = ismem;
   icfg.stream = stream;
