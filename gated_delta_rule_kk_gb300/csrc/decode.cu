@@ -48,8 +48,14 @@ constexpr uint32_t SLOT_BYTES = DK * DV * 2;  // 32 KB bf16 state slot
 constexpr uint32_t ROW_BYTES = DK * 2;        // one bf16 q/k/v row
 constexpr uint32_t VEC_BYTES = DK * 4;        // one fp32 q/k vector slot
 constexpr int ROWS_PER_THREAD = 4;
-constexpr int NSTAGE = 3;
-constexpr int PREP_AHEAD = 2;  // the first warp out of item i prepares item i + 2
+// Stages per CTA: three (prepared two items ahead) for T = 2; two (prepared
+// one ahead) for T = 1, whose item is shortest (88.1 against 92.2 us at
+// B = 256, HV = 32; two stages made T = 2 slower, 100.4 against 94.2 us).
+template <int T>
+struct Ring {
+  static constexpr int NSTAGE = T == 1 ? 2 : 3;
+  static constexpr int PREP_AHEAD = NSTAGE - 1;  // the first warp out of item i prepares i + this
+};
 
 // Stage header (32-bit words): slot index, G_{T-1}, beta_t G_t, beta_t, G_t,
 // R_{T-1,t}, beta_t R_ts (k^_s.k^_t) [t][s], R_ts (k^_s.q^_t) [t][s].
@@ -67,6 +73,7 @@ struct DecodeSmem {
   static constexpr uint32_t STAGE_BYTES = HDR + 256;
   static constexpr uint32_t TX = SLOT_BYTES + 3 * T * ROW_BYTES;
   // after the stages: full and prepared barriers, then the per-stage done counters
+  static constexpr int NSTAGE = Ring<T>::NSTAGE;
   static constexpr size_t BYTES = (size_t)NSTAGE * STAGE_BYTES + NSTAGE * 16 + NSTAGE * 4;
 };
 
@@ -304,6 +311,7 @@ __device__ __noinline__ void prepare(const DecodeParams &p, unsigned char *st, u
 template <int T, bool F32>
 __global__ void __launch_bounds__(DTHREADS, 2) decode_kernel(DecodeParams p) {
   using L = DecodeSmem<T>;
+  constexpr int NSTAGE = L::NSTAGE, PREP_AHEAD = Ring<T>::PREP_AHEAD;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NSTAGE * L::STAGE_BYTES);
   uint64_t *prep = full + NSTAGE;
