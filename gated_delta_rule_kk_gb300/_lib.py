@@ -12,7 +12,10 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "lib", "libgdn_gb300.so")
+# GDN_CHECKED=1 selects the checked build (bounds checks in every kernel; see
+# build_lib), which must have been built first.
+CHECKED = os.environ.get("GDN_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(HERE, "lib", "libgdn_gb300_checked.so" if CHECKED else "libgdn_gb300.so")
 
 c_int32, c_float, c_void_p, c_size_t = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
@@ -27,6 +30,7 @@ class Status(enum.IntEnum):
     TIMEOUT = 6
     BAD_SEQLENS = 7
     BAD_SLOT = 8
+    BOUNDS = 9
 
 
 class DType(enum.IntEnum):
@@ -134,6 +138,7 @@ SIGNATURES = {
     "gdn_chunk_fwd_noalloc": ([ctypes.POINTER(GdnChunkArgs), c_void_p], c_int32),
     "gdn_noalloc_scratch_bytes": ([], c_size_t),
     "gdn_self_test_wait": ([c_int32, c_int32, c_void_p], c_int32),
+    "gdn_self_test_bounds": ([c_int32, c_int32, ctypes.POINTER(c_int32), c_void_p], c_int32),
     "gdn_check_device_error": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),
     "gdn_status_string": ([c_int32], ctypes.c_char_p),
     "gdn_last_error_message": ([], ctypes.c_char_p),
@@ -159,9 +164,9 @@ def load(path: str | None = None):
             return _lib
         p = path or LIB_PATH
         if not os.path.exists(p):
-            raise RuntimeError(
-                f"CUDA library {p} is missing: build it with "
-                "`python -c 'import __graft_entry__ as g; g.build()'`")
+            how = ("`python -m gated_delta_rule_kk_gb300.build_lib --checked`" if p.endswith("_checked.so")
+                   else "`python -c 'import __graft_entry__ as g; g.build()'`")
+            raise RuntimeError(f"CUDA library {p} is missing: build it with {how}")
         lib = ctypes.CDLL(p)
         for name, (argtypes, restype) in SIGNATURES.items():
             fn = getattr(lib, name)

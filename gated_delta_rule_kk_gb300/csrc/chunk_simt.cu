@@ -67,6 +67,10 @@ __global__ void __launch_bounds__(THREADS, 1) chunk_fwd_simt_kernel(ChunkParams 
     bos = 0;
     eos = p.T;
   }
+  if (!bounds_ok(n < p.N && b >= 0 && b < p.B && h < H && hk < Hk && v0 < V && bos >= 0 &&
+                     bos <= eos && eos <= p.T,
+                 p.err))
+    return;
 
   const T *q = static_cast<const T *>(p.q);
   const T *k = static_cast<const T *>(p.k);

@@ -169,6 +169,7 @@ struct TcParams {
   int o_f32;               // o written as fp32 instead of bf16
   float scale;
   uint32_t block;          // bytes per (chunk, head) block
+  int nblk;                // chunk slots in `blocks` (blocks holds nblk * H blocks)
   // segment-parallel state pass (seg_count >= 2; see chain_kernel)
   int seg_count;           // segments per sequence
   int seg_phase;           // 0: whole sequences; 1: every segment from zero / identity;
@@ -446,6 +447,10 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   const int s0 = cp.bos + cp.c * BT;
   const int L = min(BT, cp.eos - s0);
   const int row0 = cp.b * p.T + s0;  // token row in the [B*T] flattening
+  if (!bounds_ok((int)blockIdx.x < p.nblk && h >= 0 && h + R <= p.H && hk < p.Hk && cp.b >= 0 &&
+                     cp.b < p.B && s0 >= 0 && s0 < cp.eos && cp.eos <= p.T,
+                 p.err))
+    return;
   unsigned char *blk = p.blocks + ((size_t)blockIdx.x * p.H + h) * p.block;
 
   // Loads first: the gate inputs into registers (warp 3: g, warps 4-5: beta)
@@ -1089,6 +1094,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
     nch = min(per, nch - cfirst);
   }
   const bool write_o = p.seg_phase != 1 || seg == 0;
+  if (!bounds_ok(n >= 0 && n < p.N && b >= 0 && b < p.B && bos >= 0 && bos <= eos && eos <= p.T &&
+                     base >= 0 && base + cfirst + nch <= p.nblk && h < p.H &&
+                     v0 + VTILE <= (trans ? KD : p.V) && (p.seg_phase == 0 || seg < p.seg_count),
+                 p.err))
+    return;
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -1416,6 +1426,7 @@ __global__ void __launch_bounds__(COMB_THREADS) segment_combine_kernel(TcParams 
   float *X = csm + 2 * KD * COMB_LDM;  // the running state's tile, [KD][COMB_COLS]
   const int h = blockIdx.y, n = blockIdx.z;
   const int S = p.seg_count, W = KD + p.V, tid = threadIdx.x;
+  if (!bounds_ok(n < p.N && h < p.H && (int)(blockIdx.x + 1) * COMB_COLS <= p.V, p.err)) return;
   const int r = tid >> 1, cq = (tid & 1) * 4, col = blockIdx.x * COMB_COLS + cq;
   auto state = [&](int sg) {
     return p.seg_state + (((size_t)n * S + sg) * p.H + h) * KD * W;
@@ -1639,6 +1650,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, bool kda, void *ws, cudaStrea
   p.v_first = cp.v_first;
   p.scale = cp.scale;
   p.block = block_bytes(cp.V, kda);
+  p.nblk = (int)max_chunks(cp.B, cp.T, cp.N, varlen);
   const int S = segment_count(cp, varlen);
   p.seg_count = S;
   p.seg_phase = 0;

@@ -168,7 +168,11 @@ __device__ __forceinline__ void issue(const DecodeParams &p, unsigned char *st, 
   const int HV = p.HV;
   const int bi = item / HV, hv = item % HV, hk = hv / (HV / p.H);
   int *hdr = reinterpret_cast<int *>(st + L::HDR);
-  if (slot < 0 || slot >= p.pool) {
+  // checked builds: an item whose batch entry or key head falls outside its
+  // tensor is skipped like a bad slot
+  const bool in_range = !kChecked || (bi < p.B && hk < p.H);
+  if (!in_range) record_error(p.err, GDN_ERR_BOUNDS);
+  if (!in_range || slot < 0 || slot >= p.pool) {
     hdr[H_SLOT] = -1;
     ptx::mbar_arrive(full);
     return;

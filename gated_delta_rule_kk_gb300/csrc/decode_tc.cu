@@ -94,11 +94,18 @@ __device__ __forceinline__ int slot_of(const DecodeParams &p, int item) {
   return p.slot_indices ? p.slot_indices[bi] : bi;
 }
 
+// Checked builds: whether an item's batch entry and key head fall inside their
+// tensors (both issuers skip an item that does not, like a bad slot).
+__device__ __forceinline__ bool item_in_range(const DecodeParams &p, int item) {
+  const int bi = item / p.HV, hk = (item % p.HV) / (p.HV / p.H);
+  return !kChecked || (bi < p.B && hk < p.H);
+}
+
 // Fill a state-slot stage (one thread); an out-of-range slot completes the
 // barrier with no copies.
 __device__ __forceinline__ void issue_sw(const DecodeParams &p, const CUtensorMap *tm_ld,
                                          unsigned char *sw, uint64_t *full, int item, int slot) {
-  if (slot < 0 || slot >= p.pool) {
+  if (!item_in_range(p, item) || slot < 0 || slot >= p.pool) {
     ptx::mbar_arrive(full);
     return;
   }
@@ -116,7 +123,9 @@ __device__ __forceinline__ void issue_aux(const DecodeParams &p, unsigned char *
   const int HV = p.HV;
   const int bi = item / HV, hv = item % HV, hk = hv / (HV / p.H);
   int *hdr = reinterpret_cast<int *>(aux + A_HDR);
-  if (slot < 0 || slot >= p.pool) {
+  const bool in_range = item_in_range(p, item);
+  if (!in_range) record_error(p.err, GDN_ERR_BOUNDS);
+  if (!in_range || slot < 0 || slot >= p.pool) {
     hdr[H_SLOT] = -1;
     ptx::mbar_arrive(full);
     return;

@@ -185,6 +185,7 @@ const char *gdn_status_string(gdn_status_t s) {
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
     case GDN_ERR_BAD_SEQLENS: return "GDN_ERR_BAD_SEQLENS";
     case GDN_ERR_BAD_SLOT: return "GDN_ERR_BAD_SLOT";
+    case GDN_ERR_BOUNDS: return "GDN_ERR_BOUNDS";
   }
   return "GDN_ERR_UNKNOWN";
 }

@@ -32,6 +32,24 @@ __device__ __forceinline__ void record_error(int *err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Checked builds (-DGDN_CHECKED): before a CTA touches memory it compares the
+// index ranges it derived with the extents of the tensors they index; on a
+// violation it records GDN_ERR_BOUNDS and returns, uniformly over the CTA and
+// before any barrier.  `cond` must be uniform over the CTA.  Release builds
+// compile the check away.
+#ifdef GDN_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ bool bounds_ok(bool cond, int *err) {
+  if (kChecked && !cond) {
+    if (threadIdx.x == 0) record_error(err, GDN_ERR_BOUNDS);
+    return false;
+  }
+  return true;
+}
+
 // Host: device address of the error word of the current device.
 int *device_error_word();
 

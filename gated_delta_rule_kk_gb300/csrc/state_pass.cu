@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(SP_THREADS, 1) state_pass_kernel(StateParams p
   const bool gk = p.gate == GDN_GATE_GK, gvg = p.gate == GDN_GATE_GV;
   const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
   const SeqInfo sq = sequence_of(p, n, tid, seq_info);
+  if (!bounds_ok(n < p.N && h < p.H && v0 < p.V && sq.bos >= 0 && sq.bos <= sq.eos && sq.eos <= p.T,
+                 p.err))
+    return;
 
   float hv[16];
   // element (key r, column col) of a [K, V] state (or [V, K] with v_first)
@@ -539,6 +542,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) state_pass_tc_kernel(StateParam
   // g_gamma: the block's per-head rate (gamma_i = rate (i + 1))
   const float gamma = p.gate == GDN_GATE_G_GAMMA ? p.gate_values[h / (H / p.HG)] : 0.f;
   const SeqInfo sq = sequence_of(p, n, tid, seq_info);
+  if (!bounds_ok(n < p.N && h < p.H && v0 < p.V && sq.bos >= 0 && sq.bos <= sq.eos && sq.eos <= p.T,
+                 p.err))
+    return;
   unsigned char *ring = tc_smem + 2 * BUF;
   const uint32_t slot_bytes = ring_slot_bytes(p.gate);
   auto slot_of = [&](int it) { return ring + (uint32_t)(it % RING) * slot_bytes; };

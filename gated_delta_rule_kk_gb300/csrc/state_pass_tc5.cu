@@ -232,6 +232,10 @@ state_pass_tc5_kernel(const __grid_constant__ CUtensorMap tm_k,
   const bool scalar_gate = p.gate == GDN_GATE_G || p.gate == GDN_GATE_G_GAMMA;
   const float gamma = p.gate == GDN_GATE_G_GAMMA ? p.gate_values[hg] : 0.f;
   const T5Seq sq = t5_sequence(p, n, tid, seq_sh);
+  if (!bounds_ok(n < p.N && h < H && hg < HG && v0 + T5_VT <= V && sq.bos >= 0 &&
+                     sq.bos <= sq.eos && sq.eos <= p.T,
+                 p.err))
+    return;
   auto chunk_at = [&](int it) { return p.reverse ? sq.nch - 1 - it : it; };
 
   if (tid == 0) {

@@ -54,7 +54,10 @@ typedef enum gdn_status {
   GDN_ERR_CUDA = 5,         /* a CUDA runtime call failed                  */
   GDN_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up              */
   GDN_ERR_BAD_SEQLENS = 7,  /* device: cu_seqlens not rising from 0 to T   */
-  GDN_ERR_BAD_SLOT = 8      /* device: a slot index outside [0, pool)      */
+  GDN_ERR_BAD_SLOT = 8,     /* device: a slot index outside [0, pool)      */
+  GDN_ERR_BOUNDS = 9        /* device, checked builds only: an index range a
+                               kernel derived falls outside its tensor; the
+                               CTA skips its work                          */
 } gdn_status_t;
 
 typedef enum gdn_dtype {
@@ -410,6 +413,22 @@ size_t gdn_noalloc_scratch_bytes(void);
  * arguments outside those ranges.
  */
 gdn_status_t gdn_self_test_wait(int32_t arrive, int32_t max_polls, gdn_stream_t stream);
+
+/*
+ * Self-test of the bounds checks of a checked build (the library compiled
+ * with -DGDN_CHECKED; the release build compiles them away).  Before a CTA of
+ * any kernel touches memory, a checked build compares the index ranges the
+ * CTA derived (chunk slots, token rows, heads, value columns, state slots)
+ * with the extents of the tensors they index; when one falls outside, the CTA
+ * records GDN_ERR_BOUNDS in the device error word and returns, uniformly and
+ * before any barrier, so that nothing waits on it.  This call runs that check
+ * in a one-CTA kernel on the index `index` against the extent `extent`: a
+ * checked build records GDN_ERR_BOUNDS unless 0 <= index < extent, a release
+ * build never does.  Read the outcome with gdn_check_device_error();
+ * *checked_build is set to 1 in a checked build, else 0 (it may be NULL).
+ */
+gdn_status_t gdn_self_test_bounds(int32_t index, int32_t extent, int32_t *checked_build,
+                                  gdn_stream_t stream);
 
 /* Wait for `stream`, then read and clear the device error word of the current
  * device into *code (a gdn_status_t value, GDN_OK if nothing was recorded).
