@@ -5,7 +5,9 @@
 // Two kernels per call (plus a small chunk-table kernel for packed
 // sequences):
 //
-// 1. intra: one CTA per (chunk, value head), all chunks in parallel.  With
+// 1. intra: one CTA per (chunk, value head) -- for the scalar gate per (chunk,
+//    key head), taking the key head's value heads in turn -- all chunks in
+//    parallel.  With
 //    gamma the chunk-local cumulative gate and S = [k; q] k^T (one M = 128
 //    tcgen05 GEMM; sglang fla/chunk_fwd.py, fused KK^T + solve kernel):
 //      A   = beta_i S_kk[i,j] exp(gamma_i - gamma_j), i > j       (Steps 1-2)
@@ -50,12 +52,15 @@
 //    (KDA _fla/ops/common/chunk_h.py, chunk_fwd_kernel_h, is the gated state
 //    recurrence that this delta form extends; the output is fused into it.)
 //
-// Shared-memory operand images use the canonical no-swizzle layout: element
+// Shared-memory operand images are rows of 128 bytes in the 128-byte swizzle
+// (the layout TMA writes): the 16-byte piece j of row r sits at piece
+// j ^ (r & 7) of the row, and wider images keep their 64-column halves a
+// fixed stride apart (swz_off, swz_row, sw128_kmajor below); v arrives in the
+// 64-byte swizzle.  Only KT keeps the canonical no-swizzle layout: element
 // (r, c) of an image with column-group stride `cs` sits at
-// (c / 8) * cs + r * 16 + (c % 8) * 2 bytes, i.e. every group of 8 columns is
-// a contiguous run of 16-byte rows.  Read with rows as M/N (K-major) its
-// descriptor has LBO = cs, SBO = 128; read with rows as K (MN-major) it has
-// LBO = 128, SBO = cs.
+// (c / 8) * cs + r * 16 + (c % 8) * 2 bytes, every group of 8 columns a
+// contiguous run of 16-byte rows; read with rows as K (MN-major) its
+// descriptor has LBO = 128, SBO = cs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
