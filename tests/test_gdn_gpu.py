@@ -51,6 +51,7 @@ def test_tiny_fp32_workload():
     (130, 100, 72, 3, 3, torch.float32, True),    # K not a multiple of 32
     (200, 128, 32, 2, 1, torch.bfloat16, True),   # tensor cores, one 32-column value tile
     (150, 128, 96, 2, 2, torch.bfloat16, False),  # tensor cores, three value tiles
+    (200, 128, 128, 8, 1, torch.bfloat16, True),  # tensor cores, 8 value heads on 1 key head
 ])
 def test_small_shapes(T, K, V, H, Hg, dtype, h0):
     inp = synth.prefill_inputs(100 + T, 2, T, H, Hg, K, V, dtype=dtype,
