@@ -968,15 +968,17 @@ constexpr uint32_t S_AW = 0, S_KT = 32768, S_AQ = 65536, S_SC = 81920, S_U = 829
 constexpr uint32_t C_H = 2 * STAGE_BYTES, C_VN = C_H + 16384, C_VN2 = C_VN + 8192,
                    C_X = C_VN2 + 8192, C_BAR = C_X + 64 * 33 * 4,
                    C_SMEM = C_BAR + 256 + 1024;  // + up to 1 KB to align the base
-constexpr int CHAIN_THREADS = 320;
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;               // four per TMEM lane quarter
+constexpr int EC = 32 / (EPI_WARPS / 4);    // state columns per epilogue thread (8)
+constexpr int CHAIN_THREADS = 32 * (EPI_WARPS + 2);
 // Named barriers of the chain kernel (1 is the epilogue warps' own).  The
 // epilogue warps arrive (without waiting) once h, or v_new, is in shared
 // memory; the MMA warp waits on them.  Each phase's arrivals depend on MMAs
 // the MMA warp issues only after it passed the previous phase, so phases
 // never overlap; every role runs every chunk, so every phase completes.
 constexpr int BAR_HREADY = 2, BAR_HREADY_THREADS = 32 * (EPI_WARPS + 1);
-constexpr int BAR_VNREADY = 3, BAR_VNREADY_THREADS = 32 * (4 + 1);  // warps 0, 1, 4, 5 + MMA
+// v_new comes from the epilogue warps of lane quarters 0-1 (rows 0..63), half of them
+constexpr int BAR_VNREADY = 3, BAR_VNREADY_THREADS = 32 * (EPI_WARPS / 2 + 1);
 constexpr int BAR_VN2READY = 4;  // (scalar gate) v_new for the output GEMM, same threads
 
 __device__ __forceinline__ void bar_sync(int id, int threads) {
@@ -991,28 +993,41 @@ __device__ __forceinline__ uint64_t adv(uint64_t desc, uint32_t bytes) {
   return desc + (uint64_t)(bytes >> 4);
 }
 
-// columns [c0, c0 + 16) of a 64-column accumulator holding the hi product in
-// columns 0..31 and the lo product in 32..63, summed
-__device__ __forceinline__ void tmem_ld_pair16(uint32_t taddr, int c0, float *v) {
-  float lo[16];
-  ptx::tmem_ld16(taddr + c0, v);
-  ptx::tmem_ld16(taddr + 32 + c0, lo);
+// columns [c0, c0 + 8) of a 64-column accumulator holding the hi product in
+// columns 0..31 and the lo product in 32..63, summed; both loads are in flight
+// before the one wait, which takes the registers so that nothing reads them
+// earlier
+__device__ __forceinline__ void tmem_ld_pair8(uint32_t taddr, int c0, float *v) {
+  uint32_t h[8], l[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]), "=r"(h[4]), "=r"(h[5]),
+                 "=r"(h[6]), "=r"(h[7])
+               : "r"(taddr + c0)
+               : "memory");
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(l[0]), "=r"(l[1]), "=r"(l[2]), "=r"(l[3]), "=r"(l[4]), "=r"(l[5]),
+                 "=r"(l[6]), "=r"(l[7])
+               : "r"(taddr + 32 + c0)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(h[0]), "+r"(h[1]), "+r"(h[2]), "+r"(h[3]), "+r"(h[4]), "+r"(h[5]),
+                 "+r"(h[6]), "+r"(h[7]), "+r"(l[0]), "+r"(l[1]), "+r"(l[2]), "+r"(l[3]),
+                 "+r"(l[4]), "+r"(l[5]), "+r"(l[6]), "+r"(l[7])
+               :
+               : "memory");
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] += lo[j];
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(h[j]) + __uint_as_float(l[j]);
 }
 
-// 16 values -> hi/lo bf16 halves of row r of a 64-column image with 128-byte
-// rows in the 128-byte swizzle (hi in columns c0.., lo in columns 32 + c0..;
-// 16-byte piece j of row r at piece j ^ (r & 7))
-__device__ __forceinline__ void store_pair16(unsigned char *img, int r, int c0, const float *v) {
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    uint4 hi, lo;
-    split8(v + 8 * g, hi, lo);
-    const int jh = (c0 >> 3) + g, jl = 4 + (c0 >> 3) + g;
-    *reinterpret_cast<uint4 *>(img + r * 128 + ((jh ^ (r & 7)) << 4)) = hi;
-    *reinterpret_cast<uint4 *>(img + r * 128 + ((jl ^ (r & 7)) << 4)) = lo;
-  }
+// 8 values -> hi/lo bf16 halves of row r of a 64-column image with 128-byte
+// rows in the 128-byte swizzle (hi in columns c0 .. c0 + 7, lo in columns
+// 32 + c0 ..; 16-byte piece j of row r at piece j ^ (r & 7))
+__device__ __forceinline__ void store_pair8(unsigned char *img, int r, int c0, const float *v) {
+  uint4 hi, lo;
+  split8(v, hi, lo);
+  const int jh = c0 >> 3, jl = 4 + (c0 >> 3);
+  *reinterpret_cast<uint4 *>(img + r * 128 + ((jh ^ (r & 7)) << 4)) = hi;
+  *reinterpret_cast<uint4 *>(img + r * 128 + ((jl ^ (r & 7)) << 4)) = lo;
 }
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int c0, int c1, int c2,
@@ -1239,46 +1254,46 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       *abort_flag = 1;
     }
   } else {
-    // ---------------- epilogue warps 0-7: row r = TMEM lane, columns c0..c0+15
+    // ---------------- epilogue warps: row r = TMEM lane, columns c0 .. c0 + EC - 1
     const int qd = warp & 3;
-    const int c0 = (warp >> 2) * 16;
+    const int c0 = (warp >> 2) * EC;
     const int r = qd * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    float hs[16];
+    float hs[EC];
     const bool from_h0 = p.seg_phase == 0 || (p.seg_phase == 1 && seg == 0);
     if (trans) {
       // columns v0 + c0 .. of the identity (key index = column)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) hs[j] = (r == v0 + c0 + j) ? 1.f : 0.f;
+      for (int j = 0; j < EC; ++j) hs[j] = (r == v0 + c0 + j) ? 1.f : 0.f;
     } else if (p.seg_phase == 2) {
       const float4 *src = reinterpret_cast<const float4 *>(
           p.seg_start + ((((size_t)n * p.seg_count + seg) * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < EC / 4; ++q) {
         const float4 x = src[q];
         hs[4 * q] = x.x; hs[4 * q + 1] = x.y; hs[4 * q + 2] = x.z; hs[4 * q + 3] = x.w;
       }
     } else if (!from_h0) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) hs[j] = 0.f;
+      for (int j = 0; j < EC; ++j) hs[j] = 0.f;
     } else if (p.h0 && p.v_first) {
       // [V, K]: the lanes of a warp read 32 consecutive keys of one value row
       const float *src = p.h0 + ((size_t)n * p.H + h) * KD * p.V + (size_t)(v0 + c0) * KD + r;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) hs[j] = src[(size_t)j * KD];
+      for (int j = 0; j < EC; ++j) hs[j] = src[(size_t)j * KD];
     } else if (p.h0) {
       const float4 *src = reinterpret_cast<const float4 *>(
           p.h0 + (((size_t)n * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < EC / 4; ++q) {
         const float4 x = src[q];
         hs[4 * q] = x.x; hs[4 * q + 1] = x.y; hs[4 * q + 2] = x.z; hs[4 * q + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) hs[j] = 0.f;
+      for (int j = 0; j < EC; ++j) hs[j] = 0.f;
     }
-    store_pair16(Himg, r, c0, hs);
+    store_pair8(Himg, r, c0, hs);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     bar_arrive(BAR_HREADY, BAR_HREADY_THREADS);
@@ -1295,15 +1310,15 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       const float qs = r >= 64 ? scs[192 + r - 64] : 0.f;
       ok = ptx::mbar_wait_bounded(d1, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
-      float qh[16];
+      float qh[EC];
       {
-        float d[16];
-        tmem_ld_pair16(dD1 + lane_base, c0, d);
+        float d[EC];
+        tmem_ld_pair8(dD1 + lane_base, c0, d);
         if (r < 64) {
           const float4 *u4 = reinterpret_cast<const float4 *>(st + S_U + r * 128);
-          float vn[16];
+          float vn[EC];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < EC / 4; ++q) {
             const float4 u = trans ? make_float4(0.f, 0.f, 0.f, 0.f)
                                    : u4[((c0 >> 2) + q) ^ (r & 7)];  // row-swizzled groups
             vn[4 * q] = u.x + d[4 * q];
@@ -1315,26 +1330,26 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
             // the state update's operand: e^{gamma_L - gamma_r} v_new (zero
             // on padding rows), then v_new itself for the output GEMM
             const float f = scs[128 + r];
-            float vt[16];
+            float vt[EC];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) vt[j] = f * vn[j];
-            store_pair16(VN, r, c0, vt);
+            for (int j = 0; j < EC; ++j) vt[j] = f * vn[j];
+            store_pair8(VN, r, c0, vt);
           } else {
-            store_pair16(VN, r, c0, vn);
+            store_pair8(VN, r, c0, vn);
           }
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
           __syncwarp();
           bar_arrive(BAR_VNREADY, BAR_VNREADY_THREADS);
           if (RAWK) {
-            store_pair16(VN2, r, c0, vn);
+            store_pair8(VN2, r, c0, vn);
             ptx::fence_proxy_async_smem();
             __syncwarp();
             bar_arrive(BAR_VN2READY, BAR_VNREADY_THREADS);
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) qh[j] = d[j];
+          for (int j = 0; j < EC; ++j) qh[j] = d[j];
         }
       }
       __syncwarp();
@@ -1342,11 +1357,11 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       ok = ptx::mbar_wait_bounded(d3, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
       {
-        float d[16];
-        tmem_ld_pair16(dDH + lane_base, c0, d);
+        float d[EC];
+        tmem_ld_pair8(dDH + lane_base, c0, d);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
-        store_pair16(Himg, r, c0, hs);
+        for (int j = 0; j < EC; ++j) hs[j] = fmaf(decay, hs[j], d[j]);
+        store_pair8(Himg, r, c0, hs);
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
@@ -1354,35 +1369,35 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       }
       ok = ptx::mbar_wait_bounded(d5, (uint32_t)(c & 1)) && ok;
       ptx::tc_fence_after();
-      float d5v[16];
-      tmem_ld_pair16(dD5 + lane_base, c0, d5v);
+      float d5v[EC];
+      tmem_ld_pair8(dD5 + lane_base, c0, d5v);
       ptx::tc_fence_before();
       if (r < 64) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) X[r * 33 + c0 + j] = d5v[j];
+        for (int j = 0; j < EC; ++j) X[r * 33 + c0 + j] = d5v[j];
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
       if (r >= 64 && write_o) {
         const int i = r - 64;
         if (i < L) {
-          float ov[16];
+          float ov[EC];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ov[j] = fmaf(qs, qh[j], d5v[j] + X[i * 33 + c0 + j]);
+          for (int j = 0; j < EC; ++j) ov[j] = fmaf(qs, qh[j], d5v[j] + X[i * 33 + c0 + j]);
           const size_t oi =
               ((size_t)(b * p.T + bos + (cfirst + c) * BT + i) * p.H + h) * p.V + v0 + c0;
           if (p.o_f32) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + oi);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < EC / 4; ++q)
               dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
           } else {
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + oi);
-            dst[0] = pack8(ov);
-            dst[1] = pack8(ov + 8);
+#pragma unroll
+            for (int q = 0; q < EC / 8; ++q) dst[q] = pack8(ov + 8 * q);
           }
         }
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
     }
     if (!ok) {
       if (lane == 0) record_error(p.err, GDN_ERR_TIMEOUT);
@@ -1393,18 +1408,18 @@ chain_kernel(const __grid_constant__ CUtensorMap tm_k, TcParams p) {
       float4 *dst = reinterpret_cast<float4 *>(
           p.seg_state + ((((size_t)n * p.seg_count + seg) * p.H + h) * KD + r) * W + col);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < EC / 4; ++q)
         dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
     } else if (p.seg_phase == 2 && seg != p.seg_count - 1) {
       // an inner segment's end is the next one's start: already formed
     } else if (p.ht && *abort_flag == 0 && p.v_first) {
       float *dst = p.ht + ((size_t)n * p.H + h) * KD * p.V + (size_t)(v0 + c0) * KD + r;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) dst[(size_t)j * KD] = hs[j];
+      for (int j = 0; j < EC; ++j) dst[(size_t)j * KD] = hs[j];
     } else if (p.ht && *abort_flag == 0) {
       float4 *dst = reinterpret_cast<float4 *>(p.ht + (((size_t)n * p.H + h) * KD + r) * p.V + v0 + c0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < EC / 4; ++q)
         dst[q] = make_float4(hs[4 * q], hs[4 * q + 1], hs[4 * q + 2], hs[4 * q + 3]);
     }
   }
