@@ -31,12 +31,12 @@
 //    k e^{gamma_L - g}.
 //
 // 2. chain: one CTA per (32-wide V tile, value head, sequence), the
-//    sequential inter-chunk pass, warp-specialised: warp 8 streams the
-//    chunk's operand block in (five bulk copies), warp 9 issues the tcgen05
-//    GEMMs, warps 0-7 run the epilogues (warps w and w + 4 share TMEM lane
-//    quarter w % 4 and split its 32 columns; each thread keeps 16 columns of
-//    one key row of the fp32 state tile h[128, 32] in registers for the
-//    whole sequence).  Per chunk
+//    sequential inter-chunk pass, warp-specialised: warp 16 streams the
+//    chunk's operand block in (five bulk copies), warp 17 issues the tcgen05
+//    GEMMs, warps 0-15 run the epilogues (warps w, w + 4, w + 8, w + 12 share
+//    TMEM lane quarter w % 4 and split its 32 columns; each thread keeps 8
+//    columns of one key row of the fp32 state tile h[128, 32] in registers for
+//    the whole sequence).  Per chunk
 //      D1  = [-w ; q~] [h_hi | h_lo]      rows 0..63: -w h, rows 64..127: q h
 //      v_new = u + D1[0..63]             (fp32; split into a hi + lo bf16 pair)
 //      DH  = k~^T v_new                  (scalar gate: k^T (e^{gamma_L - gamma} v_new),
@@ -943,7 +943,7 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
 }
 
 // ---------------------------------------------------------------------------
-// chain kernel (320 threads: warps 0-7 epilogue, warp 8 producer, warp 9 MMA)
+// chain kernel (576 threads: warps 0-15 epilogue, warp 16 producer, warp 17 MMA)
 //
 // shared memory: two stages holding one operand block each
 //   AW  [0, 32768)       [-w ; q~] (128 x 128, 128-byte swizzle, halves 16 KB apart)
