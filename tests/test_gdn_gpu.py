@@ -150,6 +150,33 @@ def test_varlen_gqa_workload_all_chains():
     assert_close(ht, ht_ref, TOL_BF16, "ht")
 
 
+# ---- more chains than SMs: the chain grid runs in several waves ----------
+
+@pytest.mark.parametrize("case", ["packed", "batch", "v64"])
+def test_chains_outnumbering_the_sms(case):
+    """(V / 32) H N chain CTAs above the SM count, so that CTAs start as
+    others finish: packed sequences with empty and one-token ones (taken
+    longest first), GQA and an initial state; an equal-length batch; and
+    V = 64 (two value tiles a head)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if case == "packed":
+        lengths = [150, 0, 1, 64, 65, 200, 3, 129, 90, 17, 256, 40]
+        H, Hg, V = 16, 4, 128
+        inp = synth.prefill_inputs(61, 1, sum(lengths), H, Hg, 128, V, dtype=torch.bfloat16,
+                                   lengths=lengths)
+        inp["h0"] = 0.1 * torch.randn(len(lengths), H, 128, V,
+                                      generator=torch.Generator().manual_seed(62))
+        N = len(lengths)
+    elif case == "batch":
+        N, H, Hg, V = 5, 16, 16, 128
+        inp = synth.prefill_inputs(63, N, 130, H, Hg, 128, V, dtype=torch.bfloat16, h0_std=0.1)
+    else:
+        N, H, Hg, V = 10, 16, 8, 64
+        inp = synth.prefill_inputs(64, N, 100, H, Hg, 128, V, dtype=torch.bfloat16, h0_std=0.1)
+    assert (V // 32) * H * N > sms
+    _check(inp)
+
+
 # ---- gates the synthetic workloads never reach, on the tensor-core path ----
 
 def _tc_problem(seed, T=256, H=2, Hg=1):
