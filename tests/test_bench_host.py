@@ -66,3 +66,39 @@ def test_reference_arm_runs_on_rank_zero_only():
                        timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_traffic_records_are_gated_on_the_kernel_source(tmp_path, monkeypatch):
+    """A DRAM-traffic record counts only while its kernel source is the one it
+    was captured on: the same file gives its bytes, any edit gives None."""
+    import hashlib
+    csrc = tmp_path / "gated_delta_rule_kk_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "k.cu").write_text("__global__ void k() {}\n")
+    sha = hashlib.sha256((csrc / "k.cu").read_bytes()).hexdigest()[:12]
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(
+        "# comment\n"
+        f"row_a source=k.cu sha={sha} bytes_per_launch=1.5e+08\n"
+        "row_b source=k.cu sha=000000000000 bytes_per_launch=2e+08\n"
+        f"row_c source=missing.cu sha={sha} bytes_per_launch=3e+08\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("row_a") == 1.5e8
+    assert bench.traffic_record("row_b") is None
+    assert bench.traffic_record("row_c") is None
+    assert bench.traffic_record("row_d") is None
+    (csrc / "k.cu").write_text("__global__ void k() { }\n")
+    assert bench.traffic_record("row_a") is None
+
+
+def test_committed_traffic_records_are_well_formed():
+    """Every record names an existing kernel source, a 12-digit hash and a
+    positive byte count."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for f in rows:
+        kv = dict(x.split("=", 1) for x in f[1:])
+        assert os.path.exists(os.path.join(ROOT, "gated_delta_rule_kk_gb300", "csrc", kv["source"]))
+        assert len(kv["sha"]) == 12 and int(kv["sha"], 16) >= 0
+        assert float(kv["bytes_per_launch"]) > 0
