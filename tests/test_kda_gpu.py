@@ -113,6 +113,30 @@ def _check(inp):
     assert_close(ht, ht_ref, TOL_BF16, "ht")
 
 
+@pytest.mark.parametrize("gate_input", ["cumsum", "raw"])
+def test_tensor_core_packed_sequences_many_chains(gate_input):
+    """bf16, K = V = 128 (the tensor-core path) on packed sequences with an
+    empty and a one-token one, 4 query/key heads for 16 value heads, an
+    initial state, and more chain CTAs than SMs; the gate given as chunk-local
+    cumsums (counted from each sequence start) or raw."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    lengths = [130, 0, 1, 64, 65, 200, 3, 90]
+    H, HV, N = 4, 16, len(lengths)
+    inp = synth.prefill_inputs(71, 1, sum(lengths), HV, H, 128, 128, dtype=torch.bfloat16,
+                               lengths=lengths, per_channel=True)
+    inp["h0"] = 0.1 * torch.randn(N, HV, 128, 128, generator=torch.Generator().manual_seed(72))
+    if gate_input == "raw":
+        r = torch.Generator().manual_seed(73)
+        inp = dict(inp, g=-torch.rand(inp["g"].shape, generator=r) * 0.05, g_is_cumsum=False)
+    assert 4 * HV * N > sms
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(o, o_ref, TOL_BF16, "o")
+    assert_close(ht, ht_ref, TOL_BF16, "ht")
+    # the empty sequence hands its initial state back unchanged
+    assert torch.equal(ht[1].cpu(), inp["h0"][1])
+
+
 def test_strong_channel_gates_take_the_exact_exponentials():
     """Channels 0..15 of head 0 fall below -80 inside chunk 1 (-2.5 per token):
     that chunk is gated with exact per-element exponentials."""
