@@ -4,8 +4,10 @@ Each case rewrites one line of an oracle function (a dropped term, a wrong
 sign, a swapped operand or index, the gate applied in the wrong place, a chunk
 reset counted from the wrong token), installs the mutant in place of the
 function for the duration of the case, and runs the pins of
-tests/test_oracle_pins.py: at least one of them must fail.  All on the CPU;
-the oracle itself is never edited.
+tests/test_oracle_pins.py (the token recurrences, decode) or
+tests/test_state_pass_pins.py (the chunk state pass, forward and backward): at
+least one of them must fail on an assertion.  All on the CPU; the oracle
+itself is never edited.
 """
 import inspect
 import textwrap
@@ -114,5 +116,76 @@ def test_planted_mistake_fails_a_pin(case, monkeypatch):
         try:
             pin(**kwargs)
         except AssertionError:  # a pin saw wrong values (a mutant that cannot run fails the case)
+            return
+    pytest.fail(f"no pin fails with the planted mistake: {case}")
+
+
+# ---- the chunk state pass (forward and backward) and its pins ----------------
+
+import test_state_pass_pins as SPP  # noqa: E402
+from oracle import state_pass as SP  # noqa: E402
+
+SP_PINS = (
+    [(SPP.test_final_state_matches_closed_form, {"gate": g}) for g in SP.GATES]
+    + [(SPP.test_gate_kinds_reduce_to_each_other, {}),
+       (SPP.test_chunk_starts_resume_the_run_and_packed_sequences_are_separate_runs, {})]
+    + [(SPP.test_state_gradient_is_the_adjoint_of_the_forward_pass, {"gate": g}) for g in SP.GATES]
+    + [(SPP.test_state_gradient_grouped_query_heads_share_the_gate, {}),
+       (SPP.test_split_size_keeps_every_split_chunk, {"split": 128}),
+       (SPP.test_state_v_first_transposes_every_state, {})])
+
+SP_MUTATIONS = {
+    "state: per-key gate averaged over the keys": (
+        "chunk_state_pass", "S = np.exp(raw[t, h])[:, None] * S", "S = np.exp(raw[t, h].mean()) * S"),
+    "state: per-value gate averaged over the values": (
+        "chunk_state_pass", "S = S * np.exp(raw[t, h])[None, :]", "S = S * np.exp(raw[t, h].mean())"),
+    "state: per-head rate with the wrong sign": (
+        "chunk_state_pass", "S = np.exp(gv_[h]) * S", "S = np.exp(-gv_[h]) * S"),
+    "state: update subtracted": (
+        "chunk_state_pass", "S = S + np.outer(k[b, t, h], v[b, t, h])",
+        "S = S - np.outer(k[b, t, h], v[b, t, h])"),
+    "state: scalar gate after the update": (
+        "chunk_state_pass",
+        "S = np.exp(raw[t, h]) * S", "pass",
+        "S = S + np.outer(k[b, t, h], v[b, t, h])",
+        "S = (np.exp(raw[t, h]) if gate == 'g' else 1.0) * (S + np.outer(k[b, t, h], v[b, t, h]))"),
+    "state: chunk-start state one token late": (
+        "chunk_state_pass", "if i % chunk_size == 0 and", "if i % chunk_size == 1 and"),
+    "grad: scale dropped": (
+        "chunk_state_grad", "G = G + scale * np.outer(q[b, t, hq], do[b, t, hq])",
+        "G = G + np.outer(q[b, t, hq], do[b, t, hq])"),
+    "grad: output term with the wrong sign": (
+        "chunk_state_grad", "G = G + scale * np.outer(q[b, t, hq], do[b, t, hq])",
+        "G = G - scale * np.outer(q[b, t, hq], do[b, t, hq])"),
+    "grad: scalar gate before the output term": (
+        "chunk_state_grad",
+        "G = G + scale * np.outer(q[b, t, hq], do[b, t, hq])", "pass",
+        "G = np.exp(raw[t, h]) * G",
+        "G = np.exp(raw[t, h]) * G + scale * np.outer(q[b, t, hq], do[b, t, hq])"),
+    "grad: wrong gate head of a query head": ("chunk_state_grad", "h = hq // group", "h = hq % H"),
+    "grad: chunk gradient stored at the chunk's start": (
+        "chunk_state_grad", "i % chunk_size == chunk_size - 1 or", "i % chunk_size == 0 or"),
+}
+
+
+def _sp_mutant(name, *edits):
+    fn = getattr(SP, name)
+    src = textwrap.dedent(inspect.getsource(fn))
+    for old, new in zip(edits[::2], edits[1::2]):
+        assert src.count(old) == 1, f"{name}: {old!r} is not one line of the oracle"
+        src = src.replace(old, new)
+    ns = dict(vars(SP))
+    exec(compile(src, f"<mutant of {name}>", "exec"), ns)
+    return ns[name]
+
+
+@pytest.mark.parametrize("case", list(SP_MUTATIONS))
+def test_planted_state_pass_mistake_fails_a_pin(case, monkeypatch):
+    name, *edits = SP_MUTATIONS[case]
+    monkeypatch.setattr(SP, name, _sp_mutant(name, *edits))
+    for pin, kwargs in SP_PINS:
+        try:
+            pin(**kwargs)
+        except AssertionError:
             return
     pytest.fail(f"no pin fails with the planted mistake: {case}")
