@@ -901,13 +901,24 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         // 16-byte group q of row i sits at group q ^ (i & 7), so that the
         // chain's per-row loads (one row per lane) hit eight different groups
         // in every quarter warp: no shared-memory bank conflicts.  The tile is
-        // staged in R1 (free once the WY GEMM is done) in the block's layout
-        // and leaves with the block's other parts in one bulk copy.
+        // staged in R1 (free once the WY GEMM is done) in the block's layout.
         float4 *dst = reinterpret_cast<float4 *>(smem + I_R1 + t * 8192 + i * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           dst[q ^ (i & 7)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        // this warp's 32 rows of the tile (4 KB) leave at once, while the
+        // other warps still form -w
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t off = t * 8192 + (qd - 2) * 32 * 128;
+          ptx::bulk_s2g(blk + OFF_U + off, smem + I_R1 + off, 4096);
+          ptx::bulk_commit();
+        }
       }
+      // the tile's rows must be read out before the buffers are reused
+      if (lane == 0) ptx::bulk_wait_read<0>();
+      __syncwarp();
     }
   }
   // The chain's A operand [-w ; q] leaves with the u tile (while another head
@@ -928,7 +939,6 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       ptx::bulk_s2g(blk + OFF_AW + 16384, AQ + 8192, 8192);
       ptx::bulk_s2g(blk + OFF_AW + 24576, KQ + 24576, 8192);
     }
-    ptx::bulk_s2g(blk + OFF_U, smem + I_R1, (uint32_t)V * 256);
     ptx::bulk_commit();
     ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   }
