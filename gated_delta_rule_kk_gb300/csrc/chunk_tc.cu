@@ -570,6 +570,12 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   }
   ptx::fence_proxy_async_smem();  // the images feed the tensor cores
   __syncthreads();
+  if (!KDA && tid == 0) {
+    // the q rows of [-w ; q] are the raw input: they leave now
+    ptx::bulk_s2g(blk + OFF_AW + 8192, KQ + 8192, 8192);
+    ptx::bulk_s2g(blk + OFF_AW + 24576, KQ + 24576, 8192);
+    ptx::bulk_commit();
+  }
   if (KDA) {
     // thread c < 128 owns key channel c: running cumsum down the TMA-loaded
     // gate tile in place (rows >= L repeat row L - 1)
@@ -678,6 +684,12 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     }
     ptx::fence_proxy_async_smem();
     __syncthreads();
+    if (tid == 0) {
+      // the q rows of [-w ; q e^g] are final: they leave now
+      ptx::bulk_s2g(blk + OFF_AW + 8192, KQ + 8192, 8192);
+      ptx::bulk_s2g(blk + OFF_AW + 24576, KQ + 24576, 8192);
+      ptx::bulk_commit();
+    }
   } else {
     ptx::fence_proxy_async_smem();
   }
@@ -892,6 +904,15 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
           *reinterpret_cast<uint4 *>(wimg + swz_off(i, q4 * 4 + q8, whalf)) = pack8(out);
         }
       }
+      // this warp's 32 rows of key half hf (4 KB) leave at once
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::bulk_s2g(blk + OFF_AW + hf * 16384 + qd * 4096, wimg + hf * whalf + qd * 4096, 4096);
+        ptx::bulk_commit();
+        ptx::bulk_wait_read<0>();
+      }
+      __syncwarp();
     } else {
       const int i = (qd - 2) * 32 + lane;
 #pragma unroll 1
@@ -921,27 +942,16 @@ intra_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       __syncwarp();
     }
   }
-  // The chain's A operand [-w ; q] leaves with the u tile (while another head
-  // follows, as four 8 KB pieces: -w from AQ, q from KQ).  After the last
-  // head the tensor memory is no longer read: free it before waiting on the
-  // store, so that the next CTA on this SM can allocate it while this one
-  // drains.
+  // Every part of the block has left in pieces as soon as it was final (the
+  // q rows of [-w ; q] once the inputs landed or the gating pass ended, each
+  // warp's -w and u rows from the epilogue).  After the last head the tensor
+  // memory is no longer read: free it before the last wait, so that the next
+  // CTA on this SM can allocate it while this one drains.
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
   if (last && warp == 0) ptx::tmem_dealloc<256>(tmem);
-  if (tid == 0) {
-    if (last) {
-      ptx::bulk_s2g(blk + OFF_AW, KQ, 32768);
-    } else {
-      ptx::bulk_s2g(blk + OFF_AW, AQ, 8192);
-      ptx::bulk_s2g(blk + OFF_AW + 8192, KQ + 8192, 8192);
-      ptx::bulk_s2g(blk + OFF_AW + 16384, AQ + 8192, 8192);
-      ptx::bulk_s2g(blk + OFF_AW + 24576, KQ + 24576, 8192);
-    }
-    ptx::bulk_commit();
-    ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
-  }
+  if (tid == 0) ptx::bulk_wait_read<0>();  // shared memory read out; the writes land on their own
   if (!(ok1 && ok2 && ok_v) && tid == 0) record_error(p.err, GDN_ERR_TIMEOUT);
   if (last) break;
   // next value head: the stores above have read AQ, R1 and the scales
